@@ -1,0 +1,382 @@
+"""Benchmark one packed paged-attention step (KV append + attention) on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pkv|reference] [--config NAME]
+
+A step is one pass of the whole path over one synthetic batch: upload of the
+step plan (host step metadata), KV append of the step's new tokens, split-KV
+attention (+ tensor-core prefill tiles when present) and the LSE merge.
+
+* value: KV tokens/s = sum(context_lens) / device time per step, inputs resident
+  in HBM, the step replayed from a CUDA graph, L2 flushed (256 MB write) before
+  every timed step and the flush kept outside the per-step CUDA-event pairs.
+* roofline: the decode kernel alone, timed with CUDA events recorded on its
+  launch stream around each launch (library profiling hook), algorithmic bytes
+  (KV + Q + O + metadata) / mean duration vs the measured HBM copy bandwidth.
+* e2e: the same metric through the public API from pinned HOST buffers: every
+  step copies q, the new K/V, slot mapping and metadata host->device, plans on
+  the host, runs append + attention and copies out back (wall time per step).
+* cpu_baseline / --impl reference: the fp64 CPU oracle as it stands, on the
+  host cores, on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+L2_FLUSH_BYTES = 256 << 20
+METRIC = "paged-attention step: KV tokens/s and achieved HBM GB/s vs peak on 1 GB300"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained"), "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+def algorithmic_bytes(meta) -> int:
+    """KV + Q + O + metadata bytes of one attention pass (split-KV scratch excluded)."""
+    d, hq, hkv = meta.head_dim, meta.num_q_heads, meta.num_kv_heads
+    live = meta.q_lens > 0
+    kv = int(meta.context_lens[live].astype(np.int64).sum()) * 2 * hkv * d * 2
+    qo = 2 * meta.total_q * hq * d * 2
+    nb = int(((meta.context_lens[live].astype(np.int64) + 15) // 16).sum())
+    return kv + qo + 4 * (2 * meta.num_seqs + 1) + 4 * nb
+
+
+def unique_bytes(meta) -> int:
+    d, hq, hkv = meta.head_dim, meta.num_q_heads, meta.num_kv_heads
+    return meta.unique_blocks() * 16 * 2 * hkv * d * 2 + 2 * meta.total_q * hq * d * 2
+
+
+def prefill_flops(meta) -> int:
+    """4*D*Hq*(visible (q, k) pairs) over sequences with q_len > 1."""
+    pairs = 0
+    for s in range(meta.num_seqs):
+        qs, ctx = int(meta.q_lens[s]), int(meta.context_lens[s])
+        if qs > 1:
+            pairs += sum(ctx - qs + i + 1 for i in range(qs))
+    return 4 * meta.head_dim * meta.num_q_heads * pairs
+
+
+class ClockSampler:
+    """nvidia-smi sampling in the background during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        if self.proc is None or self.file is None:
+            return None
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def run_oracle_sample(meta, target_s=10.0, max_reps=1000):
+    """Time the oracle (append + attention) on whole steps, or on a fixed subset of
+    query rows for steps too large to finish in about target_s."""
+    import torch
+    import oracle
+    q, k, v, pool = workloads.make_values(meta, device="cpu")
+    rows_total = meta.total_q * meta.num_q_heads
+    # cost model: one row costs ~ its visible keys
+    t0 = time.perf_counter()
+    probe_rows = np.arange(0, rows_total, max(1, rows_total // 64), dtype=np.int64)
+    oracle.run_step(meta, q, k, v, pool, rows=probe_rows)
+    per_row = (time.perf_counter() - t0) / len(probe_rows)
+    full = per_row * rows_total
+    if full <= target_s:
+        reps, rows, sample = max(1, int(target_s / max(full, 1e-6))), None, "full step"
+        reps = min(reps, max_reps)
+    else:
+        n = max(1, int(rows_total * target_s / full))
+        rows = np.sort(np.random.default_rng(0).choice(rows_total, size=n, replace=False)).astype(np.int64)
+        reps, sample = 1, f"{n} of {rows_total} query rows"
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.run_step(meta, q, k, v, pool, rows=rows)
+    dt = time.perf_counter() - t0
+    if rows is None:
+        kv_tok = meta.kv_tokens() * reps
+    else:   # credit each sampled row with its share of the step's KV tokens
+        kv_tok = meta.kv_tokens() * len(rows) / rows_total
+    del torch
+    return {"value": kv_tok / dt, "unit": "KV tokens/s", "cores": oracle.max_threads(),
+            "kind": "oracle", "seconds": dt,
+            "sample": f"{meta.name}: {sample} x {reps} (fp64 C oracle, OpenMP)"}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def bench_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    meta = workloads.make_config(args.config)
+    for _ in range(args.warmup):
+        run_oracle_sample(meta, target_s=0.5, max_reps=1)
+    times, vals = [], []
+    for _ in range(args.steps):
+        r = run_oracle_sample(meta, target_s=2.0, max_reps=1)
+        vals.append(r["value"])
+    v = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "KV tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": meta.kv_tokens() / v * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": meta.name, **workloads.describe(meta)},
+            "cpu_baseline": {k: r[k] for k in ("value", "unit", "cores", "kind", "sample")},
+            "e2e": {"value": v, "unit": "KV tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    line["cpu_baseline"]["value"] = v
+    print(json.dumps(line), flush=True)
+
+
+def bench_pkv(args):
+    import torch
+    import paged_kv_attention_append_gb300 as pkv
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    meta = workloads.make_config(args.config)
+    q, k, v, pool = workloads.make_values(meta, device=dev)
+    slots = torch.from_numpy(meta.slot_mapping).to(dev)
+    cu_d = torch.from_numpy(meta.cu_q_lens).to(dev)
+    ctx_d = torch.from_numpy(meta.context_lens).to(dev)
+    bt_d = torch.from_numpy(meta.block_tables).to(dev)
+    out = torch.empty_like(q)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    info, host_plan = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, pool,
+                                    upload=False)
+    t0 = time.perf_counter()
+    for _ in range(50):
+        pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, pool, upload=False)
+    host_plan_us = (time.perf_counter() - t0) / 50 * 1e6
+    plan_pinned = torch.from_numpy(host_plan.view(np.uint8)).pin_memory()
+    plan = pkv.StepPlan(info, host_plan, dev)
+
+    def step():
+        plan.dev[:plan_pinned.numel()].copy_(plan_pinned, non_blocking=True)
+        pkv.paged_kv_append(k, v, slots, pool, dev_status=status)
+        pkv.paged_varlen_attention(q, cu_d, ctx_d, bt_d, pool, meta.scale, plan=plan, out=out,
+                                   dev_status=status)
+
+    # warm up eagerly, then capture one step into a CUDA graph
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            step()
+    torch.cuda.synchronize(dev)
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    launches_before = pkv.kernel_launch_count()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    launches_per_step = pkv.kernel_launch_count() - launches_before
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            graph.replay()
+    torch.cuda.synchronize(dev)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            for a, b in ev:
+                flush.zero_()
+                a.record(stream)
+                graph.replay()
+                b.record(stream)
+        torch.cuda.synchronize(dev)
+        # kernel-only timing of the decode kernel (roofline), eager, L2 flushed
+        k_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)]
+        with torch.cuda.stream(stream):
+            for a, b in k_ev:
+                a.record(stream)
+                b.record(stream)
+            torch.cuda.synchronize(dev)
+            for a, b in k_ev:
+                flush.zero_()
+                pkv.set_profile_events("decode", a, b)
+                pkv.paged_varlen_attention(q, cu_d, ctx_d, bt_d, pool, meta.scale, plan=plan,
+                                           out=out, dev_status=status)
+            pkv.set_profile_events("decode")
+        torch.cuda.synchronize(dev)
+    step_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    decode_ms = statistics.mean(a.elapsed_time(b) for a, b in k_ev)
+    clocks = clk.summary()
+    if ws > 1:
+        t = torch.tensor([step_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(t.item())
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+
+    # ---- end to end from pinned host buffers through the public API
+    host = {
+        "q": q.cpu().pin_memory(), "k": k.cpu().pin_memory(), "v": v.cpu().pin_memory(),
+        "slots": slots.cpu().pin_memory(), "cu": cu_d.cpu().pin_memory(),
+        "ctx": ctx_d.cpu().pin_memory(), "bt": bt_d.cpu().pin_memory(),
+    }
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ds, dcu, dctx, dbt = (torch.empty_like(t) for t in (slots, cu_d, ctx_d, bt_d))
+    h2d = sum(t.numel() * t.element_size() for t in host.values()) + plan_pinned.numel()
+    d2h = out_h.numel() * out_h.element_size()
+    e2e_times = []
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + args.steps):
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            for dst, src in ((dq, host["q"]), (dk, host["k"]), (dv, host["v"]), (ds, host["slots"]),
+                             (dcu, host["cu"]), (dctx, host["ctx"]), (dbt, host["bt"])):
+                dst.copy_(src, non_blocking=True)
+            inf2, hp2 = pkv.plan_step(host["cu"].numpy(), host["ctx"].numpy(), meta.num_q_heads, pool,
+                                      upload=False)
+            pp = torch.from_numpy(hp2.view(np.uint8))
+            plan.dev[:pp.numel()].copy_(pp, non_blocking=False)
+            plan.info = inf2
+            pkv.paged_kv_append(dk, dv, ds, pool, dev_status=status)
+            pkv.paged_varlen_attention(dq, dcu, dctx, dbt, pool, meta.scale, plan=plan, out=out,
+                                       dev_status=status)
+            out_h.copy_(out, non_blocking=True)
+            stream.synchronize()
+            if i >= args.warmup:
+                e2e_times.append(time.perf_counter() - t0)
+    e2e_s = statistics.mean(e2e_times)
+    if ws > 1:
+        t = torch.tensor([e2e_s], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+
+    pk = peaks()
+    kv_tok = meta.kv_tokens()
+    bytes_alg = algorithmic_bytes(meta)
+    achieved = bytes_alg / (decode_ms * 1e-3) / 1e9
+    cpu = run_oracle_sample(meta) if (rank == 0 and ws == 1 and not args.no_cpu_baseline) else None
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": ws * kv_tok / (step_ms * 1e-3), "unit": "KV tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) bf16, shapes of the named workload)",
+        "config": {**workloads.describe(meta), "parallelism": f"replicas x{ws}" if ws > 1 else "single",
+                   "l2": f"flushed ({L2_FLUSH_BYTES >> 20} MB write) before every timed step",
+                   "timing": "CUDA graph replay per step, CUDA events per step"},
+        "gpu_launches": launches_per_step * args.steps,
+        "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved,
+                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                     "traffic": None, "bytes_per_launch": bytes_alg, "ms_per_launch": decode_ms,
+                     "peak_source": pk["source"]},
+        "step_gbs": bytes_alg / (step_ms * 1e-3) / 1e9,
+        "host_plan_us": host_plan_us,
+        "e2e": {"value": ws * kv_tok / e2e_s, "unit": "KV tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
+        "clocks": clocks,
+        "cpu_baseline": None if cpu is None else {k2: cpu[k2] for k2 in
+                                                  ("value", "unit", "cores", "kind", "sample")},
+        "plan": {"decode_tiles": info.num_decode_tiles, "merge_groups": info.num_merge_groups,
+                 "prefill_tiles": info.num_prefill_tiles, "split_blocks": info.split_blocks},
+    }
+    if meta.unique_blocks() * 16 < kv_tok:
+        line["unique_gbs"] = unique_bytes(meta) / (decode_ms * 1e-3) / 1e9
+    fl = prefill_flops(meta)
+    if fl:
+        line["prefill_tflops_step"] = fl / (step_ms * 1e-3) / 1e12
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
+    ap.add_argument("--config", default="small_decode", choices=list(workloads.CONFIGS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        bench_reference(args)
+    else:
+        bench_pkv(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,198 @@
+/*
+ * pkv.h -- paged KV cache append and packed varlen attention on one GB300.
+ *
+ * The problem (vllm-metal v0.4.0 release page, section "Replacing attention,
+ * reusing the rest"): a serving step is flattened onto ONE packed query axis,
+ * with cu_seqlens marking where each request's query tokens start; KV stays in
+ * fixed-size pages located through per-request block tables; one attention
+ * launch covers everything the scheduler packed into the step -- chunked
+ * prefill chunks, decode tokens and speculative-verify windows.  The same page
+ * ("What v0.4.0 adds", batched MTP) has verify windows ride in the packed
+ * target batch, and ("Prefix caching on hybrid models") rows are written into
+ * pools in place.
+ *
+ * Conventions shared by every call:
+ *  - All tensors are dense and row-major; bf16 is IEEE bfloat16 bit patterns.
+ *  - kv_pool:  bf16 [num_blocks][2][num_kv_heads][block_size][head_dim];
+ *              index 1 of the second axis selects K (0) or V (1).  Each
+ *              (block, K|V, head) slab is one contiguous block_size*head_dim run.
+ *  - q, out:   bf16 [total_q][num_q_heads][head_dim], packed in sequence order.
+ *  - k, v:     bf16 [num_tokens][num_kv_heads][head_dim] (this step's new tokens).
+ *  - cu_q_lens [num_seqs+1] int32, cu_q_lens[0] = 0, non-decreasing;
+ *    q_len(s) = cu_q_lens[s+1] - cu_q_lens[s].
+ *  - context_lens [num_seqs] int32: keys of sequence s INCLUDING this step's
+ *    new tokens (append first, then attend).  q_len(s) <= context_lens[s].
+ *  - Causality: query i of sequence s sits at position ctx - q_len + i and sees
+ *    keys 0 .. ctx - q_len + i.
+ *  - GQA: query head hq reads KV head hq / (num_q_heads / num_kv_heads).
+ *  - block_tables [num_seqs][max_blocks_per_seq] int32: logical block j of
+ *    sequence s is physical block block_tables[s][j]; entries at or past
+ *    ceil(ctx/block_size) are never read.  Several sequences may share blocks.
+ *  - Supported: block_size 16, head_dim 64 or 128, num_q_heads a multiple of
+ *    num_kv_heads with group size <= 16.  Anything else: PKV_ERR_UNSUPPORTED.
+ *
+ * Ownership and execution: the caller owns every buffer.  The library never
+ * allocates device memory, keeps no per-call state between calls, and enqueues
+ * work asynchronously on the caller's stream.  Device pointers must be
+ * 16-byte aligned.
+ *
+ * Errors: host-detectable problems return a non-zero pkv_status before any
+ * work is enqueued.  Problems only the device can see (a slot or block id
+ * outside the pool, a plan that does not match the device metadata, a pipeline
+ * wait that timed out) are written to *dev_status (int32, device memory; first
+ * error wins; caller zeroes it and reads it after synchronising); the offending
+ * token/block is skipped, nothing is read or written out of bounds, and no
+ * kernel traps or asserts.  dev_status may be NULL to ignore them.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *pkv_stream;
+
+typedef enum pkv_status {
+  PKV_OK = 0,
+  PKV_ERR_NULL = 1,          /* a required pointer is NULL */
+  PKV_ERR_SHAPE = 2,         /* inconsistent sizes (cu_q_lens not monotone, ...) */
+  PKV_ERR_RANGE = 3,         /* q_len > context_len, block id / slot out of range, ... */
+  PKV_ERR_UNSUPPORTED = 4,   /* head_dim, block_size or group size not supported */
+  PKV_ERR_WORKSPACE = 5,     /* plan or workspace buffer too small */
+  PKV_ERR_CUDA = 6,          /* a CUDA runtime call failed (launch, attribute, ...) */
+  PKV_ERR_DEVICE_CHECK = 7,  /* value written to *dev_status by a kernel */
+  PKV_ERR_ALIGN = 8          /* a device pointer is not 16-byte aligned */
+} pkv_status;
+
+/* Device-side error codes written to *dev_status (first one wins). */
+#define PKV_DEV_OK 0
+#define PKV_DEV_BAD_SLOT 1       /* append: slot >= num_blocks*block_size (token skipped) */
+#define PKV_DEV_BAD_BLOCK 2      /* attention: block id outside [0, num_blocks) (block skipped) */
+#define PKV_DEV_TIMEOUT 3        /* a pipeline wait exceeded its bound (tile abandoned) */
+#define PKV_DEV_PLAN_MISMATCH 4  /* device cu_q_lens/context_lens disagree with the plan */
+
+typedef struct pkv_pool_desc {
+  int32_t num_blocks;   /* physical blocks in kv_pool */
+  int32_t block_size;   /* tokens per block; must be 16 */
+  int32_t num_kv_heads; /* Hkv */
+  int32_t head_dim;     /* D: 64 or 128 */
+} pkv_pool_desc;
+
+/* Summary of a step plan, written by pkv_plan_step. */
+typedef struct pkv_plan_info {
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t total_q;
+  int32_t num_decode_tiles;  /* split-KV work items (each runs for every KV head) */
+  int32_t num_merge_groups;  /* row groups whose keys were split over several tiles */
+  int32_t num_partials;      /* partial-result slots used by split tiles */
+  int32_t num_prefill_tiles; /* tensor-core work items (128 query rows x 1 query head) */
+  int32_t num_kernels;       /* kernel launches one pkv_paged_varlen_attention call makes */
+  int32_t split_blocks;      /* KV blocks per split chosen for this step */
+  int32_t max_blocks_needed; /* max over sequences of ceil(context_len / block_size) */
+  int64_t kv_tokens;         /* sum of context_lens over sequences with q_len > 0 */
+  int64_t plan_bytes;        /* bytes of the plan buffer (host, then device copy) */
+  int64_t workspace_bytes;   /* device workspace the attention call needs */
+} pkv_plan_info;
+
+/* Library version (major*10000 + minor*100 + patch). */
+PKV_API int32_t pkv_version(void);
+
+/* Human-readable name of a pkv_status or a PKV_DEV_* code. */
+PKV_API const char *pkv_status_string(int32_t status);
+
+/* Total kernel launches enqueued by this library since it was loaded. */
+PKV_API int64_t pkv_kernel_launch_count(void);
+
+/* Kernel ids for pkv_set_profile_events. */
+#define PKV_KERNEL_APPEND 0
+#define PKV_KERNEL_DECODE 1
+#define PKV_KERNEL_MERGE 2
+#define PKV_KERNEL_PREFILL 3
+
+/*
+ * Profiling hook (off by default).  After this call, every launch of kernel
+ * `which` made FROM THE CALLING HOST THREAD is bracketed by
+ * cudaEventRecord(start_event) / cudaEventRecord(stop_event) on the launch
+ * stream, so the caller can time that kernel alone with its own events
+ * (cudaEvent_t handles, created and owned by the caller).  Passing NULL for
+ * both turns it off again.  Returns PKV_ERR_RANGE for an unknown kernel id.
+ */
+PKV_API pkv_status pkv_set_profile_events(int32_t which, void *start_event, void *stop_event);
+
+/*
+ * KV append (the in-place row scatter of the "Prefix caching on hybrid
+ * models" section, applied to the paged KV pool of "Replacing attention,
+ * reusing the rest").
+ *   For each token t < num_tokens with slot = slot_mapping[t]:
+ *     slot < 0                        : padding, nothing written;
+ *     0 <= slot < num_blocks*bs       : kv_pool[slot/bs][0][h][slot%bs][:] = k[t][h][:],
+ *                                       kv_pool[slot/bs][1][h][slot%bs][:] = v[t][h][:]
+ *                                       for every KV head h (raw 16-bit copies);
+ *     slot >= num_blocks*bs           : token skipped, PKV_DEV_BAD_SLOT to *dev_status.
+ *   k, v: device bf16 [num_tokens][Hkv][D]; slot_mapping: device int32 [num_tokens];
+ *   kv_pool: device, layout above.  Two tokens with the same slot: unspecified
+ *   which one lands.  num_tokens == 0 enqueues nothing and returns PKV_OK.
+ */
+PKV_API pkv_status pkv_paged_kv_append(const void *k, const void *v, const int32_t *slot_mapping,
+                               int32_t num_tokens, void *kv_pool, const pkv_pool_desc *desc,
+                               int32_t *dev_status, pkv_stream stream);
+
+/*
+ * Host step metadata (the per-threadgroup search over cu_seqlens that the
+ * vllm-metal kernel performs, moved to the host where the scheduler already
+ * holds the lengths).  Validates the lengths, splits each sequence's keys into
+ * work tiles sized for num_sms SMs, assigns partial-result slots and sizes the
+ * workspace.
+ *   cu_q_lens, context_lens: HOST arrays (num_seqs+1 and num_seqs int32).
+ *   num_sms: SMs of the target GPU (<= 0 means 152).
+ *   plan: host buffer receiving plan_capacity bytes at most; may be NULL to
+ *   query sizes only (info is always filled on success).
+ * Returns PKV_ERR_WORKSPACE if plan is non-NULL and plan_capacity < info->plan_bytes.
+ * The plan buffer is opaque; upload it unchanged (e.g. cudaMemcpyAsync) before
+ * the attention call that uses it.
+ */
+PKV_API pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *context_lens, int32_t num_seqs,
+                         int32_t num_q_heads, const pkv_pool_desc *desc, int32_t num_sms,
+                         void *plan, int64_t plan_capacity, pkv_plan_info *info);
+
+/*
+ * Packed varlen attention over the paged KV pool ("Replacing attention,
+ * reusing the rest": one launch sequence for prefill chunks, decode tokens and
+ * verify windows):
+ *   out[t][hq][:] = sum_p softmax_p(scale * q[t][hq] . K[p][hq/G]) V[p][hq/G]
+ *   over the keys p visible to token t (causal rule above), K/V of position p
+ *   read from kv_pool block block_tables[s][p/bs], offset p%bs.
+ *   q, out: device bf16 (layout above).  cu_q_lens, context_lens, block_tables:
+ *   DEVICE copies of the arrays the plan was built from.  plan_dev: device copy
+ *   of the plan buffer; info: the host summary pkv_plan_step returned.
+ *   workspace: device scratch of at least info->workspace_bytes (256-byte
+ *   aligned; contents on entry do not matter).  Rows of sequences with
+ *   q_len == 0 do not exist.  Accumulation is fp32; out is rounded once to bf16.
+ */
+PKV_API pkv_status pkv_paged_varlen_attention(const void *q, const int32_t *cu_q_lens,
+                                      const int32_t *context_lens, const int32_t *block_tables,
+                                      int32_t max_blocks_per_seq, const void *kv_pool,
+                                      const pkv_pool_desc *desc, float scale,
+                                      const pkv_plan_info *info, const void *plan_dev, void *out,
+                                      void *workspace, int64_t workspace_bytes,
+                                      int32_t *dev_status, pkv_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

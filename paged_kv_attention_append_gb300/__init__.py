@@ -1,0 +1,293 @@
+"""Paged KV append + packed varlen attention for one GB300 (sm_103a).
+
+A thin binding over the C ABI in ``include/pkv.h`` (``_lib/libpkv.so``): it
+checks torch tensors, passes their device pointers and the current CUDA stream,
+and allocates the caller-owned buffers (plan copy, workspace, output).  Every
+step of the computation runs in the library's CUDA kernels; there is no other
+implementation here.  If the library is missing, every call raises.
+
+    kv_pool = torch.empty(num_blocks, 2, Hkv, 16, D, dtype=torch.bfloat16, device="cuda")
+    paged_kv_append(k_new, v_new, slot_mapping, kv_pool)
+    out = paged_varlen_attention(q, cu_q_lens, context_lens, block_tables, kv_pool, scale)
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import numpy as np
+import torch
+
+__all__ = [
+    "PkvError", "PoolDesc", "PlanInfo", "StepPlan", "build", "library_path", "version",
+    "status_string", "kernel_launch_count", "paged_kv_append", "plan_step",
+    "paged_varlen_attention", "DEV_STATUS",
+]
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "_lib", "libpkv.so")
+_lock = threading.Lock()
+_lib = None
+
+DEV_STATUS = {0: "ok", 1: "bad slot", 2: "bad block id", 3: "pipeline wait timed out",
+              4: "plan does not match device metadata"}
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+class PoolDesc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+class PlanInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "num_seqs", "num_q_heads", "num_kv_heads", "head_dim", "total_q", "num_decode_tiles",
+        "num_merge_groups", "num_partials", "num_prefill_tiles", "num_kernels", "split_blocks",
+        "max_blocks_needed")] + [(n, ctypes.c_int64) for n in ("kv_tokens", "plan_bytes",
+                                                              "workspace_bytes")]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+def build(verbose: bool = False) -> str:
+    """Compile the CUDA library in-tree (nvcc, sm_103a) and return its path."""
+    from . import _build
+    return _build.build(verbose=verbose)
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    f"{_LIB_PATH} is missing: build the CUDA library first "
+                    "(paged_kv_attention_append_gb300.build()); there is no fallback path")
+            lib = ctypes.CDLL(_LIB_PATH)
+            P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+            lib.pkv_version.restype = i32
+            lib.pkv_status_string.argtypes = [i32]
+            lib.pkv_status_string.restype = ctypes.c_char_p
+            lib.pkv_kernel_launch_count.restype = i64
+            lib.pkv_paged_kv_append.argtypes = [P, P, P, i32, P, ctypes.POINTER(PoolDesc), P, P]
+            lib.pkv_paged_kv_append.restype = i32
+            lib.pkv_plan_step.argtypes = [P, P, i32, i32, ctypes.POINTER(PoolDesc), i32, P, i64,
+                                          ctypes.POINTER(PlanInfo)]
+            lib.pkv_plan_step.restype = i32
+            lib.pkv_paged_varlen_attention.argtypes = [P, P, P, P, i32, P, ctypes.POINTER(PoolDesc),
+                                                       ctypes.c_float, ctypes.POINTER(PlanInfo), P, P,
+                                                       P, i64, P, P]
+            lib.pkv_paged_varlen_attention.restype = i32
+            lib.pkv_set_profile_events.argtypes = [i32, P, P]
+            lib.pkv_set_profile_events.restype = i32
+            _lib = lib
+    return _lib
+
+
+def version() -> int:
+    return int(_load().pkv_version())
+
+
+def status_string(status: int) -> str:
+    return _load().pkv_status_string(int(status)).decode()
+
+
+def kernel_launch_count() -> int:
+    return int(_load().pkv_kernel_launch_count())
+
+
+KERNEL_IDS = {"append": 0, "decode": 1, "merge": 2, "prefill": 3}
+
+
+def set_profile_events(kernel: str, start=None, stop=None):
+    """Record torch.cuda.Event `start`/`stop` around every launch of `kernel` made
+    from this thread (None, None turns it off).  Events must have been recorded once."""
+    st = _load().pkv_set_profile_events(KERNEL_IDS[kernel],
+                                        None if start is None else start.cuda_event,
+                                        None if stop is None else stop.cuda_event)
+    if st:
+        raise PkvError(st, "pkv_set_profile_events")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device):
+    s = torch.cuda.current_stream(device) if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check_cuda(name, t, dtype, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+
+
+def pool_desc(kv_pool: torch.Tensor) -> PoolDesc:
+    if kv_pool.dim() != 5 or kv_pool.shape[1] != 2:
+        raise ValueError("kv_pool must be [num_blocks, 2, num_kv_heads, block_size, head_dim]")
+    nb, _, hkv, bs, d = kv_pool.shape
+    return PoolDesc(nb, bs, hkv, d)
+
+
+def paged_kv_append(k, v, slot_mapping, kv_pool, *, dev_status=None, stream=None):
+    """Write this step's K/V rows into the pool slots named by slot_mapping (negative = skip).
+
+    k, v: bf16 [n, Hkv, D]; slot_mapping: int32 [n]; kv_pool: bf16 [nb, 2, Hkv, 16, D].
+    """
+    _check_cuda("kv_pool", kv_pool, torch.bfloat16, 5)
+    _check_cuda("k", k, torch.bfloat16, 3)
+    _check_cuda("v", v, torch.bfloat16, 3)
+    _check_cuda("slot_mapping", slot_mapping, torch.int32, 1)
+    desc = pool_desc(kv_pool)
+    n = slot_mapping.shape[0]
+    if k.shape != (n, desc.num_kv_heads, desc.head_dim) or v.shape != k.shape:
+        raise ValueError(f"k/v must be [{n}, {desc.num_kv_heads}, {desc.head_dim}]")
+    if dev_status is not None:
+        _check_cuda("dev_status", dev_status, torch.int32)
+    st = _load().pkv_paged_kv_append(_ptr(k), _ptr(v), _ptr(slot_mapping), n, _ptr(kv_pool),
+                                     ctypes.byref(desc), _ptr(dev_status),
+                                     _stream(stream, kv_pool.device))
+    if st:
+        raise PkvError(st, "pkv_paged_kv_append")
+
+
+def _host_i32(x) -> np.ndarray:
+    if isinstance(x, torch.Tensor):
+        x = x.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(x), dtype=np.int32)
+
+
+class StepPlan:
+    """Host step metadata plus its device copy and the workspace it needs."""
+
+    def __init__(self, info: PlanInfo, host: np.ndarray, device: torch.device, stream=None):
+        self.info = info
+        self.host = host
+        self.device = device
+        self.dev = None
+        self.workspace = None
+        self.upload(stream)
+
+    def upload(self, stream=None):
+        dev = torch.device(self.device)
+        nbytes = max(int(self.info.plan_bytes), 16)
+        if self.dev is None or self.dev.numel() < nbytes:
+            self.dev = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        src = torch.from_numpy(self.host.view(np.uint8)[:nbytes])
+        with torch.cuda.stream(stream) if stream is not None else _nullcontext():
+            self.dev[:nbytes].copy_(src, non_blocking=False)
+        wsb = int(self.info.workspace_bytes)
+        if wsb > 0 and (self.workspace is None or self.workspace.numel() < wsb):
+            self.workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
+        return self
+
+
+class _nullcontext:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+def plan_step(cu_q_lens, context_lens, num_q_heads: int, kv_pool_or_desc, *, num_sms=None,
+              device=None, upload=True, stream=None) -> StepPlan | tuple:
+    """Build the host plan for one step (pkv_plan_step) and upload it.
+
+    cu_q_lens / context_lens: host arrays or tensors (copied to the host if on a GPU).
+    Returns a StepPlan (or (info, host_bytes) when upload=False).
+    """
+    desc = kv_pool_or_desc if isinstance(kv_pool_or_desc, PoolDesc) else pool_desc(kv_pool_or_desc)
+    if device is None:
+        device = kv_pool_or_desc.device if isinstance(kv_pool_or_desc, torch.Tensor) else "cuda"
+    cu = _host_i32(cu_q_lens)
+    ctx = _host_i32(context_lens)
+    if cu.ndim != 1 or ctx.ndim != 1 or cu.shape[0] != ctx.shape[0] + 1:
+        raise ValueError("cu_q_lens must have num_seqs + 1 entries and context_lens num_seqs")
+    if num_sms is None:
+        num_sms = (torch.cuda.get_device_properties(torch.device(device)).multi_processor_count
+                   if torch.cuda.is_available() else 152)
+    info = PlanInfo()
+    lib = _load()
+    st = lib.pkv_plan_step(cu.ctypes.data_as(ctypes.c_void_p), ctx.ctypes.data_as(ctypes.c_void_p),
+                           ctx.shape[0], int(num_q_heads), ctypes.byref(desc), int(num_sms), None, 0,
+                           ctypes.byref(info))
+    if st:
+        raise PkvError(st, "pkv_plan_step")
+    host = np.zeros((max(int(info.plan_bytes), 16) + 15) // 16 * 4, dtype=np.int32)
+    st = lib.pkv_plan_step(cu.ctypes.data_as(ctypes.c_void_p), ctx.ctypes.data_as(ctypes.c_void_p),
+                           ctx.shape[0], int(num_q_heads), ctypes.byref(desc), int(num_sms),
+                           host.ctypes.data_as(ctypes.c_void_p), host.nbytes, ctypes.byref(info))
+    if st:
+        raise PkvError(st, "pkv_plan_step")
+    if not upload:
+        return info, host
+    return StepPlan(info, host, torch.device(device), stream)
+
+
+def _dev_i32(x, device, name):
+    if isinstance(x, torch.Tensor) and x.device.type == "cuda":
+        _check_cuda(name, x, torch.int32)
+        return x
+    return torch.from_numpy(_host_i32(x)).to(device)
+
+
+def paged_varlen_attention(q, cu_q_lens, context_lens, block_tables, kv_pool, scale: float, *,
+                           plan: StepPlan | None = None, out=None, dev_status=None, stream=None):
+    """Packed varlen causal attention over the paged pool; returns out [total_q, Hq, D] bf16.
+
+    cu_q_lens / context_lens may be host or device arrays; a plan is built from
+    host copies when none is given.  block_tables: int32 [num_seqs, max_blocks].
+    """
+    _check_cuda("q", q, torch.bfloat16, 3)
+    _check_cuda("kv_pool", kv_pool, torch.bfloat16, 5)
+    desc = pool_desc(kv_pool)
+    dev = q.device
+    if plan is None:
+        plan = plan_step(cu_q_lens, context_lens, q.shape[1], desc, device=dev, stream=stream)
+    info = plan.info
+    if q.shape[0] != info.total_q or q.shape[1] != info.num_q_heads or q.shape[2] != desc.head_dim:
+        raise ValueError(f"q shape {tuple(q.shape)} does not match the plan "
+                         f"({info.total_q}, {info.num_q_heads}, {desc.head_dim})")
+    cu_d = _dev_i32(cu_q_lens, dev, "cu_q_lens")
+    ctx_d = _dev_i32(context_lens, dev, "context_lens")
+    bt_d = _dev_i32(block_tables, dev, "block_tables")
+    if bt_d.dim() != 2 or bt_d.shape[0] != info.num_seqs:
+        raise ValueError("block_tables must be [num_seqs, max_blocks_per_seq]")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _check_cuda("out", out, torch.bfloat16, 3)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    if dev_status is not None:
+        _check_cuda("dev_status", dev_status, torch.int32)
+    ws = plan.workspace
+    st = _load().pkv_paged_varlen_attention(
+        _ptr(q), _ptr(cu_d), _ptr(ctx_d), _ptr(bt_d), bt_d.shape[1], _ptr(kv_pool),
+        ctypes.byref(desc), float(scale), ctypes.byref(info), _ptr(plan.dev), _ptr(out), _ptr(ws),
+        0 if ws is None else ws.numel(), _ptr(dev_status), _stream(stream, dev))
+    if st:
+        raise PkvError(st, "pkv_paged_varlen_attention")
+    return out

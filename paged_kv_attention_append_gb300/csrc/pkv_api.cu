@@ -1,0 +1,140 @@
+// C-ABI entry points (include/pkv.h): argument validation, then kernel
+// launches on the caller's stream.  No device allocation happens here.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+
+static std::atomic<int64_t> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+struct ProfileEvents {
+  void *start[4] = {nullptr, nullptr, nullptr, nullptr};
+  void *stop[4] = {nullptr, nullptr, nullptr, nullptr};
+};
+static thread_local ProfileEvents t_prof;
+
+void profile_begin(int which, pkv_stream stream) {
+  if (t_prof.start[which]) cudaEventRecord(static_cast<cudaEvent_t>(t_prof.start[which]), stream);
+}
+void profile_end(int which, pkv_stream stream) {
+  if (t_prof.stop[which]) cudaEventRecord(static_cast<cudaEvent_t>(t_prof.stop[which]), stream);
+}
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static pkv_status check_pool(const pkv_pool_desc *desc) {
+  if (!desc) return PKV_ERR_NULL;
+  if (desc->block_size != kBlockSize) return PKV_ERR_UNSUPPORTED;
+  if (desc->head_dim != 64 && desc->head_dim != 128) return PKV_ERR_UNSUPPORTED;
+  if (desc->num_kv_heads < 1 || desc->num_blocks < 0) return PKV_ERR_SHAPE;
+  // TMA row coordinates are int32: rows = num_blocks * 2 * Hkv * 16 must fit.
+  if ((int64_t)desc->num_blocks * 2 * desc->num_kv_heads * kBlockSize >= (int64_t)1 << 31)
+    return PKV_ERR_UNSUPPORTED;
+  return PKV_OK;
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" int32_t pkv_version(void) { return 100; }
+
+extern "C" int64_t pkv_kernel_launch_count(void) { return g_launches.load(); }
+
+extern "C" pkv_status pkv_set_profile_events(int32_t which, void *start_event,
+                                             void *stop_event) {
+  if (which < 0 || which > 3) return PKV_ERR_RANGE;
+  t_prof.start[which] = start_event;
+  t_prof.stop[which] = stop_event;
+  return PKV_OK;
+}
+
+extern "C" const char *pkv_status_string(int32_t status) {
+  switch (status) {
+    case PKV_OK: return "PKV_OK";
+    case PKV_ERR_NULL: return "PKV_ERR_NULL: a required pointer is NULL";
+    case PKV_ERR_SHAPE: return "PKV_ERR_SHAPE: inconsistent sizes";
+    case PKV_ERR_RANGE: return "PKV_ERR_RANGE: a length, slot or block id is out of range";
+    case PKV_ERR_UNSUPPORTED: return "PKV_ERR_UNSUPPORTED: head_dim/block_size/group not supported";
+    case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE: plan or workspace buffer too small";
+    case PKV_ERR_CUDA: return "PKV_ERR_CUDA: a CUDA runtime call failed";
+    case PKV_ERR_DEVICE_CHECK: return "PKV_ERR_DEVICE_CHECK: a kernel reported an error";
+    case PKV_ERR_ALIGN: return "PKV_ERR_ALIGN: a device pointer is not 16-byte aligned";
+    default: return "unknown pkv status";
+  }
+}
+
+extern "C" pkv_status pkv_paged_kv_append(const void *k, const void *v,
+                                          const int32_t *slot_mapping, int32_t num_tokens,
+                                          void *kv_pool, const pkv_pool_desc *desc,
+                                          int32_t *dev_status, pkv_stream stream) {
+  pkv_status st = check_pool(desc);
+  if (st != PKV_OK) return st;
+  if (num_tokens < 0) return PKV_ERR_SHAPE;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping || !kv_pool) return PKV_ERR_NULL;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(kv_pool)) return PKV_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(slot_mapping) & 3u) return PKV_ERR_ALIGN;
+  int e = launch_append(k, v, slot_mapping, num_tokens, kv_pool, *desc, dev_status, stream);
+  return e ? PKV_ERR_CUDA : PKV_OK;
+}
+
+extern "C" pkv_status pkv_paged_varlen_attention(
+    const void *q, const int32_t *cu_q_lens, const int32_t *context_lens,
+    const int32_t *block_tables, int32_t max_blocks_per_seq, const void *kv_pool,
+    const pkv_pool_desc *desc, float scale, const pkv_plan_info *info, const void *plan_dev,
+    void *out, void *workspace, int64_t workspace_bytes, int32_t *dev_status, pkv_stream stream) {
+  pkv_status st = check_pool(desc);
+  if (st != PKV_OK) return st;
+  if (!info) return PKV_ERR_NULL;
+  if (info->num_kv_heads != desc->num_kv_heads || info->head_dim != desc->head_dim ||
+      info->num_q_heads < 1 || info->num_q_heads % desc->num_kv_heads != 0)
+    return PKV_ERR_SHAPE;
+  if (!std::isfinite(scale)) return PKV_ERR_RANGE;
+  if (info->num_kernels == 0 || info->total_q == 0) return PKV_OK;
+  if (!q || !cu_q_lens || !context_lens || !block_tables || !kv_pool || !plan_dev || !out)
+    return PKV_ERR_NULL;
+  if (max_blocks_per_seq < info->max_blocks_needed) return PKV_ERR_RANGE;
+  if (workspace_bytes < info->workspace_bytes) return PKV_ERR_WORKSPACE;
+  if (info->workspace_bytes > 0 && !workspace) return PKV_ERR_NULL;
+  if (!aligned16(q) || !aligned16(out) || !aligned16(kv_pool) || !aligned16(plan_dev) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return PKV_ERR_ALIGN;
+
+  AttnArgs a;
+  a.q = q;
+  a.out = out;
+  a.cu_q_lens = cu_q_lens;
+  a.context_lens = context_lens;
+  a.block_tables = block_tables;
+  a.max_blocks_per_seq = max_blocks_per_seq;
+  a.kv_pool = kv_pool;
+  a.desc = *desc;
+  a.num_q_heads = info->num_q_heads;
+  a.num_seqs = info->num_seqs;
+  a.scale = scale;
+  const char *pb = static_cast<const char *>(plan_dev);
+  a.decode_tiles = reinterpret_cast<const DecodeTile *>(pb + plan_decode_off());
+  a.num_decode_tiles = info->num_decode_tiles;
+  a.merge_groups = reinterpret_cast<const MergeGroup *>(pb + plan_merge_off(info->num_decode_tiles));
+  a.num_merge_groups = info->num_merge_groups;
+  a.prefill_tiles = reinterpret_cast<const PrefillTile *>(
+      pb + plan_prefill_off(info->num_decode_tiles, info->num_merge_groups));
+  a.num_prefill_tiles = info->num_prefill_tiles;
+  char *wb = static_cast<char *>(workspace);
+  a.part_o = reinterpret_cast<float *>(wb);
+  a.part_ml = reinterpret_cast<float *>(
+      wb ? wb + ws_part_o_bytes(info->num_partials, desc->num_kv_heads, desc->head_dim) : nullptr);
+  a.dev_status = dev_status;
+  a.stream = stream;
+
+  int launches = 0;
+  if (launch_decode(a, &launches)) return PKV_ERR_CUDA;
+  if (launch_merge(a, &launches)) return PKV_ERR_CUDA;
+  return PKV_OK;
+}

@@ -1,0 +1,68 @@
+// KV append: scatter this step's K/V rows into their physical pool slots.
+//
+// The pool is the fixed paged KV store of the vllm-metal page ("Replacing
+// attention, reusing the rest"); rows are written in place ("Prefix caching on
+// hybrid models": a write touches only the rows it writes, never copies the
+// pool).  Pure data movement: each thread moves one 16-byte vector (8 bf16),
+// consecutive threads cover consecutive bytes of one (token, K|V, head) row so
+// both the loads and the stores are fully coalesced 16-byte accesses.
+#include <cuda_runtime.h>
+
+#include "pkv_device.cuh"
+
+namespace pkv {
+
+template <int D>
+__global__ void __launch_bounds__(256) append_kernel(const uint4 *__restrict__ k,
+                                                     const uint4 *__restrict__ v,
+                                                     const int32_t *__restrict__ slot_mapping,
+                                                     int32_t num_tokens, uint4 *__restrict__ pool,
+                                                     int32_t num_blocks, int32_t hkv,
+                                                     int32_t *dev_status) {
+  constexpr int kVecPerRow = D / 8;  // 16-byte vectors per head row
+  const int64_t per_token = 2ll * hkv * kVecPerRow;
+  const int64_t total = per_token * num_tokens;
+  const int64_t nslots = (int64_t)num_blocks * kBlockSize;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t t = (int32_t)(idx / per_token);
+    int32_t rem = (int32_t)(idx - (int64_t)t * per_token);
+    const int32_t kv = rem / (hkv * kVecPerRow);
+    rem -= kv * hkv * kVecPerRow;
+    const int32_t h = rem / kVecPerRow;
+    const int32_t vec = rem - h * kVecPerRow;
+    const int64_t slot = __ldg(slot_mapping + t);
+    if (slot < 0) continue;  // padding token
+    if (slot >= nslots) {
+      if (kv == 0 && h == 0 && vec == 0) report(dev_status, PKV_DEV_BAD_SLOT);
+      continue;
+    }
+    const int64_t blk = slot / kBlockSize, off = slot % kBlockSize;
+    const uint4 *src = (kv == 0 ? k : v) + ((int64_t)t * hkv + h) * kVecPerRow + vec;
+    uint4 *dst = pool + (((blk * 2 + kv) * hkv + h) * kBlockSize + off) * kVecPerRow + vec;
+    *dst = ldg128_nc(src);
+  }
+}
+
+int launch_append(const void *k, const void *v, const int32_t *slot_mapping, int32_t num_tokens,
+                  void *kv_pool, const pkv_pool_desc &desc, int32_t *dev_status,
+                  pkv_stream stream) {
+  const int64_t vecs = 2ll * desc.num_kv_heads * (desc.head_dim / 8) * num_tokens;
+  const int threads = 256;
+  int64_t blocks = (vecs + threads - 1) / threads;
+  blocks = blocks < 1 ? 1 : (blocks > 152 * 16 ? 152 * 16 : blocks);
+  profile_begin(PKV_KERNEL_APPEND, stream);
+  if (desc.head_dim == 128)
+    append_kernel<128><<<(unsigned)blocks, threads, 0, stream>>>(
+        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping, num_tokens,
+        static_cast<uint4 *>(kv_pool), desc.num_blocks, desc.num_kv_heads, dev_status);
+  else
+    append_kernel<64><<<(unsigned)blocks, threads, 0, stream>>>(
+        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v), slot_mapping, num_tokens,
+        static_cast<uint4 *>(kv_pool), desc.num_blocks, desc.num_kv_heads, dev_status);
+  profile_end(PKV_KERNEL_APPEND, stream);
+  count_launches(1);
+  return (int)cudaGetLastError();
+}
+
+}  // namespace pkv

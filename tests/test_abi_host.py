@@ -1,0 +1,214 @@
+"""Host-side tests of the C ABI (no GPU needed): exported symbols, the step
+planner's tiling invariants, and argument validation that returns before any
+CUDA call."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    import paged_kv_attention_append_gb300 as m
+    m.build()
+    return m
+
+
+def test_library_exports_every_declared_symbol(pkv):
+    with open(os.path.join(ROOT, "include", "pkv.h")) as f:
+        hdr = f.read()
+    names = re.findall(r"PKV_API\s+[\w\s\*]+?\b(pkv_\w+)\s*\(", hdr)
+    assert len(names) >= 6, names
+    lib = ctypes.CDLL(pkv.library_path())
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in pkv.h but not exported"
+
+
+def test_version_and_status_strings(pkv):
+    assert pkv.version() >= 100
+    for s in range(9):
+        assert pkv.status_string(s).startswith("PKV_")
+
+
+# ---------------------------------------------------------------- planner
+
+def parse_plan(info, host):
+    words = host.view(np.int32)
+    hdr = words[:16]
+    assert hdr[0] == 0x31564B50
+    nd, nm = info.num_decode_tiles, info.num_merge_groups
+    dec = words[16:16 + 8 * nd].reshape(nd, 8)
+    mer = words[16 + 8 * nd:16 + 8 * nd + 8 * nm].reshape(nm, 8)
+    return hdr, dec, mer
+
+
+def check_plan(meta, info, host, num_sms):
+    hdr, dec, mer = parse_plan(info, host)
+    g = meta.num_q_heads // meta.num_kv_heads
+    nq_tile = max(1, 16 // g)
+    assert info.total_q == meta.total_q
+    assert info.kv_tokens == int(meta.context_lens[meta.q_lens > 0].astype(np.int64).sum())
+    # tiles sorted longest first
+    lens = dec[:, 4] - dec[:, 3]
+    assert np.all(lens[:-1] >= lens[1:])
+    assert np.all(lens > 0)
+    # row groups partition each sequence's query tokens; splits partition its keys
+    seen_parts = set()
+    for s in range(meta.num_seqs):
+        qs, ctx = int(meta.q_lens[s]), int(meta.context_lens[s])
+        mine = dec[dec[:, 0] == s]
+        if qs == 0:
+            assert len(mine) == 0
+            continue
+        qi0s = sorted(set(int(x) for x in mine[:, 1]))
+        assert qi0s == list(range(0, qs, nq_tile))
+        for qi0 in qi0s:
+            grp = mine[mine[:, 1] == qi0]
+            n_q = min(nq_tile, qs - qi0)
+            assert np.all(grp[:, 2] == n_q)
+            nb = (ctx - qs + qi0 + n_q - 1) // 16 + 1
+            order = grp[np.argsort(grp[:, 3])]
+            assert order[0, 3] == 0 and order[-1, 4] == nb
+            assert np.all(order[1:, 3] == order[:-1, 4])
+            assert list(order[:, 6]) == [0] * (len(order) - 1) + [1]
+            if len(order) == 1:
+                assert order[0, 5] == -1
+            else:
+                parts = list(order[:, 5])
+                assert parts == list(range(parts[0], parts[0] + len(parts)))
+                assert not (set(parts) & seen_parts)
+                seen_parts |= set(parts)
+                m = mer[(mer[:, 0] == s) & (mer[:, 1] == qi0)]
+                assert len(m) == 1 and m[0, 2] == n_q and m[0, 3] == parts[0] and m[0, 4] == len(parts)
+    assert len(seen_parts) == info.num_partials
+    ws = 0
+    if info.num_partials:
+        d, hkv = meta.head_dim, meta.num_kv_heads
+        a = lambda x: (x + 255) // 256 * 256
+        ws = a(info.num_partials * hkv * 16 * d * 4) + a(info.num_partials * hkv * 16 * 8)
+    assert info.workspace_bytes == ws
+    assert info.num_kernels == (info.num_decode_tiles > 0) + (info.num_merge_groups > 0) + \
+        (info.num_prefill_tiles > 0)
+
+
+@pytest.mark.parametrize("name", list(workloads.CONFIGS))
+def test_planner_tiles_cover_every_config(pkv, name):
+    meta = workloads.make_config(name)
+    desc = pkv.PoolDesc(meta.num_blocks, 16, meta.num_kv_heads, meta.head_dim)
+    for sms in (152, 20):
+        info, host = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, desc,
+                                   num_sms=sms, upload=False)
+        check_plan(meta, info, host, sms)
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_planner_random_steps(pkv, seed):
+    rng = np.random.default_rng(seed)
+    meta = workloads.random_step(rng, max_ctx=3000)
+    desc = pkv.PoolDesc(meta.num_blocks, 16, meta.num_kv_heads, meta.head_dim)
+    info, host = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, desc,
+                               num_sms=int(rng.integers(1, 200)), upload=False)
+    check_plan(meta, info, host, None)
+
+
+def test_planner_handles_zero_length_queries_and_empty_steps(pkv):
+    desc = pkv.PoolDesc(10, 16, 2, 64)
+    info, host = pkv.plan_step(np.array([0, 0, 3, 3], np.int32), np.array([5, 40, 7], np.int32), 4,
+                               desc, num_sms=152, upload=False)
+    hdr, dec, mer = parse_plan(info, host)
+    assert set(dec[:, 0]) == {1}
+    info, host = pkv.plan_step(np.array([0], np.int32), np.array([], np.int32), 4, desc,
+                               num_sms=152, upload=False)
+    assert info.num_decode_tiles == 0 and info.num_kernels == 0 and info.workspace_bytes == 0
+
+
+@pytest.mark.parametrize("cu,ctx,hq,desc,err", [
+    ([1, 2], [4], 4, (10, 16, 2, 64), "SHAPE"),             # cu[0] != 0
+    ([0, 3, 2], [4, 4], 4, (10, 16, 2, 64), "SHAPE"),       # not monotone
+    ([0, 5], [4], 4, (10, 16, 2, 64), "RANGE"),             # q_len > ctx
+    ([0, 1], [-1], 4, (10, 16, 2, 64), "RANGE"),            # negative ctx
+    ([0, 1], [4], 4, (10, 16, 2, 96), "UNSUPPORTED"),       # head_dim 96
+    ([0, 1], [4], 4, (10, 8, 2, 64), "UNSUPPORTED"),        # block size 8
+    ([0, 1], [4], 5, (10, 16, 2, 64), "SHAPE"),             # Hq % Hkv
+    ([0, 1], [4], 64, (10, 16, 2, 64), "UNSUPPORTED"),      # group 32 > 16
+])
+def test_planner_rejects_bad_steps(pkv, cu, ctx, hq, desc, err):
+    with pytest.raises(pkv.PkvError) as ei:
+        pkv.plan_step(np.array(cu, np.int32), np.array(ctx, np.int32), hq, pkv.PoolDesc(*desc),
+                      num_sms=152, upload=False)
+    assert err in str(ei.value)
+
+
+def test_planner_reports_small_plan_buffer(pkv):
+    lib = ctypes.CDLL(pkv.library_path())
+    lib.pkv_plan_step.restype = ctypes.c_int32
+    cu = np.array([0, 1, 2], np.int32)
+    ctx = np.array([100, 200], np.int32)
+    desc = pkv.PoolDesc(100, 16, 2, 64)
+    info = pkv.PlanInfo()
+    buf = np.zeros(4, np.int32)
+    st = lib.pkv_plan_step(cu.ctypes.data_as(ctypes.c_void_p), ctx.ctypes.data_as(ctypes.c_void_p),
+                           2, 4, ctypes.byref(desc), 152, buf.ctypes.data_as(ctypes.c_void_p),
+                           ctypes.c_int64(buf.nbytes), ctypes.byref(info))
+    assert st == 5 and info.plan_bytes > buf.nbytes
+
+
+# ---------------------------------------------------------------- entry-point validation
+
+def _raw(pkv):
+    lib = ctypes.CDLL(pkv.library_path())
+    lib.pkv_paged_kv_append.restype = ctypes.c_int32
+    lib.pkv_paged_varlen_attention.restype = ctypes.c_int32
+    return lib
+
+
+FAKE = 0x7F0000001000  # never dereferenced: every call below returns before touching the GPU
+
+
+def test_append_validation_returns_before_launch(pkv):
+    lib = _raw(pkv)
+    P = ctypes.c_void_p
+    ok = pkv.PoolDesc(10, 16, 2, 64)
+    # zero tokens: nothing to do
+    assert lib.pkv_paged_kv_append(None, None, None, 0, None, ctypes.byref(ok), None, None) == 0
+    assert lib.pkv_paged_kv_append(P(FAKE), P(FAKE), None, 3, P(FAKE), ctypes.byref(ok), None, None) == 1
+    assert lib.pkv_paged_kv_append(P(FAKE), P(FAKE), P(FAKE), 3, P(FAKE), None, None, None) == 1
+    bad = pkv.PoolDesc(10, 32, 2, 64)
+    assert lib.pkv_paged_kv_append(P(FAKE), P(FAKE), P(FAKE), 3, P(FAKE), ctypes.byref(bad), None, None) == 4
+    assert lib.pkv_paged_kv_append(P(FAKE + 8), P(FAKE), P(FAKE), 3, P(FAKE), ctypes.byref(ok), None, None) == 8
+    assert lib.pkv_paged_kv_append(P(FAKE), P(FAKE), P(FAKE), -1, P(FAKE), ctypes.byref(ok), None, None) == 2
+    huge = pkv.PoolDesc(1 << 27, 16, 8, 128)   # 2^31 pool rows: TMA coordinates would overflow
+    assert lib.pkv_paged_kv_append(P(FAKE), P(FAKE), P(FAKE), 3, P(FAKE), ctypes.byref(huge), None, None) == 4
+
+
+def test_attention_validation_returns_before_launch(pkv):
+    lib = _raw(pkv)
+    P = ctypes.c_void_p
+    meta = workloads.small_decode()
+    desc = pkv.PoolDesc(meta.num_blocks, 16, meta.num_kv_heads, meta.head_dim)
+    info, host = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, desc,
+                               num_sms=152, upload=False)
+
+    def call(info_=info, desc_=desc, scale=0.1, maxb=meta.max_blocks, ws=P(FAKE), wsb=1 << 30, q=P(FAKE)):
+        return lib.pkv_paged_varlen_attention(q, P(FAKE), P(FAKE), P(FAKE), maxb, P(FAKE),
+                                              ctypes.byref(desc_), ctypes.c_float(scale),
+                                              ctypes.byref(info_), P(FAKE), P(FAKE), ws,
+                                              ctypes.c_int64(wsb), None, None)
+    assert call(q=None) == 1
+    assert call(scale=float("nan")) == 3
+    assert call(maxb=info.max_blocks_needed - 1) == 3
+    if info.workspace_bytes:
+        assert call(wsb=info.workspace_bytes - 1) == 5
+    assert call(ws=P(FAKE + 16)) == 8        # workspace must be 256-byte aligned
+    other = pkv.PoolDesc(meta.num_blocks, 16, meta.num_kv_heads, 64)
+    assert call(desc_=other) == 2
+    empty, _ = pkv.plan_step(np.array([0], np.int32), np.array([], np.int32), meta.num_q_heads,
+                             desc, num_sms=152, upload=False)
+    assert call(info_=empty, q=None) == 0    # nothing to compute

@@ -1,0 +1,228 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU fp64 oracle.
+
+Bars: KV append bit-exact over the whole pool; attention within max-abs 2e-2 and
+mean-abs 2e-3 of the oracle (bf16 output, fp32 accumulation).  The output of an
+exact method rounded once to bf16 is within half a bf16 ulp (<= 2^-9 relative)
+of the oracle, so the same tests also report the error relative to that floor.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS = 2e-2
+MEAN_ABS = 2e-3
+
+
+@pytest.fixture(scope="module")
+def pkv(cuda_device):
+    import paged_kv_attention_append_gb300 as m
+    m.build()
+    return m
+
+
+def bits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def gpu_step(pkv, meta, q, k, v, pool, dev, *, num_sms=None, check_status=True):
+    """Append + attention on the GPU; returns (out bf16 cpu tensor, pool after, status)."""
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    pd = pool.to(dev) if pool.device != dev else pool.clone()
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    pkv.paged_kv_append(kd, vd, torch.from_numpy(meta.slot_mapping).to(dev), pd, dev_status=status)
+    plan = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, pd, num_sms=num_sms)
+    out = pkv.paged_varlen_attention(qd, meta.cu_q_lens, meta.context_lens,
+                                     torch.from_numpy(meta.block_tables).to(dev), pd, meta.scale,
+                                     plan=plan, dev_status=status)
+    torch.cuda.synchronize(dev)
+    st = int(status.item())
+    if check_status:
+        assert st == 0, f"device status {st}: {pkv.DEV_STATUS.get(st)}"
+    return out.cpu(), pd, st
+
+
+def assert_close(got_bf16, want, what=""):
+    got = got_bf16.to(torch.float64).numpy().reshape(want.shape)
+    err = np.abs(got - want)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    mx, mean = float(err.max()), float(err.mean())
+    assert mx <= MAX_ABS and mean <= MEAN_ABS, f"{what}: max|err| {mx:.3e} mean|err| {mean:.3e}"
+    return mx, mean
+
+
+def sample_rows(meta, rng, n):
+    total = meta.total_q * meta.num_q_heads
+    rows = set(rng.choice(total, size=min(n, total), replace=False).tolist())
+    # every sequence's first and last query token, all heads of one of them
+    for s in range(meta.num_seqs):
+        for t in (int(meta.cu_q_lens[s]), int(meta.cu_q_lens[s + 1]) - 1):
+            if t >= int(meta.cu_q_lens[s]):
+                rows.add(t * meta.num_q_heads + int(rng.integers(meta.num_q_heads)))
+    return np.array(sorted(rows), dtype=np.int64)
+
+
+# ------------------------------------------------------------------ append
+
+@pytest.mark.parametrize("name", list(workloads.CONFIGS))
+def test_append_bit_exact_full_size(pkv, cuda_device, name):
+    meta = workloads.make_config(name)
+    big = name in ("high_conc_decode",)
+    q, k, v, pool = workloads.make_values(meta, device=cuda_device if big else "cpu")
+    pool_host = pool.cpu()
+    want, bad = oracle.paged_kv_append(pool_host, k.cpu(), v.cpu(), meta.slot_mapping, block_size=16)
+    assert bad == 0
+    pd = pool.to(cuda_device) if not big else pool
+    status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    pkv.paged_kv_append(k.to(cuda_device), v.to(cuda_device),
+                        torch.from_numpy(meta.slot_mapping).to(cuda_device), pd, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(bits(pd), want)
+
+
+def test_append_padding_and_bad_slot_reported(pkv, cuda_device):
+    meta = workloads.tiny_decode()
+    q, k, v, pool = workloads.make_values(meta)
+    slots = meta.slot_mapping.copy()
+    slots[1] = -1
+    slots[2] = meta.num_blocks * 16 + 5
+    want, bad = oracle.paged_kv_append(pool, k, v, slots, block_size=16)
+    assert bad == 1
+    pd = pool.to(cuda_device)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    pkv.paged_kv_append(k.to(cuda_device), v.to(cuda_device), torch.from_numpy(slots).to(cuda_device),
+                        pd, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 1
+    assert np.array_equal(bits(pd), want)
+
+
+# ------------------------------------------------------------------ attention, full oracle
+
+@pytest.mark.parametrize("name", ["tiny_decode", "small_decode", "shared_prefix_verify"])
+def test_attention_matches_oracle_every_row(pkv, cuda_device, name):
+    meta = workloads.make_config(name)
+    q, k, v, pool = workloads.make_values(meta)
+    want, pool_want = oracle.run_step(meta, q, k, v, pool)
+    out, pd, _ = gpu_step(pkv, meta, q, k, v, pool, cuda_device)
+    assert np.array_equal(bits(pd), pool_want)
+    assert_close(out, want, name)
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_attention_random_mixed_steps(pkv, cuda_device, seed):
+    rng = np.random.default_rng(1000 + seed)
+    meta = workloads.random_step(rng, max_ctx=int(rng.choice([40, 300, 1500])))
+    q, k, v, pool = workloads.make_values(meta)
+    want, _ = oracle.run_step(meta, q, k, v, pool)
+    out, _, _ = gpu_step(pkv, meta, q, k, v, pool, cuda_device,
+                         num_sms=int(rng.choice([1, 8, 152])))
+    assert_close(out, want, f"seed {seed}")
+
+
+# ------------------------------------------------------------------ attention, full size, sampled rows
+
+@pytest.mark.parametrize("name", ["agent_mixed", "high_conc_decode", "shared_prefix_verify", "small_decode"])
+def test_attention_full_size_sampled_rows(pkv, cuda_device, name):
+    meta = workloads.make_config(name)
+    q, k, v, pool = workloads.make_values(meta, device=cuda_device)
+    qh, kh, vh, ph = q.cpu(), k.cpu(), v.cpu(), pool.cpu()
+    out, _, _ = gpu_step(pkv, meta, q, k, v, pool, cuda_device)
+    rows = sample_rows(meta, np.random.default_rng(5), 3000)
+    want, _ = oracle.run_step(meta, qh, kh, vh, ph, rows=rows)
+    got = out.view(-1, meta.head_dim)[torch.from_numpy(rows)]
+    assert_close(got, want, name)
+
+
+# ------------------------------------------------------------------ invariants on the GPU
+
+def test_split_count_invariance(pkv, cuda_device):
+    meta = workloads.small_decode()
+    q, k, v, pool = workloads.make_values(meta)
+    a, _, _ = gpu_step(pkv, meta, q, k, v, pool, cuda_device, num_sms=1)      # one split each
+    b, _, _ = gpu_step(pkv, meta, q, k, v, pool, cuda_device, num_sms=1000)   # many splits
+    diff = (a.double() - b.double()).abs()
+    assert float(diff.max()) <= 2e-2 and float(diff.mean()) <= 2e-3
+
+
+def test_block_permutation_is_bitwise_invariant(pkv, cuda_device):
+    rng = np.random.default_rng(3)
+    meta = workloads.random_step(rng, num_seqs=5, max_ctx=700)
+    q, k, v, pool = workloads.make_values(meta)
+    a, _, _ = gpu_step(pkv, meta, q, k, v, pool, cuda_device)
+    perm = rng.permutation(meta.num_blocks)
+    pool2 = torch.empty_like(pool)
+    pool2[torch.from_numpy(perm)] = pool
+    tables2 = np.where(meta.block_tables >= 0, perm[np.maximum(meta.block_tables, 0)], -1).astype(np.int32)
+    meta2 = workloads.StepMeta(**{**meta.__dict__, "block_tables": tables2,
+                                  "slot_mapping": (perm[meta.slot_mapping // 16] * 16 +
+                                                   meta.slot_mapping % 16).astype(np.int32)})
+    b, _, _ = gpu_step(pkv, meta2, q, k, v, pool2, cuda_device)
+    assert torch.equal(a, b)
+
+
+def test_constant_v_and_single_key(pkv, cuda_device):
+    meta = workloads.build_step("t", 9, [1, 1, 3], [1, 200, 3], 8, 2, 128, pool_blocks=30)
+    q, k, v, pool = workloads.make_values(meta)
+    want, _ = oracle.run_step(meta, q, k, v, pool)
+    out, _, _ = gpu_step(pkv, meta, q, k, v, pool, cuda_device)
+    assert_close(out, want)
+    # a single visible key returns its V exactly (weight 1, one bf16 rounding of an exact value)
+    assert torch.equal(out[0].float(), v[0].repeat_interleave(4, dim=0).float())
+    vv = v.clone()
+    vv[:] = 0.375
+    pool_c = pool.clone()
+    pool_c[:, 1] = 0.375
+    out2, _, _ = gpu_step(pkv, meta, q, k, vv, pool_c, cuda_device)
+    assert torch.all(out2.float() == 0.375)
+
+
+def test_edge_shapes(pkv, cuda_device):
+    cases = [
+        ([1], [1], 16, 1, 128),          # group 16, single key
+        ([1], [32768], 32, 8, 128),      # longest context of the high-concurrency mix
+        ([64], [64], 4, 4, 64),          # prefill from an empty cache (q_len = ctx)
+        ([0, 2, 0, 1], [5, 48, 7, 16], 8, 2, 64),   # q_len 0 sequences, block-aligned ctx
+        ([2] * 9, [17, 18, 31, 32, 33, 47, 48, 49, 2], 32, 8, 128),  # verify pairs on block edges
+    ]
+    for i, (ql, cl, hq, hkv, d) in enumerate(cases):
+        meta = workloads.build_step("edge", 40 + i, ql, cl, hq, hkv, d)
+        q, k, v, pool = workloads.make_values(meta)
+        want, _ = oracle.run_step(meta, q, k, v, pool)
+        out, _, _ = gpu_step(pkv, meta, q, k, v, pool, cuda_device)
+        assert_close(out, want, f"edge case {i}")
+
+
+def test_empty_step_is_a_no_op(pkv, cuda_device):
+    pool = torch.zeros(4, 2, 2, 16, 64, dtype=torch.bfloat16, device=cuda_device)
+    q = torch.zeros(0, 4, 64, dtype=torch.bfloat16, device=cuda_device)
+    before = pkv.kernel_launch_count()
+    out = pkv.paged_varlen_attention(q, np.array([0], np.int32), np.array([], np.int32),
+                                     torch.zeros(0, 1, dtype=torch.int32, device=cuda_device), pool, 0.1)
+    assert out.shape == (0, 4, 64) and pkv.kernel_launch_count() == before
+
+
+def test_bad_block_id_is_reported_not_faulted(pkv, cuda_device):
+    meta = workloads.build_step("t", 12, [1, 1], [100, 60], 8, 2, 128, pool_blocks=20)
+    q, k, v, pool = workloads.make_values(meta)
+    tables = meta.block_tables.copy()
+    tables[0, 3] = meta.num_blocks + 7      # outside the pool
+    bad = workloads.StepMeta(**{**meta.__dict__, "block_tables": tables})
+    out, _, st = gpu_step(pkv, bad, q, k, v, pool, cuda_device, check_status=False)
+    assert st == 2
+    # the other sequence is unaffected
+    want, _ = oracle.run_step(meta, q, k, v, pool)
+    assert_close(out[1:], want[1:])
+
+
+def test_in_tree_library_is_loaded(pkv):
+    import os
+    assert os.path.exists(pkv.library_path())
+    maps = open("/proc/self/maps").read()
+    assert pkv.library_path() in maps
