@@ -191,6 +191,46 @@ PKV_API pkv_status pkv_paged_varlen_attention(const void *q, const int32_t *cu_q
                                       void *workspace, int64_t workspace_bytes,
                                       int32_t *dev_status, pkv_stream stream);
 
+/*
+ * Size of the fixed scratch array used by pkv_paged_varlen_attention_noalloc
+ * (16 MiB).  Every GPU that loads this library holds these bytes until the
+ * process exits.
+ */
+#define PKV_NOALLOC_SCRATCH_BYTES (16 * 1024 * 1024)
+
+/*
+ * pkv_paged_varlen_attention without a workspace argument, for callers that
+ * cannot allocate device memory (no cudaMalloc available or allowed: a plugin
+ * that is handed only the step's tensors, a path where an allocation could
+ * block or fail, a runtime that pre-budgets all device memory).  The pages have
+ * no counterpart to this call; it exists only for such callers.
+ *
+ * Same arguments, computation and results as pkv_paged_varlen_attention; the
+ * caller still passes every input and the output.  The split-KV partial
+ * results go to a fixed array in the library's device image
+ * (PKV_NOALLOC_SCRATCH_BYTES), so this call allocates nothing: no cudaMalloc,
+ * no cudaFree, no allocating library routine.
+ *  - Returns PKV_ERR_WORKSPACE, before anything is enqueued, when the step
+ *    needs more scratch than that (info->workspace_bytes >
+ *    PKV_NOALLOC_SCRATCH_BYTES); plan such steps with more SMs' worth of
+ *    smaller splits or use pkv_paged_varlen_attention.
+ *  - The calling thread's current device must be the device of the buffers and
+ *    the stream.  The first call made with a given device current looks up the
+ *    array's device address on that device (cudaGetSymbolAddress, which may
+ *    load the library's module there); make that first call before any stream
+ *    capture.
+ *  - All calls on a device share the one array and it keeps the last call's
+ *    contents.  Nothing in it needs to start at zero (every partial is written
+ *    before it is read).  Calls whose work overlaps on the GPU (different
+ *    streams, or different host threads, without ordering between them) race
+ *    on the array and give wrong results: order them on one stream.
+ */
+PKV_API pkv_status pkv_paged_varlen_attention_noalloc(
+    const void *q, const int32_t *cu_q_lens, const int32_t *context_lens,
+    const int32_t *block_tables, int32_t max_blocks_per_seq, const void *kv_pool,
+    const pkv_pool_desc *desc, float scale, const pkv_plan_info *info, const void *plan_dev,
+    void *out, int32_t *dev_status, pkv_stream stream);
+
 #ifdef __cplusplus
 }
 #endif
