@@ -7,8 +7,9 @@ step plan (host step metadata), KV append of the step's new tokens, split-KV
 attention (+ tensor-core prefill tiles when present) and the LSE merge.
 
 * value: KV tokens/s = sum(context_lens) / device time per step, inputs resident
-  in HBM, the step replayed from a CUDA graph, L2 flushed (256 MB write) before
-  every timed step and the flush kept outside the per-step CUDA-event pairs.
+  in HBM, the step replayed from a CUDA graph, L2 flushed before every timed
+  step (a 256 MB buffer written, then another 256 MB read, so L2 holds only
+  clean unrelated lines) and the flush kept outside the per-step CUDA-event pairs.
 * roofline: the decode kernel alone, timed with CUDA events recorded on its
   launch stream around each launch (library profiling hook), algorithmic bytes
   (KV + Q + O + metadata) / mean duration vs the measured HBM copy bandwidth.
@@ -213,7 +214,13 @@ def bench_pkv(args):
     ctx_d = torch.from_numpy(meta.context_lens).to(dev)
     bt_d = torch.from_numpy(meta.block_tables).to(dev)
     out = torch.empty_like(q)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    flush_w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_acc = torch.zeros((), dtype=torch.float32, device=dev)
+
+    def flush_l2():
+        flush_w.zero_()                          # write more than L2 holds ...
+        torch.sum(flush_r, dim=0, out=flush_acc)  # ... then read more, leaving clean lines
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(dev)
 
@@ -245,7 +252,7 @@ def bench_pkv(args):
     launches_per_step = pkv.kernel_launch_count() - launches_before
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            flush.zero_()
+            flush_l2()
             graph.replay()
     torch.cuda.synchronize(dev)
 
@@ -257,7 +264,7 @@ def bench_pkv(args):
     with ClockSampler(local) as clk:
         with torch.cuda.stream(stream):
             for a, b in ev:
-                flush.zero_()
+                flush_l2()
                 a.record(stream)
                 graph.replay()
                 b.record(stream)
@@ -271,7 +278,7 @@ def bench_pkv(args):
                 b.record(stream)
             torch.cuda.synchronize(dev)
             for a, b in k_ev:
-                flush.zero_()
+                flush_l2()
                 pkv.set_profile_events("decode", a, b)
                 pkv.paged_varlen_attention(q, cu_d, ctx_d, bt_d, pool, meta.scale, plan=plan,
                                            out=out, dev_status=status)
@@ -336,7 +343,8 @@ def bench_pkv(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16, shapes of the named workload)",
         "config": {**workloads.describe(meta), "parallelism": f"replicas x{ws}" if ws > 1 else "single",
-                   "l2": f"flushed ({L2_FLUSH_BYTES >> 20} MB write) before every timed step",
+                   "l2": f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MB written, then "
+                         f"{L2_FLUSH_BYTES >> 20} MB read)",
                    "timing": "CUDA graph replay per step, CUDA events per step"},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved,
@@ -350,8 +358,8 @@ def bench_pkv(args):
         "clocks": clocks,
         "cpu_baseline": None if cpu is None else {k2: cpu[k2] for k2 in
                                                   ("value", "unit", "cores", "kind", "sample")},
-        "plan": {"decode_tiles": info.num_decode_tiles, "merge_groups": info.num_merge_groups,
-                 "prefill_tiles": info.num_prefill_tiles, "split_blocks": info.split_blocks},
+        "plan": {"decode_warps": info.num_decode_warps, "decode_pieces": info.num_decode_pieces,
+                 "merge_groups": info.num_merge_groups, "prefill_tiles": info.num_prefill_tiles},
     }
     if meta.unique_blocks() * 16 < kv_tok:
         line["unique_gbs"] = unique_bytes(meta) / (decode_ms * 1e-3) / 1e9

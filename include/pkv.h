@@ -96,14 +96,15 @@ typedef struct pkv_plan_info {
   int32_t num_kv_heads;
   int32_t head_dim;
   int32_t total_q;
-  int32_t num_decode_tiles;  /* split-KV work items (each runs for every KV head) */
-  int32_t num_merge_groups;  /* row groups whose keys were split over several tiles */
-  int32_t num_partials;      /* partial-result slots used by split tiles */
-  int32_t num_prefill_tiles; /* tensor-core work items (128 query rows x 1 query head) */
+  int32_t num_decode_warps;  /* warps of the split-KV kernel; each streams an equal share of keys */
+  int32_t num_decode_pieces; /* (row group, KV head, key range) pieces over all decode warps */
+  int32_t num_merge_groups;  /* (row group, KV head) pairs whose keys span several pieces */
+  int32_t num_partials;      /* partial-result slots (one per piece of a merge group) */
+  int32_t num_prefill_tiles; /* tensor-core work items: up to 128 query tokens x 1 query head */
   int32_t num_kernels;       /* kernel launches one pkv_paged_varlen_attention call makes */
-  int32_t split_blocks;      /* KV blocks per split chosen for this step */
   int32_t max_blocks_needed; /* max over sequences of ceil(context_len / block_size) */
   int64_t kv_tokens;         /* sum of context_lens over sequences with q_len > 0 */
+  int64_t decode_blocks;     /* (KV block, KV head) pairs streamed by the split-KV kernel */
   int64_t plan_bytes;        /* bytes of the plan buffer (host, then device copy) */
   int64_t workspace_bytes;   /* device workspace the attention call needs */
 } pkv_plan_info;

@@ -48,10 +48,10 @@ class PoolDesc(ctypes.Structure):
 
 class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
-        "num_seqs", "num_q_heads", "num_kv_heads", "head_dim", "total_q", "num_decode_tiles",
-        "num_merge_groups", "num_partials", "num_prefill_tiles", "num_kernels", "split_blocks",
-        "max_blocks_needed")] + [(n, ctypes.c_int64) for n in ("kv_tokens", "plan_bytes",
-                                                              "workspace_bytes")]
+        "num_seqs", "num_q_heads", "num_kv_heads", "head_dim", "total_q", "num_decode_warps",
+        "num_decode_pieces", "num_merge_groups", "num_partials", "num_prefill_tiles", "num_kernels",
+        "max_blocks_needed")] + [(n, ctypes.c_int64) for n in ("kv_tokens", "decode_blocks",
+                                                              "plan_bytes", "workspace_bytes")]
 
     def as_dict(self):
         return {n: getattr(self, n) for n, _ in self._fields_}

@@ -42,7 +42,7 @@ static pkv_status check_pool(const pkv_pool_desc *desc) {
 
 using namespace pkv;
 
-extern "C" int32_t pkv_version(void) { return 100; }
+extern "C" int32_t pkv_version(void) { return 200; }
 
 extern "C" int64_t pkv_kernel_launch_count(void) { return g_launches.load(); }
 
@@ -119,21 +119,25 @@ extern "C" pkv_status pkv_paged_varlen_attention(
   a.num_seqs = info->num_seqs;
   a.scale = scale;
   const char *pb = static_cast<const char *>(plan_dev);
-  a.decode_tiles = reinterpret_cast<const DecodeTile *>(pb + plan_decode_off());
-  a.num_decode_tiles = info->num_decode_tiles;
-  a.merge_groups = reinterpret_cast<const MergeGroup *>(pb + plan_merge_off(info->num_decode_tiles));
+  const PlanOffsets off = plan_offsets(info->num_decode_warps, info->num_decode_pieces,
+                                       info->num_merge_groups, info->num_prefill_tiles);
+  a.warp_begin = reinterpret_cast<const int32_t *>(pb + off.warp_begin);
+  a.num_decode_warps = info->num_decode_warps;
+  a.pieces = reinterpret_cast<const Piece *>(pb + off.pieces);
+  a.merge_groups = reinterpret_cast<const MergeGroup *>(pb + off.merges);
   a.num_merge_groups = info->num_merge_groups;
-  a.prefill_tiles = reinterpret_cast<const PrefillTile *>(
-      pb + plan_prefill_off(info->num_decode_tiles, info->num_merge_groups));
+  a.prefill_tiles = reinterpret_cast<const PrefillTile *>(pb + off.prefill);
   a.num_prefill_tiles = info->num_prefill_tiles;
   char *wb = static_cast<char *>(workspace);
   a.part_o = reinterpret_cast<float *>(wb);
   a.part_ml = reinterpret_cast<float *>(
-      wb ? wb + ws_part_o_bytes(info->num_partials, desc->num_kv_heads, desc->head_dim) : nullptr);
+      wb ? wb + ws_part_o_bytes(info->num_partials, desc->head_dim) : nullptr);
   a.dev_status = dev_status;
   a.stream = stream;
 
+  if (info->plan_bytes != off.total) return PKV_ERR_SHAPE;
   int launches = 0;
+  if (launch_prefill(a, &launches)) return PKV_ERR_CUDA;
   if (launch_decode(a, &launches)) return PKV_ERR_CUDA;
   if (launch_merge(a, &launches)) return PKV_ERR_CUDA;
   return PKV_OK;

@@ -1,4 +1,4 @@
-// Split-KV paged attention for decode-class row groups, plus the LSE merge.
+// Split-KV paged attention for decode-class rows, plus the LSE merge.
 //
 // What it computes is the packed varlen attention of the vllm-metal page
 // ("Replacing attention, reusing the rest"): every query row attends over the
@@ -6,26 +6,28 @@
 // blocks through the sequence's block table.  The page's own kernel is a Metal
 // port of a Triton kernel; this is a GB300 design:
 //
-//  * Work item = (row group, key split) x one KV head (grid.y).  A row group is
-//    n_q query tokens x all `group` query heads sharing the KV head (<= 16
-//    rows), so each KV block is read from HBM once and serves every query head
-//    of the group (GQA sharing inside the CTA).
-//  * 4 warps per CTA; each warp owns a private NSTAGE-deep ring in shared
-//    memory and streams every 4th block of the split through it with TMA
-//    (cp.async.bulk.tensor, 128-byte swizzle): one elected lane issues the
-//    K and V boxes of a block against an mbarrier, the warp waits on the
-//    barrier's phase, computes, and the lane refills the slot.  No CTA-wide
-//    barrier inside the key loop.
+//  * The host planner lays every (row group, KV head) segment's blocks end to
+//    end and cuts them into equal contiguous ranges, one per warp (8 warps per
+//    SM, one wave).  A warp's range crosses one or more segments; each piece is
+//    finished in registers and written either as final output or as an fp32
+//    partial.  No CTA-wide barrier, no shared-memory merge.
+//  * A row group is n_q query tokens x all `group` query heads sharing the KV
+//    head (<= 16 rows = one m16 MMA tile), so each KV block read from HBM serves
+//    every query head of the group (GQA sharing).
+//  * Each warp owns a private NSTAGE-deep ring in shared memory.  Lane 0 issues
+//    the K and V boxes of the next block of the warp's stream with TMA
+//    (cp.async.bulk.tensor, 128-byte swizzle) against the stage's mbarrier; the
+//    stream runs on across piece boundaries, so HBM requests never stop at a
+//    segment edge.
 //  * Q K^T and P V run on mma.sync m16n8k16 (bf16 in, fp32 accumulate) with
 //    fragments read straight from the swizzled tiles: the head_dim index is
 //    permuted identically in the Q and K fragments so each lane reads whole
 //    16-byte chunks, and the permutation is chosen so every 8-lane shared
 //    memory phase hits 8 distinct 16-byte bank groups (conflict-free).
-//  * Online softmax in the log2 domain with warp-shuffle row max/sum; the four
-//    warps' (m, l, O) states are merged through shared memory at the end.
-//  * A row group split over several CTAs writes unnormalised fp32 partials
-//    (O, m, l); merge_kernel combines them:  M = max_j m_j,
-//    out = sum_j 2^(m_j - M) O_j / sum_j 2^(m_j - M) l_j.
+//  * Online softmax in the log2 domain with warp-shuffle row max; O is rescaled
+//    only when some row's max moved.
+//  * merge_kernel combines the partials of a segment cut into several pieces:
+//    M = max_j m_j, out = sum_j 2^(m_j - M) O_j / sum_j 2^(m_j - M) l_j.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -37,7 +39,7 @@ namespace pkv {
 
 namespace {
 
-constexpr int kWarps = 4;
+constexpr int kWarps = kDecodeWarpsPerCta;
 constexpr int kThreads = kWarps * 32;
 constexpr int kBoxBytes = kBlockSize * 128;  // 16 rows x 64 bf16, 128-byte swizzled
 
@@ -48,9 +50,8 @@ struct DecodeCfg {
   static constexpr int kStageBytes = 2 * kSlabBytes;
   static constexpr int kRingBytes = NSTAGE * kStageBytes;
   static constexpr int kBarOffset = kWarps * kRingBytes;
-  static constexpr int kSmemBytes = kBarOffset + kWarps * NSTAGE * 8 + 1024;
-  static_assert(kRingBytes >= kRowsPerTile * D * 4 + kRowsPerTile * 8,
-                "the merge scratch must fit in a warp's ring");
+  static constexpr int kFlagOffset = kBarOffset + kWarps * NSTAGE * 8;
+  static constexpr int kSmemBytes = kFlagOffset + kWarps * NSTAGE * 4 + 1024;
 };
 
 struct DecodeParams {
@@ -59,11 +60,14 @@ struct DecodeParams {
   const int32_t *cu_q_lens;
   const int32_t *context_lens;
   const int32_t *block_tables;
-  const DecodeTile *tiles;
+  const int32_t *warp_begin;
+  const Piece *pieces;
   const MergeGroup *merges;
   float *part_o;
   float2 *part_ml;
   int32_t *dev_status;
+  int32_t num_warps;
+  int32_t num_seqs;
   int32_t max_blocks_per_seq;
   int32_t num_blocks;
   int32_t num_q_heads;
@@ -88,282 +92,306 @@ __global__ void __launch_bounds__(kThreads, 2)
                                               ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = lane >> 2, c = lane & 3;
-  const int h = blockIdx.y;
-  const DecodeTile tile = p.tiles[blockIdx.x];
-
-  // ---- row group metadata from the device copies of the step arrays
-  const int seq = tile.seq;
-  const int cu0 = __ldg(p.cu_q_lens + seq);
-  const int qs = __ldg(p.cu_q_lens + seq + 1) - cu0;
-  const int ctx = __ldg(p.context_lens + seq);
-  if (tile.qi0 < 0 || tile.n_q < 1 || tile.qi0 + tile.n_q > qs || qs > ctx ||
-      tile.n_q * p.group > kRowsPerTile || tile.kb_begin < 0) {
-    if (threadIdx.x == 0) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
-    return;
-  }
-  const int G = p.group;
-  const int R = tile.n_q * G;
-  const int q_pos0 = ctx - qs + tile.qi0;  // causal position of the group's first token
-  const int nb_need = (q_pos0 + tile.n_q - 1) / kBlockSize + 1;
-  int kb_end = min(tile.kb_end, nb_need);
-  kb_end = min(kb_end, p.max_blocks_per_seq);
-  if (threadIdx.x == 0 && (kb_end != tile.kb_end || (tile.last && tile.kb_end != nb_need)))
-    report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
-  const int kb0 = tile.kb_begin;
-  const int nblk = max(0, kb_end - kb0);
-  const int n_my = warp < nblk ? (nblk - warp + kWarps - 1) / kWarps : 0;
-  const int32_t *table = p.block_tables + (int64_t)seq * p.max_blocks_per_seq;
+  const int gw = blockIdx.x * kWarps + warp;
+  if (gw >= p.num_warps) return;
+  const int pb = __ldg(p.warp_begin + gw), pe = __ldg(p.warp_begin + gw + 1);
+  if (pb >= pe) return;
   const int hkv = p.num_kv_heads;
+  const int G = p.group;
 
   uint8_t *ring = smem + warp * C::kRingBytes;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOffset) + warp * NSTAGE;
+  int *stage_ok = reinterpret_cast<int *>(smem + C::kFlagOffset) + warp * NSTAGE;
   if (lane == 0) {
     for (int s = 0; s < NSTAGE; ++s) mbar_init(smem_u32(&bars[s]), 1);
     fence_mbar_init();
+    prefetch_tmap(&pool_map);
   }
-  if (threadIdx.x == 0) prefetch_tmap(&pool_map);
   __syncwarp();
 
-  auto issue = [&](int i) {  // lane 0 only: load local block i into its stage
-    const int kb = kb0 + warp + i * kWarps;
-    const int stage = i % NSTAGE;
-    const uint32_t bar = smem_u32(&bars[stage]);
-    const int phys = __ldg(table + kb);
-    if (phys >= 0 && phys < p.num_blocks) {
-      mbar_arrive_expect_tx(bar, C::kStageBytes);
-      const int row_k = ((phys * 2 + 0) * hkv + h) * kBlockSize;
-      const int row_v = row_k + hkv * kBlockSize;
-      const uint32_t dst = smem_u32(ring + stage * C::kStageBytes);
-#pragma unroll
-      for (int hh = 0; hh < C::kHalves; ++hh) {
-        tma_load_2d(dst + hh * kBoxBytes, &pool_map, hh * 64, row_k, bar);
-        tma_load_2d(dst + C::kSlabBytes + hh * kBoxBytes, &pool_map, hh * 64, row_v, bar);
+  // ---- producer: walks the warp's pieces block by block.  Called by the whole
+  // warp (uniform control flow); lane 0 issues the copies.  The block table is
+  // read 32 entries at a time with one coalesced warp load and the entries are
+  // shuffled out, so refilling a stage never waits on a dependent global load.
+  int ppi = pb, pkb = 0, issued = 0;
+  int win_base = 0, win_val = -1;  // table window: lane i holds entry win_base + i
+  bool win_ok = false;
+  Piece pp = p.pieces[pb];
+  pkb = pp.kb_begin;
+  auto issue_next = [&](int stage) {
+    while (ppi < pe && pkb >= pp.kb_end) {
+      if (++ppi < pe) {
+        pp = p.pieces[ppi];
+        pkb = pp.kb_begin;
+        win_ok = false;
       }
-    } else {
-      report(p.dev_status, PKV_DEV_BAD_BLOCK);
-      mbar_arrive(bar);  // complete the phase without data; the block is skipped
     }
+    if (ppi >= pe) return;
+    const uint32_t bar = smem_u32(&bars[stage]);
+    const bool in_table = pp.seq >= 0 && pp.seq < p.num_seqs && pp.h >= 0 && pp.h < hkv &&
+                          pkb >= 0 && pkb < p.max_blocks_per_seq;
+    if (in_table && (!win_ok || pkb >= win_base + 32)) {
+      win_base = pkb;
+      const int idx = pkb + lane;
+      win_val = idx < min(pp.kb_end, p.max_blocks_per_seq)
+                    ? __ldg(p.block_tables + (int64_t)pp.seq * p.max_blocks_per_seq + idx)
+                    : -1;
+      win_ok = true;
+    }
+    const int phys = __shfl_sync(0xffffffffu, win_val, (pkb - win_base) & 31);
+    const bool ok = in_table && phys >= 0 && phys < p.num_blocks;
+    if (lane == 0) {
+      stage_ok[stage] = ok ? 1 : 0;
+      if (ok) {
+        mbar_arrive_expect_tx(bar, C::kStageBytes);
+        const int row_k = ((phys * 2 + 0) * hkv + pp.h) * kBlockSize;
+        const int row_v = row_k + hkv * kBlockSize;
+        const uint32_t dst = smem_u32(ring + stage * C::kStageBytes);
+#pragma unroll
+        for (int hh = 0; hh < C::kHalves; ++hh) {
+          tma_load_2d(dst + hh * kBoxBytes, &pool_map, hh * 64, row_k, bar);
+          tma_load_2d(dst + C::kSlabBytes + hh * kBoxBytes, &pool_map, hh * 64, row_v, bar);
+        }
+      } else {
+        report(p.dev_status, in_table ? PKV_DEV_BAD_BLOCK : PKV_DEV_PLAN_MISMATCH);
+        mbar_arrive(bar);  // complete the phase without data; the block is skipped
+      }
+    }
+    ++pkb;
+    ++issued;
   };
-  int issued = min(NSTAGE, n_my);
-  if (lane == 0)
-    for (int i = 0; i < issued; ++i) issue(i);
+  for (int s = 0; s < NSTAGE; ++s) issue_next(s);
 
-  // ---- Q fragments (A operand), head_dim permuted to match the K fragments
-  uint32_t qa[2 * kL][4];
-  const int lim_lo = r < R ? q_pos0 + r / G : -1;            // last visible key of row r
-  const int lim_hi = r + 8 < R ? q_pos0 + (r + 8) / G : -1;  // ... of row r + 8
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const int row = r + 8 * half;
-    const bool valid = row < R;
-    const __nv_bfloat16 *qrow =
-        p.q + ((int64_t)(cu0 + tile.qi0 + (valid ? row / G : 0)) * p.num_q_heads + h * G +
-               (valid ? row % G : 0)) *
-                  D;
-#pragma unroll
-    for (int L = 0; L < kL; ++L) {
-      const int e = 8 * (L >> 1) + 2 * c + (L & 1);
-      uint4 v = valid ? ldg128_nc(qrow + 8 * e) : make_uint4(0, 0, 0, 0);
-      qa[2 * L][half] = v.x;
-      qa[2 * L][2 + half] = v.y;
-      qa[2 * L + 1][half] = v.z;
-      qa[2 * L + 1][2 + half] = v.w;
-    }
-  }
-
-  float o[kNt][4];
-#pragma unroll
-  for (int nt = 0; nt < kNt; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-  float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
   const float sl2 = p.scale_log2;
-
+  int stage = 0;
+  uint32_t phase = 0;
   int consumed = 0;
   bool abandoned = false;
-  for (int i = 0; i < n_my; ++i) {
-    const int stage = i % NSTAGE;
-    const bool ok = mbar_wait(smem_u32(&bars[stage]), (uint32_t)((i / NSTAGE) & 1));
-    if (!__all_sync(0xffffffffu, ok)) {
-      if (lane == 0) report(p.dev_status, PKV_DEV_TIMEOUT);
-      abandoned = true;
-      break;
+
+  for (int pi = pb; pi < pe && !abandoned; ++pi) {
+    const Piece pc = p.pieces[pi];
+    // ---- piece metadata, checked against the device copies of the step arrays
+    bool valid = pc.seq >= 0 && pc.seq < p.num_seqs && pc.h >= 0 && pc.h < hkv &&
+                 pc.kb_begin >= 0 && pc.kb_begin <= pc.kb_end &&
+                 pc.kb_end <= p.max_blocks_per_seq;
+    int cu0 = 0, qs = 0, ctx = 0;
+    if (valid) {
+      cu0 = __ldg(p.cu_q_lens + pc.seq);
+      qs = __ldg(p.cu_q_lens + pc.seq + 1) - cu0;
+      ctx = __ldg(p.context_lens + pc.seq);
+      valid = pc.qi0 >= 0 && pc.n_q >= 1 && pc.qi0 + pc.n_q <= qs && qs <= ctx &&
+              pc.n_q * G <= kRowsPerTile &&
+              pc.kb_end <= (ctx - qs + pc.qi0 + pc.n_q - 1) / kBlockSize + 1;
     }
-    consumed = i + 1;
-    const int kb = kb0 + warp + i * kWarps;
-    const int phys = __ldg(table + kb);
-    if (phys >= 0 && phys < p.num_blocks) {
-      const uint32_t sK = smem_u32(ring + stage * C::kStageBytes);
-      const uint32_t sV = sK + C::kSlabBytes;
-      // S = Q K^T for the block's 16 keys (two n-tiles of 8 keys)
-      float s[2][4];
+    if (!valid && lane == 0) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
+    const int R = valid ? pc.n_q * G : 0;
+    const int q_pos0 = ctx - qs + pc.qi0;  // causal position of the group's first token
+    const int lim_lo = r < R ? q_pos0 + r / G : -1;            // last visible key of row r
+    const int lim_hi = r + 8 < R ? q_pos0 + (r + 8) / G : -1;  // ... of row r + 8
+
+    // ---- Q fragments (A operand), head_dim permuted to match the K fragments
+    uint32_t qa[2 * kL][4];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-        const int t = r + 8 * nt;
+    for (int half = 0; half < 2; ++half) {
+      const int row = r + 8 * half;
+      const bool rv = row < R;
+      const __nv_bfloat16 *qrow =
+          p.q + ((int64_t)(cu0 + pc.qi0 + (rv ? row / G : 0)) * p.num_q_heads + pc.h * G +
+                 (rv ? row % G : 0)) * D;
 #pragma unroll
-        for (int L = 0; L < kL; ++L) {
-          const int e = 8 * (L >> 1) + 2 * c + (L & 1);
-          const uint4 kv = lds128(sK + (e >> 3) * kBoxBytes + swz(t, e & 7));
-          mma_16816(s[nt], qa[2 * L][0], qa[2 * L][1], qa[2 * L][2], qa[2 * L][3], kv.x, kv.y);
-          mma_16816(s[nt], qa[2 * L + 1][0], qa[2 * L + 1][1], qa[2 * L + 1][2],
-                    qa[2 * L + 1][3], kv.z, kv.w);
-        }
+      for (int L = 0; L < kL; ++L) {
+        const int e = 8 * (L >> 1) + 2 * c + (L & 1);
+        const uint4 v = rv ? ldg128_nc(qrow + 8 * e) : make_uint4(0, 0, 0, 0);
+        qa[2 * L][half] = v.x;
+        qa[2 * L][2 + half] = v.y;
+        qa[2 * L + 1][half] = v.z;
+        qa[2 * L + 1][2 + half] = v.w;
       }
-      // scale to log2 units; causal / context mask on the boundary blocks
-      const int p0 = kb * kBlockSize;
-      const bool need_mask = p0 + kBlockSize - 1 > q_pos0;
+    }
+
+    float o[kNt][4];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+    for (int nt = 0; nt < kNt; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+    float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+
+    for (int kb = pc.kb_begin; kb < pc.kb_end; ++kb) {
+      const bool ok = mbar_wait(smem_u32(&bars[stage]), phase);
+      if (!__all_sync(0xffffffffu, ok)) {
+        if (lane == 0) report(p.dev_status, PKV_DEV_TIMEOUT);
+        abandoned = true;
+        break;
+      }
+      ++consumed;
+      if (valid && stage_ok[stage]) {
+        const uint32_t sK = smem_u32(ring + stage * C::kStageBytes);
+        const uint32_t sV = sK + C::kSlabBytes;
+        // S = Q K^T for the block's 16 keys (two n-tiles of 8 keys)
+        float s[2][4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          float x = s[nt][j] * sl2;
-          if (need_mask) {
-            const int pos = p0 + 8 * nt + 2 * c + (j & 1);
-            if (pos > (j < 2 ? lim_lo : lim_hi)) x = -INFINITY;
+        for (int nt = 0; nt < 2; ++nt) {
+          s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+          const int t = r + 8 * nt;
+#pragma unroll
+          for (int L = 0; L < kL; ++L) {
+            const int e = 8 * (L >> 1) + 2 * c + (L & 1);
+            const uint4 kv = lds128(sK + (e >> 3) * kBoxBytes + swz(t, e & 7));
+            mma_16816(s[nt], qa[2 * L][0], qa[2 * L][1], qa[2 * L][2], qa[2 * L][3], kv.x, kv.y);
+            mma_16816(s[nt], qa[2 * L + 1][0], qa[2 * L + 1][1], qa[2 * L + 1][2],
+                      qa[2 * L + 1][3], kv.z, kv.w);
           }
-          s[nt][j] = x;
         }
-      // online softmax (rows r and r + 8; the 4 lanes of a row hold 4 keys each)
-      float mx_lo = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
-      float mx_hi = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
-      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
-      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
-      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
-      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
-      const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
-      const float base_lo = mn_lo == -INFINITY ? 0.f : mn_lo;
-      const float base_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
-      const float a_lo = fast_exp2(m_lo - base_lo), a_hi = fast_exp2(m_hi - base_hi);
-      m_lo = mn_lo;
-      m_hi = mn_hi;
+        // scale to log2 units; causal / context mask on the boundary blocks
+        const int p0 = kb * kBlockSize;
+        const bool need_mask = p0 + kBlockSize - 1 > q_pos0;
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        s[nt][0] = fast_exp2(s[nt][0] - base_lo);
-        s[nt][1] = fast_exp2(s[nt][1] - base_lo);
-        s[nt][2] = fast_exp2(s[nt][2] - base_hi);
-        s[nt][3] = fast_exp2(s[nt][3] - base_hi);
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float x = s[nt][j] * sl2;
+            if (need_mask) {
+              const int pos = p0 + 8 * nt + 2 * c + (j & 1);
+              if (pos > (j < 2 ? lim_lo : lim_hi)) x = -INFINITY;
+            }
+            s[nt][j] = x;
+          }
+        // online softmax (rows r and r + 8; the 4 lanes of a row hold 4 keys each)
+        float mx_lo = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+        float mx_hi = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+        mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+        mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+        mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+        mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+        const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+        const float base_lo = mn_lo == -INFINITY ? 0.f : mn_lo;
+        const float base_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
+        const float a_lo = fast_exp2(m_lo - base_lo), a_hi = fast_exp2(m_hi - base_hi);
+        m_lo = mn_lo;
+        m_hi = mn_hi;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          s[nt][0] = fast_exp2(s[nt][0] - base_lo);
+          s[nt][1] = fast_exp2(s[nt][1] - base_lo);
+          s[nt][2] = fast_exp2(s[nt][2] - base_hi);
+          s[nt][3] = fast_exp2(s[nt][3] - base_hi);
+        }
+        l_lo = l_lo * a_lo + (s[0][0] + s[0][1]) + (s[1][0] + s[1][1]);
+        l_hi = l_hi * a_hi + (s[0][2] + s[0][3]) + (s[1][2] + s[1][3]);
+        if (__any_sync(0xffffffffu, a_lo != 1.f || a_hi != 1.f)) {
+#pragma unroll
+          for (int nt = 0; nt < kNt; ++nt) {
+            o[nt][0] *= a_lo;
+            o[nt][1] *= a_lo;
+            o[nt][2] *= a_hi;
+            o[nt][3] *= a_hi;
+          }
+        }
+        // P (bf16) as the A operand: keys are the k dimension
+        const uint32_t pa0 = pack_bf16x2(s[0][0], s[0][1]);
+        const uint32_t pa1 = pack_bf16x2(s[0][2], s[0][3]);
+        const uint32_t pa2 = pack_bf16x2(s[1][0], s[1][1]);
+        const uint32_t pa3 = pack_bf16x2(s[1][2], s[1][3]);
+        // O += P V: lane (r, c) reads keys 2c, 2c+1, 2c+8, 2c+9 at head_dim chunk r (+8 per half)
+#pragma unroll
+        for (int hh = 0; hh < C::kHalves; ++hh) {
+          const uint32_t base = sV + hh * kBoxBytes;
+          const uint4 v0 = lds128(base + swz(2 * c, r));
+          const uint4 v1 = lds128(base + swz(2 * c + 1, r));
+          const uint4 v2 = lds128(base + swz(2 * c + 8, r));
+          const uint4 v3 = lds128(base + swz(2 * c + 9, r));
+          const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w};
+          const uint32_t w1[4] = {v1.x, v1.y, v1.z, v1.w};
+          const uint32_t w2[4] = {v2.x, v2.y, v2.z, v2.w};
+          const uint32_t w3[4] = {v3.x, v3.y, v3.z, v3.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            mma_16816(o[8 * hh + 2 * k], pa0, pa1, pa2, pa3, __byte_perm(w0[k], w1[k], 0x5410),
+                      __byte_perm(w2[k], w3[k], 0x5410));
+            mma_16816(o[8 * hh + 2 * k + 1], pa0, pa1, pa2, pa3,
+                      __byte_perm(w0[k], w1[k], 0x7632), __byte_perm(w2[k], w3[k], 0x7632));
+          }
+        }
       }
-      l_lo = l_lo * a_lo + (s[0][0] + s[0][1]) + (s[1][0] + s[1][1]);
-      l_hi = l_hi * a_hi + (s[0][2] + s[0][3]) + (s[1][2] + s[1][3]);
-      if (__any_sync(0xffffffffu, a_lo != 1.f || a_hi != 1.f)) {
-#pragma unroll
-        for (int nt = 0; nt < kNt; ++nt) {
-          o[nt][0] *= a_lo;
-          o[nt][1] *= a_lo;
-          o[nt][2] *= a_hi;
-          o[nt][3] *= a_hi;
-        }
-      }
-      // P (bf16) as the A operand: keys are the k dimension
-      const uint32_t pa0 = pack_bf16x2(s[0][0], s[0][1]);
-      const uint32_t pa1 = pack_bf16x2(s[0][2], s[0][3]);
-      const uint32_t pa2 = pack_bf16x2(s[1][0], s[1][1]);
-      const uint32_t pa3 = pack_bf16x2(s[1][2], s[1][3]);
-      // O += P V: lane (r, c) reads keys 2c, 2c+1, 2c+8, 2c+9 at head_dim chunk r (+8 per half)
-#pragma unroll
-      for (int hh = 0; hh < C::kHalves; ++hh) {
-        const uint32_t base = sV + hh * kBoxBytes;
-        const uint4 v0 = lds128(base + swz(2 * c, r));
-        const uint4 v1 = lds128(base + swz(2 * c + 1, r));
-        const uint4 v2 = lds128(base + swz(2 * c + 8, r));
-        const uint4 v3 = lds128(base + swz(2 * c + 9, r));
-        const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w};
-        const uint32_t w1[4] = {v1.x, v1.y, v1.z, v1.w};
-        const uint32_t w2[4] = {v2.x, v2.y, v2.z, v2.w};
-        const uint32_t w3[4] = {v3.x, v3.y, v3.z, v3.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          mma_16816(o[8 * hh + 2 * k], pa0, pa1, pa2, pa3, __byte_perm(w0[k], w1[k], 0x5410),
-                    __byte_perm(w2[k], w3[k], 0x5410));
-          mma_16816(o[8 * hh + 2 * k + 1], pa0, pa1, pa2, pa3,
-                    __byte_perm(w0[k], w1[k], 0x7632), __byte_perm(w2[k], w3[k], 0x7632));
-        }
+      __syncwarp();
+      issue_next(stage);  // refill this stage with the stream's next block
+      if (++stage == NSTAGE) {
+        stage = 0;
+        phase ^= 1u;
       }
     }
-    __syncwarp();
-    if (lane == 0 && i + NSTAGE < n_my) {
-      issue(i + NSTAGE);
+    if (abandoned || !valid) continue;
+
+    // ---- piece epilogue straight from registers: lane (r, c) holds
+    // head_dim [64j + 16c, 64j + 16c + 16) of rows r and r + 8
+    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+    l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+    l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int row = r + 8 * half;
+      if (row >= R) continue;
+      const float l = half ? l_hi : l_lo;
+      const float m = half ? m_hi : m_lo;
+      const int64_t tok = cu0 + pc.qi0 + row / G;
+      const int hq = pc.h * G + row % G;
+#pragma unroll
+      for (int j = 0; j < D / 64; ++j) {
+        float v[16];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+          v[t] = o[8 * j + t][2 * half];
+          v[8 + t] = o[8 * j + t][2 * half + 1];
+        }
+        if (pc.part < 0) {
+          const float inv = l > 0.f ? 1.f / l : 0.f;
+          uint4 a, b;
+          a.x = pack_bf16x2(v[0] * inv, v[1] * inv);
+          a.y = pack_bf16x2(v[2] * inv, v[3] * inv);
+          a.z = pack_bf16x2(v[4] * inv, v[5] * inv);
+          a.w = pack_bf16x2(v[6] * inv, v[7] * inv);
+          b.x = pack_bf16x2(v[8] * inv, v[9] * inv);
+          b.y = pack_bf16x2(v[10] * inv, v[11] * inv);
+          b.z = pack_bf16x2(v[12] * inv, v[13] * inv);
+          b.w = pack_bf16x2(v[14] * inv, v[15] * inv);
+          uint4 *dst = reinterpret_cast<uint4 *>(p.out + (tok * p.num_q_heads + hq) * D + 64 * j +
+                                                 16 * c);
+          dst[0] = a;
+          dst[1] = b;
+        } else {
+          float4 *dst = reinterpret_cast<float4 *>(
+              p.part_o + ((int64_t)pc.part * kRowsPerTile + row) * D + 64 * j + 16 * c);
+          dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+          dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+          dst[2] = make_float4(v[8], v[9], v[10], v[11]);
+          dst[3] = make_float4(v[12], v[13], v[14], v[15]);
+        }
+      }
+      if (pc.part >= 0 && c == 0)
+        p.part_ml[(int64_t)pc.part * kRowsPerTile + row] = make_float2(m, l);
     }
-    if (i + NSTAGE < n_my) issued = i + NSTAGE + 1;
   }
   if (abandoned) {
-    // drain this warp's copies still in flight (bounded) before the smem is reused
+    // drain this warp's copies still in flight (bounded) before exiting
     for (int j = consumed; j < issued; ++j)
       mbar_wait(smem_u32(&bars[j % NSTAGE]), (uint32_t)((j / NSTAGE) & 1));
-  }
-
-  // ---- merge the four warps' states
-  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
-  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
-  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
-  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
-  float *os = reinterpret_cast<float *>(ring);  // [16][D]
-  float2 *mls = reinterpret_cast<float2 *>(ring + kRowsPerTile * D * 4);
-#pragma unroll
-  for (int nt = 0; nt < kNt; ++nt) {
-    const int d0 = 16 * c + 64 * (nt >> 3) + (nt & 7);
-    os[r * D + d0] = o[nt][0];
-    os[r * D + d0 + 8] = o[nt][1];
-    os[(r + 8) * D + d0] = o[nt][2];
-    os[(r + 8) * D + d0 + 8] = o[nt][3];
-  }
-  if (c == 0) {
-    mls[r] = make_float2(m_lo, l_lo);
-    mls[r + 8] = make_float2(m_hi, l_hi);
-  }
-  __syncthreads();
-  for (int it = threadIdx.x; it < R * (D / 8); it += kThreads) {
-    const int row = it / (D / 8), ch = it % (D / 8);
-    float mw[kWarps], M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      mw[w] = reinterpret_cast<const float2 *>(smem + w * C::kRingBytes + kRowsPerTile * D * 4)[row].x;
-      M = fmaxf(M, mw[w]);
-    }
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, L = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const float sc = mw[w] == -INFINITY ? 0.f : fast_exp2(mw[w] - M);
-      const uint8_t *wr = smem + w * C::kRingBytes;
-      L += sc * reinterpret_cast<const float2 *>(wr + kRowsPerTile * D * 4)[row].y;
-      const float4 x0 = reinterpret_cast<const float4 *>(wr)[(row * D + ch * 8) / 4];
-      const float4 x1 = reinterpret_cast<const float4 *>(wr)[(row * D + ch * 8) / 4 + 1];
-      acc[0] += sc * x0.x; acc[1] += sc * x0.y; acc[2] += sc * x0.z; acc[3] += sc * x0.w;
-      acc[4] += sc * x1.x; acc[5] += sc * x1.y; acc[6] += sc * x1.z; acc[7] += sc * x1.w;
-    }
-    if (tile.part < 0) {
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-      uint4 pk;
-      pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-      pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-      pk.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-      pk.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-      const int64_t tok = cu0 + tile.qi0 + row / G;
-      *reinterpret_cast<uint4 *>(p.out + (tok * p.num_q_heads + h * G + row % G) * D + ch * 8) = pk;
-    } else {
-      const int64_t prow = ((int64_t)tile.part * hkv + h) * kRowsPerTile + row;
-      float4 *dst = reinterpret_cast<float4 *>(p.part_o + prow * D + ch * 8);
-      dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
-      if (ch == 0) p.part_ml[prow] = make_float2(M, L);
-    }
   }
 }
 
 template <int D>
 __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p) {
   const MergeGroup g = p.merges[blockIdx.x];
-  const int h = blockIdx.y;
   const int G = p.group;
   const int R = g.n_q * G;
+  if (g.seq < 0 || g.seq >= p.num_seqs || R > kRowsPerTile) return;
   const int cu0 = __ldg(p.cu_q_lens + g.seq);
   for (int it = threadIdx.x; it < R * (D / 8); it += blockDim.x) {
     const int row = it / (D / 8), ch = it % (D / 8);
     float M = -INFINITY;
     for (int j = 0; j < g.nsplit; ++j)
-      M = fmaxf(M, p.part_ml[((int64_t)(g.part0 + j) * p.num_kv_heads + h) * kRowsPerTile + row].x);
+      M = fmaxf(M, p.part_ml[(int64_t)(g.part0 + j) * kRowsPerTile + row].x);
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, L = 0.f;
     for (int j = 0; j < g.nsplit; ++j) {
-      const int64_t prow = ((int64_t)(g.part0 + j) * p.num_kv_heads + h) * kRowsPerTile + row;
+      const int64_t prow = (int64_t)(g.part0 + j) * kRowsPerTile + row;
       const float2 ml = p.part_ml[prow];
       const float sc = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
       L += sc * ml.y;
@@ -379,7 +407,7 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p) {
     pk.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
     pk.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
     const int64_t tok = cu0 + g.qi0 + row / G;
-    *reinterpret_cast<uint4 *>(p.out + (tok * p.num_q_heads + h * G + row % G) * D + ch * 8) = pk;
+    *reinterpret_cast<uint4 *>(p.out + (tok * p.num_q_heads + g.h * G + row % G) * D + ch * 8) = pk;
   }
 }
 
@@ -411,11 +439,14 @@ DecodeParams make_params(const AttnArgs &a) {
   p.cu_q_lens = a.cu_q_lens;
   p.context_lens = a.context_lens;
   p.block_tables = a.block_tables;
-  p.tiles = a.decode_tiles;
+  p.warp_begin = a.warp_begin;
+  p.pieces = a.pieces;
   p.merges = a.merge_groups;
   p.part_o = a.part_o;
   p.part_ml = reinterpret_cast<float2 *>(a.part_ml);
   p.dev_status = a.dev_status;
+  p.num_warps = a.num_decode_warps;
+  p.num_seqs = a.num_seqs;
   p.max_blocks_per_seq = a.max_blocks_per_seq;
   p.num_blocks = a.desc.num_blocks;
   p.num_q_heads = a.num_q_heads;
@@ -432,7 +463,7 @@ int launch_decode_t(const AttnArgs &a, const CUtensorMap &map) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return (int)e;
-  dim3 grid((unsigned)a.num_decode_tiles, (unsigned)a.desc.num_kv_heads);
+  const unsigned grid = (unsigned)((a.num_decode_warps + kWarps - 1) / kWarps);
   profile_begin(PKV_KERNEL_DECODE, a.stream);
   kern<<<grid, kThreads, C::kSmemBytes, a.stream>>>(map, make_params(a));
   profile_end(PKV_KERNEL_DECODE, a.stream);
@@ -443,9 +474,10 @@ int launch_decode_t(const AttnArgs &a, const CUtensorMap &map) {
 
 // 2D view of the pool: rows of head_dim bf16 (one key or value row of one
 // head), box = 16 rows x 64 elements, 128-byte swizzle.
-int make_pool_map(CUtensorMap *map, const void *pool, const pkv_pool_desc &desc) {
+int make_pool_map(void *map_out, const void *pool, const pkv_pool_desc &desc) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return (int)cudaErrorNotSupported;
+  CUtensorMap *map = static_cast<CUtensorMap *>(map_out);
   const uint64_t rows = (uint64_t)desc.num_blocks * 2 * desc.num_kv_heads * kBlockSize;
   cuuint64_t dims[2] = {(cuuint64_t)desc.head_dim, (cuuint64_t)(rows > 0 ? rows : 1)};
   cuuint64_t strides[1] = {(cuuint64_t)desc.head_dim * 2};
@@ -458,7 +490,7 @@ int make_pool_map(CUtensorMap *map, const void *pool, const pkv_pool_desc &desc)
 }
 
 int launch_decode(const AttnArgs &a, int *launches) {
-  if (a.num_decode_tiles <= 0) return 0;
+  if (a.num_decode_warps <= 0) return 0;
   CUtensorMap map;
   int e = make_pool_map(&map, a.kv_pool, a.desc);
   if (e) return e;
@@ -472,12 +504,11 @@ int launch_decode(const AttnArgs &a, int *launches) {
 
 int launch_merge(const AttnArgs &a, int *launches) {
   if (a.num_merge_groups <= 0) return 0;
-  dim3 grid((unsigned)a.num_merge_groups, (unsigned)a.desc.num_kv_heads);
   profile_begin(PKV_KERNEL_MERGE, a.stream);
   if (a.desc.head_dim == 128)
-    merge_kernel<128><<<grid, 128, 0, a.stream>>>(make_params(a));
+    merge_kernel<128><<<(unsigned)a.num_merge_groups, 128, 0, a.stream>>>(make_params(a));
   else
-    merge_kernel<64><<<grid, 128, 0, a.stream>>>(make_params(a));
+    merge_kernel<64><<<(unsigned)a.num_merge_groups, 128, 0, a.stream>>>(make_params(a));
   profile_end(PKV_KERNEL_MERGE, a.stream);
   int e = (int)cudaGetLastError();
   if (!e) {

@@ -8,12 +8,17 @@
 
 namespace pkv {
 
-constexpr int32_t kPlanMagic = 0x31564b50;  // "PKV1"
+constexpr int32_t kPlanMagic = 0x32564b50;  // "PKV2"
 constexpr int kBlockSize = 16;
-constexpr int kRowsPerTile = 16;    // query rows (token x head-in-group) per decode tile
-constexpr int kPrefillRows = 128;   // query rows per tensor-core tile
+constexpr int kRowsPerTile = 16;    // query rows (token x head-in-group) per decode row group
+constexpr int kPrefillRows = 128;   // query tokens per tensor-core tile
+constexpr int kDecodeWarpsPerCta = 4;
 
-// Plan buffer: [PlanHeader][DecodeTile x n][MergeGroup x m][PrefillTile x k]
+// Plan buffer layout (all offsets are functions of the counts):
+//   [PlanHeader 64 B]
+//   [warp_begin: int32 x (num_decode_warps + 1), padded to 32 B]
+//   [Piece x num_decode_pieces][MergeGroup x num_merge_groups]
+//   [PrefillTile x num_prefill_tiles]
 struct PlanHeader {
   int32_t magic;
   int32_t num_seqs;
@@ -21,44 +26,45 @@ struct PlanHeader {
   int32_t num_kv_heads;
   int32_t head_dim;
   int32_t total_q;
-  int32_t num_decode_tiles;
+  int32_t num_decode_warps;
+  int32_t num_decode_pieces;
   int32_t num_merge_groups;
-  int32_t num_prefill_tiles;
   int32_t num_partials;
-  int32_t split_blocks;
+  int32_t num_prefill_tiles;
   int32_t max_blocks_needed;
   int32_t reserved[4];
 };
 static_assert(sizeof(PlanHeader) == 64, "plan header is 64 bytes");
 
-// One split-KV work item.  Runs once per KV head (grid.y).  Covers query
-// tokens qi0 .. qi0+n_q-1 of sequence `seq` (all heads of the GQA group, so
-// n_q * group <= 16 rows) against logical KV blocks [kb_begin, kb_end).
-struct DecodeTile {
+// A contiguous key range of one (row group, KV head) segment, processed by one
+// warp of the split-KV kernel.  A row group is n_q consecutive query tokens of
+// sequence `seq` x all query heads of KV head h (n_q * group <= 16 rows).
+struct Piece {
   int32_t seq;
-  int32_t qi0;       // first query token, relative to the sequence's chunk
+  int32_t qi0;       // first query token of the row group, relative to the sequence's chunk
   int32_t n_q;       // query tokens in the row group
-  int32_t kb_begin;  // first logical KV block
-  int32_t kb_end;    // one past the last logical KV block
-  int32_t part;      // partial slot, or -1: the only split, write `out` directly
-  int32_t last;      // 1 if this split ends at the row group's last needed block
+  int32_t h;         // KV head
+  int32_t kb_begin;  // first logical KV block of the piece
+  int32_t kb_end;    // one past the last logical KV block of the piece
+  int32_t part;      // partial slot, or -1 when the piece is the whole segment (writes out)
   int32_t pad;
 };
-static_assert(sizeof(DecodeTile) == 32, "decode tile is 32 bytes");
+static_assert(sizeof(Piece) == 32, "piece is 32 bytes");
 
-// Row group whose keys were split over `nsplit` tiles with consecutive
-// partial slots part0 .. part0+nsplit-1.
+// A segment whose keys span nsplit pieces with partial slots part0 .. part0+nsplit-1.
 struct MergeGroup {
   int32_t seq;
   int32_t qi0;
   int32_t n_q;
+  int32_t h;
   int32_t part0;
   int32_t nsplit;
-  int32_t pad[3];
+  int32_t pad[2];
 };
 static_assert(sizeof(MergeGroup) == 32, "merge group is 32 bytes");
 
-// Tensor-core work item: 128 query tokens of one sequence x one query head.
+// Tensor-core work item: query tokens qi0 .. qi0+n_q-1 (n_q <= 128) of one
+// sequence x one query head.
 struct PrefillTile {
   int32_t seq;
   int32_t qi0;
@@ -69,22 +75,27 @@ static_assert(sizeof(PrefillTile) == 16, "prefill tile is 16 bytes");
 
 inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
-// Byte offsets inside the plan buffer, from the counts alone.
-inline int64_t plan_decode_off() { return (int64_t)sizeof(PlanHeader); }
-inline int64_t plan_merge_off(int32_t n_decode) {
-  return plan_decode_off() + (int64_t)n_decode * (int64_t)sizeof(DecodeTile);
-}
-inline int64_t plan_prefill_off(int32_t n_decode, int32_t n_merge) {
-  return plan_merge_off(n_decode) + (int64_t)n_merge * (int64_t)sizeof(MergeGroup);
+struct PlanOffsets {
+  int64_t warp_begin, pieces, merges, prefill, total;
+};
+inline PlanOffsets plan_offsets(int32_t n_warps, int32_t n_pieces, int32_t n_merge,
+                                int32_t n_prefill) {
+  PlanOffsets o;
+  o.warp_begin = (int64_t)sizeof(PlanHeader);
+  o.pieces = o.warp_begin + align_up(4ll * (n_warps + 1), 32);
+  o.merges = o.pieces + (int64_t)n_pieces * (int64_t)sizeof(Piece);
+  o.prefill = o.merges + (int64_t)n_merge * (int64_t)sizeof(MergeGroup);
+  o.total = o.prefill + (int64_t)n_prefill * (int64_t)sizeof(PrefillTile);
+  return o;
 }
 
-// Workspace: partial O [num_partials][Hkv][16][D] fp32, then (m, l) pairs
-// [num_partials][Hkv][16] float2.
-inline int64_t ws_part_o_bytes(int32_t parts, int32_t hkv, int32_t d) {
-  return align_up((int64_t)parts * hkv * kRowsPerTile * d * 4, 256);
+// Workspace: partial O [num_partials][16][D] fp32, then (m, l) pairs
+// [num_partials][16] float2 (only the row group's rows are written).
+inline int64_t ws_part_o_bytes(int32_t parts, int32_t d) {
+  return align_up((int64_t)parts * kRowsPerTile * d * 4, 256);
 }
-inline int64_t ws_part_ml_bytes(int32_t parts, int32_t hkv) {
-  return align_up((int64_t)parts * hkv * kRowsPerTile * 8, 256);
+inline int64_t ws_part_ml_bytes(int32_t parts) {
+  return align_up((int64_t)parts * kRowsPerTile * 8, 256);
 }
 
 // Kernel launchers (defined in the .cu files).  Return a cudaError_t value.
@@ -104,8 +115,9 @@ struct AttnArgs {
   int32_t num_q_heads;
   int32_t num_seqs;
   float scale;
-  const DecodeTile *decode_tiles;
-  int32_t num_decode_tiles;
+  const int32_t *warp_begin;
+  int32_t num_decode_warps;
+  const Piece *pieces;
   const MergeGroup *merge_groups;
   int32_t num_merge_groups;
   const PrefillTile *prefill_tiles;
@@ -118,6 +130,11 @@ struct AttnArgs {
 
 int launch_decode(const AttnArgs &a, int *launches);
 int launch_merge(const AttnArgs &a, int *launches);
+int launch_prefill(const AttnArgs &a, int *launches);
+
+// 2D TMA view of the pool (rows of head_dim bf16, box 16 x 64, 128B swizzle);
+// `map` points to a CUtensorMap.
+int make_pool_map(void *map, const void *pool, const pkv_pool_desc &desc);
 
 void count_launches(int n);
 

@@ -1,24 +1,28 @@
 // Host step metadata: validates one packed step's lengths and cuts it into
-// work tiles for the attention kernels.
+// work for the attention kernels.
 //
 // The vllm-metal kernel ("Replacing attention, reusing the rest") has every
 // threadgroup binary-search cu_seqlens to find the request owning its query
 // token.  Here the scheduler's host copies of cu_q_lens / context_lens are
-// turned into an explicit tile list once per step instead, so every CTA reads
-// its (sequence, query rows, key range) directly.
+// turned into explicit work lists once per step instead.
 //
-// Tiling:
+// Decode-class rows (split-KV kernel):
 //  * Query rows of a sequence are grouped GQA-first: a row group holds n_q
 //    consecutive query tokens x all `group` query heads of one KV head, with
 //    n_q * group <= 16 (one m16 MMA tile), so each KV block loaded serves every
-//    query head that reads it.
-//  * A row group's keys [0, last visible key] are cut into splits of about
-//    `split_blocks` 16-token blocks.  split_blocks is chosen from the total
-//    work so that the decode grid is ~4 CTAs per SM (2 resident x 2 waves);
-//    row groups with several splits get partial-result slots and a merge group.
-//  * Tiles are ordered longest first so the hardware block scheduler deals the
-//    long ones out before the short ones (longest-processing-time order).
+//    query head that reads it.  A segment is (row group, KV head) with the
+//    blocks [0, last visible key / 16].
+//  * All segments' blocks are laid end to end and cut into num_decode_warps
+//    equal contiguous ranges, one per warp (8 warps per SM, one wave).  A range
+//    intersects one or more segments; each intersection is a piece.  A segment
+//    cut into several pieces gets one partial slot per piece and a merge group.
+//    Equal ranges leave no tail wave and no long/short CTA imbalance.
+//
+// Prefill-class rows (tensor-core kernel, when enabled): sequences with at
+// least kPrefillMinQ query tokens are cut into tiles of 128 query tokens x one
+// query head, ordered by the number of keys they see (longest first).
 #include <algorithm>
+#include <climits>
 #include <cstring>
 #include <vector>
 
@@ -27,9 +31,11 @@
 namespace pkv {
 namespace {
 
-constexpr int kMinSplitBlocks = 16;
-constexpr int kMaxSplitBlocks = 1024;
-constexpr int kCtasPerSmTarget = 4;
+constexpr int kDecodeWarpsPerSm = 8;
+constexpr int kMinBlocksPerWarp = 4;
+// Query tokens from which a sequence's rows go to the tensor-core kernel.
+// INT_MAX keeps every row on the split-KV kernel.
+constexpr int kPrefillMinQ = INT_MAX;
 
 pkv_status check_desc(const pkv_pool_desc *desc, int32_t num_q_heads) {
   if (!desc) return PKV_ERR_NULL;
@@ -41,8 +47,8 @@ pkv_status check_desc(const pkv_pool_desc *desc, int32_t num_q_heads) {
   return PKV_OK;
 }
 
-struct RowGroup {
-  int32_t seq, qi0, n_q, nb;
+struct Segment {
+  int32_t seq, qi0, n_q, h, nb;
 };
 
 }  // namespace
@@ -65,9 +71,11 @@ extern "C" pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *con
   const int32_t group = num_q_heads / hkv;
   const int32_t nq_tile = std::max(1, kRowsPerTile / group);
 
-  // ---- validate and build row groups
+  // ---- validate; build decode segments and prefill tiles
   if (num_seqs > 0 && cu_q_lens[0] != 0) return PKV_ERR_SHAPE;
-  std::vector<RowGroup> groups;
+  std::vector<Segment> segs;
+  std::vector<PrefillTile> ptiles;
+  std::vector<int64_t> ptile_keys;
   int64_t kv_tokens = 0, total_blocks = 0;
   int32_t max_nb = 0;
   for (int32_t s = 0; s < num_seqs; ++s) {
@@ -78,78 +86,117 @@ extern "C" pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *con
     if (qs == 0) continue;
     kv_tokens += ctx;
     max_nb = std::max(max_nb, (ctx + kBlockSize - 1) / kBlockSize);
+    if (qs >= kPrefillMinQ) {
+      for (int32_t qi0 = 0; qi0 < qs; qi0 += kPrefillRows) {
+        int32_t n_q = std::min(kPrefillRows, qs - qi0);
+        for (int32_t hq = 0; hq < num_q_heads; ++hq) {
+          ptiles.push_back({s, qi0, hq, n_q});
+          ptile_keys.push_back((int64_t)ctx - qs + qi0 + n_q);
+        }
+      }
+      continue;
+    }
     for (int32_t qi0 = 0; qi0 < qs; qi0 += nq_tile) {
       int32_t n_q = std::min(nq_tile, qs - qi0);
-      int32_t last_key = ctx - qs + qi0 + n_q - 1;
-      int32_t nb = last_key / kBlockSize + 1;
-      groups.push_back({s, qi0, n_q, nb});
-      total_blocks += nb;
+      int32_t nb = (ctx - qs + qi0 + n_q - 1) / kBlockSize + 1;
+      for (int32_t h = 0; h < hkv; ++h) {
+        segs.push_back({s, qi0, n_q, h, nb});
+        total_blocks += nb;
+      }
     }
   }
 
-  // ---- split size from the total work
-  int64_t units = total_blocks * hkv;
-  int64_t target = (int64_t)num_sms * kCtasPerSmTarget;
-  int64_t split = (units + target - 1) / std::max<int64_t>(target, 1);
-  split = std::min<int64_t>(std::max<int64_t>(split, kMinSplitBlocks), kMaxSplitBlocks);
-
-  std::vector<DecodeTile> tiles;
+  // ---- cut the concatenated decode blocks into equal warp ranges
+  int64_t nw64 = (total_blocks + kMinBlocksPerWarp - 1) / kMinBlocksPerWarp;
+  nw64 = std::min<int64_t>(nw64, (int64_t)num_sms * kDecodeWarpsPerSm);
+  const int32_t num_warps = total_blocks > 0 ? (int32_t)std::max<int64_t>(nw64, 1) : 0;
+  std::vector<int32_t> warp_begin(num_warps + 1, 0);
+  std::vector<Piece> pieces;
+  std::vector<int32_t> piece_seg;
+  {
+    size_t k = 0;
+    int64_t seg_off = 0;  // global block offset of segment k
+    for (int32_t w = 0; w < num_warps; ++w) {
+      warp_begin[w] = (int32_t)pieces.size();
+      int64_t a = total_blocks * w / num_warps, b = total_blocks * (w + 1) / num_warps;
+      while (a < b) {
+        while (seg_off + segs[k].nb <= a) seg_off += segs[k++].nb;
+        const Segment &g = segs[k];
+        int64_t e = std::min<int64_t>(b, seg_off + g.nb);
+        Piece p;
+        p.seq = g.seq;
+        p.qi0 = g.qi0;
+        p.n_q = g.n_q;
+        p.h = g.h;
+        p.kb_begin = (int32_t)(a - seg_off);
+        p.kb_end = (int32_t)(e - seg_off);
+        p.part = -1;
+        p.pad = 0;
+        pieces.push_back(p);
+        piece_seg.push_back((int32_t)k);
+        a = e;
+      }
+    }
+    warp_begin[num_warps] = (int32_t)pieces.size();
+  }
+  // partial slots for segments cut into several pieces (their pieces are adjacent)
   std::vector<MergeGroup> merges;
   int32_t parts = 0;
-  for (const RowGroup &g : groups) {
-    int32_t nsplit = (int32_t)((g.nb + split - 1) / split);
-    int32_t per = (g.nb + nsplit - 1) / nsplit;
-    nsplit = (g.nb + per - 1) / per;
-    int32_t part0 = nsplit > 1 ? parts : -1;
-    for (int32_t j = 0; j < nsplit; ++j) {
-      DecodeTile t;
-      t.seq = g.seq;
-      t.qi0 = g.qi0;
-      t.n_q = g.n_q;
-      t.kb_begin = j * per;
-      t.kb_end = std::min(g.nb, (j + 1) * per);
-      t.part = nsplit > 1 ? part0 + j : -1;
-      t.last = (j == nsplit - 1) ? 1 : 0;
-      t.pad = 0;
-      tiles.push_back(t);
-    }
-    if (nsplit > 1) {
+  for (size_t i = 0; i < pieces.size();) {
+    size_t j = i;
+    while (j < pieces.size() && piece_seg[j] == piece_seg[i]) ++j;
+    if (j - i > 1) {
       MergeGroup m;
       std::memset(&m, 0, sizeof m);
-      m.seq = g.seq;
-      m.qi0 = g.qi0;
-      m.n_q = g.n_q;
-      m.part0 = part0;
-      m.nsplit = nsplit;
+      m.seq = pieces[i].seq;
+      m.qi0 = pieces[i].qi0;
+      m.n_q = pieces[i].n_q;
+      m.h = pieces[i].h;
+      m.part0 = parts;
+      m.nsplit = (int32_t)(j - i);
       merges.push_back(m);
-      parts += nsplit;
+      for (size_t t = i; t < j; ++t) pieces[t].part = parts++;
     }
+    i = j;
   }
-  std::stable_sort(tiles.begin(), tiles.end(), [](const DecodeTile &a, const DecodeTile &b) {
-    return (a.kb_end - a.kb_begin) > (b.kb_end - b.kb_begin);
-  });
+  // prefill tiles, most keys first
+  {
+    std::vector<size_t> order(ptiles.size());
+    for (size_t i = 0; i < order.size(); ++i) order[i] = i;
+    std::stable_sort(order.begin(), order.end(),
+                     [&](size_t x, size_t y) { return ptile_keys[x] > ptile_keys[y]; });
+    std::vector<PrefillTile> sorted;
+    sorted.reserve(ptiles.size());
+    for (size_t i : order) sorted.push_back(ptiles[i]);
+    ptiles.swap(sorted);
+  }
 
   // ---- sizes
+  const PlanOffsets off = plan_offsets(num_warps, (int32_t)pieces.size(), (int32_t)merges.size(),
+                                       (int32_t)ptiles.size());
   std::memset(info, 0, sizeof *info);
   info->num_seqs = num_seqs;
   info->num_q_heads = num_q_heads;
   info->num_kv_heads = hkv;
   info->head_dim = desc->head_dim;
   info->total_q = num_seqs > 0 ? cu_q_lens[num_seqs] : 0;
-  info->num_decode_tiles = (int32_t)tiles.size();
+  info->num_decode_warps = num_warps;
+  info->num_decode_pieces = (int32_t)pieces.size();
   info->num_merge_groups = (int32_t)merges.size();
   info->num_partials = parts;
-  info->num_prefill_tiles = 0;
-  info->num_kernels = (tiles.empty() ? 0 : 1) + (merges.empty() ? 0 : 1);
-  info->split_blocks = (int32_t)split;
+  info->num_prefill_tiles = (int32_t)ptiles.size();
+  info->num_kernels = (num_warps > 0 ? 1 : 0) + (merges.empty() ? 0 : 1) + (ptiles.empty() ? 0 : 1);
   info->max_blocks_needed = max_nb;
   info->kv_tokens = kv_tokens;
-  info->plan_bytes = plan_prefill_off(info->num_decode_tiles, info->num_merge_groups);
+  info->decode_blocks = total_blocks;
+  info->plan_bytes = off.total;
   info->workspace_bytes =
-      parts > 0 ? ws_part_o_bytes(parts, hkv, desc->head_dim) + ws_part_ml_bytes(parts, hkv) : 0;
+      parts > 0 ? ws_part_o_bytes(parts, desc->head_dim) + ws_part_ml_bytes(parts) : 0;
 
   if (!plan) return PKV_OK;
   if (plan_capacity < info->plan_bytes) return PKV_ERR_WORKSPACE;
+  char *p = static_cast<char *>(plan);
+  std::memset(p, 0, (size_t)info->plan_bytes);
   PlanHeader h;
   std::memset(&h, 0, sizeof h);
   h.magic = kPlanMagic;
@@ -158,18 +205,18 @@ extern "C" pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *con
   h.num_kv_heads = hkv;
   h.head_dim = desc->head_dim;
   h.total_q = info->total_q;
-  h.num_decode_tiles = info->num_decode_tiles;
+  h.num_decode_warps = num_warps;
+  h.num_decode_pieces = info->num_decode_pieces;
   h.num_merge_groups = info->num_merge_groups;
-  h.num_prefill_tiles = 0;
   h.num_partials = parts;
-  h.split_blocks = (int32_t)split;
+  h.num_prefill_tiles = info->num_prefill_tiles;
   h.max_blocks_needed = max_nb;
-  char *p = static_cast<char *>(plan);
   std::memcpy(p, &h, sizeof h);
-  if (!tiles.empty())
-    std::memcpy(p + plan_decode_off(), tiles.data(), tiles.size() * sizeof(DecodeTile));
+  std::memcpy(p + off.warp_begin, warp_begin.data(), warp_begin.size() * sizeof(int32_t));
+  if (!pieces.empty()) std::memcpy(p + off.pieces, pieces.data(), pieces.size() * sizeof(Piece));
   if (!merges.empty())
-    std::memcpy(p + plan_merge_off(info->num_decode_tiles), merges.data(),
-                merges.size() * sizeof(MergeGroup));
+    std::memcpy(p + off.merges, merges.data(), merges.size() * sizeof(MergeGroup));
+  if (!ptiles.empty())
+    std::memcpy(p + off.prefill, ptiles.data(), ptiles.size() * sizeof(PrefillTile));
   return PKV_OK;
 }

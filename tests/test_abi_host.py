@@ -42,59 +42,82 @@ def test_version_and_status_strings(pkv):
 def parse_plan(info, host):
     words = host.view(np.int32)
     hdr = words[:16]
-    assert hdr[0] == 0x31564B50
-    nd, nm = info.num_decode_tiles, info.num_merge_groups
-    dec = words[16:16 + 8 * nd].reshape(nd, 8)
-    mer = words[16 + 8 * nd:16 + 8 * nd + 8 * nm].reshape(nm, 8)
-    return hdr, dec, mer
+    assert hdr[0] == 0x32564B50
+    nw, npc, nm, npf = (info.num_decode_warps, info.num_decode_pieces, info.num_merge_groups,
+                        info.num_prefill_tiles)
+    off_w = 16
+    off_p = off_w + ((nw + 1 + 7) // 8) * 8
+    off_m = off_p + 8 * npc
+    off_f = off_m + 8 * nm
+    assert info.plan_bytes == 4 * (off_f + 4 * npf)
+    wb = words[off_w:off_w + nw + 1]
+    pieces = words[off_p:off_m].reshape(npc, 8)
+    mer = words[off_m:off_f].reshape(nm, 8)
+    pre = words[off_f:off_f + 4 * npf].reshape(npf, 4)
+    return hdr, wb, pieces, mer, pre
 
 
 def check_plan(meta, info, host, num_sms):
-    hdr, dec, mer = parse_plan(info, host)
+    hdr, wb, pieces, mer, pre = parse_plan(info, host)
     g = meta.num_q_heads // meta.num_kv_heads
+    hkv = meta.num_kv_heads
     nq_tile = max(1, 16 // g)
     assert info.total_q == meta.total_q
     assert info.kv_tokens == int(meta.context_lens[meta.q_lens > 0].astype(np.int64).sum())
-    # tiles sorted longest first
-    lens = dec[:, 4] - dec[:, 3]
-    assert np.all(lens[:-1] >= lens[1:])
-    assert np.all(lens > 0)
-    # row groups partition each sequence's query tokens; splits partition its keys
+    # warp ranges: contiguous, cover all pieces, equal block counts (+-1)
+    nw = info.num_decode_warps
+    if nw:
+        assert wb[0] == 0 and wb[-1] == len(pieces) and np.all(np.diff(wb) >= 1)
+        per_warp = [int((pieces[wb[w]:wb[w + 1], 5] - pieces[wb[w]:wb[w + 1], 4]).sum())
+                    for w in range(nw)]
+        assert sum(per_warp) == info.decode_blocks
+        assert max(per_warp) - min(per_warp) <= 1
+        if num_sms is not None:
+            assert nw <= num_sms * 8
+    assert np.all(pieces[:, 5] > pieces[:, 4])
+    # every decode segment (row group x KV head) is covered exactly once, in order
+    prefill_seqs = set(int(x) for x in pre[:, 0]) if len(pre) else set()
     seen_parts = set()
+    total_blocks = 0
     for s in range(meta.num_seqs):
         qs, ctx = int(meta.q_lens[s]), int(meta.context_lens[s])
-        mine = dec[dec[:, 0] == s]
+        mine = pieces[pieces[:, 0] == s]
         if qs == 0:
-            assert len(mine) == 0
+            assert len(mine) == 0 and s not in prefill_seqs
             continue
-        qi0s = sorted(set(int(x) for x in mine[:, 1]))
-        assert qi0s == list(range(0, qs, nq_tile))
-        for qi0 in qi0s:
-            grp = mine[mine[:, 1] == qi0]
+        if s in prefill_seqs:
+            assert len(mine) == 0
+            tiles = pre[pre[:, 0] == s]
+            assert len(tiles) == meta.num_q_heads * (-(-qs // 128))
+            continue
+        for qi0 in range(0, qs, nq_tile):
             n_q = min(nq_tile, qs - qi0)
-            assert np.all(grp[:, 2] == n_q)
             nb = (ctx - qs + qi0 + n_q - 1) // 16 + 1
-            order = grp[np.argsort(grp[:, 3])]
-            assert order[0, 3] == 0 and order[-1, 4] == nb
-            assert np.all(order[1:, 3] == order[:-1, 4])
-            assert list(order[:, 6]) == [0] * (len(order) - 1) + [1]
-            if len(order) == 1:
-                assert order[0, 5] == -1
-            else:
-                parts = list(order[:, 5])
-                assert parts == list(range(parts[0], parts[0] + len(parts)))
-                assert not (set(parts) & seen_parts)
-                seen_parts |= set(parts)
-                m = mer[(mer[:, 0] == s) & (mer[:, 1] == qi0)]
-                assert len(m) == 1 and m[0, 2] == n_q and m[0, 3] == parts[0] and m[0, 4] == len(parts)
+            for h in range(hkv):
+                seg = mine[(mine[:, 1] == qi0) & (mine[:, 3] == h)]
+                assert len(seg) >= 1 and np.all(seg[:, 2] == n_q)
+                seg = seg[np.argsort(seg[:, 4])]
+                assert seg[0, 4] == 0 and seg[-1, 5] == nb
+                assert np.all(seg[1:, 4] == seg[:-1, 5])
+                total_blocks += nb
+                if len(seg) == 1:
+                    assert seg[0, 6] == -1
+                else:
+                    parts = list(seg[:, 6])
+                    assert parts == list(range(parts[0], parts[0] + len(parts)))
+                    assert not (set(parts) & seen_parts)
+                    seen_parts |= set(parts)
+                    m = mer[(mer[:, 0] == s) & (mer[:, 1] == qi0) & (mer[:, 3] == h)]
+                    assert len(m) == 1 and m[0, 2] == n_q and m[0, 4] == parts[0] and m[0, 5] == len(parts)
+    assert total_blocks == info.decode_blocks
     assert len(seen_parts) == info.num_partials
     ws = 0
     if info.num_partials:
-        d, hkv = meta.head_dim, meta.num_kv_heads
+        d = meta.head_dim
         a = lambda x: (x + 255) // 256 * 256
-        ws = a(info.num_partials * hkv * 16 * d * 4) + a(info.num_partials * hkv * 16 * 8)
+        ws = a(info.num_partials * 16 * d * 4) + a(info.num_partials * 16 * 8)
     assert info.workspace_bytes == ws
-    assert info.num_kernels == (info.num_decode_tiles > 0) + (info.num_merge_groups > 0) + \
+    assert info.num_kernels == (info.num_decode_warps > 0) + (info.num_merge_groups > 0) + \
         (info.num_prefill_tiles > 0)
 
 
@@ -122,11 +145,11 @@ def test_planner_handles_zero_length_queries_and_empty_steps(pkv):
     desc = pkv.PoolDesc(10, 16, 2, 64)
     info, host = pkv.plan_step(np.array([0, 0, 3, 3], np.int32), np.array([5, 40, 7], np.int32), 4,
                                desc, num_sms=152, upload=False)
-    hdr, dec, mer = parse_plan(info, host)
-    assert set(dec[:, 0]) == {1}
+    hdr, wb, pieces, mer, pre = parse_plan(info, host)
+    assert set(pieces[:, 0]) == {1}
     info, host = pkv.plan_step(np.array([0], np.int32), np.array([], np.int32), 4, desc,
                                num_sms=152, upload=False)
-    assert info.num_decode_tiles == 0 and info.num_kernels == 0 and info.workspace_bytes == 0
+    assert info.num_decode_warps == 0 and info.num_kernels == 0 and info.workspace_bytes == 0
 
 
 @pytest.mark.parametrize("cu,ctx,hq,desc,err", [
