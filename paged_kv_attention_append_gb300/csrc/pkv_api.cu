@@ -117,6 +117,7 @@ extern "C" pkv_status pkv_paged_varlen_attention(
   a.desc = *desc;
   a.num_q_heads = info->num_q_heads;
   a.num_seqs = info->num_seqs;
+  a.total_q = info->total_q;
   a.scale = scale;
   const char *pb = static_cast<const char *>(plan_dev);
   const PlanOffsets off = plan_offsets(info->num_decode_warps, info->num_decode_pieces,

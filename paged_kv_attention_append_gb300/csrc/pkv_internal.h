@@ -114,6 +114,7 @@ struct AttnArgs {
   pkv_pool_desc desc;
   int32_t num_q_heads;
   int32_t num_seqs;
+  int64_t total_q;
   float scale;
   const int32_t *warp_begin;
   int32_t num_decode_warps;

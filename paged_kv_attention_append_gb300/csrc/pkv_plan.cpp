@@ -18,11 +18,12 @@
 //    cut into several pieces gets one partial slot per piece and a merge group.
 //    Equal ranges leave no tail wave and no long/short CTA imbalance.
 //
-// Prefill-class rows (tensor-core kernel, when enabled): sequences with at
-// least kPrefillMinQ query tokens are cut into tiles of 128 query tokens x one
-// query head, ordered by the number of keys they see (longest first).
+// Prefill-class rows (tensor-core kernel): sequences with at least 64 query
+// tokens are cut into tiles of 128 query tokens x one query head, ordered by
+// the number of keys they see (longest first).
 #include <algorithm>
 #include <climits>
+#include <cstdlib>
 #include <cstring>
 #include <vector>
 
@@ -33,9 +34,17 @@ namespace {
 
 constexpr int kDecodeWarpsPerSm = 8;
 constexpr int kMinBlocksPerWarp = 4;
-// Query tokens from which a sequence's rows go to the tensor-core kernel.
-// INT_MAX keeps every row on the split-KV kernel.
-constexpr int kPrefillMinQ = INT_MAX;
+// Query tokens from which a sequence's rows go to the tensor-core kernel
+// (default 64; the environment variable PKV_PREFILL_MIN_Q overrides it, 0 or
+// a negative value keeps every row on the split-KV kernel).
+constexpr int kPrefillMinQDefault = 64;
+
+int prefill_min_q() {
+  const char *env = std::getenv("PKV_PREFILL_MIN_Q");
+  if (!env || !*env) return kPrefillMinQDefault;
+  const long v = std::strtol(env, nullptr, 10);
+  return v <= 0 ? INT_MAX : (int)std::min<long>(v, INT_MAX);
+}
 
 pkv_status check_desc(const pkv_pool_desc *desc, int32_t num_q_heads) {
   if (!desc) return PKV_ERR_NULL;
@@ -73,6 +82,7 @@ extern "C" pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *con
 
   // ---- validate; build decode segments and prefill tiles
   if (num_seqs > 0 && cu_q_lens[0] != 0) return PKV_ERR_SHAPE;
+  const int min_q_prefill = prefill_min_q();
   std::vector<Segment> segs;
   std::vector<PrefillTile> ptiles;
   std::vector<int64_t> ptile_keys;
@@ -86,7 +96,7 @@ extern "C" pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *con
     if (qs == 0) continue;
     kv_tokens += ctx;
     max_nb = std::max(max_nb, (ctx + kBlockSize - 1) / kBlockSize);
-    if (qs >= kPrefillMinQ) {
+    if (qs >= min_q_prefill) {
       for (int32_t qi0 = 0; qi0 < qs; qi0 += kPrefillRows) {
         int32_t n_q = std::min(kPrefillRows, qs - qi0);
         for (int32_t hq = 0; hq < num_q_heads; ++hq) {

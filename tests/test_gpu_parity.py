@@ -226,3 +226,35 @@ def test_in_tree_library_is_loaded(pkv):
     assert os.path.exists(pkv.library_path())
     maps = open("/proc/self/maps").read()
     assert pkv.library_path() in maps
+
+
+# ------------------------------------------------------------------ tensor-core prefill path
+
+@pytest.mark.parametrize("ql,cl,hq,hkv,d", [
+    ([128], [128], 1, 1, 128),                  # one exact tile, prefill from an empty cache
+    ([64], [64], 2, 1, 64),                     # D = 64, group 2
+    ([200], [700], 5, 1, 128),                  # ragged tile, context before the chunk
+    ([130, 1, 300], [900, 50, 301], 8, 2, 128), # prefill + decode in one step
+    ([256], [4096 + 256], 4, 1, 128),           # long context, several key tiles
+])
+def test_prefill_kernel_matches_oracle(pkv, cuda_device, ql, cl, hq, hkv, d):
+    meta = workloads.build_step("prefill", 77 + len(ql), ql, cl, hq, hkv, d)
+    q, k, v, pool = workloads.make_values(meta)
+    plan_info, _ = pkv.plan_step(meta.cu_q_lens, meta.context_lens, hq, pkv.pool_desc(pool),
+                                 upload=False)
+    assert plan_info.num_prefill_tiles > 0
+    want, _ = oracle.run_step(meta, q, k, v, pool)
+    out, _, _ = gpu_step(pkv, meta, q, k, v, pool, cuda_device)
+    assert_close(out, want, f"prefill {ql} {cl}")
+
+
+def test_prefill_and_split_kv_paths_agree(pkv, cuda_device, monkeypatch):
+    meta = workloads.build_step("paths", 91, [300, 2, 1], [1000, 500, 40], 8, 2, 128)
+    q, k, v, pool = workloads.make_values(meta)
+    tc_out, _, _ = gpu_step(pkv, meta, q, k, v, pool, cuda_device)
+    monkeypatch.setenv("PKV_PREFILL_MIN_Q", "0")     # every row on the split-KV kernel
+    info, _ = pkv.plan_step(meta.cu_q_lens, meta.context_lens, 8, pkv.pool_desc(pool), upload=False)
+    assert info.num_prefill_tiles == 0
+    kv_out, _, _ = gpu_step(pkv, meta, q, k, v, pool, cuda_device)
+    diff = (tc_out.double() - kv_out.double()).abs()
+    assert float(diff.max()) <= MAX_ABS and float(diff.mean()) <= MEAN_ABS
