@@ -53,14 +53,22 @@ def peaks():
                 "source": "fallback"}
 
 
-def algorithmic_bytes(meta) -> int:
-    """KV + Q + O + metadata bytes of one attention pass (split-KV scratch excluded)."""
+PREFILL_MIN_Q = 64   # sequences with at least this many query tokens run on the tensor-core kernel
+
+
+def algorithmic_bytes(meta, prefill=None) -> int:
+    """KV + Q + O + metadata bytes of one attention pass (split-KV scratch excluded).
+
+    prefill=None counts every sequence; False only the split-KV (decode-class)
+    sequences; True only the tensor-core (prefill-class) ones."""
     d, hq, hkv = meta.head_dim, meta.num_q_heads, meta.num_kv_heads
     live = meta.q_lens > 0
+    if prefill is not None:
+        live &= (meta.q_lens >= PREFILL_MIN_Q) == prefill
     kv = int(meta.context_lens[live].astype(np.int64).sum()) * 2 * hkv * d * 2
-    qo = 2 * meta.total_q * hq * d * 2
+    qo = 2 * int(meta.q_lens[live].astype(np.int64).sum()) * hq * d * 2
     nb = int(((meta.context_lens[live].astype(np.int64) + 15) // 16).sum())
-    return kv + qo + 4 * (2 * meta.num_seqs + 1) + 4 * nb
+    return kv + qo + 4 * (2 * int(live.sum()) + 1) + 4 * nb
 
 
 def unique_bytes(meta) -> int:
@@ -69,11 +77,11 @@ def unique_bytes(meta) -> int:
 
 
 def prefill_flops(meta) -> int:
-    """4*D*Hq*(visible (q, k) pairs) over sequences with q_len > 1."""
+    """4*D*Hq*(visible (q, k) pairs) over the tensor-core (prefill-class) sequences."""
     pairs = 0
     for s in range(meta.num_seqs):
         qs, ctx = int(meta.q_lens[s]), int(meta.context_lens[s])
-        if qs > 1:
+        if qs >= PREFILL_MIN_Q:
             pairs += sum(ctx - qs + i + 1 for i in range(qs))
     return 4 * meta.head_dim * meta.num_q_heads * pairs
 
@@ -269,23 +277,32 @@ def bench_pkv(args):
                 graph.replay()
                 b.record(stream)
         torch.cuda.synchronize(dev)
-        # kernel-only timing of the decode kernel (roofline), eager, L2 flushed
-        k_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(args.steps)]
+        # kernel-only timing of the decode and prefill kernels (roofline), eager, L2
+        # flushed: the library records our events around each launch on its stream
+        def ev_pairs():
+            return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    for _ in range(args.steps)]
+        k_ev = {"decode": ev_pairs(), "prefill": ev_pairs()}
         with torch.cuda.stream(stream):
-            for a, b in k_ev:
-                a.record(stream)
-                b.record(stream)
+            for pairs in k_ev.values():
+                for a, b in pairs:
+                    a.record(stream)
+                    b.record(stream)
             torch.cuda.synchronize(dev)
-            for a, b in k_ev:
+            for i in range(args.steps):
                 flush_l2()
-                pkv.set_profile_events("decode", a, b)
+                for name, pairs in k_ev.items():
+                    pkv.set_profile_events(name, *pairs[i])
                 pkv.paged_varlen_attention(q, cu_d, ctx_d, bt_d, pool, meta.scale, plan=plan,
                                            out=out, dev_status=status)
-            pkv.set_profile_events("decode")
+            for name in k_ev:
+                pkv.set_profile_events(name)
         torch.cuda.synchronize(dev)
     step_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
-    decode_ms = statistics.mean(a.elapsed_time(b) for a, b in k_ev)
+    decode_ms = (statistics.mean(a.elapsed_time(b) for a, b in k_ev["decode"])
+                 if info.num_decode_warps else 0.0)
+    prefill_ms = (statistics.mean(a.elapsed_time(b) for a, b in k_ev["prefill"])
+                  if info.num_prefill_tiles else 0.0)
     clocks = clk.summary()
     if ws > 1:
         t = torch.tensor([step_ms], device=dev)
@@ -333,7 +350,27 @@ def bench_pkv(args):
     pk = peaks()
     kv_tok = meta.kv_tokens()
     bytes_alg = algorithmic_bytes(meta)
-    achieved = bytes_alg / (decode_ms * 1e-3) / 1e9
+    dec_bytes = algorithmic_bytes(meta, prefill=False)
+    fl = prefill_flops(meta)
+    kernels = {}
+    if decode_ms:
+        kernels["decode_kernel"] = {"ms_per_launch": decode_ms, "bytes_per_launch": dec_bytes,
+                                    "gbs": dec_bytes / (decode_ms * 1e-3) / 1e9}
+    if prefill_ms:
+        kernels["prefill_kernel"] = {"ms_per_launch": prefill_ms, "flops_per_launch": fl,
+                                     "tflops": fl / (prefill_ms * 1e-3) / 1e12}
+    if prefill_ms > decode_ms:     # the dominant kernel is a dense contraction
+        achieved = fl / (prefill_ms * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "kernel": "prefill_kernel", "achieved": achieved,
+                    "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
+                    "traffic": None, "flops_per_launch": fl, "ms_per_launch": prefill_ms,
+                    "peak_source": pk["source"] + " (bf16 burst)"}
+    else:
+        achieved = dec_bytes / (decode_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved,
+                    "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                    "traffic": None, "bytes_per_launch": dec_bytes, "ms_per_launch": decode_ms,
+                    "peak_source": pk["source"]}
     cpu = run_oracle_sample(meta) if (rank == 0 and ws == 1 and not args.no_cpu_baseline) else None
     if rank != 0:
         return
@@ -347,10 +384,8 @@ def bench_pkv(args):
                          f"{L2_FLUSH_BYTES >> 20} MB read)",
                    "timing": "CUDA graph replay per step, CUDA events per step"},
         "gpu_launches": launches_per_step * args.steps,
-        "roofline": {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved,
-                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
-                     "traffic": None, "bytes_per_launch": bytes_alg, "ms_per_launch": decode_ms,
-                     "peak_source": pk["source"]},
+        "roofline": roofline,
+        "kernels": kernels,
         "step_gbs": bytes_alg / (step_ms * 1e-3) / 1e9,
         "host_plan_us": host_plan_us,
         "e2e": {"value": ws * kv_tok / e2e_s, "unit": "KV tokens/s", "h2d_bytes_per_step": h2d,
@@ -361,9 +396,8 @@ def bench_pkv(args):
         "plan": {"decode_warps": info.num_decode_warps, "decode_pieces": info.num_decode_pieces,
                  "merge_groups": info.num_merge_groups, "prefill_tiles": info.num_prefill_tiles},
     }
-    if meta.unique_blocks() * 16 < kv_tok:
+    if meta.unique_blocks() * 16 < kv_tok and decode_ms:
         line["unique_gbs"] = unique_bytes(meta) / (decode_ms * 1e-3) / 1e9
-    fl = prefill_flops(meta)
     if fl:
         line["prefill_tflops_step"] = fl / (step_ms * 1e-3) / 1e12
     print(json.dumps(line), flush=True)

@@ -158,7 +158,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   if (warp == kProducerWarp) {
-    // ======================================================== TMA producer
+    // ======================================================== TMA producer (whole warp)
+    // Lane b < 8 owns paged block b of every 128-key tile: it reads that block's
+    // table entry (one coalesced 32-byte load for the tile, issued before the
+    // wait for a free stage so the latency hides behind it) and issues the
+    // block's K and V boxes itself.
     if (lane == 0) {
       prefetch_tmap(&q_map);
       prefetch_tmap(&pool_map);
@@ -168,44 +172,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int hh = 0; hh < C::kHalves; ++hh)
         tma_load_3d(sq + hh * C::kHalfBytes, &q_map, hh * 64, tile.hq, cu0 + tile.qi0,
                     bar(B_Q_FULL));
-      const int32_t *table = p.block_tables + (int64_t)tile.seq * p.max_blocks_per_seq;
-      const int hkv = p.num_kv_heads;
-      int issued[2] = {0, 0};
-      for (int j = 0; j < ntiles; ++j) {
-        if (*abort_flag) break;
-        const int s = j & 1;
-        if (j >= 2 && !mbar_wait(bar(B_KV_EMPTY + s), (uint32_t)(((j >> 1) - 1) & 1))) {
-          fail();
-          break;
+    }
+    const int32_t *table = p.block_tables + (int64_t)tile.seq * p.max_blocks_per_seq;
+    const int hkv = p.num_kv_heads;
+    int issued0 = 0, issued1 = 0;
+    for (int j = 0; j < ntiles; ++j) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+      const int s = j & 1;
+      const int kb = j * kBlocksPerTile + lane;
+      int row_k = p.pool_rows, row_v = p.pool_rows;  // out of range: zero fill
+      if (lane < kBlocksPerTile && kb < nblk_ctx && kb < p.max_blocks_per_seq) {
+        const int phys = __ldg(table + kb);
+        if (phys >= 0 && phys < p.num_blocks) {
+          row_k = ((phys * 2 + 0) * hkv + h) * kBlockSize;
+          row_v = row_k + hkv * kBlockSize;
+        } else {
+          report(p.dev_status, PKV_DEV_BAD_BLOCK);
         }
-        const uint32_t sk = smem_u32(smem + C::kOffStage + s * C::kStageBytes);
-        const uint32_t sv = sk + C::kKBytes;
-        mbar_arrive_expect_tx(bar(B_KV_FULL + s), C::kStageBytes);
-        for (int b = 0; b < kBlocksPerTile; ++b) {
-          const int kb = j * kBlocksPerTile + b;
-          int row_k = p.pool_rows, row_v = p.pool_rows;  // out of range: zero fill
-          if (kb < nblk_ctx && kb < p.max_blocks_per_seq) {
-            const int phys = __ldg(table + kb);
-            if (phys >= 0 && phys < p.num_blocks) {
-              row_k = ((phys * 2 + 0) * hkv + h) * kBlockSize;
-              row_v = row_k + hkv * kBlockSize;
-            } else {
-              report(p.dev_status, PKV_DEV_BAD_BLOCK);
-            }
-          }
-#pragma unroll
-          for (int hh = 0; hh < C::kHalves; ++hh) {
-            tma_load_2d(sk + hh * C::kHalfBytes + b * kBoxBytesTC, &pool_map, hh * 64, row_k,
-                        bar(B_KV_FULL + s));
-            tma_load_2d(sv + hh * C::kHalfBytes + b * kBoxBytesTC, &pool_map, hh * 64, row_v,
-                        bar(B_KV_FULL + s));
-          }
-        }
-        ++issued[s];
       }
-      // our copies still in flight land before the CTA can exit
-      for (int s = 0; s < 2; ++s)
-        if (issued[s]) mbar_wait(bar(B_KV_FULL + s), (uint32_t)((issued[s] - 1) & 1));
+      if (j >= 2 && !__all_sync(0xffffffffu, mbar_wait(bar(B_KV_EMPTY + s),
+                                                        (uint32_t)(((j >> 1) - 1) & 1)))) {
+        if (lane == 0) fail();
+        break;
+      }
+      const uint32_t sk = smem_u32(smem + C::kOffStage + s * C::kStageBytes);
+      const uint32_t sv = sk + C::kKBytes;
+      if (lane == 0) mbar_arrive_expect_tx(bar(B_KV_FULL + s), C::kStageBytes);
+      __syncwarp();
+      if (lane < kBlocksPerTile) {
+#pragma unroll
+        for (int hh = 0; hh < C::kHalves; ++hh) {
+          tma_load_2d(sk + hh * C::kHalfBytes + lane * kBoxBytesTC, &pool_map, hh * 64, row_k,
+                      bar(B_KV_FULL + s));
+          tma_load_2d(sv + hh * C::kHalfBytes + lane * kBoxBytesTC, &pool_map, hh * 64, row_v,
+                      bar(B_KV_FULL + s));
+        }
+      }
+      if (s == 0) ++issued0; else ++issued1;
+    }
+    // our copies still in flight land before the CTA can exit
+    if (lane == 0) {
+      if (issued0) mbar_wait(bar(B_KV_FULL), (uint32_t)((issued0 - 1) & 1));
+      if (issued1) mbar_wait(bar(B_KV_FULL + 1), (uint32_t)((issued1 - 1) & 1));
       mbar_wait(bar(B_Q_FULL), 0);
     }
   } else if (warp == kMmaWarp) {
@@ -277,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool good = true;
     const uint32_t sp = smem_u32(smem + C::kOffP);
     for (int j = 0; j < ntiles; ++j) {
-      if (*abort_flag) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) {
         good = false;
         break;
       }
@@ -288,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc::fence_after_sync();
-      float x[kKeysPerTile];
+      float x[kKeysPerTile];  // raw scores q.k of this row
       {
         uint32_t raw[4][32];
 #pragma unroll
@@ -303,22 +311,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_S_FREE + s));
 
-      // scale to log2 units, causal mask, row max
+      // row max of the scaled visible scores (log2 units); -inf if none visible.
+      // For a positive scale the max is taken on the raw scores (4 independent
+      // chains) and scaled once; the scale is folded into the exponent below.
       const int rel = lim - j * kKeysPerTile;  // keys k <= rel are visible
-      float mt = -INFINITY;
-      if (rel >= kKeysPerTile - 1) {
+      const bool diag = rel < kKeysPerTile - 1;
+      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      if (sl2 > 0.f) {
+        if (!diag) {
 #pragma unroll
-        for (int k = 0; k < kKeysPerTile; ++k) {
-          x[k] *= sl2;
-          mt = fmaxf(mt, x[k]);
-        }
-      } else {
+          for (int k = 0; k < kKeysPerTile; ++k) m4[k & 3] = fmaxf(m4[k & 3], x[k]);
+        } else {
 #pragma unroll
-        for (int k = 0; k < kKeysPerTile; ++k) {
-          x[k] = k <= rel ? x[k] * sl2 : -INFINITY;
-          mt = fmaxf(mt, x[k]);
+          for (int k = 0; k < kKeysPerTile; ++k)
+            m4[k & 3] = fmaxf(m4[k & 3], k <= rel ? x[k] : -INFINITY);
         }
+      } else {  // zero or negative scale: scale first
+#pragma unroll
+        for (int k = 0; k < kKeysPerTile; ++k)
+          m4[k & 3] = fmaxf(m4[k & 3], k <= rel ? x[k] * sl2 : -INFINITY);
       }
+      float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+      if (sl2 > 0.f && mt != -INFINITY) mt *= sl2;
       // lazy rescale of O (TMEM) and l when the max grew by more than 2^8
       const bool need = m_used != -INFINITY && mt > m_used + kRescaleLog2;
       bool o_ready = false;
@@ -345,17 +359,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (need) m_used = mt;
       }
       if (m_used == -INFINITY) m_used = mt;  // first keys this row sees
-      const float base = m_used == -INFINITY ? 0.f : m_used;
+      const float nbase = m_used == -INFINITY ? 0.f : -m_used;
+      // p = 2^(scale_log2 * s - m) for visible keys, 0 for masked ones
       uint32_t pk[kKeysPerTile / 2];
-      float lsum = 0.f;
+      float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int i = 0; i < kKeysPerTile / 2; ++i) {
-        const float p0 = fast_exp2(x[2 * i] - base);
-        const float p1 = fast_exp2(x[2 * i + 1] - base);
-        lsum += p0 + p1;
+        float p0 = fast_exp2(fmaf(x[2 * i], sl2, nbase));
+        float p1 = fast_exp2(fmaf(x[2 * i + 1], sl2, nbase));
+        if (diag) {
+          p0 = 2 * i <= rel ? p0 : 0.f;
+          p1 = 2 * i + 1 <= rel ? p1 : 0.f;
+        }
+        ls[i & 3] += p0 + p1;
         pk[i] = pack_bf16x2(p0, p1);
       }
-      l += lsum;
+      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
       // the P buffer is free once P_{j-1} V_{j-1} completed
       if (j >= 1 && !o_ready) {
         if (!__all_sync(0xffffffffu, mbar_wait(bar(B_O_DONE), (uint32_t)((j - 1) & 1)))) {
@@ -380,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar(B_P_FULL));
     }
     // ---- epilogue: O / l from TMEM to bf16 rows
-    if (good && !*abort_flag) {
+    if (good && !__any_sync(0xffffffffu, *abort_flag != 0)) {
       if (!__all_sync(0xffffffffu, mbar_wait(bar(B_O_DONE), (uint32_t)((ntiles - 1) & 1)))) {
         fail();
       } else {
