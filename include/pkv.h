@@ -183,6 +183,9 @@ PKV_API pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *contex
  *   workspace: device scratch of at least info->workspace_bytes (256-byte
  *   aligned; contents on entry do not matter).  Rows of sequences with
  *   q_len == 0 do not exist.  Accumulation is fp32; out is rounded once to bf16.
+ *   Kernels are launched with programmatic stream serialisation: their launch
+ *   overlaps the tail of the preceding kernel on the stream, and each waits for
+ *   that kernel to complete (griddepcontrol.wait) before reading any input.
  */
 PKV_API pkv_status pkv_paged_varlen_attention(const void *q, const int32_t *cu_q_lens,
                                       const int32_t *context_lens, const int32_t *block_tables,

@@ -24,6 +24,11 @@ void profile_begin(int which, pkv_stream stream) {
 void profile_end(int which, pkv_stream stream) {
   if (t_prof.stop[which]) cudaEventRecord(static_cast<cudaEvent_t>(t_prof.stop[which]), stream);
 }
+bool profiling_active() {
+  for (int i = 0; i < 4; ++i)
+    if (t_prof.start[i] || t_prof.stop[i]) return true;
+  return false;
+}
 
 static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

@@ -20,6 +20,7 @@ __global__ void __launch_bounds__(256) append_kernel(const uint4 *__restrict__ k
                                                      int32_t num_blocks, int32_t hkv,
                                                      int32_t *dev_status) {
   constexpr int kVecPerRow = D / 8;  // 16-byte vectors per head row
+  pdl_trigger();  // the attention kernels may launch now; they wait for our writes
   const int64_t per_token = 2ll * hkv * kVecPerRow;
   const int64_t total = per_token * num_tokens;
   const int64_t nslots = (int64_t)num_blocks * kBlockSize;

@@ -26,7 +26,8 @@
 //    memory phase hits 8 distinct 16-byte bank groups (conflict-free).
 //  * Online softmax in the log2 domain with warp-shuffle row max; O is rescaled
 //    only when some row's max moved.
-//  * merge_kernel combines the partials of a segment cut into several pieces:
+//  * merge_kernel (launched behind the decode kernel with programmatic stream
+//    serialisation) combines the partials of a segment cut into pieces:
 //    M = max_j m_j, out = sum_j 2^(m_j - M) O_j / sum_j 2^(m_j - M) l_j.
 #include <cuda_runtime.h>
 
@@ -66,6 +67,7 @@ struct DecodeParams {
   float *part_o;
   float2 *part_ml;
   int32_t *dev_status;
+  int32_t num_merges;
   int32_t num_warps;
   int32_t num_seqs;
   int32_t max_blocks_per_seq;
@@ -81,6 +83,69 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
+template <int D>
+__device__ __forceinline__ void write_piece(const DecodeParams &p, const Piece &pc,
+                                            float (&o)[D / 8][4], float m_lo, float m_hi,
+                                            float l_lo, float l_hi, int R, int cu0, int r, int c);
+
+// LSE merge of the segments cut into several pieces:
+//   M = max_j m_j,  out = sum_j 2^(m_j - M) O_j / sum_j 2^(m_j - M) l_j.
+// One thread per (merge group, row, 4 output columns) makes a single pass over
+// the group's splits with a running max (each new split rescales the running
+// sums), unrolled so several splits' loads are in flight at once.
+constexpr int kMergeThreads = 256;
+
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams p,
+                                                              int32_t num_groups) {
+  constexpr int kChunks = D / 4;  // float4 chunks of a row
+  pdl_wait();                     // the split-KV partials are complete and visible
+  const int64_t t = (int64_t)blockIdx.x * kMergeThreads + threadIdx.x;
+  const int64_t gi = t / (kRowsPerTile * kChunks);
+  const int rem = (int)(t % (kRowsPerTile * kChunks));
+  const int row = rem / kChunks, ch = rem % kChunks;
+  if (gi >= num_groups) return;
+  const MergeGroup g = p.merges[gi];
+  const int G = p.group;
+  if (row >= g.n_q * G || g.seq < 0 || g.seq >= p.num_seqs || g.n_q * G > kRowsPerTile) return;
+  const float2 *ml = p.part_ml + (int64_t)g.part0 * kRowsPerTile + row;
+  const float4 *po =
+      reinterpret_cast<const float4 *>(p.part_o + ((int64_t)g.part0 * kRowsPerTile + row) * D) + ch;
+  float M = -INFINITY, L = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  constexpr int kBatch = 8;  // splits whose loads are all issued before any is used
+  for (int j0 = 0; j0 < g.nsplit; j0 += kBatch) {
+    float2 v[kBatch];
+    float4 x[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int j = min(j0 + u, g.nsplit - 1);  // past the end: reload the last split, unused
+      v[u] = ml[(int64_t)j * kRowsPerTile];
+      x[u] = po[(int64_t)j * kRowsPerTile * kChunks];
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      // skip padding entries and splits in which this row saw no key
+      if (j0 + u >= g.nsplit || v[u].x == -INFINITY) continue;
+      const float mn = fmaxf(M, v[u].x);
+      const float a = fast_exp2(M - mn), b = fast_exp2(v[u].x - mn);
+      L = L * a + v[u].y * b;
+      acc.x = acc.x * a + x[u].x * b;
+      acc.y = acc.y * a + x[u].y * b;
+      acc.z = acc.z * a + x[u].z * b;
+      acc.w = acc.w * a + x[u].w * b;
+      M = mn;
+    }
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const int cu0 = __ldg(p.cu_q_lens + g.seq);
+  const int64_t tok = cu0 + g.qi0 + row / G;
+  uint2 pk;
+  pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+  pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2 *>(p.out + (tok * p.num_q_heads + g.h * G + row % G) * D + 4 * ch) = pk;
+}
+
 template <int D, int NSTAGE>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_kernel(const __grid_constant__ CUtensorMap pool_map, const DecodeParams p) {
@@ -92,6 +157,10 @@ __global__ void __launch_bounds__(kThreads, 2)
                                               ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = lane >> 2, c = lane & 3;
+  // launched early behind the preceding kernel: let our dependents launch, then
+  // wait for the predecessor's writes (pool, q, metadata) before reading anything
+  pdl_trigger();
+  pdl_wait();
   const int gw = blockIdx.x * kWarps + warp;
   if (gw >= p.num_warps) return;
   const int pb = __ldg(p.warp_begin + gw), pe = __ldg(p.warp_begin + gw + 1);
@@ -318,11 +387,25 @@ __global__ void __launch_bounds__(kThreads, 2)
         phase ^= 1u;
       }
     }
-    if (abandoned || !valid) continue;
+    if (abandoned) break;
+    if (valid) write_piece<D>(p, pc, o, m_lo, m_hi, l_lo, l_hi, R, cu0, r, c);
+  }
+  if (abandoned) {
+    // drain this warp's copies still in flight (bounded) before exiting
+    for (int j = consumed; j < issued; ++j)
+      mbar_wait(smem_u32(&bars[j % NSTAGE]), (uint32_t)((j / NSTAGE) & 1));
+  }
+}
 
-    // ---- piece epilogue straight from registers: lane (r, c) holds
-    // head_dim [64j + 16c, 64j + 16c + 16) of rows r and r + 8
-    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+// ---- piece epilogue straight from registers: lane (r, c) holds head_dim
+// [64j + 16c, 64j + 16c + 16) of rows r and r + 8.  A whole segment writes the
+// normalised bf16 output; a split piece writes its fp32 partial (O, m, l).
+template <int D>
+__device__ __forceinline__ void write_piece(const DecodeParams &p, const Piece &pc,
+                                            float (&o)[D / 8][4], float m_lo, float m_hi,
+                                            float l_lo, float l_hi, int R, int cu0, int r, int c) {
+  const int G = p.group;
+  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
     l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
     l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
     l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
@@ -368,46 +451,6 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       if (pc.part >= 0 && c == 0)
         p.part_ml[(int64_t)pc.part * kRowsPerTile + row] = make_float2(m, l);
-    }
-  }
-  if (abandoned) {
-    // drain this warp's copies still in flight (bounded) before exiting
-    for (int j = consumed; j < issued; ++j)
-      mbar_wait(smem_u32(&bars[j % NSTAGE]), (uint32_t)((j / NSTAGE) & 1));
-  }
-}
-
-template <int D>
-__global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p) {
-  const MergeGroup g = p.merges[blockIdx.x];
-  const int G = p.group;
-  const int R = g.n_q * G;
-  if (g.seq < 0 || g.seq >= p.num_seqs || R > kRowsPerTile) return;
-  const int cu0 = __ldg(p.cu_q_lens + g.seq);
-  for (int it = threadIdx.x; it < R * (D / 8); it += blockDim.x) {
-    const int row = it / (D / 8), ch = it % (D / 8);
-    float M = -INFINITY;
-    for (int j = 0; j < g.nsplit; ++j)
-      M = fmaxf(M, p.part_ml[(int64_t)(g.part0 + j) * kRowsPerTile + row].x);
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f}, L = 0.f;
-    for (int j = 0; j < g.nsplit; ++j) {
-      const int64_t prow = (int64_t)(g.part0 + j) * kRowsPerTile + row;
-      const float2 ml = p.part_ml[prow];
-      const float sc = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
-      L += sc * ml.y;
-      const float4 *src = reinterpret_cast<const float4 *>(p.part_o + prow * D + ch * 8);
-      const float4 x0 = src[0], x1 = src[1];
-      acc[0] += sc * x0.x; acc[1] += sc * x0.y; acc[2] += sc * x0.z; acc[3] += sc * x0.w;
-      acc[4] += sc * x1.x; acc[5] += sc * x1.y; acc[6] += sc * x1.z; acc[7] += sc * x1.w;
-    }
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    uint4 pk;
-    pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-    pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-    pk.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-    pk.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-    const int64_t tok = cu0 + g.qi0 + row / G;
-    *reinterpret_cast<uint4 *>(p.out + (tok * p.num_q_heads + g.h * G + row % G) * D + ch * 8) = pk;
   }
 }
 
@@ -444,6 +487,7 @@ DecodeParams make_params(const AttnArgs &a) {
   p.merges = a.merge_groups;
   p.part_o = a.part_o;
   p.part_ml = reinterpret_cast<float2 *>(a.part_ml);
+  p.num_merges = a.num_merge_groups;
   p.dev_status = a.dev_status;
   p.num_warps = a.num_decode_warps;
   p.num_seqs = a.num_seqs;
@@ -465,9 +509,12 @@ int launch_decode_t(const AttnArgs &a, const CUtensorMap &map) {
   if (e != cudaSuccess) return (int)e;
   const unsigned grid = (unsigned)((a.num_decode_warps + kWarps - 1) / kWarps);
   profile_begin(PKV_KERNEL_DECODE, a.stream);
-  kern<<<grid, kThreads, C::kSmemBytes, a.stream>>>(map, make_params(a));
+  // programmatic launch only when no profiling event sits between us and our
+  // predecessor (an event in between would serialise anyway)
+  e = launch_kernel(kern, dim3(grid), dim3(kThreads), C::kSmemBytes, a.stream,
+                    !profiling_active(), map, make_params(a));
   profile_end(PKV_KERNEL_DECODE, a.stream);
-  return (int)cudaGetLastError();
+  return e != cudaSuccess ? (int)e : (int)cudaGetLastError();
 }
 
 }  // namespace
@@ -504,13 +551,18 @@ int launch_decode(const AttnArgs &a, int *launches) {
 
 int launch_merge(const AttnArgs &a, int *launches) {
   if (a.num_merge_groups <= 0) return 0;
+  const int64_t threads = (int64_t)a.num_merge_groups * kRowsPerTile * (a.desc.head_dim / 4);
+  const dim3 grid((unsigned)((threads + kMergeThreads - 1) / kMergeThreads));
+  const bool pdl = !profiling_active();
   profile_begin(PKV_KERNEL_MERGE, a.stream);
-  if (a.desc.head_dim == 128)
-    merge_kernel<128><<<(unsigned)a.num_merge_groups, 128, 0, a.stream>>>(make_params(a));
-  else
-    merge_kernel<64><<<(unsigned)a.num_merge_groups, 128, 0, a.stream>>>(make_params(a));
+  const cudaError_t le =
+      a.desc.head_dim == 128
+          ? launch_kernel(merge_kernel<128>, grid, dim3(kMergeThreads), 0, a.stream, pdl,
+                          make_params(a), a.num_merge_groups)
+          : launch_kernel(merge_kernel<64>, grid, dim3(kMergeThreads), 0, a.stream, pdl,
+                          make_params(a), a.num_merge_groups);
   profile_end(PKV_KERNEL_MERGE, a.stream);
-  int e = (int)cudaGetLastError();
+  const int e = le != cudaSuccess ? (int)le : (int)cudaGetLastError();
   if (!e) {
     ++*launches;
     count_launches(1);

@@ -4,7 +4,10 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <utility>
 
 #include "pkv_internal.h"
 
@@ -26,6 +29,17 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 
 __device__ __forceinline__ void report(int32_t *dev_status, int32_t code) {
   if (dev_status) atomicCAS(dev_status, 0, code);
+}
+
+// ---------------------------------------------------------------- programmatic dependent launch
+// Wait until the preceding kernel of the stream (launched before this one with
+// programmatic stream serialization) has completed and its writes are
+// visible; a no-op when this kernel was launched without that attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Allow the next kernel of the stream to be launched once every CTA of this
+// grid has executed this (or exited).
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- mbarrier
@@ -161,6 +175,26 @@ __device__ __forceinline__ uint4 ldg128_nc(const void *p) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
+}
+
+// ---------------------------------------------------------------- host: launches
+// Launch `kern` on `stream`; with `pdl` the launch may begin before the
+// preceding kernel of the stream completes (the kernel must call pdl_wait()
+// before it touches that kernel's outputs).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t stream, bool pdl, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
 
 }  // namespace pkv

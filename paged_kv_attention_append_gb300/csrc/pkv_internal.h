@@ -47,7 +47,7 @@ struct Piece {
   int32_t kb_begin;  // first logical KV block of the piece
   int32_t kb_end;    // one past the last logical KV block of the piece
   int32_t part;      // partial slot, or -1 when the piece is the whole segment (writes out)
-  int32_t pad;
+  int32_t merge;     // merge group of the segment when part >= 0, else -1
 };
 static_assert(sizeof(Piece) == 32, "piece is 32 bytes");
 
@@ -143,5 +143,8 @@ void count_launches(int n);
 // one kernel id on the launching stream; per host thread.
 void profile_begin(int which, pkv_stream stream);
 void profile_end(int which, pkv_stream stream);
+// True when any profiling event is set on this host thread; kernels are then
+// launched without programmatic stream serialisation so events bracket them.
+bool profiling_active();
 
 }  // namespace pkv

@@ -141,7 +141,7 @@ extern "C" pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *con
         p.kb_begin = (int32_t)(a - seg_off);
         p.kb_end = (int32_t)(e - seg_off);
         p.part = -1;
-        p.pad = 0;
+        p.merge = -1;
         pieces.push_back(p);
         piece_seg.push_back((int32_t)k);
         a = e;
@@ -164,8 +164,11 @@ extern "C" pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *con
       m.h = pieces[i].h;
       m.part0 = parts;
       m.nsplit = (int32_t)(j - i);
+      for (size_t t = i; t < j; ++t) {
+        pieces[t].part = parts++;
+        pieces[t].merge = (int32_t)merges.size();
+      }
       merges.push_back(m);
-      for (size_t t = i; t < j; ++t) pieces[t].part = parts++;
     }
     i = j;
   }

@@ -112,6 +112,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // launched early behind the preceding kernel: let our dependents launch, then
+  // wait for the predecessor's writes (pool, q, metadata) before reading anything
+  pdl_trigger();
+  pdl_wait();
   const PrefillTile tile = p.tiles[blockIdx.x];
 
   // ---- tile metadata from the device copies of the step arrays (CTA-uniform)
@@ -553,9 +557,10 @@ int launch_prefill_t(const AttnArgs &a, const CUtensorMap &qmap, const CUtensorM
   p.pool_rows = a.desc.num_blocks * 2 * a.desc.num_kv_heads * kBlockSize;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   profile_begin(PKV_KERNEL_PREFILL, a.stream);
-  kern<<<(unsigned)a.num_prefill_tiles, kThreads, C::kSmemBytes, a.stream>>>(qmap, pmap, p);
+  e = launch_kernel(kern, dim3((unsigned)a.num_prefill_tiles), dim3(kThreads), C::kSmemBytes,
+                    a.stream, !profiling_active(), qmap, pmap, p);
   profile_end(PKV_KERNEL_PREFILL, a.stream);
-  return (int)cudaGetLastError();
+  return e != cudaSuccess ? (int)e : (int)cudaGetLastError();
 }
 
 }  // namespace
