@@ -3,7 +3,7 @@
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pkv|reference] [--config NAME]
 
 A step is one pass of the whole path over one synthetic batch: KV append of
-the step's new tokens, split-KV attention with its fused LSE merge, and the
+the step's new tokens, split-KV attention and its LSE merge, and the
 tensor-core prefill tiles when present.  The step plan (host step metadata) is
 an input like the block tables: resident in HBM for `value`, computed and
 uploaded per step inside `e2e`.
@@ -58,6 +58,34 @@ def peaks():
 
 
 PREFILL_MIN_Q = 64   # sequences with at least this many query tokens run on the tensor-core kernel
+
+
+def source_sha256() -> str:
+    """Hash of the kernel sources, as recorded next to the ncu traffic figures."""
+    import hashlib
+    d = os.path.join(ROOT, "paged_kv_attention_append_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(d)):
+        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
+            h.update(f.encode())
+            with open(os.path.join(d, f), "rb") as fh:
+                h.update(fh.read())
+    with open(os.path.join(ROOT, "include", "pkv.h"), "rb") as fh:
+        h.update(fh.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """ncu DRAM bytes per launch for this kernel/workload, or None when no capture
+    exists or the kernels changed since it was taken."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f).get(f"{kernel}/{workload}")
+        if rec and rec.get("source_sha256") == source_sha256():
+            return int(rec["dram_bytes"])
+    except Exception:
+        pass
+    return None
 
 
 def algorithmic_bytes(meta, prefill=None) -> int:
@@ -373,13 +401,13 @@ def bench_pkv(args):
         achieved = fl / (prefill_ms * 1e-3) / 1e12
         roofline = {"bound": "tensor", "kernel": "prefill_kernel", "achieved": achieved,
                     "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
-                    "traffic": None, "flops_per_launch": fl, "ms_per_launch": prefill_ms,
+                    "traffic": recorded_traffic("prefill_kernel", meta.name), "flops_per_launch": fl, "ms_per_launch": prefill_ms,
                     "peak_source": pk["source"] + " (bf16 burst)"}
     else:
         achieved = dec_bytes / (decode_ms * 1e-3) / 1e9
         roofline = {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved,
                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
-                    "traffic": None, "bytes_per_launch": dec_bytes, "ms_per_launch": decode_ms,
+                    "traffic": recorded_traffic("decode_kernel", meta.name), "bytes_per_launch": dec_bytes, "ms_per_launch": decode_ms,
                     "peak_source": pk["source"]}
     cpu = run_oracle_sample(meta) if (rank == 0 and ws == 1 and not args.no_cpu_baseline) else None
     if rank != 0:
