@@ -213,6 +213,35 @@ def dist_env():
     return ws, rank, local
 
 
+def _dist_active() -> bool:
+    import torch.distributed as dist
+    return dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1
+
+
+def barrier():
+    """Barrier over all ranks (no-op in a single process)."""
+    if _dist_active():
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Max of a per-rank scalar (a step time) over all ranks; identity in one process."""
+    if not _dist_active():
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world_size: int, seconds: float) -> float:
+    """Whole-job throughput of independent replicas: every rank processes the same
+    number of units (weak scaling) and the job takes the slowest rank's time."""
+    return world_size * units_per_rank / seconds
+
+
 def bench_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -299,8 +328,8 @@ def bench_pkv(args):
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
-    if ws > 1:
-        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    barrier()
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
         with torch.cuda.stream(stream):
@@ -340,10 +369,7 @@ def bench_pkv(args):
                for n in k_ev}
     decode_ms, prefill_ms = kern_ms["decode"], kern_ms["prefill"]
     clocks = clk.summary()
-    if ws > 1:
-        t = torch.tensor([step_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(step_ms, dev)
     assert int(status.item()) == 0, f"device status {int(status.item())}"
 
     # ---- end to end from pinned host buffers through the public API
@@ -377,11 +403,7 @@ def bench_pkv(args):
             stream.synchronize()
             if i >= args.warmup:
                 e2e_times.append(time.perf_counter() - t0)
-    e2e_s = statistics.mean(e2e_times)
-    if ws > 1:
-        t = torch.tensor([e2e_s], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(statistics.mean(e2e_times), dev)
 
     pk = peaks()
     kv_tok = meta.kv_tokens()
@@ -413,7 +435,7 @@ def bench_pkv(args):
     if rank != 0:
         return
     line = {
-        "metric": METRIC, "value": ws * kv_tok / (step_ms * 1e-3), "unit": "KV tokens/s",
+        "metric": METRIC, "value": job_throughput(kv_tok, ws, step_ms * 1e-3), "unit": "KV tokens/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16, shapes of the named workload)",
@@ -426,7 +448,8 @@ def bench_pkv(args):
         "kernels": kernels,
         "step_gbs": bytes_alg / (step_ms * 1e-3) / 1e9,
         "host_plan_us": host_plan_us,
-        "e2e": {"value": ws * kv_tok / e2e_s, "unit": "KV tokens/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": job_throughput(kv_tok, ws, e2e_s), "unit": "KV tokens/s",
+                "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
         "clocks": clocks,
         "cpu_baseline": None if cpu is None else {k2: cpu[k2] for k2 in
