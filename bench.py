@@ -172,38 +172,57 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
 
 
-def run_oracle_sample(meta, target_s=10.0, max_reps=1000):
-    """Time the oracle (append + attention) on whole steps, or on a fixed subset of
-    query rows for steps too large to finish in about target_s."""
-    import torch
+ORACLE_MAX_KV_TOKENS = 60000   # bound on the oracle sample's pool (host memory and set-up time)
+
+
+def oracle_sample_step(meta):
+    """The workload itself, or its first sequences up to ORACLE_MAX_KV_TOKENS of
+    context (same shapes and length distribution, a smaller pool)."""
+    if meta.kv_tokens() <= ORACLE_MAX_KV_TOKENS:
+        return meta, "full step"
+    n, tok = 0, 0
+    while n < meta.num_seqs and (n == 0 or tok + int(meta.context_lens[n]) <= ORACLE_MAX_KV_TOKENS):
+        tok += int(meta.context_lens[n])
+        n += 1
+    sub = workloads.build_step(meta.name, meta.seed, meta.q_lens[:n], meta.context_lens[:n],
+                               meta.num_q_heads, meta.num_kv_heads, meta.head_dim,
+                               scale=meta.scale)
+    return sub, f"first {n} of {meta.num_seqs} sequences"
+
+
+def run_oracle_sample(meta, target_s=10.0, max_reps=1000, num_threads=0):
+    """Time the oracle (append + attention) on whole steps of a bounded sample of the
+    workload, or on a fixed subset of its query rows when even one step would take
+    longer than about target_s.  Reports KV tokens/s of the work actually done."""
     import oracle
-    q, k, v, pool = workloads.make_values(meta, device="cpu")
-    rows_total = meta.total_q * meta.num_q_heads
+    step, what = oracle_sample_step(meta)
+    q, k, v, pool = workloads.make_values(step, device="cpu")
+    rows_total = step.total_q * step.num_q_heads
     # cost model: one row costs ~ its visible keys
     t0 = time.perf_counter()
     probe_rows = np.arange(0, rows_total, max(1, rows_total // 64), dtype=np.int64)
-    oracle.run_step(meta, q, k, v, pool, rows=probe_rows)
+    oracle.run_step(step, q, k, v, pool, rows=probe_rows, num_threads=num_threads)
     per_row = (time.perf_counter() - t0) / len(probe_rows)
     full = per_row * rows_total
     if full <= target_s:
-        reps, rows, sample = max(1, int(target_s / max(full, 1e-6))), None, "full step"
-        reps = min(reps, max_reps)
+        reps, rows = min(max(1, int(target_s / max(full, 1e-6))), max_reps), None
+        sample = what
     else:
         n = max(1, int(rows_total * target_s / full))
         rows = np.sort(np.random.default_rng(0).choice(rows_total, size=n, replace=False)).astype(np.int64)
-        reps, sample = 1, f"{n} of {rows_total} query rows"
+        reps, sample = 1, f"{what}, {n} of {rows_total} query rows"
     t0 = time.perf_counter()
     for _ in range(reps):
-        oracle.run_step(meta, q, k, v, pool, rows=rows)
+        oracle.run_step(step, q, k, v, pool, rows=rows, num_threads=num_threads)
     dt = time.perf_counter() - t0
     if rows is None:
-        kv_tok = meta.kv_tokens() * reps
+        kv_tok = step.kv_tokens() * reps
     else:   # credit each sampled row with its share of the step's KV tokens
-        kv_tok = meta.kv_tokens() * len(rows) / rows_total
-    del torch
-    return {"value": kv_tok / dt, "unit": "KV tokens/s", "cores": oracle.max_threads(),
+        kv_tok = step.kv_tokens() * len(rows) / rows_total
+    cores = num_threads if num_threads > 0 else oracle.max_threads()
+    return {"value": kv_tok / dt, "unit": "KV tokens/s", "cores": cores,
             "kind": "oracle", "seconds": dt,
-            "sample": f"{meta.name}: {sample} x {reps} (fp64 C oracle, OpenMP)"}
+            "sample": f"{meta.name}: {sample} x {reps} (fp64 C oracle, OpenMP, {cores} threads)"}
 
 
 def dist_env():
@@ -431,7 +450,10 @@ def bench_pkv(args):
                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
                     "traffic": recorded_traffic("decode_kernel", meta.name), "bytes_per_launch": dec_bytes, "ms_per_launch": decode_ms,
                     "peak_source": pk["source"]}
-    cpu = run_oracle_sample(meta) if (rank == 0 and ws == 1 and not args.no_cpu_baseline) else None
+    cpu = cpu1 = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = run_oracle_sample(meta)                                   # all host cores
+        cpu1 = run_oracle_sample(meta, target_s=3.0, num_threads=1)     # one core
     if rank != 0:
         return
     line = {
@@ -452,8 +474,9 @@ def bench_pkv(args):
                 "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
         "clocks": clocks,
-        "cpu_baseline": None if cpu is None else {k2: cpu[k2] for k2 in
-                                                  ("value", "unit", "cores", "kind", "sample")},
+        "cpu_baseline": None if cpu is None else {
+            **{k2: cpu[k2] for k2 in ("value", "unit", "cores", "kind", "sample")},
+            "value_1core": cpu1["value"], "sample_1core": cpu1["sample"]},
         "plan": {"decode_warps": info.num_decode_warps, "decode_pieces": info.num_decode_pieces,
                  "merge_groups": info.num_merge_groups, "prefill_tiles": info.num_prefill_tiles},
     }
