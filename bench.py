@@ -358,34 +358,40 @@ def bench_pkv(args):
                 graph.replay()
                 b.record(stream)
         torch.cuda.synchronize(dev)
-        # kernel-only timing of the decode and prefill kernels (roofline), eager, L2
-        # flushed: the library records our events around each launch on its stream
-        def ev_pairs():
-            return [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                    for _ in range(args.steps)]
-        k_ev = {"append": ev_pairs(), "decode": ev_pairs(), "merge": ev_pairs(),
-                "prefill": ev_pairs()}
+        # kernel-only timing (roofline): the library records our events around each
+        # launch; captured into a second graph they are event nodes beside the
+        # kernels, so an interval holds the kernel and no host launch gap.  L2 is
+        # flushed before every replay, as for the step.
+        present = {"append": True, "decode": info.num_decode_warps > 0,
+                   "merge": info.num_merge_groups > 0, "prefill": info.num_prefill_tiles > 0}
+        k_ev = {n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for n in present}
+        samples = {n: [] for n in present}
         with torch.cuda.stream(stream):
-            for pairs in k_ev.values():
-                for a, b in pairs:
-                    a.record(stream)
-                    b.record(stream)
+            for a, b in k_ev.values():
+                a.record(stream)
+                b.record(stream)
             torch.cuda.synchronize(dev)
-            for i in range(args.steps):
+            for name, (a, b) in k_ev.items():
+                pkv.set_profile_events(name, a, b)
+            graph_k = torch.cuda.CUDAGraph()
+            try:
+                with torch.cuda.graph(graph_k, stream=stream):
+                    step()
+            finally:
+                for name in k_ev:
+                    pkv.set_profile_events(name)
+            for i in range(args.warmup + args.steps):
                 flush_l2()
-                for name, pairs in k_ev.items():
-                    pkv.set_profile_events(name, *pairs[i])
-                pkv.paged_kv_append(k, v, slots, pool, dev_status=status)
-                pkv.paged_varlen_attention(q, cu_d, ctx_d, bt_d, pool, meta.scale, plan=plan,
-                                           out=out, dev_status=status)
-            for name in k_ev:
-                pkv.set_profile_events(name)
+                graph_k.replay()
+                stream.synchronize()
+                if i >= args.warmup:
+                    for name, (a, b) in k_ev.items():
+                        if present[name]:
+                            samples[name].append(a.elapsed_time(b))
         torch.cuda.synchronize(dev)
     step_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
-    present = {"append": True, "decode": info.num_decode_warps > 0,
-               "merge": info.num_merge_groups > 0, "prefill": info.num_prefill_tiles > 0}
-    kern_ms = {n: (statistics.mean(a.elapsed_time(b) for a, b in k_ev[n]) if present[n] else 0.0)
-               for n in k_ev}
+    kern_ms = {n: (statistics.mean(samples[n]) if present[n] else 0.0) for n in k_ev}
     decode_ms, prefill_ms = kern_ms["decode"], kern_ms["prefill"]
     clocks = clk.summary()
     step_ms = max_over_ranks(step_ms, dev)
@@ -464,7 +470,9 @@ def bench_pkv(args):
         "config": {**workloads.describe(meta), "parallelism": f"replicas x{ws}" if ws > 1 else "single",
                    "l2": f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MB written, then "
                          f"{L2_FLUSH_BYTES >> 20} MB read)",
-                   "timing": "CUDA graph replay per step, CUDA events per step"},
+                   "timing": "CUDA graph replay per step, CUDA events per step; kernel "
+                             "intervals from event nodes captured around each kernel "
+                             "(second graph, no programmatic launch)"},
         "gpu_launches": launches_per_step * args.steps,
         "roofline": roofline,
         "kernels": kernels,

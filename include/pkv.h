@@ -129,8 +129,13 @@ PKV_API int64_t pkv_kernel_launch_count(void);
  * `which` made FROM THE CALLING HOST THREAD is bracketed by
  * cudaEventRecord(start_event) / cudaEventRecord(stop_event) on the launch
  * stream, so the caller can time that kernel alone with its own events
- * (cudaEvent_t handles, created and owned by the caller).  Passing NULL for
- * both turns it off again.  Returns PKV_ERR_RANGE for an unknown kernel id.
+ * (cudaEvent_t handles, created and owned by the caller).  When the launch
+ * stream is being captured into a CUDA graph the records are made with
+ * cudaEventRecordExternal, i.e. they become event-record nodes that fire on
+ * every replay.  While any event is set, kernels launch without programmatic
+ * dependent launch, so each one's interval holds that kernel alone.  Passing
+ * NULL for both turns it off again.  Returns PKV_ERR_RANGE for an unknown
+ * kernel id.
  */
 PKV_API pkv_status pkv_set_profile_events(int32_t which, void *start_event, void *stop_event);
 

@@ -18,12 +18,20 @@ struct ProfileEvents {
 };
 static thread_local ProfileEvents t_prof;
 
-void profile_begin(int which, pkv_stream stream) {
-  if (t_prof.start[which]) cudaEventRecord(static_cast<cudaEvent_t>(t_prof.start[which]), stream);
+// While the stream is being captured into a CUDA graph, the record becomes an
+// event-record node of the graph (cudaEventRecordExternal), so a replay times
+// the kernel with no host launch gap between the event and the kernel.
+static void record(void *ev, pkv_stream stream) {
+  if (!ev) return;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(stream, &cs);
+  if (cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev), stream, cudaEventRecordExternal);
+  else
+    cudaEventRecord(static_cast<cudaEvent_t>(ev), stream);
 }
-void profile_end(int which, pkv_stream stream) {
-  if (t_prof.stop[which]) cudaEventRecord(static_cast<cudaEvent_t>(t_prof.stop[which]), stream);
-}
+void profile_begin(int which, pkv_stream stream) { record(t_prof.start[which], stream); }
+void profile_end(int which, pkv_stream stream) { record(t_prof.stop[which], stream); }
 bool profiling_active() {
   for (int i = 0; i < 4; ++i)
     if (t_prof.start[i] || t_prof.stop[i]) return true;

@@ -8,7 +8,7 @@
 
 namespace pkv {
 
-constexpr int32_t kPlanMagic = 0x32564b50;  // "PKV2"
+constexpr int32_t kPlanMagic = 0x33564b50;  // "PKV3"
 constexpr int kBlockSize = 16;
 constexpr int kRowsPerTile = 16;    // query rows (token x head-in-group) per decode row group
 constexpr int kPrefillRows = 128;   // query tokens per tensor-core tile
@@ -63,15 +63,19 @@ struct MergeGroup {
 };
 static_assert(sizeof(MergeGroup) == 32, "merge group is 32 bytes");
 
-// Tensor-core work item: query tokens qi0 .. qi0+n_q-1 (n_q <= 128) of one
-// sequence x one query head.
+// Tensor-core work item: up to two query sub-tiles of one sequence whose query
+// heads share KV head h, so every K/V tile loaded serves both.  Sub-tile x is
+// query tokens qi0[x] .. qi0[x]+n_q[x]-1 (n_q <= 128) of query head hq[x];
+// sub-tile 0 sees at least as many keys as sub-tile 1; n_q[1] == 0 means a
+// single sub-tile.
 struct PrefillTile {
   int32_t seq;
-  int32_t qi0;
-  int32_t hq;
-  int32_t n_q;
+  int32_t h;
+  int32_t hq[2];
+  int32_t qi0[2];
+  int32_t n_q[2];
 };
-static_assert(sizeof(PrefillTile) == 16, "prefill tile is 16 bytes");
+static_assert(sizeof(PrefillTile) == 32, "prefill tile is 32 bytes");
 
 inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 

@@ -19,8 +19,10 @@
 //    Equal ranges leave no tail wave and no long/short CTA imbalance.
 //
 // Prefill-class rows (tensor-core kernel): sequences with at least 64 query
-// tokens are cut into tiles of 128 query tokens x one query head, ordered by
-// the number of keys they see (longest first).
+// tokens are cut into units of 128 query tokens x one query head.  Units of the
+// same KV head are paired (neighbours in key count: the heads of one token tile,
+// then adjacent token tiles), so one CTA loads each K/V tile once for two query
+// tiles.  Work items are ordered by the keys they see, longest first.
 #include <algorithm>
 #include <climits>
 #include <cstdlib>
@@ -97,11 +99,36 @@ extern "C" pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *con
     kv_tokens += ctx;
     max_nb = std::max(max_nb, (ctx + kBlockSize - 1) / kBlockSize);
     if (qs >= min_q_prefill) {
-      for (int32_t qi0 = 0; qi0 < qs; qi0 += kPrefillRows) {
-        int32_t n_q = std::min(kPrefillRows, qs - qi0);
-        for (int32_t hq = 0; hq < num_q_heads; ++hq) {
-          ptiles.push_back({s, qi0, hq, n_q});
-          ptile_keys.push_back((int64_t)ctx - qs + qi0 + n_q);
+      // units of 128 tokens x 1 query head; within one KV head, sorted by the
+      // keys they see, neighbours pair up into one work item (sub-tile 0 sees
+      // at least as many keys as sub-tile 1)
+      struct Unit {
+        int32_t hq, qi0, n_q;
+        int64_t keys;
+      };
+      std::vector<Unit> units;
+      for (int32_t h = 0; h < hkv; ++h) {
+        units.clear();
+        for (int32_t qi0 = qs - 1 - (qs - 1) % kPrefillRows; qi0 >= 0; qi0 -= kPrefillRows) {
+          const int32_t n_q = std::min(kPrefillRows, qs - qi0);
+          for (int32_t hq = h * group; hq < (h + 1) * group; ++hq)
+            units.push_back({hq, qi0, n_q, (int64_t)ctx - qs + qi0 + n_q});
+        }
+        for (size_t u = 0; u < units.size(); u += 2) {
+          PrefillTile t;
+          std::memset(&t, 0, sizeof t);
+          t.seq = s;
+          t.h = h;
+          t.hq[0] = units[u].hq;
+          t.qi0[0] = units[u].qi0;
+          t.n_q[0] = units[u].n_q;
+          if (u + 1 < units.size()) {
+            t.hq[1] = units[u + 1].hq;
+            t.qi0[1] = units[u + 1].qi0;
+            t.n_q[1] = units[u + 1].n_q;
+          }
+          ptiles.push_back(t);
+          ptile_keys.push_back(units[u].keys);
         }
       }
       continue;

@@ -42,19 +42,45 @@ def test_version_and_status_strings(pkv):
 def parse_plan(info, host):
     words = host.view(np.int32)
     hdr = words[:16]
-    assert hdr[0] == 0x32564B50
+    assert hdr[0] == 0x33564B50
     nw, npc, nm, npf = (info.num_decode_warps, info.num_decode_pieces, info.num_merge_groups,
                         info.num_prefill_tiles)
     off_w = 16
     off_p = off_w + ((nw + 1 + 7) // 8) * 8
     off_m = off_p + 8 * npc
     off_f = off_m + 8 * nm
-    assert info.plan_bytes == 4 * (off_f + 4 * npf)
+    assert info.plan_bytes == 4 * (off_f + 8 * npf)
     wb = words[off_w:off_w + nw + 1]
     pieces = words[off_p:off_m].reshape(npc, 8)
     mer = words[off_m:off_f].reshape(nm, 8)
-    pre = words[off_f:off_f + 4 * npf].reshape(npf, 4)
+    pre = words[off_f:off_f + 8 * npf].reshape(npf, 8)
     return hdr, wb, pieces, mer, pre
+
+
+def check_prefill_items(meta, pre, s):
+    """Work items of prefill-class sequence s: (seq, h, hq0, hq1, qi0_0, qi0_1, n0, n1).
+    Every (query head, 128-token tile) unit is covered exactly once; both sub-tiles
+    of an item read KV head h; sub-tile 0 sees at least as many keys as sub-tile 1."""
+    g = meta.num_q_heads // meta.num_kv_heads
+    qs, ctx = int(meta.q_lens[s]), int(meta.context_lens[s])
+    items = pre[pre[:, 0] == s]
+    units = []
+    for it in items:
+        _, h, hq0, hq1, qa, qb, na, nb = (int(v) for v in it)
+        assert 1 <= na <= 128 and 0 <= nb <= 128
+        subs = [(hq0, qa, na)] + ([(hq1, qb, nb)] if nb else [])
+        for hq, q0, n in subs:
+            assert hq // g == h and q0 % 128 == 0 and n == min(128, qs - q0)
+            units.append((hq, q0))
+        if nb:
+            assert ctx - qs + qa + na >= ctx - qs + qb + nb
+    expect = [(hq, q0) for hq in range(meta.num_q_heads) for q0 in range(0, qs, 128)]
+    assert sorted(units) == sorted(expect)
+    # pairing: at most one single sub-tile item per KV head
+    for h in range(meta.num_kv_heads):
+        mine = items[items[:, 1] == h]
+        assert int((mine[:, 7] == 0).sum()) <= 1
+    return len(items)
 
 
 def check_plan(meta, info, host, num_sms):
@@ -87,8 +113,10 @@ def check_plan(meta, info, host, num_sms):
             continue
         if s in prefill_seqs:
             assert len(mine) == 0
-            tiles = pre[pre[:, 0] == s]
-            assert len(tiles) == meta.num_q_heads * (-(-qs // 128))
+            units = meta.num_q_heads * (-(-qs // 128))
+            n_items = check_prefill_items(meta, pre, s)
+            assert n_items == sum(-(-(g * (-(-qs // 128))) // 2) for _ in range(hkv))
+            assert 2 * n_items >= units
             continue
         for qi0 in range(0, qs, nq_tile):
             n_q = min(nq_tile, qs - qi0)
