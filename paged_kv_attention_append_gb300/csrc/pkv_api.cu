@@ -136,6 +136,7 @@ extern "C" pkv_status pkv_paged_varlen_attention(
   const PlanOffsets off = plan_offsets(info->num_decode_warps, info->num_decode_pieces,
                                        info->num_merge_groups, info->num_prefill_tiles);
   a.warp_begin = reinterpret_cast<const int32_t *>(pb + off.warp_begin);
+  a.warp_first = reinterpret_cast<const Piece *>(pb + off.warp_first);
   a.num_decode_warps = info->num_decode_warps;
   a.pieces = reinterpret_cast<const Piece *>(pb + off.pieces);
   a.merge_groups = reinterpret_cast<const MergeGroup *>(pb + off.merges);

@@ -62,6 +62,7 @@ struct DecodeParams {
   const int32_t *context_lens;
   const int32_t *block_tables;
   const int32_t *warp_begin;
+  const Piece *warp_first;
   const Piece *pieces;
   const MergeGroup *merges;
   float *part_o;
@@ -76,6 +77,9 @@ struct DecodeParams {
   int32_t num_kv_heads;
   int32_t group;
   float scale_log2;
+  int64_t total_q;
+  const uint8_t *pool;  // for address-translation warm-up only (data goes through pool_map)
+  int64_t pool_bytes;
 };
 
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
@@ -157,16 +161,60 @@ __global__ void __launch_bounds__(kThreads, 2)
                                               ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = lane >> 2, c = lane & 3;
-  // launched early behind the preceding kernel: let our dependents launch, then
-  // wait for the predecessor's writes (pool, q, metadata) before reading anything
+  // launched early behind the preceding kernel: let our dependents launch.  The
+  // plan, the block tables and q are not written by the kernels this one follows
+  // (the KV append writes only the pool), so the warp's range, first piece and
+  // first block-table window are read before waiting for the predecessor; the
+  // pool, the workspace and out are touched only after the wait.
   pdl_trigger();
-  pdl_wait();
   const int gw = blockIdx.x * kWarps + warp;
-  if (gw >= p.num_warps) return;
-  const int pb = __ldg(p.warp_begin + gw), pe = __ldg(p.warp_begin + gw + 1);
-  if (pb >= pe) return;
+  const bool has_warp = gw < p.num_warps;
+  // Start-up is a chain of dependent reads (range -> piece -> table -> pool).
+  // After other work has cycled the caches, each step of that chain also pays
+  // address-translation misses; touching the pages of the block tables, of the
+  // step's small arrays and of the pool now, all independently, takes those
+  // misses in parallel with the first read.  (L2 prefetches only: no data is used.)
+  {
+    constexpr int64_t kPage = 2 << 20;
+    const int64_t tab_bytes = (int64_t)p.num_seqs * p.max_blocks_per_seq * 4;
+    const int64_t npool = (p.pool_bytes + kPage - 1) / kPage;
+    const int nw_all = gridDim.x * kWarps;
+    if (lane == 0 && (int64_t)gw * kPage < tab_bytes)
+      prefetch_l2(reinterpret_cast<const uint8_t *>(p.block_tables) + (int64_t)gw * kPage);
+    if (lane < 4) {  // a few pool pages per warp, spread over the whole pool
+      const int64_t pg = (int64_t)gw + (int64_t)lane * nw_all;
+      if (pg < npool) prefetch_l2(p.pool + pg * kPage);
+    }
+    if (gw == 0 && lane == 4) prefetch_l2(p.cu_q_lens);
+    if (gw == 0 && lane == 5) prefetch_l2(p.context_lens);
+    if (gw == 0 && lane == 6) prefetch_l2(p.q);
+  }
+  const int pb = has_warp ? __ldg(p.warp_begin + gw) : 0;
+  const int pe = has_warp ? __ldg(p.warp_begin + gw + 1) : 0;
+  Piece pp;
+  if (has_warp) pp = p.warp_first[gw];  // == pieces[pb], loaded beside the range
   const int hkv = p.num_kv_heads;
   const int G = p.group;
+  int win_base = 0, win_val = -1;  // table window: lane i holds entry win_base + i
+  bool win_ok = false;
+  if (has_warp && pb < pe && pp.seq >= 0 && pp.seq < p.num_seqs && pp.kb_begin >= 0 &&
+      pp.kb_begin < p.max_blocks_per_seq) {
+    win_base = pp.kb_begin;
+    const int idx = win_base + lane;
+    win_val = idx < min(pp.kb_end, p.max_blocks_per_seq)
+                  ? __ldg(p.block_tables + (int64_t)pp.seq * p.max_blocks_per_seq + idx)
+                  : -1;
+    win_ok = true;
+  }
+  // the first piece's sequence lengths, also ahead of the wait
+  int f_cu0 = 0, f_cu1 = 0, f_ctx = 0;
+  if (has_warp && pb < pe && pp.seq >= 0 && pp.seq < p.num_seqs) {
+    f_cu0 = __ldg(p.cu_q_lens + pp.seq);
+    f_cu1 = __ldg(p.cu_q_lens + pp.seq + 1);
+    f_ctx = __ldg(p.context_lens + pp.seq);
+  }
+  pdl_wait();
+  if (!has_warp || pb >= pe) return;
 
   uint8_t *ring = smem + warp * C::kRingBytes;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOffset) + warp * NSTAGE;
@@ -182,17 +230,22 @@ __global__ void __launch_bounds__(kThreads, 2)
   // warp (uniform control flow); lane 0 issues the copies.  The block table is
   // read 32 entries at a time with one coalesced warp load and the entries are
   // shuffled out, so refilling a stage never waits on a dependent global load.
-  int ppi = pb, pkb = 0, issued = 0;
-  int win_base = 0, win_val = -1;  // table window: lane i holds entry win_base + i
-  bool win_ok = false;
-  Piece pp = p.pieces[pb];
-  pkb = pp.kb_begin;
+  const Piece first = pp;  // the producer below moves pp ahead of the consumer
+  int ppi = pb, pkb = pp.kb_begin, issued = 0;
   auto issue_next = [&](int stage) {
     while (ppi < pe && pkb >= pp.kb_end) {
       if (++ppi < pe) {
         pp = p.pieces[ppi];
         pkb = pp.kb_begin;
         win_ok = false;
+        // the consumer reaches this piece NSTAGE blocks later: bring its q rows
+        // (n_q tokens x the group's G heads, G * 2D contiguous bytes per token) into L2
+        const int lpt = (G * D * 2 + 127) / 128;  // 128-byte lines per token
+        const int t = lane / lpt;
+        if (t < pp.n_q && pp.q_row0 >= 0 && pp.q_row0 + pp.n_q <= p.total_q && pp.h >= 0 &&
+            pp.h < hkv)
+          prefetch_l2(p.q + ((int64_t)(pp.q_row0 + t) * p.num_q_heads + pp.h * G) * D +
+                      (lane % lpt) * 64);
       }
     }
     if (ppi >= pe) return;
@@ -238,34 +291,26 @@ __global__ void __launch_bounds__(kThreads, 2)
   bool abandoned = false;
 
   for (int pi = pb; pi < pe && !abandoned; ++pi) {
-    const Piece pc = p.pieces[pi];
+    // the producer runs ahead and usually already holds this piece
+    const Piece pc = pi == pb ? first : (pi == ppi ? pp : p.pieces[pi]);
     // ---- piece metadata, checked against the device copies of the step arrays
     bool valid = pc.seq >= 0 && pc.seq < p.num_seqs && pc.h >= 0 && pc.h < hkv &&
                  pc.kb_begin >= 0 && pc.kb_begin <= pc.kb_end &&
-                 pc.kb_end <= p.max_blocks_per_seq;
-    int cu0 = 0, qs = 0, ctx = 0;
-    if (valid) {
-      cu0 = __ldg(p.cu_q_lens + pc.seq);
-      qs = __ldg(p.cu_q_lens + pc.seq + 1) - cu0;
-      ctx = __ldg(p.context_lens + pc.seq);
-      valid = pc.qi0 >= 0 && pc.n_q >= 1 && pc.qi0 + pc.n_q <= qs && qs <= ctx &&
-              pc.n_q * G <= kRowsPerTile &&
-              pc.kb_end <= (ctx - qs + pc.qi0 + pc.n_q - 1) / kBlockSize + 1;
-    }
-    if (!valid && lane == 0) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
-    const int R = valid ? pc.n_q * G : 0;
-    const int q_pos0 = ctx - qs + pc.qi0;  // causal position of the group's first token
-    const int lim_lo = r < R ? q_pos0 + r / G : -1;            // last visible key of row r
-    const int lim_hi = r + 8 < R ? q_pos0 + (r + 8) / G : -1;  // ... of row r + 8
-
-    // ---- Q fragments (A operand), head_dim permuted to match the K fragments
+                 pc.kb_end <= p.max_blocks_per_seq && pc.n_q >= 1 &&
+                 pc.n_q * G <= kRowsPerTile && pc.q_row0 >= 0 &&
+                 pc.q_row0 + pc.n_q <= p.total_q;
+    // ---- Q fragments (A operand), head_dim permuted to match the K fragments.
+    // Rows come straight from the plan's packed index (bounds-checked above), so
+    // these loads do not wait for the length loads below; a piece that then
+    // fails the check (R = 0) uses none of them.
+    const int Rq = valid ? pc.n_q * G : 0;
     uint32_t qa[2 * kL][4];
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       const int row = r + 8 * half;
-      const bool rv = row < R;
+      const bool rv = row < Rq;
       const __nv_bfloat16 *qrow =
-          p.q + ((int64_t)(cu0 + pc.qi0 + (rv ? row / G : 0)) * p.num_q_heads + pc.h * G +
+          p.q + ((int64_t)(pc.q_row0 + (rv ? row / G : 0)) * p.num_q_heads + pc.h * G +
                  (rv ? row % G : 0)) * D;
 #pragma unroll
       for (int L = 0; L < kL; ++L) {
@@ -277,6 +322,19 @@ __global__ void __launch_bounds__(kThreads, 2)
         qa[2 * L + 1][2 + half] = v.w;
       }
     }
+    int cu0 = 0, qs = 0, ctx = 0;
+    if (valid) {
+      cu0 = pi == pb ? f_cu0 : __ldg(p.cu_q_lens + pc.seq);
+      qs = (pi == pb ? f_cu1 : __ldg(p.cu_q_lens + pc.seq + 1)) - cu0;
+      ctx = pi == pb ? f_ctx : __ldg(p.context_lens + pc.seq);
+      valid = pc.qi0 >= 0 && pc.qi0 + pc.n_q <= qs && qs <= ctx && pc.q_row0 == cu0 + pc.qi0 &&
+              pc.kb_end <= (ctx - qs + pc.qi0 + pc.n_q - 1) / kBlockSize + 1;
+    }
+    if (!valid && lane == 0) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
+    const int R = valid ? pc.n_q * G : 0;
+    const int q_pos0 = ctx - qs + pc.qi0;  // causal position of the group's first token
+    const int lim_lo = r < R ? q_pos0 + r / G : -1;            // last visible key of row r
+    const int lim_hi = r + 8 < R ? q_pos0 + (r + 8) / G : -1;  // ... of row r + 8
 
     float o[kNt][4];
 #pragma unroll
@@ -483,6 +541,7 @@ DecodeParams make_params(const AttnArgs &a) {
   p.context_lens = a.context_lens;
   p.block_tables = a.block_tables;
   p.warp_begin = a.warp_begin;
+  p.warp_first = a.warp_first;
   p.pieces = a.pieces;
   p.merges = a.merge_groups;
   p.part_o = a.part_o;
@@ -497,6 +556,10 @@ DecodeParams make_params(const AttnArgs &a) {
   p.num_kv_heads = a.desc.num_kv_heads;
   p.group = a.num_q_heads / a.desc.num_kv_heads;
   p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.total_q = a.total_q;
+  p.pool = static_cast<const uint8_t *>(a.kv_pool);
+  p.pool_bytes = (int64_t)a.desc.num_blocks * 2 * a.desc.num_kv_heads * kBlockSize *
+                 a.desc.head_dim * 2;
   return p;
 }
 

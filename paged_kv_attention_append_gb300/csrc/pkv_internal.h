@@ -17,6 +17,8 @@ constexpr int kDecodeWarpsPerCta = 4;
 // Plan buffer layout (all offsets are functions of the counts):
 //   [PlanHeader 64 B]
 //   [warp_begin: int32 x (num_decode_warps + 1), padded to 32 B]
+//   [warp_first: Piece x num_decode_warps] (copy of each warp's first piece, so a
+//    warp reads its range and first piece with two independent loads)
 //   [Piece x num_decode_pieces][MergeGroup x num_merge_groups]
 //   [PrefillTile x num_prefill_tiles]
 struct PlanHeader {
@@ -47,7 +49,7 @@ struct Piece {
   int32_t kb_begin;  // first logical KV block of the piece
   int32_t kb_end;    // one past the last logical KV block of the piece
   int32_t part;      // partial slot, or -1 when the piece is the whole segment (writes out)
-  int32_t merge;     // merge group of the segment when part >= 0, else -1
+  int32_t q_row0;    // packed query index of token qi0 (cu_q_lens[seq] + qi0)
 };
 static_assert(sizeof(Piece) == 32, "piece is 32 bytes");
 
@@ -80,13 +82,14 @@ static_assert(sizeof(PrefillTile) == 32, "prefill tile is 32 bytes");
 inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
 struct PlanOffsets {
-  int64_t warp_begin, pieces, merges, prefill, total;
+  int64_t warp_begin, warp_first, pieces, merges, prefill, total;
 };
 inline PlanOffsets plan_offsets(int32_t n_warps, int32_t n_pieces, int32_t n_merge,
                                 int32_t n_prefill) {
   PlanOffsets o;
   o.warp_begin = (int64_t)sizeof(PlanHeader);
-  o.pieces = o.warp_begin + align_up(4ll * (n_warps + 1), 32);
+  o.warp_first = o.warp_begin + align_up(4ll * (n_warps + 1), 32);
+  o.pieces = o.warp_first + (int64_t)n_warps * (int64_t)sizeof(Piece);
   o.merges = o.pieces + (int64_t)n_pieces * (int64_t)sizeof(Piece);
   o.prefill = o.merges + (int64_t)n_merge * (int64_t)sizeof(MergeGroup);
   o.total = o.prefill + (int64_t)n_prefill * (int64_t)sizeof(PrefillTile);
@@ -121,6 +124,7 @@ struct AttnArgs {
   int64_t total_q;
   float scale;
   const int32_t *warp_begin;
+  const Piece *warp_first;
   int32_t num_decode_warps;
   const Piece *pieces;
   const MergeGroup *merge_groups;

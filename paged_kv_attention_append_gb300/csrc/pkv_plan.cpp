@@ -13,7 +13,8 @@
 //    query head that reads it.  A segment is (row group, KV head) with the
 //    blocks [0, last visible key / 16].
 //  * All segments' blocks are laid end to end and cut into num_decode_warps
-//    equal contiguous ranges, one per warp (8 warps per SM, one wave).  A range
+//    contiguous ranges of equal cost (blocks plus a fixed charge per segment
+//    start), one per warp (8 warps per SM, one wave).  A range
 //    intersects one or more segments; each intersection is a piece.  A segment
 //    cut into several pieces gets one partial slot per piece and a merge group.
 //    Equal ranges leave no tail wave and no long/short CTA imbalance.
@@ -151,11 +152,34 @@ extern "C" pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *con
   std::vector<Piece> pieces;
   std::vector<int32_t> piece_seg;
   {
+    // Equal cost, not equal blocks: a block costs kBlockCost and starting a
+    // segment (its q rows and lengths, a fresh table window) costs kPieceCost, so
+    // a warp whose range crosses into another segment gets fewer blocks.  Block
+    // i of segment k sits at cost position start_k + kPieceCost + kBlockCost*i
+    // (+ half a block) and goes to the warp whose equal share of the total cost
+    // holds that position; the ranges stay contiguous in the block stream.  With
+    // at least kMinBlocksPerWarp blocks per warp every share holds a block.
+    constexpr int64_t kBlockCost = 2, kPieceCost = 3;
+    const int64_t total_cost = kBlockCost * total_blocks + kPieceCost * (int64_t)segs.size();
+    std::vector<int64_t> cut(num_warps + 1, total_blocks);  // first block of each warp
+    {
+      int64_t blk = 0, cost = 0;
+      int32_t w = 0;
+      cut[0] = 0;
+      for (const Segment &g : segs) {
+        cost += kPieceCost;
+        for (int32_t i = 0; i < g.nb; ++i, ++blk, cost += kBlockCost) {
+          const int64_t owner = (cost + kBlockCost / 2) * num_warps / total_cost;
+          while (w < owner && w < num_warps) cut[++w] = blk;
+        }
+      }
+      while (w < num_warps) cut[++w] = total_blocks;
+    }
     size_t k = 0;
     int64_t seg_off = 0;  // global block offset of segment k
     for (int32_t w = 0; w < num_warps; ++w) {
       warp_begin[w] = (int32_t)pieces.size();
-      int64_t a = total_blocks * w / num_warps, b = total_blocks * (w + 1) / num_warps;
+      int64_t a = cut[w], b = cut[w + 1];
       while (a < b) {
         while (seg_off + segs[k].nb <= a) seg_off += segs[k++].nb;
         const Segment &g = segs[k];
@@ -168,7 +192,7 @@ extern "C" pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *con
         p.kb_begin = (int32_t)(a - seg_off);
         p.kb_end = (int32_t)(e - seg_off);
         p.part = -1;
-        p.merge = -1;
+        p.q_row0 = cu_q_lens[g.seq] + g.qi0;
         pieces.push_back(p);
         piece_seg.push_back((int32_t)k);
         a = e;
@@ -191,10 +215,7 @@ extern "C" pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *con
       m.h = pieces[i].h;
       m.part0 = parts;
       m.nsplit = (int32_t)(j - i);
-      for (size_t t = i; t < j; ++t) {
-        pieces[t].part = parts++;
-        pieces[t].merge = (int32_t)merges.size();
-      }
+      for (size_t t = i; t < j; ++t) pieces[t].part = parts++;
       merges.push_back(m);
     }
     i = j;
@@ -253,6 +274,9 @@ extern "C" pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *con
   h.max_blocks_needed = max_nb;
   std::memcpy(p, &h, sizeof h);
   std::memcpy(p + off.warp_begin, warp_begin.data(), warp_begin.size() * sizeof(int32_t));
+  for (int32_t w = 0; w < num_warps; ++w)
+    std::memcpy(p + off.warp_first + (int64_t)w * sizeof(Piece), &pieces[warp_begin[w]],
+                sizeof(Piece));
   if (!pieces.empty()) std::memcpy(p + off.pieces, pieces.data(), pieces.size() * sizeof(Piece));
   if (!merges.empty())
     std::memcpy(p + off.merges, merges.data(), merges.size() * sizeof(MergeGroup));

@@ -46,12 +46,16 @@ def parse_plan(info, host):
     nw, npc, nm, npf = (info.num_decode_warps, info.num_decode_pieces, info.num_merge_groups,
                         info.num_prefill_tiles)
     off_w = 16
-    off_p = off_w + ((nw + 1 + 7) // 8) * 8
+    off_first = off_w + ((nw + 1 + 7) // 8) * 8
+    off_p = off_first + 8 * nw
     off_m = off_p + 8 * npc
     off_f = off_m + 8 * nm
     assert info.plan_bytes == 4 * (off_f + 8 * npf)
     wb = words[off_w:off_w + nw + 1]
     pieces = words[off_p:off_m].reshape(npc, 8)
+    first = words[off_first:off_p].reshape(nw, 8)
+    if nw:
+        assert np.array_equal(first, pieces[wb[:-1]])  # each warp's first piece, copied
     mer = words[off_m:off_f].reshape(nm, 8)
     pre = words[off_f:off_f + 8 * npf].reshape(npf, 8)
     return hdr, wb, pieces, mer, pre
@@ -90,14 +94,18 @@ def check_plan(meta, info, host, num_sms):
     nq_tile = max(1, 16 // g)
     assert info.total_q == meta.total_q
     assert info.kv_tokens == int(meta.context_lens[meta.q_lens > 0].astype(np.int64).sum())
-    # warp ranges: contiguous, cover all pieces, equal block counts (+-1)
+    # warp ranges: contiguous, cover all pieces, equal cost: 2 per block plus 3
+    # per segment start; each of a range's two ends may be off by one block and
+    # one segment start
     nw = info.num_decode_warps
     if nw:
         assert wb[0] == 0 and wb[-1] == len(pieces) and np.all(np.diff(wb) >= 1)
         per_warp = [int((pieces[wb[w]:wb[w + 1], 5] - pieces[wb[w]:wb[w + 1], 4]).sum())
                     for w in range(nw)]
         assert sum(per_warp) == info.decode_blocks
-        assert max(per_warp) - min(per_warp) <= 1
+        cost = [2 * per_warp[w] + 3 * int((pieces[wb[w]:wb[w + 1], 4] == 0).sum())
+                for w in range(nw)]
+        assert max(cost) - min(cost) <= 2 * (2 + 3)
         if num_sms is not None:
             assert nw <= num_sms * 8
     assert np.all(pieces[:, 5] > pieces[:, 4])
