@@ -98,11 +98,19 @@ typedef struct pkv_plan_info {
   int32_t total_q;
   int32_t num_decode_warps;  /* warps of the split-KV kernel; each streams an equal share of keys */
   int32_t num_decode_pieces; /* (row group, KV head, key range) pieces over all decode warps */
-  int32_t num_merge_groups;  /* (row group, KV head) pairs whose keys span several pieces */
-  int32_t num_partials;      /* partial-result slots (one per piece of a merge group) */
-  int32_t num_prefill_tiles; /* tensor-core work items: up to 128 query tokens x 1 query head */
+  int32_t num_merge_groups;  /* results combined from partials: decode (row group, KV head)
+                                pairs whose keys span several pieces, then prefill sub-tiles
+                                whose keys span several work items */
+  int32_t num_partials;      /* decode partial-result slots (one per piece of a merge group) */
+  int32_t num_prefill_tiles; /* tensor-core work items: a key range of two 128-token x 1-head
+                                query tiles of one KV head */
   int32_t num_kernels;       /* kernel launches one pkv_paged_varlen_attention call makes */
   int32_t max_blocks_needed; /* max over sequences of ceil(context_len / block_size) */
+  int32_t num_prefill_ctas;  /* persistent tensor-core CTAs (one per SM at most); each runs
+                                an equal-cost range of the work items' key tiles */
+  int32_t num_prefill_partials; /* prefill partial-result slots (128 rows each) */
+  int32_t num_prefill_merges;   /* prefill merge groups (the last ones of num_merge_groups) */
+  int32_t reserved;
   int64_t kv_tokens;         /* sum of context_lens over sequences with q_len > 0 */
   int64_t decode_blocks;     /* (KV block, KV head) pairs streamed by the split-KV kernel */
   int64_t plan_bytes;        /* bytes of the plan buffer (host, then device copy) */

@@ -50,7 +50,9 @@ class PlanInfo(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "num_seqs", "num_q_heads", "num_kv_heads", "head_dim", "total_q", "num_decode_warps",
         "num_decode_pieces", "num_merge_groups", "num_partials", "num_prefill_tiles", "num_kernels",
-        "max_blocks_needed")] + [(n, ctypes.c_int64) for n in ("kv_tokens", "decode_blocks",
+        "max_blocks_needed", "num_prefill_ctas", "num_prefill_partials", "num_prefill_merges",
+        "reserved")] + [(n, ctypes.c_int64) for n in (
+            "kv_tokens", "decode_blocks",
                                                               "plan_bytes", "workspace_bytes")]
 
     def as_dict(self):

@@ -133,20 +133,37 @@ extern "C" pkv_status pkv_paged_varlen_attention(
   a.total_q = info->total_q;
   a.scale = scale;
   const char *pb = static_cast<const char *>(plan_dev);
+  if (info->num_prefill_ctas < 0 || info->num_prefill_ctas > info->num_prefill_tiles ||
+      (info->num_prefill_tiles > 0 && info->num_prefill_ctas == 0))
+    return PKV_ERR_SHAPE;
   const PlanOffsets off = plan_offsets(info->num_decode_warps, info->num_decode_pieces,
-                                       info->num_merge_groups, info->num_prefill_tiles);
+                                       info->num_merge_groups, info->num_prefill_tiles,
+                                       info->num_prefill_ctas);
   a.warp_begin = reinterpret_cast<const int32_t *>(pb + off.warp_begin);
   a.warp_first = reinterpret_cast<const Piece *>(pb + off.warp_first);
   a.num_decode_warps = info->num_decode_warps;
   a.pieces = reinterpret_cast<const Piece *>(pb + off.pieces);
   a.merge_groups = reinterpret_cast<const MergeGroup *>(pb + off.merges);
   a.num_merge_groups = info->num_merge_groups;
+  a.prefill_begin = reinterpret_cast<const int32_t *>(pb + off.prefill_begin);
   a.prefill_tiles = reinterpret_cast<const PrefillTile *>(pb + off.prefill);
   a.num_prefill_tiles = info->num_prefill_tiles;
+  a.num_prefill_ctas = info->num_prefill_ctas;
+  if (info->num_prefill_merges < 0 || info->num_prefill_merges > info->num_merge_groups ||
+      info->num_prefill_partials < 0 || info->num_partials < 0)
+    return PKV_ERR_SHAPE;
   char *wb = static_cast<char *>(workspace);
+  const int d = desc->head_dim;
+  const int64_t off_ml = ws_part_o_bytes(info->num_partials, d);
+  const int64_t off_po = off_ml + ws_part_ml_bytes(info->num_partials);
+  const int64_t off_pml = off_po + ws_ppart_o_bytes(info->num_prefill_partials, d);
   a.part_o = reinterpret_cast<float *>(wb);
-  a.part_ml = reinterpret_cast<float *>(
-      wb ? wb + ws_part_o_bytes(info->num_partials, desc->head_dim) : nullptr);
+  a.part_ml = reinterpret_cast<float *>(wb ? wb + off_ml : nullptr);
+  a.ppart_o = reinterpret_cast<float *>(wb ? wb + off_po : nullptr);
+  a.ppart_ml = reinterpret_cast<float *>(wb ? wb + off_pml : nullptr);
+  a.num_decode_merges = info->num_merge_groups - info->num_prefill_merges;
+  if (ws_total_bytes(info->num_partials, info->num_prefill_partials, d) > workspace_bytes)
+    return PKV_ERR_WORKSPACE;
   a.dev_status = dev_status;
   a.stream = stream;
 

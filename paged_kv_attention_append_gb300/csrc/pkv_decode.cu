@@ -67,8 +67,11 @@ struct DecodeParams {
   const MergeGroup *merges;
   float *part_o;
   float2 *part_ml;
+  const float *ppart_o;
+  const float2 *ppart_ml;
   int32_t *dev_status;
-  int32_t num_merges;
+  int32_t num_merges;          // all merge groups: decode ones, then prefill ones
+  int32_t num_decode_merges;
   int32_t num_warps;
   int32_t num_seqs;
   int32_t max_blocks_per_seq;
@@ -92,45 +95,38 @@ __device__ __forceinline__ void write_piece(const DecodeParams &p, const Piece &
                                             float (&o)[D / 8][4], float m_lo, float m_hi,
                                             float l_lo, float l_hi, int R, int cu0, int r, int c);
 
-// LSE merge of the segments cut into several pieces:
+// LSE merge of results whose keys were cut into several parts (decode segments
+// cut into several pieces; prefill sub-tiles cut into several work items):
 //   M = max_j m_j,  out = sum_j 2^(m_j - M) O_j / sum_j 2^(m_j - M) l_j.
 // One thread per (merge group, row, 4 output columns) makes a single pass over
 // the group's splits with a running max (each new split rescales the running
-// sums), unrolled so several splits' loads are in flight at once.
+// sums), unrolled so several splits' loads are in flight at once.  Decode
+// groups come first (partial slots of 16 rows), then prefill groups (slots of
+// 128 rows); both write bf16 rows of out.
 constexpr int kMergeThreads = 256;
 
+// Combines one row's 4 columns over nsplit partial slots (slot stride `rows`).
 template <int D>
-__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams p,
-                                                              int32_t num_groups) {
-  constexpr int kChunks = D / 4;  // float4 chunks of a row
-  pdl_wait();                     // the split-KV partials are complete and visible
-  const int64_t t = (int64_t)blockIdx.x * kMergeThreads + threadIdx.x;
-  const int64_t gi = t / (kRowsPerTile * kChunks);
-  const int rem = (int)(t % (kRowsPerTile * kChunks));
-  const int row = rem / kChunks, ch = rem % kChunks;
-  if (gi >= num_groups) return;
-  const MergeGroup g = p.merges[gi];
-  const int G = p.group;
-  if (row >= g.n_q * G || g.seq < 0 || g.seq >= p.num_seqs || g.n_q * G > kRowsPerTile) return;
-  const float2 *ml = p.part_ml + (int64_t)g.part0 * kRowsPerTile + row;
-  const float4 *po =
-      reinterpret_cast<const float4 *>(p.part_o + ((int64_t)g.part0 * kRowsPerTile + row) * D) + ch;
-  float M = -INFINITY, L = 0.f;
+__device__ __forceinline__ float4 merge_row(const float2 *ml, const float4 *po, int nsplit,
+                                            int rows, float &L) {
+  constexpr int kChunks = D / 4;
+  float M = -INFINITY;
+  L = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   constexpr int kBatch = 8;  // splits whose loads are all issued before any is used
-  for (int j0 = 0; j0 < g.nsplit; j0 += kBatch) {
+  for (int j0 = 0; j0 < nsplit; j0 += kBatch) {
     float2 v[kBatch];
     float4 x[kBatch];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int j = min(j0 + u, g.nsplit - 1);  // past the end: reload the last split, unused
-      v[u] = ml[(int64_t)j * kRowsPerTile];
-      x[u] = po[(int64_t)j * kRowsPerTile * kChunks];
+    for (int u = 0; u < kBatch; ++u) {  // predicated: nothing is loaded past the last split
+      const bool in = j0 + u < nsplit;
+      v[u] = in ? ml[(int64_t)(j0 + u) * rows] : make_float2(-INFINITY, 0.f);
+      x[u] = in ? po[(int64_t)(j0 + u) * rows * kChunks] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       // skip padding entries and splits in which this row saw no key
-      if (j0 + u >= g.nsplit || v[u].x == -INFINITY) continue;
+      if (v[u].x == -INFINITY) continue;
       const float mn = fmaxf(M, v[u].x);
       const float a = fast_exp2(M - mn), b = fast_exp2(v[u].x - mn);
       L = L * a + v[u].y * b;
@@ -141,13 +137,42 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
       M = mn;
     }
   }
+  return acc;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams p) {
+  constexpr int kChunks = D / 4;  // float4 chunks of a row
+  pdl_wait();                     // the partials are complete and visible
+  const int64_t t = (int64_t)blockIdx.x * kMergeThreads + threadIdx.x;
+  const int64_t n_dec = (int64_t)p.num_decode_merges * kRowsPerTile * kChunks;
+  const bool dec = t < n_dec;
+  const int rows = dec ? kRowsPerTile : kPrefillRows;
+  const int64_t tt = dec ? t : t - n_dec;
+  const int64_t gi = tt / (rows * kChunks);
+  const int rem = (int)(tt % (rows * kChunks));
+  const int row = rem / kChunks, ch = rem % kChunks;
+  if (gi >= (dec ? p.num_decode_merges : p.num_merges - p.num_decode_merges)) return;
+  const MergeGroup g = p.merges[dec ? gi : p.num_decode_merges + gi];
+  const int G = p.group;
+  const int nrows = dec ? g.n_q * G : g.n_q;
+  if (row >= nrows || nrows > rows || g.seq < 0 || g.seq >= p.num_seqs || g.nsplit < 1 ||
+      g.kind != (dec ? 0 : 1))
+    return;
+  const float2 *ml = (dec ? p.part_ml : p.ppart_ml) + (int64_t)g.part0 * rows + row;
+  const float4 *po = reinterpret_cast<const float4 *>((dec ? p.part_o : p.ppart_o) +
+                                                      ((int64_t)g.part0 * rows + row) * D) +
+                     ch;
+  float L;
+  const float4 acc = merge_row<D>(ml, po, g.nsplit, rows, L);
   const float inv = L > 0.f ? 1.f / L : 0.f;
   const int cu0 = __ldg(p.cu_q_lens + g.seq);
-  const int64_t tok = cu0 + g.qi0 + row / G;
+  const int64_t tok = cu0 + g.qi0 + (dec ? row / G : row);
+  const int hq = dec ? g.h * G + row % G : g.h;
   uint2 pk;
   pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
   pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-  *reinterpret_cast<uint2 *>(p.out + (tok * p.num_q_heads + g.h * G + row % G) * D + 4 * ch) = pk;
+  *reinterpret_cast<uint2 *>(p.out + (tok * p.num_q_heads + hq) * D + 4 * ch) = pk;
 }
 
 template <int D, int NSTAGE>
@@ -547,6 +572,9 @@ DecodeParams make_params(const AttnArgs &a) {
   p.part_o = a.part_o;
   p.part_ml = reinterpret_cast<float2 *>(a.part_ml);
   p.num_merges = a.num_merge_groups;
+  p.num_decode_merges = a.num_decode_merges;
+  p.ppart_o = a.ppart_o;
+  p.ppart_ml = reinterpret_cast<const float2 *>(a.ppart_ml);
   p.dev_status = a.dev_status;
   p.num_warps = a.num_decode_warps;
   p.num_seqs = a.num_seqs;
@@ -614,16 +642,18 @@ int launch_decode(const AttnArgs &a, int *launches) {
 
 int launch_merge(const AttnArgs &a, int *launches) {
   if (a.num_merge_groups <= 0) return 0;
-  const int64_t threads = (int64_t)a.num_merge_groups * kRowsPerTile * (a.desc.head_dim / 4);
+  const int64_t threads = ((int64_t)a.num_decode_merges * kRowsPerTile +
+                           (int64_t)(a.num_merge_groups - a.num_decode_merges) * kPrefillRows) *
+                          (a.desc.head_dim / 4);
   const dim3 grid((unsigned)((threads + kMergeThreads - 1) / kMergeThreads));
   const bool pdl = !profiling_active();
   profile_begin(PKV_KERNEL_MERGE, a.stream);
   const cudaError_t le =
       a.desc.head_dim == 128
           ? launch_kernel(merge_kernel<128>, grid, dim3(kMergeThreads), 0, a.stream, pdl,
-                          make_params(a), a.num_merge_groups)
+                          make_params(a))
           : launch_kernel(merge_kernel<64>, grid, dim3(kMergeThreads), 0, a.stream, pdl,
-                          make_params(a), a.num_merge_groups);
+                          make_params(a));
   profile_end(PKV_KERNEL_MERGE, a.stream);
   const int e = le != cudaSuccess ? (int)le : (int)cudaGetLastError();
   if (!e) {

@@ -20,7 +20,8 @@ constexpr int kDecodeWarpsPerCta = 4;
 //   [warp_first: Piece x num_decode_warps] (copy of each warp's first piece, so a
 //    warp reads its range and first piece with two independent loads)
 //   [Piece x num_decode_pieces][MergeGroup x num_merge_groups]
-//   [PrefillTile x num_prefill_tiles]
+//   [prefill_begin: int32 x (num_prefill_ctas + 1), padded to 32 B; absent when 0 CTAs]
+//   [PrefillTile x num_prefill_tiles, grouped by CTA]
 struct PlanHeader {
   int32_t magic;
   int32_t num_seqs;
@@ -53,7 +54,11 @@ struct Piece {
 };
 static_assert(sizeof(Piece) == 32, "piece is 32 bytes");
 
-// A segment whose keys span nsplit pieces with partial slots part0 .. part0+nsplit-1.
+// A set of nsplit partial results (slots part0 .. part0+nsplit-1) to combine.
+// kind 0: a decode segment -- rows are n_q tokens x the group's heads of KV
+//         head h, partial slots of kRowsPerTile rows;
+// kind 1: a prefill sub-tile cut along its keys -- rows are the n_q tokens of
+//         query head h (here a query head), partial slots of kPrefillRows rows.
 struct MergeGroup {
   int32_t seq;
   int32_t qi0;
@@ -61,7 +66,8 @@ struct MergeGroup {
   int32_t h;
   int32_t part0;
   int32_t nsplit;
-  int32_t pad[2];
+  int32_t kind;
+  int32_t pad;
 };
 static_assert(sizeof(MergeGroup) == 32, "merge group is 32 bytes");
 
@@ -69,40 +75,59 @@ static_assert(sizeof(MergeGroup) == 32, "merge group is 32 bytes");
 // heads share KV head h, so every K/V tile loaded serves both.  Sub-tile x is
 // query tokens qi0[x] .. qi0[x]+n_q[x]-1 (n_q <= 128) of query head hq[x];
 // sub-tile 0 sees at least as many keys as sub-tile 1; n_q[1] == 0 means a
-// single sub-tile.
+// single sub-tile.  The item covers key tiles kt0 .. kt1-1 (128 keys each) of
+// the pair; a sub-tile whose keys the item covers only in part writes its
+// unnormalised result to prefill partial slot part[x] (else part[x] = -1 and it
+// writes out directly).
 struct PrefillTile {
   int32_t seq;
   int32_t h;
   int32_t hq[2];
   int32_t qi0[2];
   int32_t n_q[2];
+  int32_t kt0;
+  int32_t kt1;
+  int32_t part[2];
 };
-static_assert(sizeof(PrefillTile) == 32, "prefill tile is 32 bytes");
+static_assert(sizeof(PrefillTile) == 48, "prefill tile is 48 bytes");
 
 inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
 struct PlanOffsets {
-  int64_t warp_begin, warp_first, pieces, merges, prefill, total;
+  int64_t warp_begin, warp_first, pieces, merges, prefill_begin, prefill, total;
 };
 inline PlanOffsets plan_offsets(int32_t n_warps, int32_t n_pieces, int32_t n_merge,
-                                int32_t n_prefill) {
+                                int32_t n_prefill, int32_t n_prefill_ctas) {
   PlanOffsets o;
   o.warp_begin = (int64_t)sizeof(PlanHeader);
   o.warp_first = o.warp_begin + align_up(4ll * (n_warps + 1), 32);
   o.pieces = o.warp_first + (int64_t)n_warps * (int64_t)sizeof(Piece);
   o.merges = o.pieces + (int64_t)n_pieces * (int64_t)sizeof(Piece);
-  o.prefill = o.merges + (int64_t)n_merge * (int64_t)sizeof(MergeGroup);
+  o.prefill_begin = o.merges + (int64_t)n_merge * (int64_t)sizeof(MergeGroup);
+  o.prefill = o.prefill_begin + (n_prefill_ctas > 0 ? align_up(4ll * (n_prefill_ctas + 1), 32) : 0);
   o.total = o.prefill + (int64_t)n_prefill * (int64_t)sizeof(PrefillTile);
   return o;
 }
 
-// Workspace: partial O [num_partials][16][D] fp32, then (m, l) pairs
-// [num_partials][16] float2 (only the row group's rows are written).
+// Workspace: decode partial O [num_partials][16][D] fp32, then (m, l) pairs
+// [num_partials][16] float2 (only the row group's rows are written); then
+// prefill partial O [num_prefill_partials][128][D] fp32 and (m, l)
+// [num_prefill_partials][128] float2.
 inline int64_t ws_part_o_bytes(int32_t parts, int32_t d) {
   return align_up((int64_t)parts * kRowsPerTile * d * 4, 256);
 }
 inline int64_t ws_part_ml_bytes(int32_t parts) {
   return align_up((int64_t)parts * kRowsPerTile * 8, 256);
+}
+inline int64_t ws_ppart_o_bytes(int32_t pparts, int32_t d) {
+  return align_up((int64_t)pparts * kPrefillRows * d * 4, 256);
+}
+inline int64_t ws_ppart_ml_bytes(int32_t pparts) {
+  return align_up((int64_t)pparts * kPrefillRows * 8, 256);
+}
+inline int64_t ws_total_bytes(int32_t parts, int32_t pparts, int32_t d) {
+  return ws_part_o_bytes(parts, d) + ws_part_ml_bytes(parts) + ws_ppart_o_bytes(pparts, d) +
+         ws_ppart_ml_bytes(pparts);
 }
 
 // Kernel launchers (defined in the .cu files).  Return a cudaError_t value.
@@ -129,10 +154,15 @@ struct AttnArgs {
   const Piece *pieces;
   const MergeGroup *merge_groups;
   int32_t num_merge_groups;
+  const int32_t *prefill_begin;
   const PrefillTile *prefill_tiles;
   int32_t num_prefill_tiles;
+  int32_t num_prefill_ctas;
   float *part_o;
   float *part_ml;
+  float *ppart_o;
+  float *ppart_ml;
+  int32_t num_decode_merges;  // merge_groups[0 .. num_decode_merges) are kind 0
   int32_t *dev_status;
   pkv_stream stream;
 };

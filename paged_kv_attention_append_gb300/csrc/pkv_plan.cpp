@@ -23,8 +23,11 @@
 // tokens are cut into units of 128 query tokens x one query head.  Units of the
 // same KV head are paired (neighbours in key count: the heads of one token tile,
 // then adjacent token tiles), so one CTA loads each K/V tile once for two query
-// tiles.  Work items are ordered by the keys they see, longest first.
+// tiles.  One persistent CTA per SM (at most) runs a list of work items of
+// equal total cost: whole pairs first, then pieces of the leftover sub-tiles
+// cut along their keys, whose partial results a merge combines.
 #include <algorithm>
+#include <array>
 #include <climits>
 #include <cstdlib>
 #include <cstring>
@@ -41,6 +44,13 @@ constexpr int kMinBlocksPerWarp = 4;
 // (default 64; the environment variable PKV_PREFILL_MIN_Q overrides it, 0 or
 // a negative value keeps every row on the split-KV kernel).
 constexpr int kPrefillMinQDefault = 64;
+// Relative costs used to give the persistent prefill CTAs equal work: a key
+// tile both sub-tiles of a pair run (their MMAs and softmaxes overlap), a key
+// tile only one sub-tile runs, and starting a work item (Q load, pipeline fill,
+// epilogue).
+constexpr int64_t kPairTileCost = 10, kSingleTileCost = 8, kItemStartCost = 10;
+// CTAs get at least this many key tiles of work.
+constexpr int64_t kMinTilesPerCta = 4;
 
 int prefill_min_q() {
   const char *env = std::getenv("PKV_PREFILL_MIN_Q");
@@ -87,8 +97,8 @@ extern "C" pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *con
   if (num_seqs > 0 && cu_q_lens[0] != 0) return PKV_ERR_SHAPE;
   const int min_q_prefill = prefill_min_q();
   std::vector<Segment> segs;
-  std::vector<PrefillTile> ptiles;
-  std::vector<int64_t> ptile_keys;
+  std::vector<PrefillTile> pairs;                 // sub-tile pairs, key range not yet cut
+  std::vector<std::array<int32_t, 2>> pair_nt;   // key tiles seen by each sub-tile
   int64_t kv_tokens = 0, total_blocks = 0;
   int32_t max_nb = 0;
   for (int32_t s = 0; s < num_seqs; ++s) {
@@ -128,8 +138,12 @@ extern "C" pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *con
             t.qi0[1] = units[u + 1].qi0;
             t.n_q[1] = units[u + 1].n_q;
           }
-          ptiles.push_back(t);
-          ptile_keys.push_back(units[u].keys);
+          t.part[0] = t.part[1] = -1;
+          pairs.push_back(t);
+          pair_nt.push_back({(int32_t)((units[u].keys + kPrefillRows - 1) / kPrefillRows),
+                             u + 1 < units.size()
+                                 ? (int32_t)((units[u + 1].keys + kPrefillRows - 1) / kPrefillRows)
+                                 : 0});
         }
       }
       continue;
@@ -220,21 +234,138 @@ extern "C" pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *con
     }
     i = j;
   }
-  // prefill tiles, most keys first
-  {
-    std::vector<size_t> order(ptiles.size());
+  // ---- prefill work per persistent CTA (at most one per SM), equal cost:
+  //  1. whole pairs, largest first, each into the least-loaded CTA that stays
+  //     within the per-CTA target;
+  //  2. the pairs left over are split into their sub-tiles, whose key tiles are
+  //     laid end to end and cut at the CTAs' remaining capacities.  A sub-tile
+  //     cut there gets one partial slot per piece and a merge group (kind 1).
+  std::vector<PrefillTile> ptiles;
+  std::vector<int32_t> pf_begin;
+  std::vector<MergeGroup> pmerges;
+  int32_t pparts = 0;
+  int32_t n_pf_ctas = 0;
+  if (!pairs.empty()) {
+    auto pair_cost = [&](size_t pi) {
+      const int64_t nt0 = pair_nt[pi][0], nt1 = pair_nt[pi][1];
+      return kItemStartCost + kPairTileCost * nt1 + kSingleTileCost * (nt0 - nt1);
+    };
+    int64_t total = 0, ntiles = 0;
+    for (size_t pi = 0; pi < pairs.size(); ++pi) {
+      total += pair_cost(pi);
+      ntiles += pair_nt[pi][0];
+    }
+    n_pf_ctas = (int32_t)std::max<int64_t>(
+        1, std::min<int64_t>(num_sms, ntiles / kMinTilesPerCta));
+    const int64_t target = (total + n_pf_ctas - 1) / n_pf_ctas;
+    std::vector<size_t> order(pairs.size());
     for (size_t i = 0; i < order.size(); ++i) order[i] = i;
     std::stable_sort(order.begin(), order.end(),
-                     [&](size_t x, size_t y) { return ptile_keys[x] > ptile_keys[y]; });
-    std::vector<PrefillTile> sorted;
-    sorted.reserve(ptiles.size());
-    for (size_t i : order) sorted.push_back(ptiles[i]);
-    ptiles.swap(sorted);
+                     [&](size_t x, size_t y) { return pair_cost(x) > pair_cost(y); });
+    std::vector<int64_t> load(n_pf_ctas, 0);
+    std::vector<std::vector<PrefillTile>> per_cta(n_pf_ctas);
+    std::vector<size_t> leftover;
+    for (size_t pi : order) {
+      int32_t best = -1;
+      for (int32_t b = 0; b < n_pf_ctas; ++b)
+        if (load[b] + pair_cost(pi) <= target && (best < 0 || load[b] < load[best])) best = b;
+      if (best < 0) {
+        leftover.push_back(pi);
+        continue;
+      }
+      load[best] += pair_cost(pi);
+      PrefillTile t = pairs[pi];
+      t.kt0 = 0;
+      t.kt1 = pair_nt[pi][0];
+      t.part[0] = t.part[1] = -1;
+      per_cta[best].push_back(t);
+    }
+    // leftover sub-tiles, cut at the remaining capacities (CTA order)
+    struct Sub {
+      size_t pi;
+      int x;
+    };
+    std::vector<Sub> subs;
+    int64_t rest = 0;
+    for (size_t pi : leftover)
+      for (int x = 0; x < 2; ++x)
+        if (pair_nt[pi][x] > 0) {
+          subs.push_back({pi, x});
+          rest += kItemStartCost + kSingleTileCost * pair_nt[pi][x];
+        }
+    if (!subs.empty()) {
+      std::vector<int64_t> room(n_pf_ctas), room_end(n_pf_ctas);
+      int64_t room_total = 0;
+      for (int32_t b = 0; b < n_pf_ctas; ++b) {
+        room[b] = std::max<int64_t>(0, target - load[b]);
+        room_total += room[b];
+      }
+      // CTA b takes the part of the stream [room_end[b-1], room_end[b]) scaled
+      // to the stream's total
+      int64_t acc = 0;
+      for (int32_t b = 0; b < n_pf_ctas; ++b) {
+        acc += room[b];
+        room_end[b] = room_total > 0 ? acc * rest / room_total : (int64_t)(b + 1) * rest / n_pf_ctas;
+      }
+      int64_t cost = 0;
+      int32_t cta = 0;
+      for (const Sub &u : subs) {
+        const PrefillTile &src = pairs[u.pi];
+        const int32_t nt = pair_nt[u.pi][u.x];
+        cost += kItemStartCost;
+        std::vector<std::array<int32_t, 3>> pcs;  // (cta, j0, j1)
+        for (int32_t j = 0; j < nt; ++j) {
+          const int64_t mid = cost + kSingleTileCost / 2;
+          while (cta < n_pf_ctas - 1 && mid >= room_end[cta]) ++cta;
+          cost += kSingleTileCost;
+          if (pcs.empty() || pcs.back()[0] != cta)
+            pcs.push_back({cta, j, j + 1});
+          else
+            pcs.back()[2] = j + 1;
+        }
+        int32_t part0 = -1;
+        if (pcs.size() > 1) {
+          part0 = pparts;
+          MergeGroup m;
+          std::memset(&m, 0, sizeof m);
+          m.seq = src.seq;
+          m.qi0 = src.qi0[u.x];
+          m.n_q = src.n_q[u.x];
+          m.h = src.hq[u.x];
+          m.part0 = pparts;
+          m.nsplit = (int32_t)pcs.size();
+          m.kind = 1;
+          pmerges.push_back(m);
+          pparts += (int32_t)pcs.size();
+        }
+        for (size_t k = 0; k < pcs.size(); ++k) {
+          PrefillTile t;
+          std::memset(&t, 0, sizeof t);
+          t.seq = src.seq;
+          t.h = src.h;
+          t.hq[0] = src.hq[u.x];
+          t.qi0[0] = src.qi0[u.x];
+          t.n_q[0] = src.n_q[u.x];
+          t.kt0 = pcs[k][1];
+          t.kt1 = pcs[k][2];
+          t.part[0] = part0 >= 0 ? part0 + (int32_t)k : -1;
+          t.part[1] = -1;
+          per_cta[pcs[k][0]].push_back(t);
+        }
+      }
+    }
+    pf_begin.assign(n_pf_ctas + 1, 0);
+    for (int32_t b = 0; b < n_pf_ctas; ++b) {
+      pf_begin[b] = (int32_t)ptiles.size();
+      for (const PrefillTile &t : per_cta[b]) ptiles.push_back(t);
+    }
+    pf_begin[n_pf_ctas] = (int32_t)ptiles.size();
   }
+  for (const MergeGroup &m : pmerges) merges.push_back(m);  // after the decode groups
 
   // ---- sizes
   const PlanOffsets off = plan_offsets(num_warps, (int32_t)pieces.size(), (int32_t)merges.size(),
-                                       (int32_t)ptiles.size());
+                                       (int32_t)ptiles.size(), n_pf_ctas);
   std::memset(info, 0, sizeof *info);
   info->num_seqs = num_seqs;
   info->num_q_heads = num_q_heads;
@@ -246,13 +377,15 @@ extern "C" pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *con
   info->num_merge_groups = (int32_t)merges.size();
   info->num_partials = parts;
   info->num_prefill_tiles = (int32_t)ptiles.size();
+  info->num_prefill_ctas = n_pf_ctas;
+  info->num_prefill_partials = pparts;
+  info->num_prefill_merges = (int32_t)pmerges.size();
   info->num_kernels = (num_warps > 0 ? 1 : 0) + (merges.empty() ? 0 : 1) + (ptiles.empty() ? 0 : 1);
   info->max_blocks_needed = max_nb;
   info->kv_tokens = kv_tokens;
   info->decode_blocks = total_blocks;
   info->plan_bytes = off.total;
-  info->workspace_bytes =
-      parts > 0 ? ws_part_o_bytes(parts, desc->head_dim) + ws_part_ml_bytes(parts) : 0;
+  info->workspace_bytes = ws_total_bytes(parts, pparts, desc->head_dim);
 
   if (!plan) return PKV_OK;
   if (plan_capacity < info->plan_bytes) return PKV_ERR_WORKSPACE;
@@ -280,7 +413,9 @@ extern "C" pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *con
   if (!pieces.empty()) std::memcpy(p + off.pieces, pieces.data(), pieces.size() * sizeof(Piece));
   if (!merges.empty())
     std::memcpy(p + off.merges, merges.data(), merges.size() * sizeof(MergeGroup));
-  if (!ptiles.empty())
+  if (!ptiles.empty()) {
+    std::memcpy(p + off.prefill_begin, pf_begin.data(), pf_begin.size() * sizeof(int32_t));
     std::memcpy(p + off.prefill, ptiles.data(), ptiles.size() * sizeof(PrefillTile));
+  }
   return PKV_OK;
 }

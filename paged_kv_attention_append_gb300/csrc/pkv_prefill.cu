@@ -58,8 +58,9 @@ constexpr float kRescaleLog2 = 8.0f;
 constexpr int kMaxSlots = 8;
 
 enum {
-  B_Q_FULL = 0,
-  B_FULL = 1,                   // + slot: K or V tile landed
+  B_Q_FULL = 0,                  // both Q sub-tiles of an item landed
+  B_Q_EMPTY = 1,                 // every S MMA of an item completed (Q may be reloaded)
+  B_FULL = 2,                    // + slot: K or V tile landed
   B_EMPTY = B_FULL + kMaxSlots,  // + slot: every MMA reading it completed
   B_S_FULL = B_EMPTY + kMaxSlots,  // + sub-tile: S_x = Q_x K^T completed
   B_P_FULL = B_S_FULL + 2,       // + sub-tile: P_x written to TMEM (4 warps arrive)
@@ -94,7 +95,10 @@ struct PrefillParams {
   const int32_t *cu_q_lens;
   const int32_t *context_lens;
   const int32_t *block_tables;
+  const int32_t *bin_begin;  // work items of CTA b: tiles[bin_begin[b] .. bin_begin[b+1])
   const PrefillTile *tiles;
+  float *ppart_o;     // [part][128][D] fp32: unnormalised O of a sub-tile cut along keys
+  float2 *ppart_ml;   // [part][128]: (row max in log2 units, row sum) of the same
   int32_t *dev_status;
   int32_t num_seqs;
   int32_t max_blocks_per_seq;
@@ -115,6 +119,53 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *m, 
       : "memory");
 }
 
+// One work item's metadata, computed identically by every role (so every role
+// skips the same invalid items and agrees on all barrier phases).
+struct ItemMeta {
+  PrefillTile t;
+  int cu0, qs, ctx;
+  int nt[2];  // key tiles sub-tile x runs in this item, from t.kt0 (0 when absent)
+  int nkt;    // key tiles loaded: t.kt0 .. t.kt1-1
+  bool ok;
+};
+
+__device__ __forceinline__ ItemMeta load_item(const PrefillParams &p, int it) {
+  ItemMeta m;
+  m.t = p.tiles[it];
+  const PrefillTile &t = m.t;
+  bool ok = t.seq >= 0 && t.seq < p.num_seqs && t.h >= 0 && t.h < p.num_kv_heads &&
+            t.n_q[0] >= 1 && t.n_q[0] <= kPrefillRows && t.n_q[1] >= 0 &&
+            t.n_q[1] <= kPrefillRows;
+#pragma unroll
+  for (int x = 0; x < 2; ++x)
+    if (t.n_q[x] > 0)
+      ok = ok && t.hq[x] / p.group == t.h && t.hq[x] >= 0 && t.hq[x] < p.num_q_heads &&
+           t.qi0[x] >= 0;
+  ok = ok && t.kt0 >= 0 && t.kt0 < t.kt1;
+  m.cu0 = m.qs = m.ctx = 0;
+  if (ok) {
+    m.cu0 = __ldg(p.cu_q_lens + t.seq);
+    m.qs = __ldg(p.cu_q_lens + t.seq + 1) - m.cu0;
+    m.ctx = __ldg(p.context_lens + t.seq);
+    ok = m.qs <= m.ctx;
+#pragma unroll
+    for (int x = 0; x < 2; ++x)
+      if (t.n_q[x] > 0) ok = ok && t.qi0[x] + t.n_q[x] <= m.qs;
+  }
+  int seen[2];  // key tiles sub-tile x sees in all
+#pragma unroll
+  for (int x = 0; x < 2; ++x)
+    seen[x] = ok && t.n_q[x] > 0 ? (m.ctx - m.qs + t.qi0[x] + t.n_q[x] - 1) / kKeysPerTile + 1 : 0;
+  // the item's key range lies inside what sub-tile 0 sees; a present sub-tile
+  // runs at least one of its tiles
+  ok = ok && t.kt1 <= seen[0] && (t.n_q[1] == 0 || t.kt0 < seen[1]);
+#pragma unroll
+  for (int x = 0; x < 2; ++x) m.nt[x] = ok && t.n_q[x] > 0 ? min(t.kt1, seen[x]) - t.kt0 : 0;
+  m.nkt = ok ? t.kt1 - t.kt0 : 0;
+  m.ok = ok;
+  return m;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap q_map,
@@ -128,37 +179,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // wait for the predecessor's writes (pool, q, metadata) before reading anything
   pdl_trigger();
   pdl_wait();
-  const PrefillTile tile = p.tiles[blockIdx.x];
-
-  // ---- work item metadata from the device copies of the step arrays (CTA-uniform)
-  bool ok = tile.seq >= 0 && tile.seq < p.num_seqs && tile.h >= 0 && tile.h < p.num_kv_heads &&
-            tile.n_q[0] >= 1 && tile.n_q[0] <= kPrefillRows && tile.n_q[1] >= 0 &&
-            tile.n_q[1] <= kPrefillRows;
-  for (int x = 0; x < 2; ++x)
-    if (tile.n_q[x] > 0)
-      ok = ok && tile.hq[x] / p.group == tile.h && tile.hq[x] >= 0 &&
-           tile.hq[x] < p.num_q_heads && tile.qi0[x] >= 0;
-  int cu0 = 0, qs = 0, ctx = 0;
-  if (ok) {
-    cu0 = __ldg(p.cu_q_lens + tile.seq);
-    qs = __ldg(p.cu_q_lens + tile.seq + 1) - cu0;
-    ctx = __ldg(p.context_lens + tile.seq);
-    ok = qs <= ctx;
-    for (int x = 0; x < 2; ++x)
-      if (tile.n_q[x] > 0) ok = ok && tile.qi0[x] + tile.n_q[x] <= qs;
-  }
-  if (!ok) {
-    if (threadIdx.x == 0) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
-    return;
-  }
-  const int h = tile.h;
-  int q_pos0[2], nt[2];  // causal position of row 0; key tiles seen
-  for (int x = 0; x < 2; ++x) {
-    q_pos0[x] = ctx - qs + tile.qi0[x];
-    nt[x] = tile.n_q[x] > 0 ? (q_pos0[x] + tile.n_q[x] - 1) / kKeysPerTile + 1 : 0;
-  }
-  const int nkt = max(nt[0], nt[1]);
-  const int nblk_ctx = (ctx + kBlockSize - 1) / kBlockSize;
+  // this CTA's bin of work items, run one after another; every barrier keeps
+  // counting phases across items
+  const int it0 = __ldg(p.bin_begin + blockIdx.x), it1 = __ldg(p.bin_begin + blockIdx.x + 1);
+  if (threadIdx.x == 0)
+    for (int it = it0; it < it1; ++it)
+      if (!load_item(p, it).ok) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
 
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + B_COUNT);
@@ -167,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_Q_FULL), 1);
+    mbar_init(bar(B_Q_EMPTY), 1);
     for (int s = 0; s < C::kSlots; ++s) {
       mbar_init(bar(B_FULL + s), 1);
       mbar_init(bar(B_EMPTY + s), 1);
@@ -202,73 +229,100 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       prefetch_tmap(&q_map);
       prefetch_tmap(&kv_map);
-      const int nsub = tile.n_q[1] > 0 ? 2 : 1;
-      mbar_arrive_expect_tx(bar(B_Q_FULL), nsub * C::kQBytes);
-#pragma unroll
-      for (int x = 0; x < 2; ++x) {
-        if (x >= nsub) break;
-        const uint32_t sq = smem_u32(smem + C::kOffQ + x * C::kQBytes);
-#pragma unroll
-        for (int hh = 0; hh < C::kHalves; ++hh)
-          tma_load_3d(sq + hh * C::kQHalfBytes, &q_map, hh * 64, tile.hq[x], cu0 + tile.qi0[x],
-                      bar(B_Q_FULL));
-      }
     }
-    // Load L of the ring is K_{L/2} (L even) or V_{L/2} (L odd), in slot
-    // L % kSlots.  Lane b < 8 owns paged block b of every tile: it reads that
-    // block's table entry once per tile (a coalesced 32-byte load, issued before
-    // the wait for a free slot) and issues the block's K and V boxes itself.
-    const int32_t *table = p.block_tables + (int64_t)tile.seq * p.max_blocks_per_seq;
+    // Ring load L (counted over the CTA's items) is K_j (even) or V_j (odd) of
+    // the current item, in slot L % kSlots.  Lane b < 8 owns paged block b of
+    // every tile: it reads that block's table entry once per tile (a coalesced
+    // 32-byte load, issued before the wait for a free slot) and issues the
+    // block's K and V boxes itself.  The Q tiles of an item wait until every
+    // S MMA of the previous item has read its Q (B_Q_EMPTY).
     const int hkv = p.num_kv_heads;
-    int issued = 0;
-    int g_k = p.pool_groups;  // this lane's K group coordinate for the current tile
-    for (int L = 0; L < 2 * nkt; ++L) {
+    int L = 0, nq = 0;  // ring loads and Q loads issued
+    bool good = true;
+    for (int it = it0; it < it1 && good; ++it) {
+      const ItemMeta m = load_item(p, it);
+      if (!m.ok) continue;
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-      const int j = L >> 1;
-      if ((L & 1) == 0) {
-        const int kb = j * kBlocksPerTile + lane;
-        g_k = p.pool_groups;  // out of range: zero fill, no memory traffic
-        if (lane < kBlocksPerTile && kb < nblk_ctx && kb < p.max_blocks_per_seq) {
-          const int phys = __ldg(table + kb);
-          if (phys >= 0 && phys < p.num_blocks)
-            g_k = ((phys * 2 + 0) * hkv + h) * (kBlockSize / 8);
-          else
-            report(p.dev_status, PKV_DEV_BAD_BLOCK);
-        }
-      }
-      const int s = L % C::kSlots;
-      if (L >= C::kSlots &&
-          !__all_sync(0xffffffffu,
-                      mbar_wait(bar(B_EMPTY + s), (uint32_t)(((L / C::kSlots) - 1) & 1)))) {
+      if (nq > 0 &&
+          !__all_sync(0xffffffffu, mbar_wait(bar(B_Q_EMPTY), (uint32_t)((nq - 1) & 1)))) {
         if (lane == 0) fail();
         break;
       }
-      if (lane == 0) mbar_arrive_expect_tx(bar(B_FULL + s), C::kSlotBytes);
-      __syncwarp();
-      if (lane < kBlocksPerTile) {
-        const int g = (L & 1) == 0 || g_k == p.pool_groups ? g_k : g_k + hkv * (kBlockSize / 8);
-        tma_load_4d(smem_u32(smem + C::kOffRing + s * C::kSlotBytes) + lane * C::kBlockBytes,
-                    &kv_map, 0, 0, 0, g, bar(B_FULL + s));
+      if (lane == 0) {
+        const int nsub = m.t.n_q[1] > 0 ? 2 : 1;
+        mbar_arrive_expect_tx(bar(B_Q_FULL), nsub * C::kQBytes);
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          if (x >= nsub) break;
+          const uint32_t sq = smem_u32(smem + C::kOffQ + x * C::kQBytes);
+#pragma unroll
+          for (int hh = 0; hh < C::kHalves; ++hh)
+            tma_load_3d(sq + hh * C::kQHalfBytes, &q_map, hh * 64, m.t.hq[x],
+                        m.cu0 + m.t.qi0[x], bar(B_Q_FULL));
+        }
       }
-      ++issued;
+      __syncwarp();
+      ++nq;
+      const int32_t *table = p.block_tables + (int64_t)m.t.seq * p.max_blocks_per_seq;
+      const int nblk_ctx = (m.ctx + kBlockSize - 1) / kBlockSize;
+      int g_k = p.pool_groups;  // this lane's K group coordinate for the current tile
+      for (int jl = 0; jl < 2 * m.nkt; ++jl) {
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) {
+          good = false;
+          break;
+        }
+        const int j = m.t.kt0 + (jl >> 1);  // absolute key tile
+        if ((jl & 1) == 0) {
+          const int kb = j * kBlocksPerTile + lane;
+          g_k = p.pool_groups;  // out of range: zero fill, no memory traffic
+          if (lane < kBlocksPerTile && kb < nblk_ctx && kb < p.max_blocks_per_seq) {
+            const int phys = __ldg(table + kb);
+            if (phys >= 0 && phys < p.num_blocks)
+              g_k = ((phys * 2 + 0) * hkv + m.t.h) * (kBlockSize / 8);
+            else
+              report(p.dev_status, PKV_DEV_BAD_BLOCK);
+          }
+        }
+        const int s = L % C::kSlots;
+        if (L >= C::kSlots &&
+            !__all_sync(0xffffffffu,
+                        mbar_wait(bar(B_EMPTY + s), (uint32_t)(((L / C::kSlots) - 1) & 1)))) {
+          if (lane == 0) fail();
+          good = false;
+          break;
+        }
+        if (lane == 0) mbar_arrive_expect_tx(bar(B_FULL + s), C::kSlotBytes);
+        __syncwarp();
+        if (lane < kBlocksPerTile) {
+          const int g =
+              (jl & 1) == 0 || g_k == p.pool_groups ? g_k : g_k + hkv * (kBlockSize / 8);
+          tma_load_4d(smem_u32(smem + C::kOffRing + s * C::kSlotBytes) + lane * C::kBlockBytes,
+                      &kv_map, 0, 0, 0, g, bar(B_FULL + s));
+        }
+        ++L;
+      }
     }
     // our copies still in flight land before the CTA can exit: only the last
     // load of each slot can be pending (a slot is refilled after it was consumed)
     if (lane == 0) {
-      for (int L = max(0, issued - C::kSlots); L < issued; ++L)
-        mbar_wait(bar(B_FULL + L % C::kSlots), (uint32_t)((L / C::kSlots) & 1));
-      mbar_wait(bar(B_Q_FULL), 0);
+      for (int l = max(0, L - C::kSlots); l < L; ++l)
+        mbar_wait(bar(B_FULL + l % C::kSlots), (uint32_t)((l / C::kSlots) & 1));
+      if (nq > 0) mbar_wait(bar(B_Q_FULL), (uint32_t)((nq - 1) & 1));
     }
   } else if (warp == kMmaWarp) {
     // ======================================================== MMA issuer
-    // A fixed ping-pong order: S_0(0) S_1(0), then per key tile j
+    // Per item a fixed ping-pong order: S_0(0) S_1(0), then per key tile j
     //   O_0 += P_0(j) V_j, S_0(j+1), O_1 += P_1(j) V_j, S_1(j+1),
     // so each sub-tile's softmax of tile j runs while the tensor pipe works on
     // the other sub-tile's two MMA groups.  (An MMA group of 8 instructions
     // blocks the issuing thread for about its execution time, so the order of
-    // issue is the order of execution.)  A ring slot is released by a commit
-    // once every MMA reading it has been issued.  Waits are bounded
-    // (PKV_DEV_TIMEOUT) and stop at an abort.
+    // issue is the order of execution.)  S_x of any tile waits for the previous
+    // O_x += P_x V (it writes over P_x), also across items; the first O_x += P_x V
+    // of an item needs nothing more, since the softmax warps finish reading O_x
+    // of the previous item before they write the new P_x.  A ring slot is
+    // released by a commit once every MMA reading it has been issued; B_Q_EMPTY
+    // once every S MMA of the item has.  Waits are bounded (PKV_DEV_TIMEOUT)
+    // and stop at an abort.
     if (lane == 0) {
       constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kPrefillRows, kKeysPerTile, 0, 0);
       constexpr uint32_t kIdescO = tc::idesc_bf16_f32(kPrefillRows, D, 0, 1);
@@ -278,12 +332,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         fail();
         return false;
       };
-      // S_x(j) = Q_x K_j^T once K_j landed and P_x(j-1) was consumed (the MMA
-      // writes over it)
+      int L0 = 0, nq = 0;       // ring index of the item's K_0; items (Q loads) done
+      int tx0 = 0, tx1 = 0;     // key tiles sub-tile 0 / 1 ran in earlier items
+      int n_s = 0, n_s_item = 0;  // S MMAs issued in this item / due in it
+      // S_x(j) = Q_x K_j^T once K_j landed and the previous P_x was consumed
       auto issue_s = [&](int x, int j) -> bool {
-        const int L = 2 * j, s = L % C::kSlots;
+        const int L = L0 + 2 * j, s = L % C::kSlots;
+        const int run = (x ? tx1 : tx0) + j;  // running tile index of sub-tile x
         if (!wait(B_FULL + s, L / C::kSlots)) return false;
-        if (j > 0 && !wait(B_O_DONE + x, j - 1)) return false;
+        if (run > 0 && !wait(B_O_DONE + x, run - 1)) return false;
         tc::fence_after_sync();
         const uint32_t sq = smem_u32(smem + C::kOffQ + x * C::kQBytes);
         const uint32_t sk = smem_u32(smem + C::kOffRing + s * C::kSlotBytes);
@@ -296,12 +353,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mma_bf16(t_s(x), a, b, kIdescS, ks > 0 ? 1u : 0u);
         }
         tc::commit(bar(B_S_FULL + x));
+        if (++n_s == n_s_item) tc::commit(bar(B_Q_EMPTY));  // every S of the item issued
         return true;
       };
       // O_x += P_x(j) V_j once P_x(j) is in TMEM and V_j landed
       auto issue_pv = [&](int x, int j) -> bool {
-        const int L = 2 * j + 1, s = L % C::kSlots;
-        if (!wait(B_P_FULL + x, j)) return false;
+        const int L = L0 + 2 * j + 1, s = L % C::kSlots;
+        if (!wait(B_P_FULL + x, (x ? tx1 : tx0) + j)) return false;
         if (!wait(B_FULL + s, L / C::kSlots)) return false;
         tc::fence_after_sync();
         const uint32_t sv = smem_u32(smem + C::kOffRing + s * C::kSlotBytes);
@@ -313,19 +371,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::commit(bar(B_O_DONE + x));
         return true;
       };
-      bool good = wait(B_Q_FULL, 0);
-      for (int x = 0; x < 2 && good; ++x)
-        if (nt[x] > 0) good = issue_s(x, 0);
-      if (good) tc::commit(bar(B_EMPTY + 0));  // K_0 read by every S(0)
-      for (int j = 0; good && j < nkt; ++j) {
-        for (int x = 0; x < 2 && good; ++x) {
-          if (j >= nt[x]) continue;
-          good = issue_pv(x, j);
-          if (good && j + 1 < nt[x]) good = issue_s(x, j + 1);
+      bool good = true;
+      for (int it = it0; it < it1 && good; ++it) {
+        const ItemMeta m = load_item(p, it);
+        if (!m.ok) continue;
+        const int nt0 = m.nt[0], nt1 = m.nt[1];
+        good = wait(B_Q_FULL, nq);
+        n_s = 0;
+        n_s_item = nt0 + nt1;
+        for (int x = 0; x < 2 && good; ++x)
+          if ((x ? nt1 : nt0) > 0) good = issue_s(x, 0);
+        if (good) tc::commit(bar(B_EMPTY + L0 % C::kSlots));  // K_0 read by every S(0)
+        for (int j = 0; good && j < m.nkt; ++j) {
+          for (int x = 0; x < 2 && good; ++x) {
+            const int ntx = x ? nt1 : nt0;
+            if (j >= ntx) continue;
+            good = issue_pv(x, j);
+            if (good && j + 1 < ntx) good = issue_s(x, j + 1);
+          }
+          if (!good) break;
+          tc::commit(bar(B_EMPTY + (L0 + 2 * j + 1) % C::kSlots));  // V_j
+          if (j + 1 < m.nkt) tc::commit(bar(B_EMPTY + (L0 + 2 * j + 2) % C::kSlots));  // K_{j+1}
         }
-        if (!good) break;
-        tc::commit(bar(B_EMPTY + (2 * j + 1) % C::kSlots));  // V_j
-        if (j + 1 < nkt) tc::commit(bar(B_EMPTY + (2 * j + 2) % C::kSlots));  // K_{j+1}
+        L0 += 2 * m.nkt;
+        tx0 += nt0;
+        tx1 += nt1;
+        ++nq;
       }
       // every MMA issued so far completes before TMEM is released
       tc::commit(bar(B_DRAIN));
@@ -337,140 +408,177 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3;         // TMEM lane quarter
     const int row = quarter * 32 + lane;  // query row = TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    // per-sub-tile fields by selects (no dynamically indexed local arrays)
-    const int n_q = x ? tile.n_q[1] : tile.n_q[0];
-    const int ntx = x ? nt[1] : nt[0];
-    const int qi0 = x ? tile.qi0[1] : tile.qi0[0];
-    const int hq = x ? tile.hq[1] : tile.hq[0];
-    const int lim = row < n_q ? ctx - qs + qi0 + row : -1;  // last visible key of this row
     const float sl2 = p.scale_log2;
     const uint32_t ts = t_s(x) + lane_off, to = t_o(x) + lane_off;
-    float m_used = -INFINITY, l = 0.f;
+    int run0 = 0;  // key tiles this sub-tile ran in earlier items
     bool good = true;
-    for (int j = 0; j < ntx; ++j) {
-      if (__any_sync(0xffffffffu, *abort_flag != 0)) {
-        good = false;
-        break;
+    for (int it = it0; it < it1 && good; ++it) {
+      const ItemMeta m = load_item(p, it);
+      // per-sub-tile fields by selects (no dynamically indexed local arrays)
+      const int n_q = x ? m.t.n_q[1] : m.t.n_q[0];
+      const int ntx = x ? m.nt[1] : m.nt[0];
+      if (!m.ok || ntx == 0) continue;
+      // last visible key of this row
+      const int lim = row < n_q ? m.ctx - m.qs + (x ? m.t.qi0[1] : m.t.qi0[0]) + row : -1;
+      float m_used = -INFINITY, l = 0.f;
+      for (int j = 0; j < ntx; ++j) {
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) {
+          good = false;
+          break;
+        }
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(bar(B_S_FULL + x), (uint32_t)((run0 + j) & 1)))) {
+          fail();
+          good = false;
+          break;
+        }
+        tc::fence_after_sync();
+        const int rel = lim - (m.t.kt0 + j) * kKeysPerTile;  // keys k <= rel are visible
+        uint32_t sv[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tc::ld32(ts + 32 * c, sv[c]);
+        tc::wait_ld();
+        // scores in the log2 domain are sv * mult: a positive scale is applied in
+        // the exponent's FMA; a zero or negative one is applied here first
+        const float mult = sl2 > 0.f ? sl2 : 1.f;
+        if (!(sl2 > 0.f)) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) sv[c][i] = __float_as_uint(__uint_as_float(sv[c][i]) * sl2);
+        }
+        if (rel < kKeysPerTile - 1) {  // diagonal tile: invisible keys become -inf
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) sv[c][i] = 32 * c + i <= rel ? sv[c][i] : 0xff800000u;
+        }
+        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < 4; ++c)  // two per instruction, four chains
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            m4[i & 3] = max3(m4[i & 3], __uint_as_float(sv[c][2 * i]),
+                             __uint_as_float(sv[c][2 * i + 1]));
+        const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * mult;
+        // lazy rescale of O_x (TMEM) and l when the max grew by more than 2^8 (O_x
+        // itself is rescaled below, once the scores are no longer live)
+        const bool need = m_used != -INFINITY && mt > m_used + kRescaleLog2;
+        const bool any_need = __any_sync(0xffffffffu, need);
+        const float alpha = need ? fast_exp2(m_used - mt) : 1.f;
+        if (need) {
+          l *= alpha;
+          m_used = mt;
+        }
+        if (m_used == -INFINITY) m_used = mt;  // first keys this row sees
+        const float nbase = m_used == -INFINITY ? 0.f : -m_used;
+        // p = 2^(sv * mult - m): 0 for masked keys (-inf); packed two per column
+        // over S_x columns 0-63
+        const uint64_t mx2 = f2_pack(mult, mult), nbx2 = f2_pack(nbase, nbase);
+        uint64_t acc[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int k0 = 32 * c + 2 * i;  // key index of the low element
+            float p0, p1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[k0 >> 5][k0 & 31]),
+                                     __uint_as_float(sv[k0 >> 5][(k0 & 31) + 1])),
+                             mx2, nbx2),
+                      p0, p1);
+            p0 = fast_exp2(p0);
+            p1 = fast_exp2(p1);
+            acc[i & 1] = f2_add(acc[i & 1], f2_pack(p0, p1));
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          tc::st16(ts + 16 * c, pk);
+        }
+        {
+          float a0, a1, b0, b1;
+          f2_unpack(acc[0], a0, a1);
+          f2_unpack(acc[1], b0, b1);
+          l += (a0 + a1) + (b0 + b1);
+        }
+        // O_x is idle here: its last update (P_x(j-1) V) completed before S_x(j)
+        // was issued, and the next one waits for this tile's P
+        if (any_need) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t ov[32];
+            tc::ld32(to + 32 * c, ov);
+            tc::wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tc::st32(to + 32 * c, ov);
+          }
+        }
+        tc::wait_st();
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_P_FULL + x));
       }
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_S_FULL + x), (uint32_t)(j & 1)))) {
+      if (!good) break;
+      // ---- epilogue: O / l.  The next item's first O_x += P_x V waits for this
+      // warp's next P_x, which comes after these TMEM reads.
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(bar(B_O_DONE + x), (uint32_t)((run0 + ntx - 1) & 1)))) {
         fail();
-        good = false;
         break;
       }
       tc::fence_after_sync();
-      const int rel = lim - j * kKeysPerTile;  // keys k <= rel are visible
-      uint32_t sv[4][32];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tc::ld32(ts + 32 * c, sv[c]);
-      tc::wait_ld();
-      // scores in the log2 domain are sv * mult: a positive scale is applied in
-      // the exponent's FMA; a zero or negative one is applied here first
-      const float mult = sl2 > 0.f ? sl2 : 1.f;
-      if (!(sl2 > 0.f)) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int i = 0; i < 32; ++i) sv[c][i] = __float_as_uint(__uint_as_float(sv[c][i]) * sl2);
-      }
-      if (rel < kKeysPerTile - 1) {  // diagonal tile: invisible keys become -inf
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-#pragma unroll
-          for (int i = 0; i < 32; ++i) sv[c][i] = 32 * c + i <= rel ? sv[c][i] : 0xff800000u;
-      }
-      float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-      for (int c = 0; c < 4; ++c)  // two per instruction, four chains
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          m4[i & 3] = max3(m4[i & 3], __uint_as_float(sv[c][2 * i]),
-                           __uint_as_float(sv[c][2 * i + 1]));
-      const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * mult;
-      // lazy rescale of O_x (TMEM) and l when the max grew by more than 2^8 (O_x
-      // itself is rescaled below, once the scores are no longer live)
-      const bool need = m_used != -INFINITY && mt > m_used + kRescaleLog2;
-      const bool any_need = __any_sync(0xffffffffu, need);
-      const float alpha = need ? fast_exp2(m_used - mt) : 1.f;
-      if (need) {
-        l *= alpha;
-        m_used = mt;
-      }
-      if (m_used == -INFINITY) m_used = mt;  // first keys this row sees
-      const float nbase = m_used == -INFINITY ? 0.f : -m_used;
-      // p = 2^(sv * mult - m): 0 for masked keys (-inf); packed two per column
-      // over S_x columns 0-63
-      const uint64_t mx2 = f2_pack(mult, mult), nbx2 = f2_pack(nbase, nbase);
-      uint64_t acc[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int k0 = 32 * c + 2 * i;  // key index of the low element
-          float p0, p1;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[k0 >> 5][k0 & 31]),
-                                   __uint_as_float(sv[k0 >> 5][(k0 & 31) + 1])),
-                           mx2, nbx2),
-                    p0, p1);
-          p0 = fast_exp2(p0);
-          p1 = fast_exp2(p1);
-          acc[i & 1] = f2_add(acc[i & 1], f2_pack(p0, p1));
-          pk[i] = pack_bf16x2(p0, p1);
-        }
-        tc::st16(ts + 16 * c, pk);
-      }
+      int out_row, hq, part;  // re-read rather than kept live through the tile loop
       {
-        float a0, a1, b0, b1;
-        f2_unpack(acc[0], a0, a1);
-        f2_unpack(acc[1], b0, b1);
-        l += (a0 + a1) + (b0 + b1);
+        const ItemMeta me = load_item(p, it);
+        out_row = me.cu0 + (x ? me.t.qi0[1] : me.t.qi0[0]) + row;
+        hq = x ? me.t.hq[1] : me.t.hq[0];
+        part = x ? me.t.part[1] : me.t.part[0];
       }
-      // O_x is idle here: its last update (P_x(j-1) V) completed before S_x(j)
-      // was issued, and the next one waits for this tile's P
-      if (any_need) {
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t ov[32];
-          tc::ld32(to + 32 * c, ov);
-          tc::wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-          tc::st32(to + 32 * c, ov);
-        }
-      }
-      tc::wait_st();
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_P_FULL + x));
-    }
-    // ---- epilogue: O / l
-    if (ntx > 0 && good && !__any_sync(0xffffffffu, *abort_flag != 0)) {
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(B_O_DONE + x), (uint32_t)((ntx - 1) & 1)))) {
-        fail();
-      } else {
-        tc::fence_after_sync();
-        const float inv = l > 0.f ? 1.f / l : 0.f;
-        __nv_bfloat16 *orow =
-            p.out + ((int64_t)(cu0 + qi0 + row) * p.num_q_heads + hq) * D;
+      if (part >= 0) {
+        // keys of this sub-tile are split over several items: unnormalised O
+        // and (m, l) to its partial slot, combined by the merge kernel
+        float *prow = p.ppart_o + ((int64_t)part * kPrefillRows + row) * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t ov[32];
           tc::ld32(to + 32 * c, ov);
           tc::wait_ld();
           if (row < n_q) {
-            uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
+            float4 *dst = reinterpret_cast<float4 *>(prow + 32 * c);
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
-              uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(ov[8 * v4 + 0]) * inv, __uint_as_float(ov[8 * v4 + 1]) * inv);
-              w.y = pack_bf16x2(__uint_as_float(ov[8 * v4 + 2]) * inv, __uint_as_float(ov[8 * v4 + 3]) * inv);
-              w.z = pack_bf16x2(__uint_as_float(ov[8 * v4 + 4]) * inv, __uint_as_float(ov[8 * v4 + 5]) * inv);
-              w.w = pack_bf16x2(__uint_as_float(ov[8 * v4 + 6]) * inv, __uint_as_float(ov[8 * v4 + 7]) * inv);
-              dst[v4] = w;
-            }
+            for (int v4 = 0; v4 < 8; ++v4)
+              dst[v4] = make_float4(__uint_as_float(ov[4 * v4]), __uint_as_float(ov[4 * v4 + 1]),
+                                    __uint_as_float(ov[4 * v4 + 2]), __uint_as_float(ov[4 * v4 + 3]));
+          }
+        }
+        if (row < n_q) p.ppart_ml[(int64_t)part * kPrefillRows + row] = make_float2(m_used, l);
+        tc::fence_before_sync();
+        run0 += ntx;
+        continue;
+      }
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16 *orow = p.out + ((int64_t)out_row * p.num_q_heads + hq) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t ov[32];
+        tc::ld32(to + 32 * c, ov);
+        tc::wait_ld();
+        if (row < n_q) {
+          uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
+#pragma unroll
+          for (int v4 = 0; v4 < 4; ++v4) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(ov[8 * v4 + 0]) * inv, __uint_as_float(ov[8 * v4 + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(ov[8 * v4 + 2]) * inv, __uint_as_float(ov[8 * v4 + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(ov[8 * v4 + 4]) * inv, __uint_as_float(ov[8 * v4 + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(ov[8 * v4 + 6]) * inv, __uint_as_float(ov[8 * v4 + 7]) * inv);
+            dst[v4] = w;
           }
         }
       }
+      tc::fence_before_sync();
+      run0 += ntx;
     }
   }
 
@@ -544,7 +652,10 @@ int launch_prefill_t(const AttnArgs &a, const CUtensorMap &qmap, const CUtensorM
   p.cu_q_lens = a.cu_q_lens;
   p.context_lens = a.context_lens;
   p.block_tables = a.block_tables;
+  p.bin_begin = a.prefill_begin;
   p.tiles = a.prefill_tiles;
+  p.ppart_o = a.ppart_o;
+  p.ppart_ml = reinterpret_cast<float2 *>(a.ppart_ml);
   p.dev_status = a.dev_status;
   p.num_seqs = a.num_seqs;
   p.max_blocks_per_seq = a.max_blocks_per_seq;
@@ -555,7 +666,7 @@ int launch_prefill_t(const AttnArgs &a, const CUtensorMap &qmap, const CUtensorM
   p.pool_groups = a.desc.num_blocks * 2 * a.desc.num_kv_heads * (kBlockSize / 8);
   p.scale_log2 = a.scale * 1.4426950408889634f;
   profile_begin(PKV_KERNEL_PREFILL, a.stream);
-  e = launch_kernel(kern, dim3((unsigned)a.num_prefill_tiles), dim3(kThreads), C::kSmemBytes,
+  e = launch_kernel(kern, dim3((unsigned)a.num_prefill_ctas), dim3(kThreads), C::kSmemBytes,
                     a.stream, !profiling_active(), qmap, kvmap, p);
   profile_end(PKV_KERNEL_PREFILL, a.stream);
   return e != cudaSuccess ? (int)e : (int)cudaGetLastError();
@@ -564,7 +675,7 @@ int launch_prefill_t(const AttnArgs &a, const CUtensorMap &qmap, const CUtensorM
 }  // namespace
 
 int launch_prefill(const AttnArgs &a, int *launches) {
-  if (a.num_prefill_tiles <= 0) return 0;
+  if (a.num_prefill_tiles <= 0 || a.num_prefill_ctas <= 0) return 0;
   CUtensorMap qmap, kvmap;
   int e = make_q_map(&qmap, a.q, a.total_q, a.num_q_heads, a.desc.head_dim);
   if (e) return e;

@@ -49,41 +49,56 @@ def parse_plan(info, host):
     off_first = off_w + ((nw + 1 + 7) // 8) * 8
     off_p = off_first + 8 * nw
     off_m = off_p + 8 * npc
-    off_f = off_m + 8 * nm
-    assert info.plan_bytes == 4 * (off_f + 8 * npf)
+    ncta = info.num_prefill_ctas
+    off_b = off_m + 8 * nm
+    off_f = off_b + (((ncta + 1 + 7) // 8) * 8 if ncta else 0)
+    assert info.plan_bytes == 4 * (off_f + 12 * npf)
     wb = words[off_w:off_w + nw + 1]
     pieces = words[off_p:off_m].reshape(npc, 8)
     first = words[off_first:off_p].reshape(nw, 8)
     if nw:
         assert np.array_equal(first, pieces[wb[:-1]])  # each warp's first piece, copied
-    mer = words[off_m:off_f].reshape(nm, 8)
-    pre = words[off_f:off_f + 8 * npf].reshape(npf, 8)
+    mer = words[off_m:off_b].reshape(nm, 8)
+    pre = words[off_f:off_f + 12 * npf].reshape(npf, 12)
+    pb = words[off_b:off_b + ncta + 1] if ncta else np.zeros(1, np.int32)
+    if ncta:
+        assert pb[0] == 0 and pb[-1] == npf and np.all(np.diff(pb) >= 0)
     return hdr, wb, pieces, mer, pre
 
 
-def check_prefill_items(meta, pre, s):
-    """Work items of prefill-class sequence s: (seq, h, hq0, hq1, qi0_0, qi0_1, n0, n1).
-    Every (query head, 128-token tile) unit is covered exactly once; both sub-tiles
-    of an item read KV head h; sub-tile 0 sees at least as many keys as sub-tile 1."""
+def check_prefill_items(meta, pre, mer, s):
+    """Work items of prefill-class sequence s:
+    (seq, h, hq0, hq1, qi0_0, qi0_1, n0, n1, kt0, kt1, part0, part1).
+    Every (query head, 128-token tile) unit sees each of its key tiles in exactly
+    one item; both sub-tiles of an item read KV head h; a unit whose key tiles
+    span several items has one partial slot per item and one merge group (kind
+    1) naming exactly those slots; a unit in one item writes out directly."""
     g = meta.num_q_heads // meta.num_kv_heads
     qs, ctx = int(meta.q_lens[s]), int(meta.context_lens[s])
     items = pre[pre[:, 0] == s]
-    units = []
+    seen = {}    # (hq, q0) -> list of (kt0, kt1, part)
     for it in items:
-        _, h, hq0, hq1, qa, qb, na, nb = (int(v) for v in it)
-        assert 1 <= na <= 128 and 0 <= nb <= 128
-        subs = [(hq0, qa, na)] + ([(hq1, qb, nb)] if nb else [])
-        for hq, q0, n in subs:
+        _, h, hq0, hq1, qa, qb, na, nb, kt0, kt1, pa, pb = (int(v) for v in it)
+        assert 1 <= na <= 128 and 0 <= nb <= 128 and 0 <= kt0 < kt1
+        for hq, q0, n, part in [(hq0, qa, na, pa)] + ([(hq1, qb, nb, pb)] if nb else []):
             assert hq // g == h and q0 % 128 == 0 and n == min(128, qs - q0)
-            units.append((hq, q0))
-        if nb:
-            assert ctx - qs + qa + na >= ctx - qs + qb + nb
+            nt = (ctx - qs + q0 + n - 1) // 128 + 1
+            assert kt0 < nt
+            seen.setdefault((hq, q0), []).append((kt0, min(kt1, nt), part, nt))
     expect = [(hq, q0) for hq in range(meta.num_q_heads) for q0 in range(0, qs, 128)]
-    assert sorted(units) == sorted(expect)
-    # pairing: at most one single sub-tile item per KV head
-    for h in range(meta.num_kv_heads):
-        mine = items[items[:, 1] == h]
-        assert int((mine[:, 7] == 0).sum()) <= 1
+    assert sorted(seen) == sorted(expect)
+    pm = mer[(mer[:, 0] == s) & (mer[:, 6] == 1)]
+    for (hq, q0), rs in seen.items():
+        rs.sort()
+        nt = rs[0][3]
+        assert rs[0][0] == 0 and rs[-1][1] == nt
+        assert all(rs[i][1] == rs[i + 1][0] for i in range(len(rs) - 1))   # no gap, no overlap
+        m = pm[(pm[:, 3] == hq) & (pm[:, 1] == q0)]
+        if len(rs) == 1:
+            assert rs[0][2] == -1 and len(m) == 0
+        else:
+            parts = sorted(r[2] for r in rs)
+            assert len(m) == 1 and m[0, 5] == len(rs) and parts == list(range(m[0, 4], m[0, 4] + len(rs)))
     return len(items)
 
 
@@ -121,10 +136,7 @@ def check_plan(meta, info, host, num_sms):
             continue
         if s in prefill_seqs:
             assert len(mine) == 0
-            units = meta.num_q_heads * (-(-qs // 128))
-            n_items = check_prefill_items(meta, pre, s)
-            assert n_items == sum(-(-(g * (-(-qs // 128))) // 2) for _ in range(hkv))
-            assert 2 * n_items >= units
+            check_prefill_items(meta, pre, mer, s)
             continue
         for qi0 in range(0, qs, nq_tile):
             n_q = min(nq_tile, qs - qi0)
@@ -143,16 +155,19 @@ def check_plan(meta, info, host, num_sms):
                     assert parts == list(range(parts[0], parts[0] + len(parts)))
                     assert not (set(parts) & seen_parts)
                     seen_parts |= set(parts)
-                    m = mer[(mer[:, 0] == s) & (mer[:, 1] == qi0) & (mer[:, 3] == h)]
+                    m = mer[(mer[:, 0] == s) & (mer[:, 1] == qi0) & (mer[:, 3] == h) & (mer[:, 6] == 0)]
                     assert len(m) == 1 and m[0, 2] == n_q and m[0, 4] == parts[0] and m[0, 5] == len(parts)
     assert total_blocks == info.decode_blocks
     assert len(seen_parts) == info.num_partials
-    ws = 0
-    if info.num_partials:
-        d = meta.head_dim
-        a = lambda x: (x + 255) // 256 * 256
-        ws = a(info.num_partials * 16 * d * 4) + a(info.num_partials * 16 * 8)
+    d = meta.head_dim
+    a = lambda x: (x + 255) // 256 * 256
+    pp = info.num_prefill_partials
+    ws = a(info.num_partials * 16 * d * 4) + a(info.num_partials * 16 * 8) + \
+        a(pp * 128 * d * 4) + a(pp * 128 * 8)
     assert info.workspace_bytes == ws
+    nm = info.num_merge_groups
+    assert info.num_prefill_merges == int((mer[:, 6] == 1).sum())
+    assert np.all(mer[:nm - info.num_prefill_merges, 6] == 0)   # decode groups first
     assert info.num_kernels == (info.num_decode_warps > 0) + (info.num_merge_groups > 0) + \
         (info.num_prefill_tiles > 0)
 
