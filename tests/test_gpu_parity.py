@@ -258,3 +258,22 @@ def test_prefill_and_split_kv_paths_agree(pkv, cuda_device, monkeypatch):
     kv_out, _, _ = gpu_step(pkv, meta, q, k, v, pool, cuda_device)
     diff = (tc_out.double() - kv_out.double()).abs()
     assert float(diff.max()) <= MAX_ABS and float(diff.mean()) <= MEAN_ABS
+
+
+@pytest.mark.parametrize("num_sms", [1, 5, 7, 19])
+def test_prefill_split_kv_and_persistent_items_match_oracle(pkv, cuda_device, num_sms):
+    """Persistent prefill CTAs: with few SMs one CTA runs many work items in a
+    row (barrier phases carried across items); with an odd split of the work the
+    leftover query tiles are cut along their keys into partials that the merge
+    kernel combines.  Every row is checked against the oracle."""
+    meta = workloads.build_step("split_prefill", 123 + num_sms, [384, 1, 200], [3000, 700, 900],
+                                8, 2, 128)
+    q, k, v, pool = workloads.make_values(meta)
+    info, _ = pkv.plan_step(meta.cu_q_lens, meta.context_lens, 8, pkv.pool_desc(pool),
+                            num_sms=num_sms, upload=False)
+    assert info.num_prefill_ctas == min(num_sms, info.num_prefill_tiles)
+    if num_sms in (5, 7):
+        assert info.num_prefill_merges > 0      # some query tiles are cut along their keys
+    want, _ = oracle.run_step(meta, q, k, v, pool)
+    out, _, _ = gpu_step(pkv, meta, q, k, v, pool, cuda_device, num_sms=num_sms)
+    assert_close(out, want, f"split prefill on {num_sms} SMs")
