@@ -72,7 +72,7 @@ def sample_rows(meta, rng, n):
 @pytest.mark.parametrize("name", list(workloads.CONFIGS))
 def test_append_bit_exact_full_size(pkv, cuda_device, name):
     meta = workloads.make_config(name)
-    big = name in ("high_conc_decode",)
+    big = name in ("high_conc_decode", "long_context_mix")
     q, k, v, pool = workloads.make_values(meta, device=cuda_device if big else "cpu")
     pool_host = pool.cpu()
     want, bad = oracle.paged_kv_append(pool_host, k.cpu(), v.cpu(), meta.slot_mapping, block_size=16)
@@ -128,7 +128,8 @@ def test_attention_random_mixed_steps(pkv, cuda_device, seed):
 
 # ------------------------------------------------------------------ attention, full size, sampled rows
 
-@pytest.mark.parametrize("name", ["agent_mixed", "high_conc_decode", "shared_prefix_verify", "small_decode"])
+@pytest.mark.parametrize("name", ["agent_mixed", "high_conc_decode", "shared_prefix_verify", "small_decode",
+                                  "long_context_mix"])
 def test_attention_full_size_sampled_rows(pkv, cuda_device, name):
     meta = workloads.make_config(name)
     q, k, v, pool = workloads.make_values(meta, device=cuda_device)

@@ -188,12 +188,23 @@ def shared_prefix_verify(seed=1238, num_seqs=64):
                       shared_prefix_blocks=256, rng=rng)
 
 
+def long_context_mix(seed=1239):
+    """The vllm-metal page's packed-step example, "30,000 + 5,000 + 10" tokens
+    ("Replacing attention, reusing the rest", the padded-rectangle figure): three
+    requests prefilled in one step, each from an empty cache (context = query
+    length; a reading, the page gives only the token counts), with the mixed
+    step's model shape, 40 q / 8 KV heads, D=128 (also a reading: the example
+    names no model)."""
+    return build_step("long_context_mix", seed, [30000, 5000, 10], [30000, 5000, 10], 40, 8, 128)
+
+
 CONFIGS = {
     "tiny_decode": tiny_decode,
     "small_decode": small_decode,
     "agent_mixed": agent_mixed,
     "high_conc_decode": high_conc_decode,
     "shared_prefix_verify": shared_prefix_verify,
+    "long_context_mix": long_context_mix,
 }
 
 
