@@ -105,7 +105,8 @@ def test_append_padding_and_bad_slot_reported(pkv, cuda_device):
 
 # ------------------------------------------------------------------ attention, full oracle
 
-@pytest.mark.parametrize("name", ["tiny_decode", "small_decode", "shared_prefix_verify"])
+@pytest.mark.parametrize("name", ["tiny_decode", "small_decode", "shared_prefix_verify", "mtp_draft",
+                                  "wide_verify"])
 def test_attention_matches_oracle_every_row(pkv, cuda_device, name):
     meta = workloads.make_config(name)
     q, k, v, pool = workloads.make_values(meta)

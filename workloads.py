@@ -97,12 +97,15 @@ def _slots(q_lens, ctx_lens, tables, bs) -> np.ndarray:
 
 def build_step(name, seed, q_lens, ctx_lens, hq, hkv, d, *, pool_blocks=None,
                shared_prefix_blocks=0, bs=BLOCK_SIZE, scale=None, notes="",
-               rng=None) -> StepMeta:
+               rng=None, append=True) -> StepMeta:
     """Assign physical blocks by a seeded random permutation and derive slots.
 
     ``shared_prefix_blocks`` > 0 makes every sequence's first that many logical
     blocks point at the same physical blocks (a shared prompt prefix).
     ``pool_blocks`` defaults to the distinct blocks needed + 10 %.
+    ``append=False`` marks every query token's slot as skip (-1): the step
+    attends over K/V already in the pool and writes none (a draft pass over the
+    target's cache).
     """
     rng = np.random.default_rng(seed) if rng is None else rng
     q_lens = np.asarray(q_lens, dtype=np.int32)
@@ -129,7 +132,9 @@ def build_step(name, seed, q_lens, ctx_lens, hq, hkv, d, *, pool_blocks=None,
     return StepMeta(name=name, seed=seed, num_q_heads=hq, num_kv_heads=hkv,
                     head_dim=d, block_size=bs, num_blocks=pool_blocks,
                     q_lens=q_lens, context_lens=ctx_lens, cu_q_lens=_cu(q_lens),
-                    block_tables=tables, slot_mapping=_slots(q_lens, ctx_lens, tables, bs),
+                    block_tables=tables,
+                    slot_mapping=(_slots(q_lens, ctx_lens, tables, bs) if append else
+                                  np.full(int(q_lens.sum()), -1, dtype=np.int32)),
                     scale=float(scale), notes=notes)
 
 
@@ -198,6 +203,31 @@ def long_context_mix(seed=1239):
     return build_step("long_context_mix", seed, [30000, 5000, 10], [30000, 5000, 10], 40, 8, 128)
 
 
+def mtp_draft(seed=1240, num_seqs=64):
+    """The batched draft pass of the vllm-metal page ("Batched MTP under
+    concurrent load"): every request's seed token in one packed dispatch against
+    the target's shared KV cache, nothing appended (the seed's K/V is already
+    cached).  The shared-prefix step's shapes: 64 requests on a shared 4096-token
+    prefix plus a private suffix U[0, 1024], 1 query each, 32 q / 8 KV heads,
+    D=128."""
+    rng = np.random.default_rng(seed)
+    suffix = rng.integers(0, 1024, size=num_seqs, endpoint=True)
+    ctx = 4096 + suffix + 1
+    return build_step("mtp_draft", seed, [1] * num_seqs, ctx, 32, 8, 128,
+                      shared_prefix_blocks=256, rng=rng, append=False)
+
+
+def wide_verify(seed=1241, num_seqs=64):
+    """Verify windows wider than the page's 2 ("values above 1 are ignored" in
+    its MTP runs): 64 requests, alternately 4 and 8 query tokens (3 or 7 draft
+    tokens plus the seed, causal within the window), contexts uniform in
+    [1024, 8192], 32 q / 8 KV heads, D=128."""
+    rng = np.random.default_rng(seed)
+    ql = np.array([4, 8] * (num_seqs // 2), dtype=np.int32)
+    ctx = rng.integers(1024, 8192, size=num_seqs, endpoint=True)
+    return build_step("wide_verify", seed, ql, ctx, 32, 8, 128, rng=rng)
+
+
 CONFIGS = {
     "tiny_decode": tiny_decode,
     "small_decode": small_decode,
@@ -205,6 +235,8 @@ CONFIGS = {
     "high_conc_decode": high_conc_decode,
     "shared_prefix_verify": shared_prefix_verify,
     "long_context_mix": long_context_mix,
+    "mtp_draft": mtp_draft,
+    "wide_verify": wide_verify,
 }
 
 
