@@ -50,6 +50,9 @@ def _load():
             i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
             lib.oracle_paged_kv_append.argtypes = [P, i32, i32, i32, i32, P, P, P, i32]
             lib.oracle_paged_kv_append.restype = i32
+            lib.oracle_state_checkpoint.argtypes = [P, ctypes.c_int64, ctypes.c_int64, P, P,
+                                                    ctypes.c_int64]
+            lib.oracle_state_checkpoint.restype = ctypes.c_int64
             lib.oracle_check_step.argtypes = [i32, P, P, P, i32, i32, i32]
             lib.oracle_check_step.restype = i32
             lib.oracle_paged_varlen_attention.argtypes = [P, i32, i32, P, P, i32, P, i32, P, i32,
@@ -93,6 +96,19 @@ def paged_kv_append(pool_bits: np.ndarray, k, v, slot_mapping, *, block_size: in
     n = sm.shape[0]
     assert kb.shape == (n, hkv, d) and vb.shape == (n, hkv, d)
     bad = _load().oracle_paged_kv_append(_ptr(pool), nb, bs, hkv, d, _ptr(kb), _ptr(vb), _ptr(sm), n)
+    return pool, int(bad)
+
+
+def state_checkpoint(pool_bytes: np.ndarray, src_bytes: np.ndarray, slots):
+    """Return (new_pool, n_bad_slots).  pool_bytes: uint8 [num_slots, row_bytes];
+    src_bytes: uint8 [n_rows, row_bytes]; slots: int32 [n_rows] (negative = skip)."""
+    pool = np.array(np.ascontiguousarray(pool_bytes, dtype=np.uint8), copy=True)
+    src = np.ascontiguousarray(src_bytes, dtype=np.uint8)
+    sl = _i32(slots)
+    assert pool.ndim == 2 and src.ndim == 2 and src.shape[1] == pool.shape[1]
+    assert sl.shape == (src.shape[0],)
+    bad = _load().oracle_state_checkpoint(_ptr(pool), pool.shape[0], pool.shape[1], _ptr(src),
+                                          _ptr(sl), src.shape[0])
     return pool, int(bad)
 
 

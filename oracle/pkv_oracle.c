@@ -27,6 +27,13 @@
  *              w_p = exp(x_p - max x) / sum_p' exp(x_p' - max x)
  *              out[t][hq][:] = sum_p w_p * V[p][h][:]
  *
+ *  state checkpoint (same page, "Prefix caching on hybrid models": linear-
+ *            attention state cannot be addressed by a block table, so reusing a
+ *            prefix checkpoints that state at block boundaries, written into the
+ *            state pools in place).  For each row i in order whose slot is >= 0,
+ *            the row_bytes raw bytes of src row i are copied to pool row slot;
+ *            nothing else of the pool changes.
+ *
  * Readings where the pages are silent: context_lens includes this step's
  * tokens; the q_s queries are the last q_s positions of the context; KV head of
  * query head hq is hq / G (contiguous groups); a negative slot is padding; a
@@ -77,6 +84,20 @@ int oracle_paged_kv_append(uint16_t *pool, int num_blocks, int block_size, int n
       memcpy(pool + pool_row(b, 1, h, off, num_kv_heads, block_size, head_dim), vs,
              (size_t)head_dim * sizeof(uint16_t));
     }
+  }
+  return bad;
+}
+
+/* State-row checkpoint.  Returns the number of rows skipped because their slot
+ * was outside the pool (negative slots are skipped silently). */
+int64_t oracle_state_checkpoint(uint8_t *pool, int64_t num_slots, int64_t row_bytes,
+                                const uint8_t *src, const int32_t *slots, int64_t n_rows) {
+  int64_t bad = 0;
+  for (int64_t i = 0; i < n_rows; ++i) {
+    int64_t slot = slots[i];
+    if (slot < 0) continue;
+    if (slot >= num_slots) { ++bad; continue; }
+    memcpy(pool + slot * row_bytes, src + i * row_bytes, (size_t)row_bytes);
   }
   return bad;
 }

@@ -355,3 +355,35 @@ def test_append_then_attend_sees_new_token():
     out, pool_after = oracle.run_step(meta, q, k, v, pool)
     np.testing.assert_array_equal(out[0, 0], v[0, 0].to(torch.float64).numpy())
     np.testing.assert_array_equal(out[0, 1], v[0, 0].to(torch.float64).numpy())
+
+
+# ------------------------------------------------------------------ state checkpoint
+
+def test_state_checkpoint_equals_indexed_assignment():
+    """Rows land where their slots say, byte for byte, by a second route (numpy
+    indexed assignment); negative slots write nothing; other rows are untouched."""
+    rng = np.random.default_rng(7)
+    num_slots, row_bytes, n = 50, 48, 20
+    pool = rng.integers(0, 256, size=(num_slots, row_bytes), dtype=np.uint8)
+    src = rng.integers(0, 256, size=(n, row_bytes), dtype=np.uint8)
+    slots = rng.permutation(num_slots)[:n].astype(np.int32)
+    slots[[3, 11]] = -1
+    got, bad = oracle.state_checkpoint(pool, src, slots)
+    want = pool.copy()
+    keep = slots >= 0
+    want[slots[keep]] = src[keep]
+    assert bad == 0 and np.array_equal(got, want)
+    untouched = np.setdiff1d(np.arange(num_slots), slots[keep])
+    assert np.array_equal(got[untouched], pool[untouched])
+
+
+def test_state_checkpoint_bad_slots_and_empty():
+    pool = np.arange(4 * 16, dtype=np.uint8).reshape(4, 16)
+    src = np.full((3, 16), 255, dtype=np.uint8)
+    got, bad = oracle.state_checkpoint(pool, src, np.array([4, -1, 1], dtype=np.int32))
+    assert bad == 1                                  # slot 4 is past the pool: skipped
+    want = pool.copy()
+    want[1] = 255
+    assert np.array_equal(got, want)
+    got0, bad0 = oracle.state_checkpoint(pool, src[:0], np.zeros(0, dtype=np.int32))
+    assert bad0 == 0 and np.array_equal(got0, pool)
