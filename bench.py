@@ -495,18 +495,135 @@ def bench_pkv(args):
     print(json.dumps(line), flush=True)
 
 
+STATE_POOL_SLOTS = 1650        # ~1,650 cached blocks ...
+STATE_ROW_BYTES = 1 << 20      # ... of ~1 MiB state rows: a ~1.6 GiB pool
+STATE_ROWS_PER_CALL = 64       # sequences checkpointing at a block boundary in one step
+
+
+def bench_state_checkpoint(args):
+    """State-row checkpoint (in-place row writes into a state pool): bytes read +
+    written per second against the measured copy bandwidth.  The pool has the
+    page's size; each call writes STATE_ROWS_PER_CALL rows to random slots."""
+    import torch
+    import paged_kv_attention_append_gb300 as pkv
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    g = torch.Generator(device=dev).manual_seed(1242)
+    pool = torch.randint(0, 256, (STATE_POOL_SLOTS, STATE_ROW_BYTES), dtype=torch.uint8, device=dev,
+                         generator=g)
+    src = torch.randint(0, 256, (STATE_ROWS_PER_CALL, STATE_ROW_BYTES), dtype=torch.uint8, device=dev,
+                        generator=g)
+    slots = torch.randperm(STATE_POOL_SLOTS, device=dev, generator=g)[:STATE_ROWS_PER_CALL].to(torch.int32)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush_w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_acc = torch.zeros((), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(dev)
+
+    def flush_l2():
+        flush_w.zero_()
+        torch.sum(flush_r, dim=0, out=flush_acc)
+
+    def step():
+        pkv.state_checkpoint(src, slots, pool, dev_status=status)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush_l2()
+            step()
+    torch.cuda.synchronize(dev)
+    launches_before = pkv.kernel_launch_count()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    pkv.set_profile_events("state", a, b)
+    graph = torch.cuda.CUDAGraph()
+    try:
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+    finally:
+        pkv.set_profile_events("state")
+    launches = pkv.kernel_launch_count() - launches_before
+    times = []
+    barrier()
+    with ClockSampler(local) as clk:
+        with torch.cuda.stream(stream):
+            for _ in range(args.steps):
+                flush_l2()
+                graph.replay()
+                stream.synchronize()
+                times.append(a.elapsed_time(b))
+    torch.cuda.synchronize(dev)
+    assert int(status.item()) == 0
+    ms = max_over_ranks(statistics.mean(times), dev)
+    nbytes = 2 * STATE_ROWS_PER_CALL * STATE_ROW_BYTES
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    # end to end: host rows pinned -> device, checkpoint, read one row back
+    src_h = src.cpu().pin_memory()
+    back = torch.empty(STATE_ROW_BYTES, dtype=torch.uint8).pin_memory()
+    src_d = torch.empty_like(src)
+    e2e = []
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup + args.steps):
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            src_d.copy_(src_h, non_blocking=True)
+            pkv.state_checkpoint(src_d, slots, pool, dev_status=status)
+            back.copy_(pool[int(slots[0])], non_blocking=True)
+            stream.synchronize()
+            if i >= args.warmup:
+                e2e.append(time.perf_counter() - t0)
+    e2e_s = max_over_ranks(statistics.mean(e2e), dev)
+    pk = peaks()
+    if rank != 0:
+        return
+    line = {
+        "metric": "state-row checkpoint: GB/s (bytes read + written) vs peak on 1 GB300",
+        "value": job_throughput(nbytes / 1e9, ws, ms * 1e-3), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8",
+        "data": "synthetic (seeded random bytes)",
+        "config": {"workload": "state_checkpoint", "pool_slots": STATE_POOL_SLOTS,
+                   "row_bytes": STATE_ROW_BYTES, "rows_per_call": STATE_ROWS_PER_CALL,
+                   "l2": f"flushed before every timed call ({L2_FLUSH_BYTES >> 20} MB written, then read)",
+                   "timing": "CUDA graph replay per call, event nodes around the kernel"},
+        "gpu_launches": launches * args.steps,
+        "roofline": {"bound": "hbm", "kernel": "state_checkpoint_kernel", "achieved": gbs,
+                     "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": gbs / pk["hbm_gbs"],
+                     "traffic": recorded_traffic("state_checkpoint_kernel", "state_checkpoint"),
+                     "bytes_per_launch": nbytes, "ms_per_launch": ms, "peak_source": pk["source"]},
+        "e2e": {"value": job_throughput(nbytes / 1e9, ws, e2e_s), "unit": "GB/s",
+                "h2d_bytes_per_step": src_h.numel(), "d2h_bytes_per_step": back.numel(),
+                "ms_per_step": e2e_s * 1e3},
+        "clocks": clk.summary(),
+        "cpu_baseline": None,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
-    ap.add_argument("--config", default="small_decode", choices=list(workloads.CONFIGS))
+    ap.add_argument("--config", default="small_decode",
+                    choices=list(workloads.CONFIGS) + ["state_checkpoint"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.config == "state_checkpoint":
+        if args.impl == "reference":
+            print(json.dumps({"impl": "reference", "unavailable": "the state checkpoint has no "
+                              "oracle arm in the benchmark (its parity tests use the oracle)"}))
+            return
+        bench_state_checkpoint(args)
+    elif args.impl == "reference":
         bench_reference(args)
     else:
         bench_pkv(args)

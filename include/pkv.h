@@ -131,6 +131,7 @@ PKV_API int64_t pkv_kernel_launch_count(void);
 #define PKV_KERNEL_DECODE 1
 #define PKV_KERNEL_MERGE 2
 #define PKV_KERNEL_PREFILL 3
+#define PKV_KERNEL_STATE 4
 
 /*
  * Profiling hook (off by default).  After this call, every launch of kernel
@@ -207,6 +208,29 @@ PKV_API pkv_status pkv_paged_varlen_attention(const void *q, const int32_t *cu_q
                                       const pkv_plan_info *info, const void *plan_dev, void *out,
                                       void *workspace, int64_t workspace_bytes,
                                       int32_t *dev_status, pkv_stream stream);
+
+/*
+ * State-row checkpoint (the vllm-metal v0.4.0 page, "Prefix caching on hybrid
+ * models"): linear-attention layers keep a recurrent state per sequence that a
+ * block table cannot address, so reusing a prefix means checkpointing that
+ * state at block boundaries into state pools, and the rows are written in place
+ * rather than by copying the pool.
+ *   For each row i < num_rows with slot = dst_slots[i]:
+ *     slot < 0               : nothing written;
+ *     0 <= slot < num_slots  : pool[slot][0 .. row_bytes) = src[i][0 .. row_bytes)
+ *                              (raw bytes);
+ *     slot >= num_slots      : row skipped, PKV_DEV_BAD_SLOT to *dev_status.
+ *   src: device [num_rows][row_bytes]; dst_slots: device int32 [num_rows];
+ *   pool: device [num_slots][row_bytes].  row_bytes must be a positive multiple
+ *   of 16 (else PKV_ERR_SHAPE) and src, pool 16-byte aligned (else
+ *   PKV_ERR_ALIGN).  Bytes outside the written rows are untouched.  Two rows
+ *   with the same slot: unspecified which one lands.  num_rows == 0 enqueues
+ *   nothing and returns PKV_OK.
+ */
+PKV_API pkv_status pkv_state_checkpoint(const void *src, const int32_t *dst_slots,
+                                        int32_t num_rows, void *pool, int64_t num_slots,
+                                        int64_t row_bytes, int32_t *dev_status,
+                                        pkv_stream stream);
 
 /*
  * Size of the fixed scratch array used by pkv_paged_varlen_attention_noalloc

@@ -92,6 +92,8 @@ def _load():
                                                        ctypes.c_float, ctypes.POINTER(PlanInfo), P, P,
                                                        P, i64, P, P]
             lib.pkv_paged_varlen_attention.restype = i32
+            lib.pkv_state_checkpoint.argtypes = [P, P, i32, P, i64, i64, P, P]
+            lib.pkv_state_checkpoint.restype = i32
             lib.pkv_set_profile_events.argtypes = [i32, P, P]
             lib.pkv_set_profile_events.restype = i32
             _lib = lib
@@ -110,7 +112,7 @@ def kernel_launch_count() -> int:
     return int(_load().pkv_kernel_launch_count())
 
 
-KERNEL_IDS = {"append": 0, "decode": 1, "merge": 2, "prefill": 3}
+KERNEL_IDS = {"append": 0, "decode": 1, "merge": 2, "prefill": 3, "state": 4}
 
 
 def set_profile_events(kernel: str, start=None, stop=None):
@@ -172,6 +174,33 @@ def paged_kv_append(k, v, slot_mapping, kv_pool, *, dev_status=None, stream=None
                                      _stream(stream, kv_pool.device))
     if st:
         raise PkvError(st, "pkv_paged_kv_append")
+
+
+def state_checkpoint(src, dst_slots, pool, *, dev_status=None, stream=None):
+    """Write row i of src into pool row dst_slots[i] in place (negative = skip).
+
+    src: [n, ...] and pool: [num_slots, ...] contiguous CUDA tensors whose rows
+    (everything after the first axis) have the same byte size, a multiple of 16;
+    dst_slots: int32 [n].  Rows are copied as raw bytes, whatever the dtype.
+    """
+    for name, t in (("src", src), ("pool", pool)):
+        if not isinstance(t, torch.Tensor) or t.device.type != "cuda" or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous CUDA tensor")
+    _check_cuda("dst_slots", dst_slots, torch.int32, 1)
+    n = dst_slots.shape[0]
+    if src.dim() < 1 or pool.dim() < 1 or src.shape[0] != n:
+        raise ValueError("src must have one row per dst_slots entry")
+    row_bytes = src[0].numel() * src.element_size() if n else 0
+    pool_row = pool[0].numel() * pool.element_size() if pool.shape[0] else 0
+    if n and row_bytes != pool_row:
+        raise ValueError(f"row sizes differ: src {row_bytes} B, pool {pool_row} B")
+    if dev_status is not None:
+        _check_cuda("dev_status", dev_status, torch.int32)
+    st = _load().pkv_state_checkpoint(_ptr(src), _ptr(dst_slots), n, _ptr(pool), pool.shape[0],
+                                      max(row_bytes, 16), _ptr(dev_status),
+                                      _stream(stream, pool.device))
+    if st:
+        raise PkvError(st, "pkv_state_checkpoint")
 
 
 def _host_i32(x) -> np.ndarray:

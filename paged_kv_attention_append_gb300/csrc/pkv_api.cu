@@ -12,9 +12,11 @@ namespace pkv {
 static std::atomic<int64_t> g_launches{0};
 void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
+constexpr int kNumKernelIds = 5;  // PKV_KERNEL_APPEND .. PKV_KERNEL_STATE
+
 struct ProfileEvents {
-  void *start[4] = {nullptr, nullptr, nullptr, nullptr};
-  void *stop[4] = {nullptr, nullptr, nullptr, nullptr};
+  void *start[kNumKernelIds] = {};
+  void *stop[kNumKernelIds] = {};
 };
 static thread_local ProfileEvents t_prof;
 
@@ -33,7 +35,7 @@ static void record(void *ev, pkv_stream stream) {
 void profile_begin(int which, pkv_stream stream) { record(t_prof.start[which], stream); }
 void profile_end(int which, pkv_stream stream) { record(t_prof.stop[which], stream); }
 bool profiling_active() {
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < kNumKernelIds; ++i)
     if (t_prof.start[i] || t_prof.stop[i]) return true;
   return false;
 }
@@ -61,7 +63,7 @@ extern "C" int64_t pkv_kernel_launch_count(void) { return g_launches.load(); }
 
 extern "C" pkv_status pkv_set_profile_events(int32_t which, void *start_event,
                                              void *stop_event) {
-  if (which < 0 || which > 3) return PKV_ERR_RANGE;
+  if (which < 0 || which >= kNumKernelIds) return PKV_ERR_RANGE;
   t_prof.start[which] = start_event;
   t_prof.stop[which] = stop_event;
   return PKV_OK;
@@ -94,6 +96,20 @@ extern "C" pkv_status pkv_paged_kv_append(const void *k, const void *v,
   if (!aligned16(k) || !aligned16(v) || !aligned16(kv_pool)) return PKV_ERR_ALIGN;
   if (reinterpret_cast<uintptr_t>(slot_mapping) & 3u) return PKV_ERR_ALIGN;
   int e = launch_append(k, v, slot_mapping, num_tokens, kv_pool, *desc, dev_status, stream);
+  return e ? PKV_ERR_CUDA : PKV_OK;
+}
+
+extern "C" pkv_status pkv_state_checkpoint(const void *src, const int32_t *dst_slots,
+                                           int32_t num_rows, void *pool, int64_t num_slots,
+                                           int64_t row_bytes, int32_t *dev_status,
+                                           pkv_stream stream) {
+  if (num_rows < 0 || num_slots < 0 || row_bytes <= 0 || row_bytes % 16 != 0) return PKV_ERR_SHAPE;
+  if (num_rows == 0) return PKV_OK;
+  if (!src || !dst_slots || !pool) return PKV_ERR_NULL;
+  if (!aligned16(src) || !aligned16(pool) || (reinterpret_cast<uintptr_t>(dst_slots) & 3u))
+    return PKV_ERR_ALIGN;
+  int e = launch_state_checkpoint(src, dst_slots, num_rows, pool, num_slots, row_bytes,
+                                  dev_status, stream);
   return e ? PKV_ERR_CUDA : PKV_OK;
 }
 

@@ -167,6 +167,10 @@ struct AttnArgs {
   pkv_stream stream;
 };
 
+int launch_state_checkpoint(const void *src, const int32_t *dst_slots, int32_t num_rows,
+                            void *pool, int64_t num_slots, int64_t row_bytes, int32_t *dev_status,
+                            pkv_stream stream);
+
 int launch_decode(const AttnArgs &a, int *launches);
 int launch_merge(const AttnArgs &a, int *launches);
 int launch_prefill(const AttnArgs &a, int *launches);

@@ -286,3 +286,18 @@ def test_attention_validation_returns_before_launch(pkv):
     empty, _ = pkv.plan_step(np.array([0], np.int32), np.array([], np.int32), meta.num_q_heads,
                              desc, num_sms=152, upload=False)
     assert call(info_=empty, q=None) == 0    # nothing to compute
+
+
+def test_state_checkpoint_argument_checks_return_before_any_cuda_call(pkv):
+    lib = ctypes.CDLL(pkv.library_path())
+    f = lib.pkv_state_checkpoint
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32, ctypes.c_void_p,
+                  ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p]
+    f.restype = ctypes.c_int32
+    fake = ctypes.c_void_p(0x1000)     # never dereferenced: every case returns before a launch
+    assert f(fake, fake, 4, fake, 10, 24, None, None) == 2       # row_bytes not a multiple of 16
+    assert f(fake, fake, 4, fake, 10, 0, None, None) == 2        # empty rows
+    assert f(fake, fake, -1, fake, 10, 32, None, None) == 2      # negative count
+    assert f(None, None, 0, None, 10, 32, None, None) == 0       # nothing to do
+    assert f(None, fake, 4, fake, 10, 32, None, None) == 1       # NULL src
+    assert f(ctypes.c_void_p(0x1008), fake, 4, fake, 10, 32, None, None) == 8   # misaligned src

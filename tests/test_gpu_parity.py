@@ -279,3 +279,63 @@ def test_prefill_split_kv_and_persistent_items_match_oracle(pkv, cuda_device, nu
     want, _ = oracle.run_step(meta, q, k, v, pool)
     out, _, _ = gpu_step(pkv, meta, q, k, v, pool, cuda_device, num_sms=num_sms)
     assert_close(out, want, f"split prefill on {num_sms} SMs")
+
+
+# ------------------------------------------------------------------ state-row checkpoint
+
+@pytest.mark.parametrize("num_slots,row_bytes,n", [
+    (40, 16, 7),            # the smallest row
+    (300, 4096, 64),        # many short rows
+    (96, 1 << 20, 24),      # MiB rows, as in the page's state pools
+    (8, 48, 0),             # nothing to write
+])
+def test_state_checkpoint_bit_exact(pkv, cuda_device, num_slots, row_bytes, n):
+    rng = np.random.default_rng(row_bytes + n)
+    pool = rng.integers(0, 256, size=(num_slots, row_bytes), dtype=np.uint8)
+    src = rng.integers(0, 256, size=(n, row_bytes), dtype=np.uint8)
+    slots = rng.permutation(num_slots)[:n].astype(np.int32)
+    if n > 3:
+        slots[1] = -1
+    want, bad = oracle.state_checkpoint(pool, src, slots)
+    assert bad == 0
+    pd = torch.from_numpy(pool).to(cuda_device)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    pkv.state_checkpoint(torch.from_numpy(src).to(cuda_device), torch.from_numpy(slots).to(cuda_device),
+                         pd, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(pd.cpu().numpy(), want)
+
+
+def test_state_checkpoint_bad_slot_reported_and_skipped(pkv, cuda_device):
+    rng = np.random.default_rng(11)
+    pool = rng.integers(0, 256, size=(20, 64), dtype=np.uint8)
+    src = rng.integers(0, 256, size=(3, 64), dtype=np.uint8)
+    slots = np.array([5, 20, 7], dtype=np.int32)          # 20 is past the pool
+    want, bad = oracle.state_checkpoint(pool, src, slots)
+    assert bad == 1
+    pd = torch.from_numpy(pool).to(cuda_device)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    pkv.state_checkpoint(torch.from_numpy(src).to(cuda_device), torch.from_numpy(slots).to(cuda_device),
+                         pd, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 1
+    assert np.array_equal(pd.cpu().numpy(), want)
+
+
+def test_state_checkpoint_full_size_pool(pkv, cuda_device):
+    """The page's pool size: about 1,650 cached blocks of ~1 MiB state rows
+    (~1.6 GiB); 64 rows written, checked row by row, other rows unchanged."""
+    num_slots, row_bytes, n = 1650, 1 << 20, 64
+    g = torch.Generator(device=cuda_device).manual_seed(5)
+    pool = torch.randint(0, 256, (num_slots, row_bytes), dtype=torch.uint8, device=cuda_device,
+                         generator=g)
+    before = pool.clone()
+    src = torch.randint(0, 256, (n, row_bytes), dtype=torch.uint8, device=cuda_device, generator=g)
+    slots = torch.randperm(num_slots, device=cuda_device, generator=g)[:n].to(torch.int32)
+    pkv.state_checkpoint(src, slots, pool)
+    torch.cuda.synchronize()
+    written = torch.zeros(num_slots, dtype=torch.bool, device=cuda_device)
+    written[slots.long()] = True
+    assert torch.equal(pool[slots.long()], src)
+    assert torch.equal(pool[~written], before[~written])
