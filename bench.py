@@ -296,12 +296,21 @@ def bench_pkv(args):
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     meta = workloads.make_config(args.config)
+    # a chained workload runs nch decode steps per timed unit (one graph), with
+    # the contexts and slots moved on by the device between steps
+    nch = workloads.chain_steps(meta)
+    metas = [workloads.chain_step(meta, meta.context_lens, t) for t in range(nch)]
     q, k, v, pool = workloads.make_values(meta, device=dev)
-    slots = torch.from_numpy(meta.slot_mapping).to(dev)
+    vals = [(q, k, v)] + [tuple(workloads.make_values(m, seed=meta.seed + t, device=dev)[:3])
+                          for t, m in enumerate(metas) if t > 0]
+    slots0 = torch.from_numpy(meta.slot_mapping).to(dev)
+    slots = slots0.clone()
     cu_d = torch.from_numpy(meta.cu_q_lens).to(dev)
-    ctx_d = torch.from_numpy(meta.context_lens).to(dev)
+    ctx0_d = torch.from_numpy(meta.context_lens).to(dev)
+    ctx_d = ctx0_d.clone()
     bt_d = torch.from_numpy(meta.block_tables).to(dev)
-    out = torch.empty_like(q)
+    outs = [torch.empty_like(x[0]) for x in vals]
+    out = outs[0]
     flush_w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_acc = torch.zeros((), dtype=torch.float32, device=dev)
@@ -312,11 +321,13 @@ def bench_pkv(args):
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(dev)
 
+    chain_arg = nch if nch > 1 else None
     info, host_plan = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, pool,
-                                    upload=False)
+                                    upload=False, chain_steps=chain_arg)
     t0 = time.perf_counter()
     for _ in range(50):
-        pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, pool, upload=False)
+        pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, pool, upload=False,
+                      chain_steps=chain_arg)
     host_plan_us = (time.perf_counter() - t0) / 50 * 1e6
     plan_pinned = torch.from_numpy(host_plan.view(np.uint8)).pin_memory()
     plan = pkv.StepPlan(info, host_plan, dev)
@@ -324,9 +335,15 @@ def bench_pkv(args):
     def step():
         # the plan is a step input like the block tables: uploaded before the timed
         # region (StepPlan); host planning and its upload are timed inside e2e
-        pkv.paged_kv_append(k, v, slots, pool, dev_status=status)
-        pkv.paged_varlen_attention(q, cu_d, ctx_d, bt_d, pool, meta.scale, plan=plan, out=out,
-                                   dev_status=status)
+        if nch > 1:
+            ctx_d.copy_(ctx0_d)
+            slots.copy_(slots0)
+        for t, (qt, kt, vt) in enumerate(vals):
+            pkv.paged_kv_append(kt, vt, slots, pool, dev_status=status)
+            pkv.paged_varlen_attention(qt, cu_d, ctx_d, bt_d, pool, meta.scale, plan=plan,
+                                       out=outs[t], dev_status=status)
+            if t + 1 < nch:
+                pkv.decode_advance(ctx_d, slots, cu_d, bt_d, pool, dev_status=status)
 
     # warm up eagerly, then capture one step into a CUDA graph
     with torch.cuda.stream(stream):
@@ -397,43 +414,53 @@ def bench_pkv(args):
     step_ms = max_over_ranks(step_ms, dev)
     assert int(status.item()) == 0, f"device status {int(status.item())}"
 
-    # ---- end to end from pinned host buffers through the public API
+    # ---- end to end from pinned host buffers through the public API (a chained
+    # workload: all its steps' inputs in, one plan, every step's output back)
     host = {
-        "q": q.cpu().pin_memory(), "k": k.cpu().pin_memory(), "v": v.cpu().pin_memory(),
-        "slots": slots.cpu().pin_memory(), "cu": cu_d.cpu().pin_memory(),
-        "ctx": ctx_d.cpu().pin_memory(), "bt": bt_d.cpu().pin_memory(),
+        "slots": slots0.cpu().pin_memory(), "cu": cu_d.cpu().pin_memory(),
+        "ctx": ctx0_d.cpu().pin_memory(), "bt": bt_d.cpu().pin_memory(),
     }
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    ds, dcu, dctx, dbt = (torch.empty_like(t) for t in (slots, cu_d, ctx_d, bt_d))
-    h2d = sum(t.numel() * t.element_size() for t in host.values()) + plan_pinned.numel()
-    d2h = out_h.numel() * out_h.element_size()
+    host_vals = [tuple(x.cpu().pin_memory() for x in qkv) for qkv in vals]
+    outs_h = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
+    dvals = [tuple(torch.empty_like(x) for x in qkv) for qkv in vals]
+    ds, dcu, dctx, dbt = (torch.empty_like(t) for t in (slots0, cu_d, ctx0_d, bt_d))
+    h2d = (sum(t.numel() * t.element_size() for t in host.values()) + plan_pinned.numel() +
+           sum(x.numel() * x.element_size() for qkv in host_vals for x in qkv))
+    d2h = sum(o.numel() * o.element_size() for o in outs_h)
     e2e_times = []
     with torch.cuda.stream(stream):
         for i in range(args.warmup + args.steps):
             torch.cuda.synchronize(dev)
             t0 = time.perf_counter()
-            for dst, src in ((dq, host["q"]), (dk, host["k"]), (dv, host["v"]), (ds, host["slots"]),
-                             (dcu, host["cu"]), (dctx, host["ctx"]), (dbt, host["bt"])):
+            for dst, src in ((ds, host["slots"]), (dcu, host["cu"]), (dctx, host["ctx"]),
+                             (dbt, host["bt"])):
                 dst.copy_(src, non_blocking=True)
+            for dqkv, hqkv in zip(dvals, host_vals):
+                for dst, src in zip(dqkv, hqkv):
+                    dst.copy_(src, non_blocking=True)
             inf2, hp2 = pkv.plan_step(host["cu"].numpy(), host["ctx"].numpy(), meta.num_q_heads, pool,
-                                      upload=False)
+                                      upload=False, chain_steps=chain_arg)
             pp = torch.from_numpy(hp2.view(np.uint8))
             plan.dev[:pp.numel()].copy_(pp, non_blocking=False)
             plan.info = inf2
-            pkv.paged_kv_append(dk, dv, ds, pool, dev_status=status)
-            pkv.paged_varlen_attention(dq, dcu, dctx, dbt, pool, meta.scale, plan=plan, out=out,
-                                       dev_status=status)
-            out_h.copy_(out, non_blocking=True)
+            for t, (dq, dk, dv) in enumerate(dvals):
+                pkv.paged_kv_append(dk, dv, ds, pool, dev_status=status)
+                pkv.paged_varlen_attention(dq, dcu, dctx, dbt, pool, meta.scale, plan=plan,
+                                           out=outs[t], dev_status=status)
+                if t + 1 < nch:
+                    pkv.decode_advance(dctx, ds, dcu, dbt, pool, dev_status=status)
+            for oh, o in zip(outs_h, outs):
+                oh.copy_(o, non_blocking=True)
             stream.synchronize()
             if i >= args.warmup:
                 e2e_times.append(time.perf_counter() - t0)
     e2e_s = max_over_ranks(statistics.mean(e2e_times), dev)
 
     pk = peaks()
-    kv_tok = meta.kv_tokens()
-    bytes_alg = algorithmic_bytes(meta)
-    dec_bytes = algorithmic_bytes(meta, prefill=False)
+    kv_tok = sum(m.kv_tokens() for m in metas)          # over the chain's steps
+    bytes_alg = sum(algorithmic_bytes(m) for m in metas)
+    # kernel events keep the last launch of a chain: its step's bytes
+    dec_bytes = algorithmic_bytes(metas[-1], prefill=False)
     fl = prefill_flops(meta)
     kernels = {"append_kernel": {"ms_per_launch": kern_ms["append"]}}
     if kern_ms["merge"]:
@@ -467,7 +494,8 @@ def bench_pkv(args):
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16, shapes of the named workload)",
-        "config": {**workloads.describe(meta), "parallelism": f"replicas x{ws}" if ws > 1 else "single",
+        "config": {**workloads.describe(meta), **({"chain_steps": nch} if nch > 1 else {}),
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single",
                    "l2": f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MB written, then "
                          f"{L2_FLUSH_BYTES >> 20} MB read)",
                    "timing": "CUDA graph replay per step, CUDA events per step; kernel "

@@ -110,7 +110,8 @@ typedef struct pkv_plan_info {
                                 an equal-cost range of the work items' key tiles */
   int32_t num_prefill_partials; /* prefill partial-result slots (128 rows each) */
   int32_t num_prefill_merges;   /* prefill merge groups (the last ones of num_merge_groups) */
-  int32_t reserved;
+  int32_t lookahead;            /* further decode steps the plan stays valid for (chained
+                                   decode, pkv_plan_decode_chain); 0 for a single step */
   int64_t kv_tokens;         /* sum of context_lens over sequences with q_len > 0 */
   int64_t decode_blocks;     /* (KV block, KV head) pairs streamed by the split-KV kernel */
   int64_t plan_bytes;        /* bytes of the plan buffer (host, then device copy) */
@@ -183,6 +184,41 @@ PKV_API pkv_status pkv_paged_kv_append(const void *k, const void *v, const int32
 PKV_API pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *context_lens, int32_t num_seqs,
                          int32_t num_q_heads, const pkv_pool_desc *desc, int32_t num_sms,
                          void *plan, int64_t plan_capacity, pkv_plan_info *info);
+
+/*
+ * Plan for a chain of `steps` decode steps of the same batch (the vllm-metal
+ * page's MLX engine, "Chained greedy decode": several decode steps built into
+ * one graph and run with a single sync per chunk).  context_lens are those of
+ * the first step; every later step adds each sequence's q_len tokens.  The one
+ * plan serves all steps: it is sized for the last step's contexts, and each
+ * step reads the current contexts from the device copy of context_lens, which
+ * pkv_decode_advance moves on between steps.  Block tables must already hold
+ * the blocks of the last step's contexts (info->max_blocks_needed counts them).
+ * Sequences with q_len >= 64 (tensor-core prefill rows) are not supported here:
+ * PKV_ERR_UNSUPPORTED.  steps < 1: PKV_ERR_RANGE.  Otherwise as pkv_plan_step;
+ * info->lookahead = steps - 1.
+ */
+PKV_API pkv_status pkv_plan_decode_chain(const int32_t *cu_q_lens, const int32_t *context_lens,
+                                         int32_t num_seqs, int32_t num_q_heads,
+                                         const pkv_pool_desc *desc, int32_t num_sms, int32_t steps,
+                                         void *plan, int64_t plan_capacity, pkv_plan_info *info);
+
+/*
+ * Device-side move to the next step of a decode chain: for every sequence s
+ * with q = cu_q_lens[s+1] - cu_q_lens[s] > 0, context_lens[s] += q and
+ * slot_mapping[cu_q_lens[s] + i] = the pool slot of position
+ * context_lens[s] - q + i (new value), i.e. block_tables[s][pos / block_size] *
+ * block_size + pos % block_size, for i < q.  A position whose block lies
+ * outside the table or the pool gets slot -1 (not written by the next append)
+ * and PKV_DEV_BAD_BLOCK goes to *dev_status.  All arrays are device int32;
+ * the kernel runs after the preceding attention call in stream order, so that
+ * call read the old contexts.
+ */
+PKV_API pkv_status pkv_decode_advance(int32_t *context_lens, int32_t *slot_mapping,
+                                      const int32_t *cu_q_lens, const int32_t *block_tables,
+                                      int32_t max_blocks_per_seq, int32_t num_seqs,
+                                      const pkv_pool_desc *desc, int32_t *dev_status,
+                                      pkv_stream stream);
 
 /*
  * Packed varlen attention over the paged KV pool ("Replacing attention,

@@ -51,7 +51,7 @@ class PlanInfo(ctypes.Structure):
         "num_seqs", "num_q_heads", "num_kv_heads", "head_dim", "total_q", "num_decode_warps",
         "num_decode_pieces", "num_merge_groups", "num_partials", "num_prefill_tiles", "num_kernels",
         "max_blocks_needed", "num_prefill_ctas", "num_prefill_partials", "num_prefill_merges",
-        "reserved")] + [(n, ctypes.c_int64) for n in (
+        "lookahead")] + [(n, ctypes.c_int64) for n in (
             "kv_tokens", "decode_blocks",
                                                               "plan_bytes", "workspace_bytes")]
 
@@ -94,6 +94,12 @@ def _load():
             lib.pkv_paged_varlen_attention.restype = i32
             lib.pkv_state_checkpoint.argtypes = [P, P, i32, P, i64, i64, P, P]
             lib.pkv_state_checkpoint.restype = i32
+            lib.pkv_plan_decode_chain.argtypes = [P, P, i32, i32, ctypes.POINTER(PoolDesc), i32,
+                                                  i32, P, i64, ctypes.POINTER(PlanInfo)]
+            lib.pkv_plan_decode_chain.restype = i32
+            lib.pkv_decode_advance.argtypes = [P, P, P, P, i32, i32, ctypes.POINTER(PoolDesc), P,
+                                               P]
+            lib.pkv_decode_advance.restype = i32
             lib.pkv_set_profile_events.argtypes = [i32, P, P]
             lib.pkv_set_profile_events.restype = i32
             _lib = lib
@@ -243,10 +249,11 @@ class _nullcontext:
 
 
 def plan_step(cu_q_lens, context_lens, num_q_heads: int, kv_pool_or_desc, *, num_sms=None,
-              device=None, upload=True, stream=None) -> StepPlan | tuple:
+              device=None, upload=True, stream=None, chain_steps=None) -> StepPlan | tuple:
     """Build the host plan for one step (pkv_plan_step) and upload it.
 
     cu_q_lens / context_lens: host arrays or tensors (copied to the host if on a GPU).
+    chain_steps: plan a chain of that many decode steps instead (pkv_plan_decode_chain).
     Returns a StepPlan (or (info, host_bytes) when upload=False).
     """
     desc = kv_pool_or_desc if isinstance(kv_pool_or_desc, PoolDesc) else pool_desc(kv_pool_or_desc)
@@ -261,20 +268,48 @@ def plan_step(cu_q_lens, context_lens, num_q_heads: int, kv_pool_or_desc, *, num
                    if torch.cuda.is_available() else 152)
     info = PlanInfo()
     lib = _load()
-    st = lib.pkv_plan_step(cu.ctypes.data_as(ctypes.c_void_p), ctx.ctypes.data_as(ctypes.c_void_p),
-                           ctx.shape[0], int(num_q_heads), ctypes.byref(desc), int(num_sms), None, 0,
-                           ctypes.byref(info))
+    name = "pkv_plan_step" if chain_steps is None else "pkv_plan_decode_chain"
+
+    def call(buf, cap):
+        args = [cu.ctypes.data_as(ctypes.c_void_p), ctx.ctypes.data_as(ctypes.c_void_p),
+                ctx.shape[0], int(num_q_heads), ctypes.byref(desc), int(num_sms)]
+        if chain_steps is not None:
+            args.append(int(chain_steps))
+        return getattr(lib, name)(*args, buf, cap, ctypes.byref(info))
+    st = call(None, 0)
     if st:
-        raise PkvError(st, "pkv_plan_step")
+        raise PkvError(st, name)
     host = np.zeros((max(int(info.plan_bytes), 16) + 15) // 16 * 4, dtype=np.int32)
-    st = lib.pkv_plan_step(cu.ctypes.data_as(ctypes.c_void_p), ctx.ctypes.data_as(ctypes.c_void_p),
-                           ctx.shape[0], int(num_q_heads), ctypes.byref(desc), int(num_sms),
-                           host.ctypes.data_as(ctypes.c_void_p), host.nbytes, ctypes.byref(info))
+    st = call(host.ctypes.data_as(ctypes.c_void_p), host.nbytes)
     if st:
-        raise PkvError(st, "pkv_plan_step")
+        raise PkvError(st, name)
     if not upload:
         return info, host
     return StepPlan(info, host, torch.device(device), stream)
+
+
+def decode_advance(context_lens, slot_mapping, cu_q_lens, block_tables, kv_pool, *,
+                   dev_status=None, stream=None):
+    """Move a decode chain to its next step on the device (pkv_decode_advance):
+    context_lens += q_len and slot_mapping <- the slots of the new positions.
+    All four arrays are device int32 tensors; context_lens and slot_mapping are
+    updated in place."""
+    _check_cuda("context_lens", context_lens, torch.int32, 1)
+    _check_cuda("slot_mapping", slot_mapping, torch.int32, 1)
+    _check_cuda("cu_q_lens", cu_q_lens, torch.int32, 1)
+    _check_cuda("block_tables", block_tables, torch.int32, 2)
+    desc = pool_desc(kv_pool)
+    n = context_lens.shape[0]
+    if cu_q_lens.shape[0] != n + 1 or block_tables.shape[0] != n:
+        raise ValueError("cu_q_lens needs num_seqs + 1 entries and block_tables num_seqs rows")
+    if dev_status is not None:
+        _check_cuda("dev_status", dev_status, torch.int32)
+    st = _load().pkv_decode_advance(_ptr(context_lens), _ptr(slot_mapping), _ptr(cu_q_lens),
+                                    _ptr(block_tables), block_tables.shape[1], n,
+                                    ctypes.byref(desc), _ptr(dev_status),
+                                    _stream(stream, context_lens.device))
+    if st:
+        raise PkvError(st, "pkv_decode_advance")
 
 
 def _dev_i32(x, device, name):

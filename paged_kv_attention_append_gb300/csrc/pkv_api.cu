@@ -113,6 +113,21 @@ extern "C" pkv_status pkv_state_checkpoint(const void *src, const int32_t *dst_s
   return e ? PKV_ERR_CUDA : PKV_OK;
 }
 
+extern "C" pkv_status pkv_decode_advance(int32_t *context_lens, int32_t *slot_mapping,
+                                         const int32_t *cu_q_lens, const int32_t *block_tables,
+                                         int32_t max_blocks_per_seq, int32_t num_seqs,
+                                         const pkv_pool_desc *desc, int32_t *dev_status,
+                                         pkv_stream stream) {
+  pkv_status st = check_pool(desc);
+  if (st != PKV_OK) return st;
+  if (num_seqs < 0 || max_blocks_per_seq < 0) return PKV_ERR_SHAPE;
+  if (num_seqs == 0) return PKV_OK;
+  if (!context_lens || !slot_mapping || !cu_q_lens || !block_tables) return PKV_ERR_NULL;
+  int e = launch_decode_advance(context_lens, slot_mapping, cu_q_lens, block_tables,
+                                max_blocks_per_seq, num_seqs, desc->num_blocks, dev_status, stream);
+  return e ? PKV_ERR_CUDA : PKV_OK;
+}
+
 extern "C" pkv_status pkv_paged_varlen_attention(
     const void *q, const int32_t *cu_q_lens, const int32_t *context_lens,
     const int32_t *block_tables, int32_t max_blocks_per_seq, const void *kv_pool,
@@ -178,6 +193,9 @@ extern "C" pkv_status pkv_paged_varlen_attention(
   a.ppart_o = reinterpret_cast<float *>(wb ? wb + off_po : nullptr);
   a.ppart_ml = reinterpret_cast<float *>(wb ? wb + off_pml : nullptr);
   a.num_decode_merges = info->num_merge_groups - info->num_prefill_merges;
+  if (info->lookahead < 0 || (info->lookahead > 0 && info->num_prefill_tiles > 0))
+    return PKV_ERR_SHAPE;
+  a.lookahead = info->lookahead;
   if (ws_total_bytes(info->num_partials, info->num_prefill_partials, d) > workspace_bytes)
     return PKV_ERR_WORKSPACE;
   a.dev_status = dev_status;

@@ -66,4 +66,42 @@ int launch_append(const void *k, const void *v, const int32_t *slot_mapping, int
   return (int)cudaGetLastError();
 }
 
+// Chained decode: moves a decode batch to its next step on the device (the
+// vllm-metal page's "Chained greedy decode" keeps the token loop off the CPU).
+// One thread per sequence: context += q_len, and the slots of the q_len new
+// positions are read from the block table.
+__global__ void __launch_bounds__(128) decode_advance_kernel(
+    int32_t *__restrict__ context_lens, int32_t *__restrict__ slot_mapping,
+    const int32_t *__restrict__ cu_q_lens, const int32_t *__restrict__ block_tables,
+    int32_t max_blocks_per_seq, int32_t num_seqs, int32_t num_blocks, int32_t *dev_status) {
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= num_seqs) return;
+  const int32_t c0 = cu_q_lens[s], q = cu_q_lens[s + 1] - c0;
+  if (q <= 0) return;
+  const int32_t ctx = context_lens[s] + q;
+  context_lens[s] = ctx;
+  for (int32_t i = 0; i < q; ++i) {
+    const int32_t pos = ctx - q + i, blk = pos / kBlockSize;
+    const int32_t phys =
+        blk < max_blocks_per_seq ? block_tables[(int64_t)s * max_blocks_per_seq + blk] : -1;
+    int32_t slot = -1;
+    if (phys >= 0 && phys < num_blocks)
+      slot = phys * kBlockSize + pos % kBlockSize;
+    else
+      report(dev_status, PKV_DEV_BAD_BLOCK);
+    slot_mapping[c0 + i] = slot;
+  }
+}
+
+int launch_decode_advance(int32_t *context_lens, int32_t *slot_mapping, const int32_t *cu_q_lens,
+                          const int32_t *block_tables, int32_t max_blocks_per_seq,
+                          int32_t num_seqs, int32_t num_blocks, int32_t *dev_status,
+                          pkv_stream stream) {
+  decode_advance_kernel<<<(unsigned)((num_seqs + 127) / 128), 128, 0, stream>>>(
+      context_lens, slot_mapping, cu_q_lens, block_tables, max_blocks_per_seq, num_seqs,
+      num_blocks, dev_status);
+  count_launches(1);
+  return (int)cudaGetLastError();
+}
+
 }  // namespace pkv

@@ -70,6 +70,7 @@ struct DecodeParams {
   const float *ppart_o;
   const float2 *ppart_ml;
   int32_t *dev_status;
+  int32_t lookahead;           // plan sized for this many further steps (chained decode)
   int32_t num_merges;          // all merge groups: decode ones, then prefill ones
   int32_t num_decode_merges;
   int32_t num_warps;
@@ -353,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       qs = (pi == pb ? f_cu1 : __ldg(p.cu_q_lens + pc.seq + 1)) - cu0;
       ctx = pi == pb ? f_ctx : __ldg(p.context_lens + pc.seq);
       valid = pc.qi0 >= 0 && pc.qi0 + pc.n_q <= qs && qs <= ctx && pc.q_row0 == cu0 + pc.qi0 &&
-              pc.kb_end <= (ctx - qs + pc.qi0 + pc.n_q - 1) / kBlockSize + 1;
+              pc.kb_end <= (ctx + p.lookahead * qs - qs + pc.qi0 + pc.n_q - 1) / kBlockSize + 1;
     }
     if (!valid && lane == 0) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
     const int R = valid ? pc.n_q * G : 0;
@@ -572,6 +573,7 @@ DecodeParams make_params(const AttnArgs &a) {
   p.part_o = a.part_o;
   p.part_ml = reinterpret_cast<float2 *>(a.part_ml);
   p.num_merges = a.num_merge_groups;
+  p.lookahead = a.lookahead;
   p.num_decode_merges = a.num_decode_merges;
   p.ppart_o = a.ppart_o;
   p.ppart_ml = reinterpret_cast<const float2 *>(a.ppart_ml);

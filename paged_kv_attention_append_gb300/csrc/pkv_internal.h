@@ -163,6 +163,7 @@ struct AttnArgs {
   float *ppart_o;
   float *ppart_ml;
   int32_t num_decode_merges;  // merge_groups[0 .. num_decode_merges) are kind 0
+  int32_t lookahead;          // further decode steps the plan covers (chained decode)
   int32_t *dev_status;
   pkv_stream stream;
 };
@@ -170,6 +171,11 @@ struct AttnArgs {
 int launch_state_checkpoint(const void *src, const int32_t *dst_slots, int32_t num_rows,
                             void *pool, int64_t num_slots, int64_t row_bytes, int32_t *dev_status,
                             pkv_stream stream);
+
+int launch_decode_advance(int32_t *context_lens, int32_t *slot_mapping, const int32_t *cu_q_lens,
+                          const int32_t *block_tables, int32_t max_blocks_per_seq,
+                          int32_t num_seqs, int32_t num_blocks, int32_t *dev_status,
+                          pkv_stream stream);
 
 int launch_decode(const AttnArgs &a, int *launches);
 int launch_merge(const AttnArgs &a, int *launches);

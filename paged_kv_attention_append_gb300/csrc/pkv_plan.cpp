@@ -78,11 +78,16 @@ struct Segment {
 
 using namespace pkv;
 
-extern "C" pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *context_lens,
-                                    int32_t num_seqs, int32_t num_q_heads,
-                                    const pkv_pool_desc *desc, int32_t num_sms, void *plan,
-                                    int64_t plan_capacity, pkv_plan_info *info) {
+// lookahead > 0: a plan for `lookahead` further decode steps of the same batch
+// (chained decode): every sequence then gains its q_len tokens per step, so the
+// decode segments are sized for context + lookahead * q_len; prefill-class
+// sequences are not supported there.
+static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_lens,
+                            int32_t num_seqs, int32_t num_q_heads, const pkv_pool_desc *desc,
+                            int32_t num_sms, int32_t lookahead, void *plan, int64_t plan_capacity,
+                            pkv_plan_info *info) {
   if (!info) return PKV_ERR_NULL;
+  if (lookahead < 0) return PKV_ERR_RANGE;
   pkv_status st = check_desc(desc, num_q_heads);
   if (st != PKV_OK) return st;
   if (num_seqs < 0) return PKV_ERR_SHAPE;
@@ -108,7 +113,11 @@ extern "C" pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *con
     if (ctx < 0 || qs > ctx) return PKV_ERR_RANGE;
     if (qs == 0) continue;
     kv_tokens += ctx;
-    max_nb = std::max(max_nb, (ctx + kBlockSize - 1) / kBlockSize);
+    if (lookahead > 0 && qs >= min_q_prefill) return PKV_ERR_UNSUPPORTED;
+    const int64_t ctx_plan64 = (int64_t)ctx + (int64_t)lookahead * qs;  // context at the last step
+    if (ctx_plan64 > INT32_MAX - kBlockSize) return PKV_ERR_RANGE;
+    const int32_t ctx_plan = (int32_t)ctx_plan64;
+    max_nb = std::max(max_nb, (ctx_plan + kBlockSize - 1) / kBlockSize);
     if (qs >= min_q_prefill) {
       // units of 128 tokens x 1 query head; within one KV head, sorted by the
       // keys they see, neighbours pair up into one work item (sub-tile 0 sees
@@ -150,7 +159,7 @@ extern "C" pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *con
     }
     for (int32_t qi0 = 0; qi0 < qs; qi0 += nq_tile) {
       int32_t n_q = std::min(nq_tile, qs - qi0);
-      int32_t nb = (ctx - qs + qi0 + n_q - 1) / kBlockSize + 1;
+      int32_t nb = (ctx_plan - qs + qi0 + n_q - 1) / kBlockSize + 1;
       for (int32_t h = 0; h < hkv; ++h) {
         segs.push_back({s, qi0, n_q, h, nb});
         total_blocks += nb;
@@ -386,6 +395,7 @@ extern "C" pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *con
   info->decode_blocks = total_blocks;
   info->plan_bytes = off.total;
   info->workspace_bytes = ws_total_bytes(parts, pparts, desc->head_dim);
+  info->lookahead = lookahead;
 
   if (!plan) return PKV_OK;
   if (plan_capacity < info->plan_bytes) return PKV_ERR_WORKSPACE;
@@ -418,4 +428,22 @@ extern "C" pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *con
     std::memcpy(p + off.prefill, ptiles.data(), ptiles.size() * sizeof(PrefillTile));
   }
   return PKV_OK;
+}
+
+extern "C" pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *context_lens,
+                                    int32_t num_seqs, int32_t num_q_heads,
+                                    const pkv_pool_desc *desc, int32_t num_sms, void *plan,
+                                    int64_t plan_capacity, pkv_plan_info *info) {
+  return plan_impl(cu_q_lens, context_lens, num_seqs, num_q_heads, desc, num_sms, 0, plan,
+                   plan_capacity, info);
+}
+
+extern "C" pkv_status pkv_plan_decode_chain(const int32_t *cu_q_lens, const int32_t *context_lens,
+                                            int32_t num_seqs, int32_t num_q_heads,
+                                            const pkv_pool_desc *desc, int32_t num_sms,
+                                            int32_t steps, void *plan, int64_t plan_capacity,
+                                            pkv_plan_info *info) {
+  if (steps < 1) return PKV_ERR_RANGE;
+  return plan_impl(cu_q_lens, context_lens, num_seqs, num_q_heads, desc, num_sms, steps - 1, plan,
+                   plan_capacity, info);
 }

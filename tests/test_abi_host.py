@@ -301,3 +301,25 @@ def test_state_checkpoint_argument_checks_return_before_any_cuda_call(pkv):
     assert f(None, None, 0, None, 10, 32, None, None) == 0       # nothing to do
     assert f(None, fake, 4, fake, 10, 32, None, None) == 1       # NULL src
     assert f(ctypes.c_void_p(0x1008), fake, 4, fake, 10, 32, None, None) == 8   # misaligned src
+
+
+def test_decode_chain_plan_covers_the_last_step(pkv):
+    """A chain plan for S steps is a single-step plan of the last step's contexts
+    (each step adds q_len tokens), with lookahead S - 1; prefill rows are refused."""
+    meta = workloads.small_decode()
+    desc = pkv.PoolDesc(meta.num_blocks, 16, meta.num_kv_heads, meta.head_dim)
+    steps = 7
+    info, host = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, desc,
+                               num_sms=152, upload=False, chain_steps=steps)
+    last = meta.context_lens + (steps - 1) * meta.q_lens
+    info1, host1 = pkv.plan_step(meta.cu_q_lens, last, meta.num_q_heads, desc, num_sms=152,
+                                 upload=False)
+    assert info.lookahead == steps - 1 and info1.lookahead == 0
+    assert info.decode_blocks == info1.decode_blocks
+    assert info.kv_tokens == int(meta.context_lens.sum())
+    assert np.array_equal(host[16:], host1[16:])          # same work lists after the header
+    with pytest.raises(pkv.PkvError):                       # prefill-class rows
+        pkv.plan_step([0, 100], [300], 8, pkv.PoolDesc(100, 16, 2, 128), upload=False, chain_steps=2)
+    with pytest.raises(pkv.PkvError):
+        pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, desc, upload=False,
+                      chain_steps=0)

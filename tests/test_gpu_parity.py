@@ -339,3 +339,110 @@ def test_state_checkpoint_full_size_pool(pkv, cuda_device):
     written[slots.long()] = True
     assert torch.equal(pool[slots.long()], src)
     assert torch.equal(pool[~written], before[~written])
+
+
+# ------------------------------------------------------------------ chained decode
+
+def _chain_case(steps, seed=77):
+    """A decode batch whose tables already hold the blocks of the chain's last step,
+    and the per-step (context_lens, slot_mapping) the chain must go through."""
+    ctx0 = np.array([15, 16, 17, 100, 31, 255, 2], dtype=np.int32)
+    ql = np.array([1, 1, 1, 2, 1, 1, 1], dtype=np.int32)    # one verify pair rides along
+    last = ctx0 + (steps - 1) * ql
+    meta = workloads.build_step("chain", seed, ql, last, 8, 2, 128)
+    per_step = []
+    for t in range(steps):
+        ctx = ctx0 + t * ql
+        slots = []
+        for s in range(len(ql)):
+            for i in range(int(ql[s])):
+                pos = int(ctx[s]) - int(ql[s]) + i
+                slots.append(int(meta.block_tables[s, pos // 16]) * 16 + pos % 16)
+        per_step.append(workloads.StepMeta(**{**meta.__dict__, "context_lens": ctx.astype(np.int32),
+                                              "slot_mapping": np.array(slots, dtype=np.int32)}))
+    return meta, per_step
+
+
+def test_decode_chain_matches_oracle_every_step(pkv, cuda_device):
+    steps = 6
+    meta, per_step = _chain_case(steps)
+    _, _, _, pool = workloads.make_values(per_step[0])
+    vals = [workloads.make_values(m, seed=500 + t)[:3] for t, m in enumerate(per_step)]
+    # oracle: append then attend, step by step
+    pool_o = pool
+    want = []
+    for m, (q, k, v) in zip(per_step, vals):
+        out, pool_o = oracle.run_step(m, q, k, v, pool_o)
+        want.append(out)
+    # GPU: one chain plan, device-side advance between steps
+    dev = cuda_device
+    pd = pool.to(dev)
+    cu = torch.from_numpy(meta.cu_q_lens).to(dev)
+    ctx = torch.from_numpy(per_step[0].context_lens).to(dev)
+    slots = torch.from_numpy(per_step[0].slot_mapping).to(dev)
+    bt = torch.from_numpy(meta.block_tables).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    plan = pkv.plan_step(per_step[0].cu_q_lens, per_step[0].context_lens, 8, pd, chain_steps=steps)
+    outs = []
+    for t, (q, k, v) in enumerate(vals):
+        pkv.paged_kv_append(k.to(dev), v.to(dev), slots, pd, dev_status=status)
+        outs.append(pkv.paged_varlen_attention(q.to(dev), cu, ctx, bt, pd, meta.scale, plan=plan,
+                                               dev_status=status))
+        if t + 1 < steps:
+            pkv.decode_advance(ctx, slots, cu, bt, pd, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert np.array_equal(ctx.cpu().numpy(), per_step[-1].context_lens)
+    assert np.array_equal(slots.cpu().numpy(), per_step[-1].slot_mapping)
+    assert np.array_equal(bits(pd), pool_o)
+    for t in range(steps):
+        assert_close(outs[t].cpu(), want[t], f"chain step {t}")
+
+
+def test_decode_chain_graph_replay_matches_eager(pkv, cuda_device):
+    """The whole chain (append, attention, advance per step) captured once into a
+    CUDA graph, with the first step's lengths restored at its start, replays to
+    the same bits as the eager chain."""
+    steps = 4
+    meta, per_step = _chain_case(steps, seed=78)
+    _, _, _, pool = workloads.make_values(per_step[0])
+    dev = cuda_device
+    vals = [tuple(x.to(dev) for x in workloads.make_values(m, seed=600 + t)[:3])
+            for t, m in enumerate(per_step)]
+    cu = torch.from_numpy(meta.cu_q_lens).to(dev)
+    ctx0 = torch.from_numpy(per_step[0].context_lens).to(dev)
+    slots0 = torch.from_numpy(per_step[0].slot_mapping).to(dev)
+    bt = torch.from_numpy(meta.block_tables).to(dev)
+    plan = pkv.plan_step(per_step[0].cu_q_lens, per_step[0].context_lens, 8, pool.to(dev),
+                         chain_steps=steps)
+    ctx, slots = ctx0.clone(), slots0.clone()
+    outs = [torch.empty_like(v[0]) for v in vals]
+
+    def chain(pd):
+        ctx.copy_(ctx0)
+        slots.copy_(slots0)
+        for t, (q, k, v) in enumerate(vals):
+            pkv.paged_kv_append(k, v, slots, pd)
+            pkv.paged_varlen_attention(q, cu, ctx, bt, pd, meta.scale, plan=plan, out=outs[t])
+            if t + 1 < steps:
+                pkv.decode_advance(ctx, slots, cu, bt, pd)
+    pd_e = pool.to(dev)
+    chain(pd_e)
+    torch.cuda.synchronize()
+    eager = [o.clone() for o in outs]
+    pd_g = pool.to(dev)
+    s = torch.cuda.Stream(dev)
+    with torch.cuda.stream(s):
+        chain(pd_g)                          # warm-up on the capture stream
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        chain(pd_g)
+    for o in outs:
+        o.zero_()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    for t in range(steps):
+        assert torch.equal(outs[t], eager[t])
+    assert torch.equal(pd_g, pd_e)

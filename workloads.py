@@ -228,6 +228,41 @@ def wide_verify(seed=1241, num_seqs=64):
     return build_step("wide_verify", seed, ql, ctx, 32, 8, 128, rng=rng)
 
 
+def decode_chain(seed=1243, steps=8):
+    """The small-model decode batch run as a chain of `steps` decode steps in one
+    graph (the vllm-metal page's "Chained greedy decode", 4-8 tokens a chunk):
+    16 decodes, first-step contexts uniform in [512, 4096], 16 q / 8 KV heads,
+    D=128; block tables already hold the blocks of the last step.  Returns the
+    first step; each later step adds one token per sequence."""
+    rng = np.random.default_rng(seed)
+    ctx = rng.integers(512, 4096, size=16, endpoint=True).astype(np.int32)
+    last = build_step("decode_chain", seed, [1] * 16, ctx + (steps - 1), 16, 8, 128, rng=rng,
+                      notes=f"chain_steps={steps}")
+    return chain_step(last, ctx, 0)
+
+
+def chain_step(last: StepMeta, ctx0, t: int) -> StepMeta:
+    """Step t of a decode chain whose last step is `last` and whose first-step
+    contexts are ctx0: contexts ctx0 + t * q_len, slots of the new positions."""
+    ctx = (np.asarray(ctx0, dtype=np.int32) + t * last.q_lens).astype(np.int32)
+    slots = []
+    for s in range(last.num_seqs):
+        for i in range(int(last.q_lens[s])):
+            pos = int(ctx[s]) - int(last.q_lens[s]) + i
+            slots.append(int(last.block_tables[s, pos // last.block_size]) * last.block_size +
+                         pos % last.block_size)
+    return StepMeta(**{**last.__dict__, "context_lens": ctx,
+                       "slot_mapping": np.array(slots, dtype=np.int32)})
+
+
+def chain_steps(meta: StepMeta) -> int:
+    """Chain length recorded in a chained workload's notes (1 for a single step)."""
+    for tok in meta.notes.split():
+        if tok.startswith("chain_steps="):
+            return int(tok.split("=", 1)[1])
+    return 1
+
+
 CONFIGS = {
     "tiny_decode": tiny_decode,
     "small_decode": small_decode,
@@ -237,6 +272,7 @@ CONFIGS = {
     "long_context_mix": long_context_mix,
     "mtp_draft": mtp_draft,
     "wide_verify": wide_verify,
+    "decode_chain": decode_chain,
 }
 
 
