@@ -323,11 +323,12 @@ def bench_pkv(args):
 
     chain_arg = nch if nch > 1 else None
     info, host_plan = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, pool,
-                                    upload=False, chain_steps=chain_arg)
+                                    upload=False, chain_steps=chain_arg,
+                                    block_tables=meta.block_tables)
     t0 = time.perf_counter()
     for _ in range(50):
         pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, pool, upload=False,
-                      chain_steps=chain_arg)
+                      chain_steps=chain_arg, block_tables=meta.block_tables)
     host_plan_us = (time.perf_counter() - t0) / 50 * 1e6
     plan_pinned = torch.from_numpy(host_plan.view(np.uint8)).pin_memory()
     plan = pkv.StepPlan(info, host_plan, dev)
@@ -439,7 +440,8 @@ def bench_pkv(args):
                 for dst, src in zip(dqkv, hqkv):
                     dst.copy_(src, non_blocking=True)
             inf2, hp2 = pkv.plan_step(host["cu"].numpy(), host["ctx"].numpy(), meta.num_q_heads, pool,
-                                      upload=False, chain_steps=chain_arg)
+                                      upload=False, chain_steps=chain_arg,
+                                      block_tables=host["bt"].numpy())
             pp = torch.from_numpy(hp2.view(np.uint8))
             plan.dev[:pp.numel()].copy_(pp, non_blocking=False)
             plan.info = inf2

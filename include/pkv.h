@@ -204,6 +204,22 @@ PKV_API pkv_status pkv_plan_decode_chain(const int32_t *cu_q_lens, const int32_t
                                          void *plan, int64_t plan_capacity, pkv_plan_info *info);
 
 /*
+ * The general form of pkv_plan_step / pkv_plan_decode_chain: steps = 1 is a
+ * single step, steps > 1 a decode chain.  block_tables, when not NULL, is a
+ * HOST copy of the step's block tables ([num_seqs][max_blocks_per_seq] int32,
+ * the same entries the device copy holds): the plan then also carries the
+ * physical ids of the first blocks each split-KV warp reads, so its first copies
+ * start without waiting for a block-table read.  The attention kernel checks
+ * those ids against the device block tables and reports a disagreement as
+ * PKV_DEV_PLAN_MISMATCH.
+ */
+PKV_API pkv_status pkv_plan_step_ex(const int32_t *cu_q_lens, const int32_t *context_lens,
+                                    int32_t num_seqs, int32_t num_q_heads,
+                                    const pkv_pool_desc *desc, int32_t num_sms, int32_t steps,
+                                    const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                    void *plan, int64_t plan_capacity, pkv_plan_info *info);
+
+/*
  * Device-side move to the next step of a decode chain: for every sequence s
  * with q = cu_q_lens[s+1] - cu_q_lens[s] > 0, context_lens[s] += q and
  * slot_mapping[cu_q_lens[s] + i] = the pool slot of position

@@ -97,6 +97,9 @@ def _load():
             lib.pkv_plan_decode_chain.argtypes = [P, P, i32, i32, ctypes.POINTER(PoolDesc), i32,
                                                   i32, P, i64, ctypes.POINTER(PlanInfo)]
             lib.pkv_plan_decode_chain.restype = i32
+            lib.pkv_plan_step_ex.argtypes = [P, P, i32, i32, ctypes.POINTER(PoolDesc), i32, i32,
+                                             P, i32, P, i64, ctypes.POINTER(PlanInfo)]
+            lib.pkv_plan_step_ex.restype = i32
             lib.pkv_decode_advance.argtypes = [P, P, P, P, i32, i32, ctypes.POINTER(PoolDesc), P,
                                                P]
             lib.pkv_decode_advance.restype = i32
@@ -249,11 +252,14 @@ class _nullcontext:
 
 
 def plan_step(cu_q_lens, context_lens, num_q_heads: int, kv_pool_or_desc, *, num_sms=None,
-              device=None, upload=True, stream=None, chain_steps=None) -> StepPlan | tuple:
-    """Build the host plan for one step (pkv_plan_step) and upload it.
+              device=None, upload=True, stream=None, chain_steps=None,
+              block_tables=None) -> StepPlan | tuple:
+    """Build the host plan for one step (pkv_plan_step_ex) and upload it.
 
     cu_q_lens / context_lens: host arrays or tensors (copied to the host if on a GPU).
-    chain_steps: plan a chain of that many decode steps instead (pkv_plan_decode_chain).
+    chain_steps: plan a chain of that many decode steps instead.
+    block_tables: the step's block tables (host copy) -- lets the plan carry each
+    split-KV warp's first block ids (checked on the device against the tables).
     Returns a StepPlan (or (info, host_bytes) when upload=False).
     """
     desc = kv_pool_or_desc if isinstance(kv_pool_or_desc, PoolDesc) else pool_desc(kv_pool_or_desc)
@@ -268,14 +274,20 @@ def plan_step(cu_q_lens, context_lens, num_q_heads: int, kv_pool_or_desc, *, num
                    if torch.cuda.is_available() else 152)
     info = PlanInfo()
     lib = _load()
-    name = "pkv_plan_step" if chain_steps is None else "pkv_plan_decode_chain"
+    name = "pkv_plan_step_ex"
+    bt = None
+    if block_tables is not None:
+        bt = _host_i32(block_tables)
+        if bt.ndim != 2 or bt.shape[0] != ctx.shape[0]:
+            raise ValueError("block_tables must be [num_seqs, max_blocks_per_seq]")
 
     def call(buf, cap):
-        args = [cu.ctypes.data_as(ctypes.c_void_p), ctx.ctypes.data_as(ctypes.c_void_p),
-                ctx.shape[0], int(num_q_heads), ctypes.byref(desc), int(num_sms)]
-        if chain_steps is not None:
-            args.append(int(chain_steps))
-        return getattr(lib, name)(*args, buf, cap, ctypes.byref(info))
+        return lib.pkv_plan_step_ex(
+            cu.ctypes.data_as(ctypes.c_void_p), ctx.ctypes.data_as(ctypes.c_void_p), ctx.shape[0],
+            int(num_q_heads), ctypes.byref(desc), int(num_sms),
+            1 if chain_steps is None else int(chain_steps),
+            None if bt is None else bt.ctypes.data_as(ctypes.c_void_p),
+            0 if bt is None else bt.shape[1], buf, cap, ctypes.byref(info))
     st = call(None, 0)
     if st:
         raise PkvError(st, name)

@@ -171,7 +171,7 @@ extern "C" pkv_status pkv_paged_varlen_attention(
                                        info->num_merge_groups, info->num_prefill_tiles,
                                        info->num_prefill_ctas);
   a.warp_begin = reinterpret_cast<const int32_t *>(pb + off.warp_begin);
-  a.warp_first = reinterpret_cast<const Piece *>(pb + off.warp_first);
+  a.warp_head = reinterpret_cast<const WarpHead *>(pb + off.warp_head);
   a.num_decode_warps = info->num_decode_warps;
   a.pieces = reinterpret_cast<const Piece *>(pb + off.pieces);
   a.merge_groups = reinterpret_cast<const MergeGroup *>(pb + off.merges);

@@ -62,7 +62,7 @@ struct DecodeParams {
   const int32_t *context_lens;
   const int32_t *block_tables;
   const int32_t *warp_begin;
-  const Piece *warp_first;
+  const WarpHead *warp_head;
   const Piece *pieces;
   const MergeGroup *merges;
   float *part_o;
@@ -218,7 +218,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int pb = has_warp ? __ldg(p.warp_begin + gw) : 0;
   const int pe = has_warp ? __ldg(p.warp_begin + gw + 1) : 0;
   Piece pp;
-  if (has_warp) pp = p.warp_first[gw];  // == pieces[pb], loaded beside the range
+  int fb0 = -1, fb1 = -1, fb2 = -1;  // physical ids of the first piece's first blocks, if known
+  if (has_warp) {
+    const WarpHead &wh = p.warp_head[gw];  // pp == pieces[pb], loaded beside the range
+    pp = wh.first;
+    fb0 = wh.blk[0];
+    fb1 = wh.blk[1];
+    fb2 = wh.blk[2];
+  }
   const int hkv = p.num_kv_heads;
   const int G = p.group;
   int win_base = 0, win_val = -1;  // table window: lane i holds entry win_base + i
@@ -257,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   // read 32 entries at a time with one coalesced warp load and the entries are
   // shuffled out, so refilling a stage never waits on a dependent global load.
   const Piece first = pp;  // the producer below moves pp ahead of the consumer
+  const int win_first = win_val;  // first window, kept to check the inline block ids
   int ppi = pb, pkb = pp.kb_begin, issued = 0;
   auto issue_next = [&](int stage) {
     while (ppi < pe && pkb >= pp.kb_end) {
@@ -286,7 +294,12 @@ __global__ void __launch_bounds__(kThreads, 2)
                     : -1;
       win_ok = true;
     }
-    const int phys = __shfl_sync(0xffffffffu, win_val, (pkb - win_base) & 31);
+    // the first copies use the block ids the plan carries, so they do not wait
+    // for the block-table window (checked against it once data has arrived)
+    const int inl = ppi == pb && issued < kHeadBlocks
+                        ? (issued == 0 ? fb0 : issued == 1 ? fb1 : fb2)
+                        : -1;
+    const int phys = inl >= 0 ? inl : __shfl_sync(0xffffffffu, win_val, (pkb - win_base) & 31);
     const bool ok = in_table && phys >= 0 && phys < p.num_blocks;
     if (lane == 0) {
       stage_ok[stage] = ok ? 1 : 0;
@@ -375,6 +388,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         break;
       }
       ++consumed;
+      if (consumed == 1) {  // the first window has landed by now: check the inline ids
+        const int want = lane == 0 ? fb0 : lane == 1 ? fb1 : lane == 2 ? fb2 : -1;
+        if (want >= 0 && want != win_first) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
+      }
       if (valid && stage_ok[stage]) {
         const uint32_t sK = smem_u32(ring + stage * C::kStageBytes);
         const uint32_t sV = sK + C::kSlabBytes;
@@ -567,7 +584,7 @@ DecodeParams make_params(const AttnArgs &a) {
   p.context_lens = a.context_lens;
   p.block_tables = a.block_tables;
   p.warp_begin = a.warp_begin;
-  p.warp_first = a.warp_first;
+  p.warp_head = a.warp_head;
   p.pieces = a.pieces;
   p.merges = a.merge_groups;
   p.part_o = a.part_o;

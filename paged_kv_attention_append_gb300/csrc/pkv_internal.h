@@ -17,8 +17,10 @@ constexpr int kDecodeWarpsPerCta = 4;
 // Plan buffer layout (all offsets are functions of the counts):
 //   [PlanHeader 64 B]
 //   [warp_begin: int32 x (num_decode_warps + 1), padded to 32 B]
-//   [warp_first: Piece x num_decode_warps] (copy of each warp's first piece, so a
-//    warp reads its range and first piece with two independent loads)
+//   [warp_head: WarpHead x num_decode_warps] (each warp's first piece and, when
+//    the planner was given the host block tables, its first blocks' physical
+//    ids: a warp reads its range and head with two independent loads and can
+//    start its first copies without waiting for a block-table read)
 //   [Piece x num_decode_pieces][MergeGroup x num_merge_groups]
 //   [prefill_begin: int32 x (num_prefill_ctas + 1), padded to 32 B; absent when 0 CTAs]
 //   [PrefillTile x num_prefill_tiles, grouped by CTA]
@@ -53,6 +55,16 @@ struct Piece {
   int32_t q_row0;    // packed query index of token qi0 (cu_q_lens[seq] + qi0)
 };
 static_assert(sizeof(Piece) == 32, "piece is 32 bytes");
+
+// Per-warp head of the split-KV work: a copy of the warp's first piece, and
+// the physical block ids of that piece's first kHeadBlocks blocks (-1 where not
+// known at planning time or past the piece).
+constexpr int kHeadBlocks = 3;
+struct WarpHead {
+  Piece first;
+  int32_t blk[4];
+};
+static_assert(sizeof(WarpHead) == 48, "warp head is 48 bytes");
 
 // A set of nsplit partial results (slots part0 .. part0+nsplit-1) to combine.
 // kind 0: a decode segment -- rows are n_q tokens x the group's heads of KV
@@ -94,14 +106,14 @@ static_assert(sizeof(PrefillTile) == 48, "prefill tile is 48 bytes");
 inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
 struct PlanOffsets {
-  int64_t warp_begin, warp_first, pieces, merges, prefill_begin, prefill, total;
+  int64_t warp_begin, warp_head, pieces, merges, prefill_begin, prefill, total;
 };
 inline PlanOffsets plan_offsets(int32_t n_warps, int32_t n_pieces, int32_t n_merge,
                                 int32_t n_prefill, int32_t n_prefill_ctas) {
   PlanOffsets o;
   o.warp_begin = (int64_t)sizeof(PlanHeader);
-  o.warp_first = o.warp_begin + align_up(4ll * (n_warps + 1), 32);
-  o.pieces = o.warp_first + (int64_t)n_warps * (int64_t)sizeof(Piece);
+  o.warp_head = o.warp_begin + align_up(4ll * (n_warps + 1), 32);
+  o.pieces = o.warp_head + (int64_t)n_warps * (int64_t)sizeof(WarpHead);
   o.merges = o.pieces + (int64_t)n_pieces * (int64_t)sizeof(Piece);
   o.prefill_begin = o.merges + (int64_t)n_merge * (int64_t)sizeof(MergeGroup);
   o.prefill = o.prefill_begin + (n_prefill_ctas > 0 ? align_up(4ll * (n_prefill_ctas + 1), 32) : 0);
@@ -149,7 +161,7 @@ struct AttnArgs {
   int64_t total_q;
   float scale;
   const int32_t *warp_begin;
-  const Piece *warp_first;
+  const WarpHead *warp_head;
   int32_t num_decode_warps;
   const Piece *pieces;
   const MergeGroup *merge_groups;

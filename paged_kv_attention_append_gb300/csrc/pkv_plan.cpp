@@ -82,9 +82,12 @@ using namespace pkv;
 // (chained decode): every sequence then gains its q_len tokens per step, so the
 // decode segments are sized for context + lookahead * q_len; prefill-class
 // sequences are not supported there.
+// block_tables (host, may be NULL): each warp's first blocks are then written
+// into its head.
 static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_lens,
                             int32_t num_seqs, int32_t num_q_heads, const pkv_pool_desc *desc,
-                            int32_t num_sms, int32_t lookahead, void *plan, int64_t plan_capacity,
+                            int32_t num_sms, int32_t lookahead, const int32_t *block_tables,
+                            int32_t max_blocks_per_seq, void *plan, int64_t plan_capacity,
                             pkv_plan_info *info) {
   if (!info) return PKV_ERR_NULL;
   if (lookahead < 0) return PKV_ERR_RANGE;
@@ -417,9 +420,18 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   h.max_blocks_needed = max_nb;
   std::memcpy(p, &h, sizeof h);
   std::memcpy(p + off.warp_begin, warp_begin.data(), warp_begin.size() * sizeof(int32_t));
-  for (int32_t w = 0; w < num_warps; ++w)
-    std::memcpy(p + off.warp_first + (int64_t)w * sizeof(Piece), &pieces[warp_begin[w]],
-                sizeof(Piece));
+  for (int32_t w = 0; w < num_warps; ++w) {
+    WarpHead wh;
+    std::memset(&wh, 0, sizeof wh);
+    wh.first = pieces[warp_begin[w]];
+    for (int i = 0; i < 4; ++i) {
+      const int32_t kb = wh.first.kb_begin + i;
+      wh.blk[i] = -1;
+      if (i < kHeadBlocks && block_tables && kb < wh.first.kb_end && kb < max_blocks_per_seq)
+        wh.blk[i] = block_tables[(int64_t)wh.first.seq * max_blocks_per_seq + kb];
+    }
+    std::memcpy(p + off.warp_head + (int64_t)w * sizeof(WarpHead), &wh, sizeof wh);
+  }
   if (!pieces.empty()) std::memcpy(p + off.pieces, pieces.data(), pieces.size() * sizeof(Piece));
   if (!merges.empty())
     std::memcpy(p + off.merges, merges.data(), merges.size() * sizeof(MergeGroup));
@@ -430,12 +442,23 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   return PKV_OK;
 }
 
+extern "C" pkv_status pkv_plan_step_ex(const int32_t *cu_q_lens, const int32_t *context_lens,
+                                       int32_t num_seqs, int32_t num_q_heads,
+                                       const pkv_pool_desc *desc, int32_t num_sms, int32_t steps,
+                                       const int32_t *block_tables, int32_t max_blocks_per_seq,
+                                       void *plan, int64_t plan_capacity, pkv_plan_info *info) {
+  if (steps < 1) return PKV_ERR_RANGE;
+  if (block_tables && max_blocks_per_seq < 0) return PKV_ERR_SHAPE;
+  return plan_impl(cu_q_lens, context_lens, num_seqs, num_q_heads, desc, num_sms, steps - 1,
+                   block_tables, max_blocks_per_seq, plan, plan_capacity, info);
+}
+
 extern "C" pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *context_lens,
                                     int32_t num_seqs, int32_t num_q_heads,
                                     const pkv_pool_desc *desc, int32_t num_sms, void *plan,
                                     int64_t plan_capacity, pkv_plan_info *info) {
-  return plan_impl(cu_q_lens, context_lens, num_seqs, num_q_heads, desc, num_sms, 0, plan,
-                   plan_capacity, info);
+  return plan_impl(cu_q_lens, context_lens, num_seqs, num_q_heads, desc, num_sms, 0, nullptr, 0,
+                   plan, plan_capacity, info);
 }
 
 extern "C" pkv_status pkv_plan_decode_chain(const int32_t *cu_q_lens, const int32_t *context_lens,
@@ -443,7 +466,6 @@ extern "C" pkv_status pkv_plan_decode_chain(const int32_t *cu_q_lens, const int3
                                             const pkv_pool_desc *desc, int32_t num_sms,
                                             int32_t steps, void *plan, int64_t plan_capacity,
                                             pkv_plan_info *info) {
-  if (steps < 1) return PKV_ERR_RANGE;
-  return plan_impl(cu_q_lens, context_lens, num_seqs, num_q_heads, desc, num_sms, steps - 1, plan,
-                   plan_capacity, info);
+  return pkv_plan_step_ex(cu_q_lens, context_lens, num_seqs, num_q_heads, desc, num_sms, steps,
+                          nullptr, 0, plan, plan_capacity, info);
 }

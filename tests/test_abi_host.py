@@ -47,7 +47,7 @@ def parse_plan(info, host):
                         info.num_prefill_tiles)
     off_w = 16
     off_first = off_w + ((nw + 1 + 7) // 8) * 8
-    off_p = off_first + 8 * nw
+    off_p = off_first + 12 * nw
     off_m = off_p + 8 * npc
     ncta = info.num_prefill_ctas
     off_b = off_m + 8 * nm
@@ -55,9 +55,9 @@ def parse_plan(info, host):
     assert info.plan_bytes == 4 * (off_f + 12 * npf)
     wb = words[off_w:off_w + nw + 1]
     pieces = words[off_p:off_m].reshape(npc, 8)
-    first = words[off_first:off_p].reshape(nw, 8)
+    heads = words[off_first:off_p].reshape(nw, 12)
     if nw:
-        assert np.array_equal(first, pieces[wb[:-1]])  # each warp's first piece, copied
+        assert np.array_equal(heads[:, :8], pieces[wb[:-1]])  # each warp's first piece, copied
     mer = words[off_m:off_b].reshape(nm, 8)
     pre = words[off_f:off_f + 12 * npf].reshape(npf, 12)
     pb = words[off_b:off_b + ncta + 1] if ncta else np.zeros(1, np.int32)
@@ -323,3 +323,23 @@ def test_decode_chain_plan_covers_the_last_step(pkv):
     with pytest.raises(pkv.PkvError):
         pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, desc, upload=False,
                       chain_steps=0)
+
+
+def test_plan_carries_first_block_ids_when_given_the_tables(pkv):
+    meta = workloads.small_decode()
+    desc = pkv.PoolDesc(meta.num_blocks, 16, meta.num_kv_heads, meta.head_dim)
+    info, host = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, desc,
+                               num_sms=152, upload=False, block_tables=meta.block_tables)
+    info0, host0 = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, desc,
+                                 num_sms=152, upload=False)
+    nw = info.num_decode_warps
+    off = 16 + ((nw + 1 + 7) // 8) * 8
+    heads = host.view(np.int32)[off:off + 12 * nw].reshape(nw, 12)
+    heads0 = host0.view(np.int32)[off:off + 12 * nw].reshape(nw, 12)
+    assert np.array_equal(heads[:, :8], heads0[:, :8]) and np.all(heads0[:, 8:] == -1)
+    for w in range(nw):
+        seq, kb0, kb1 = heads[w, 0], heads[w, 4], heads[w, 5]
+        for i in range(3):
+            want = meta.block_tables[seq, kb0 + i] if kb0 + i < kb1 else -1
+            assert heads[w, 8 + i] == want
+        assert heads[w, 11] == -1

@@ -446,3 +446,35 @@ def test_decode_chain_graph_replay_matches_eager(pkv, cuda_device):
     for t in range(steps):
         assert torch.equal(outs[t], eager[t])
     assert torch.equal(pd_g, pd_e)
+
+
+def test_plan_with_block_tables_same_result_and_mismatch_reported(pkv, cuda_device):
+    """A plan that carries the first block ids (from the host tables) gives the
+    same bits as one that does not; host tables that disagree with the device
+    copy are reported as a plan mismatch (the ids are range-checked first, so
+    only in-pool blocks are read)."""
+    meta = workloads.small_decode()
+    q, k, v, pool = workloads.make_values(meta)
+    dev = cuda_device
+    pd = pool.to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    pkv.paged_kv_append(k.to(dev), v.to(dev), torch.from_numpy(meta.slot_mapping).to(dev), pd,
+                        dev_status=status)
+    bt = torch.from_numpy(meta.block_tables).to(dev)
+    qd = q.to(dev)
+    outs = []
+    for tables in (None, meta.block_tables):
+        plan = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, pd,
+                             block_tables=tables)
+        outs.append(pkv.paged_varlen_attention(qd, meta.cu_q_lens, meta.context_lens, bt, pd,
+                                               meta.scale, plan=plan, dev_status=status))
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(outs[0], outs[1])
+    wrong = np.roll(meta.block_tables, 1, axis=0)          # other sequences' blocks
+    plan = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, pd,
+                         block_tables=wrong)
+    pkv.paged_varlen_attention(qd, meta.cu_q_lens, meta.context_lens, bt, pd, meta.scale,
+                               plan=plan, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 4      # PKV_DEV_PLAN_MISMATCH
