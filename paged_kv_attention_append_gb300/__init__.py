@@ -251,6 +251,9 @@ class _nullcontext:
         return False
 
 
+_plan_scratch = np.zeros(1 << 18, dtype=np.int32)   # 1 MiB, grown on demand
+
+
 def plan_step(cu_q_lens, context_lens, num_q_heads: int, kv_pool_or_desc, *, num_sms=None,
               device=None, upload=True, stream=None, chain_steps=None,
               block_tables=None) -> StepPlan | tuple:
@@ -288,13 +291,16 @@ def plan_step(cu_q_lens, context_lens, num_q_heads: int, kv_pool_or_desc, *, num
             1 if chain_steps is None else int(chain_steps),
             None if bt is None else bt.ctypes.data_as(ctypes.c_void_p),
             0 if bt is None else bt.shape[1], buf, cap, ctypes.byref(info))
-    st = call(None, 0)
+    # one planning pass into a reused buffer (grown and redone only when a plan
+    # outgrows it), then a copy of the plan's bytes
+    global _plan_scratch
+    st = call(_plan_scratch.ctypes.data_as(ctypes.c_void_p), _plan_scratch.nbytes)
+    if st == 5 and int(info.plan_bytes) > _plan_scratch.nbytes:   # PKV_ERR_WORKSPACE
+        _plan_scratch = np.zeros((int(info.plan_bytes) * 2 + 15) // 16 * 4, dtype=np.int32)
+        st = call(_plan_scratch.ctypes.data_as(ctypes.c_void_p), _plan_scratch.nbytes)
     if st:
         raise PkvError(st, name)
-    host = np.zeros((max(int(info.plan_bytes), 16) + 15) // 16 * 4, dtype=np.int32)
-    st = call(host.ctypes.data_as(ctypes.c_void_p), host.nbytes)
-    if st:
-        raise PkvError(st, name)
+    host = _plan_scratch[:(max(int(info.plan_bytes), 16) + 15) // 16 * 4].copy()
     if not upload:
         return info, host
     return StepPlan(info, host, torch.device(device), stream)

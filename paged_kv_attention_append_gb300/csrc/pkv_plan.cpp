@@ -177,6 +177,8 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   std::vector<int32_t> warp_begin(num_warps + 1, 0);
   std::vector<Piece> pieces;
   std::vector<int32_t> piece_seg;
+  pieces.reserve(segs.size() + num_warps);  // a range adds at most one piece beyond its segments
+  piece_seg.reserve(segs.size() + num_warps);
   {
     // Equal cost, not equal blocks: a block costs kBlockCost and starting a
     // segment (its q rows and lengths, a fresh table window) costs kPieceCost, so
@@ -188,18 +190,27 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
     constexpr int64_t kBlockCost = 2, kPieceCost = 3;
     const int64_t total_cost = kBlockCost * total_blocks + kPieceCost * (int64_t)segs.size();
     std::vector<int64_t> cut(num_warps + 1, total_blocks);  // first block of each warp
+    cut[0] = 0;
     {
-      int64_t blk = 0, cost = 0;
-      int32_t w = 0;
-      cut[0] = 0;
+      // warp w >= 1 starts at the first block whose midpoint m satisfies
+      // m * num_warps >= w * total_cost; the midpoints of a segment starting at
+      // cost c are c + kPieceCost + kBlockCost * i + kBlockCost / 2, so each
+      // boundary is found with one division per warp, not a walk over blocks
+      int64_t cost = 0, blk = 0;
+      int32_t w = 1;
       for (const Segment &g : segs) {
-        cost += kPieceCost;
-        for (int32_t i = 0; i < g.nb; ++i, ++blk, cost += kBlockCost) {
-          const int64_t owner = (cost + kBlockCost / 2) * num_warps / total_cost;
-          while (w < owner && w < num_warps) cut[++w] = blk;
+        const int64_t first_mid = cost + kPieceCost + kBlockCost / 2;
+        const int64_t last_mid = first_mid + kBlockCost * (g.nb - 1);
+        while (w < num_warps && last_mid * num_warps >= (int64_t)w * total_cost) {
+          const int64_t need = (int64_t)w * total_cost - first_mid * num_warps;  // >= 2i * nw
+          int64_t i = need <= 0 ? 0 : (need + kBlockCost * num_warps - 1) / (kBlockCost * num_warps);
+          if (i > g.nb - 1) i = g.nb - 1;
+          cut[w++] = blk + i;
         }
+        cost += kPieceCost + kBlockCost * g.nb;
+        blk += g.nb;
       }
-      while (w < num_warps) cut[++w] = total_blocks;
+      while (w < num_warps) cut[w++] = total_blocks;
     }
     size_t k = 0;
     int64_t seg_off = 0;  // global block offset of segment k
