@@ -86,9 +86,14 @@ struct DecodeParams {
   int64_t pool_bytes;
 };
 
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {
-  // byte offset of 16-byte chunk `chunk` (0..7) of row `row` in a 128B-swizzled box
-  return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
+// Byte offset of 16-byte chunk `chunk` (0 .. D/8-1) of key row `row` (0..15) of
+// a paged block as one 4-D TMA box lands it: [8-row group][64-column half]
+// [8 rows][128 B], 128-byte swizzled (the 16-byte chunk index XOR the row within
+// its 8-row atom).
+template <int kHalves>
+__device__ __forceinline__ uint32_t blk_off(int row, int chunk) {
+  return (uint32_t)((((row >> 3) * kHalves + (chunk >> 3)) << 10) + ((row & 7) << 7) +
+                    (((chunk & 7) ^ (row & 7)) << 4));
 }
 
 template <int D>
@@ -309,10 +314,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int row_v = row_k + hkv * kBlockSize;
         const uint32_t dst = smem_u32(ring + stage * C::kStageBytes);
 #pragma unroll
-        for (int hh = 0; hh < C::kHalves; ++hh) {
-          tma_load_2d(dst + hh * kBoxBytes, &pool_map, hh * 64, row_k, bar);
-          tma_load_2d(dst + C::kSlabBytes + hh * kBoxBytes, &pool_map, hh * 64, row_v, bar);
-        }
+        // one 4-D box per slab: the whole block of one head (rows / 8 = group coordinate)
+        tma_load_4d(dst, &pool_map, 0, 0, 0, row_k >> 3, bar);
+        tma_load_4d(dst + C::kSlabBytes, &pool_map, 0, 0, 0, row_v >> 3, bar);
       } else {
         report(p.dev_status, in_table ? PKV_DEV_BAD_BLOCK : PKV_DEV_PLAN_MISMATCH);
         mbar_arrive(bar);  // complete the phase without data; the block is skipped
@@ -404,7 +408,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
           for (int L = 0; L < kL; ++L) {
             const int e = 8 * (L >> 1) + 2 * c + (L & 1);
-            const uint4 kv = lds128(sK + (e >> 3) * kBoxBytes + swz(t, e & 7));
+            const uint4 kv = lds128(sK + blk_off<C::kHalves>(t, e));
             mma_16816(s[nt], qa[2 * L][0], qa[2 * L][1], qa[2 * L][2], qa[2 * L][3], kv.x, kv.y);
             mma_16816(s[nt], qa[2 * L + 1][0], qa[2 * L + 1][1], qa[2 * L + 1][2],
                       qa[2 * L + 1][3], kv.z, kv.w);
@@ -463,11 +467,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         // O += P V: lane (r, c) reads keys 2c, 2c+1, 2c+8, 2c+9 at head_dim chunk r (+8 per half)
 #pragma unroll
         for (int hh = 0; hh < C::kHalves; ++hh) {
-          const uint32_t base = sV + hh * kBoxBytes;
-          const uint4 v0 = lds128(base + swz(2 * c, r));
-          const uint4 v1 = lds128(base + swz(2 * c + 1, r));
-          const uint4 v2 = lds128(base + swz(2 * c + 8, r));
-          const uint4 v3 = lds128(base + swz(2 * c + 9, r));
+          const int ch = hh * 8 + r;  // head_dim chunk
+          const uint4 v0 = lds128(sV + blk_off<C::kHalves>(2 * c, ch));
+          const uint4 v1 = lds128(sV + blk_off<C::kHalves>(2 * c + 1, ch));
+          const uint4 v2 = lds128(sV + blk_off<C::kHalves>(2 * c + 8, ch));
+          const uint4 v3 = lds128(sV + blk_off<C::kHalves>(2 * c + 9, ch));
           const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w};
           const uint32_t w1[4] = {v1.x, v1.y, v1.z, v1.w};
           const uint32_t w2[4] = {v2.x, v2.y, v2.z, v2.w};
@@ -635,12 +639,16 @@ int make_pool_map(void *map_out, const void *pool, const pkv_pool_desc &desc) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return (int)cudaErrorNotSupported;
   CUtensorMap *map = static_cast<CUtensorMap *>(map_out);
-  const uint64_t rows = (uint64_t)desc.num_blocks * 2 * desc.num_kv_heads * kBlockSize;
-  cuuint64_t dims[2] = {(cuuint64_t)desc.head_dim, (cuuint64_t)(rows > 0 ? rows : 1)};
-  cuuint64_t strides[1] = {(cuuint64_t)desc.head_dim * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)kBlockSize};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(pool), dims, strides,
+  // rows of D bf16 ([num_blocks][2][Hkv][16] rows) seen as (64 columns, 8 rows,
+  // D/64 column halves, row groups of 8) with strides (2D, 128, 16D) bytes: a box
+  // (64, 8, D/64, 2) is one paged block of one head
+  const int d = desc.head_dim, halves = d / 64;
+  const int64_t rows = (int64_t)desc.num_blocks * 2 * desc.num_kv_heads * kBlockSize;
+  cuuint64_t dims[4] = {64, 8, (cuuint64_t)halves, (cuuint64_t)(rows > 0 ? rows / 8 : 1)};
+  cuuint64_t strides[3] = {(cuuint64_t)d * 2, 128, (cuuint64_t)d * 2 * 8};
+  cuuint32_t box[4] = {64, 8, (cuuint32_t)halves, 2};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(pool), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;

@@ -193,8 +193,9 @@ int launch_decode(const AttnArgs &a, int *launches);
 int launch_merge(const AttnArgs &a, int *launches);
 int launch_prefill(const AttnArgs &a, int *launches);
 
-// 2D TMA view of the pool (rows of head_dim bf16, box 16 x 64, 128B swizzle);
-// `map` points to a CUtensorMap.
+// 4-D TMA view of the pool whose box is one paged block of one head, landing
+// as [8-row group][64-column half][8 rows][128 B], 128-byte swizzled; `map`
+// points to a CUtensorMap.
 int make_pool_map(void *map, const void *pool, const pkv_pool_desc &desc);
 
 void count_launches(int n);

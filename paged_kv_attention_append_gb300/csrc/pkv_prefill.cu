@@ -110,14 +110,6 @@ struct PrefillParams {
   float scale_log2;
 };
 
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *m, int32_t c0,
-                                            int32_t c1, int32_t c2, int32_t c3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
-      : "memory");
-}
 
 // One work item's metadata, computed identically by every role (so every role
 // skips the same invalid items and agrees on all barrier phases).
@@ -620,26 +612,6 @@ int make_q_map(CUtensorMap *map, const void *q, int64_t total_q, int hq, int d) 
   return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;
 }
 
-// 4-D view of the pool for whole paged blocks: the pool is rows of D bf16
-// ([num_blocks][2][Hkv][16] rows); dimensions (64 columns, 8 rows of a group,
-// kHalves column halves, row groups of 8), strides (2D, 128, 16D) bytes.  A box
-// (64, 8, kHalves, 2) is one paged block of one head and lands in shared memory
-// as [group][half][8 rows][128 B], 128-byte swizzled.
-int make_kv_map(CUtensorMap *map, const void *pool, const pkv_pool_desc &desc) {
-  EncodeTiledFn enc = encoder();
-  if (!enc) return (int)cudaErrorNotSupported;
-  const int d = desc.head_dim, halves = d / 64;
-  const int64_t rows = (int64_t)desc.num_blocks * 2 * desc.num_kv_heads * kBlockSize;
-  cuuint64_t dims[4] = {64, 8, (cuuint64_t)halves, (cuuint64_t)(rows > 0 ? rows / 8 : 1)};
-  cuuint64_t strides[3] = {(cuuint64_t)d * 2, 128, (cuuint64_t)d * 2 * 8};
-  cuuint32_t box[4] = {64, 8, (cuuint32_t)halves, 2};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(pool), dims,
-                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? 0 : (int)cudaErrorInvalidValue;
-}
-
 template <int D>
 int launch_prefill_t(const AttnArgs &a, const CUtensorMap &qmap, const CUtensorMap &kvmap) {
   using C = PrefillCfg<D>;
@@ -679,7 +651,7 @@ int launch_prefill(const AttnArgs &a, int *launches) {
   CUtensorMap qmap, kvmap;
   int e = make_q_map(&qmap, a.q, a.total_q, a.num_q_heads, a.desc.head_dim);
   if (e) return e;
-  e = make_kv_map(&kvmap, a.kv_pool, a.desc);
+  e = make_pool_map(&kvmap, a.kv_pool, a.desc);
   if (e) return e;
   e = a.desc.head_dim == 128 ? launch_prefill_t<128>(a, qmap, kvmap)
                              : launch_prefill_t<64>(a, qmap, kvmap);
