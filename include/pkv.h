@@ -112,6 +112,9 @@ typedef struct pkv_plan_info {
   int32_t num_prefill_merges;   /* prefill merge groups (the last ones of num_merge_groups) */
   int32_t lookahead;            /* further decode steps the plan stays valid for (chained
                                    decode, pkv_plan_decode_chain); 0 for a single step */
+  int32_t num_shared_ctas;      /* split-KV CTAs that read a prefix several sequences share
+                                   once for up to 4 row groups (needs host block tables) */
+  int32_t reserved;
   int64_t kv_tokens;         /* sum of context_lens over sequences with q_len > 0 */
   int64_t decode_blocks;     /* (KV block, KV head) pairs streamed by the split-KV kernel */
   int64_t plan_bytes;        /* bytes of the plan buffer (host, then device copy) */

@@ -51,7 +51,9 @@ struct DecodeCfg {
   static constexpr int kStageBytes = 2 * kSlabBytes;
   static constexpr int kRingBytes = NSTAGE * kStageBytes;
   static constexpr int kBarOffset = kWarps * kRingBytes;
-  static constexpr int kFlagOffset = kBarOffset + kWarps * NSTAGE * 8;
+  // barriers: the warps' own rings use kWarps * NSTAGE; a shared-prefix CTA uses
+  // that many full and as many empty barriers for its pooled ring
+  static constexpr int kFlagOffset = kBarOffset + 2 * kWarps * NSTAGE * 8;
   static constexpr int kSmemBytes = kFlagOffset + kWarps * NSTAGE * 4 + 1024;
 };
 
@@ -64,6 +66,8 @@ struct DecodeParams {
   const int32_t *warp_begin;
   const WarpHead *warp_head;
   const Piece *pieces;
+  const SharedItem *shared;    // shared-prefix CTAs, after the num_indep_ctas CTAs of warp ranges
+  int32_t num_indep_ctas;
   const MergeGroup *merges;
   float *part_o;
   float2 *part_ml;
@@ -181,6 +185,270 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
   *reinterpret_cast<uint2 *>(p.out + (tok * p.num_q_heads + hq) * D + 4 * ch) = pk;
 }
 
+// Q fragments (A operand) of a row group: rows r and r + 8 of the group's R rows
+// (token row / G, head h * G + row % G from packed query row q_row0), head_dim
+// permuted to match the K fragments.  Rows >= R read as zeros.
+template <int D>
+__device__ __forceinline__ void load_q_frags(const DecodeParams &p, int q_row0, int R, int h,
+                                             int r, int c, uint32_t (&qa)[D / 16][4]) {
+  constexpr int kL = D / 32;
+  const int G = p.group;
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int row = r + 8 * half;
+    const bool rv = row < R;
+    const __nv_bfloat16 *qrow =
+        p.q + ((int64_t)(q_row0 + (rv ? row / G : 0)) * p.num_q_heads + h * G +
+               (rv ? row % G : 0)) * D;
+#pragma unroll
+    for (int L = 0; L < kL; ++L) {
+      const int e = 8 * (L >> 1) + 2 * c + (L & 1);
+      const uint4 v = rv ? ldg128_nc(qrow + 8 * e) : make_uint4(0, 0, 0, 0);
+      qa[2 * L][half] = v.x;
+      qa[2 * L][2 + half] = v.y;
+      qa[2 * L + 1][half] = v.z;
+      qa[2 * L + 1][2 + half] = v.w;
+    }
+  }
+}
+
+// One paged block (16 keys at positions p0 ..) of a row group: S = Q K^T, causal
+// mask, online softmax in log2 units, O += P V.  sK / sV: the block's K and V in
+// shared memory (blk_off layout).  The warp's running (m, l, O) are updated.
+template <int D>
+__device__ __forceinline__ void block_update(uint32_t sK, uint32_t sV, const uint32_t (&qa)[D / 16][4],
+                                             int p0, int q_pos0, int lim_lo, int lim_hi, float sl2,
+                                             int r, int c, float &m_lo, float &m_hi, float &l_lo,
+                                             float &l_hi, float (&o)[D / 8][4]) {
+  constexpr int kL = D / 32;
+  constexpr int kNt = D / 8;
+  constexpr int kHalves = D / 64;
+  // S = Q K^T for the block's 16 keys (two n-tiles of 8 keys)
+  float s[2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+    const int t = r + 8 * nt;
+#pragma unroll
+    for (int L = 0; L < kL; ++L) {
+      const int e = 8 * (L >> 1) + 2 * c + (L & 1);
+      const uint4 kv = lds128(sK + blk_off<kHalves>(t, e));
+      mma_16816(s[nt], qa[2 * L][0], qa[2 * L][1], qa[2 * L][2], qa[2 * L][3], kv.x, kv.y);
+      mma_16816(s[nt], qa[2 * L + 1][0], qa[2 * L + 1][1], qa[2 * L + 1][2],
+                qa[2 * L + 1][3], kv.z, kv.w);
+    }
+  }
+  // scale to log2 units; causal / context mask on the boundary blocks
+  const bool need_mask = p0 + kBlockSize - 1 > q_pos0;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float x = s[nt][j] * sl2;
+      if (need_mask) {
+        const int pos = p0 + 8 * nt + 2 * c + (j & 1);
+        if (pos > (j < 2 ? lim_lo : lim_hi)) x = -INFINITY;
+      }
+      s[nt][j] = x;
+    }
+  // online softmax (rows r and r + 8; the 4 lanes of a row hold 4 keys each)
+  float mx_lo = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
+  float mx_hi = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
+  mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+  mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+  mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+  mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+  const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+  const float base_lo = mn_lo == -INFINITY ? 0.f : mn_lo;
+  const float base_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
+  const float a_lo = fast_exp2(m_lo - base_lo), a_hi = fast_exp2(m_hi - base_hi);
+  m_lo = mn_lo;
+  m_hi = mn_hi;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    s[nt][0] = fast_exp2(s[nt][0] - base_lo);
+    s[nt][1] = fast_exp2(s[nt][1] - base_lo);
+    s[nt][2] = fast_exp2(s[nt][2] - base_hi);
+    s[nt][3] = fast_exp2(s[nt][3] - base_hi);
+  }
+  l_lo = l_lo * a_lo + (s[0][0] + s[0][1]) + (s[1][0] + s[1][1]);
+  l_hi = l_hi * a_hi + (s[0][2] + s[0][3]) + (s[1][2] + s[1][3]);
+  if (__any_sync(0xffffffffu, a_lo != 1.f || a_hi != 1.f)) {
+#pragma unroll
+    for (int nt = 0; nt < kNt; ++nt) {
+      o[nt][0] *= a_lo;
+      o[nt][1] *= a_lo;
+      o[nt][2] *= a_hi;
+      o[nt][3] *= a_hi;
+    }
+  }
+  // P (bf16) as the A operand: keys are the k dimension
+  const uint32_t pa0 = pack_bf16x2(s[0][0], s[0][1]);
+  const uint32_t pa1 = pack_bf16x2(s[0][2], s[0][3]);
+  const uint32_t pa2 = pack_bf16x2(s[1][0], s[1][1]);
+  const uint32_t pa3 = pack_bf16x2(s[1][2], s[1][3]);
+  // O += P V: lane (r, c) reads keys 2c, 2c+1, 2c+8, 2c+9 at head_dim chunk r (+8 per half)
+#pragma unroll
+  for (int hh = 0; hh < kHalves; ++hh) {
+    const int ch = hh * 8 + r;  // head_dim chunk
+    const uint4 v0 = lds128(sV + blk_off<kHalves>(2 * c, ch));
+    const uint4 v1 = lds128(sV + blk_off<kHalves>(2 * c + 1, ch));
+    const uint4 v2 = lds128(sV + blk_off<kHalves>(2 * c + 8, ch));
+    const uint4 v3 = lds128(sV + blk_off<kHalves>(2 * c + 9, ch));
+    const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w};
+    const uint32_t w1[4] = {v1.x, v1.y, v1.z, v1.w};
+    const uint32_t w2[4] = {v2.x, v2.y, v2.z, v2.w};
+    const uint32_t w3[4] = {v3.x, v3.y, v3.z, v3.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      mma_16816(o[8 * hh + 2 * k], pa0, pa1, pa2, pa3, __byte_perm(w0[k], w1[k], 0x5410),
+                __byte_perm(w2[k], w3[k], 0x5410));
+      mma_16816(o[8 * hh + 2 * k + 1], pa0, pa1, pa2, pa3,
+                __byte_perm(w0[k], w1[k], 0x7632), __byte_perm(w2[k], w3[k], 0x7632));
+    }
+  }
+}
+
+// Shared-prefix CTA: the kWarps warps attend their row groups (usually of
+// different sequences that share the prefix blocks) to the same blocks, loaded
+// once into one ring pooled from the warps' rings.  Warp 0 resolves the block
+// table and issues the copies; a stage is refilled once every warp has released
+// it (an empty mbarrier with kWarps arrivals).  Every wait is bounded.
+template <int D, int NSTAGE>
+__device__ __forceinline__ void shared_cta(const CUtensorMap &pool_map, const DecodeParams &p,
+                                           uint8_t *smem, int warp, int lane) {
+  using C = DecodeCfg<D, NSTAGE>;
+  constexpr int kS = kWarps * NSTAGE;  // stages of the pooled ring
+  constexpr int kL = D / 32, kNt = D / 8;
+  const int r = lane >> 2, c = lane & 3;
+  const int G = p.group, hkv = p.num_kv_heads;
+  const SharedItem &item = p.shared[blockIdx.x - p.num_indep_ctas];
+  const int seq0 = item.seq0, h = item.h, kb0 = item.kb_begin, kb1 = item.kb_end;
+  const int n_rg = item.n_rg;
+  const bool item_ok = seq0 >= 0 && seq0 < p.num_seqs && h >= 0 && h < hkv && kb0 >= 0 &&
+                       kb0 <= kb1 && kb1 <= p.max_blocks_per_seq && n_rg >= 1 && n_rg <= kWarps;
+  SharedRowGroup rg;
+  rg.seq = -1;
+  rg.qi0 = rg.n_q = rg.q_row0 = 0;
+  rg.part = -1;
+  if (item_ok && warp < n_rg) rg = item.rg[warp];
+  bool mine = item_ok && warp < n_rg && rg.seq >= 0 && rg.seq < p.num_seqs && rg.qi0 >= 0 &&
+              rg.n_q >= 1 && rg.n_q * G <= kRowsPerTile && rg.q_row0 >= 0 &&
+              rg.q_row0 + rg.n_q <= p.total_q;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOffset);
+  uint64_t *empty = full + kS;
+  int *stage_ok = reinterpret_cast<int *>(smem + C::kFlagOffset);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kS; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), kWarps);
+    }
+    fence_mbar_init();
+    prefetch_tmap(&pool_map);
+    if (!item_ok) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
+  }
+  // q rows, lengths and the first table window are not written by the kernels
+  // this one follows: read before the programmatic-launch wait
+  uint32_t qa[2 * kL][4];
+  load_q_frags<D>(p, mine ? rg.q_row0 : 0, mine ? rg.n_q * G : 0, h, r, c, qa);
+  int cu0 = 0, qs = 0, ctx = 0;
+  if (mine) {
+    cu0 = __ldg(p.cu_q_lens + rg.seq);
+    qs = __ldg(p.cu_q_lens + rg.seq + 1) - cu0;
+    ctx = __ldg(p.context_lens + rg.seq);
+    mine = rg.qi0 + rg.n_q <= qs && qs <= ctx && rg.q_row0 == cu0 + rg.qi0 &&
+           kb1 <= (ctx + p.lookahead * qs - qs + rg.qi0 + rg.n_q - 1) / kBlockSize + 1;
+    if (!mine && lane == 0) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
+  }
+  const int32_t *table = p.block_tables + (int64_t)(item_ok ? seq0 : 0) * p.max_blocks_per_seq;
+  int win_base = kb0, win_val = -1;
+  if (warp == 0 && item_ok && kb0 + lane < kb1) win_val = __ldg(table + kb0 + lane);
+  __syncthreads();  // barrier initialisation visible to every warp
+  pdl_wait();
+  const int nblk = item_ok ? kb1 - kb0 : 0;
+  int issued = 0;
+  auto issue = [&](int j) {  // warp 0, whole warp
+    const int kb = kb0 + j;
+    if (kb >= win_base + 32) {
+      win_base = kb;
+      win_val = kb + lane < kb1 ? __ldg(table + kb + lane) : -1;
+    }
+    const int phys = __shfl_sync(0xffffffffu, win_val, (kb - win_base) & 31);
+    const bool ok = phys >= 0 && phys < p.num_blocks;
+    const int s = j % kS;
+    const uint32_t bar = smem_u32(&full[s]);
+    if (lane == 0) {
+      stage_ok[s] = ok ? 1 : 0;
+      if (ok) {
+        mbar_arrive_expect_tx(bar, C::kStageBytes);
+        const int row_k = ((phys * 2 + 0) * hkv + h) * kBlockSize;
+        const uint32_t dst = smem_u32(smem + s * C::kStageBytes);
+        tma_load_4d(dst, &pool_map, 0, 0, 0, row_k >> 3, bar);
+        tma_load_4d(dst + C::kSlabBytes, &pool_map, 0, 0, 0, (row_k + hkv * kBlockSize) >> 3, bar);
+      } else {
+        report(p.dev_status, PKV_DEV_BAD_BLOCK);
+        mbar_arrive(bar);  // complete the phase without data; the block is skipped
+      }
+    }
+    ++issued;
+  };
+  if (warp == 0)
+    for (int j = 0; j < min(nblk, kS); ++j) issue(j);
+
+  const float sl2 = p.scale_log2;
+  const int R = mine ? rg.n_q * G : 0;
+  const int q_pos0 = ctx - qs + rg.qi0;
+  const int lim_lo = r < R ? q_pos0 + r / G : -1;
+  const int lim_hi = r + 8 < R ? q_pos0 + (r + 8) / G : -1;
+  float o[kNt][4];
+#pragma unroll
+  for (int nt = 0; nt < kNt; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+  float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+  bool good = true;
+  int done = 0;
+  for (int j = 0; j < nblk; ++j) {
+    const int s = j % kS;
+    const uint32_t par = (uint32_t)((j / kS) & 1);
+    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full[s]), par))) {
+      if (lane == 0) report(p.dev_status, PKV_DEV_TIMEOUT);
+      good = false;
+      break;
+    }
+    ++done;
+    if (mine && stage_ok[s]) {
+      const uint32_t sK = smem_u32(smem + s * C::kStageBytes);
+      block_update<D>(sK, sK + C::kSlabBytes, qa, (kb0 + j) * kBlockSize, q_pos0, lim_lo, lim_hi,
+                      sl2, r, c, m_lo, m_hi, l_lo, l_hi, o);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+    if (warp == 0 && j + kS < nblk) {  // refill once every warp released the stage
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[s]), par))) {
+        if (lane == 0) report(p.dev_status, PKV_DEV_TIMEOUT);
+        good = false;
+        break;
+      }
+      issue(j + kS);
+    }
+  }
+  // warp 0's copies still in flight land before the CTA exits
+  if (warp == 0 && lane == 0)
+    for (int j = done; j < issued; ++j)
+      mbar_wait(smem_u32(&full[j % kS]), (uint32_t)((j / kS) & 1));
+  if (good && mine) {
+    Piece pc;
+    pc.seq = rg.seq;
+    pc.qi0 = rg.qi0;
+    pc.n_q = rg.n_q;
+    pc.h = h;
+    pc.kb_begin = kb0;
+    pc.kb_end = kb1;
+    pc.part = rg.part;
+    pc.q_row0 = rg.q_row0;
+    write_piece<D>(p, pc, o, m_lo, m_hi, l_lo, l_hi, R, cu0, r, c);
+  }
+}
+
 template <int D, int NSTAGE>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_kernel(const __grid_constant__ CUtensorMap pool_map, const DecodeParams p) {
@@ -198,6 +466,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   // first block-table window are read before waiting for the predecessor; the
   // pool, the workspace and out are touched only after the wait.
   pdl_trigger();
+  if (blockIdx.x >= p.num_indep_ctas) {  // CTA-uniform: a shared-prefix CTA
+    shared_cta<D, NSTAGE>(pool_map, p, smem, warp, lane);
+    return;
+  }
   const int gw = blockIdx.x * kWarps + warp;
   const bool has_warp = gw < p.num_warps;
   // Start-up is a chain of dependent reads (range -> piece -> table -> pool).
@@ -346,25 +618,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     // Rows come straight from the plan's packed index (bounds-checked above), so
     // these loads do not wait for the length loads below; a piece that then
     // fails the check (R = 0) uses none of them.
-    const int Rq = valid ? pc.n_q * G : 0;
     uint32_t qa[2 * kL][4];
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int row = r + 8 * half;
-      const bool rv = row < Rq;
-      const __nv_bfloat16 *qrow =
-          p.q + ((int64_t)(pc.q_row0 + (rv ? row / G : 0)) * p.num_q_heads + pc.h * G +
-                 (rv ? row % G : 0)) * D;
-#pragma unroll
-      for (int L = 0; L < kL; ++L) {
-        const int e = 8 * (L >> 1) + 2 * c + (L & 1);
-        const uint4 v = rv ? ldg128_nc(qrow + 8 * e) : make_uint4(0, 0, 0, 0);
-        qa[2 * L][half] = v.x;
-        qa[2 * L][2 + half] = v.y;
-        qa[2 * L + 1][half] = v.z;
-        qa[2 * L + 1][2 + half] = v.w;
-      }
-    }
+    load_q_frags<D>(p, pc.q_row0, valid ? pc.n_q * G : 0, pc.h, r, c, qa);
     int cu0 = 0, qs = 0, ctx = 0;
     if (valid) {
       cu0 = pi == pb ? f_cu0 : __ldg(p.cu_q_lens + pc.seq);
@@ -398,92 +653,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       if (valid && stage_ok[stage]) {
         const uint32_t sK = smem_u32(ring + stage * C::kStageBytes);
-        const uint32_t sV = sK + C::kSlabBytes;
-        // S = Q K^T for the block's 16 keys (two n-tiles of 8 keys)
-        float s[2][4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-          const int t = r + 8 * nt;
-#pragma unroll
-          for (int L = 0; L < kL; ++L) {
-            const int e = 8 * (L >> 1) + 2 * c + (L & 1);
-            const uint4 kv = lds128(sK + blk_off<C::kHalves>(t, e));
-            mma_16816(s[nt], qa[2 * L][0], qa[2 * L][1], qa[2 * L][2], qa[2 * L][3], kv.x, kv.y);
-            mma_16816(s[nt], qa[2 * L + 1][0], qa[2 * L + 1][1], qa[2 * L + 1][2],
-                      qa[2 * L + 1][3], kv.z, kv.w);
-          }
-        }
-        // scale to log2 units; causal / context mask on the boundary blocks
-        const int p0 = kb * kBlockSize;
-        const bool need_mask = p0 + kBlockSize - 1 > q_pos0;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            float x = s[nt][j] * sl2;
-            if (need_mask) {
-              const int pos = p0 + 8 * nt + 2 * c + (j & 1);
-              if (pos > (j < 2 ? lim_lo : lim_hi)) x = -INFINITY;
-            }
-            s[nt][j] = x;
-          }
-        // online softmax (rows r and r + 8; the 4 lanes of a row hold 4 keys each)
-        float mx_lo = fmaxf(fmaxf(s[0][0], s[0][1]), fmaxf(s[1][0], s[1][1]));
-        float mx_hi = fmaxf(fmaxf(s[0][2], s[0][3]), fmaxf(s[1][2], s[1][3]));
-        mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
-        mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
-        mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
-        mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
-        const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
-        const float base_lo = mn_lo == -INFINITY ? 0.f : mn_lo;
-        const float base_hi = mn_hi == -INFINITY ? 0.f : mn_hi;
-        const float a_lo = fast_exp2(m_lo - base_lo), a_hi = fast_exp2(m_hi - base_hi);
-        m_lo = mn_lo;
-        m_hi = mn_hi;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-          s[nt][0] = fast_exp2(s[nt][0] - base_lo);
-          s[nt][1] = fast_exp2(s[nt][1] - base_lo);
-          s[nt][2] = fast_exp2(s[nt][2] - base_hi);
-          s[nt][3] = fast_exp2(s[nt][3] - base_hi);
-        }
-        l_lo = l_lo * a_lo + (s[0][0] + s[0][1]) + (s[1][0] + s[1][1]);
-        l_hi = l_hi * a_hi + (s[0][2] + s[0][3]) + (s[1][2] + s[1][3]);
-        if (__any_sync(0xffffffffu, a_lo != 1.f || a_hi != 1.f)) {
-#pragma unroll
-          for (int nt = 0; nt < kNt; ++nt) {
-            o[nt][0] *= a_lo;
-            o[nt][1] *= a_lo;
-            o[nt][2] *= a_hi;
-            o[nt][3] *= a_hi;
-          }
-        }
-        // P (bf16) as the A operand: keys are the k dimension
-        const uint32_t pa0 = pack_bf16x2(s[0][0], s[0][1]);
-        const uint32_t pa1 = pack_bf16x2(s[0][2], s[0][3]);
-        const uint32_t pa2 = pack_bf16x2(s[1][0], s[1][1]);
-        const uint32_t pa3 = pack_bf16x2(s[1][2], s[1][3]);
-        // O += P V: lane (r, c) reads keys 2c, 2c+1, 2c+8, 2c+9 at head_dim chunk r (+8 per half)
-#pragma unroll
-        for (int hh = 0; hh < C::kHalves; ++hh) {
-          const int ch = hh * 8 + r;  // head_dim chunk
-          const uint4 v0 = lds128(sV + blk_off<C::kHalves>(2 * c, ch));
-          const uint4 v1 = lds128(sV + blk_off<C::kHalves>(2 * c + 1, ch));
-          const uint4 v2 = lds128(sV + blk_off<C::kHalves>(2 * c + 8, ch));
-          const uint4 v3 = lds128(sV + blk_off<C::kHalves>(2 * c + 9, ch));
-          const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w};
-          const uint32_t w1[4] = {v1.x, v1.y, v1.z, v1.w};
-          const uint32_t w2[4] = {v2.x, v2.y, v2.z, v2.w};
-          const uint32_t w3[4] = {v3.x, v3.y, v3.z, v3.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            mma_16816(o[8 * hh + 2 * k], pa0, pa1, pa2, pa3, __byte_perm(w0[k], w1[k], 0x5410),
-                      __byte_perm(w2[k], w3[k], 0x5410));
-            mma_16816(o[8 * hh + 2 * k + 1], pa0, pa1, pa2, pa3,
-                      __byte_perm(w0[k], w1[k], 0x7632), __byte_perm(w2[k], w3[k], 0x7632));
-          }
-        }
+        block_update<D>(sK, sK + C::kSlabBytes, qa, kb * kBlockSize, q_pos0, lim_lo, lim_hi, sl2,
+                        r, c, m_lo, m_hi, l_lo, l_hi, o);
       }
       __syncwarp();
       issue_next(stage);  // refill this stage with the stream's next block
@@ -589,6 +760,8 @@ DecodeParams make_params(const AttnArgs &a) {
   p.block_tables = a.block_tables;
   p.warp_begin = a.warp_begin;
   p.warp_head = a.warp_head;
+  p.shared = a.shared_items;
+  p.num_indep_ctas = (a.num_decode_warps + kWarps - 1) / kWarps;
   p.pieces = a.pieces;
   p.merges = a.merge_groups;
   p.part_o = a.part_o;
@@ -621,7 +794,7 @@ int launch_decode_t(const AttnArgs &a, const CUtensorMap &map) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::kSmemBytes);
   if (e != cudaSuccess) return (int)e;
-  const unsigned grid = (unsigned)((a.num_decode_warps + kWarps - 1) / kWarps);
+  const unsigned grid = (unsigned)((a.num_decode_warps + kWarps - 1) / kWarps + a.num_shared_ctas);
   profile_begin(PKV_KERNEL_DECODE, a.stream);
   // programmatic launch only when no profiling event sits between us and our
   // predecessor (an event in between would serialise anyway)
@@ -633,8 +806,6 @@ int launch_decode_t(const AttnArgs &a, const CUtensorMap &map) {
 
 }  // namespace
 
-// 2D view of the pool: rows of head_dim bf16 (one key or value row of one
-// head), box = 16 rows x 64 elements, 128-byte swizzle.
 int make_pool_map(void *map_out, const void *pool, const pkv_pool_desc &desc) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return (int)cudaErrorNotSupported;
@@ -655,7 +826,7 @@ int make_pool_map(void *map_out, const void *pool, const pkv_pool_desc &desc) {
 }
 
 int launch_decode(const AttnArgs &a, int *launches) {
-  if (a.num_decode_warps <= 0) return 0;
+  if (a.num_decode_warps <= 0 && a.num_shared_ctas <= 0) return 0;
   CUtensorMap map;
   int e = make_pool_map(&map, a.kv_pool, a.desc);
   if (e) return e;

@@ -22,6 +22,7 @@ constexpr int kDecodeWarpsPerCta = 4;
 //    ids: a warp reads its range and head with two independent loads and can
 //    start its first copies without waiting for a block-table read)
 //   [Piece x num_decode_pieces][MergeGroup x num_merge_groups]
+//   [SharedItem x num_shared_ctas]
 //   [prefill_begin: int32 x (num_prefill_ctas + 1), padded to 32 B; absent when 0 CTAs]
 //   [PrefillTile x num_prefill_tiles, grouped by CTA]
 struct PlanHeader {
@@ -66,6 +67,31 @@ struct WarpHead {
 };
 static_assert(sizeof(WarpHead) == 48, "warp head is 48 bytes");
 
+// Shared-prefix work for one split-KV CTA: sequences whose block tables start
+// with the same physical blocks read those blocks once per CTA, each of the CTA's
+// warps attending one row group of one of them to every loaded block.  Blocks
+// kb_begin .. kb_end-1 of sequence seq0's table, KV head h; warp w < n_rg takes
+// row group rg[w] and writes its partial to rg[w].part (or its result directly
+// when part < 0).
+struct SharedRowGroup {
+  int32_t seq;
+  int32_t qi0;
+  int32_t n_q;
+  int32_t part;
+  int32_t q_row0;  // packed query index of token qi0
+  int32_t pad[3];
+};
+struct SharedItem {
+  int32_t seq0;
+  int32_t h;
+  int32_t kb_begin;
+  int32_t kb_end;
+  int32_t n_rg;
+  int32_t pad[3];
+  SharedRowGroup rg[kDecodeWarpsPerCta];
+};
+static_assert(sizeof(SharedItem) == 32 + 32 * kDecodeWarpsPerCta, "shared item layout");
+
 // A set of nsplit partial results (slots part0 .. part0+nsplit-1) to combine.
 // kind 0: a decode segment -- rows are n_q tokens x the group's heads of KV
 //         head h, partial slots of kRowsPerTile rows;
@@ -106,16 +132,17 @@ static_assert(sizeof(PrefillTile) == 48, "prefill tile is 48 bytes");
 inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
 struct PlanOffsets {
-  int64_t warp_begin, warp_head, pieces, merges, prefill_begin, prefill, total;
+  int64_t warp_begin, warp_head, pieces, merges, shared, prefill_begin, prefill, total;
 };
 inline PlanOffsets plan_offsets(int32_t n_warps, int32_t n_pieces, int32_t n_merge,
-                                int32_t n_prefill, int32_t n_prefill_ctas) {
+                                int32_t n_shared, int32_t n_prefill, int32_t n_prefill_ctas) {
   PlanOffsets o;
   o.warp_begin = (int64_t)sizeof(PlanHeader);
   o.warp_head = o.warp_begin + align_up(4ll * (n_warps + 1), 32);
   o.pieces = o.warp_head + (int64_t)n_warps * (int64_t)sizeof(WarpHead);
   o.merges = o.pieces + (int64_t)n_pieces * (int64_t)sizeof(Piece);
-  o.prefill_begin = o.merges + (int64_t)n_merge * (int64_t)sizeof(MergeGroup);
+  o.shared = o.merges + (int64_t)n_merge * (int64_t)sizeof(MergeGroup);
+  o.prefill_begin = o.shared + (int64_t)n_shared * (int64_t)sizeof(SharedItem);
   o.prefill = o.prefill_begin + (n_prefill_ctas > 0 ? align_up(4ll * (n_prefill_ctas + 1), 32) : 0);
   o.total = o.prefill + (int64_t)n_prefill * (int64_t)sizeof(PrefillTile);
   return o;
@@ -163,6 +190,8 @@ struct AttnArgs {
   const int32_t *warp_begin;
   const WarpHead *warp_head;
   int32_t num_decode_warps;
+  const SharedItem *shared_items;
+  int32_t num_shared_ctas;
   const Piece *pieces;
   const MergeGroup *merge_groups;
   int32_t num_merge_groups;

@@ -31,6 +31,7 @@
 #include <climits>
 #include <cstdlib>
 #include <cstring>
+#include <map>
 #include <vector>
 
 #include "pkv_internal.h"
@@ -70,8 +71,13 @@ pkv_status check_desc(const pkv_pool_desc *desc, int32_t num_q_heads) {
 }
 
 struct Segment {
-  int32_t seq, qi0, n_q, h, nb;
+  int32_t seq, qi0, n_q, h, kb0, nb;  // blocks kb0 .. kb0 + nb - 1
 };
+struct DUnit {  // a decode row group: n_q tokens from qi0 of seq, reading blocks 0 .. nb-1
+  int32_t seq, qi0, n_q, nb;
+};
+// Shared prefixes shorter than this many blocks stay on the per-warp ranges.
+constexpr int32_t kMinSharedBlocks = 8;
 
 }  // namespace
 }  // namespace pkv
@@ -105,6 +111,7 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   if (num_seqs > 0 && cu_q_lens[0] != 0) return PKV_ERR_SHAPE;
   const int min_q_prefill = prefill_min_q();
   std::vector<Segment> segs;
+  std::vector<DUnit> dunits;
   std::vector<PrefillTile> pairs;                 // sub-tile pairs, key range not yet cut
   std::vector<std::array<int32_t, 2>> pair_nt;   // key tiles seen by each sub-tile
   int64_t kv_tokens = 0, total_blocks = 0;
@@ -163,16 +170,118 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
     for (int32_t qi0 = 0; qi0 < qs; qi0 += nq_tile) {
       int32_t n_q = std::min(nq_tile, qs - qi0);
       int32_t nb = (ctx_plan - qs + qi0 + n_q - 1) / kBlockSize + 1;
-      for (int32_t h = 0; h < hkv; ++h) {
-        segs.push_back({s, qi0, n_q, h, nb});
-        total_blocks += nb;
-      }
+      dunits.push_back({s, qi0, n_q, nb});
     }
   }
 
-  // ---- cut the concatenated decode blocks into equal warp ranges
+  // ---- shared prefixes (needs the host block tables): decode-class sequences
+  // whose tables start with the same physical blocks, over blocks every query
+  // row of each of them sees in full.  Those blocks are read once per CTA by
+  // shared items; the rest of each row group's keys (its suffix) go to the
+  // per-warp ranges below.
+  std::vector<int32_t> shared_len(num_seqs, 0);
+  struct Group {
+    std::vector<int32_t> members;
+    int32_t len;
+  };
+  std::vector<Group> groups;
+  if (block_tables && max_blocks_per_seq > 0) {
+    std::map<int32_t, std::vector<int32_t>> by_first;
+    for (int32_t s = 0; s < num_seqs; ++s) {
+      const int32_t qs = cu_q_lens[s + 1] - cu_q_lens[s];
+      if (qs <= 0 || qs >= min_q_prefill) continue;
+      const int32_t vis = std::min((context_lens[s] - qs + 1) / kBlockSize, max_blocks_per_seq);
+      if (vis >= kMinSharedBlocks) by_first[block_tables[(int64_t)s * max_blocks_per_seq]].push_back(s);
+    }
+    for (auto &kv : by_first) {
+      const std::vector<int32_t> &mem = kv.second;
+      if (mem.size() < 2) continue;
+      int32_t len = INT32_MAX;
+      for (int32_t m : mem)
+        len = std::min(len, std::min((context_lens[m] - (cu_q_lens[m + 1] - cu_q_lens[m]) + 1) /
+                                         kBlockSize, max_blocks_per_seq));
+      const int32_t *t0 = block_tables + (int64_t)mem[0] * max_blocks_per_seq;
+      for (int32_t b = 1; b < len; ++b)
+        for (size_t i = 1; i < mem.size(); ++i)
+          if (block_tables[(int64_t)mem[i] * max_blocks_per_seq + b] != t0[b]) {
+            len = b;
+            break;
+          }
+      if (len < kMinSharedBlocks) continue;
+      groups.push_back({mem, len});
+      for (int32_t m : mem) shared_len[m] = len;
+    }
+  }
+  // suffix segments: (row group, KV head) keys past the shared prefix
+  std::vector<int32_t> seg_of(dunits.size() * hkv, -1);
+  for (size_t u = 0; u < dunits.size(); ++u) {
+    const DUnit &du = dunits[u];
+    const int32_t kb0 = std::min(shared_len[du.seq], du.nb);
+    if (du.nb <= kb0) continue;
+    for (int32_t h = 0; h < hkv; ++h) {
+      seg_of[u * hkv + h] = (int32_t)segs.size();
+      segs.push_back({du.seq, du.qi0, du.n_q, h, kb0, du.nb - kb0});
+      total_blocks += du.nb - kb0;
+    }
+  }
+
+  // ---- shared items: per group and KV head, the members' row groups in sets of
+  // one per warp of a CTA, the prefix cut into chunks so a chunk costs what a
+  // warp range costs (a CTA-chunk of B blocks holds kDecodeWarpsPerCta warp
+  // slots for B block steps)
+  const int64_t slots = (int64_t)num_sms * kDecodeWarpsPerSm;
+  std::vector<SharedItem> sitems;
+  // shared parts of each (decode unit, KV head): (item, warp slot)
+  std::vector<std::vector<std::array<int32_t, 2>>> unit_shared(dunits.size() * hkv);
+  if (!groups.empty()) {
+    std::vector<int32_t> unit_of_seq_first(num_seqs, -1);  // decode units are in seq order
+    for (size_t u = dunits.size(); u-- > 0;) unit_of_seq_first[dunits[u].seq] = (int32_t)u;
+    int64_t sh_blocks = 0;
+    for (const Group &g : groups) {
+      int64_t nrg = 0;
+      for (int32_t m : g.members)
+        for (size_t u = unit_of_seq_first[m]; u < dunits.size() && dunits[u].seq == m; ++u) ++nrg;
+      sh_blocks += (int64_t)hkv * ((nrg + kDecodeWarpsPerCta - 1) / kDecodeWarpsPerCta) * g.len;
+    }
+    const int64_t ind_cost = 2 * total_blocks + 3 * (int64_t)segs.size();
+    const int64_t per_slot = std::max<int64_t>(1, (ind_cost + 2 * kDecodeWarpsPerCta * sh_blocks) / slots);
+    // chunk length in blocks: about a warp slot's share (a block costs 2); each
+    // prefix is then cut into equal chunks, their count rounded to the nearest
+    const int64_t chunk = std::max<int64_t>(kMinBlocksPerWarp, per_slot / 2);
+    for (const Group &g : groups) {
+      std::vector<int32_t> us;
+      for (int32_t m : g.members)
+        for (size_t u = unit_of_seq_first[m]; u < dunits.size() && dunits[u].seq == m; ++u)
+          us.push_back((int32_t)u);
+      const int64_t nch = std::max<int64_t>(1, (g.len + chunk / 2) / chunk);
+      for (int32_t h = 0; h < hkv; ++h)
+        for (size_t i0 = 0; i0 < us.size(); i0 += kDecodeWarpsPerCta)
+          for (int64_t ci = 0; ci < nch; ++ci) {
+            SharedItem it;
+            std::memset(&it, 0, sizeof it);
+            it.seq0 = g.members[0];
+            it.h = h;
+            it.kb_begin = (int32_t)(g.len * ci / nch);
+            it.kb_end = (int32_t)(g.len * (ci + 1) / nch);
+            it.n_rg = (int32_t)std::min<size_t>(kDecodeWarpsPerCta, us.size() - i0);
+            for (int32_t w = 0; w < it.n_rg; ++w) {
+              const DUnit &du = dunits[us[i0 + w]];
+              it.rg[w].seq = du.seq;
+              it.rg[w].qi0 = du.qi0;
+              it.rg[w].n_q = du.n_q;
+              it.rg[w].part = -1;
+              it.rg[w].q_row0 = cu_q_lens[du.seq] + du.qi0;
+              unit_shared[(size_t)us[i0 + w] * hkv + h].push_back({(int32_t)sitems.size(), w});
+            }
+            sitems.push_back(it);
+          }
+    }
+  }
+  const int64_t shared_slots = (int64_t)sitems.size() * kDecodeWarpsPerCta;
+
+  // ---- cut the concatenated suffix blocks into equal-cost warp ranges
   int64_t nw64 = (total_blocks + kMinBlocksPerWarp - 1) / kMinBlocksPerWarp;
-  nw64 = std::min<int64_t>(nw64, (int64_t)num_sms * kDecodeWarpsPerSm);
+  nw64 = std::min<int64_t>(nw64, std::max<int64_t>(slots - shared_slots, 1));
   const int32_t num_warps = total_blocks > 0 ? (int32_t)std::max<int64_t>(nw64, 1) : 0;
   std::vector<int32_t> warp_begin(num_warps + 1, 0);
   std::vector<Piece> pieces;
@@ -226,8 +335,8 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
         p.qi0 = g.qi0;
         p.n_q = g.n_q;
         p.h = g.h;
-        p.kb_begin = (int32_t)(a - seg_off);
-        p.kb_end = (int32_t)(e - seg_off);
+        p.kb_begin = g.kb0 + (int32_t)(a - seg_off);
+        p.kb_end = g.kb0 + (int32_t)(e - seg_off);
         p.part = -1;
         p.q_row0 = cu_q_lens[g.seq] + g.qi0;
         pieces.push_back(p);
@@ -237,25 +346,37 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
     }
     warp_begin[num_warps] = (int32_t)pieces.size();
   }
-  // partial slots for segments cut into several pieces (their pieces are adjacent)
+  // partial slots: every (decode unit, KV head) result whose keys are split over
+  // several parts (shared-prefix chunks and suffix pieces) gets one slot per part
+  // and a merge group; a result in one part is written directly
   std::vector<MergeGroup> merges;
   int32_t parts = 0;
-  for (size_t i = 0; i < pieces.size();) {
-    size_t j = i;
-    while (j < pieces.size() && piece_seg[j] == piece_seg[i]) ++j;
-    if (j - i > 1) {
-      MergeGroup m;
-      std::memset(&m, 0, sizeof m);
-      m.seq = pieces[i].seq;
-      m.qi0 = pieces[i].qi0;
-      m.n_q = pieces[i].n_q;
-      m.h = pieces[i].h;
-      m.part0 = parts;
-      m.nsplit = (int32_t)(j - i);
-      for (size_t t = i; t < j; ++t) pieces[t].part = parts++;
-      merges.push_back(m);
+  {
+    std::vector<int32_t> seg_first(segs.size(), -1), seg_count(segs.size(), 0);
+    for (size_t i = 0; i < pieces.size(); ++i) {
+      const int32_t k = piece_seg[i];
+      if (seg_first[k] < 0) seg_first[k] = (int32_t)i;
+      ++seg_count[k];
     }
-    i = j;
+    for (size_t u = 0; u < dunits.size(); ++u)
+      for (int32_t h = 0; h < hkv; ++h) {
+        const auto &sh = unit_shared[u * hkv + h];
+        const int32_t k = seg_of[u * hkv + h];
+        const int32_t np = k >= 0 ? seg_count[k] : 0;
+        const int32_t total = (int32_t)sh.size() + np;
+        if (total <= 1) continue;
+        MergeGroup m;
+        std::memset(&m, 0, sizeof m);
+        m.seq = dunits[u].seq;
+        m.qi0 = dunits[u].qi0;
+        m.n_q = dunits[u].n_q;
+        m.h = h;
+        m.part0 = parts;
+        m.nsplit = total;
+        for (const auto &si : sh) sitems[si[0]].rg[si[1]].part = parts++;
+        for (int32_t t = 0; t < np; ++t) pieces[seg_first[k] + t].part = parts++;
+        merges.push_back(m);
+      }
   }
   // ---- prefill work per persistent CTA (at most one per SM), equal cost:
   //  1. whole pairs, largest first, each into the least-loaded CTA that stays
@@ -388,7 +509,7 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
 
   // ---- sizes
   const PlanOffsets off = plan_offsets(num_warps, (int32_t)pieces.size(), (int32_t)merges.size(),
-                                       (int32_t)ptiles.size(), n_pf_ctas);
+                                       (int32_t)sitems.size(), (int32_t)ptiles.size(), n_pf_ctas);
   std::memset(info, 0, sizeof *info);
   info->num_seqs = num_seqs;
   info->num_q_heads = num_q_heads;
@@ -403,7 +524,9 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   info->num_prefill_ctas = n_pf_ctas;
   info->num_prefill_partials = pparts;
   info->num_prefill_merges = (int32_t)pmerges.size();
-  info->num_kernels = (num_warps > 0 ? 1 : 0) + (merges.empty() ? 0 : 1) + (ptiles.empty() ? 0 : 1);
+  info->num_kernels = (num_warps > 0 || !sitems.empty() ? 1 : 0) + (merges.empty() ? 0 : 1) +
+                      (ptiles.empty() ? 0 : 1);
+  info->num_shared_ctas = (int32_t)sitems.size();
   info->max_blocks_needed = max_nb;
   info->kv_tokens = kv_tokens;
   info->decode_blocks = total_blocks;
@@ -446,6 +569,8 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   if (!pieces.empty()) std::memcpy(p + off.pieces, pieces.data(), pieces.size() * sizeof(Piece));
   if (!merges.empty())
     std::memcpy(p + off.merges, merges.data(), merges.size() * sizeof(MergeGroup));
+  if (!sitems.empty())
+    std::memcpy(p + off.shared, sitems.data(), sitems.size() * sizeof(SharedItem));
   if (!ptiles.empty()) {
     std::memcpy(p + off.prefill_begin, pf_begin.data(), pf_begin.size() * sizeof(int32_t));
     std::memcpy(p + off.prefill, ptiles.data(), ptiles.size() * sizeof(PrefillTile));

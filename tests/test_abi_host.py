@@ -50,7 +50,9 @@ def parse_plan(info, host):
     off_p = off_first + 12 * nw
     off_m = off_p + 8 * npc
     ncta = info.num_prefill_ctas
-    off_b = off_m + 8 * nm
+    nsh = info.num_shared_ctas
+    off_s = off_m + 8 * nm
+    off_b = off_s + 40 * nsh
     off_f = off_b + (((ncta + 1 + 7) // 8) * 8 if ncta else 0)
     assert info.plan_bytes == 4 * (off_f + 12 * npf)
     wb = words[off_w:off_w + nw + 1]
@@ -58,8 +60,9 @@ def parse_plan(info, host):
     heads = words[off_first:off_p].reshape(nw, 12)
     if nw:
         assert np.array_equal(heads[:, :8], pieces[wb[:-1]])  # each warp's first piece, copied
-    mer = words[off_m:off_b].reshape(nm, 8)
+    mer = words[off_m:off_s].reshape(nm, 8)
     pre = words[off_f:off_f + 12 * npf].reshape(npf, 12)
+    parse_plan.shared = words[off_s:off_b].reshape(nsh, 40)
     pb = words[off_b:off_b + ncta + 1] if ncta else np.zeros(1, np.int32)
     if ncta:
         assert pb[0] == 0 and pb[-1] == npf and np.all(np.diff(pb) >= 0)
@@ -343,3 +346,52 @@ def test_plan_carries_first_block_ids_when_given_the_tables(pkv):
             want = meta.block_tables[seq, kb0 + i] if kb0 + i < kb1 else -1
             assert heads[w, 8 + i] == want
         assert heads[w, 11] == -1
+
+
+
+def test_shared_prefix_items_cover_the_shared_blocks(pkv):
+    """With the host tables, sequences whose tables start with the same blocks get
+    shared-prefix CTAs over those blocks; every (row group, KV head) result is then
+    its shared chunks over [0, L) plus its suffix pieces over [L, nb), with one
+    merge group naming exactly those parts."""
+    meta = workloads.shared_prefix_verify()
+    desc = pkv.PoolDesc(meta.num_blocks, 16, meta.num_kv_heads, meta.head_dim)
+    info, host = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, desc,
+                               num_sms=152, upload=False, block_tables=meta.block_tables)
+    assert info.num_shared_ctas > 0
+    hdr, wb, pieces, mer, pre = parse_plan(info, host)
+    sh = parse_plan.shared
+    g = meta.num_q_heads // meta.num_kv_heads
+    nq_tile = max(1, 16 // g)
+    # shared chunks per (seq, qi0, h): list of (kb_begin, kb_end, part)
+    got = {}
+    for it in sh:
+        seq0, h, kb0, kb1, nrg = (int(x) for x in it[:5])
+        assert 1 <= nrg <= 4 and 0 <= kb0 < kb1
+        # the blocks are the same physical blocks in every member's table
+        for w in range(nrg):
+            seq, qi0, n_q, part, qrow = (int(x) for x in it[8 + 8 * w: 13 + 8 * w])
+            assert np.array_equal(meta.block_tables[seq, kb0:kb1], meta.block_tables[seq0, kb0:kb1])
+            assert qrow == meta.cu_q_lens[seq] + qi0
+            got.setdefault((seq, qi0, h), []).append((kb0, kb1, part))
+    assert got
+    for (seq, qi0, h), chunks in got.items():
+        chunks.sort()
+        L = chunks[-1][1]
+        assert chunks[0][0] == 0 and all(chunks[i][1] == chunks[i + 1][0] for i in range(len(chunks) - 1))
+        qs, ctx = int(meta.q_lens[seq]), int(meta.context_lens[seq])
+        n_q = min(nq_tile, qs - qi0)
+        nb = (ctx - qs + qi0 + n_q - 1) // 16 + 1
+        assert L <= (ctx - qs + 1) // 16          # every row sees the shared blocks in full
+        mine = pieces[(pieces[:, 0] == seq) & (pieces[:, 1] == qi0) & (pieces[:, 3] == h)]
+        mine = mine[np.argsort(mine[:, 4])]
+        if len(mine):
+            assert mine[0, 4] == L and mine[-1, 5] == nb
+            assert np.all(mine[1:, 4] == mine[:-1, 5])
+        parts = sorted([c[2] for c in chunks] + [int(x) for x in mine[:, 6]])
+        m = mer[(mer[:, 0] == seq) & (mer[:, 1] == qi0) & (mer[:, 3] == h) & (mer[:, 6] == 0)]
+        if len(parts) > 1:
+            assert len(m) == 1 and m[0, 5] == len(parts)
+            assert parts == list(range(m[0, 4], m[0, 4] + len(parts)))
+        else:
+            assert parts == [-1] and len(m) == 0

@@ -30,13 +30,16 @@ def bits(t):
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def gpu_step(pkv, meta, q, k, v, pool, dev, *, num_sms=None, check_status=True):
-    """Append + attention on the GPU; returns (out bf16 cpu tensor, pool after, status)."""
+def gpu_step(pkv, meta, q, k, v, pool, dev, *, num_sms=None, check_status=True, tables=True):
+    """Append + attention on the GPU; returns (out bf16 cpu tensor, pool after, status).
+    tables=True plans with the host block tables (first block ids in the plan,
+    shared-prefix CTAs where sequences share leading blocks)."""
     qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
     pd = pool.to(dev) if pool.device != dev else pool.clone()
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     pkv.paged_kv_append(kd, vd, torch.from_numpy(meta.slot_mapping).to(dev), pd, dev_status=status)
-    plan = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, pd, num_sms=num_sms)
+    plan = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, pd, num_sms=num_sms,
+                         block_tables=meta.block_tables if tables else None)
     out = pkv.paged_varlen_attention(qd, meta.cu_q_lens, meta.context_lens,
                                      torch.from_numpy(meta.block_tables).to(dev), pd, meta.scale,
                                      plan=plan, dev_status=status)
@@ -478,3 +481,23 @@ def test_plan_with_block_tables_same_result_and_mismatch_reported(pkv, cuda_devi
                                plan=plan, dev_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 4      # PKV_DEV_PLAN_MISMATCH
+
+
+
+@pytest.mark.parametrize("name,num_sms", [("shared_prefix_verify", 152), ("mtp_draft", 152),
+                                          ("shared_prefix_verify", 7)])
+def test_shared_prefix_ctas_match_oracle_and_per_warp_path(pkv, cuda_device, name, num_sms):
+    """Sequences sharing leading blocks read them once per shared-prefix CTA; the
+    result matches the oracle on every row and the per-warp plan (no tables)."""
+    meta = workloads.make_config(name)
+    q, k, v, pool = workloads.make_values(meta)
+    info, _ = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads,
+                            pkv.pool_desc(pool), num_sms=num_sms, upload=False,
+                            block_tables=meta.block_tables)
+    assert info.num_shared_ctas > 0
+    want, _ = oracle.run_step(meta, q, k, v, pool)
+    shared, _, _ = gpu_step(pkv, meta, q, k, v, pool, cuda_device, num_sms=num_sms)
+    per_warp, _, _ = gpu_step(pkv, meta, q, k, v, pool, cuda_device, num_sms=num_sms, tables=False)
+    assert_close(shared, want, f"{name} shared-prefix CTAs")
+    diff = (shared.double() - per_warp.double()).abs()
+    assert float(diff.max()) <= MAX_ABS and float(diff.mean()) <= MEAN_ABS
