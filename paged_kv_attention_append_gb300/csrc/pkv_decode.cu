@@ -153,7 +153,6 @@ __device__ __forceinline__ float4 merge_row(const float2 *ml, const float4 *po, 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams p) {
   constexpr int kChunks = D / 4;  // float4 chunks of a row
-  pdl_wait();                     // the partials are complete and visible
   const int64_t t = (int64_t)blockIdx.x * kMergeThreads + threadIdx.x;
   const int64_t n_dec = (int64_t)p.num_decode_merges * kRowsPerTile * kChunks;
   const bool dec = t < n_dec;
@@ -162,12 +161,17 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
   const int64_t gi = tt / (rows * kChunks);
   const int rem = (int)(tt % (rows * kChunks));
   const int row = rem / kChunks, ch = rem % kChunks;
-  if (gi >= (dec ? p.num_decode_merges : p.num_merges - p.num_decode_merges)) return;
-  const MergeGroup g = p.merges[dec ? gi : p.num_decode_merges + gi];
+  const bool in = gi < (dec ? p.num_decode_merges : p.num_merges - p.num_decode_merges);
+  // the plan is not written by the kernels before this one: the group is read
+  // while they finish; only the partials wait
+  MergeGroup g;
+  if (in) g = p.merges[dec ? gi : p.num_decode_merges + gi];
+  pdl_wait();  // the partials are complete and visible
+  if (!in) return;
   const int G = p.group;
   const int nrows = dec ? g.n_q * G : g.n_q;
   if (row >= nrows || nrows > rows || g.seq < 0 || g.seq >= p.num_seqs || g.nsplit < 1 ||
-      g.kind != (dec ? 0 : 1))
+      g.kind != (dec ? 0 : 1) || g.q_row0 < 0 || g.q_row0 + (dec ? g.n_q : nrows) > p.total_q)
     return;
   const float2 *ml = (dec ? p.part_ml : p.ppart_ml) + (int64_t)g.part0 * rows + row;
   const float4 *po = reinterpret_cast<const float4 *>((dec ? p.part_o : p.ppart_o) +
@@ -176,8 +180,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
   float L;
   const float4 acc = merge_row<D>(ml, po, g.nsplit, rows, L);
   const float inv = L > 0.f ? 1.f / L : 0.f;
-  const int cu0 = __ldg(p.cu_q_lens + g.seq);
-  const int64_t tok = cu0 + g.qi0 + (dec ? row / G : row);
+  const int64_t tok = g.q_row0 + (dec ? row / G : row);
   const int hq = dec ? g.h * G + row % G : g.h;
   uint2 pk;
   pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
@@ -344,7 +347,6 @@ __device__ __forceinline__ void shared_cta(const CUtensorMap &pool_map, const De
       mbar_init(smem_u32(&empty[s]), kWarps);
     }
     fence_mbar_init();
-    prefetch_tmap(&pool_map);
     if (!item_ok) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
   }
   // q rows, lengths and the first table window are not written by the kernels
@@ -463,17 +465,19 @@ __global__ void __launch_bounds__(kThreads, 2)
   // launched early behind the preceding kernel: let our dependents launch.  The
   // plan, the block tables and q are not written by the kernels this one follows
   // (the KV append writes only the pool), so the warp's range, first piece and
-  // first block-table window are read before waiting for the predecessor; the
-  // pool, the workspace and out are touched only after the wait.
+  // sequence lengths are read and its barriers set up before waiting for the
+  // predecessor; the pool, the workspace and out are touched only after the wait.
   pdl_trigger();
+  if (lane == 0) prefetch_tmap(&pool_map);  // fetched beside the metadata reads below
   if (blockIdx.x >= p.num_indep_ctas) {  // CTA-uniform: a shared-prefix CTA
     shared_cta<D, NSTAGE>(pool_map, p, smem, warp, lane);
     return;
   }
   const int gw = blockIdx.x * kWarps + warp;
   const bool has_warp = gw < p.num_warps;
-  // Start-up is a chain of dependent reads (range -> piece -> table -> pool).
-  // After other work has cycled the caches, each step of that chain also pays
+  // Start-up is a chain of dependent reads (plan -> pool: the first copies take
+  // their block ids from the plan).  After other work has cycled the caches,
+  // each step of that chain also pays
   // address-translation misses; touching the pages of the block tables, of the
   // step's small arrays and of the pool now, all independently, takes those
   // misses in parallel with the first read.  (L2 prefetches only: no data is used.)
@@ -507,15 +511,13 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int G = p.group;
   int win_base = 0, win_val = -1;  // table window: lane i holds entry win_base + i
   bool win_ok = false;
+  // The first copies use the block ids the plan carries, so no table read sits
+  // between the plan read and the first copy; lanes 0-2 read the same entries
+  // from the device table here, checked once the first block has landed.
+  int head_chk = -1;
   if (has_warp && pb < pe && pp.seq >= 0 && pp.seq < p.num_seqs && pp.kb_begin >= 0 &&
-      pp.kb_begin < p.max_blocks_per_seq) {
-    win_base = pp.kb_begin;
-    const int idx = win_base + lane;
-    win_val = idx < min(pp.kb_end, p.max_blocks_per_seq)
-                  ? __ldg(p.block_tables + (int64_t)pp.seq * p.max_blocks_per_seq + idx)
-                  : -1;
-    win_ok = true;
-  }
+      lane < kHeadBlocks && pp.kb_begin + lane < min(pp.kb_end, p.max_blocks_per_seq))
+    head_chk = __ldg(p.block_tables + (int64_t)pp.seq * p.max_blocks_per_seq + pp.kb_begin + lane);
   // the first piece's sequence lengths, also ahead of the wait
   int f_cu0 = 0, f_cu1 = 0, f_ctx = 0;
   if (has_warp && pb < pe && pp.seq >= 0 && pp.seq < p.num_seqs) {
@@ -523,17 +525,15 @@ __global__ void __launch_bounds__(kThreads, 2)
     f_cu1 = __ldg(p.cu_q_lens + pp.seq + 1);
     f_ctx = __ldg(p.context_lens + pp.seq);
   }
-  pdl_wait();
-  if (!has_warp || pb >= pe) return;
-
   uint8_t *ring = smem + warp * C::kRingBytes;
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kBarOffset) + warp * NSTAGE;
   int *stage_ok = reinterpret_cast<int *>(smem + C::kFlagOffset) + warp * NSTAGE;
-  if (lane == 0) {
+  if (lane == 0 && has_warp) {
     for (int s = 0; s < NSTAGE; ++s) mbar_init(smem_u32(&bars[s]), 1);
     fence_mbar_init();
-    prefetch_tmap(&pool_map);
   }
+  pdl_wait();
+  if (!has_warp || pb >= pe) return;
   __syncwarp();
 
   // ---- producer: walks the warp's pieces block by block.  Called by the whole
@@ -541,8 +541,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   // read 32 entries at a time with one coalesced warp load and the entries are
   // shuffled out, so refilling a stage never waits on a dependent global load.
   const Piece first = pp;  // the producer below moves pp ahead of the consumer
-  const int win_first = win_val;  // first window, kept to check the inline block ids
   int ppi = pb, pkb = pp.kb_begin, issued = 0;
+  auto load_window = [&]() {  // whole warp: entries pkb .. pkb + 31 of pp's table
+    win_base = pkb;
+    const int idx = pkb + lane;
+    win_val = idx < min(pp.kb_end, p.max_blocks_per_seq)
+                  ? __ldg(p.block_tables + (int64_t)pp.seq * p.max_blocks_per_seq + idx)
+                  : -1;
+    win_ok = true;
+  };
   auto issue_next = [&](int stage) {
     while (ppi < pe && pkb >= pp.kb_end) {
       if (++ppi < pe) {
@@ -563,19 +570,12 @@ __global__ void __launch_bounds__(kThreads, 2)
     const uint32_t bar = smem_u32(&bars[stage]);
     const bool in_table = pp.seq >= 0 && pp.seq < p.num_seqs && pp.h >= 0 && pp.h < hkv &&
                           pkb >= 0 && pkb < p.max_blocks_per_seq;
-    if (in_table && (!win_ok || pkb >= win_base + 32)) {
-      win_base = pkb;
-      const int idx = pkb + lane;
-      win_val = idx < min(pp.kb_end, p.max_blocks_per_seq)
-                    ? __ldg(p.block_tables + (int64_t)pp.seq * p.max_blocks_per_seq + idx)
-                    : -1;
-      win_ok = true;
-    }
-    // the first copies use the block ids the plan carries, so they do not wait
-    // for the block-table window (checked against it once data has arrived)
+    // the first copies use the block ids the plan carries; no window is read
+    // for them (none is pending, so the shuffle below does not wait either)
     const int inl = ppi == pb && issued < kHeadBlocks
                         ? (issued == 0 ? fb0 : issued == 1 ? fb1 : fb2)
                         : -1;
+    if (inl < 0 && in_table && (!win_ok || pkb >= win_base + 32)) load_window();
     const int phys = inl >= 0 ? inl : __shfl_sync(0xffffffffu, win_val, (pkb - win_base) & 31);
     const bool ok = in_table && phys >= 0 && phys < p.num_blocks;
     if (lane == 0) {
@@ -598,6 +598,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     ++issued;
   };
   for (int s = 0; s < NSTAGE; ++s) issue_next(s);
+  // the window for the next copies, read while the first ones are in flight
+  if (ppi < pe && pkb < pp.kb_end && pp.seq >= 0 && pp.seq < p.num_seqs && pkb >= 0 &&
+      pkb < p.max_blocks_per_seq && (!win_ok || pkb >= win_base + 32))
+    load_window();
 
   const float sl2 = p.scale_log2;
   int stage = 0;
@@ -647,9 +651,9 @@ __global__ void __launch_bounds__(kThreads, 2)
         break;
       }
       ++consumed;
-      if (consumed == 1) {  // the first window has landed by now: check the inline ids
+      if (consumed == 1) {  // the check entries have landed by now: compare the inline ids
         const int want = lane == 0 ? fb0 : lane == 1 ? fb1 : lane == 2 ? fb2 : -1;
-        if (want >= 0 && want != win_first) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
+        if (want >= 0 && want != head_chk) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
       }
       if (valid && stage_ok[stage]) {
         const uint32_t sK = smem_u32(ring + stage * C::kStageBytes);

@@ -105,7 +105,7 @@ struct MergeGroup {
   int32_t part0;
   int32_t nsplit;
   int32_t kind;
-  int32_t pad;
+  int32_t q_row0;  // packed query index of token qi0 (cu_q_lens[seq] + qi0)
 };
 static_assert(sizeof(MergeGroup) == 32, "merge group is 32 bytes");
 

@@ -369,6 +369,7 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
         std::memset(&m, 0, sizeof m);
         m.seq = dunits[u].seq;
         m.qi0 = dunits[u].qi0;
+        m.q_row0 = cu_q_lens[dunits[u].seq] + dunits[u].qi0;
         m.n_q = dunits[u].n_q;
         m.h = h;
         m.part0 = parts;
@@ -474,6 +475,7 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
           std::memset(&m, 0, sizeof m);
           m.seq = src.seq;
           m.qi0 = src.qi0[u.x];
+          m.q_row0 = cu_q_lens[src.seq] + src.qi0[u.x];
           m.n_q = src.n_q[u.x];
           m.h = src.hq[u.x];
           m.part0 = pparts;

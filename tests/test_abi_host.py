@@ -169,6 +169,7 @@ def check_plan(meta, info, host, num_sms):
         a(pp * 128 * d * 4) + a(pp * 128 * 8)
     assert info.workspace_bytes == ws
     nm = info.num_merge_groups
+    assert np.array_equal(mer[:, 7], meta.cu_q_lens[mer[:, 0]] + mer[:, 1])   # packed first row
     assert info.num_prefill_merges == int((mer[:, 6] == 1).sum())
     assert np.all(mer[:nm - info.num_prefill_merges, 6] == 0)   # decode groups first
     assert info.num_kernels == (info.num_decode_warps > 0) + (info.num_merge_groups > 0) + \
