@@ -15,8 +15,12 @@ uploaded per step inside `e2e`.
 * roofline: the dominant kernel alone (split-KV decode: bytes vs the measured
   HBM copy bandwidth; tensor-core prefill: FLOPs vs the measured bf16 peak),
   timed with CUDA events recorded on its launch stream around each launch
-  (library profiling hook), algorithmic bytes (KV + Q + O + metadata) or FLOPs
-  (4 * D * Hq * visible pairs) / mean duration.
+  (library profiling hook), algorithmic bytes or FLOPs / mean duration.  The
+  split-KV kernel's bytes are the K/V blocks its plan streams (a shared prefix
+  the plan reads once per CTA counted once, one gathered onto the tensor cores
+  not at all) plus q, out and metadata; the tensor-core kernel's FLOPs are
+  4 * D * (query row, key) pairs: the causal pairs of prefill-class sequences
+  plus the gathered shared-prefix pairs.
 * e2e: the same metric through the public API from pinned HOST buffers: every
   step copies q, the new K/V, slot mapping and metadata host->device, plans on
   the host, runs append + attention and copies out back (wall time per step).
@@ -98,6 +102,19 @@ def algorithmic_bytes(meta, prefill=None) -> int:
     if prefill is not None:
         live &= (meta.q_lens >= PREFILL_MIN_Q) == prefill
     kv = int(meta.context_lens[live].astype(np.int64).sum()) * 2 * hkv * d * 2
+    qo = 2 * int(meta.q_lens[live].astype(np.int64).sum()) * hq * d * 2
+    nb = int(((meta.context_lens[live].astype(np.int64) + 15) // 16).sum())
+    return kv + qo + 4 * (2 * int(live.sum()) + 1) + 4 * nb
+
+
+def decode_kernel_bytes(meta, info) -> int:
+    """Bytes the split-KV kernel must move for one launch of this plan: the K and V
+    of every (KV block, KV head) pair it streams (a prefix the plan reads once per
+    shared-prefix CTA counted once; a prefix gathered onto the tensor cores not at
+    all), plus the q and out rows of the split-KV sequences and their metadata."""
+    d, hq = meta.head_dim, meta.num_q_heads
+    live = (meta.q_lens > 0) & (meta.q_lens < PREFILL_MIN_Q)
+    kv = int(info.decode_blocks) * 16 * 2 * d * 2
     qo = 2 * int(meta.q_lens[live].astype(np.int64).sum()) * hq * d * 2
     nb = int(((meta.context_lens[live].astype(np.int64) + 15) // 16).sum())
     return kv + qo + 4 * (2 * int(live.sum()) + 1) + 4 * nb
@@ -461,9 +478,11 @@ def bench_pkv(args):
     pk = peaks()
     kv_tok = sum(m.kv_tokens() for m in metas)          # over the chain's steps
     bytes_alg = sum(algorithmic_bytes(m) for m in metas)
-    # kernel events keep the last launch of a chain: its step's bytes
-    dec_bytes = algorithmic_bytes(metas[-1], prefill=False)
-    fl = prefill_flops(meta)
+    # kernel events keep the last launch of a chain: its step's bytes (the plan
+    # of a chain is sized for its last step)
+    dec_bytes = decode_kernel_bytes(metas[-1], info)
+    # tensor-core work: prefill-class sequences and gathered shared-prefix rows
+    fl = prefill_flops(meta) + 4 * meta.head_dim * int(info.gather_pairs)
     kernels = {"append_kernel": {"ms_per_launch": kern_ms["append"]}}
     if kern_ms["merge"]:
         kernels["merge_kernel"] = {"ms_per_launch": kern_ms["merge"]}
@@ -516,7 +535,9 @@ def bench_pkv(args):
             **{k2: cpu[k2] for k2 in ("value", "unit", "cores", "kind", "sample")},
             "value_1core": cpu1["value"], "sample_1core": cpu1["sample"]},
         "plan": {"decode_warps": info.num_decode_warps, "decode_pieces": info.num_decode_pieces,
-                 "merge_groups": info.num_merge_groups, "prefill_tiles": info.num_prefill_tiles},
+                 "merge_groups": info.num_merge_groups, "prefill_tiles": info.num_prefill_tiles,
+                 "shared_prefix_ctas": info.num_shared_ctas,
+                 "gathered_rows": info.num_gather_rows * (meta.num_q_heads // meta.num_kv_heads)},
     }
     if meta.unique_blocks() * 16 < kv_tok and decode_ms:
         line["unique_gbs"] = unique_bytes(meta) / (decode_ms * 1e-3) / 1e9

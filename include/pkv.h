@@ -114,11 +114,18 @@ typedef struct pkv_plan_info {
                                    decode, pkv_plan_decode_chain); 0 for a single step */
   int32_t num_shared_ctas;      /* split-KV CTAs that read a prefix several sequences share
                                    once for up to 4 row groups (needs host block tables) */
-  int32_t reserved;
+  int32_t num_gather_rows;      /* query tokens listed by the tensor-core shared-prefix
+                                   items (a prefix many query rows share is read once per
+                                   128 rows on the tensor cores; needs host block tables) */
   int64_t kv_tokens;         /* sum of context_lens over sequences with q_len > 0 */
-  int64_t decode_blocks;     /* (KV block, KV head) pairs streamed by the split-KV kernel */
+  int64_t decode_blocks;     /* (KV block, KV head) pairs the split-KV kernel attends, each
+                                counted once: per sequence (however many row groups read
+                                it), a prefix its shared-prefix CTAs read once per group,
+                                a prefix gathered onto the tensor cores not at all */
   int64_t plan_bytes;        /* bytes of the plan buffer (host, then device copy) */
   int64_t workspace_bytes;   /* device workspace the attention call needs */
+  int64_t gather_pairs;      /* (query row, key) pairs the tensor-core kernel computes for
+                                gathered shared-prefix rows (row = token x query head) */
 } pkv_plan_info;
 
 /* Library version (major*10000 + minor*100 + patch). */
@@ -253,8 +260,13 @@ PKV_API pkv_status pkv_decode_advance(int32_t *context_lens, int32_t *slot_mappi
  *   aligned; contents on entry do not matter).  Rows of sequences with
  *   q_len == 0 do not exist.  Accumulation is fp32; out is rounded once to bf16.
  *   Kernels are launched with programmatic stream serialisation: their launch
- *   overlaps the tail of the preceding kernel on the stream, and each waits for
- *   that kernel to complete (griddepcontrol.wait) before reading any input.
+ *   overlaps the tail of the preceding kernel on the stream.  Each waits for
+ *   that kernel to complete (griddepcontrol.wait) before it reads kv_pool or
+ *   the workspace; the plan, q, cu_q_lens, context_lens and block_tables are
+ *   read before that wait.  A kernel that lets its dependents launch early
+ *   (griddepcontrol.launch_dependents) and runs right before this call must
+ *   therefore not write those five: this library's KV append writes only
+ *   kv_pool; kernels that do not signal early are simply waited for.
  */
 PKV_API pkv_status pkv_paged_varlen_attention(const void *q, const int32_t *cu_q_lens,
                                       const int32_t *context_lens, const int32_t *block_tables,

@@ -167,10 +167,11 @@ extern "C" pkv_status pkv_paged_varlen_attention(
   if (info->num_prefill_ctas < 0 || info->num_prefill_ctas > info->num_prefill_tiles ||
       (info->num_prefill_tiles > 0 && info->num_prefill_ctas == 0))
     return PKV_ERR_SHAPE;
-  if (info->num_shared_ctas < 0) return PKV_ERR_SHAPE;
-  const PlanOffsets off = plan_offsets(info->num_decode_warps, info->num_decode_pieces,
-                                       info->num_merge_groups, info->num_shared_ctas,
-                                       info->num_prefill_tiles, info->num_prefill_ctas);
+  if (info->num_shared_ctas < 0 || info->num_gather_rows < 0) return PKV_ERR_SHAPE;
+  const PlanOffsets off =
+      plan_offsets(info->num_decode_warps, info->num_decode_pieces, info->num_merge_groups,
+                   info->num_shared_ctas, info->num_prefill_tiles, info->num_prefill_ctas,
+                   info->num_gather_rows);
   a.warp_begin = reinterpret_cast<const int32_t *>(pb + off.warp_begin);
   a.warp_head = reinterpret_cast<const WarpHead *>(pb + off.warp_head);
   a.num_decode_warps = info->num_decode_warps;
@@ -181,6 +182,9 @@ extern "C" pkv_status pkv_paged_varlen_attention(
   a.num_merge_groups = info->num_merge_groups;
   a.prefill_begin = reinterpret_cast<const int32_t *>(pb + off.prefill_begin);
   a.prefill_tiles = reinterpret_cast<const PrefillTile *>(pb + off.prefill);
+  a.gather_rows = reinterpret_cast<const GatherRow *>(pb + off.gather);
+  a.num_gather_rows = info->num_gather_rows;
+  a.num_partials = info->num_partials;
   a.num_prefill_tiles = info->num_prefill_tiles;
   a.num_prefill_ctas = info->num_prefill_ctas;
   if (info->num_prefill_merges < 0 || info->num_prefill_merges > info->num_merge_groups ||

@@ -25,6 +25,7 @@ constexpr int kDecodeWarpsPerCta = 4;
 //   [SharedItem x num_shared_ctas]
 //   [prefill_begin: int32 x (num_prefill_ctas + 1), padded to 32 B; absent when 0 CTAs]
 //   [PrefillTile x num_prefill_tiles, grouped by CTA]
+//   [GatherRow x num_gather_rows] (the query tokens of gathered sub-tiles)
 struct PlanHeader {
   int32_t magic;
   int32_t num_seqs;
@@ -109,14 +110,23 @@ struct MergeGroup {
 };
 static_assert(sizeof(MergeGroup) == 32, "merge group is 32 bytes");
 
-// Tensor-core work item: up to two query sub-tiles of one sequence whose query
-// heads share KV head h, so every K/V tile loaded serves both.  Sub-tile x is
-// query tokens qi0[x] .. qi0[x]+n_q[x]-1 (n_q <= 128) of query head hq[x];
-// sub-tile 0 sees at least as many keys as sub-tile 1; n_q[1] == 0 means a
-// single sub-tile.  The item covers key tiles kt0 .. kt1-1 (128 keys each) of
-// the pair; a sub-tile whose keys the item covers only in part writes its
-// unnormalised result to prefill partial slot part[x] (else part[x] = -1 and it
-// writes out directly).
+// Tensor-core work item: up to two query sub-tiles whose query heads share KV
+// head h, so every K/V tile loaded serves both; keys are read through sequence
+// seq's block table.  The item covers key tiles kt0 .. kt1-1 (128 keys each).
+// n_q[1] == 0 means a single sub-tile.  Sub-tile x is either
+//  * contiguous (gather[x] < 0): query tokens qi0[x] .. qi0[x]+n_q[x]-1 (n_q <=
+//    128) of sequence seq, query head hq[x], causal; sub-tile 0 sees at least as
+//    many keys as sub-tile 1.  A sub-tile whose keys the item covers only in
+//    part writes its unnormalised result to prefill partial slot part[x] (else
+//    part[x] = -1 and it writes out directly); or
+//  * gathered (gather[x] >= 0): rows (token t, head g) = row t * G + g for the
+//    n_q[x] tokens GatherRow[gather[x] ..] (n_q * G <= 128), all G query heads
+//    of KV head h, tokens of any sequences whose tables hold the same physical
+//    blocks over the item's keys, every key visible to every row (no mask).
+//    Row (t, g) writes its unnormalised result to decode partial slot
+//    GatherRow.part0 + part[x], row GatherRow.row0 + g.  When bit x of `runs`
+//    is set the tokens are consecutive packed indices from qi0[x] (loaded as
+//    one box of 128 / G tokens).
 struct PrefillTile {
   int32_t seq;
   int32_t h;
@@ -126,16 +136,31 @@ struct PrefillTile {
   int32_t kt0;
   int32_t kt1;
   int32_t part[2];
+  int32_t gather[2];
+  int32_t runs;
+  int32_t pad;
 };
-static_assert(sizeof(PrefillTile) == 48, "prefill tile is 48 bytes");
+static_assert(sizeof(PrefillTile) == 64, "prefill tile is 64 bytes");
+
+// One query token of a gathered sub-tile: its packed index, the decode partial
+// slot its row group's first key chunk writes, and the row of its first head in
+// that slot.
+struct GatherRow {
+  int32_t q_tok;
+  int32_t part0;
+  int32_t row0;
+  int32_t pad;
+};
+static_assert(sizeof(GatherRow) == 16, "gather row is 16 bytes");
 
 inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
 
 struct PlanOffsets {
-  int64_t warp_begin, warp_head, pieces, merges, shared, prefill_begin, prefill, total;
+  int64_t warp_begin, warp_head, pieces, merges, shared, prefill_begin, prefill, gather, total;
 };
 inline PlanOffsets plan_offsets(int32_t n_warps, int32_t n_pieces, int32_t n_merge,
-                                int32_t n_shared, int32_t n_prefill, int32_t n_prefill_ctas) {
+                                int32_t n_shared, int32_t n_prefill, int32_t n_prefill_ctas,
+                                int32_t n_gather) {
   PlanOffsets o;
   o.warp_begin = (int64_t)sizeof(PlanHeader);
   o.warp_head = o.warp_begin + align_up(4ll * (n_warps + 1), 32);
@@ -144,7 +169,8 @@ inline PlanOffsets plan_offsets(int32_t n_warps, int32_t n_pieces, int32_t n_mer
   o.shared = o.merges + (int64_t)n_merge * (int64_t)sizeof(MergeGroup);
   o.prefill_begin = o.shared + (int64_t)n_shared * (int64_t)sizeof(SharedItem);
   o.prefill = o.prefill_begin + (n_prefill_ctas > 0 ? align_up(4ll * (n_prefill_ctas + 1), 32) : 0);
-  o.total = o.prefill + (int64_t)n_prefill * (int64_t)sizeof(PrefillTile);
+  o.gather = o.prefill + (int64_t)n_prefill * (int64_t)sizeof(PrefillTile);
+  o.total = o.gather + (int64_t)n_gather * (int64_t)sizeof(GatherRow);
   return o;
 }
 
@@ -197,6 +223,9 @@ struct AttnArgs {
   int32_t num_merge_groups;
   const int32_t *prefill_begin;
   const PrefillTile *prefill_tiles;
+  const GatherRow *gather_rows;
+  int32_t num_gather_rows;
+  int32_t num_partials;       // decode partial slots (gathered sub-tiles write into them)
   int32_t num_prefill_tiles;
   int32_t num_prefill_ctas;
   float *part_o;

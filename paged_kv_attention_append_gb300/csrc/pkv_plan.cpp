@@ -19,6 +19,15 @@
 //    cut into several pieces gets one partial slot per piece and a merge group.
 //    Equal ranges leave no tail wave and no long/short CTA imbalance.
 //
+// Shared prefixes (when the planner has the host block tables): decode-class
+// sequences whose tables start with the same physical blocks read those blocks
+// once per work unit rather than once per row group.  When at least 64 query
+// rows per KV head share a prefix of whole 128-key tiles, the prefix goes to the
+// tensor-core kernel as gathered sub-tiles: 128 rows (token x query head) taken
+// from all those sequences attend one key tile per MMA, each row writing a
+// partial result that the merge combines with its own suffix.  Smaller groups
+// use split-KV CTAs that stream the prefix once for up to 4 row groups.
+//
 // Prefill-class rows (tensor-core kernel): sequences with at least 64 query
 // tokens are cut into units of 128 query tokens x one query head.  Units of the
 // same KV head are paired (neighbours in key count: the heads of one token tile,
@@ -78,6 +87,18 @@ struct DUnit {  // a decode row group: n_q tokens from qi0 of seq, reading block
 };
 // Shared prefixes shorter than this many blocks stay on the per-warp ranges.
 constexpr int32_t kMinSharedBlocks = 8;
+// Blocks per 128-key tile of the tensor-core kernel, and the query rows per KV
+// head from which a shared prefix goes to it as gathered sub-tiles.
+constexpr int32_t kKeyTileBlocks = 128 / kBlockSize;
+constexpr int64_t kGatherMinRows = 64;
+
+PrefillTile new_tile() {
+  PrefillTile t;
+  std::memset(&t, 0, sizeof t);
+  t.part[0] = t.part[1] = -1;
+  t.gather[0] = t.gather[1] = -1;
+  return t;
+}
 
 }  // namespace
 }  // namespace pkv
@@ -145,8 +166,7 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
             units.push_back({hq, qi0, n_q, (int64_t)ctx - qs + qi0 + n_q});
         }
         for (size_t u = 0; u < units.size(); u += 2) {
-          PrefillTile t;
-          std::memset(&t, 0, sizeof t);
+          PrefillTile t = new_tile();
           t.seq = s;
           t.h = h;
           t.hq[0] = units[u].hq;
@@ -182,7 +202,8 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   std::vector<int32_t> shared_len(num_seqs, 0);
   struct Group {
     std::vector<int32_t> members;
-    int32_t len;
+    int32_t len;  // shared blocks handled as shared (whole key tiles when tc)
+    bool tc;      // gathered sub-tiles on the tensor-core kernel, else split-KV CTAs
   };
   std::vector<Group> groups;
   if (block_tables && max_blocks_per_seq > 0) {
@@ -208,7 +229,12 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
             break;
           }
       if (len < kMinSharedBlocks) continue;
-      groups.push_back({mem, len});
+      int64_t rows = 0;
+      for (int32_t m : mem) rows += (int64_t)(cu_q_lens[m + 1] - cu_q_lens[m]) * group;
+      const int32_t len_tc = len / kKeyTileBlocks * kKeyTileBlocks;
+      const bool tc = lookahead == 0 && len_tc >= kKeyTileBlocks && rows >= kGatherMinRows;
+      if (tc) len = len_tc;
+      groups.push_back({mem, len, tc});
       for (int32_t m : mem) shared_len[m] = len;
     }
   }
@@ -238,6 +264,7 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
     for (size_t u = dunits.size(); u-- > 0;) unit_of_seq_first[dunits[u].seq] = (int32_t)u;
     int64_t sh_blocks = 0;
     for (const Group &g : groups) {
+      if (g.tc) continue;
       int64_t nrg = 0;
       for (int32_t m : g.members)
         for (size_t u = unit_of_seq_first[m]; u < dunits.size() && dunits[u].seq == m; ++u) ++nrg;
@@ -249,6 +276,7 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
     // prefix is then cut into equal chunks, their count rounded to the nearest
     const int64_t chunk = std::max<int64_t>(kMinBlocksPerWarp, per_slot / 2);
     for (const Group &g : groups) {
+      if (g.tc) continue;
       std::vector<int32_t> us;
       for (int32_t m : g.members)
         for (size_t u = unit_of_seq_first[m]; u < dunits.size() && dunits[u].seq == m; ++u)
@@ -278,6 +306,92 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
     }
   }
   const int64_t shared_slots = (int64_t)sitems.size() * kDecodeWarpsPerCta;
+
+  // ---- gathered sub-tiles (tc groups): per group and KV head, the members'
+  // query tokens in sub-tiles of up to 128 / G tokens (G rows each), neighbours
+  // paired; every pair is cut along the prefix's key tiles into nc equal chunks,
+  // nc chosen so the items about fill the SMs (at least 2 key tiles each)
+  std::vector<GatherRow> gather;          // part0 filled once partial slots are known
+  std::vector<int32_t> gather_uh;         // (decode unit * hkv + KV head) of each entry
+  std::vector<PrefillTile> casc_items;    // already cut along keys
+  std::vector<int32_t> unit_casc(dunits.size(), 0);  // key chunks of each unit's prefix
+  {
+    struct Sub {
+      int32_t first, n;
+    };
+    struct CPair {
+      int32_t gi, h;
+      Sub sub[2];
+      int32_t nsub;
+    };
+    std::vector<CPair> cpairs;
+    const int32_t tok_per_sub = std::max(1, kPrefillRows / group);
+    std::vector<int32_t> unit_first(num_seqs, -1);  // decode units are in sequence order
+    for (size_t u = dunits.size(); u-- > 0;) unit_first[dunits[u].seq] = (int32_t)u;
+    for (size_t gi = 0; gi < groups.size(); ++gi) {
+      const Group &g = groups[gi];
+      if (!g.tc) continue;
+      std::vector<std::array<int32_t, 3>> toks;  // (unit, packed token, row of its first head)
+      for (int32_t m : g.members)
+        for (size_t u = unit_first[m]; u < dunits.size() && dunits[u].seq == m; ++u)
+          for (int32_t i = 0; i < dunits[u].n_q; ++i)
+            toks.push_back({(int32_t)u, cu_q_lens[m] + dunits[u].qi0 + i, i * group});
+      for (int32_t h = 0; h < hkv; ++h) {
+        std::vector<Sub> subs;
+        for (size_t t0 = 0; t0 < toks.size(); t0 += tok_per_sub) {
+          const int32_t n = (int32_t)std::min<size_t>(tok_per_sub, toks.size() - t0);
+          subs.push_back({(int32_t)gather.size(), n});
+          for (int32_t i = 0; i < n; ++i) {
+            const auto &tk = toks[t0 + i];
+            gather.push_back({tk[1], -1, tk[2], 0});
+            gather_uh.push_back(tk[0] * hkv + h);
+          }
+        }
+        for (size_t k = 0; k < subs.size(); k += 2) {
+          CPair cp;
+          cp.gi = (int32_t)gi;
+          cp.h = h;
+          cp.sub[0] = subs[k];
+          cp.sub[1] = k + 1 < subs.size() ? subs[k + 1] : Sub{-1, 0};
+          cp.nsub = k + 1 < subs.size() ? 2 : 1;
+          cpairs.push_back(cp);
+        }
+      }
+    }
+    if (!cpairs.empty()) {
+      const int64_t want = std::max<int64_t>(1, num_sms / (int64_t)cpairs.size());
+      for (const CPair &cp : cpairs) {
+        const Group &g = groups[cp.gi];
+        const int32_t kt = g.len / kKeyTileBlocks;
+        const int32_t nc = (int32_t)std::max<int64_t>(1, std::min<int64_t>(want, kt / 2));
+        for (int32_t m : g.members)
+          for (size_t u = unit_first[m]; u < dunits.size() && dunits[u].seq == m; ++u)
+            unit_casc[u] = nc;
+        for (int32_t c = 0; c < nc; ++c) {
+          PrefillTile t = new_tile();
+          t.seq = g.members[0];
+          t.h = cp.h;
+          t.kt0 = (int32_t)((int64_t)kt * c / nc);
+          t.kt1 = (int32_t)((int64_t)kt * (c + 1) / nc);
+          for (int x = 0; x < cp.nsub; ++x) {
+            t.hq[x] = cp.h * group;
+            t.n_q[x] = cp.sub[x].n;
+            t.gather[x] = cp.sub[x].first;
+            t.part[x] = c;
+            // consecutive packed tokens: one q box for the whole sub-tile
+            bool run = true;
+            for (int32_t i = 1; i < cp.sub[x].n && run; ++i)
+              run = gather[cp.sub[x].first + i].q_tok == gather[cp.sub[x].first].q_tok + i;
+            if (run) {
+              t.runs |= 1 << x;
+              t.qi0[x] = gather[cp.sub[x].first].q_tok;
+            }
+          }
+          casc_items.push_back(t);
+        }
+      }
+    }
+  }
 
   // ---- cut the concatenated suffix blocks into equal-cost warp ranges
   int64_t nw64 = (total_blocks + kMinBlocksPerWarp - 1) / kMinBlocksPerWarp;
@@ -358,13 +472,17 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
       if (seg_first[k] < 0) seg_first[k] = (int32_t)i;
       ++seg_count[k];
     }
+    // gathered prefix chunks always write partials: their unit gets a merge
+    // group even when nothing else splits it
+    std::vector<int32_t> casc_part0(dunits.size() * hkv, -1);
     for (size_t u = 0; u < dunits.size(); ++u)
       for (int32_t h = 0; h < hkv; ++h) {
         const auto &sh = unit_shared[u * hkv + h];
         const int32_t k = seg_of[u * hkv + h];
         const int32_t np = k >= 0 ? seg_count[k] : 0;
-        const int32_t total = (int32_t)sh.size() + np;
-        if (total <= 1) continue;
+        const int32_t nc = unit_casc[u];
+        const int32_t total = nc + (int32_t)sh.size() + np;
+        if (total <= 1 && nc == 0) continue;
         MergeGroup m;
         std::memset(&m, 0, sizeof m);
         m.seq = dunits[u].seq;
@@ -374,12 +492,17 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
         m.h = h;
         m.part0 = parts;
         m.nsplit = total;
+        casc_part0[u * hkv + h] = nc > 0 ? parts : -1;
+        parts += nc;
         for (const auto &si : sh) sitems[si[0]].rg[si[1]].part = parts++;
         for (int32_t t = 0; t < np; ++t) pieces[seg_first[k] + t].part = parts++;
         merges.push_back(m);
       }
+    for (size_t i = 0; i < gather.size(); ++i) gather[i].part0 = casc_part0[gather_uh[i]];
   }
   // ---- prefill work per persistent CTA (at most one per SM), equal cost:
+  //  0. the gathered prefix items (already cut along keys), largest first, each
+  //     into the least-loaded CTA;
   //  1. whole pairs, largest first, each into the least-loaded CTA that stays
   //     within the per-CTA target;
   //  2. the pairs left over are split into their sub-tiles, whose key tiles are
@@ -390,18 +513,26 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   std::vector<MergeGroup> pmerges;
   int32_t pparts = 0;
   int32_t n_pf_ctas = 0;
-  if (!pairs.empty()) {
+  if (!pairs.empty() || !casc_items.empty()) {
     auto pair_cost = [&](size_t pi) {
       const int64_t nt0 = pair_nt[pi][0], nt1 = pair_nt[pi][1];
       return kItemStartCost + kPairTileCost * nt1 + kSingleTileCost * (nt0 - nt1);
+    };
+    auto item_cost = [&](const PrefillTile &t) {
+      return kItemStartCost + (t.n_q[1] > 0 ? kPairTileCost : kSingleTileCost) * (t.kt1 - t.kt0);
     };
     int64_t total = 0, ntiles = 0;
     for (size_t pi = 0; pi < pairs.size(); ++pi) {
       total += pair_cost(pi);
       ntiles += pair_nt[pi][0];
     }
+    for (const PrefillTile &t : casc_items) {
+      total += item_cost(t);
+      ntiles += t.kt1 - t.kt0;
+    }
     n_pf_ctas = (int32_t)std::max<int64_t>(
-        1, std::min<int64_t>(num_sms, ntiles / kMinTilesPerCta));
+        1, std::min<int64_t>(num_sms, std::max<int64_t>(ntiles / kMinTilesPerCta,
+                                                        (int64_t)casc_items.size())));
     const int64_t target = (total + n_pf_ctas - 1) / n_pf_ctas;
     std::vector<size_t> order(pairs.size());
     for (size_t i = 0; i < order.size(); ++i) order[i] = i;
@@ -409,6 +540,18 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
                      [&](size_t x, size_t y) { return pair_cost(x) > pair_cost(y); });
     std::vector<int64_t> load(n_pf_ctas, 0);
     std::vector<std::vector<PrefillTile>> per_cta(n_pf_ctas);
+    {
+      std::vector<size_t> corder(casc_items.size());
+      for (size_t i = 0; i < corder.size(); ++i) corder[i] = i;
+      std::stable_sort(corder.begin(), corder.end(), [&](size_t x, size_t y) {
+        return item_cost(casc_items[x]) > item_cost(casc_items[y]);
+      });
+      for (size_t ci : corder) {
+        const int32_t best = (int32_t)(std::min_element(load.begin(), load.end()) - load.begin());
+        load[best] += item_cost(casc_items[ci]);
+        per_cta[best].push_back(casc_items[ci]);
+      }
+    }
     std::vector<size_t> leftover;
     for (size_t pi : order) {
       int32_t best = -1;
@@ -485,8 +628,7 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
           pparts += (int32_t)pcs.size();
         }
         for (size_t k = 0; k < pcs.size(); ++k) {
-          PrefillTile t;
-          std::memset(&t, 0, sizeof t);
+          PrefillTile t = new_tile();
           t.seq = src.seq;
           t.h = src.h;
           t.hq[0] = src.hq[u.x];
@@ -510,8 +652,9 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   for (const MergeGroup &m : pmerges) merges.push_back(m);  // after the decode groups
 
   // ---- sizes
-  const PlanOffsets off = plan_offsets(num_warps, (int32_t)pieces.size(), (int32_t)merges.size(),
-                                       (int32_t)sitems.size(), (int32_t)ptiles.size(), n_pf_ctas);
+  const PlanOffsets off =
+      plan_offsets(num_warps, (int32_t)pieces.size(), (int32_t)merges.size(),
+                   (int32_t)sitems.size(), (int32_t)ptiles.size(), n_pf_ctas, (int32_t)gather.size());
   std::memset(info, 0, sizeof *info);
   info->num_seqs = num_seqs;
   info->num_q_heads = num_q_heads;
@@ -529,9 +672,24 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   info->num_kernels = (num_warps > 0 || !sitems.empty() ? 1 : 0) + (merges.empty() ? 0 : 1) +
                       (ptiles.empty() ? 0 : 1);
   info->num_shared_ctas = (int32_t)sitems.size();
+  info->num_gather_rows = (int32_t)gather.size();
   info->max_blocks_needed = max_nb;
   info->kv_tokens = kv_tokens;
-  info->decode_blocks = total_blocks;
+  // blocks the split-KV kernel attends, each once: every decode-class sequence's
+  // blocks past its shared part, plus each CTA-path group's shared blocks
+  int64_t dec_blocks = 0, gather_pairs = 0;
+  {
+    std::vector<int32_t> seq_nb(num_seqs, 0);
+    for (const DUnit &du : dunits) seq_nb[du.seq] = std::max(seq_nb[du.seq], du.nb);
+    for (int32_t s = 0; s < num_seqs; ++s)
+      if (seq_nb[s] > shared_len[s]) dec_blocks += (int64_t)hkv * (seq_nb[s] - shared_len[s]);
+    for (const Group &g : groups)
+      if (!g.tc) dec_blocks += (int64_t)hkv * g.len;
+  }
+  for (const PrefillTile &t : casc_items)
+    gather_pairs += (int64_t)(t.n_q[0] + t.n_q[1]) * group * (t.kt1 - t.kt0) * 128;
+  info->decode_blocks = dec_blocks;
+  info->gather_pairs = gather_pairs;
   info->plan_bytes = off.total;
   info->workspace_bytes = ws_total_bytes(parts, pparts, desc->head_dim);
   info->lookahead = lookahead;
@@ -554,6 +712,7 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   h.num_partials = parts;
   h.num_prefill_tiles = info->num_prefill_tiles;
   h.max_blocks_needed = max_nb;
+  h.reserved[0] = (int32_t)gather.size();
   std::memcpy(p, &h, sizeof h);
   std::memcpy(p + off.warp_begin, warp_begin.data(), warp_begin.size() * sizeof(int32_t));
   for (int32_t w = 0; w < num_warps; ++w) {
@@ -577,6 +736,8 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
     std::memcpy(p + off.prefill_begin, pf_begin.data(), pf_begin.size() * sizeof(int32_t));
     std::memcpy(p + off.prefill, ptiles.data(), ptiles.size() * sizeof(PrefillTile));
   }
+  if (!gather.empty())
+    std::memcpy(p + off.gather, gather.data(), gather.size() * sizeof(GatherRow));
   return PKV_OK;
 }
 

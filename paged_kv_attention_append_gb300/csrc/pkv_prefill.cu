@@ -10,6 +10,15 @@
 //
 // One CTA = two query sub-tiles (x = 0, 1) of 128 tokens x one query head each,
 // whose heads share one KV head: every K/V tile is loaded once for both.
+// A sub-tile may instead be gathered: 128 rows (query token x query head, all
+// G heads of the KV head) from several sequences whose block tables hold the
+// same physical blocks over the item's keys -- a shared prefix, read once per
+// 128 rows on the tensor cores instead of once per row group.  Its tokens are
+// loaded one 3-D box each (G heads x 64 columns), landing at rows t*G .. in the
+// same swizzled layout; no mask applies (the planner keeps only keys every row
+// sees), and each row's unnormalised result goes to the split-KV kernel's
+// partial slot of its row group, where the merge combines it with the rest of
+// that row group's keys.
 // Ten warps with fixed roles:
 //   warp 8     TMA producer: both Q sub-tiles (3-D tensor map over
 //              [total_q][Hq][D]) and, per 128-key tile, K then V into a ring of
@@ -38,6 +47,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <cmath>
 
 #include "pkv_device.cuh"
@@ -99,6 +109,12 @@ struct PrefillParams {
   const PrefillTile *tiles;
   float *ppart_o;     // [part][128][D] fp32: unnormalised O of a sub-tile cut along keys
   float2 *ppart_ml;   // [part][128]: (row max in log2 units, row sum) of the same
+  const GatherRow *gather;  // tokens of gathered sub-tiles
+  float *dpart_o;     // split-KV partial slots [part][16][D]: gathered rows' results
+  float2 *dpart_ml;   // [part][16]
+  int32_t num_gather;
+  int32_t num_dparts;
+  int64_t total_q;
   int32_t *dev_status;
   int32_t num_seqs;
   int32_t max_blocks_per_seq;
@@ -111,6 +127,32 @@ struct PrefillParams {
 };
 
 
+// 8 x 8 transpose of 16-byte pieces within each group of 8 lanes: lane g of a
+// group holds pieces a[0..7] of row g on entry and piece g of rows 0..7 of its
+// group on exit.  Three butterfly stages: at stage s a lane swaps, with lane
+// g ^ s, the four pieces whose index differs from g in bit s.
+__device__ __forceinline__ void transpose8x8(float4 (&a)[8], int g) {
+#pragma unroll
+  for (int s = 1; s < 8; s <<= 1) {
+    const bool hi = (g & s) != 0;
+#pragma unroll
+    for (int j0 = 0; j0 < 8; ++j0) {
+      if (j0 & s) continue;
+      const int j1 = j0 | s;
+      const float4 send = hi ? a[j0] : a[j1];
+      float4 recv;
+      recv.x = __shfl_xor_sync(0xffffffffu, send.x, s);
+      recv.y = __shfl_xor_sync(0xffffffffu, send.y, s);
+      recv.z = __shfl_xor_sync(0xffffffffu, send.z, s);
+      recv.w = __shfl_xor_sync(0xffffffffu, send.w, s);
+      if (hi)
+        a[j0] = recv;
+      else
+        a[j1] = recv;
+    }
+  }
+}
+
 // One work item's metadata, computed identically by every role (so every role
 // skips the same invalid items and agrees on all barrier phases).
 struct ItemMeta {
@@ -118,6 +160,7 @@ struct ItemMeta {
   int cu0, qs, ctx;
   int nt[2];  // key tiles sub-tile x runs in this item, from t.kt0 (0 when absent)
   int nkt;    // key tiles loaded: t.kt0 .. t.kt1-1
+  bool gathered;  // both present sub-tiles are gathered (else both contiguous)
   bool ok;
 };
 
@@ -125,14 +168,21 @@ __device__ __forceinline__ ItemMeta load_item(const PrefillParams &p, int it) {
   ItemMeta m;
   m.t = p.tiles[it];
   const PrefillTile &t = m.t;
+  m.gathered = t.gather[0] >= 0;
+  // rows of a sub-tile: tokens, or tokens x G heads when gathered
+  const int rmul = m.gathered ? p.group : 1;
   bool ok = t.seq >= 0 && t.seq < p.num_seqs && t.h >= 0 && t.h < p.num_kv_heads &&
-            t.n_q[0] >= 1 && t.n_q[0] <= kPrefillRows && t.n_q[1] >= 0 &&
-            t.n_q[1] <= kPrefillRows;
+            t.n_q[0] >= 1 && t.n_q[0] * rmul <= kPrefillRows && t.n_q[1] >= 0 &&
+            t.n_q[1] * rmul <= kPrefillRows;
 #pragma unroll
   for (int x = 0; x < 2; ++x)
-    if (t.n_q[x] > 0)
-      ok = ok && t.hq[x] / p.group == t.h && t.hq[x] >= 0 && t.hq[x] < p.num_q_heads &&
-           t.qi0[x] >= 0;
+    if (t.n_q[x] > 0) {
+      if (m.gathered)
+        ok = ok && t.gather[x] >= 0 && t.gather[x] + t.n_q[x] <= p.num_gather && t.part[x] >= 0;
+      else
+        ok = ok && t.gather[x] < 0 && t.hq[x] / p.group == t.h && t.hq[x] >= 0 &&
+             t.hq[x] < p.num_q_heads && t.qi0[x] >= 0;
+    }
   ok = ok && t.kt0 >= 0 && t.kt0 < t.kt1;
   m.cu0 = m.qs = m.ctx = 0;
   if (ok) {
@@ -140,14 +190,19 @@ __device__ __forceinline__ ItemMeta load_item(const PrefillParams &p, int it) {
     m.qs = __ldg(p.cu_q_lens + t.seq + 1) - m.cu0;
     m.ctx = __ldg(p.context_lens + t.seq);
     ok = m.qs <= m.ctx;
+    if (m.gathered)  // every row of the table's own sequence sees all of the item's keys
+      ok = ok && (int64_t)t.kt1 * kKeysPerTile <= (int64_t)m.ctx - m.qs + 1;
+    else
 #pragma unroll
-    for (int x = 0; x < 2; ++x)
-      if (t.n_q[x] > 0) ok = ok && t.qi0[x] + t.n_q[x] <= m.qs;
+      for (int x = 0; x < 2; ++x)
+        if (t.n_q[x] > 0) ok = ok && t.qi0[x] + t.n_q[x] <= m.qs;
   }
   int seen[2];  // key tiles sub-tile x sees in all
 #pragma unroll
   for (int x = 0; x < 2; ++x)
-    seen[x] = ok && t.n_q[x] > 0 ? (m.ctx - m.qs + t.qi0[x] + t.n_q[x] - 1) / kKeysPerTile + 1 : 0;
+    seen[x] = !ok || t.n_q[x] == 0 ? 0
+              : m.gathered         ? t.kt1
+                                   : (m.ctx - m.qs + t.qi0[x] + t.n_q[x] - 1) / kKeysPerTile + 1;
   // the item's key range lies inside what sub-tile 0 sees; a present sub-tile
   // runs at least one of its tiles
   ok = ok && t.kt1 <= seen[0] && (t.n_q[1] == 0 || t.kt0 < seen[1]);
@@ -161,22 +216,24 @@ __device__ __forceinline__ ItemMeta load_item(const PrefillParams &p, int it) {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap q_map,
+                   const __grid_constant__ CUtensorMap qg_map,
+                   const __grid_constant__ CUtensorMap qr_map,
                    const __grid_constant__ CUtensorMap kv_map, const PrefillParams p) {
   using C = PrefillCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // launched early behind the preceding kernel: let our dependents launch, then
-  // wait for the predecessor's writes (pool, q, metadata) before reading anything
+  // launched early behind the preceding kernel: let our dependents launch.  The
+  // plan, q and the step metadata are not written by the kernels this one
+  // follows (the KV append writes only the pool), so barriers, TMEM, the work
+  // items and the q tiles go ahead; the producer waits for the predecessor
+  // before its first pool read, and no other role reads the pool.
   pdl_trigger();
-  pdl_wait();
   // this CTA's bin of work items, run one after another; every barrier keeps
-  // counting phases across items
+  // counting phases across items (an item that fails its checks is skipped by
+  // every role alike and reported by the producer)
   const int it0 = __ldg(p.bin_begin + blockIdx.x), it1 = __ldg(p.bin_begin + blockIdx.x + 1);
-  if (threadIdx.x == 0)
-    for (int it = it0; it < it1; ++it)
-      if (!load_item(p, it).ok) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
 
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + B_COUNT);
@@ -220,6 +277,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ======================================================== TMA producer (whole warp)
     if (lane == 0) {
       prefetch_tmap(&q_map);
+      prefetch_tmap(&qg_map);
+      prefetch_tmap(&qr_map);
       prefetch_tmap(&kv_map);
     }
     // Ring load L (counted over the CTA's items) is K_j (even) or V_j (odd) of
@@ -230,33 +289,98 @@ __global__ void __launch_bounds__(kThreads, 1)
     // S MMA of the previous item has read its Q (B_Q_EMPTY).
     const int hkv = p.num_kv_heads;
     int L = 0, nq = 0;  // ring loads and Q loads issued
-    bool good = true;
+    bool good = true, waited = false;
     for (int it = it0; it < it1 && good; ++it) {
       const ItemMeta m = load_item(p, it);
-      if (!m.ok) continue;
+      if (!m.ok) {
+        if (lane == 0) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
+        continue;
+      }
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+      const int32_t *table = p.block_tables + (int64_t)m.t.seq * p.max_blocks_per_seq;
+      const int nblk_ctx = (m.ctx + kBlockSize - 1) / kBlockSize;
+      // lane b < 8: the physical id of block b of key tile j (-1: none, zero fill)
+      auto tile_block = [&](int j) -> int {
+        const int kb = j * kBlocksPerTile + lane;
+        return lane < kBlocksPerTile && kb < nblk_ctx && kb < p.max_blocks_per_seq
+                   ? __ldg(table + kb)
+                   : -1;
+      };
+      int phys_first = tile_block(m.t.kt0);  // read now: it lands while q is loaded
       if (nq > 0 &&
           !__all_sync(0xffffffffu, mbar_wait(bar(B_Q_EMPTY), (uint32_t)((nq - 1) & 1)))) {
         if (lane == 0) fail();
         break;
       }
-      if (lane == 0) {
-        const int nsub = m.t.n_q[1] > 0 ? 2 : 1;
-        mbar_arrive_expect_tx(bar(B_Q_FULL), nsub * C::kQBytes);
+      const int nsub = m.t.n_q[1] > 0 ? 2 : 1;
+      if (!m.gathered) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar(B_Q_FULL), nsub * C::kQBytes);
 #pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          if (x >= nsub) break;
-          const uint32_t sq = smem_u32(smem + C::kOffQ + x * C::kQBytes);
+          for (int x = 0; x < 2; ++x) {
+            if (x >= nsub) break;
+            const uint32_t sq = smem_u32(smem + C::kOffQ + x * C::kQBytes);
+#pragma unroll
+            for (int hh = 0; hh < C::kHalves; ++hh)
+              tma_load_3d(sq + hh * C::kQHalfBytes, &q_map, hh * 64, m.t.hq[x],
+                          m.cu0 + m.t.qi0[x], bar(B_Q_FULL));
+          }
+        }
+        __syncwarp();
+      } else {
+        // one box per token (its G heads x 64 columns, rows t*G ..); a token
+        // index outside q reads as zeros (and is reported), so the byte count
+        // the barrier expects holds either way
+        // a sub-tile of consecutive tokens is one box of 128 / G tokens (rows
+        // past its n_q * G hold other tokens or zeros and are masked); any
+        // other gets one box per token
+        const int G = p.group, row_bytes = G * 128, run_tokens = kPrefillRows / G;
+        const bool r0 = (m.t.runs & 1) != 0, r1 = nsub > 1 && (m.t.runs & 2) != 0;
+        const int n0 = m.t.n_q[0], n1 = nsub > 1 ? m.t.n_q[1] : 0;
+        const int l0 = r0 ? 0 : n0, l1 = r1 ? 0 : n1;  // tokens loaded one by one
+        if (lane == 0) {
+          mbar_arrive_expect_tx(
+              bar(B_Q_FULL),
+              ((r0 ? run_tokens : n0) + (nsub > 1 ? (r1 ? run_tokens : n1) : 0)) * row_bytes *
+                  C::kHalves);
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
+            if (!(x ? r1 : r0)) continue;
+            const uint32_t sq = smem_u32(smem + C::kOffQ + x * C::kQBytes);
+#pragma unroll
+            for (int hh = 0; hh < C::kHalves; ++hh)
+              tma_load_3d(sq + hh * C::kQHalfBytes, &qr_map, hh * 64, m.t.h * G,
+                          x ? m.t.qi0[1] : m.t.qi0[0], bar(B_Q_FULL));
+          }
+        }
+        __syncwarp();
+        // token tk = lane + 32 r of sub-tile x (<= 128 tokens each): all token
+        // indices are read first, so their latencies overlap
+        int qt[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int x = i >> 2, tk = lane + 32 * (i & 3);
+          qt[i] = tk < (x ? l1 : l0) ? __ldg(&p.gather[(x ? m.t.gather[1] : m.t.gather[0]) + tk].q_tok)
+                                     : 0;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int x = i >> 2, tk = lane + 32 * (i & 3);
+          if (tk >= (x ? l1 : l0)) continue;
+          if (qt[i] < 0 || qt[i] >= p.total_q) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
+          const uint32_t sq = smem_u32(smem + C::kOffQ + x * C::kQBytes) + tk * row_bytes;
 #pragma unroll
           for (int hh = 0; hh < C::kHalves; ++hh)
-            tma_load_3d(sq + hh * C::kQHalfBytes, &q_map, hh * 64, m.t.hq[x],
-                        m.cu0 + m.t.qi0[x], bar(B_Q_FULL));
+            tma_load_3d(sq + hh * C::kQHalfBytes, &qg_map, hh * 64, m.t.h * G, qt[i], bar(B_Q_FULL));
         }
+        __syncwarp();
       }
-      __syncwarp();
       ++nq;
-      const int32_t *table = p.block_tables + (int64_t)m.t.seq * p.max_blocks_per_seq;
-      const int nblk_ctx = (m.ctx + kBlockSize - 1) / kBlockSize;
+      // the pool is the predecessor's output: wait for it before the first copy
+      if (!waited) {
+        pdl_wait();
+        waited = true;
+      }
       int g_k = p.pool_groups;  // this lane's K group coordinate for the current tile
       for (int jl = 0; jl < 2 * m.nkt; ++jl) {
         if (__any_sync(0xffffffffu, *abort_flag != 0)) {
@@ -265,15 +389,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int j = m.t.kt0 + (jl >> 1);  // absolute key tile
         if ((jl & 1) == 0) {
-          const int kb = j * kBlocksPerTile + lane;
+          const int phys = jl == 0 ? phys_first : tile_block(j);
           g_k = p.pool_groups;  // out of range: zero fill, no memory traffic
-          if (lane < kBlocksPerTile && kb < nblk_ctx && kb < p.max_blocks_per_seq) {
-            const int phys = __ldg(table + kb);
-            if (phys >= 0 && phys < p.num_blocks)
-              g_k = ((phys * 2 + 0) * hkv + m.t.h) * (kBlockSize / 8);
-            else
-              report(p.dev_status, PKV_DEV_BAD_BLOCK);
-          }
+          if (phys >= 0 && phys < p.num_blocks)
+            g_k = ((phys * 2 + 0) * hkv + m.t.h) * (kBlockSize / 8);
+          else if (phys != -1 || (lane < kBlocksPerTile &&
+                                  j * kBlocksPerTile + lane < min(nblk_ctx, p.max_blocks_per_seq)))
+            report(p.dev_status, PKV_DEV_BAD_BLOCK);
         }
         const int s = L % C::kSlots;
         if (L >= C::kSlots &&
@@ -294,6 +416,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++L;
       }
     }
+    // the kernel must not complete before its predecessor (the next kernel's
+    // wait covers ours only), even when this CTA had no valid item
+    if (!waited) pdl_wait();
     // our copies still in flight land before the CTA can exit: only the last
     // load of each slot can be pending (a slot is refilled after it was consumed)
     if (lane == 0) {
@@ -410,8 +535,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n_q = x ? m.t.n_q[1] : m.t.n_q[0];
       const int ntx = x ? m.nt[1] : m.nt[0];
       if (!m.ok || ntx == 0) continue;
-      // last visible key of this row
-      const int lim = row < n_q ? m.ctx - m.qs + (x ? m.t.qi0[1] : m.t.qi0[0]) + row : -1;
+      // last visible key of this row (gathered rows see every key of the item)
+      const int rows_x = m.gathered ? n_q * p.group : n_q;
+      const int lim = row >= rows_x ? -1
+                      : m.gathered  ? INT_MAX / 2
+                                    : m.ctx - m.qs + (x ? m.t.qi0[1] : m.t.qi0[0]) + row;
       float m_used = -INFINITY, l = 0.f;
       for (int j = 0; j < ntx; ++j) {
         if (__any_sync(0xffffffffu, *abort_flag != 0)) {
@@ -521,30 +649,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::fence_after_sync();
       int out_row, hq, part;  // re-read rather than kept live through the tile loop
+      float *prow = nullptr;  // partial destination of this row, if any
+      float2 *pml = nullptr;
       {
         const ItemMeta me = load_item(p, it);
         out_row = me.cu0 + (x ? me.t.qi0[1] : me.t.qi0[0]) + row;
         hq = x ? me.t.hq[1] : me.t.hq[0];
         part = x ? me.t.part[1] : me.t.part[0];
+        if (me.gathered) {
+          // row (t, g): the split-KV partial slot of token t's row group for
+          // this key chunk, at the row of head g
+          if (row < rows_x) {
+            const GatherRow gr = p.gather[(x ? me.t.gather[1] : me.t.gather[0]) + row / p.group];
+            const int slot = gr.part0 + part, srow = gr.row0 + row % p.group;
+            if (gr.part0 >= 0 && slot < p.num_dparts && srow >= 0 && srow < kRowsPerTile) {
+              prow = p.dpart_o + ((int64_t)slot * kRowsPerTile + srow) * D;
+              pml = p.dpart_ml + (int64_t)slot * kRowsPerTile + srow;
+            } else {
+              report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
+            }
+          }
+        } else if (part >= 0 && row < n_q) {
+          // keys of this sub-tile are split over several items: unnormalised O
+          // and (m, l) to its partial slot, combined by the merge kernel
+          prow = p.ppart_o + ((int64_t)part * kPrefillRows + row) * D;
+          pml = p.ppart_ml + (int64_t)part * kPrefillRows + row;
+        }
+        if (me.gathered) part = 0;  // never written out directly
       }
       if (part >= 0) {
-        // keys of this sub-tile are split over several items: unnormalised O
-        // and (m, l) to its partial slot, combined by the merge kernel
-        float *prow = p.ppart_o + ((int64_t)part * kPrefillRows + row) * D;
+        // unnormalised O: each lane holds its row's 32-column chunk as 8 pieces
+        // of 16 bytes; transposed within groups of 8 lanes, one store covers
+        // 4 rows x 128 contiguous bytes rather than 32 rows x 16 bytes
+        const int gl = lane & 7, gbase = lane & ~7;
+        float *rows8[8];  // destination rows of this lane's group
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          rows8[k] = reinterpret_cast<float *>(
+              __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(prow), gbase + k));
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t ov[32];
           tc::ld32(to + 32 * c, ov);
           tc::wait_ld();
-          if (row < n_q) {
-            float4 *dst = reinterpret_cast<float4 *>(prow + 32 * c);
+          float4 pc[8];
 #pragma unroll
-            for (int v4 = 0; v4 < 8; ++v4)
-              dst[v4] = make_float4(__uint_as_float(ov[4 * v4]), __uint_as_float(ov[4 * v4 + 1]),
-                                    __uint_as_float(ov[4 * v4 + 2]), __uint_as_float(ov[4 * v4 + 3]));
-          }
+          for (int v4 = 0; v4 < 8; ++v4)
+            pc[v4] = make_float4(__uint_as_float(ov[4 * v4]), __uint_as_float(ov[4 * v4 + 1]),
+                                 __uint_as_float(ov[4 * v4 + 2]), __uint_as_float(ov[4 * v4 + 3]));
+          transpose8x8(pc, gl);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            if (rows8[k]) reinterpret_cast<float4 *>(rows8[k] + 32 * c)[gl] = pc[k];
         }
-        if (row < n_q) p.ppart_ml[(int64_t)part * kPrefillRows + row] = make_float2(m_used, l);
+        if (pml) *pml = make_float2(m_used, l);
         tc::fence_before_sync();
         run0 += ntx;
         continue;
@@ -598,13 +756,15 @@ EncodeTiledFn encoder() {
   return reinterpret_cast<EncodeTiledFn>(ptr);
 }
 
-// 3-D view of q: [total_q][Hq][D], box = 128 tokens x 1 head x 64 elements.
-int make_q_map(CUtensorMap *map, const void *q, int64_t total_q, int hq, int d) {
+// 3-D view of q: [total_q][Hq][D], box = `tokens` tokens x `heads` heads x 64
+// elements (128 x 1 for contiguous sub-tiles, 1 x G for gathered ones).
+int make_q_map(CUtensorMap *map, const void *q, int64_t total_q, int hq, int d, int heads,
+               int tokens) {
   EncodeTiledFn enc = encoder();
   if (!enc) return (int)cudaErrorNotSupported;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)hq, (cuuint64_t)(total_q > 0 ? total_q : 1)};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)hq * d * 2};
-  cuuint32_t box[3] = {64, 1, (cuuint32_t)kPrefillRows};
+  cuuint32_t box[3] = {64, (cuuint32_t)heads, (cuuint32_t)tokens};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -613,7 +773,8 @@ int make_q_map(CUtensorMap *map, const void *q, int64_t total_q, int hq, int d) 
 }
 
 template <int D>
-int launch_prefill_t(const AttnArgs &a, const CUtensorMap &qmap, const CUtensorMap &kvmap) {
+int launch_prefill_t(const AttnArgs &a, const CUtensorMap &qmap, const CUtensorMap &qgmap,
+                     const CUtensorMap &qrmap, const CUtensorMap &kvmap) {
   using C = PrefillCfg<D>;
   auto kern = prefill_kernel<D>;
   cudaError_t e =
@@ -628,6 +789,12 @@ int launch_prefill_t(const AttnArgs &a, const CUtensorMap &qmap, const CUtensorM
   p.tiles = a.prefill_tiles;
   p.ppart_o = a.ppart_o;
   p.ppart_ml = reinterpret_cast<float2 *>(a.ppart_ml);
+  p.gather = a.gather_rows;
+  p.num_gather = a.num_gather_rows;
+  p.dpart_o = a.part_o;
+  p.dpart_ml = reinterpret_cast<float2 *>(a.part_ml);
+  p.num_dparts = a.num_partials;
+  p.total_q = a.total_q;
   p.dev_status = a.dev_status;
   p.num_seqs = a.num_seqs;
   p.max_blocks_per_seq = a.max_blocks_per_seq;
@@ -639,7 +806,7 @@ int launch_prefill_t(const AttnArgs &a, const CUtensorMap &qmap, const CUtensorM
   p.scale_log2 = a.scale * 1.4426950408889634f;
   profile_begin(PKV_KERNEL_PREFILL, a.stream);
   e = launch_kernel(kern, dim3((unsigned)a.num_prefill_ctas), dim3(kThreads), C::kSmemBytes,
-                    a.stream, !profiling_active(), qmap, kvmap, p);
+                    a.stream, !profiling_active(), qmap, qgmap, qrmap, kvmap, p);
   profile_end(PKV_KERNEL_PREFILL, a.stream);
   return e != cudaSuccess ? (int)e : (int)cudaGetLastError();
 }
@@ -648,13 +815,19 @@ int launch_prefill_t(const AttnArgs &a, const CUtensorMap &qmap, const CUtensorM
 
 int launch_prefill(const AttnArgs &a, int *launches) {
   if (a.num_prefill_tiles <= 0 || a.num_prefill_ctas <= 0) return 0;
-  CUtensorMap qmap, kvmap;
-  int e = make_q_map(&qmap, a.q, a.total_q, a.num_q_heads, a.desc.head_dim);
+  CUtensorMap qmap, qgmap, qrmap, kvmap;
+  const int group = a.num_q_heads / a.desc.num_kv_heads;
+  int e = make_q_map(&qmap, a.q, a.total_q, a.num_q_heads, a.desc.head_dim, 1, kPrefillRows);
+  if (e) return e;
+  e = make_q_map(&qgmap, a.q, a.total_q, a.num_q_heads, a.desc.head_dim, group, 1);
+  if (e) return e;
+  e = make_q_map(&qrmap, a.q, a.total_q, a.num_q_heads, a.desc.head_dim, group,
+                 kPrefillRows / group);
   if (e) return e;
   e = make_pool_map(&kvmap, a.kv_pool, a.desc);
   if (e) return e;
-  e = a.desc.head_dim == 128 ? launch_prefill_t<128>(a, qmap, kvmap)
-                             : launch_prefill_t<64>(a, qmap, kvmap);
+  e = a.desc.head_dim == 128 ? launch_prefill_t<128>(a, qmap, qgmap, qrmap, kvmap)
+                             : launch_prefill_t<64>(a, qmap, qgmap, qrmap, kvmap);
   if (!e) {
     ++*launches;
     count_launches(1);

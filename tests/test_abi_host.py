@@ -54,14 +54,18 @@ def parse_plan(info, host):
     off_s = off_m + 8 * nm
     off_b = off_s + 40 * nsh
     off_f = off_b + (((ncta + 1 + 7) // 8) * 8 if ncta else 0)
-    assert info.plan_bytes == 4 * (off_f + 12 * npf)
+    off_g = off_f + 16 * npf
+    ng = info.num_gather_rows
+    assert hdr[12] == ng
+    assert info.plan_bytes == 4 * (off_g + 4 * ng)
     wb = words[off_w:off_w + nw + 1]
     pieces = words[off_p:off_m].reshape(npc, 8)
     heads = words[off_first:off_p].reshape(nw, 12)
     if nw:
         assert np.array_equal(heads[:, :8], pieces[wb[:-1]])  # each warp's first piece, copied
     mer = words[off_m:off_s].reshape(nm, 8)
-    pre = words[off_f:off_f + 12 * npf].reshape(npf, 12)
+    pre = words[off_f:off_g].reshape(npf, 16)
+    parse_plan.gather = words[off_g:off_g + 4 * ng].reshape(ng, 4)
     parse_plan.shared = words[off_s:off_b].reshape(nsh, 40)
     pb = words[off_b:off_b + ncta + 1] if ncta else np.zeros(1, np.int32)
     if ncta:
@@ -78,10 +82,11 @@ def check_prefill_items(meta, pre, mer, s):
     1) naming exactly those slots; a unit in one item writes out directly."""
     g = meta.num_q_heads // meta.num_kv_heads
     qs, ctx = int(meta.q_lens[s]), int(meta.context_lens[s])
-    items = pre[pre[:, 0] == s]
+    items = pre[(pre[:, 0] == s) & (pre[:, 12] < 0)]     # contiguous sub-tiles only
     seen = {}    # (hq, q0) -> list of (kt0, kt1, part)
     for it in items:
-        _, h, hq0, hq1, qa, qb, na, nb, kt0, kt1, pa, pb = (int(v) for v in it)
+        _, h, hq0, hq1, qa, qb, na, nb, kt0, kt1, pa, pb = (int(v) for v in it[:12])
+        assert it[13] < 0
         assert 1 <= na <= 128 and 0 <= nb <= 128 and 0 <= kt0 < kt1
         for hq, q0, n, part in [(hq0, qa, na, pa)] + ([(hq1, qb, nb, pb)] if nb else []):
             assert hq // g == h and q0 % 128 == 0 and n == min(128, qs - q0)
@@ -105,6 +110,21 @@ def check_prefill_items(meta, pre, mer, s):
     return len(items)
 
 
+def sum_segment_blocks(meta):
+    """Blocks over all (row group, KV head) segments of the decode-class rows."""
+    g = meta.num_q_heads // meta.num_kv_heads
+    nq_tile = max(1, 16 // g)
+    tot = 0
+    for s in range(meta.num_seqs):
+        qs, ctx = int(meta.q_lens[s]), int(meta.context_lens[s])
+        if qs == 0 or qs >= 64:
+            continue
+        for qi0 in range(0, qs, nq_tile):
+            n_q = min(nq_tile, qs - qi0)
+            tot += ((ctx - qs + qi0 + n_q - 1) // 16 + 1) * meta.num_kv_heads
+    return tot
+
+
 def check_plan(meta, info, host, num_sms):
     hdr, wb, pieces, mer, pre = parse_plan(info, host)
     g = meta.num_q_heads // meta.num_kv_heads
@@ -120,7 +140,7 @@ def check_plan(meta, info, host, num_sms):
         assert wb[0] == 0 and wb[-1] == len(pieces) and np.all(np.diff(wb) >= 1)
         per_warp = [int((pieces[wb[w]:wb[w + 1], 5] - pieces[wb[w]:wb[w + 1], 4]).sum())
                     for w in range(nw)]
-        assert sum(per_warp) == info.decode_blocks
+        assert sum(per_warp) == sum_segment_blocks(meta)
         cost = [2 * per_warp[w] + 3 * int((pieces[wb[w]:wb[w + 1], 4] == 0).sum())
                 for w in range(nw)]
         assert max(cost) - min(cost) <= 2 * (2 + 3)
@@ -128,7 +148,7 @@ def check_plan(meta, info, host, num_sms):
             assert nw <= num_sms * 8
     assert np.all(pieces[:, 5] > pieces[:, 4])
     # every decode segment (row group x KV head) is covered exactly once, in order
-    prefill_seqs = set(int(x) for x in pre[:, 0]) if len(pre) else set()
+    prefill_seqs = set(int(x) for x in pre[pre[:, 12] < 0, 0]) if len(pre) else set()
     seen_parts = set()
     total_blocks = 0
     for s in range(meta.num_seqs):
@@ -160,7 +180,10 @@ def check_plan(meta, info, host, num_sms):
                     seen_parts |= set(parts)
                     m = mer[(mer[:, 0] == s) & (mer[:, 1] == qi0) & (mer[:, 3] == h) & (mer[:, 6] == 0)]
                     assert len(m) == 1 and m[0, 2] == n_q and m[0, 4] == parts[0] and m[0, 5] == len(parts)
-    assert total_blocks == info.decode_blocks
+    assert total_blocks == sum_segment_blocks(meta)
+    # the split-KV kernel's attended blocks, each (sequence, block, KV head) once
+    dec = [s for s in range(meta.num_seqs) if 0 < meta.q_lens[s] and s not in prefill_seqs]
+    assert info.decode_blocks == hkv * sum((int(meta.context_lens[s]) + 15) // 16 for s in dec)
     assert len(seen_parts) == info.num_partials
     d = meta.head_dim
     a = lambda x: (x + 255) // 256 * 256
@@ -355,11 +378,13 @@ def test_shared_prefix_items_cover_the_shared_blocks(pkv):
     shared-prefix CTAs over those blocks; every (row group, KV head) result is then
     its shared chunks over [0, L) plus its suffix pieces over [L, nb), with one
     merge group naming exactly those parts."""
-    meta = workloads.shared_prefix_verify()
+    # a small group (under 64 query rows per KV head) stays on the split-KV CTAs
+    meta = workloads.random_step(np.random.default_rng(11), num_seqs=6, group=2, max_q=2,
+                                 max_ctx=600, shared_prefix_blocks=16)
     desc = pkv.PoolDesc(meta.num_blocks, 16, meta.num_kv_heads, meta.head_dim)
     info, host = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, desc,
                                num_sms=152, upload=False, block_tables=meta.block_tables)
-    assert info.num_shared_ctas > 0
+    assert info.num_shared_ctas > 0 and info.num_gather_rows == 0
     hdr, wb, pieces, mer, pre = parse_plan(info, host)
     sh = parse_plan.shared
     g = meta.num_q_heads // meta.num_kv_heads
@@ -396,3 +421,93 @@ def test_shared_prefix_items_cover_the_shared_blocks(pkv):
             assert parts == list(range(m[0, 4], m[0, 4] + len(parts)))
         else:
             assert parts == [-1] and len(m) == 0
+
+
+def check_gathered_prefix(meta, info, host):
+    """Gathered sub-tiles (a prefix many query rows share, on the tensor cores):
+    every token of every sharing sequence appears once per KV head and key chunk,
+    at the right row of its row group's partial slot; each (row group, KV head)
+    has its prefix key tiles [0, KT) covered once, by chunks whose slots are
+    consecutive from its merge group's first slot, and its suffix pieces cover
+    blocks [8 KT, nb); the gathered keys are the same physical blocks in every
+    member's table.  Returns the number of (row group, KV head) pairs covered."""
+    hdr, wb, pieces, mer, pre = parse_plan(info, host)
+    gat = parse_plan.gather
+    g = meta.num_q_heads // meta.num_kv_heads
+    nq_tile = max(1, 16 // g)
+    cu = meta.cu_q_lens
+    items = pre[pre[:, 12] >= 0]
+    assert len(items) and info.num_gather_rows == len(gat)
+    cover = {}   # (seq, qi0, h) -> list of (kt0, kt1, slot)
+    for it in items:
+        seq0, h, kt0, kt1 = int(it[0]), int(it[1]), int(it[8]), int(it[9])
+        assert 0 <= kt0 < kt1
+        for x in range(2):
+            n, c, g0 = int(it[6 + x]), int(it[10 + x]), int(it[12 + x])
+            if n == 0:
+                assert x == 1 and g0 < 0
+                continue
+            assert 1 <= n * g <= 128 and c >= 0 and g0 >= 0
+            toks = gat[g0:g0 + n, 0]
+            run = bool(np.all(np.diff(toks) == 1))
+            assert bool(it[14] >> x & 1) == run          # consecutive tokens: one q box
+            if run:
+                assert it[4 + x] == toks[0]
+            for q_tok, part0, row0, _ in gat[g0:g0 + n]:
+                s = int(np.searchsorted(cu, q_tok, side="right")) - 1
+                i = int(q_tok - cu[s])
+                qi0 = i // nq_tile * nq_tile
+                assert row0 == (i - qi0) * g
+                assert np.array_equal(meta.block_tables[s, 8 * kt0:8 * kt1],
+                                      meta.block_tables[seq0, 8 * kt0:8 * kt1])
+                qs, ctx = int(meta.q_lens[s]), int(meta.context_lens[s])
+                assert 128 * kt1 <= ctx - qs + 1          # every row sees these keys
+                cover.setdefault((s, qi0, h), {}).setdefault(i, []).append((kt0, kt1, part0 + c))
+    for (s, qi0, h), per_tok in cover.items():
+        qs, ctx = int(meta.q_lens[s]), int(meta.context_lens[s])
+        n_q = min(nq_tile, qs - qi0)
+        assert sorted(per_tok) == list(range(qi0, qi0 + n_q))   # every token of the row group
+        chunks = sorted(set(per_tok[qi0]))
+        assert all(sorted(set(v)) == chunks for v in per_tok.values())
+        assert chunks[0][0] == 0 and all(chunks[k][1] == chunks[k + 1][0] for k in range(len(chunks) - 1))
+        kt = chunks[-1][1]
+        slots = [c[2] for c in chunks]
+        m = mer[(mer[:, 0] == s) & (mer[:, 1] == qi0) & (mer[:, 3] == h) & (mer[:, 6] == 0)]
+        assert len(m) == 1 and slots == list(range(m[0, 4], m[0, 4] + len(slots)))
+        nb = (ctx - qs + qi0 + n_q - 1) // 16 + 1
+        mine = pieces[(pieces[:, 0] == s) & (pieces[:, 1] == qi0) & (pieces[:, 3] == h)]
+        mine = mine[np.argsort(mine[:, 4])]
+        if 8 * kt < nb:
+            assert mine[0, 4] == 8 * kt and mine[-1, 5] == nb and np.all(mine[1:, 4] == mine[:-1, 5])
+        assert m[0, 5] == len(slots) + len(mine)
+        if len(mine):
+            assert sorted(mine[:, 6]) == list(range(m[0, 4] + len(slots), m[0, 4] + m[0, 5]))
+    return len(cover)
+
+
+@pytest.mark.parametrize("name", ["shared_prefix_verify", "mtp_draft"])
+def test_gathered_prefix_items_cover_every_row_group(pkv, name):
+    meta = workloads.make_config(name)
+    desc = pkv.PoolDesc(meta.num_blocks, 16, meta.num_kv_heads, meta.head_dim)
+    for sms in (152, 13):
+        info, host = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, desc,
+                                   num_sms=sms, upload=False, block_tables=meta.block_tables)
+        assert info.num_shared_ctas == 0 and info.num_gather_rows > 0
+        g = meta.num_q_heads // meta.num_kv_heads
+        units = sum((int(q) + max(1, 16 // g) - 1) // max(1, 16 // g) for q in meta.q_lens)
+        assert check_gathered_prefix(meta, info, host) == units * meta.num_kv_heads
+
+
+def test_step_generator_slots_are_distinct():
+    """Every generated step appends each new token to its own slot (a slot written
+    twice would make the pool depend on write order), also when sequences share
+    prefix blocks."""
+    metas = [workloads.make_config(n) for n in workloads.CONFIGS]
+    for seed in range(30):
+        rng = np.random.default_rng(900 + seed)
+        metas.append(workloads.random_step(rng, num_seqs=int(rng.integers(2, 40)), max_q=3,
+                                           shared_prefix_blocks=int(rng.choice([0, 3, 8, 20])),
+                                           max_ctx=500))
+    for meta in metas:
+        sl = meta.slot_mapping[meta.slot_mapping >= 0]
+        assert len(np.unique(sl)) == len(sl), meta.name

@@ -487,17 +487,38 @@ def test_plan_with_block_tables_same_result_and_mismatch_reported(pkv, cuda_devi
 @pytest.mark.parametrize("name,num_sms", [("shared_prefix_verify", 152), ("mtp_draft", 152),
                                           ("shared_prefix_verify", 7)])
 def test_shared_prefix_ctas_match_oracle_and_per_warp_path(pkv, cuda_device, name, num_sms):
-    """Sequences sharing leading blocks read them once per shared-prefix CTA; the
-    result matches the oracle on every row and the per-warp plan (no tables)."""
+    """Sequences sharing leading blocks read them once per work unit (here the
+    tensor-core gathered sub-tiles); the result matches the oracle on every row and
+    the per-warp plan (no tables)."""
     meta = workloads.make_config(name)
     q, k, v, pool = workloads.make_values(meta)
     info, _ = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads,
                             pkv.pool_desc(pool), num_sms=num_sms, upload=False,
                             block_tables=meta.block_tables)
-    assert info.num_shared_ctas > 0
+    assert info.num_gather_rows > 0
     want, _ = oracle.run_step(meta, q, k, v, pool)
     shared, _, _ = gpu_step(pkv, meta, q, k, v, pool, cuda_device, num_sms=num_sms)
     per_warp, _, _ = gpu_step(pkv, meta, q, k, v, pool, cuda_device, num_sms=num_sms, tables=False)
     assert_close(shared, want, f"{name} shared-prefix CTAs")
     diff = (shared.double() - per_warp.double()).abs()
     assert float(diff.max()) <= MAX_ABS and float(diff.mean()) <= MEAN_ABS
+
+
+@pytest.mark.parametrize("seed,num_seqs,group,hkv,d,pre", [
+    (0, 40, 1, 2, 128, 8), (1, 40, 2, 1, 64, 20), (2, 24, 4, 2, 128, 33), (3, 12, 8, 1, 64, 20),
+    (4, 70, 1, 1, 128, 17), (5, 6, 2, 2, 128, 16)])
+def test_shared_prefix_random_steps_match_oracle(pkv, cuda_device, seed, num_seqs, group, hkv, d, pre):
+    """Random steps whose sequences share a prefix: gathered tensor-core sub-tiles
+    (G = 1 .. 8, so 128 .. 16 tokens per sub-tile, one or two per item) or, for a
+    small group, the split-KV shared-prefix CTAs; against the oracle on every row."""
+    rng = np.random.default_rng(500 + seed)
+    meta = workloads.random_step(rng, num_seqs=num_seqs, group=group, hkv=hkv, d=d, max_q=3,
+                                 max_ctx=pre * 16 + 700, shared_prefix_blocks=pre)
+    q, k, v, pool = workloads.make_values(meta)
+    info, _ = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads,
+                            pkv.pool_desc(pool), upload=False, block_tables=meta.block_tables)
+    assert info.num_gather_rows > 0 or info.num_shared_ctas > 0
+    want, _ = oracle.run_step(meta, q, k, v, pool)
+    for sms in (152, 9):
+        out, _, _ = gpu_step(pkv, meta, q, k, v, pool, cuda_device, num_sms=sms)
+        assert_close(out, want, f"seed {seed} sms {sms}")

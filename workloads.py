@@ -296,6 +296,10 @@ def random_step(rng: np.random.Generator, *, num_seqs=None, hkv=None, group=None
         kind = rng.integers(0, 3)
         mq = int(c) if max_q is None else min(int(c), max_q)
         q.append(1 if kind == 0 else min(int(c), 2) if kind == 1 else int(rng.integers(1, mq + 1)))
+    if shared_prefix_blocks:
+        # the step's new tokens land past the shared blocks: two sequences never
+        # write the same slot of a block they share
+        ctx = np.maximum(ctx, shared_prefix_blocks * BLOCK_SIZE + np.array(q))
     nb = sum(-(-int(c) // BLOCK_SIZE) for c in ctx)
     return build_step("random", int(rng.integers(1 << 30)), q, ctx, hkv * group, hkv, d,
                       pool_blocks=int(nb * pool_extra) + 2,
