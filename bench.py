@@ -64,16 +64,25 @@ def peaks():
 PREFILL_MIN_Q = 64   # sequences with at least this many query tokens run on the tensor-core kernel
 
 
-def source_sha256() -> str:
-    """Hash of the kernel sources, as recorded next to the ncu traffic figures."""
+# Sources that decide what a kernel does for a given workload: its own file,
+# the planner (its work lists), the entry points and the shared headers.
+KERNEL_SOURCES = {
+    "decode_kernel": ["pkv_decode.cu", "pkv_plan.cpp"],
+    "prefill_kernel": ["pkv_prefill.cu", "pkv_plan.cpp"],
+    "state_checkpoint_kernel": ["pkv_state.cu"],
+}
+COMMON_SOURCES = ["pkv_api.cu", "pkv_device.cuh", "pkv_tc.cuh", "pkv_internal.h"]
+
+
+def source_sha256(kernel: str) -> str:
+    """Hash of the sources behind one kernel, as recorded next to its ncu traffic."""
     import hashlib
     d = os.path.join(ROOT, "paged_kv_attention_append_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(d)):
-        if f.endswith((".cu", ".cuh", ".h", ".cpp")):
-            h.update(f.encode())
-            with open(os.path.join(d, f), "rb") as fh:
-                h.update(fh.read())
+    for f in sorted(KERNEL_SOURCES[kernel] + COMMON_SOURCES):
+        h.update(f.encode())
+        with open(os.path.join(d, f), "rb") as fh:
+            h.update(fh.read())
     with open(os.path.join(ROOT, "include", "pkv.h"), "rb") as fh:
         h.update(fh.read())
     return h.hexdigest()
@@ -85,7 +94,7 @@ def recorded_traffic(kernel: str, workload: str):
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f).get(f"{kernel}/{workload}")
-        if rec and rec.get("source_sha256") == source_sha256():
+        if rec and rec.get("source_sha256") == source_sha256(kernel):
             return int(rec["dram_bytes"])
     except Exception:
         pass
