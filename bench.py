@@ -22,8 +22,10 @@ uploaded per step inside `e2e`.
   4 * D * (query row, key) pairs: the causal pairs of prefill-class sequences
   plus the gathered shared-prefix pairs.
 * e2e: the same metric through the public API from pinned HOST buffers: every
-  step copies q, the new K/V, slot mapping and metadata host->device, plans on
-  the host, runs append + attention and copies out back (wall time per step).
+  step copies q, the new K/V, slot mapping and metadata host->device (two pinned
+  buffers, one transfer each), plans on the host into pinned memory and uploads
+  the plan asynchronously, runs append + attention and copies out back (wall
+  time per step).
 * cpu_baseline / --impl reference: the fp64 CPU oracle as it stands, on the
   host cores, on a bounded sample of the same workload.
 """
@@ -356,7 +358,6 @@ def bench_pkv(args):
         pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, pool, upload=False,
                       chain_steps=chain_arg, block_tables=meta.block_tables)
     host_plan_us = (time.perf_counter() - t0) / 50 * 1e6
-    plan_pinned = torch.from_numpy(host_plan.view(np.uint8)).pin_memory()
     plan = pkv.StepPlan(info, host_plan, dev)
 
     def step():
@@ -442,34 +443,51 @@ def bench_pkv(args):
     assert int(status.item()) == 0, f"device status {int(status.item())}"
 
     # ---- end to end from pinned host buffers through the public API (a chained
-    # workload: all its steps' inputs in, one plan, every step's output back)
-    host = {
-        "slots": slots0.cpu().pin_memory(), "cu": cu_d.cpu().pin_memory(),
-        "ctx": ctx0_d.cpu().pin_memory(), "bt": bt_d.cpu().pin_memory(),
-    }
-    host_vals = [tuple(x.cpu().pin_memory() for x in qkv) for qkv in vals]
+    # workload: all its steps' inputs in, one plan, every step's output back).  The
+    # step's host inputs sit in two pinned buffers -- the int32 metadata (slots,
+    # cu_q_lens, context_lens, block tables) and every step's bf16 q/k/v -- each
+    # copied in one transfer; the plan is written straight into pinned memory and
+    # uploaded asynchronously.
+    def packed(parts, dtype):
+        """One pinned host buffer holding `parts` (each start 16-byte aligned), the
+        matching device buffer, and the device and host views of each part."""
+        per = 16 // torch.tensor([], dtype=dtype).element_size()
+        offs, n = [], 0
+        for t in parts:
+            offs.append(n)
+            n += (t.numel() + per - 1) // per * per
+        hbuf = torch.zeros(max(n, per), dtype=dtype).pin_memory()
+        dbuf = torch.empty(max(n, per), dtype=dtype, device=dev)
+        dviews, hviews = [], []
+        for t, o in zip(parts, offs):
+            hbuf[o:o + t.numel()].copy_(t.reshape(-1).cpu())
+            dviews.append(dbuf[o:o + t.numel()].view(t.shape))
+            hviews.append(hbuf[o:o + t.numel()].view(t.shape))
+        return hbuf, dbuf, dviews, hviews
+
+    meta_h, meta_d, (ds, dcu, dctx, dbt), (_, cu_h, ctx_h, bt_h) = packed(
+        [slots0, cu_d, ctx0_d, bt_d], torch.int32)
+    qkv_h, qkv_d, qkv_dv, _ = packed([x for qkv in vals for x in qkv], torch.bfloat16)
+    dvals = [tuple(qkv_dv[3 * t:3 * t + 3]) for t in range(len(vals))]
+    cu_np, ctx_np, bt_np = cu_h.numpy(), ctx_h.numpy(), bt_h.numpy()
+    plan_h = torch.empty((int(info.plan_bytes) + 4095) // 4096 * 4096 + 4096,
+                         dtype=torch.uint8).pin_memory()
+    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     outs_h = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
-    dvals = [tuple(torch.empty_like(x) for x in qkv) for qkv in vals]
-    ds, dcu, dctx, dbt = (torch.empty_like(t) for t in (slots0, cu_d, ctx0_d, bt_d))
-    h2d = (sum(t.numel() * t.element_size() for t in host.values()) + plan_pinned.numel() +
-           sum(x.numel() * x.element_size() for qkv in host_vals for x in qkv))
+    h2d = (meta_h.numel() * meta_h.element_size() + qkv_h.numel() * qkv_h.element_size() +
+           int(info.plan_bytes))
     d2h = sum(o.numel() * o.element_size() for o in outs_h)
     e2e_times = []
     with torch.cuda.stream(stream):
         for i in range(args.warmup + args.steps):
             torch.cuda.synchronize(dev)
             t0 = time.perf_counter()
-            for dst, src in ((ds, host["slots"]), (dcu, host["cu"]), (dctx, host["ctx"]),
-                             (dbt, host["bt"])):
-                dst.copy_(src, non_blocking=True)
-            for dqkv, hqkv in zip(dvals, host_vals):
-                for dst, src in zip(dqkv, hqkv):
-                    dst.copy_(src, non_blocking=True)
-            inf2, hp2 = pkv.plan_step(host["cu"].numpy(), host["ctx"].numpy(), meta.num_q_heads, pool,
-                                      upload=False, chain_steps=chain_arg,
-                                      block_tables=host["bt"].numpy())
-            pp = torch.from_numpy(hp2.view(np.uint8))
-            plan.dev[:pp.numel()].copy_(pp, non_blocking=False)
+            meta_d.copy_(meta_h, non_blocking=True)
+            qkv_d.copy_(qkv_h, non_blocking=True)
+            inf2, hp2 = pkv.plan_step(cu_np, ctx_np, meta.num_q_heads, pool, upload=False,
+                                      chain_steps=chain_arg, block_tables=bt_np,
+                                      num_sms=num_sms, out=plan_h)
+            plan.dev[:hp2.nbytes].copy_(plan_h[:hp2.nbytes], non_blocking=True)
             plan.info = inf2
             for t, (dq, dk, dv) in enumerate(dvals):
                 pkv.paged_kv_append(dk, dv, ds, pool, dev_status=status)

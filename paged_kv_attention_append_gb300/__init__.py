@@ -255,13 +255,16 @@ _plan_scratch = np.zeros(1 << 18, dtype=np.int32)   # 1 MiB, grown on demand
 
 def plan_step(cu_q_lens, context_lens, num_q_heads: int, kv_pool_or_desc, *, num_sms=None,
               device=None, upload=True, stream=None, chain_steps=None,
-              block_tables=None) -> StepPlan | tuple:
+              block_tables=None, out=None) -> StepPlan | tuple:
     """Build the host plan for one step (pkv_plan_step_ex) and upload it.
 
     cu_q_lens / context_lens: host arrays or tensors (copied to the host if on a GPU).
     chain_steps: plan a chain of that many decode steps instead.
     block_tables: the step's block tables (host copy) -- lets the plan carry each
     split-KV warp's first block ids (checked on the device against the tables).
+    out (with upload=False): a writable host buffer (numpy array or CPU tensor,
+    e.g. pinned memory for an asynchronous upload) the plan is written into; the
+    returned host bytes are then a view of it.
     Returns a StepPlan (or (info, host_bytes) when upload=False).
     """
     desc = kv_pool_or_desc if isinstance(kv_pool_or_desc, PoolDesc) else pool_desc(kv_pool_or_desc)
@@ -290,6 +293,15 @@ def plan_step(cu_q_lens, context_lens, num_q_heads: int, kv_pool_or_desc, *, num
             1 if chain_steps is None else int(chain_steps),
             None if bt is None else bt.ctypes.data_as(ctypes.c_void_p),
             0 if bt is None else bt.shape[1], buf, cap, ctypes.byref(info))
+    if out is not None and not upload:
+        buf = out.numpy() if isinstance(out, torch.Tensor) else out
+        if not buf.flags.c_contiguous or not buf.flags.writeable:
+            raise ValueError("out must be a contiguous writable host buffer")
+        st = call(buf.ctypes.data_as(ctypes.c_void_p), buf.nbytes)
+        if st:
+            raise PkvError(st, name)
+        n = (max(int(info.plan_bytes), 16) + 15) // 16 * 16
+        return info, buf.reshape(-1).view(np.uint8)[:n].view(np.int32)
     # one planning pass into a reused buffer (grown and redone only when a plan
     # outgrows it), then a copy of the plan's bytes
     global _plan_scratch

@@ -585,7 +585,6 @@ __global__ void __launch_bounds__(kThreads, 2)
         const int row_k = ((phys * 2 + 0) * hkv + pp.h) * kBlockSize;
         const int row_v = row_k + hkv * kBlockSize;
         const uint32_t dst = smem_u32(ring + stage * C::kStageBytes);
-#pragma unroll
         // one 4-D box per slab: the whole block of one head (rows / 8 = group coordinate)
         tma_load_4d(dst, &pool_map, 0, 0, 0, row_k >> 3, bar);
         tma_load_4d(dst + C::kSlabBytes, &pool_map, 0, 0, 0, row_v >> 3, bar);
