@@ -394,8 +394,19 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   }
 
   // ---- cut the concatenated suffix blocks into equal-cost warp ranges
+  const int64_t avail = std::max<int64_t>(slots - shared_slots, 1);
   int64_t nw64 = (total_blocks + kMinBlocksPerWarp - 1) / kMinBlocksPerWarp;
-  nw64 = std::min<int64_t>(nw64, std::max<int64_t>(slots - shared_slots, 1));
+  nw64 = std::min<int64_t>(nw64, avail);
+  // Small steps: when every segment fits a warp slot and the longest is within a
+  // few blocks of the equal share, one warp per whole segment runs about as long
+  // as the equal-cost cut and needs no partials or merge launch.
+  int32_t max_seg = 0;
+  for (const Segment &g : segs) max_seg = std::max(max_seg, g.nb);
+  const bool whole_segments =
+      !segs.empty() && (int64_t)segs.size() <= avail &&
+      max_seg <= std::max<int64_t>(2 * kMinBlocksPerWarp,
+                                   (total_blocks + avail - 1) / avail + kMinBlocksPerWarp);
+  if (whole_segments) nw64 = (int64_t)segs.size();
   const int32_t num_warps = total_blocks > 0 ? (int32_t)std::max<int64_t>(nw64, 1) : 0;
   std::vector<int32_t> warp_begin(num_warps + 1, 0);
   std::vector<Piece> pieces;
@@ -414,7 +425,13 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
     const int64_t total_cost = kBlockCost * total_blocks + kPieceCost * (int64_t)segs.size();
     std::vector<int64_t> cut(num_warps + 1, total_blocks);  // first block of each warp
     cut[0] = 0;
-    {
+    if (whole_segments) {
+      int64_t blk = 0;
+      for (int32_t w = 0; w < num_warps; ++w) {
+        cut[w] = blk;
+        blk += segs[w].nb;
+      }
+    } else {
       // warp w >= 1 starts at the first block whose midpoint m satisfies
       // m * num_warps >= w * total_cost; the midpoints of a segment starting at
       // cost c are c + kPieceCost + kBlockCost * i + kBlockCost / 2, so each
