@@ -312,42 +312,49 @@ __device__ __forceinline__ void block_update(uint32_t sK, uint32_t sV, const uin
   }
 }
 
-// Shared-prefix CTA: the kWarps warps attend their row groups (usually of
-// different sequences that share the prefix blocks) to the same blocks, loaded
-// once into one ring pooled from the warps' rings.  Warp 0 resolves the block
-// table and issues the copies; a stage is refilled once every warp has released
-// it (an empty mbarrier with kWarps arrivals).  Every wait is bounded.
+// Shared-block CTA: two independent pairs of warps.  Each pair takes one item --
+// up to two row groups that read the same blocks: the row groups of one verify
+// window wider than 16 rows, or row groups of sequences whose tables hold the same
+// prefix blocks -- and streams those blocks once through a ring pooled from its
+// two warps' rings.  The pair's first warp resolves the block table and issues
+// the copies; a stage is refilled once both warps have released it (an empty
+// mbarrier with two arrivals).  An item with no row group leaves its pair idle.
+// Every wait is bounded.
 template <int D, int NSTAGE>
 __device__ __forceinline__ void shared_cta(const CUtensorMap &pool_map, const DecodeParams &p,
                                            uint8_t *smem, int warp, int lane) {
   using C = DecodeCfg<D, NSTAGE>;
-  constexpr int kS = kWarps * NSTAGE;  // stages of the pooled ring
+  constexpr int kS = kSharedRowGroups * NSTAGE;  // stages of a pair's pooled ring
   constexpr int kL = D / 32, kNt = D / 8;
   const int r = lane >> 2, c = lane & 3;
   const int G = p.group, hkv = p.num_kv_heads;
-  const SharedItem &item = p.shared[blockIdx.x - p.num_indep_ctas];
+  const int pair = warp / kSharedRowGroups, lw = warp % kSharedRowGroups;
+  const SharedItem &item =
+      p.shared[(blockIdx.x - p.num_indep_ctas) * kSharedItemsPerCta + pair];
   const int seq0 = item.seq0, h = item.h, kb0 = item.kb_begin, kb1 = item.kb_end;
   const int n_rg = item.n_rg;
   const bool item_ok = seq0 >= 0 && seq0 < p.num_seqs && h >= 0 && h < hkv && kb0 >= 0 &&
-                       kb0 <= kb1 && kb1 <= p.max_blocks_per_seq && n_rg >= 1 && n_rg <= kWarps;
+                       kb0 <= kb1 && kb1 <= p.max_blocks_per_seq && n_rg >= 1 &&
+                       n_rg <= kSharedRowGroups;
   SharedRowGroup rg;
   rg.seq = -1;
   rg.qi0 = rg.n_q = rg.q_row0 = 0;
   rg.part = -1;
-  if (item_ok && warp < n_rg) rg = item.rg[warp];
-  bool mine = item_ok && warp < n_rg && rg.seq >= 0 && rg.seq < p.num_seqs && rg.qi0 >= 0 &&
+  if (item_ok && lw < n_rg) rg = item.rg[lw];
+  bool mine = item_ok && lw < n_rg && rg.seq >= 0 && rg.seq < p.num_seqs && rg.qi0 >= 0 &&
               rg.n_q >= 1 && rg.n_q * G <= kRowsPerTile && rg.q_row0 >= 0 &&
               rg.q_row0 + rg.n_q <= p.total_q;
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOffset);
+  uint8_t *ring = smem + pair * kSharedRowGroups * C::kRingBytes;  // the pair's warps' rings
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOffset) + pair * 2 * kS;
   uint64_t *empty = full + kS;
-  int *stage_ok = reinterpret_cast<int *>(smem + C::kFlagOffset);
-  if (threadIdx.x == 0) {
+  int *stage_ok = reinterpret_cast<int *>(smem + C::kFlagOffset) + pair * kS;
+  if (lw == 0 && lane == 0) {
     for (int s = 0; s < kS; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), kWarps);
+      mbar_init(smem_u32(&empty[s]), kSharedRowGroups);
     }
     fence_mbar_init();
-    if (!item_ok) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
+    if (!item_ok && n_rg != 0) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
   }
   // q rows, lengths and the first table window are not written by the kernels
   // this one follows: read before the programmatic-launch wait
@@ -364,12 +371,12 @@ __device__ __forceinline__ void shared_cta(const CUtensorMap &pool_map, const De
   }
   const int32_t *table = p.block_tables + (int64_t)(item_ok ? seq0 : 0) * p.max_blocks_per_seq;
   int win_base = kb0, win_val = -1;
-  if (warp == 0 && item_ok && kb0 + lane < kb1) win_val = __ldg(table + kb0 + lane);
+  if (lw == 0 && item_ok && kb0 + lane < kb1) win_val = __ldg(table + kb0 + lane);
   __syncthreads();  // barrier initialisation visible to every warp
   pdl_wait();
   const int nblk = item_ok ? kb1 - kb0 : 0;
   int issued = 0;
-  auto issue = [&](int j) {  // warp 0, whole warp
+  auto issue = [&](int j) {  // the pair's first warp, whole warp
     const int kb = kb0 + j;
     if (kb >= win_base + 32) {
       win_base = kb;
@@ -384,7 +391,7 @@ __device__ __forceinline__ void shared_cta(const CUtensorMap &pool_map, const De
       if (ok) {
         mbar_arrive_expect_tx(bar, C::kStageBytes);
         const int row_k = ((phys * 2 + 0) * hkv + h) * kBlockSize;
-        const uint32_t dst = smem_u32(smem + s * C::kStageBytes);
+        const uint32_t dst = smem_u32(ring + s * C::kStageBytes);
         tma_load_4d(dst, &pool_map, 0, 0, 0, row_k >> 3, bar);
         tma_load_4d(dst + C::kSlabBytes, &pool_map, 0, 0, 0, (row_k + hkv * kBlockSize) >> 3, bar);
       } else {
@@ -394,7 +401,7 @@ __device__ __forceinline__ void shared_cta(const CUtensorMap &pool_map, const De
     }
     ++issued;
   };
-  if (warp == 0)
+  if (lw == 0)
     for (int j = 0; j < min(nblk, kS); ++j) issue(j);
 
   const float sl2 = p.scale_log2;
@@ -418,13 +425,13 @@ __device__ __forceinline__ void shared_cta(const CUtensorMap &pool_map, const De
     }
     ++done;
     if (mine && stage_ok[s]) {
-      const uint32_t sK = smem_u32(smem + s * C::kStageBytes);
+      const uint32_t sK = smem_u32(ring + s * C::kStageBytes);
       block_update<D>(sK, sK + C::kSlabBytes, qa, (kb0 + j) * kBlockSize, q_pos0, lim_lo, lim_hi,
                       sl2, r, c, m_lo, m_hi, l_lo, l_hi, o);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
-    if (warp == 0 && j + kS < nblk) {  // refill once every warp released the stage
+    if (lw == 0 && j + kS < nblk) {  // refill once both warps released the stage
       if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[s]), par))) {
         if (lane == 0) report(p.dev_status, PKV_DEV_TIMEOUT);
         good = false;
@@ -433,8 +440,8 @@ __device__ __forceinline__ void shared_cta(const CUtensorMap &pool_map, const De
       issue(j + kS);
     }
   }
-  // warp 0's copies still in flight land before the CTA exits
-  if (warp == 0 && lane == 0)
+  // the issuing warp's copies still in flight land before the CTA exits
+  if (lw == 0 && lane == 0)
     for (int j = done; j < issued; ++j)
       mbar_wait(smem_u32(&full[j % kS]), (uint32_t)((j / kS) & 1));
   if (good && mine) {

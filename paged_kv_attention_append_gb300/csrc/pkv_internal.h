@@ -22,7 +22,7 @@ constexpr int kDecodeWarpsPerCta = 4;
 //    ids: a warp reads its range and head with two independent loads and can
 //    start its first copies without waiting for a block-table read)
 //   [Piece x num_decode_pieces][MergeGroup x num_merge_groups]
-//   [SharedItem x num_shared_ctas]
+//   [SharedItem x num_shared_ctas * kSharedItemsPerCta]
 //   [prefill_begin: int32 x (num_prefill_ctas + 1), padded to 32 B; absent when 0 CTAs]
 //   [PrefillTile x num_prefill_tiles, grouped by CTA]
 //   [GatherRow x num_gather_rows] (the query tokens of gathered sub-tiles)
@@ -68,12 +68,14 @@ struct WarpHead {
 };
 static_assert(sizeof(WarpHead) == 48, "warp head is 48 bytes");
 
-// Shared-prefix work for one split-KV CTA: sequences whose block tables start
-// with the same physical blocks read those blocks once per CTA, each of the CTA's
-// warps attending one row group of one of them to every loaded block.  Blocks
-// kb_begin .. kb_end-1 of sequence seq0's table, KV head h; warp w < n_rg takes
-// row group rg[w] and writes its partial to rg[w].part (or its result directly
-// when part < 0).
+// Shared-block work for one pair of split-KV warps (a CTA runs
+// kSharedItemsPerCta of them): row groups that read the same blocks -- of one
+// verify window wider than 16 rows, or of sequences whose block tables start
+// with the same physical blocks -- read them once, each of the pair's warps
+// attending one row group to every loaded block.  Blocks kb_begin .. kb_end-1 of
+// sequence seq0's table, KV head h; warp w < n_rg of the pair takes row group
+// rg[w] and writes its partial to rg[w].part (or its result directly when part
+// < 0).  n_rg == 0: an empty item (its pair idles).
 struct SharedRowGroup {
   int32_t seq;
   int32_t qi0;
@@ -82,6 +84,8 @@ struct SharedRowGroup {
   int32_t q_row0;  // packed query index of token qi0
   int32_t pad[3];
 };
+constexpr int kSharedRowGroups = 2;   // row groups (warps) per shared item
+constexpr int kSharedItemsPerCta = kDecodeWarpsPerCta / kSharedRowGroups;
 struct SharedItem {
   int32_t seq0;
   int32_t h;
@@ -89,9 +93,9 @@ struct SharedItem {
   int32_t kb_end;
   int32_t n_rg;
   int32_t pad[3];
-  SharedRowGroup rg[kDecodeWarpsPerCta];
+  SharedRowGroup rg[kSharedRowGroups];
 };
-static_assert(sizeof(SharedItem) == 32 + 32 * kDecodeWarpsPerCta, "shared item layout");
+static_assert(sizeof(SharedItem) == 32 + 32 * kSharedRowGroups, "shared item layout");
 
 // A set of nsplit partial results (slots part0 .. part0+nsplit-1) to combine.
 // kind 0: a decode segment -- rows are n_q tokens x the group's heads of KV

@@ -238,11 +238,56 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
       for (int32_t m : mem) shared_len[m] = len;
     }
   }
-  // suffix segments: (row group, KV head) keys past the shared prefix
+  // ---- shared streams for the split-KV shared-block items: each CTA-path
+  // group's prefix (all its members' row groups), and each verify window wider
+  // than one row group (its row groups in pairs, over the blocks the pair's first
+  // row group sees; the second row group keeps its few later blocks as a
+  // suffix).  unit_kb0: where each row group's own (suffix) segment starts.
+  struct Stream {
+    int32_t seq0, len;
+    std::vector<int32_t> units;
+  };
+  std::vector<Stream> streams;
+  std::vector<int32_t> unit_kb0(dunits.size(), 0);
+  {
+    std::vector<int32_t> unit_first(num_seqs, -1);  // decode units are in sequence order
+    for (size_t u = dunits.size(); u-- > 0;) unit_first[dunits[u].seq] = (int32_t)u;
+    for (size_t u = 0; u < dunits.size(); ++u) unit_kb0[u] = shared_len[dunits[u].seq];
+    for (const Group &g : groups) {
+      if (g.tc) continue;
+      Stream st{g.members[0], g.len, {}};
+      for (int32_t m : g.members)
+        for (size_t u = unit_first[m]; u < dunits.size() && dunits[u].seq == m; ++u)
+          st.units.push_back((int32_t)u);
+      streams.push_back(st);
+    }
+    const size_t n_group_streams = streams.size();
+    int64_t window_items = 0;
+    for (int32_t sq = 0; sq < num_seqs; ++sq) {
+      if (shared_len[sq] > 0 || unit_first[sq] < 0) continue;
+      const size_t u0 = unit_first[sq];
+      size_t u1 = u0;
+      while (u1 < dunits.size() && dunits[u1].seq == sq) ++u1;
+      for (size_t u = u0; u + 1 < u1; u += 2) {
+        const int32_t len = std::min(dunits[u].nb, dunits[u + 1].nb);
+        if (len < kMinSharedBlocks) continue;
+        streams.push_back({sq, len, {(int32_t)u, (int32_t)u + 1}});
+        window_items += hkv;
+      }
+    }
+    // windows only while one chunk each leaves half the warp slots to the rest
+    // (else the shared items alone would take more than a wave)
+    if (kSharedRowGroups * window_items * 2 > (int64_t)num_sms * kDecodeWarpsPerSm)
+      streams.resize(n_group_streams);
+    for (size_t i = n_group_streams; i < streams.size(); ++i)
+      for (int32_t u : streams[i].units) unit_kb0[u] = streams[i].len;
+  }
+
+  // suffix segments: (row group, KV head) keys past the shared blocks
   std::vector<int32_t> seg_of(dunits.size() * hkv, -1);
   for (size_t u = 0; u < dunits.size(); ++u) {
     const DUnit &du = dunits[u];
-    const int32_t kb0 = std::min(shared_len[du.seq], du.nb);
+    const int32_t kb0 = std::min(unit_kb0[u], du.nb);
     if (du.nb <= kb0) continue;
     for (int32_t h = 0; h < hkv; ++h) {
       seg_of[u * hkv + h] = (int32_t)segs.size();
@@ -251,61 +296,72 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
     }
   }
 
-  // ---- shared items: per group and KV head, the members' row groups in sets of
-  // one per warp of a CTA, the prefix cut into chunks so a chunk costs what a
-  // warp range costs (a CTA-chunk of B blocks holds kDecodeWarpsPerCta warp
-  // slots for B block steps)
+  // ---- shared-block items: per stream and KV head, its row groups in pairs (one
+  // item per pair of warps), the stream cut into equal chunks.  A chunk of B
+  // blocks holds two warp slots for about B block steps, as long as a warp range
+  // of B blocks; the chunk length is the smallest (from half a slot's cost) at
+  // which the warps left over for the independent segments carry no more
+  // than one chunk each.
   const int64_t slots = (int64_t)num_sms * kDecodeWarpsPerSm;
   std::vector<SharedItem> sitems;
   // shared parts of each (decode unit, KV head): (item, warp slot)
   std::vector<std::vector<std::array<int32_t, 2>>> unit_shared(dunits.size() * hkv);
-  if (!groups.empty()) {
-    std::vector<int32_t> unit_of_seq_first(num_seqs, -1);  // decode units are in seq order
-    for (size_t u = dunits.size(); u-- > 0;) unit_of_seq_first[dunits[u].seq] = (int32_t)u;
-    int64_t sh_blocks = 0;
-    for (const Group &g : groups) {
-      if (g.tc) continue;
-      int64_t nrg = 0;
-      for (int32_t m : g.members)
-        for (size_t u = unit_of_seq_first[m]; u < dunits.size() && dunits[u].seq == m; ++u) ++nrg;
-      sh_blocks += (int64_t)hkv * ((nrg + kDecodeWarpsPerCta - 1) / kDecodeWarpsPerCta) * g.len;
+  if (!streams.empty()) {
+    int64_t sh_blocks = 0, max_len = 0;
+    for (const Stream &st : streams) {
+      const int64_t pairs = (int64_t)(st.units.size() + kSharedRowGroups - 1) / kSharedRowGroups;
+      sh_blocks += (int64_t)hkv * pairs * st.len;
+      max_len = std::max<int64_t>(max_len, st.len);
     }
     const int64_t ind_cost = 2 * total_blocks + 3 * (int64_t)segs.size();
-    const int64_t per_slot = std::max<int64_t>(1, (ind_cost + 2 * kDecodeWarpsPerCta * sh_blocks) / slots);
-    // chunk length in blocks: about a warp slot's share (a block costs 2); each
-    // prefix is then cut into equal chunks, their count rounded to the nearest
-    const int64_t chunk = std::max<int64_t>(kMinBlocksPerWarp, per_slot / 2);
-    for (const Group &g : groups) {
-      if (g.tc) continue;
-      std::vector<int32_t> us;
-      for (int32_t m : g.members)
-        for (size_t u = unit_of_seq_first[m]; u < dunits.size() && dunits[u].seq == m; ++u)
-          us.push_back((int32_t)u);
-      const int64_t nch = std::max<int64_t>(1, (g.len + chunk / 2) / chunk);
+    const int64_t per_slot =
+        std::max<int64_t>(1, (ind_cost + 2 * kSharedRowGroups * sh_blocks) / slots);
+    auto items_for = [&](int64_t chunk) {
+      int64_t n = 0;
+      for (const Stream &st : streams) {
+        const int64_t pairs = (int64_t)(st.units.size() + kSharedRowGroups - 1) / kSharedRowGroups;
+        n += (int64_t)hkv * pairs * std::max<int64_t>(1, (st.len + chunk - 1) / chunk);
+      }
+      return n;
+    };
+    int64_t chunk = std::max<int64_t>(kMinBlocksPerWarp, per_slot / 2);
+    for (;;) {
+      const int64_t left = slots - kSharedRowGroups * items_for(chunk);
+      if (chunk >= max_len || (left > 0 && total_blocks <= left * chunk)) break;
+      chunk = std::min<int64_t>(max_len, chunk + std::max<int64_t>(1, chunk / 8));
+    }
+    for (const Stream &st : streams) {
+      const int64_t nch = std::max<int64_t>(1, (st.len + chunk - 1) / chunk);
       for (int32_t h = 0; h < hkv; ++h)
-        for (size_t i0 = 0; i0 < us.size(); i0 += kDecodeWarpsPerCta)
+        for (size_t i0 = 0; i0 < st.units.size(); i0 += kSharedRowGroups)
           for (int64_t ci = 0; ci < nch; ++ci) {
             SharedItem it;
             std::memset(&it, 0, sizeof it);
-            it.seq0 = g.members[0];
+            it.seq0 = st.seq0;
             it.h = h;
-            it.kb_begin = (int32_t)(g.len * ci / nch);
-            it.kb_end = (int32_t)(g.len * (ci + 1) / nch);
-            it.n_rg = (int32_t)std::min<size_t>(kDecodeWarpsPerCta, us.size() - i0);
+            it.kb_begin = (int32_t)(st.len * ci / nch);
+            it.kb_end = (int32_t)(st.len * (ci + 1) / nch);
+            it.n_rg = (int32_t)std::min<size_t>(kSharedRowGroups, st.units.size() - i0);
             for (int32_t w = 0; w < it.n_rg; ++w) {
-              const DUnit &du = dunits[us[i0 + w]];
+              const DUnit &du = dunits[st.units[i0 + w]];
               it.rg[w].seq = du.seq;
               it.rg[w].qi0 = du.qi0;
               it.rg[w].n_q = du.n_q;
               it.rg[w].part = -1;
               it.rg[w].q_row0 = cu_q_lens[du.seq] + du.qi0;
-              unit_shared[(size_t)us[i0 + w] * hkv + h].push_back({(int32_t)sitems.size(), w});
+              unit_shared[(size_t)st.units[i0 + w] * hkv + h].push_back({(int32_t)sitems.size(), w});
             }
             sitems.push_back(it);
           }
     }
+    // a CTA runs kSharedItemsPerCta items: pad with empty ones
+    while (sitems.size() % kSharedItemsPerCta) {
+      SharedItem it;
+      std::memset(&it, 0, sizeof it);
+      sitems.push_back(it);
+    }
   }
-  const int64_t shared_slots = (int64_t)sitems.size() * kDecodeWarpsPerCta;
+  const int64_t shared_slots = (int64_t)sitems.size() * kSharedRowGroups;
 
   // ---- gathered sub-tiles (tc groups): per group and KV head, the members'
   // query tokens in sub-tiles of up to 128 / G tokens (G rows each), neighbours
@@ -688,7 +744,7 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   info->num_prefill_merges = (int32_t)pmerges.size();
   info->num_kernels = (num_warps > 0 || !sitems.empty() ? 1 : 0) + (merges.empty() ? 0 : 1) +
                       (ptiles.empty() ? 0 : 1);
-  info->num_shared_ctas = (int32_t)sitems.size();
+  info->num_shared_ctas = (int32_t)(sitems.size() / kSharedItemsPerCta);
   info->num_gather_rows = (int32_t)gather.size();
   info->max_blocks_needed = max_nb;
   info->kv_tokens = kv_tokens;

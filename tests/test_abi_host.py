@@ -52,7 +52,7 @@ def parse_plan(info, host):
     ncta = info.num_prefill_ctas
     nsh = info.num_shared_ctas
     off_s = off_m + 8 * nm
-    off_b = off_s + 40 * nsh
+    off_b = off_s + 24 * 2 * nsh         # two 96-byte items per shared CTA
     off_f = off_b + (((ncta + 1 + 7) // 8) * 8 if ncta else 0)
     off_g = off_f + 16 * npf
     ng = info.num_gather_rows
@@ -66,7 +66,7 @@ def parse_plan(info, host):
     mer = words[off_m:off_s].reshape(nm, 8)
     pre = words[off_f:off_g].reshape(npf, 16)
     parse_plan.gather = words[off_g:off_g + 4 * ng].reshape(ng, 4)
-    parse_plan.shared = words[off_s:off_b].reshape(nsh, 40)
+    parse_plan.shared = words[off_s:off_b].reshape(2 * nsh, 24)
     pb = words[off_b:off_b + ncta + 1] if ncta else np.zeros(1, np.int32)
     if ncta:
         assert pb[0] == 0 and pb[-1] == npf and np.all(np.diff(pb) >= 0)
@@ -135,18 +135,30 @@ def check_plan(meta, info, host, num_sms):
     # warp ranges: contiguous, cover all pieces, equal cost: 2 per block plus 3
     # per segment start; each of a range's two ends may be off by one block and
     # one segment start
+    # shared-block items (verify windows wider than one row group): as pieces
+    # (seq, qi0, n_q, h, kb_begin, kb_end, part, q_row0), one per row group
+    sh = parse_plan.shared
+    rows = []
+    for it in sh:
+        for w in range(int(it[4])):
+            rg = it[8 + 8 * w:16 + 8 * w]
+            rows.append([rg[0], rg[1], rg[2], it[1], it[2], it[3], rg[3], rg[4]])
+    sh_pieces = np.array(rows, dtype=np.int32).reshape(-1, 8)
     nw = info.num_decode_warps
     if nw:
         assert wb[0] == 0 and wb[-1] == len(pieces) and np.all(np.diff(wb) >= 1)
         per_warp = [int((pieces[wb[w]:wb[w + 1], 5] - pieces[wb[w]:wb[w + 1], 4]).sum())
                     for w in range(nw)]
-        assert sum(per_warp) == sum_segment_blocks(meta)
-        cost = [2 * per_warp[w] + 3 * int((pieces[wb[w]:wb[w + 1], 4] == 0).sum())
-                for w in range(nw)]
-        assert max(cost) - min(cost) <= 2 * (2 + 3)
+        sh_blocks = int((sh_pieces[:, 5] - sh_pieces[:, 4]).sum())
+        assert sum(per_warp) + sh_blocks == sum_segment_blocks(meta)
+        if not len(sh_pieces):
+            cost = [2 * per_warp[w] + 3 * int((pieces[wb[w]:wb[w + 1], 4] == 0).sum())
+                    for w in range(nw)]
+            assert max(cost) - min(cost) <= 2 * (2 + 3)
         if num_sms is not None:
-            assert nw <= num_sms * 8
+            assert nw + 2 * len(sh) <= num_sms * 8
     assert np.all(pieces[:, 5] > pieces[:, 4])
+    pieces = np.concatenate([pieces, sh_pieces])
     # every decode segment (row group x KV head) is covered exactly once, in order
     prefill_seqs = set(int(x) for x in pre[pre[:, 12] < 0, 0]) if len(pre) else set()
     seen_parts = set()
@@ -393,7 +405,9 @@ def test_shared_prefix_items_cover_the_shared_blocks(pkv):
     got = {}
     for it in sh:
         seq0, h, kb0, kb1, nrg = (int(x) for x in it[:5])
-        assert 1 <= nrg <= 4 and 0 <= kb0 < kb1
+        if nrg == 0:                              # an empty item (pads a CTA's pair)
+            continue
+        assert 1 <= nrg <= 2 and 0 <= kb0 < kb1
         # the blocks are the same physical blocks in every member's table
         for w in range(nrg):
             seq, qi0, n_q, part, qrow = (int(x) for x in it[8 + 8 * w: 13 + 8 * w])
