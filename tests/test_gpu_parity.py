@@ -346,11 +346,13 @@ def test_state_checkpoint_full_size_pool(pkv, cuda_device):
 
 # ------------------------------------------------------------------ chained decode
 
-def _chain_case(steps, seed=77):
+def _chain_case(steps, seed=77, window=False):
     """A decode batch whose tables already hold the blocks of the chain's last step,
-    and the per-step (context_lens, slot_mapping) the chain must go through."""
-    ctx0 = np.array([15, 16, 17, 100, 31, 255, 2], dtype=np.int32)
-    ql = np.array([1, 1, 1, 2, 1, 1, 1], dtype=np.int32)    # one verify pair rides along
+    and the per-step (context_lens, slot_mapping) the chain must go through.
+    window: an 8-token verify window (two row groups: a shared-block item) rides
+    along too."""
+    ctx0 = np.array([15, 16, 17, 100, 31, 255, 2] + ([300] if window else []), dtype=np.int32)
+    ql = np.array([1, 1, 1, 2, 1, 1, 1] + ([8] if window else []), dtype=np.int32)
     last = ctx0 + (steps - 1) * ql
     meta = workloads.build_step("chain", seed, ql, last, 8, 2, 128)
     per_step = []
@@ -366,9 +368,10 @@ def _chain_case(steps, seed=77):
     return meta, per_step
 
 
-def test_decode_chain_matches_oracle_every_step(pkv, cuda_device):
+@pytest.mark.parametrize("window", [False, True])
+def test_decode_chain_matches_oracle_every_step(pkv, cuda_device, window):
     steps = 6
-    meta, per_step = _chain_case(steps)
+    meta, per_step = _chain_case(steps, window=window)
     _, _, _, pool = workloads.make_values(per_step[0])
     vals = [workloads.make_values(m, seed=500 + t)[:3] for t, m in enumerate(per_step)]
     # oracle: append then attend, step by step
@@ -386,6 +389,7 @@ def test_decode_chain_matches_oracle_every_step(pkv, cuda_device):
     bt = torch.from_numpy(meta.block_tables).to(dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     plan = pkv.plan_step(per_step[0].cu_q_lens, per_step[0].context_lens, 8, pd, chain_steps=steps)
+    assert (plan.info.num_shared_ctas > 0) == window
     outs = []
     for t, (q, k, v) in enumerate(vals):
         pkv.paged_kv_append(k.to(dev), v.to(dev), slots, pd, dev_status=status)
