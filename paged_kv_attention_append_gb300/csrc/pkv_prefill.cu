@@ -19,18 +19,20 @@
 // sees), and each row's unnormalised result goes to the split-KV kernel's
 // partial slot of its row group, where the merge combines it with the rest of
 // that row group's keys.
-// Ten warps with fixed roles:
+// Eleven warps with fixed roles:
 //   warp 8     TMA producer: both Q sub-tiles (3-D tensor map over
 //              [total_q][Hq][D]) and, per 128-key tile, K then V into a ring of
 //              K/V slots.  One 4-D TMA box is one paged block of one KV head
 //              (16 rows x D, both 64-column halves), issued by lanes 0-7 in
 //              parallel; blocks past the context are read out of bounds, i.e.
 //              zero-filled without memory traffic.
-//   warp 9     allocates 512 TMEM columns; one thread issues the MMAs:
+//   warps 9, 10  one thread each issues the MMAs of sub-tile x = warp - 9:
 //                S_x  = Q_x K_j^T        (M=128, N=128 keys, K=D; A and B from smem)
 //                O_x += P_x V_j          (M=128, N=D, K=128 keys; A = P from TMEM)
-//              in a fixed ping-pong order, and signals completion with
-//              tcgen05.commit on mbarriers.
+//              and signals completion with tcgen05.commit on mbarriers.  A
+//              thread that issues a group of MMAs is held for most of its
+//              execution time, so one issuer per sub-tile keeps the tensor pipe
+//              fed from two threads.  Warp 9 also allocates 512 TMEM columns.
 //   warps 4x .. 4x+3  softmax of sub-tile x: warp w owns TMEM lane quarter
 //              w % 4, i.e. query rows 32(w%4) .. +31, one row per thread and all
 //              128 keys of a tile.  It reads S_x, masks, takes the row max,
@@ -61,22 +63,22 @@ constexpr int kKeysPerTile = 128;
 constexpr int kBlocksPerTile = kKeysPerTile / kBlockSize;
 constexpr int kSoftmaxWarpsPerSub = 4;
 constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kMmaWarp = 9;  // warps kMmaWarp + x issue the MMAs of sub-tile x
+constexpr int kThreads = 352;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kMaxSlots = 8;
 
 enum {
   B_Q_FULL = 0,                  // both Q sub-tiles of an item landed
-  B_Q_EMPTY = 1,                 // every S MMA of an item completed (Q may be reloaded)
+  B_Q_EMPTY = 1,                 // every S MMA of an item completed (one arrival per issuer)
   B_FULL = 2,                    // + slot: K or V tile landed
-  B_EMPTY = B_FULL + kMaxSlots,  // + slot: every MMA reading it completed
+  B_EMPTY = B_FULL + kMaxSlots,  // + slot: every MMA reading it completed (one per issuer)
   B_S_FULL = B_EMPTY + kMaxSlots,  // + sub-tile: S_x = Q_x K^T completed
   B_P_FULL = B_S_FULL + 2,       // + sub-tile: P_x written to TMEM (4 warps arrive)
   B_O_DONE = B_P_FULL + 2,       // + sub-tile: O_x += P_x V completed
-  B_DRAIN = B_O_DONE + 2,
-  B_COUNT = B_DRAIN + 1
+  B_DRAIN = B_O_DONE + 2,        // + sub-tile: every MMA its issuer issued completed
+  B_COUNT = B_DRAIN + 2
 };
 
 template <int D>
@@ -242,17 +244,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_Q_FULL), 1);
-    mbar_init(bar(B_Q_EMPTY), 1);
+    mbar_init(bar(B_Q_EMPTY), 2);
     for (int s = 0; s < C::kSlots; ++s) {
       mbar_init(bar(B_FULL + s), 1);
-      mbar_init(bar(B_EMPTY + s), 1);
+      mbar_init(bar(B_EMPTY + s), 2);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(bar(B_S_FULL + x), 1);
       mbar_init(bar(B_P_FULL + x), kSoftmaxWarpsPerSub);
       mbar_init(bar(B_O_DONE + x), 1);
     }
-    mbar_init(bar(B_DRAIN), 1);
+    mbar_init(bar(B_DRAIN + 0), 1);
+    mbar_init(bar(B_DRAIN + 1), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -426,21 +429,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(bar(B_FULL + l % C::kSlots), (uint32_t)((l / C::kSlots) & 1));
       if (nq > 0) mbar_wait(bar(B_Q_FULL), (uint32_t)((nq - 1) & 1));
     }
-  } else if (warp == kMmaWarp) {
-    // ======================================================== MMA issuer
-    // Per item a fixed ping-pong order: S_0(0) S_1(0), then per key tile j
-    //   O_0 += P_0(j) V_j, S_0(j+1), O_1 += P_1(j) V_j, S_1(j+1),
-    // so each sub-tile's softmax of tile j runs while the tensor pipe works on
-    // the other sub-tile's two MMA groups.  (An MMA group of 8 instructions
-    // blocks the issuing thread for about its execution time, so the order of
-    // issue is the order of execution.)  S_x of any tile waits for the previous
-    // O_x += P_x V (it writes over P_x), also across items; the first O_x += P_x V
-    // of an item needs nothing more, since the softmax warps finish reading O_x
-    // of the previous item before they write the new P_x.  A ring slot is
-    // released by a commit once every MMA reading it has been issued; B_Q_EMPTY
-    // once every S MMA of the item has.  Waits are bounded (PKV_DEV_TIMEOUT)
-    // and stop at an abort.
+  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+    // ======================================================== MMA issuer of sub-tile x
+    // Per item: S_x(0), then per key tile j < nt_x: O_x += P_x(j) V_j, S_x(j+1).
+    // While sub-tile x's softmax of tile j runs, its issuer waits and the
+    // other sub-tile's MMAs run.  S_x of any tile waits for the previous
+    // O_x += P_x V (it writes over P_x), also across items; the first
+    // O_x += P_x V of an item needs nothing more, since the softmax warps finish
+    // reading O_x of the previous item before they write the new P_x.  Both
+    // issuers arrive (tcgen05.commit) on the release of every ring slot and of
+    // Q once per use, in ring order, also for key tiles past their own nt_x;
+    // each waits for a slot's load before releasing it, so an issuer running
+    // ahead never arrives on the slot's next use early.  Waits are bounded
+    // (PKV_DEV_TIMEOUT) and stop at an abort.
     if (lane == 0) {
+      const int x = warp - kMmaWarp;
       constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kPrefillRows, kKeysPerTile, 0, 0);
       constexpr uint32_t kIdescO = tc::idesc_bf16_f32(kPrefillRows, D, 0, 1);
       auto wait = [&](int b, int parity) -> bool {
@@ -449,17 +452,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         fail();
         return false;
       };
-      int L0 = 0, nq = 0;       // ring index of the item's K_0; items (Q loads) done
-      int tx0 = 0, tx1 = 0;     // key tiles sub-tile 0 / 1 ran in earlier items
-      int n_s = 0, n_s_item = 0;  // S MMAs issued in this item / due in it
+      const uint32_t sq = smem_u32(smem + C::kOffQ + x * C::kQBytes);
+      int L0 = 0, nq = 0;  // ring index of the item's K_0; items (Q loads) done
+      int tx = 0;          // key tiles this sub-tile ran in earlier items
       // S_x(j) = Q_x K_j^T once K_j landed and the previous P_x was consumed
-      auto issue_s = [&](int x, int j) -> bool {
+      auto issue_s = [&](int j) -> bool {
         const int L = L0 + 2 * j, s = L % C::kSlots;
-        const int run = (x ? tx1 : tx0) + j;  // running tile index of sub-tile x
         if (!wait(B_FULL + s, L / C::kSlots)) return false;
-        if (run > 0 && !wait(B_O_DONE + x, run - 1)) return false;
+        if (tx + j > 0 && !wait(B_O_DONE + x, tx + j - 1)) return false;
         tc::fence_after_sync();
-        const uint32_t sq = smem_u32(smem + C::kOffQ + x * C::kQBytes);
         const uint32_t sk = smem_u32(smem + C::kOffRing + s * C::kSlotBytes);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
@@ -470,13 +471,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::mma_bf16(t_s(x), a, b, kIdescS, ks > 0 ? 1u : 0u);
         }
         tc::commit(bar(B_S_FULL + x));
-        if (++n_s == n_s_item) tc::commit(bar(B_Q_EMPTY));  // every S of the item issued
         return true;
       };
       // O_x += P_x(j) V_j once P_x(j) is in TMEM and V_j landed
-      auto issue_pv = [&](int x, int j) -> bool {
+      auto issue_pv = [&](int j) -> bool {
         const int L = L0 + 2 * j + 1, s = L % C::kSlots;
-        if (!wait(B_P_FULL + x, (x ? tx1 : tx0) + j)) return false;
+        if (!wait(B_P_FULL + x, tx + j)) return false;
         if (!wait(B_FULL + s, L / C::kSlots)) return false;
         tc::fence_after_sync();
         const uint32_t sv = smem_u32(smem + C::kOffRing + s * C::kSlotBytes);
@@ -488,36 +488,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::commit(bar(B_O_DONE + x));
         return true;
       };
+      // release ring load L (after its landing, so the arrival is for this use)
+      auto release = [&](int L) -> bool {
+        if (!wait(B_FULL + L % C::kSlots, L / C::kSlots)) return false;
+        tc::commit(bar(B_EMPTY + L % C::kSlots));
+        return true;
+      };
       bool good = true;
       for (int it = it0; it < it1 && good; ++it) {
         const ItemMeta m = load_item(p, it);
         if (!m.ok) continue;
-        const int nt0 = m.nt[0], nt1 = m.nt[1];
+        const int ntx = x ? m.nt[1] : m.nt[0];
         good = wait(B_Q_FULL, nq);
-        n_s = 0;
-        n_s_item = nt0 + nt1;
-        for (int x = 0; x < 2 && good; ++x)
-          if ((x ? nt1 : nt0) > 0) good = issue_s(x, 0);
-        if (good) tc::commit(bar(B_EMPTY + L0 % C::kSlots));  // K_0 read by every S(0)
+        if (good && ntx > 0) good = issue_s(0);
+        if (good && ntx <= 1) tc::commit(bar(B_Q_EMPTY));  // every S of the item issued
+        if (good) good = release(L0);                       // K_0
         for (int j = 0; good && j < m.nkt; ++j) {
-          for (int x = 0; x < 2 && good; ++x) {
-            const int ntx = x ? nt1 : nt0;
-            if (j >= ntx) continue;
-            good = issue_pv(x, j);
-            if (good && j + 1 < ntx) good = issue_s(x, j + 1);
+          if (j < ntx) {
+            good = issue_pv(j);
+            if (good && j + 1 < ntx) {
+              good = issue_s(j + 1);
+              if (good && j + 2 == ntx) tc::commit(bar(B_Q_EMPTY));
+            }
           }
-          if (!good) break;
-          tc::commit(bar(B_EMPTY + (L0 + 2 * j + 1) % C::kSlots));  // V_j
-          if (j + 1 < m.nkt) tc::commit(bar(B_EMPTY + (L0 + 2 * j + 2) % C::kSlots));  // K_{j+1}
+          if (good) good = release(L0 + 2 * j + 1);                        // V_j
+          if (good && j + 1 < m.nkt) good = release(L0 + 2 * j + 2);      // K_{j+1}
         }
         L0 += 2 * m.nkt;
-        tx0 += nt0;
-        tx1 += nt1;
+        tx += ntx;
         ++nq;
       }
       // every MMA issued so far completes before TMEM is released
-      tc::commit(bar(B_DRAIN));
-      mbar_wait(bar(B_DRAIN), 0);
+      tc::commit(bar(B_DRAIN + x));
+      mbar_wait(bar(B_DRAIN + x), 0);
     }
   } else {
     // ======================================================== softmax (4 warps per sub-tile)
