@@ -8,8 +8,9 @@
 // ("Faster prefill on M5") is the prior art for putting this on the tensor
 // units; here QK^T and PV are tcgen05 MMAs with fp32 accumulators in TMEM.
 //
-// One CTA = two query sub-tiles (x = 0, 1) of 128 tokens x one query head each,
-// whose heads share one KV head: every K/V tile is loaded once for both.
+// A work item holds two query sub-tiles (x = 0, 1) of 128 tokens x one query
+// head each, whose heads share one KV head.  A CTA runs an item's sub-tiles one
+// after the other as passes; a pass streams the sub-tile's key tiles.
 // A sub-tile may instead be gathered: 128 rows (query token x query head, all
 // G heads of the KV head) from several sequences whose block tables hold the
 // same physical blocks over the item's keys -- a shared prefix, read once per
@@ -19,31 +20,32 @@
 // sees), and each row's unnormalised result goes to the split-KV kernel's
 // partial slot of its row group, where the merge combines it with the rest of
 // that row group's keys.
-// Eleven warps with fixed roles:
-//   warp 8     TMA producer: both Q sub-tiles (3-D tensor map over
-//              [total_q][Hq][D]) and, per 128-key tile, K then V into a ring of
-//              K/V slots.  One 4-D TMA box is one paged block of one KV head
-//              (16 rows x D, both 64-column halves), issued by lanes 0-7 in
-//              parallel; blocks past the context are read out of bounds, i.e.
-//              zero-filled without memory traffic.
-//   warps 9, 10  one thread each issues the MMAs of sub-tile x = warp - 9:
-//                S_x  = Q_x K_j^T        (M=128, N=128 keys, K=D; A and B from smem)
-//                O_x += P_x V_j          (M=128, N=D, K=128 keys; A = P from TMEM)
-//              and signals completion with tcgen05.commit on mbarriers.  A
-//              thread that issues a group of MMAs is held for most of its
-//              execution time, so one issuer per sub-tile keeps the tensor pipe
-//              fed from two threads.  Warp 9 also allocates 512 TMEM columns.
-//   warps 4x .. 4x+3  softmax of sub-tile x: warp w owns TMEM lane quarter
-//              w % 4, i.e. query rows 32(w%4) .. +31, one row per thread and all
-//              128 keys of a tile.  It reads S_x, masks, takes the row max,
-//              computes 2^(scale*s - m) and the row sum, and writes P_x as bf16
-//              over the first 64 columns of S_x in TMEM, where the PV MMA reads
-//              it.  O_x is rescaled in TMEM only when a row's max grows by more
-//              than 2^8 (the softmax is exact for any reference point; the
-//              threshold only bounds P <= 2^8).
-// The two sub-tiles ping-pong on the tensor pipe: while one sub-tile's softmax
-// runs, the other's MMAs do.  S_x(j+1) overwrites P_x(j), so it is issued once
-// O_x += P_x(j) V_j has completed.
+// Seven warps with fixed roles:
+//   warp 4     TMA producer: the pass's Q sub-tile (3-D tensor map over
+//              [total_q][Hq][D]) and, per 128-key tile, K into a ring of K slots
+//              and V into a ring of V slots, K one tile ahead of V.  One 4-D TMA
+//              box is one paged block of one KV head (16 rows x D, both
+//              64-column halves), issued by lanes 0-7 in parallel; blocks past
+//              the context are read out of bounds, i.e. zero-filled without
+//              memory traffic.  Block-table entries are read 32 at a time (four
+//              tiles), one group ahead.
+//   warp 5     allocates 512 TMEM columns; one thread issues S(j) = Q K_j^T
+//              (M=128, N=128 keys, K=D; A and B from smem) into S buffer j % 3.
+//   warp 6     one thread issues O += P(j) V_j (M=128, N=D, K=128 keys; A = P
+//              from TMEM, over the first 64 columns of S buffer j % 3).
+//   warps 0-3  softmax: warp w owns TMEM lane quarter w, i.e. query rows
+//              32w .. 32w+31, one row per thread and all 128 keys of a tile.
+//              It reads S(j), masks, takes the row max, computes
+//              2^(scale*s - m) and the row sum, and writes P(j) as bf16 over
+//              the first 64 columns of S(j) in TMEM.  O is rescaled in TMEM
+//              only when a row's max grows by more than 2^8 (the softmax is
+//              exact for any reference point; the threshold only bounds
+//              P <= 2^8).
+// TMEM holds three S buffers and O (3 x 128 + D <= 512 columns), so S(j+1) and
+// S(j+2) are computed while the softmax of tile j runs; S(j+3) reuses the
+// buffer of S(j) once O += P(j) V_j has read P(j).  Only the softmax and the
+// PV chain are serial per tile; the two issuers keep two independent
+// accumulators (an S buffer and O) in flight on the tensor pipe.
 // Every wait is bounded; a timeout reports PKV_DEV_TIMEOUT, every role drains
 // what it issued, and TMEM is always freed.
 #include <cuda_runtime.h>
@@ -61,23 +63,26 @@ namespace {
 
 constexpr int kKeysPerTile = 128;
 constexpr int kBlocksPerTile = kKeysPerTile / kBlockSize;
-constexpr int kSoftmaxWarpsPerSub = 4;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;  // warps kMmaWarp + x issue the MMAs of sub-tile x
-constexpr int kThreads = 352;
+constexpr int kSoftmaxWarps = 4;
+constexpr int kProducerWarp = 4;
+constexpr int kSWarp = 5;   // issues the S MMAs; owns the TMEM allocation
+constexpr int kPvWarp = 6;  // issues the PV MMAs
+constexpr int kThreads = 224;
 constexpr uint32_t kTmemCols = 512;
+constexpr int kSBufs = 3;
 constexpr float kRescaleLog2 = 8.0f;
-constexpr int kMaxSlots = 8;
+constexpr int kMaxSlots = 4;  // per ring (K, V)
+constexpr int kTablePrefetchTiles = 32 / kBlocksPerTile;  // tiles per warp-wide table read
 
 enum {
-  B_Q_FULL = 0,                  // both Q sub-tiles of an item landed
-  B_Q_EMPTY = 1,                 // every S MMA of an item completed (one arrival per issuer)
-  B_FULL = 2,                    // + slot: K or V tile landed
-  B_EMPTY = B_FULL + kMaxSlots,  // + slot: every MMA reading it completed (one per issuer)
-  B_S_FULL = B_EMPTY + kMaxSlots,  // + sub-tile: S_x = Q_x K^T completed
-  B_P_FULL = B_S_FULL + 2,       // + sub-tile: P_x written to TMEM (4 warps arrive)
-  B_O_DONE = B_P_FULL + 2,       // + sub-tile: O_x += P_x V completed
-  B_DRAIN = B_O_DONE + 2,        // + sub-tile: every MMA its issuer issued completed
+  B_Q_FULL = 0,                  // the pass's Q sub-tile landed
+  B_Q_EMPTY = 1,                 // every S MMA of a pass completed (Q may be reloaded)
+  B_FULL = 2,                    // + ring * kMaxSlots + slot: K (ring 0) or V (ring 1) tile landed
+  B_EMPTY = B_FULL + 2 * kMaxSlots,  // + ring * kMaxSlots + slot: the MMAs reading it completed
+  B_S_FULL = B_EMPTY + 2 * kMaxSlots,  // + buffer: S(j) = Q K_j^T completed
+  B_P_FULL = B_S_FULL + kSBufs,  // + buffer: P(j) written to TMEM (4 warps arrive)
+  B_FREE = B_P_FULL + kSBufs,    // + buffer: O += P(j) V_j completed (buffer reusable)
+  B_DRAIN = B_FREE + kSBufs,     // + issuer: every MMA it issued completed
   B_COUNT = B_DRAIN + 2
 };
 
@@ -91,15 +96,18 @@ struct PrefillCfg {
   // inside a slot, paged block b sits at b * kBlockBytes as
   // [8-row group g (2)][64-column half (kHalves)][8 rows][128 B], 128-byte swizzle
   static constexpr int kGroupStride = kHalves * 1024;
-  static constexpr int kSlots = D == 128 ? 5 : kMaxSlots;
+  // slots per ring: K_j is refilled once S(j) completed, V_j once O += P(j) V_j
+  // did; S runs up to two tiles ahead of the softmax
+  static constexpr int kSlots = D == 128 ? 3 : kMaxSlots;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffRing = 2 * kQBytes;
-  static constexpr int kOffBar = kOffRing + kSlots * kSlotBytes;
+  static constexpr int kOffRing = kQBytes;  // K ring, then V ring
+  static constexpr int kOffBar = kOffRing + 2 * kSlots * kSlotBytes;
   static constexpr int kUsed = kOffBar + B_COUNT * 8 + 16;
   // at least 120 KB so a second CTA never shares the SM (and its TMEM)
   static constexpr int kSmemBytes = (kUsed + 1024) > 120 * 1024 ? (kUsed + 1024) : 120 * 1024;
   static_assert(kSlots <= kMaxSlots, "ring too deep");
   static_assert(kUsed + 1024 <= 227 * 1024, "shared memory budget");
+  static_assert(kSBufs * kKeysPerTile + D <= (int)kTmemCols, "TMEM budget");
 };
 
 struct PrefillParams {
@@ -232,9 +240,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // items and the q tiles go ahead; the producer waits for the predecessor
   // before its first pool read, and no other role reads the pool.
   pdl_trigger();
-  // this CTA's bin of work items, run one after another; every barrier keeps
-  // counting phases across items (an item that fails its checks is skipped by
-  // every role alike and reported by the producer)
+  // this CTA's bin of work items, run one after another, each as one pass per
+  // present sub-tile; every barrier keeps counting phases across passes (an
+  // item that fails its checks is skipped by every role alike and reported by
+  // the producer)
   const int it0 = __ldg(p.bin_begin + blockIdx.x), it1 = __ldg(p.bin_begin + blockIdx.x + 1);
 
   uint64_t *bars = reinterpret_cast<uint64_t *>(smem + C::kOffBar);
@@ -244,22 +253,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(B_Q_FULL), 1);
-    mbar_init(bar(B_Q_EMPTY), 2);
-    for (int s = 0; s < C::kSlots; ++s) {
-      mbar_init(bar(B_FULL + s), 1);
-      mbar_init(bar(B_EMPTY + s), 2);
-    }
-    for (int x = 0; x < 2; ++x) {
-      mbar_init(bar(B_S_FULL + x), 1);
-      mbar_init(bar(B_P_FULL + x), kSoftmaxWarpsPerSub);
-      mbar_init(bar(B_O_DONE + x), 1);
+    mbar_init(bar(B_Q_EMPTY), 1);
+    for (int r = 0; r < 2; ++r)
+      for (int s = 0; s < C::kSlots; ++s) {
+        mbar_init(bar(B_FULL + r * kMaxSlots + s), 1);
+        mbar_init(bar(B_EMPTY + r * kMaxSlots + s), 1);
+      }
+    for (int b = 0; b < kSBufs; ++b) {
+      mbar_init(bar(B_S_FULL + b), 1);
+      mbar_init(bar(B_P_FULL + b), kSoftmaxWarps);
+      mbar_init(bar(B_FREE + b), 1);
     }
     mbar_init(bar(B_DRAIN + 0), 1);
     mbar_init(bar(B_DRAIN + 1), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kSWarp) {
     tc::alloc(smem_u32(tmem_slot), kTmemCols);
     tc::relinquish_alloc_permit();
   }
@@ -267,9 +277,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
-  // TMEM columns: S_x at 128 x; O_x at 256 + D x.  P_x overlays S_x columns 0-63.
-  auto t_s = [&](int x) { return tmem + (uint32_t)(x * kKeysPerTile); };
-  auto t_o = [&](int x) { return tmem + (uint32_t)(2 * kKeysPerTile + x * D); };
+  // TMEM columns: S buffer b at 128 b; O at 384.  P(j) overlays columns 0-63 of
+  // its S buffer.
+  auto t_s = [&](int b) { return tmem + (uint32_t)(b * kKeysPerTile); };
+  const uint32_t t_o = tmem + (uint32_t)(kSBufs * kKeysPerTile);
 
   auto fail = [&]() {
     report(p.dev_status, PKV_DEV_TIMEOUT);
@@ -284,139 +295,156 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&qr_map);
       prefetch_tmap(&kv_map);
     }
-    // Ring load L (counted over the CTA's items) is K_j (even) or V_j (odd) of
-    // the current item, in slot L % kSlots.  Lane b < 8 owns paged block b of
-    // every tile: it reads that block's table entry once per tile (a coalesced
-    // 32-byte load, issued before the wait for a free slot) and issues the
-    // block's K and V boxes itself.  The Q tiles of an item wait until every
-    // S MMA of the previous item has read its Q (B_Q_EMPTY).
+    // Ring r (0: K, 1: V) load n_r (counted over the CTA's passes) sits in slot
+    // n_r % kSlots.  Per pass the loads go K_0, then K_{j+1}, V_j for each tile
+    // j, so a wait for a V slot (its O += P V) never holds up the K that the S
+    // MMAs need next.  Lane b < 8 issues paged block b of every tile; the
+    // table entries of four tiles come with one coalesced read by the whole
+    // warp, the next four read while the current ones are used.  The Q
+    // sub-tile of a pass waits until every S MMA of the previous pass has read
+    // its Q (B_Q_EMPTY).
     const int hkv = p.num_kv_heads;
-    int L = 0, nq = 0;  // ring loads and Q loads issued
+    int nld[2] = {0, 0};  // loads issued per ring
+    int npass = 0;        // passes (Q loads) issued
     bool good = true, waited = false;
+    // one K (r = 0) or V (r = 1) tile of KV head h into ring r; lane b < 8
+    // copies paged block `phys` (-1 or out of range: zero fill)
+    auto load_tile = [&](int r, int h, int phys) -> bool {
+      const int n = nld[r], s = n % C::kSlots;
+      if (n >= C::kSlots &&
+          !__all_sync(0xffffffffu, mbar_wait(bar(B_EMPTY + r * kMaxSlots + s),
+                                             (uint32_t)(((n / C::kSlots) - 1) & 1)))) {
+        if (lane == 0) fail();
+        return false;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(bar(B_FULL + r * kMaxSlots + s), C::kSlotBytes);
+      __syncwarp();
+      if (lane < kBlocksPerTile) {
+        int g = p.pool_groups;  // out of range: zero fill, no memory traffic
+        if (phys >= 0 && phys < p.num_blocks) g = ((phys * 2 + r) * hkv + h) * (kBlockSize / 8);
+        tma_load_4d(smem_u32(smem + C::kOffRing + (r * C::kSlots + s) * C::kSlotBytes) +
+                        lane * C::kBlockBytes,
+                    &kv_map, 0, 0, 0, g, bar(B_FULL + r * kMaxSlots + s));
+      }
+      ++nld[r];
+      return true;
+    };
     for (int it = it0; it < it1 && good; ++it) {
       const ItemMeta m = load_item(p, it);
       if (!m.ok) {
         if (lane == 0) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
         continue;
       }
-      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
       const int32_t *table = p.block_tables + (int64_t)m.t.seq * p.max_blocks_per_seq;
       const int nblk_ctx = (m.ctx + kBlockSize - 1) / kBlockSize;
-      // lane b < 8: the physical id of block b of key tile j (-1: none, zero fill)
-      auto tile_block = [&](int j) -> int {
-        const int kb = j * kBlocksPerTile + lane;
-        return lane < kBlocksPerTile && kb < nblk_ctx && kb < p.max_blocks_per_seq
-                   ? __ldg(table + kb)
-                   : -1;
+      const int nblk = min(nblk_ctx, p.max_blocks_per_seq);
+      // entry of block `lane` of the four tiles from relative tile 4 k on
+      // (-1: past the context or the table, zero fill)
+      auto read_group = [&](int k) -> int {
+        const int kb = (m.t.kt0 + kTablePrefetchTiles * k) * kBlocksPerTile + lane;
+        return kb < nblk ? __ldg(table + kb) : -1;
       };
-      int phys_first = tile_block(m.t.kt0);  // read now: it lands while q is loaded
-      if (nq > 0 &&
-          !__all_sync(0xffffffffu, mbar_wait(bar(B_Q_EMPTY), (uint32_t)((nq - 1) & 1)))) {
-        if (lane == 0) fail();
-        break;
-      }
-      const int nsub = m.t.n_q[1] > 0 ? 2 : 1;
-      if (!m.gathered) {
-        if (lane == 0) {
-          mbar_arrive_expect_tx(bar(B_Q_FULL), nsub * C::kQBytes);
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            if (x >= nsub) break;
-            const uint32_t sq = smem_u32(smem + C::kOffQ + x * C::kQBytes);
-#pragma unroll
-            for (int hh = 0; hh < C::kHalves; ++hh)
-              tma_load_3d(sq + hh * C::kQHalfBytes, &q_map, hh * 64, m.t.hq[x],
-                          m.cu0 + m.t.qi0[x], bar(B_Q_FULL));
-          }
-        }
-        __syncwarp();
-      } else {
-        // one box per token (its G heads x 64 columns, rows t*G ..); a token
-        // index outside q reads as zeros (and is reported), so the byte count
-        // the barrier expects holds either way
-        // a sub-tile of consecutive tokens is one box of 128 / G tokens (rows
-        // past its n_q * G hold other tokens or zeros and are masked); any
-        // other gets one box per token
-        const int G = p.group, row_bytes = G * 128, run_tokens = kPrefillRows / G;
-        const bool r0 = (m.t.runs & 1) != 0, r1 = nsub > 1 && (m.t.runs & 2) != 0;
-        const int n0 = m.t.n_q[0], n1 = nsub > 1 ? m.t.n_q[1] : 0;
-        const int l0 = r0 ? 0 : n0, l1 = r1 ? 0 : n1;  // tokens loaded one by one
-        if (lane == 0) {
-          mbar_arrive_expect_tx(
-              bar(B_Q_FULL),
-              ((r0 ? run_tokens : n0) + (nsub > 1 ? (r1 ? run_tokens : n1) : 0)) * row_bytes *
-                  C::kHalves);
-#pragma unroll
-          for (int x = 0; x < 2; ++x) {
-            if (!(x ? r1 : r0)) continue;
-            const uint32_t sq = smem_u32(smem + C::kOffQ + x * C::kQBytes);
-#pragma unroll
-            for (int hh = 0; hh < C::kHalves; ++hh)
-              tma_load_3d(sq + hh * C::kQHalfBytes, &qr_map, hh * 64, m.t.h * G,
-                          x ? m.t.qi0[1] : m.t.qi0[0], bar(B_Q_FULL));
-          }
-        }
-        __syncwarp();
-        // token tk = lane + 32 r of sub-tile x (<= 128 tokens each): all token
-        // indices are read first, so their latencies overlap
-        int qt[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int x = i >> 2, tk = lane + 32 * (i & 3);
-          qt[i] = tk < (x ? l1 : l0) ? __ldg(&p.gather[(x ? m.t.gather[1] : m.t.gather[0]) + tk].q_tok)
-                                     : 0;
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int x = i >> 2, tk = lane + 32 * (i & 3);
-          if (tk >= (x ? l1 : l0)) continue;
-          if (qt[i] < 0 || qt[i] >= p.total_q) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
-          const uint32_t sq = smem_u32(smem + C::kOffQ + x * C::kQBytes) + tk * row_bytes;
-#pragma unroll
-          for (int hh = 0; hh < C::kHalves; ++hh)
-            tma_load_3d(sq + hh * C::kQHalfBytes, &qg_map, hh * 64, m.t.h * G, qt[i], bar(B_Q_FULL));
-        }
-        __syncwarp();
-      }
-      ++nq;
-      // the pool is the predecessor's output: wait for it before the first copy
-      if (!waited) {
-        pdl_wait();
-        waited = true;
-      }
-      int g_k = p.pool_groups;  // this lane's K group coordinate for the current tile
-      for (int jl = 0; jl < 2 * m.nkt; ++jl) {
+      for (int x = 0; x < 2 && good; ++x) {
+        const int ntx = x ? m.nt[1] : m.nt[0];
+        if (ntx == 0) continue;
         if (__any_sync(0xffffffffu, *abort_flag != 0)) {
           good = false;
           break;
         }
-        const int j = m.t.kt0 + (jl >> 1);  // absolute key tile
-        if ((jl & 1) == 0) {
-          const int phys = jl == 0 ? phys_first : tile_block(j);
-          g_k = p.pool_groups;  // out of range: zero fill, no memory traffic
-          if (phys >= 0 && phys < p.num_blocks)
-            g_k = ((phys * 2 + 0) * hkv + m.t.h) * (kBlockSize / 8);
-          else if (phys != -1 || (lane < kBlocksPerTile &&
-                                  j * kBlocksPerTile + lane < min(nblk_ctx, p.max_blocks_per_seq)))
-            report(p.dev_status, PKV_DEV_BAD_BLOCK);
-        }
-        const int s = L % C::kSlots;
-        if (L >= C::kSlots &&
-            !__all_sync(0xffffffffu,
-                        mbar_wait(bar(B_EMPTY + s), (uint32_t)(((L / C::kSlots) - 1) & 1)))) {
+        int ent_cur = read_group(0), ent_next = read_group(1);  // land while q is loaded
+        if (npass > 0 &&
+            !__all_sync(0xffffffffu, mbar_wait(bar(B_Q_EMPTY), (uint32_t)((npass - 1) & 1)))) {
           if (lane == 0) fail();
           good = false;
           break;
         }
-        if (lane == 0) mbar_arrive_expect_tx(bar(B_FULL + s), C::kSlotBytes);
-        __syncwarp();
-        if (lane < kBlocksPerTile) {
-          const int g =
-              (jl & 1) == 0 || g_k == p.pool_groups ? g_k : g_k + hkv * (kBlockSize / 8);
-          tma_load_4d(smem_u32(smem + C::kOffRing + s * C::kSlotBytes) + lane * C::kBlockBytes,
-                      &kv_map, 0, 0, 0, g, bar(B_FULL + s));
+        const uint32_t sq = smem_u32(smem + C::kOffQ);
+        const int qi0 = x ? m.t.qi0[1] : m.t.qi0[0];
+        if (!m.gathered) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar(B_Q_FULL), C::kQBytes);
+#pragma unroll
+            for (int hh = 0; hh < C::kHalves; ++hh)
+              tma_load_3d(sq + hh * C::kQHalfBytes, &q_map, hh * 64, x ? m.t.hq[1] : m.t.hq[0],
+                          m.cu0 + qi0, bar(B_Q_FULL));
+          }
+          __syncwarp();
+        } else {
+          // a sub-tile of consecutive tokens is one box of 128 / G tokens (rows
+          // past its n_q * G hold other tokens or zeros and are masked); any
+          // other gets one box per token (its G heads x 64 columns, rows t*G ..);
+          // a token index outside q reads as zeros (and is reported), so the
+          // byte count the barrier expects holds either way
+          const int G = p.group, row_bytes = G * 128, run_tokens = kPrefillRows / G;
+          const bool run = ((m.t.runs >> x) & 1) != 0;
+          const int nx = x ? m.t.n_q[1] : m.t.n_q[0];
+          const int lx = run ? 0 : nx;  // tokens loaded one by one
+          if (lane == 0) {
+            mbar_arrive_expect_tx(bar(B_Q_FULL), (run ? run_tokens : nx) * row_bytes * C::kHalves);
+            if (run)
+#pragma unroll
+              for (int hh = 0; hh < C::kHalves; ++hh)
+                tma_load_3d(sq + hh * C::kQHalfBytes, &qr_map, hh * 64, m.t.h * G, qi0,
+                            bar(B_Q_FULL));
+          }
+          __syncwarp();
+          // token tk = lane + 32 i (<= 128 tokens): all token indices are read
+          // first, so their latencies overlap
+          const int gbase = x ? m.t.gather[1] : m.t.gather[0];
+          int qt[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int tk = lane + 32 * i;
+            qt[i] = tk < lx ? __ldg(&p.gather[gbase + tk].q_tok) : 0;
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int tk = lane + 32 * i;
+            if (tk >= lx) continue;
+            if (qt[i] < 0 || qt[i] >= p.total_q) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
+#pragma unroll
+            for (int hh = 0; hh < C::kHalves; ++hh)
+              tma_load_3d(sq + tk * row_bytes + hh * C::kQHalfBytes, &qg_map, hh * 64, m.t.h * G,
+                          qt[i], bar(B_Q_FULL));
+          }
+          __syncwarp();
         }
-        ++L;
+        ++npass;
+        // the pool is the predecessor's output: wait for it before the first copy
+        if (!waited) {
+          pdl_wait();
+          waited = true;
+        }
+        // the physical block of this lane (< 8) in relative tile j: checked once
+        // per tile; ids past the context (-1) are zero-filled
+        int phys_k = -1, phys_v = -1;  // of the next K tile to load / the next V
+        auto tile_phys = [&](int j) -> int {
+          if ((j % kTablePrefetchTiles) == 0 && j > 0) {
+            ent_cur = ent_next;
+            ent_next = read_group(j / kTablePrefetchTiles + 1);
+          }
+          const int e = __shfl_sync(0xffffffffu, ent_cur,
+                                    (j % kTablePrefetchTiles) * kBlocksPerTile + (lane & 7));
+          const int kb = (m.t.kt0 + j) * kBlocksPerTile + lane;
+          if (lane < kBlocksPerTile && ((e != -1 && (e < 0 || e >= p.num_blocks)) ||
+                                        (e == -1 && kb < nblk)))
+            report(p.dev_status, PKV_DEV_BAD_BLOCK);
+          return lane < kBlocksPerTile ? e : -1;
+        };
+        phys_k = tile_phys(0);
+        good = load_tile(0, m.t.h, phys_k);
+        for (int j = 0; good && j < ntx; ++j) {
+          if (__any_sync(0xffffffffu, *abort_flag != 0)) {
+            good = false;
+            break;
+          }
+          phys_v = phys_k;
+          if (j + 1 < ntx) {
+            phys_k = tile_phys(j + 1);
+            good = load_tile(0, m.t.h, phys_k);
+          }
+          if (good) good = load_tile(1, m.t.h, phys_v);
+        }
       }
     }
     // the kernel must not complete before its predecessor (the next kernel's
@@ -425,25 +453,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     // our copies still in flight land before the CTA can exit: only the last
     // load of each slot can be pending (a slot is refilled after it was consumed)
     if (lane == 0) {
-      for (int l = max(0, L - C::kSlots); l < L; ++l)
-        mbar_wait(bar(B_FULL + l % C::kSlots), (uint32_t)((l / C::kSlots) & 1));
-      if (nq > 0) mbar_wait(bar(B_Q_FULL), (uint32_t)((nq - 1) & 1));
+      for (int r = 0; r < 2; ++r)
+        for (int l = max(0, nld[r] - C::kSlots); l < nld[r]; ++l)
+          mbar_wait(bar(B_FULL + r * kMaxSlots + l % C::kSlots), (uint32_t)((l / C::kSlots) & 1));
+      if (npass > 0) mbar_wait(bar(B_Q_FULL), (uint32_t)((npass - 1) & 1));
     }
-  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
-    // ======================================================== MMA issuer of sub-tile x
-    // Per item: S_x(0), then per key tile j < nt_x: O_x += P_x(j) V_j, S_x(j+1).
-    // While sub-tile x's softmax of tile j runs, its issuer waits and the
-    // other sub-tile's MMAs run.  S_x of any tile waits for the previous
-    // O_x += P_x V (it writes over P_x), also across items; the first
-    // O_x += P_x V of an item needs nothing more, since the softmax warps finish
-    // reading O_x of the previous item before they write the new P_x.  Both
-    // issuers arrive (tcgen05.commit) on the release of every ring slot and of
-    // Q once per use, in ring order, also for key tiles past their own nt_x;
-    // each waits for a slot's load before releasing it, so an issuer running
-    // ahead never arrives on the slot's next use early.  Waits are bounded
-    // (PKV_DEV_TIMEOUT) and stop at an abort.
+  } else if (warp == kSWarp || warp == kPvWarp) {
+    // ======================================================== MMA issuers
+    // Tile g (counted over the CTA's passes) uses S buffer g % 3 and load g of
+    // the K and of the V ring.  The S issuer
+    // runs S(g) once K_j landed and O += P(g-3) V has completed (it read P(g-3)
+    // from the same buffer); the PV issuer runs O += P(g) V_j once P(g) is in
+    // TMEM and V_j landed.  Consecutive PV MMAs accumulate into O in issue
+    // order; the softmax rescales O only after waiting for the previous PV.
+    // Each issuer releases the ring slots it reads (K: S issuer, V: PV issuer)
+    // and the S issuer releases Q after the last S of a pass.  Waits are
+    // bounded (PKV_DEV_TIMEOUT) and stop at an abort.
     if (lane == 0) {
-      const int x = warp - kMmaWarp;
+      const bool is_s = warp == kSWarp;
       constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kPrefillRows, kKeysPerTile, 0, 0);
       constexpr uint32_t kIdescO = tc::idesc_bf16_f32(kPrefillRows, D, 0, 1);
       auto wait = [&](int b, int parity) -> bool {
@@ -452,293 +479,291 @@ __global__ void __launch_bounds__(kThreads, 1)
         fail();
         return false;
       };
-      const uint32_t sq = smem_u32(smem + C::kOffQ + x * C::kQBytes);
-      int L0 = 0, nq = 0;  // ring index of the item's K_0; items (Q loads) done
-      int tx = 0;          // key tiles this sub-tile ran in earlier items
-      // S_x(j) = Q_x K_j^T once K_j landed and the previous P_x was consumed
-      auto issue_s = [&](int j) -> bool {
-        const int L = L0 + 2 * j, s = L % C::kSlots;
-        if (!wait(B_FULL + s, L / C::kSlots)) return false;
-        if (tx + j > 0 && !wait(B_O_DONE + x, tx + j - 1)) return false;
-        tc::fence_after_sync();
-        const uint32_t sk = smem_u32(smem + C::kOffRing + s * C::kSlotBytes);
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint64_t a =
-              tc::smem_desc_sw128(sq + (ks >> 2) * C::kQHalfBytes + (ks & 3) * 32, 16, 1024);
-          const uint64_t b =
-              tc::smem_desc_sw128(sk + (ks >> 2) * 1024 + (ks & 3) * 32, 16, C::kGroupStride);
-          tc::mma_bf16(t_s(x), a, b, kIdescS, ks > 0 ? 1u : 0u);
-        }
-        tc::commit(bar(B_S_FULL + x));
-        return true;
-      };
-      // O_x += P_x(j) V_j once P_x(j) is in TMEM and V_j landed
-      auto issue_pv = [&](int j) -> bool {
-        const int L = L0 + 2 * j + 1, s = L % C::kSlots;
-        if (!wait(B_P_FULL + x, tx + j)) return false;
-        if (!wait(B_FULL + s, L / C::kSlots)) return false;
-        tc::fence_after_sync();
-        const uint32_t sv = smem_u32(smem + C::kOffRing + s * C::kSlotBytes);
-#pragma unroll
-        for (int ks = 0; ks < kKeysPerTile / 16; ++ks) {
-          const uint64_t b = tc::smem_desc_sw128(sv + ks * C::kBlockBytes, 1024, C::kGroupStride);
-          tc::mma_bf16_ts(t_o(x), t_s(x) + ks * 8, b, kIdescO, (j > 0 || ks > 0) ? 1u : 0u);
-        }
-        tc::commit(bar(B_O_DONE + x));
-        return true;
-      };
-      // release ring load L (after its landing, so the arrival is for this use)
-      auto release = [&](int L) -> bool {
-        if (!wait(B_FULL + L % C::kSlots, L / C::kSlots)) return false;
-        tc::commit(bar(B_EMPTY + L % C::kSlots));
-        return true;
-      };
+      const uint32_t sq = smem_u32(smem + C::kOffQ);
+      int npass = 0, g = 0;  // passes; tiles
       bool good = true;
       for (int it = it0; it < it1 && good; ++it) {
         const ItemMeta m = load_item(p, it);
         if (!m.ok) continue;
-        const int ntx = x ? m.nt[1] : m.nt[0];
-        good = wait(B_Q_FULL, nq);
-        if (good && ntx > 0) good = issue_s(0);
-        if (good && ntx <= 1) tc::commit(bar(B_Q_EMPTY));  // every S of the item issued
-        if (good) good = release(L0);                       // K_0
-        for (int j = 0; good && j < m.nkt; ++j) {
-          if (j < ntx) {
-            good = issue_pv(j);
-            if (good && j + 1 < ntx) {
-              good = issue_s(j + 1);
-              if (good && j + 2 == ntx) tc::commit(bar(B_Q_EMPTY));
+        for (int x = 0; x < 2 && good; ++x) {
+          const int ntx = x ? m.nt[1] : m.nt[0];
+          if (ntx == 0) continue;
+          if (is_s) {
+            good = wait(B_Q_FULL, npass);
+            for (int j = 0; good && j < ntx; ++j, ++g) {
+              const int s = g % C::kSlots, b = g % kSBufs;
+              if (!wait(B_FULL + s, g / C::kSlots)) good = false;
+              else if (g >= kSBufs && !wait(B_FREE + b, g / kSBufs - 1)) good = false;
+              if (!good) break;
+              tc::fence_after_sync();
+              const uint32_t sk = smem_u32(smem + C::kOffRing + s * C::kSlotBytes);  // K ring
+#pragma unroll
+              for (int ks = 0; ks < D / 16; ++ks) {
+                const uint64_t a =
+                    tc::smem_desc_sw128(sq + (ks >> 2) * C::kQHalfBytes + (ks & 3) * 32, 16, 1024);
+                const uint64_t bd =
+                    tc::smem_desc_sw128(sk + (ks >> 2) * 1024 + (ks & 3) * 32, 16, C::kGroupStride);
+                tc::mma_bf16(t_s(b), a, bd, kIdescS, ks > 0 ? 1u : 0u);
+              }
+              tc::commit(bar(B_S_FULL + b));
+              tc::commit(bar(B_EMPTY + s));  // K_j
+            }
+            if (good) tc::commit(bar(B_Q_EMPTY));  // every S of the pass issued
+          } else {
+            for (int j = 0; good && j < ntx; ++j, ++g) {
+              const int s = g % C::kSlots, b = g % kSBufs;
+              if (!wait(B_P_FULL + b, g / kSBufs)) good = false;
+              else if (!wait(B_FULL + kMaxSlots + s, g / C::kSlots)) good = false;
+              if (!good) break;
+              tc::fence_after_sync();
+              const uint32_t sv = smem_u32(smem + C::kOffRing + (C::kSlots + s) * C::kSlotBytes);
+#pragma unroll
+              for (int ks = 0; ks < kKeysPerTile / 16; ++ks) {
+                const uint64_t bd =
+                    tc::smem_desc_sw128(sv + ks * C::kBlockBytes, 1024, C::kGroupStride);
+                tc::mma_bf16_ts(t_o, t_s(b) + ks * 8, bd, kIdescO, (j > 0 || ks > 0) ? 1u : 0u);
+              }
+              tc::commit(bar(B_FREE + b));
+              tc::commit(bar(B_EMPTY + kMaxSlots + s));  // V_j
             }
           }
-          if (good) good = release(L0 + 2 * j + 1);                        // V_j
-          if (good && j + 1 < m.nkt) good = release(L0 + 2 * j + 2);      // K_{j+1}
+          ++npass;
         }
-        L0 += 2 * m.nkt;
-        tx += ntx;
-        ++nq;
       }
       // every MMA issued so far completes before TMEM is released
-      tc::commit(bar(B_DRAIN + x));
-      mbar_wait(bar(B_DRAIN + x), 0);
+      const int d = is_s ? 0 : 1;
+      tc::commit(bar(B_DRAIN + d));
+      mbar_wait(bar(B_DRAIN + d), 0);
     }
-  } else {
-    // ======================================================== softmax (4 warps per sub-tile)
-    const int x = warp >> 2;              // sub-tile
-    const int quarter = warp & 3;         // TMEM lane quarter
+  } else if (warp < kSoftmaxWarps) {
+    // ======================================================== softmax (4 warps)
+    const int quarter = warp;             // TMEM lane quarter
     const int row = quarter * 32 + lane;  // query row = TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
-    const uint32_t ts = t_s(x) + lane_off, to = t_o(x) + lane_off;
-    int run0 = 0;  // key tiles this sub-tile ran in earlier items
+    const uint32_t to = t_o + lane_off;
+    int g = 0;  // tiles of earlier passes
     bool good = true;
     for (int it = it0; it < it1 && good; ++it) {
       const ItemMeta m = load_item(p, it);
-      // per-sub-tile fields by selects (no dynamically indexed local arrays)
-      const int n_q = x ? m.t.n_q[1] : m.t.n_q[0];
-      const int ntx = x ? m.nt[1] : m.nt[0];
-      if (!m.ok || ntx == 0) continue;
-      // last visible key of this row (gathered rows see every key of the item)
-      const int rows_x = m.gathered ? n_q * p.group : n_q;
-      const int lim = row >= rows_x ? -1
-                      : m.gathered  ? INT_MAX / 2
-                                    : m.ctx - m.qs + (x ? m.t.qi0[1] : m.t.qi0[0]) + row;
-      float m_used = -INFINITY, l = 0.f;
-      for (int j = 0; j < ntx; ++j) {
-        if (__any_sync(0xffffffffu, *abort_flag != 0)) {
-          good = false;
-          break;
+      if (!m.ok) continue;
+      for (int x = 0; x < 2 && good; ++x) {
+        // per-sub-tile fields by selects (no dynamically indexed local arrays)
+        const int n_q = x ? m.t.n_q[1] : m.t.n_q[0];
+        const int ntx = x ? m.nt[1] : m.nt[0];
+        if (ntx == 0) continue;
+        // last visible key of this row (gathered rows see every key of the item)
+        const int rows_x = m.gathered ? n_q * p.group : n_q;
+        const int lim = row >= rows_x ? -1
+                        : m.gathered  ? INT_MAX / 2
+                                      : m.ctx - m.qs + (x ? m.t.qi0[1] : m.t.qi0[0]) + row;
+        float m_used = -INFINITY, l = 0.f;
+        for (int j = 0; j < ntx; ++j, ++g) {
+          const int b = g % kSBufs;
+          const uint32_t ts = t_s(b) + lane_off;
+          if (__any_sync(0xffffffffu, *abort_flag != 0)) {
+            good = false;
+            break;
+          }
+          if (!__all_sync(0xffffffffu,
+                          mbar_wait(bar(B_S_FULL + b), (uint32_t)((g / kSBufs) & 1)))) {
+            fail();
+            good = false;
+            break;
+          }
+          tc::fence_after_sync();
+          const int rel = lim - (m.t.kt0 + j) * kKeysPerTile;  // keys k <= rel are visible
+          uint32_t sv[4][32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) tc::ld32(ts + 32 * c, sv[c]);
+          tc::wait_ld();
+          // scores in the log2 domain are sv * mult: a positive scale is applied
+          // in the exponent's FMA; a zero or negative one is applied here first
+          const float mult = sl2 > 0.f ? sl2 : 1.f;
+          if (!(sl2 > 0.f)) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+              for (int i = 0; i < 32; ++i) sv[c][i] = __float_as_uint(__uint_as_float(sv[c][i]) * sl2);
+          }
+          if (rel < kKeysPerTile - 1) {  // diagonal tile: invisible keys become -inf
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+              for (int i = 0; i < 32; ++i) sv[c][i] = 32 * c + i <= rel ? sv[c][i] : 0xff800000u;
+          }
+          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int c = 0; c < 4; ++c)  // two per instruction, four chains
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              m4[i & 3] = max3(m4[i & 3], __uint_as_float(sv[c][2 * i]),
+                               __uint_as_float(sv[c][2 * i + 1]));
+          const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * mult;
+          // lazy rescale of O (TMEM) and l when the max grew by more than 2^8 (O
+          // itself is rescaled below, once the scores are no longer live)
+          const bool need = m_used != -INFINITY && mt > m_used + kRescaleLog2;
+          const bool any_need = __any_sync(0xffffffffu, need);
+          const float alpha = need ? fast_exp2(m_used - mt) : 1.f;
+          if (need) {
+            l *= alpha;
+            m_used = mt;
+          }
+          if (m_used == -INFINITY) m_used = mt;  // first keys this row sees
+          const float nbase = m_used == -INFINITY ? 0.f : -m_used;
+          // p = 2^(sv * mult - m): 0 for masked keys (-inf); packed two per
+          // column over columns 0-63 of the S buffer
+          const uint64_t mx2 = f2_pack(mult, mult), nbx2 = f2_pack(nbase, nbase);
+          uint64_t acc[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int k0 = 32 * c + 2 * i;  // key index of the low element
+              float p0, p1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[k0 >> 5][k0 & 31]),
+                                       __uint_as_float(sv[k0 >> 5][(k0 & 31) + 1])),
+                               mx2, nbx2),
+                        p0, p1);
+              p0 = fast_exp2(p0);
+              p1 = fast_exp2(p1);
+              acc[i & 1] = f2_add(acc[i & 1], f2_pack(p0, p1));
+              pk[i] = pack_bf16x2(p0, p1);
+            }
+            tc::st16(ts + 16 * c, pk);
+          }
+          {
+            float a0, a1, b0, b1;
+            f2_unpack(acc[0], a0, a1);
+            f2_unpack(acc[1], b0, b1);
+            l += (a0 + a1) + (b0 + b1);
+          }
+          if (any_need) {
+            // O may be updated by O += P(g-1) V (j > 0 here: the first tile of a
+            // pass never rescales); wait for it, then scale O in TMEM
+            const int gp = g - 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(B_FREE + gp % kSBufs),
+                                                   (uint32_t)((gp / kSBufs) & 1)))) {
+              fail();
+              good = false;
+              break;
+            }
+            tc::fence_after_sync();
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t ov[32];
+              tc::ld32(to + 32 * c, ov);
+              tc::wait_ld();
+#pragma unroll
+              for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+              tc::st32(to + 32 * c, ov);
+            }
+          }
+          tc::wait_st();
+          tc::fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_P_FULL + b));
         }
+        if (!good) break;
+        // ---- epilogue: O / l, once the pass's last O += P V completed.  The
+        // next pass's first O += P V (which overwrites O) waits for this warp's
+        // next P, which comes after these TMEM reads.
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+        const int gl = g - 1;
         if (!__all_sync(0xffffffffu,
-                        mbar_wait(bar(B_S_FULL + x), (uint32_t)((run0 + j) & 1)))) {
+                        mbar_wait(bar(B_FREE + gl % kSBufs), (uint32_t)((gl / kSBufs) & 1)))) {
           fail();
-          good = false;
           break;
         }
         tc::fence_after_sync();
-        const int rel = lim - (m.t.kt0 + j) * kKeysPerTile;  // keys k <= rel are visible
-        uint32_t sv[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) tc::ld32(ts + 32 * c, sv[c]);
-        tc::wait_ld();
-        // scores in the log2 domain are sv * mult: a positive scale is applied in
-        // the exponent's FMA; a zero or negative one is applied here first
-        const float mult = sl2 > 0.f ? sl2 : 1.f;
-        if (!(sl2 > 0.f)) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int i = 0; i < 32; ++i) sv[c][i] = __float_as_uint(__uint_as_float(sv[c][i]) * sl2);
-        }
-        if (rel < kKeysPerTile - 1) {  // diagonal tile: invisible keys become -inf
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-#pragma unroll
-            for (int i = 0; i < 32; ++i) sv[c][i] = 32 * c + i <= rel ? sv[c][i] : 0xff800000u;
-        }
-        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-        for (int c = 0; c < 4; ++c)  // two per instruction, four chains
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            m4[i & 3] = max3(m4[i & 3], __uint_as_float(sv[c][2 * i]),
-                             __uint_as_float(sv[c][2 * i + 1]));
-        const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * mult;
-        // lazy rescale of O_x (TMEM) and l when the max grew by more than 2^8 (O_x
-        // itself is rescaled below, once the scores are no longer live)
-        const bool need = m_used != -INFINITY && mt > m_used + kRescaleLog2;
-        const bool any_need = __any_sync(0xffffffffu, need);
-        const float alpha = need ? fast_exp2(m_used - mt) : 1.f;
-        if (need) {
-          l *= alpha;
-          m_used = mt;
-        }
-        if (m_used == -INFINITY) m_used = mt;  // first keys this row sees
-        const float nbase = m_used == -INFINITY ? 0.f : -m_used;
-        // p = 2^(sv * mult - m): 0 for masked keys (-inf); packed two per column
-        // over S_x columns 0-63
-        const uint64_t mx2 = f2_pack(mult, mult), nbx2 = f2_pack(nbase, nbase);
-        uint64_t acc[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int k0 = 32 * c + 2 * i;  // key index of the low element
-            float p0, p1;
-            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[k0 >> 5][k0 & 31]),
-                                     __uint_as_float(sv[k0 >> 5][(k0 & 31) + 1])),
-                             mx2, nbx2),
-                      p0, p1);
-            p0 = fast_exp2(p0);
-            p1 = fast_exp2(p1);
-            acc[i & 1] = f2_add(acc[i & 1], f2_pack(p0, p1));
-            pk[i] = pack_bf16x2(p0, p1);
-          }
-          tc::st16(ts + 16 * c, pk);
-        }
+        int out_row, hq, part;  // re-read rather than kept live through the tile loop
+        float *prow = nullptr;  // partial destination of this row, if any
+        float2 *pml = nullptr;
         {
-          float a0, a1, b0, b1;
-          f2_unpack(acc[0], a0, a1);
-          f2_unpack(acc[1], b0, b1);
-          l += (a0 + a1) + (b0 + b1);
+          const ItemMeta me = load_item(p, it);
+          out_row = me.cu0 + (x ? me.t.qi0[1] : me.t.qi0[0]) + row;
+          hq = x ? me.t.hq[1] : me.t.hq[0];
+          part = x ? me.t.part[1] : me.t.part[0];
+          if (me.gathered) {
+            // row (t, g): the split-KV partial slot of token t's row group for
+            // this key chunk, at the row of head g
+            if (row < rows_x) {
+              const GatherRow gr = p.gather[(x ? me.t.gather[1] : me.t.gather[0]) + row / p.group];
+              const int slot = gr.part0 + part, srow = gr.row0 + row % p.group;
+              if (gr.part0 >= 0 && slot < p.num_dparts && srow >= 0 && srow < kRowsPerTile) {
+                prow = p.dpart_o + ((int64_t)slot * kRowsPerTile + srow) * D;
+                pml = p.dpart_ml + (int64_t)slot * kRowsPerTile + srow;
+              } else {
+                report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
+              }
+            }
+          } else if (part >= 0 && row < n_q) {
+            // keys of this sub-tile are split over several items: unnormalised O
+            // and (m, l) to its partial slot, combined by the merge kernel
+            prow = p.ppart_o + ((int64_t)part * kPrefillRows + row) * D;
+            pml = p.ppart_ml + (int64_t)part * kPrefillRows + row;
+          }
+          if (me.gathered) part = 0;  // never written out directly
         }
-        // O_x is idle here: its last update (P_x(j-1) V) completed before S_x(j)
-        // was issued, and the next one waits for this tile's P
-        if (any_need) {
+        if (part >= 0) {
+          // unnormalised O: each lane holds its row's 32-column chunk as 8 pieces
+          // of 16 bytes; transposed within groups of 8 lanes, one store covers
+          // 4 rows x 128 contiguous bytes rather than 32 rows x 16 bytes
+          const int gl8 = lane & 7, gbase = lane & ~7;
+          float *rows8[8];  // destination rows of this lane's group
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            rows8[k] = reinterpret_cast<float *>(
+                __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(prow), gbase + k));
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t ov[32];
             tc::ld32(to + 32 * c, ov);
             tc::wait_ld();
+            float4 pc[8];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
-            tc::st32(to + 32 * c, ov);
-          }
-        }
-        tc::wait_st();
-        tc::fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_P_FULL + x));
-      }
-      if (!good) break;
-      // ---- epilogue: O / l.  The next item's first O_x += P_x V waits for this
-      // warp's next P_x, which comes after these TMEM reads.
-      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-      if (!__all_sync(0xffffffffu,
-                      mbar_wait(bar(B_O_DONE + x), (uint32_t)((run0 + ntx - 1) & 1)))) {
-        fail();
-        break;
-      }
-      tc::fence_after_sync();
-      int out_row, hq, part;  // re-read rather than kept live through the tile loop
-      float *prow = nullptr;  // partial destination of this row, if any
-      float2 *pml = nullptr;
-      {
-        const ItemMeta me = load_item(p, it);
-        out_row = me.cu0 + (x ? me.t.qi0[1] : me.t.qi0[0]) + row;
-        hq = x ? me.t.hq[1] : me.t.hq[0];
-        part = x ? me.t.part[1] : me.t.part[0];
-        if (me.gathered) {
-          // row (t, g): the split-KV partial slot of token t's row group for
-          // this key chunk, at the row of head g
-          if (row < rows_x) {
-            const GatherRow gr = p.gather[(x ? me.t.gather[1] : me.t.gather[0]) + row / p.group];
-            const int slot = gr.part0 + part, srow = gr.row0 + row % p.group;
-            if (gr.part0 >= 0 && slot < p.num_dparts && srow >= 0 && srow < kRowsPerTile) {
-              prow = p.dpart_o + ((int64_t)slot * kRowsPerTile + srow) * D;
-              pml = p.dpart_ml + (int64_t)slot * kRowsPerTile + srow;
-            } else {
-              report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
-            }
-          }
-        } else if (part >= 0 && row < n_q) {
-          // keys of this sub-tile are split over several items: unnormalised O
-          // and (m, l) to its partial slot, combined by the merge kernel
-          prow = p.ppart_o + ((int64_t)part * kPrefillRows + row) * D;
-          pml = p.ppart_ml + (int64_t)part * kPrefillRows + row;
-        }
-        if (me.gathered) part = 0;  // never written out directly
-      }
-      if (part >= 0) {
-        // unnormalised O: each lane holds its row's 32-column chunk as 8 pieces
-        // of 16 bytes; transposed within groups of 8 lanes, one store covers
-        // 4 rows x 128 contiguous bytes rather than 32 rows x 16 bytes
-        const int gl = lane & 7, gbase = lane & ~7;
-        float *rows8[8];  // destination rows of this lane's group
+            for (int v4 = 0; v4 < 8; ++v4)
+              pc[v4] = make_float4(__uint_as_float(ov[4 * v4]), __uint_as_float(ov[4 * v4 + 1]),
+                                   __uint_as_float(ov[4 * v4 + 2]), __uint_as_float(ov[4 * v4 + 3]));
+            transpose8x8(pc, gl8);
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          rows8[k] = reinterpret_cast<float *>(
-              __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(prow), gbase + k));
+            for (int k = 0; k < 8; ++k)
+              if (rows8[k]) reinterpret_cast<float4 *>(rows8[k] + 32 * c)[gl8] = pc[k];
+          }
+          if (pml) *pml = make_float2(m_used, l);
+          tc::fence_before_sync();
+          continue;
+        }
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        __nv_bfloat16 *orow = p.out + ((int64_t)out_row * p.num_q_heads + hq) * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t ov[32];
           tc::ld32(to + 32 * c, ov);
           tc::wait_ld();
-          float4 pc[8];
+          if (row < n_q) {
+            uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
 #pragma unroll
-          for (int v4 = 0; v4 < 8; ++v4)
-            pc[v4] = make_float4(__uint_as_float(ov[4 * v4]), __uint_as_float(ov[4 * v4 + 1]),
-                                 __uint_as_float(ov[4 * v4 + 2]), __uint_as_float(ov[4 * v4 + 3]));
-          transpose8x8(pc, gl);
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            if (rows8[k]) reinterpret_cast<float4 *>(rows8[k] + 32 * c)[gl] = pc[k];
-        }
-        if (pml) *pml = make_float2(m_used, l);
-        tc::fence_before_sync();
-        run0 += ntx;
-        continue;
-      }
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16 *orow = p.out + ((int64_t)out_row * p.num_q_heads + hq) * D;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t ov[32];
-        tc::ld32(to + 32 * c, ov);
-        tc::wait_ld();
-        if (row < n_q) {
-          uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
-#pragma unroll
-          for (int v4 = 0; v4 < 4; ++v4) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(ov[8 * v4 + 0]) * inv, __uint_as_float(ov[8 * v4 + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(ov[8 * v4 + 2]) * inv, __uint_as_float(ov[8 * v4 + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(ov[8 * v4 + 4]) * inv, __uint_as_float(ov[8 * v4 + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(ov[8 * v4 + 6]) * inv, __uint_as_float(ov[8 * v4 + 7]) * inv);
-            dst[v4] = w;
+            for (int v4 = 0; v4 < 4; ++v4) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(ov[8 * v4 + 0]) * inv, __uint_as_float(ov[8 * v4 + 1]) * inv);
+              w.y = pack_bf16x2(__uint_as_float(ov[8 * v4 + 2]) * inv, __uint_as_float(ov[8 * v4 + 3]) * inv);
+              w.z = pack_bf16x2(__uint_as_float(ov[8 * v4 + 4]) * inv, __uint_as_float(ov[8 * v4 + 5]) * inv);
+              w.w = pack_bf16x2(__uint_as_float(ov[8 * v4 + 6]) * inv, __uint_as_float(ov[8 * v4 + 7]) * inv);
+              dst[v4] = w;
+            }
           }
         }
+        tc::fence_before_sync();
       }
-      tc::fence_before_sync();
-      run0 += ntx;
     }
   }
 
   // ---- teardown: every role has drained its own asynchronous work
   tc::fence_before_sync();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kSWarp) {
     tc::fence_after_sync();
     tc::dealloc(tmem, kTmemCols);
   }
