@@ -54,11 +54,11 @@ constexpr int kMinBlocksPerWarp = 4;
 // (default 64; the environment variable PKV_PREFILL_MIN_Q overrides it, 0 or
 // a negative value keeps every row on the split-KV kernel).
 constexpr int kPrefillMinQDefault = 64;
-// Relative costs used to give the persistent prefill CTAs equal work: a key
-// tile both sub-tiles of a pair run (their MMAs and softmaxes overlap), a key
-// tile only one sub-tile runs, and starting a work item (Q load, pipeline fill,
-// epilogue).
-constexpr int64_t kPairTileCost = 10, kSingleTileCost = 8, kItemStartCost = 10;
+// Relative costs used to give the persistent prefill CTAs equal work: a CTA
+// runs a work item's sub-tiles one after the other, each a pass over its key
+// tiles, so a pair costs the sum of its sub-tiles' passes: a key tile of one
+// sub-tile, and starting a pass (Q load, pipeline fill, epilogue).
+constexpr int64_t kTileCost = 8, kPassStartCost = 10;
 // CTAs get at least this many key tiles of work.
 constexpr int64_t kMinTilesPerCta = 4;
 
@@ -591,19 +591,19 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   if (!pairs.empty() || !casc_items.empty()) {
     auto pair_cost = [&](size_t pi) {
       const int64_t nt0 = pair_nt[pi][0], nt1 = pair_nt[pi][1];
-      return kItemStartCost + kPairTileCost * nt1 + kSingleTileCost * (nt0 - nt1);
+      return kPassStartCost * (nt1 > 0 ? 2 : 1) + kTileCost * (nt0 + nt1);
     };
     auto item_cost = [&](const PrefillTile &t) {
-      return kItemStartCost + (t.n_q[1] > 0 ? kPairTileCost : kSingleTileCost) * (t.kt1 - t.kt0);
+      return (kPassStartCost + kTileCost * (t.kt1 - t.kt0)) * (t.n_q[1] > 0 ? 2 : 1);
     };
     int64_t total = 0, ntiles = 0;
     for (size_t pi = 0; pi < pairs.size(); ++pi) {
       total += pair_cost(pi);
-      ntiles += pair_nt[pi][0];
+      ntiles += pair_nt[pi][0] + pair_nt[pi][1];
     }
     for (const PrefillTile &t : casc_items) {
       total += item_cost(t);
-      ntiles += t.kt1 - t.kt0;
+      ntiles += (t.kt1 - t.kt0) * (t.n_q[1] > 0 ? 2 : 1);
     }
     n_pf_ctas = (int32_t)std::max<int64_t>(
         1, std::min<int64_t>(num_sms, std::max<int64_t>(ntiles / kMinTilesPerCta,
@@ -654,7 +654,7 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
       for (int x = 0; x < 2; ++x)
         if (pair_nt[pi][x] > 0) {
           subs.push_back({pi, x});
-          rest += kItemStartCost + kSingleTileCost * pair_nt[pi][x];
+          rest += kPassStartCost + kTileCost * pair_nt[pi][x];
         }
     if (!subs.empty()) {
       std::vector<int64_t> room(n_pf_ctas), room_end(n_pf_ctas);
@@ -675,12 +675,12 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
       for (const Sub &u : subs) {
         const PrefillTile &src = pairs[u.pi];
         const int32_t nt = pair_nt[u.pi][u.x];
-        cost += kItemStartCost;
+        cost += kPassStartCost;
         std::vector<std::array<int32_t, 3>> pcs;  // (cta, j0, j1)
         for (int32_t j = 0; j < nt; ++j) {
-          const int64_t mid = cost + kSingleTileCost / 2;
+          const int64_t mid = cost + kTileCost / 2;
           while (cta < n_pf_ctas - 1 && mid >= room_end[cta]) ++cta;
-          cost += kSingleTileCost;
+          cost += kTileCost;
           if (pcs.empty() || pcs.back()[0] != cta)
             pcs.push_back({cta, j, j + 1});
           else
@@ -717,6 +717,12 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
         }
       }
     }
+    // CTAs the assignment left without work are dropped (a CTA always has at
+    // least one item)
+    per_cta.erase(std::remove_if(per_cta.begin(), per_cta.end(),
+                                 [](const std::vector<PrefillTile> &v) { return v.empty(); }),
+                  per_cta.end());
+    n_pf_ctas = (int32_t)per_cta.size();
     pf_begin.assign(n_pf_ctas + 1, 0);
     for (int32_t b = 0; b < n_pf_ctas; ++b) {
       pf_begin[b] = (int32_t)ptiles.size();

@@ -69,7 +69,7 @@ def parse_plan(info, host):
     parse_plan.shared = words[off_s:off_b].reshape(2 * nsh, 24)
     pb = words[off_b:off_b + ncta + 1] if ncta else np.zeros(1, np.int32)
     if ncta:
-        assert pb[0] == 0 and pb[-1] == npf and np.all(np.diff(pb) >= 0)
+        assert pb[0] == 0 and pb[-1] == npf and np.all(np.diff(pb) >= 1)   # no CTA without work
     return hdr, wb, pieces, mer, pre
 
 
