@@ -20,15 +20,17 @@
 // sees), and each row's unnormalised result goes to the split-KV kernel's
 // partial slot of its row group, where the merge combines it with the rest of
 // that row group's keys.
-// Seven warps with fixed roles:
-//   warp 4     TMA producer: the pass's Q sub-tile (3-D tensor map over
-//              [total_q][Hq][D]) and, per 128-key tile, K into a ring of K slots
-//              and V into a ring of V slots, K one tile ahead of V.  One 4-D TMA
-//              box is one paged block of one KV head (16 rows x D, both
-//              64-column halves), issued by lanes 0-7 in parallel; blocks past
-//              the context are read out of bounds, i.e. zero-filled without
-//              memory traffic.  Block-table entries are read 32 at a time (four
-//              tiles), one group ahead.
+// Eight warps with fixed roles:
+//   warp 4     TMA producer of the pass's Q sub-tile (3-D tensor map over
+//              [total_q][Hq][D]) and, per 128-key tile, of K into a ring of K
+//              slots;
+//   warp 7     TMA producer of V into a ring of V slots.  The two walk the same
+//              tiles independently, so neither ring's slot waits hold up the
+//              other's copies.  One 4-D TMA box is one paged block of one KV
+//              head (16 rows x D, both 64-column halves), issued by lanes 0-7
+//              in parallel; blocks past the context are read out of bounds,
+//              i.e. zero-filled without memory traffic.  Block-table entries
+//              are read 32 at a time (four tiles), one group ahead.
 //   warp 5     allocates 512 TMEM columns; one thread issues S(j) = Q K_j^T
 //              (M=128, N=128 keys, K=D; A and B from smem) into S buffer j % 3.
 //   warp 6     one thread issues O += P(j) V_j (M=128, N=D, K=128 keys; A = P
@@ -64,10 +66,11 @@ namespace {
 constexpr int kKeysPerTile = 128;
 constexpr int kBlocksPerTile = kKeysPerTile / kBlockSize;
 constexpr int kSoftmaxWarps = 4;
-constexpr int kProducerWarp = 4;
+constexpr int kProducerWarp = 4;   // K tiles and the pass's Q
+constexpr int kVProducerWarp = 7;  // V tiles
 constexpr int kSWarp = 5;   // issues the S MMAs; owns the TMEM allocation
 constexpr int kPvWarp = 6;  // issues the PV MMAs
-constexpr int kThreads = 224;
+constexpr int kThreads = 256;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kSBufs = 3;
 constexpr float kRescaleLog2 = 8.0f;
@@ -287,30 +290,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 1;
   };
 
-  if (warp == kProducerWarp) {
-    // ======================================================== TMA producer (whole warp)
-    if (lane == 0) {
-      prefetch_tmap(&q_map);
-      prefetch_tmap(&qg_map);
-      prefetch_tmap(&qr_map);
-      prefetch_tmap(&kv_map);
-    }
-    // Ring r (0: K, 1: V) load n_r (counted over the CTA's passes) sits in slot
-    // n_r % kSlots.  Per pass the loads go K_0, then K_{j+1}, V_j for each tile
-    // j, so a wait for a V slot (its O += P V) never holds up the K that the S
-    // MMAs need next.  Lane b < 8 issues paged block b of every tile; the
+  if (warp == kProducerWarp || warp == kVProducerWarp) {
+    // ======================================================== TMA producers (whole warps)
+    // Two warps, one per ring (r = 0: K and the pass's Q; r = 1: V), each
+    // walking every pass's key tiles on its own, so a K copy never waits for a
+    // V slot (released only by O += P V, well behind the S MMAs) nor a V copy
+    // for a K slot.  Load n of ring r (counted over the CTA's passes) sits in
+    // slot n % kSlots.  Lane b < 8 issues paged block b of every tile; the
     // table entries of four tiles come with one coalesced read by the whole
     // warp, the next four read while the current ones are used.  The Q
     // sub-tile of a pass waits until every S MMA of the previous pass has read
-    // its Q (B_Q_EMPTY).
+    // its Q (B_Q_EMPTY).  Only the K warp reports bad items and blocks.
+    const int r = warp == kVProducerWarp ? 1 : 0;
+    if (lane == 0) {
+      if (r == 0) {
+        prefetch_tmap(&q_map);
+        prefetch_tmap(&qg_map);
+        prefetch_tmap(&qr_map);
+      }
+      prefetch_tmap(&kv_map);
+    }
     const int hkv = p.num_kv_heads;
-    int nld[2] = {0, 0};  // loads issued per ring
-    int npass = 0;        // passes (Q loads) issued
+    int nld = 0;    // loads issued into this warp's ring
+    int npass = 0;  // passes (Q loads) issued
     bool good = true, waited = false;
-    // one K (r = 0) or V (r = 1) tile of KV head h into ring r; lane b < 8
-    // copies paged block `phys` (-1 or out of range: zero fill)
-    auto load_tile = [&](int r, int h, int phys) -> bool {
-      const int n = nld[r], s = n % C::kSlots;
+    // one tile of KV head h into ring r; lane b < 8 copies paged block `phys`
+    // (-1 or out of range: zero fill)
+    auto load_tile = [&](int h, int phys) -> bool {
+      const int n = nld, s = n % C::kSlots;
       if (n >= C::kSlots &&
           !__all_sync(0xffffffffu, mbar_wait(bar(B_EMPTY + r * kMaxSlots + s),
                                              (uint32_t)(((n / C::kSlots) - 1) & 1)))) {
@@ -326,13 +333,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         lane * C::kBlockBytes,
                     &kv_map, 0, 0, 0, g, bar(B_FULL + r * kMaxSlots + s));
       }
-      ++nld[r];
+      ++nld;
       return true;
     };
     for (int it = it0; it < it1 && good; ++it) {
       const ItemMeta m = load_item(p, it);
       if (!m.ok) {
-        if (lane == 0) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
+        if (lane == 0 && r == 0) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
         continue;
       }
       const int32_t *table = p.block_tables + (int64_t)m.t.seq * p.max_blocks_per_seq;
@@ -352,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         int ent_cur = read_group(0), ent_next = read_group(1);  // land while q is loaded
-        if (npass > 0 &&
+        if (r == 0 && npass > 0 &&
             !__all_sync(0xffffffffu, mbar_wait(bar(B_Q_EMPTY), (uint32_t)((npass - 1) & 1)))) {
           if (lane == 0) fail();
           good = false;
@@ -360,7 +367,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const uint32_t sq = smem_u32(smem + C::kOffQ);
         const int qi0 = x ? m.t.qi0[1] : m.t.qi0[0];
-        if (!m.gathered) {
+        if (r == 1) {
+          // V warp: no Q
+        } else if (!m.gathered) {
           if (lane == 0) {
             mbar_arrive_expect_tx(bar(B_Q_FULL), C::kQBytes);
 #pragma unroll
@@ -417,7 +426,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // the physical block of this lane (< 8) in relative tile j: checked once
         // per tile; ids past the context (-1) are zero-filled
-        int phys_k = -1, phys_v = -1;  // of the next K tile to load / the next V
         auto tile_phys = [&](int j) -> int {
           if ((j % kTablePrefetchTiles) == 0 && j > 0) {
             ent_cur = ent_next;
@@ -426,24 +434,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int e = __shfl_sync(0xffffffffu, ent_cur,
                                     (j % kTablePrefetchTiles) * kBlocksPerTile + (lane & 7));
           const int kb = (m.t.kt0 + j) * kBlocksPerTile + lane;
-          if (lane < kBlocksPerTile && ((e != -1 && (e < 0 || e >= p.num_blocks)) ||
+          if (r == 0 && lane < kBlocksPerTile && ((e != -1 && (e < 0 || e >= p.num_blocks)) ||
                                         (e == -1 && kb < nblk)))
             report(p.dev_status, PKV_DEV_BAD_BLOCK);
           return lane < kBlocksPerTile ? e : -1;
         };
-        phys_k = tile_phys(0);
-        good = load_tile(0, m.t.h, phys_k);
         for (int j = 0; good && j < ntx; ++j) {
           if (__any_sync(0xffffffffu, *abort_flag != 0)) {
             good = false;
             break;
           }
-          phys_v = phys_k;
-          if (j + 1 < ntx) {
-            phys_k = tile_phys(j + 1);
-            good = load_tile(0, m.t.h, phys_k);
-          }
-          if (good) good = load_tile(1, m.t.h, phys_v);
+          good = load_tile(m.t.h, tile_phys(j));
         }
       }
     }
@@ -453,10 +454,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // our copies still in flight land before the CTA can exit: only the last
     // load of each slot can be pending (a slot is refilled after it was consumed)
     if (lane == 0) {
-      for (int r = 0; r < 2; ++r)
-        for (int l = max(0, nld[r] - C::kSlots); l < nld[r]; ++l)
-          mbar_wait(bar(B_FULL + r * kMaxSlots + l % C::kSlots), (uint32_t)((l / C::kSlots) & 1));
-      if (npass > 0) mbar_wait(bar(B_Q_FULL), (uint32_t)((npass - 1) & 1));
+      for (int l = max(0, nld - C::kSlots); l < nld; ++l)
+        mbar_wait(bar(B_FULL + r * kMaxSlots + l % C::kSlots), (uint32_t)((l / C::kSlots) & 1));
+      if (r == 0 && npass > 0) mbar_wait(bar(B_Q_FULL), (uint32_t)((npass - 1) & 1));
     }
   } else if (warp == kSWarp || warp == kPvWarp) {
     // ======================================================== MMA issuers
