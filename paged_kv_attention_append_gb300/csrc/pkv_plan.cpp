@@ -58,7 +58,7 @@ constexpr int kPrefillMinQDefault = 64;
 // runs a work item's sub-tiles one after the other, each a pass over its key
 // tiles, so a pair costs the sum of its sub-tiles' passes: a key tile of one
 // sub-tile, and starting a pass (Q load, pipeline fill, epilogue).
-constexpr int64_t kTileCost = 8, kPassStartCost = 10;
+constexpr int64_t kTileCost = 8, kPassStartCost = 24;
 // CTAs get at least this many key tiles of work.
 constexpr int64_t kMinTilesPerCta = 4;
 

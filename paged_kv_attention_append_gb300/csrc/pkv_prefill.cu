@@ -668,16 +668,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!good) break;
         // ---- epilogue: O / l, once the pass's last O += P V completed.  The
         // next pass's first O += P V (which overwrites O) waits for this warp's
-        // next P, which comes after these TMEM reads.
+        // next P, which comes after these TMEM reads.  The row's destination is
+        // re-read (rather than kept live through the tile loop) while that last
+        // O += P V runs.
         if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-        const int gl = g - 1;
-        if (!__all_sync(0xffffffffu,
-                        mbar_wait(bar(B_FREE + gl % kSBufs), (uint32_t)((gl / kSBufs) & 1)))) {
-          fail();
-          break;
-        }
-        tc::fence_after_sync();
-        int out_row, hq, part;  // re-read rather than kept live through the tile loop
+        int out_row, hq, part;
         float *prow = nullptr;  // partial destination of this row, if any
         float2 *pml = nullptr;
         {
@@ -706,6 +701,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (me.gathered) part = 0;  // never written out directly
         }
+        const int gl = g - 1;
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(bar(B_FREE + gl % kSBufs), (uint32_t)((gl / kSBufs) & 1)))) {
+          fail();
+          break;
+        }
+        tc::fence_after_sync();
+        // the row's whole O in one round trip
+        uint32_t ov[D / 32][32];
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) tc::ld32(to + 32 * c, ov[c]);
+        tc::wait_ld();
         if (part >= 0) {
           // unnormalised O: each lane holds its row's 32-column chunk as 8 pieces
           // of 16 bytes; transposed within groups of 8 lanes, one store covers
@@ -718,14 +725,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __shfl_sync(0xffffffffu, reinterpret_cast<uintptr_t>(prow), gbase + k));
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
-            uint32_t ov[32];
-            tc::ld32(to + 32 * c, ov);
-            tc::wait_ld();
             float4 pc[8];
 #pragma unroll
             for (int v4 = 0; v4 < 8; ++v4)
-              pc[v4] = make_float4(__uint_as_float(ov[4 * v4]), __uint_as_float(ov[4 * v4 + 1]),
-                                   __uint_as_float(ov[4 * v4 + 2]), __uint_as_float(ov[4 * v4 + 3]));
+              pc[v4] = make_float4(__uint_as_float(ov[c][4 * v4]), __uint_as_float(ov[c][4 * v4 + 1]),
+                                   __uint_as_float(ov[c][4 * v4 + 2]), __uint_as_float(ov[c][4 * v4 + 3]));
             transpose8x8(pc, gl8);
 #pragma unroll
             for (int k = 0; k < 8; ++k)
@@ -739,18 +743,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         __nv_bfloat16 *orow = p.out + ((int64_t)out_row * p.num_q_heads + hq) * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
-          uint32_t ov[32];
-          tc::ld32(to + 32 * c, ov);
-          tc::wait_ld();
           if (row < n_q) {
             uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
 #pragma unroll
             for (int v4 = 0; v4 < 4; ++v4) {
               uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(ov[8 * v4 + 0]) * inv, __uint_as_float(ov[8 * v4 + 1]) * inv);
-              w.y = pack_bf16x2(__uint_as_float(ov[8 * v4 + 2]) * inv, __uint_as_float(ov[8 * v4 + 3]) * inv);
-              w.z = pack_bf16x2(__uint_as_float(ov[8 * v4 + 4]) * inv, __uint_as_float(ov[8 * v4 + 5]) * inv);
-              w.w = pack_bf16x2(__uint_as_float(ov[8 * v4 + 6]) * inv, __uint_as_float(ov[8 * v4 + 7]) * inv);
+              w.x = pack_bf16x2(__uint_as_float(ov[c][8 * v4 + 0]) * inv, __uint_as_float(ov[c][8 * v4 + 1]) * inv);
+              w.y = pack_bf16x2(__uint_as_float(ov[c][8 * v4 + 2]) * inv, __uint_as_float(ov[c][8 * v4 + 3]) * inv);
+              w.z = pack_bf16x2(__uint_as_float(ov[c][8 * v4 + 4]) * inv, __uint_as_float(ov[c][8 * v4 + 5]) * inv);
+              w.w = pack_bf16x2(__uint_as_float(ov[c][8 * v4 + 6]) * inv, __uint_as_float(ov[c][8 * v4 + 7]) * inv);
               dst[v4] = w;
             }
           }
