@@ -41,6 +41,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <map>
+#include <queue>
 #include <vector>
 
 #include "pkv_internal.h"
@@ -614,7 +615,14 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
     std::stable_sort(order.begin(), order.end(),
                      [&](size_t x, size_t y) { return pair_cost(x) > pair_cost(y); });
     std::vector<int64_t> load(n_pf_ctas, 0);
-    std::vector<std::vector<PrefillTile>> per_cta(n_pf_ctas);
+    // (CTA, item) in assignment order; grouped by CTA at the end
+    std::vector<std::pair<int32_t, PrefillTile>> assigned;
+    assigned.reserve(casc_items.size() + 2 * pairs.size());
+    // least-loaded CTA first (lowest index among equals): a min-heap of (load, CTA)
+    std::priority_queue<std::pair<int64_t, int32_t>, std::vector<std::pair<int64_t, int32_t>>,
+                        std::greater<std::pair<int64_t, int32_t>>>
+        least;
+    for (int32_t b = 0; b < n_pf_ctas; ++b) least.push({0, b});
     {
       std::vector<size_t> corder(casc_items.size());
       for (size_t i = 0; i < corder.size(); ++i) corder[i] = i;
@@ -622,26 +630,31 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
         return item_cost(casc_items[x]) > item_cost(casc_items[y]);
       });
       for (size_t ci : corder) {
-        const int32_t best = (int32_t)(std::min_element(load.begin(), load.end()) - load.begin());
+        const int32_t best = least.top().second;
+        least.pop();
         load[best] += item_cost(casc_items[ci]);
-        per_cta[best].push_back(casc_items[ci]);
+        least.push({load[best], best});
+        assigned.push_back({best, casc_items[ci]});
       }
     }
     std::vector<size_t> leftover;
     for (size_t pi : order) {
-      int32_t best = -1;
-      for (int32_t b = 0; b < n_pf_ctas; ++b)
-        if (load[b] + pair_cost(pi) <= target && (best < 0 || load[b] < load[best])) best = b;
-      if (best < 0) {
+      // the least-loaded CTA takes the pair if it stays within the target (then
+      // no CTA can)
+      const int64_t pc = pair_cost(pi);
+      const int32_t best = least.top().second;
+      if (load[best] + pc > target) {
         leftover.push_back(pi);
         continue;
       }
-      load[best] += pair_cost(pi);
+      least.pop();
+      load[best] += pc;
+      least.push({load[best], best});
       PrefillTile t = pairs[pi];
       t.kt0 = 0;
       t.kt1 = pair_nt[pi][0];
       t.part[0] = t.part[1] = -1;
-      per_cta[best].push_back(t);
+      assigned.push_back({best, t});
     }
     // leftover sub-tiles, cut at the remaining capacities (CTA order)
     struct Sub {
@@ -672,11 +685,12 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
       }
       int64_t cost = 0;
       int32_t cta = 0;
+      std::vector<std::array<int32_t, 3>> pcs;  // (cta, j0, j1) of one sub-tile
       for (const Sub &u : subs) {
         const PrefillTile &src = pairs[u.pi];
         const int32_t nt = pair_nt[u.pi][u.x];
         cost += kPassStartCost;
-        std::vector<std::array<int32_t, 3>> pcs;  // (cta, j0, j1)
+        pcs.clear();
         for (int32_t j = 0; j < nt; ++j) {
           const int64_t mid = cost + kTileCost / 2;
           while (cta < n_pf_ctas - 1 && mid >= room_end[cta]) ++cta;
@@ -713,22 +727,29 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
           t.kt1 = pcs[k][2];
           t.part[0] = part0 >= 0 ? part0 + (int32_t)k : -1;
           t.part[1] = -1;
-          per_cta[pcs[k][0]].push_back(t);
+          assigned.push_back({pcs[k][0], t});
         }
       }
     }
     // CTAs the assignment left without work are dropped (a CTA always has at
     // least one item)
-    per_cta.erase(std::remove_if(per_cta.begin(), per_cta.end(),
-                                 [](const std::vector<PrefillTile> &v) { return v.empty(); }),
-                  per_cta.end());
-    n_pf_ctas = (int32_t)per_cta.size();
-    pf_begin.assign(n_pf_ctas + 1, 0);
+    std::vector<int32_t> slot(n_pf_ctas + 1, 0);  // items per CTA, then each kept CTA's first slot
+    for (const auto &a : assigned) ++slot[a.first];
+    int32_t kept = 0, at = 0;
+    pf_begin.clear();
     for (int32_t b = 0; b < n_pf_ctas; ++b) {
-      pf_begin[b] = (int32_t)ptiles.size();
-      for (const PrefillTile &t : per_cta[b]) ptiles.push_back(t);
+      const int32_t cnt = slot[b];
+      slot[b] = at;
+      if (cnt > 0) {
+        pf_begin.push_back(at);
+        ++kept;
+      }
+      at += cnt;
     }
-    pf_begin[n_pf_ctas] = (int32_t)ptiles.size();
+    pf_begin.push_back(at);
+    n_pf_ctas = kept;
+    ptiles.resize(assigned.size());
+    for (const auto &a : assigned) ptiles[slot[a.first]++] = a.second;  // stable within a CTA
   }
   for (const MergeGroup &m : pmerges) merges.push_back(m);  // after the decode groups
 
