@@ -70,6 +70,8 @@ def library_path() -> str:
 
 def _load():
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is None:
             if not os.path.exists(_LIB_PATH):
@@ -133,19 +135,30 @@ def set_profile_events(kernel: str, start=None, stop=None):
         raise PkvError(st, "pkv_set_profile_events")
 
 
+# The per-call wrappers below sit on the host side of every step, so they keep
+# Python work small: pointers go to ctypes as plain ints (the prototypes say
+# void*), the current stream comes from torch's raw-stream query, and a pool's
+# descriptor is built once per pool shape.
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
-def _stream(stream, device):
-    s = torch.cuda.current_stream(device) if stream is None else stream
-    return ctypes.c_void_p(s.cuda_stream)
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream, t):
+    """Raw handle of `stream`, else of the current stream of tensor t's device."""
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        return _raw_stream(t.get_device())
+    return torch.cuda.current_stream(t.device).cuda_stream
 
 
 def _check_cuda(name, t, dtype, ndim=None):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.device.type != "cuda":
+    if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
@@ -155,11 +168,21 @@ def _check_cuda(name, t, dtype, ndim=None):
         raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
 
 
+_desc_cache: dict = {}
+
+
 def pool_desc(kv_pool: torch.Tensor) -> PoolDesc:
-    if kv_pool.dim() != 5 or kv_pool.shape[1] != 2:
+    shape = kv_pool.shape
+    d = _desc_cache.get(shape)
+    if d is not None:
+        return d
+    if len(shape) != 5 or shape[1] != 2:
         raise ValueError("kv_pool must be [num_blocks, 2, num_kv_heads, block_size, head_dim]")
-    nb, _, hkv, bs, d = kv_pool.shape
-    return PoolDesc(nb, bs, hkv, d)
+    nb, _, hkv, bs, hd = shape
+    d = PoolDesc(nb, bs, hkv, hd)
+    if len(_desc_cache) < 64:
+        _desc_cache[shape] = d
+    return d
 
 
 def paged_kv_append(k, v, slot_mapping, kv_pool, *, dev_status=None, stream=None):
@@ -179,7 +202,7 @@ def paged_kv_append(k, v, slot_mapping, kv_pool, *, dev_status=None, stream=None
         _check_cuda("dev_status", dev_status, torch.int32)
     st = _load().pkv_paged_kv_append(_ptr(k), _ptr(v), _ptr(slot_mapping), n, _ptr(kv_pool),
                                      ctypes.byref(desc), _ptr(dev_status),
-                                     _stream(stream, kv_pool.device))
+                                     _stream(stream, kv_pool))
     if st:
         raise PkvError(st, "pkv_paged_kv_append")
 
@@ -206,7 +229,7 @@ def state_checkpoint(src, dst_slots, pool, *, dev_status=None, stream=None):
         _check_cuda("dev_status", dev_status, torch.int32)
     st = _load().pkv_state_checkpoint(_ptr(src), _ptr(dst_slots), n, _ptr(pool), pool.shape[0],
                                       max(row_bytes, 16), _ptr(dev_status),
-                                      _stream(stream, pool.device))
+                                      _stream(stream, pool))
     if st:
         raise PkvError(st, "pkv_state_checkpoint")
 
@@ -336,13 +359,13 @@ def decode_advance(context_lens, slot_mapping, cu_q_lens, block_tables, kv_pool,
     st = _load().pkv_decode_advance(_ptr(context_lens), _ptr(slot_mapping), _ptr(cu_q_lens),
                                     _ptr(block_tables), block_tables.shape[1], n,
                                     ctypes.byref(desc), _ptr(dev_status),
-                                    _stream(stream, context_lens.device))
+                                    _stream(stream, context_lens))
     if st:
         raise PkvError(st, "pkv_decode_advance")
 
 
 def _dev_i32(x, device, name):
-    if isinstance(x, torch.Tensor) and x.device.type == "cuda":
+    if isinstance(x, torch.Tensor) and x.is_cuda:
         _check_cuda(name, x, torch.int32)
         return x
     return torch.from_numpy(_host_i32(x)).to(device)
@@ -382,7 +405,7 @@ def paged_varlen_attention(q, cu_q_lens, context_lens, block_tables, kv_pool, sc
     st = _load().pkv_paged_varlen_attention(
         _ptr(q), _ptr(cu_d), _ptr(ctx_d), _ptr(bt_d), bt_d.shape[1], _ptr(kv_pool),
         ctypes.byref(desc), float(scale), ctypes.byref(info), _ptr(plan.dev), _ptr(out), _ptr(ws),
-        0 if ws is None else ws.numel(), _ptr(dev_status), _stream(stream, dev))
+        0 if ws is None else ws.numel(), _ptr(dev_status), _stream(stream, q))
     if st:
         raise PkvError(st, "pkv_paged_varlen_attention")
     return out
