@@ -592,46 +592,71 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int i = 0; i < 32; ++i) sv[c][i] = 32 * c + i <= rel ? sv[c][i] : 0xff800000u;
           }
-          float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          // p = 2^(sv * mult - m): 0 for masked keys (-inf); packed two per
+          // column over columns 0-63 of the S buffer, summed into acc.  With
+          // track, the row max of the raw scores comes out of the same pass.
+          const uint64_t mx2 = f2_pack(mult, mult);
+          uint64_t acc[2];
+          float m4[4];
+          auto exp_pass = [&](float nbase, bool track) {
+            const uint64_t nbx2 = f2_pack(nbase, nbase);
+            acc[0] = acc[1] = f2_pack(0.f, 0.f);
+            m4[0] = m4[1] = m4[2] = m4[3] = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < 4; ++c)  // two per instruction, four chains
+            for (int c = 0; c < 4; ++c) {
+              uint32_t pk[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              m4[i & 3] = max3(m4[i & 3], __uint_as_float(sv[c][2 * i]),
-                               __uint_as_float(sv[c][2 * i + 1]));
-          const float mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * mult;
+              for (int i = 0; i < 16; ++i) {
+                const int k0 = 32 * c + 2 * i;  // key index of the low element
+                const float x0 = __uint_as_float(sv[k0 >> 5][k0 & 31]);
+                const float x1 = __uint_as_float(sv[k0 >> 5][(k0 & 31) + 1]);
+                if (track) m4[i & 3] = max3(m4[i & 3], x0, x1);
+                float p0, p1;
+                f2_unpack(f2_fma(f2_pack(x0, x1), mx2, nbx2), p0, p1);
+                p0 = fast_exp2(p0);
+                p1 = fast_exp2(p1);
+                acc[i & 1] = f2_add(acc[i & 1], f2_pack(p0, p1));
+                pk[i] = pack_bf16x2(p0, p1);
+              }
+              tc::st16(ts + 16 * c, pk);
+            }
+          };
+          auto ref_of = [](float m) { return m == -INFINITY ? 0.f : -m; };
+          // After a pass's first tile the exponentials go first, against the
+          // row's current reference m_used, with the row max taken alongside;
+          // they stand unless some row's max passed m_used + 2^8 (or a row saw
+          // its first keys), and then the tile is redone as below -- so the
+          // result is the same either way, and the max is off the critical path.
+          float mt;
+          bool redo = true;
+          if (j > 0) {
+            exp_pass(ref_of(m_used), true);
+            mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * mult;
+            redo = !(mt <= m_used + kRescaleLog2);
+          } else {
+            m4[0] = m4[1] = m4[2] = m4[3] = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)  // two per instruction, four chains
+#pragma unroll
+              for (int i = 0; i < 16; ++i)
+                m4[i & 3] = max3(m4[i & 3], __uint_as_float(sv[c][2 * i]),
+                                 __uint_as_float(sv[c][2 * i + 1]));
+            mt = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * mult;
+          }
           // lazy rescale of O (TMEM) and l when the max grew by more than 2^8 (O
           // itself is rescaled below, once the scores are no longer live)
-          const bool need = m_used != -INFINITY && mt > m_used + kRescaleLog2;
-          const bool any_need = __any_sync(0xffffffffu, need);
-          const float alpha = need ? fast_exp2(m_used - mt) : 1.f;
-          if (need) {
-            l *= alpha;
-            m_used = mt;
-          }
-          if (m_used == -INFINITY) m_used = mt;  // first keys this row sees
-          const float nbase = m_used == -INFINITY ? 0.f : -m_used;
-          // p = 2^(sv * mult - m): 0 for masked keys (-inf); packed two per
-          // column over columns 0-63 of the S buffer
-          const uint64_t mx2 = f2_pack(mult, mult), nbx2 = f2_pack(nbase, nbase);
-          uint64_t acc[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int k0 = 32 * c + 2 * i;  // key index of the low element
-              float p0, p1;
-              f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[k0 >> 5][k0 & 31]),
-                                       __uint_as_float(sv[k0 >> 5][(k0 & 31) + 1])),
-                               mx2, nbx2),
-                        p0, p1);
-              p0 = fast_exp2(p0);
-              p1 = fast_exp2(p1);
-              acc[i & 1] = f2_add(acc[i & 1], f2_pack(p0, p1));
-              pk[i] = pack_bf16x2(p0, p1);
+          bool any_need = false;
+          float alpha = 1.f;
+          if (__any_sync(0xffffffffu, redo)) {
+            const bool need = m_used != -INFINITY && mt > m_used + kRescaleLog2;
+            any_need = __any_sync(0xffffffffu, need);
+            alpha = need ? fast_exp2(m_used - mt) : 1.f;
+            if (need) {
+              l *= alpha;
+              m_used = mt;
             }
-            tc::st16(ts + 16 * c, pk);
+            if (m_used == -INFINITY) m_used = mt;  // first keys this row sees
+            exp_pass(ref_of(m_used), false);
           }
           {
             float a0, a1, b0, b1;
