@@ -477,33 +477,37 @@ def bench_pkv(args):
             hviews.append(hbuf[o:o + t.numel()].view(t.shape))
         return hbuf, dbuf, dviews, hviews
 
-    meta_h, meta_d, (ds, dcu, dctx, dbt), (_, cu_h, ctx_h, bt_h) = packed(
-        [slots0, cu_d, ctx0_d, bt_d], torch.int32)
+    # the plan is written by the host planner into the metadata buffer, after
+    # the arrays, so one copy carries both
+    plan_words = ((int(info.plan_bytes) + 4095) // 4096 + 1) * 1024
+    meta_h, meta_d, (ds, dcu, dctx, dbt, dplan), (_, cu_h, ctx_h, bt_h, plan_hv) = packed(
+        [slots0, cu_d, ctx0_d, bt_d, torch.zeros(plan_words, dtype=torch.int32)], torch.int32)
+    plan_off = plan_hv.data_ptr() - meta_h.data_ptr()          # bytes, 16-byte aligned
     qkv_h, qkv_d, qkv_dv, _ = packed([x for qkv in vals for x in qkv], torch.bfloat16)
     dvals = [tuple(qkv_dv[3 * t:3 * t + 3]) for t in range(len(vals))]
-    cu_np, ctx_np, bt_np = cu_h.numpy(), ctx_h.numpy(), bt_h.numpy()
-    plan_h = torch.empty((int(info.plan_bytes) + 4095) // 4096 * 4096 + 4096,
-                         dtype=torch.uint8).pin_memory()
+    cu_np, ctx_np, bt_np, plan_np = cu_h.numpy(), ctx_h.numpy(), bt_h.numpy(), plan_hv.numpy()
     num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     outs_h = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
-    h2d = (meta_h.numel() * meta_h.element_size() + qkv_h.numel() * qkv_h.element_size() +
-           int(info.plan_bytes))
+    meta_used = (plan_off + int(info.plan_bytes) + 15) // 16 * 4  # int32 words copied per step
+    h2d = meta_used * 4 + qkv_h.numel() * qkv_h.element_size()
+    plan_e2e = pkv.StepPlan(info, host_plan, dev)
+    plan_e2e.dev = dplan.view(torch.uint8)
     d2h = sum(o.numel() * o.element_size() for o in outs_h)
     e2e_times = []
     with torch.cuda.stream(stream):
         for i in range(args.warmup + args.steps):
             torch.cuda.synchronize(dev)
             t0 = time.perf_counter()
-            meta_d.copy_(meta_h, non_blocking=True)
             qkv_d.copy_(qkv_h, non_blocking=True)
             inf2, hp2 = pkv.plan_step(cu_np, ctx_np, meta.num_q_heads, pool, upload=False,
                                       chain_steps=chain_arg, block_tables=bt_np,
-                                      num_sms=num_sms, out=plan_h)
-            plan.dev[:hp2.nbytes].copy_(plan_h[:hp2.nbytes], non_blocking=True)
-            plan.info = inf2
+                                      num_sms=num_sms, out=plan_np)
+            n = (plan_off + hp2.nbytes + 15) // 16 * 4
+            meta_d[:n].copy_(meta_h[:n], non_blocking=True)
+            plan_e2e.info = inf2
             for t, (dq, dk, dv) in enumerate(dvals):
                 pkv.paged_kv_append(dk, dv, ds, pool, dev_status=status)
-                pkv.paged_varlen_attention(dq, dcu, dctx, dbt, pool, meta.scale, plan=plan,
+                pkv.paged_varlen_attention(dq, dcu, dctx, dbt, pool, meta.scale, plan=plan_e2e,
                                            out=outs[t], dev_status=status)
                 if t + 1 < nch:
                     pkv.decode_advance(dctx, ds, dcu, dbt, pool, dev_status=status)
