@@ -799,7 +799,14 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   if (!plan) return PKV_OK;
   if (plan_capacity < info->plan_bytes) return PKV_ERR_WORKSPACE;
   char *p = static_cast<char *>(plan);
-  std::memset(p, 0, (size_t)info->plan_bytes);
+  // every section below is written whole; only the alignment padding after
+  // the two offset arrays is cleared
+  {
+    const int64_t wb_end = off.warp_begin + (int64_t)warp_begin.size() * 4;
+    std::memset(p + wb_end, 0, (size_t)(off.warp_head - wb_end));
+    const int64_t pb_end = off.prefill_begin + (int64_t)pf_begin.size() * 4;
+    if (off.prefill > pb_end) std::memset(p + pb_end, 0, (size_t)(off.prefill - pb_end));
+  }
   PlanHeader h;
   std::memset(&h, 0, sizeof h);
   h.magic = kPlanMagic;
@@ -817,9 +824,9 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   h.reserved[0] = (int32_t)gather.size();
   std::memcpy(p, &h, sizeof h);
   std::memcpy(p + off.warp_begin, warp_begin.data(), warp_begin.size() * sizeof(int32_t));
+  WarpHead *heads = reinterpret_cast<WarpHead *>(p + off.warp_head);
   for (int32_t w = 0; w < num_warps; ++w) {
-    WarpHead wh;
-    std::memset(&wh, 0, sizeof wh);
+    WarpHead &wh = heads[w];
     wh.first = pieces[warp_begin[w]];
     for (int i = 0; i < 4; ++i) {
       const int32_t kb = wh.first.kb_begin + i;
@@ -827,7 +834,6 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
       if (i < kHeadBlocks && block_tables && kb < wh.first.kb_end && kb < max_blocks_per_seq)
         wh.blk[i] = block_tables[(int64_t)wh.first.seq * max_blocks_per_seq + kb];
     }
-    std::memcpy(p + off.warp_head + (int64_t)w * sizeof(WarpHead), &wh, sizeof wh);
   }
   if (!pieces.empty()) std::memcpy(p + off.pieces, pieces.data(), pieces.size() * sizeof(Piece));
   if (!merges.empty())

@@ -253,6 +253,28 @@ def test_prefill_kernel_matches_oracle(pkv, cuda_device, ql, cl, hq, hkv, d):
     assert_close(out, want, f"prefill {ql} {cl}")
 
 
+@pytest.mark.parametrize("d", [128, 64])
+def test_prefill_rescales_when_scores_grow_along_the_keys(pkv, cuda_device, d):
+    """Scores that grow from one 128-key tile to the next by more than 2^8 (in
+    the exponent's log2 units) make every row's running max jump at each tile,
+    so the tensor-core softmax takes its rescale path (O and l rescaled, the
+    tile's exponentials redone) on every tile after the first; the result
+    still matches the oracle."""
+    meta = workloads.build_step("grow", 131, [640], [640], 4, 2, d)   # prefill from empty, 5 key tiles
+    q, k, v, pool = workloads.make_values(meta)
+    g = torch.Generator().manual_seed(5)
+    q.copy_((1.0 + 0.1 * torch.randn(q.shape, generator=g)).to(torch.bfloat16))
+    tile = (torch.arange(meta.total_q) // 128).to(torch.float32)
+    # score of key p for any row: about scale * D * 0.9 * tile(p) -> +(0.9 * sqrt(D) / ln 2) log2 units per tile (> 10)
+    k.copy_((0.9 * tile[:, None, None] + 0.3 * torch.randn(k.shape, generator=g)).to(torch.bfloat16))
+    plan_info, _ = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads,
+                                 pkv.pool_desc(pool), upload=False)
+    assert plan_info.num_prefill_tiles > 0
+    want, _ = oracle.run_step(meta, q, k, v, pool)
+    out, _, _ = gpu_step(pkv, meta, q, k, v, pool, cuda_device)
+    assert_close(out, want, f"growing scores D={d}")
+
+
 def test_prefill_and_split_kv_paths_agree(pkv, cuda_device, monkeypatch):
     meta = workloads.build_step("paths", 91, [300, 2, 1], [1000, 500, 40], 8, 2, 128)
     q, k, v, pool = workloads.make_values(meta)
