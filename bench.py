@@ -460,36 +460,46 @@ def bench_pkv(args):
     # cu_q_lens, context_lens, block tables) and every step's bf16 q/k/v -- each
     # copied in one transfer; the plan is written straight into pinned memory and
     # uploaded asynchronously.
-    def packed(parts, dtype):
-        """One pinned host buffer holding `parts` (each start 16-byte aligned), the
-        matching device buffer, and the device and host views of each part."""
-        per = 16 // torch.tensor([], dtype=dtype).element_size()
+    def packed(parts):
+        """One pinned host byte buffer holding `parts` (any dtypes, each start
+        16-byte aligned), the matching device buffer, and the device and host
+        views of each part."""
         offs, n = [], 0
         for t in parts:
             offs.append(n)
-            n += (t.numel() + per - 1) // per * per
-        hbuf = torch.zeros(max(n, per), dtype=dtype).pin_memory()
-        dbuf = torch.empty(max(n, per), dtype=dtype, device=dev)
+            n += (t.numel() * t.element_size() + 15) // 16 * 16
+        hbuf = torch.zeros(max(n, 16), dtype=torch.uint8).pin_memory()
+        dbuf = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
         dviews, hviews = [], []
         for t, o in zip(parts, offs):
-            hbuf[o:o + t.numel()].copy_(t.reshape(-1).cpu())
-            dviews.append(dbuf[o:o + t.numel()].view(t.shape))
-            hviews.append(hbuf[o:o + t.numel()].view(t.shape))
+            nb = t.numel() * t.element_size()
+            hv = hbuf[o:o + nb].view(t.dtype).view(t.shape)
+            hv.copy_(t.cpu())
+            dviews.append(dbuf[o:o + nb].view(t.dtype).view(t.shape))
+            hviews.append(hv)
         return hbuf, dbuf, dviews, hviews
 
-    # the plan is written by the host planner into the metadata buffer, after
-    # the arrays, so one copy carries both
+    # the step's int32 metadata, every step's bf16 q/k/v and, last, the plan
+    # (written by the host planner each step) share one pinned buffer, so one
+    # copy carries all of them
     plan_words = ((int(info.plan_bytes) + 4095) // 4096 + 1) * 1024
-    meta_h, meta_d, (ds, dcu, dctx, dbt, dplan), (_, cu_h, ctx_h, bt_h, plan_hv) = packed(
-        [slots0, cu_d, ctx0_d, bt_d, torch.zeros(plan_words, dtype=torch.int32)], torch.int32)
-    plan_off = plan_hv.data_ptr() - meta_h.data_ptr()          # bytes, 16-byte aligned
-    qkv_h, qkv_d, qkv_dv, _ = packed([x for qkv in vals for x in qkv], torch.bfloat16)
+    qkv_parts = [x for qkv in vals for x in qkv]
+    buf_h, buf_d, dviews, hviews = packed(
+        [slots0, cu_d, ctx0_d, bt_d] + qkv_parts + [torch.zeros(plan_words, dtype=torch.int32)])
+    ds, dcu, dctx, dbt = dviews[:4]
+    dplan = dviews[-1]
+    cu_h, ctx_h, bt_h, plan_hv = hviews[1], hviews[2], hviews[3], hviews[-1]
+    plan_off = plan_hv.data_ptr() - buf_h.data_ptr()          # bytes, 16-byte aligned
+    qkv_dv = dviews[4:-1]
     dvals = [tuple(qkv_dv[3 * t:3 * t + 3]) for t in range(len(vals))]
     cu_np, ctx_np, bt_np, plan_np = cu_h.numpy(), ctx_h.numpy(), bt_h.numpy(), plan_hv.numpy()
     num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
     outs_h = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
-    meta_used = (plan_off + int(info.plan_bytes) + 15) // 16 * 4  # int32 words copied per step
-    h2d = meta_used * 4 + qkv_h.numel() * qkv_h.element_size()
+    h2d = (plan_off + int(info.plan_bytes) + 15) // 16 * 16  # bytes copied per step
+    # one copy after planning, or -- when the step's inputs are large enough for
+    # their transfer to matter -- the inputs first, overlapping the planning,
+    # then the plan
+    split_copy = plan_off > (4 << 20)
     plan_e2e = pkv.StepPlan(info, host_plan, dev)
     plan_e2e.dev = dplan.view(torch.uint8)
     d2h = sum(o.numel() * o.element_size() for o in outs_h)
@@ -498,12 +508,14 @@ def bench_pkv(args):
         for i in range(args.warmup + args.steps):
             torch.cuda.synchronize(dev)
             t0 = time.perf_counter()
-            qkv_d.copy_(qkv_h, non_blocking=True)
+            if split_copy:  # large inputs go up while the host plans
+                buf_d[:plan_off].copy_(buf_h[:plan_off], non_blocking=True)
             inf2, hp2 = pkv.plan_step(cu_np, ctx_np, meta.num_q_heads, pool, upload=False,
                                       chain_steps=chain_arg, block_tables=bt_np,
                                       num_sms=num_sms, out=plan_np)
-            n = (plan_off + hp2.nbytes + 15) // 16 * 4
-            meta_d[:n].copy_(meta_h[:n], non_blocking=True)
+            n = (plan_off + hp2.nbytes + 15) // 16 * 16
+            n0 = plan_off if split_copy else 0
+            buf_d[n0:n].copy_(buf_h[n0:n], non_blocking=True)
             plan_e2e.info = inf2
             for t, (dq, dk, dv) in enumerate(dvals):
                 pkv.paged_kv_append(dk, dv, ds, pool, dev_status=status)
