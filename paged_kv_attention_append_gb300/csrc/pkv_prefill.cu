@@ -37,12 +37,14 @@
 //              from TMEM, over the first 64 columns of S buffer j % 3).
 //   warps 0-3  softmax: warp w owns TMEM lane quarter w, i.e. query rows
 //              32w .. 32w+31, one row per thread and all 128 keys of a tile.
-//              It reads S(j), masks, takes the row max, computes
-//              2^(scale*s - m) and the row sum, and writes P(j) as bf16 over
-//              the first 64 columns of S(j) in TMEM.  O is rescaled in TMEM
-//              only when a row's max grows by more than 2^8 (the softmax is
-//              exact for any reference point; the threshold only bounds
-//              P <= 2^8).
+//              It reads S(j), masks, computes 2^(scale*s - m) and the row
+//              sum, and writes P(j) as bf16 over the first 64 columns of S(j)
+//              in TMEM.  The reference m moves only when a row's max grows by
+//              more than 2^8 (the softmax is exact for any reference point; the
+//              threshold only bounds P <= 2^8), and then O is rescaled in
+//              TMEM; so after a pass's first tile the exponentials are taken
+//              against the current reference with the row max found in the
+//              same sweep, and a tile whose max moved the reference is redone.
 // TMEM holds three S buffers and O (3 x 128 + D <= 512 columns), so S(j+1) and
 // S(j+2) are computed while the softmax of tile j runs; S(j+3) reuses the
 // buffer of S(j) once O += P(j) V_j has read P(j).  Only the softmax and the
