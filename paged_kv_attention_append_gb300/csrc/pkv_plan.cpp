@@ -480,7 +480,7 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
     // (+ half a block) and goes to the warp whose equal share of the total cost
     // holds that position; the ranges stay contiguous in the block stream.  With
     // at least kMinBlocksPerWarp blocks per warp every share holds a block.
-    constexpr int64_t kBlockCost = 2, kPieceCost = 3;
+    constexpr int64_t kBlockCost = 2, kPieceCost = 6;
     const int64_t total_cost = kBlockCost * total_blocks + kPieceCost * (int64_t)segs.size();
     std::vector<int64_t> cut(num_warps + 1, total_blocks);  // first block of each warp
     cut[0] = 0;

@@ -132,7 +132,7 @@ def check_plan(meta, info, host, num_sms):
     nq_tile = max(1, 16 // g)
     assert info.total_q == meta.total_q
     assert info.kv_tokens == int(meta.context_lens[meta.q_lens > 0].astype(np.int64).sum())
-    # warp ranges: contiguous, cover all pieces, equal cost: 2 per block plus 3
+    # warp ranges: contiguous, cover all pieces, equal cost: 2 per block plus 6
     # per segment start; each of a range's two ends may be off by one block and
     # one segment start
     # shared-block items (verify windows wider than one row group): as pieces
@@ -152,9 +152,9 @@ def check_plan(meta, info, host, num_sms):
         sh_blocks = int((sh_pieces[:, 5] - sh_pieces[:, 4]).sum())
         assert sum(per_warp) + sh_blocks == sum_segment_blocks(meta)
         if not len(sh_pieces):
-            cost = [2 * per_warp[w] + 3 * int((pieces[wb[w]:wb[w + 1], 4] == 0).sum())
+            cost = [2 * per_warp[w] + 6 * int((pieces[wb[w]:wb[w + 1], 4] == 0).sum())
                     for w in range(nw)]
-            assert max(cost) - min(cost) <= 2 * (2 + 3)
+            assert max(cost) - min(cost) <= 2 * (2 + 6)
         if num_sms is not None:
             assert nw + 2 * len(sh) <= num_sms * 8
     assert np.all(pieces[:, 5] > pieces[:, 4])
