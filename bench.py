@@ -1,12 +1,18 @@
 """Benchmark one packed paged-attention step (KV append + attention) on GB300.
 
-python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pkv|reference] [--config NAME]
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pkv|reference] [--config NAME] [--only]
 
 A step is one pass of the whole path over one synthetic batch: KV append of
-the step's new tokens, split-KV attention and its LSE merge, and the
+the step's new tokens, split-KV attention with its LSE merge, and the
 tensor-core prefill tiles when present.  The step plan (host step metadata) is
 an input like the block tables: resident in HBM for `value`, computed and
 uploaded per step inside `e2e`.
+
+The line's workload is the high-concurrency decode step (256 sequences, 3.4 GB
+of KV), the largest of the five step shapes the metric is quoted on; the other
+four (tiny decode, small-model decode, the agent-shaped mixed step, the
+shared-prefix verify step) are timed in the same process, the same way, and
+reported under `configs` (--only skips them).
 
 * value: KV tokens/s = sum(context_lens) / device time per step, inputs resident
   in HBM, the step replayed from a CUDA graph, L2 flushed before every timed
@@ -20,12 +26,13 @@ uploaded per step inside `e2e`.
   the plan reads once per CTA counted once, one gathered onto the tensor cores
   not at all) plus q, out and metadata; the tensor-core kernel's FLOPs are
   4 * D * (query row, key) pairs: the causal pairs of prefill-class sequences
-  plus the gathered shared-prefix pairs.
+  plus the gathered shared-prefix pairs.  A step with tensor-core work also
+  reports the step against both roofs (step_roofline: t = max(bytes / BW,
+  FLOPs / peak) over the measured step time).
 * e2e: the same metric through the public API from pinned HOST buffers: every
-  step copies q, the new K/V, slot mapping and metadata host->device (two pinned
-  buffers, one transfer each), plans on the host into pinned memory and uploads
-  the plan asynchronously, runs append + attention and copies out back (wall
-  time per step).
+  step copies q, the new K/V, slot mapping, metadata and the plan host->device
+  (one pinned buffer, one transfer), plans on the host into pinned memory, runs
+  append + attention and copies out back (wall time per step).
 * cpu_baseline / --impl reference: the fp64 CPU oracle as it stands, on the
   host cores, on a bounded sample of the same workload.
 """
@@ -305,12 +312,318 @@ def bench_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": meta.kv_tokens() / v * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": meta.name, **workloads.describe(meta)},
+            "config": config_of(meta, ws),
             "cpu_baseline": {k: r[k] for k in ("value", "unit", "cores", "kind", "sample")},
             "e2e": {"value": v, "unit": "KV tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     line["cpu_baseline"]["value"] = v
     print(json.dumps(line), flush=True)
+
+
+L2_NOTE = (f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MB written, then "
+           f"{L2_FLUSH_BYTES >> 20} MB read)")
+TIMING_NOTE = ("CUDA graph replay per step, CUDA events per step; kernel intervals from event "
+               "nodes captured around each kernel (second graph, no programmatic launch)")
+# the five step shapes the metric is quoted on (the first is correctness-only
+# and launch-bound); the line's own workload is the largest that fits one GPU
+BASELINE_CONFIGS = ["tiny_decode", "small_decode", "agent_mixed", "high_conc_decode",
+                    "shared_prefix_verify"]
+HEADLINE = "high_conc_decode"
+
+
+def config_of(meta, ws: int) -> dict:
+    """The workload keys of a bench line (identical for the pkv and reference arms)."""
+    nch = workloads.chain_steps(meta)
+    return {**workloads.describe(meta), **({"chain_steps": nch} if nch > 1 else {}),
+            "parallelism": f"replicas x{ws}" if ws > 1 else "single"}
+
+
+class StepBench:
+    """One workload resident on the GPU: its inputs, plan, a CUDA graph of one
+    step, and the timings of the step and of each kernel in it."""
+
+    def __init__(self, pkv, meta, dev, stream):
+        import torch
+        self.pkv, self.meta, self.dev, self.stream = pkv, meta, dev, stream
+        nch = self.nch = workloads.chain_steps(meta)
+        self.metas = [workloads.chain_step(meta, meta.context_lens, t) for t in range(nch)]
+        q, k, v, pool = workloads.make_values(meta, device=dev)
+        self.pool = pool
+        self.vals = [(q, k, v)] + [tuple(workloads.make_values(m, seed=meta.seed + t, device=dev)[:3])
+                                   for t, m in enumerate(self.metas) if t > 0]
+        self.slots0 = torch.from_numpy(meta.slot_mapping).to(dev)
+        self.slots = self.slots0.clone()
+        self.cu_d = torch.from_numpy(meta.cu_q_lens).to(dev)
+        self.ctx0_d = torch.from_numpy(meta.context_lens).to(dev)
+        self.ctx_d = self.ctx0_d.clone()
+        self.bt_d = torch.from_numpy(meta.block_tables).to(dev)
+        self.outs = [torch.empty_like(x[0]) for x in self.vals]
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.chain_arg = nch if nch > 1 else None
+        self.info, self.host_plan = pkv.plan_step(
+            meta.cu_q_lens, meta.context_lens, meta.num_q_heads, pool, upload=False,
+            chain_steps=self.chain_arg, block_tables=meta.block_tables)
+        self.plan = pkv.StepPlan(self.info, self.host_plan, dev)
+
+    def host_plan_us(self, reps=50):
+        m = self.meta
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            self.pkv.plan_step(m.cu_q_lens, m.context_lens, m.num_q_heads, self.pool, upload=False,
+                               chain_steps=self.chain_arg, block_tables=m.block_tables)
+        return (time.perf_counter() - t0) / reps * 1e6
+
+    def step(self):
+        # the plan is a step input like the block tables: uploaded before the
+        # timed region (StepPlan); host planning and its upload are timed in e2e
+        pkv, m = self.pkv, self.meta
+        if self.nch > 1:
+            self.ctx_d.copy_(self.ctx0_d)
+            self.slots.copy_(self.slots0)
+        for t, (qt, kt, vt) in enumerate(self.vals):
+            pkv.paged_kv_append(kt, vt, self.slots, self.pool, dev_status=self.status)
+            pkv.paged_varlen_attention(qt, self.cu_d, self.ctx_d, self.bt_d, self.pool, m.scale,
+                                       plan=self.plan, out=self.outs[t], dev_status=self.status)
+            if t + 1 < self.nch:
+                pkv.decode_advance(self.ctx_d, self.slots, self.cu_d, self.bt_d, self.pool,
+                                   dev_status=self.status)
+
+    def measure(self, args, flush_l2, clock_sampler=None):
+        """Step time (graph replay, L2 flushed before each) and per-kernel times
+        (event nodes around each kernel in a second graph)."""
+        import torch
+        pkv, dev, stream = self.pkv, self.dev, self.stream
+        with torch.cuda.stream(stream):
+            for _ in range(max(1, args.warmup)):
+                self.step()
+        torch.cuda.synchronize(dev)
+        assert int(self.status.item()) == 0, f"device status {int(self.status.item())}"
+        launches_before = pkv.kernel_launch_count()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            self.step()
+        self.launches_per_step = pkv.kernel_launch_count() - launches_before
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                flush_l2()
+                graph.replay()
+        torch.cuda.synchronize(dev)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        torch.cuda.synchronize(dev)
+        barrier()
+        torch.cuda.synchronize(dev)
+        with (clock_sampler if clock_sampler is not None else _nullctx()):
+            with torch.cuda.stream(stream):
+                for a, b in ev:
+                    flush_l2()
+                    a.record(stream)
+                    graph.replay()
+                    b.record(stream)
+            torch.cuda.synchronize(dev)
+            info = self.info
+            present = {"append": True, "decode": info.num_decode_warps + info.num_shared_ctas > 0,
+                       "merge": info.num_kernels > (1 if info.num_decode_warps + info.num_shared_ctas > 0 else 0)
+                       + (1 if info.num_prefill_tiles > 0 else 0),
+                       "prefill": info.num_prefill_tiles > 0}
+            k_ev = {n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    for n in present}
+            samples = {n: [] for n in present}
+            with torch.cuda.stream(stream):
+                for a, b in k_ev.values():
+                    a.record(stream)
+                    b.record(stream)
+                torch.cuda.synchronize(dev)
+                for name, (a, b) in k_ev.items():
+                    pkv.set_profile_events(name, a, b)
+                graph_k = torch.cuda.CUDAGraph()
+                try:
+                    with torch.cuda.graph(graph_k, stream=stream):
+                        self.step()
+                finally:
+                    for name in k_ev:
+                        pkv.set_profile_events(name)
+                for i in range(args.warmup + args.steps):
+                    flush_l2()
+                    graph_k.replay()
+                    stream.synchronize()
+                    if i >= args.warmup:
+                        for name, (a, b) in k_ev.items():
+                            if present[name]:
+                                samples[name].append(a.elapsed_time(b))
+            torch.cuda.synchronize(dev)
+        self.step_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev) / args.steps, dev)
+        self.kern_ms = {n: (statistics.mean(samples[n]) if present[n] and samples[n] else 0.0)
+                        for n in k_ev}
+        assert int(self.status.item()) == 0, f"device status {int(self.status.item())}"
+        # warm: the same step replayed back to back without the L2 flush
+        ev_w = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)]
+        with torch.cuda.stream(stream):
+            graph.replay()
+            for a, b in ev_w:
+                a.record(stream)
+                graph.replay()
+                b.record(stream)
+        torch.cuda.synchronize(dev)
+        self.warm_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev_w) / args.steps, dev)
+        self.graph = graph
+
+    def summary(self, ws: int, steps: int) -> dict:
+        """Throughput, the dominant kernel's roofline, per-kernel times; for a step
+        with tensor-core work, the step-level pair of fractions."""
+        meta, info, pk = self.meta, self.info, peaks()
+        kv_tok = sum(m.kv_tokens() for m in self.metas)          # over the chain's steps
+        bytes_alg = sum(algorithmic_bytes(m) for m in self.metas)
+        # kernel events keep the last launch of a chain: its step's bytes (the
+        # plan of a chain is sized for its last step)
+        dec_bytes = decode_kernel_bytes(self.metas[-1], info)
+        # tensor-core work: prefill-class sequences and gathered shared-prefix rows
+        fl = prefill_flops(meta) + 4 * meta.head_dim * int(info.gather_pairs)
+        km = self.kern_ms
+        decode_ms, prefill_ms = km["decode"], km["prefill"]
+        kernels = {"append_kernel": {"ms_per_launch": km["append"]}}
+        if km["merge"]:
+            kernels["merge_kernel"] = {"ms_per_launch": km["merge"]}
+        if decode_ms:
+            kernels["decode_kernel"] = {"ms_per_launch": decode_ms, "bytes_per_launch": dec_bytes,
+                                        "gbs": dec_bytes / (decode_ms * 1e-3) / 1e9,
+                                        "frac_hbm": dec_bytes / (decode_ms * 1e-3) / 1e9 / pk["hbm_gbs"]}
+        if prefill_ms:
+            kernels["prefill_kernel"] = {"ms_per_launch": prefill_ms, "flops_per_launch": fl,
+                                         "tflops": fl / (prefill_ms * 1e-3) / 1e12,
+                                         "frac_bf16": fl / (prefill_ms * 1e-3) / 1e12 / pk["bf16_tflops"]}
+        if prefill_ms > decode_ms:     # the dominant kernel is a dense contraction
+            achieved = fl / (prefill_ms * 1e-3) / 1e12
+            roofline = {"bound": "tensor", "kernel": "prefill_kernel", "achieved": achieved,
+                        "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
+                        "traffic": recorded_traffic("prefill_kernel", meta.name),
+                        "flops_per_launch": fl, "ms_per_launch": prefill_ms,
+                        "peak_source": pk["source"] + " (bf16 burst)",
+                        "frac_sustained": achieved / (pk["bf16_tflops_sustained"] or pk["bf16_tflops"])}
+        elif decode_ms:
+            achieved = dec_bytes / (decode_ms * 1e-3) / 1e9
+            roofline = {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved,
+                        "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
+                        "traffic": recorded_traffic("decode_kernel", meta.name),
+                        "bytes_per_launch": dec_bytes, "ms_per_launch": decode_ms,
+                        "peak_source": pk["source"]}
+        else:
+            roofline = None
+        out = {
+            "value": job_throughput(kv_tok, ws, self.step_ms * 1e-3), "unit": "KV tokens/s",
+            "ms_per_step": self.step_ms, "roofline": roofline, "kernels": kernels,
+            "step_gbs": bytes_alg / (self.step_ms * 1e-3) / 1e9,
+            "step_frac_hbm": bytes_alg / (self.step_ms * 1e-3) / 1e9 / pk["hbm_gbs"],
+            "gpu_launches": self.launches_per_step * steps,
+            "warm": {"value": job_throughput(kv_tok, ws, self.warm_ms * 1e-3),
+                     "ms_per_step": self.warm_ms, "l2": "not flushed: the step replayed back to back"},
+            "plan": {"decode_warps": info.num_decode_warps, "decode_pieces": info.num_decode_pieces,
+                     "merge_groups": info.num_merge_groups, "prefill_tiles": info.num_prefill_tiles,
+                     "shared_prefix_ctas": info.num_shared_ctas, "kernels_per_call": info.num_kernels,
+                     "gathered_rows": info.num_gather_rows * (meta.num_q_heads // meta.num_kv_heads)},
+        }
+        if fl:
+            # the step as a whole against both roofs: t_roofline = max(bytes / BW, flops / peak)
+            t_b = bytes_alg / (pk["hbm_gbs"] * 1e9)
+            t_f = fl / (pk["bf16_tflops"] * 1e12)
+            t_s = self.step_ms * 1e-3
+            out["step_roofline"] = {
+                "bytes": bytes_alg, "flops": fl, "t_bytes_ms": t_b * 1e3, "t_flops_ms": t_f * 1e3,
+                "t_roofline_ms": max(t_b, t_f) * 1e3, "frac": max(t_b, t_f) / t_s,
+                "frac_hbm": t_b / t_s, "frac_tensor": t_f / t_s,
+                "bound": "tensor" if t_f >= t_b else "hbm"}
+            out["prefill_tflops_step"] = fl / t_s / 1e12
+        if meta.unique_blocks() * 16 < kv_tok and decode_ms:
+            out["unique_gbs"] = unique_bytes(meta) / (decode_ms * 1e-3) / 1e9
+        return out
+
+    def e2e(self, args, ws):
+        """Wall time per step through the public API from pinned host buffers (a
+        chained workload: all its steps' inputs in, one plan, every output back).
+        The step's int32 metadata, every step's bf16 q/k/v and, last, the plan
+        (written by the host planner each step) share one pinned buffer, so one
+        copy carries all of them."""
+        import torch
+        pkv, dev, stream, meta, info = self.pkv, self.dev, self.stream, self.meta, self.info
+
+        def packed(parts):
+            offs, n = [], 0
+            for t in parts:
+                offs.append(n)
+                n += (t.numel() * t.element_size() + 15) // 16 * 16
+            hbuf = torch.zeros(max(n, 16), dtype=torch.uint8).pin_memory()
+            dbuf = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
+            dviews, hviews = [], []
+            for t, o in zip(parts, offs):
+                nb = t.numel() * t.element_size()
+                hv = hbuf[o:o + nb].view(t.dtype).view(t.shape)
+                hv.copy_(t.cpu())
+                dviews.append(dbuf[o:o + nb].view(t.dtype).view(t.shape))
+                hviews.append(hv)
+            return hbuf, dbuf, dviews, hviews
+
+        plan_words = ((int(info.plan_bytes) + 4095) // 4096 + 1) * 1024
+        qkv_parts = [x for qkv in self.vals for x in qkv]
+        buf_h, buf_d, dviews, hviews = packed(
+            [self.slots0, self.cu_d, self.ctx0_d, self.bt_d] + qkv_parts +
+            [torch.zeros(plan_words, dtype=torch.int32)])
+        ds, dcu, dctx, dbt = dviews[:4]
+        dplan = dviews[-1]
+        cu_h, ctx_h, bt_h, plan_hv = hviews[1], hviews[2], hviews[3], hviews[-1]
+        plan_off = plan_hv.data_ptr() - buf_h.data_ptr()          # bytes, 16-byte aligned
+        qkv_dv = dviews[4:-1]
+        dvals = [tuple(qkv_dv[3 * t:3 * t + 3]) for t in range(len(self.vals))]
+        cu_np, ctx_np, bt_np, plan_np = cu_h.numpy(), ctx_h.numpy(), bt_h.numpy(), plan_hv.numpy()
+        num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        outs_h = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in self.outs]
+        h2d = (plan_off + int(info.plan_bytes) + 15) // 16 * 16  # bytes copied per step
+        # one copy after planning, or -- when the step's inputs are large enough
+        # for their transfer to matter -- the inputs first, overlapping the
+        # planning, then the plan
+        split_copy = plan_off > (4 << 20)
+        plan_e2e = pkv.StepPlan(info, self.host_plan, dev)
+        plan_e2e.dev = dplan.view(torch.uint8)
+        d2h = sum(o.numel() * o.element_size() for o in outs_h)
+        times = []
+        with torch.cuda.stream(stream):
+            for i in range(args.warmup + args.steps):
+                torch.cuda.synchronize(dev)
+                t0 = time.perf_counter()
+                if split_copy:  # large inputs go up while the host plans
+                    buf_d[:plan_off].copy_(buf_h[:plan_off], non_blocking=True)
+                inf2, hp2 = pkv.plan_step(cu_np, ctx_np, meta.num_q_heads, self.pool, upload=False,
+                                          chain_steps=self.chain_arg, block_tables=bt_np,
+                                          num_sms=num_sms, out=plan_np)
+                n = (plan_off + hp2.nbytes + 15) // 16 * 16
+                n0 = plan_off if split_copy else 0
+                buf_d[n0:n].copy_(buf_h[n0:n], non_blocking=True)
+                plan_e2e.info = inf2
+                for t, (dq, dk, dv) in enumerate(dvals):
+                    pkv.paged_kv_append(dk, dv, ds, self.pool, dev_status=self.status)
+                    pkv.paged_varlen_attention(dq, dcu, dctx, dbt, self.pool, meta.scale,
+                                               plan=plan_e2e, out=self.outs[t],
+                                               dev_status=self.status)
+                    if t + 1 < self.nch:
+                        pkv.decode_advance(dctx, ds, dcu, dbt, self.pool, dev_status=self.status)
+                for oh, o in zip(outs_h, self.outs):
+                    oh.copy_(o, non_blocking=True)
+                stream.synchronize()
+                if i >= args.warmup:
+                    times.append(time.perf_counter() - t0)
+        assert int(self.status.item()) == 0, f"device status {int(self.status.item())}"
+        e2e_s = max_over_ranks(statistics.mean(times), dev)
+        kv_tok = sum(m.kv_tokens() for m in self.metas)
+        return {"value": job_throughput(kv_tok, ws, e2e_s), "unit": "KV tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3}
+
+
+class _nullctx:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
 
 
 def bench_pkv(args):
@@ -323,22 +636,6 @@ def bench_pkv(args):
         dist.init_process_group("nccl")
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
-    meta = workloads.make_config(args.config)
-    # a chained workload runs nch decode steps per timed unit (one graph), with
-    # the contexts and slots moved on by the device between steps
-    nch = workloads.chain_steps(meta)
-    metas = [workloads.chain_step(meta, meta.context_lens, t) for t in range(nch)]
-    q, k, v, pool = workloads.make_values(meta, device=dev)
-    vals = [(q, k, v)] + [tuple(workloads.make_values(m, seed=meta.seed + t, device=dev)[:3])
-                          for t, m in enumerate(metas) if t > 0]
-    slots0 = torch.from_numpy(meta.slot_mapping).to(dev)
-    slots = slots0.clone()
-    cu_d = torch.from_numpy(meta.cu_q_lens).to(dev)
-    ctx0_d = torch.from_numpy(meta.context_lens).to(dev)
-    ctx_d = ctx0_d.clone()
-    bt_d = torch.from_numpy(meta.block_tables).to(dev)
-    outs = [torch.empty_like(x[0]) for x in vals]
-    out = outs[0]
     flush_w = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_r = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     flush_acc = torch.zeros((), dtype=torch.float32, device=dev)
@@ -346,219 +643,28 @@ def bench_pkv(args):
     def flush_l2():
         flush_w.zero_()                          # write more than L2 holds ...
         torch.sum(flush_r, dim=0, out=flush_acc)  # ... then read more, leaving clean lines
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.Stream(dev)
 
-    chain_arg = nch if nch > 1 else None
-    info, host_plan = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, pool,
-                                    upload=False, chain_steps=chain_arg,
-                                    block_tables=meta.block_tables)
-    t0 = time.perf_counter()
-    for _ in range(50):
-        pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, pool, upload=False,
-                      chain_steps=chain_arg, block_tables=meta.block_tables)
-    host_plan_us = (time.perf_counter() - t0) / 50 * 1e6
-    plan = pkv.StepPlan(info, host_plan, dev)
+    # the other configurations first, each timed the same way and then freed
+    others = {}
+    if not args.only:
+        for name in BASELINE_CONFIGS:
+            if name == args.config:
+                continue
+            b = StepBench(pkv, workloads.make_config(name), dev, stream)
+            b.measure(args, flush_l2)
+            others[name] = b.summary(ws, args.steps)
+            del b
+            torch.cuda.empty_cache()
 
-    def step():
-        # the plan is a step input like the block tables: uploaded before the timed
-        # region (StepPlan); host planning and its upload are timed inside e2e
-        if nch > 1:
-            ctx_d.copy_(ctx0_d)
-            slots.copy_(slots0)
-        for t, (qt, kt, vt) in enumerate(vals):
-            pkv.paged_kv_append(kt, vt, slots, pool, dev_status=status)
-            pkv.paged_varlen_attention(qt, cu_d, ctx_d, bt_d, pool, meta.scale, plan=plan,
-                                       out=outs[t], dev_status=status)
-            if t + 1 < nch:
-                pkv.decode_advance(ctx_d, slots, cu_d, bt_d, pool, dev_status=status)
-
-    # warm up eagerly, then capture one step into a CUDA graph
-    with torch.cuda.stream(stream):
-        for _ in range(max(1, args.warmup)):
-            step()
-    torch.cuda.synchronize(dev)
-    assert int(status.item()) == 0, f"device status {int(status.item())}"
-    launches_before = pkv.kernel_launch_count()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        step()
-    launches_per_step = pkv.kernel_launch_count() - launches_before
-    with torch.cuda.stream(stream):
-        for _ in range(args.warmup):
-            flush_l2()
-            graph.replay()
-    torch.cuda.synchronize(dev)
-
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
-    torch.cuda.synchronize(dev)
-    barrier()
-    torch.cuda.synchronize(dev)
+    meta = workloads.make_config(args.config)
+    b = StepBench(pkv, meta, dev, stream)
+    host_plan_us = b.host_plan_us()
     with ClockSampler(local) as clk:
-        with torch.cuda.stream(stream):
-            for a, b in ev:
-                flush_l2()
-                a.record(stream)
-                graph.replay()
-                b.record(stream)
-        torch.cuda.synchronize(dev)
-        # kernel-only timing (roofline): the library records our events around each
-        # launch; captured into a second graph they are event nodes beside the
-        # kernels, so an interval holds the kernel and no host launch gap.  L2 is
-        # flushed before every replay, as for the step.
-        present = {"append": True, "decode": info.num_decode_warps > 0,
-                   "merge": info.num_merge_groups > 0, "prefill": info.num_prefill_tiles > 0}
-        k_ev = {n: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for n in present}
-        samples = {n: [] for n in present}
-        with torch.cuda.stream(stream):
-            for a, b in k_ev.values():
-                a.record(stream)
-                b.record(stream)
-            torch.cuda.synchronize(dev)
-            for name, (a, b) in k_ev.items():
-                pkv.set_profile_events(name, a, b)
-            graph_k = torch.cuda.CUDAGraph()
-            try:
-                with torch.cuda.graph(graph_k, stream=stream):
-                    step()
-            finally:
-                for name in k_ev:
-                    pkv.set_profile_events(name)
-            for i in range(args.warmup + args.steps):
-                flush_l2()
-                graph_k.replay()
-                stream.synchronize()
-                if i >= args.warmup:
-                    for name, (a, b) in k_ev.items():
-                        if present[name]:
-                            samples[name].append(a.elapsed_time(b))
-        torch.cuda.synchronize(dev)
-    step_ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
-    kern_ms = {n: (statistics.mean(samples[n]) if present[n] else 0.0) for n in k_ev}
-    decode_ms, prefill_ms = kern_ms["decode"], kern_ms["prefill"]
+        b.measure(args, flush_l2, None)
     clocks = clk.summary()
-    step_ms = max_over_ranks(step_ms, dev)
-    assert int(status.item()) == 0, f"device status {int(status.item())}"
-    # warm: the same step replayed back to back without the L2 flush (the
-    # flushed figure above is the headline)
-    ev_w = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-            for _ in range(args.steps)]
-    with torch.cuda.stream(stream):
-        graph.replay()
-        for a, b in ev_w:
-            a.record(stream)
-            graph.replay()
-            b.record(stream)
-    torch.cuda.synchronize(dev)
-    warm_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev_w) / args.steps, dev)
-
-    # ---- end to end from pinned host buffers through the public API (a chained
-    # workload: all its steps' inputs in, one plan, every step's output back).  The
-    # step's host inputs sit in two pinned buffers -- the int32 metadata (slots,
-    # cu_q_lens, context_lens, block tables) and every step's bf16 q/k/v -- each
-    # copied in one transfer; the plan is written straight into pinned memory and
-    # uploaded asynchronously.
-    def packed(parts):
-        """One pinned host byte buffer holding `parts` (any dtypes, each start
-        16-byte aligned), the matching device buffer, and the device and host
-        views of each part."""
-        offs, n = [], 0
-        for t in parts:
-            offs.append(n)
-            n += (t.numel() * t.element_size() + 15) // 16 * 16
-        hbuf = torch.zeros(max(n, 16), dtype=torch.uint8).pin_memory()
-        dbuf = torch.empty(max(n, 16), dtype=torch.uint8, device=dev)
-        dviews, hviews = [], []
-        for t, o in zip(parts, offs):
-            nb = t.numel() * t.element_size()
-            hv = hbuf[o:o + nb].view(t.dtype).view(t.shape)
-            hv.copy_(t.cpu())
-            dviews.append(dbuf[o:o + nb].view(t.dtype).view(t.shape))
-            hviews.append(hv)
-        return hbuf, dbuf, dviews, hviews
-
-    # the step's int32 metadata, every step's bf16 q/k/v and, last, the plan
-    # (written by the host planner each step) share one pinned buffer, so one
-    # copy carries all of them
-    plan_words = ((int(info.plan_bytes) + 4095) // 4096 + 1) * 1024
-    qkv_parts = [x for qkv in vals for x in qkv]
-    buf_h, buf_d, dviews, hviews = packed(
-        [slots0, cu_d, ctx0_d, bt_d] + qkv_parts + [torch.zeros(plan_words, dtype=torch.int32)])
-    ds, dcu, dctx, dbt = dviews[:4]
-    dplan = dviews[-1]
-    cu_h, ctx_h, bt_h, plan_hv = hviews[1], hviews[2], hviews[3], hviews[-1]
-    plan_off = plan_hv.data_ptr() - buf_h.data_ptr()          # bytes, 16-byte aligned
-    qkv_dv = dviews[4:-1]
-    dvals = [tuple(qkv_dv[3 * t:3 * t + 3]) for t in range(len(vals))]
-    cu_np, ctx_np, bt_np, plan_np = cu_h.numpy(), ctx_h.numpy(), bt_h.numpy(), plan_hv.numpy()
-    num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    outs_h = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs]
-    h2d = (plan_off + int(info.plan_bytes) + 15) // 16 * 16  # bytes copied per step
-    # one copy after planning, or -- when the step's inputs are large enough for
-    # their transfer to matter -- the inputs first, overlapping the planning,
-    # then the plan
-    split_copy = plan_off > (4 << 20)
-    plan_e2e = pkv.StepPlan(info, host_plan, dev)
-    plan_e2e.dev = dplan.view(torch.uint8)
-    d2h = sum(o.numel() * o.element_size() for o in outs_h)
-    e2e_times = []
-    with torch.cuda.stream(stream):
-        for i in range(args.warmup + args.steps):
-            torch.cuda.synchronize(dev)
-            t0 = time.perf_counter()
-            if split_copy:  # large inputs go up while the host plans
-                buf_d[:plan_off].copy_(buf_h[:plan_off], non_blocking=True)
-            inf2, hp2 = pkv.plan_step(cu_np, ctx_np, meta.num_q_heads, pool, upload=False,
-                                      chain_steps=chain_arg, block_tables=bt_np,
-                                      num_sms=num_sms, out=plan_np)
-            n = (plan_off + hp2.nbytes + 15) // 16 * 16
-            n0 = plan_off if split_copy else 0
-            buf_d[n0:n].copy_(buf_h[n0:n], non_blocking=True)
-            plan_e2e.info = inf2
-            for t, (dq, dk, dv) in enumerate(dvals):
-                pkv.paged_kv_append(dk, dv, ds, pool, dev_status=status)
-                pkv.paged_varlen_attention(dq, dcu, dctx, dbt, pool, meta.scale, plan=plan_e2e,
-                                           out=outs[t], dev_status=status)
-                if t + 1 < nch:
-                    pkv.decode_advance(dctx, ds, dcu, dbt, pool, dev_status=status)
-            for oh, o in zip(outs_h, outs):
-                oh.copy_(o, non_blocking=True)
-            stream.synchronize()
-            if i >= args.warmup:
-                e2e_times.append(time.perf_counter() - t0)
-    e2e_s = max_over_ranks(statistics.mean(e2e_times), dev)
-
-    pk = peaks()
-    kv_tok = sum(m.kv_tokens() for m in metas)          # over the chain's steps
-    bytes_alg = sum(algorithmic_bytes(m) for m in metas)
-    # kernel events keep the last launch of a chain: its step's bytes (the plan
-    # of a chain is sized for its last step)
-    dec_bytes = decode_kernel_bytes(metas[-1], info)
-    # tensor-core work: prefill-class sequences and gathered shared-prefix rows
-    fl = prefill_flops(meta) + 4 * meta.head_dim * int(info.gather_pairs)
-    kernels = {"append_kernel": {"ms_per_launch": kern_ms["append"]}}
-    if kern_ms["merge"]:
-        kernels["merge_kernel"] = {"ms_per_launch": kern_ms["merge"]}
-    if decode_ms:
-        kernels["decode_kernel"] = {"ms_per_launch": decode_ms, "bytes_per_launch": dec_bytes,
-                                    "gbs": dec_bytes / (decode_ms * 1e-3) / 1e9}
-    if prefill_ms:
-        kernels["prefill_kernel"] = {"ms_per_launch": prefill_ms, "flops_per_launch": fl,
-                                     "tflops": fl / (prefill_ms * 1e-3) / 1e12}
-    if prefill_ms > decode_ms:     # the dominant kernel is a dense contraction
-        achieved = fl / (prefill_ms * 1e-3) / 1e12
-        roofline = {"bound": "tensor", "kernel": "prefill_kernel", "achieved": achieved,
-                    "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
-                    "traffic": recorded_traffic("prefill_kernel", meta.name), "flops_per_launch": fl, "ms_per_launch": prefill_ms,
-                    "peak_source": pk["source"] + " (bf16 burst)"}
-    else:
-        achieved = dec_bytes / (decode_ms * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "kernel": "decode_kernel", "achieved": achieved,
-                    "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": achieved / pk["hbm_gbs"],
-                    "traffic": recorded_traffic("decode_kernel", meta.name), "bytes_per_launch": dec_bytes, "ms_per_launch": decode_ms,
-                    "peak_source": pk["source"]}
+    head = b.summary(ws, args.steps)
+    e2e = b.e2e(args, ws)
     cpu = cpu1 = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = run_oracle_sample(meta)                                   # all host cores
@@ -566,40 +672,36 @@ def bench_pkv(args):
     if rank != 0:
         return
     line = {
-        "metric": METRIC, "value": job_throughput(kv_tok, ws, step_ms * 1e-3), "unit": "KV tokens/s",
-        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "metric": METRIC, "value": head["value"], "unit": "KV tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) bf16, shapes of the named workload)",
-        "config": {**workloads.describe(meta), **({"chain_steps": nch} if nch > 1 else {}),
-                   "parallelism": f"replicas x{ws}" if ws > 1 else "single",
-                   "l2": f"flushed before every timed step ({L2_FLUSH_BYTES >> 20} MB written, then "
-                         f"{L2_FLUSH_BYTES >> 20} MB read)",
-                   "timing": "CUDA graph replay per step, CUDA events per step; kernel "
-                             "intervals from event nodes captured around each kernel "
-                             "(second graph, no programmatic launch)"},
-        "gpu_launches": launches_per_step * args.steps,
-        "roofline": roofline,
-        "kernels": kernels,
-        "step_gbs": bytes_alg / (step_ms * 1e-3) / 1e9,
-        "warm": {"value": job_throughput(kv_tok, ws, warm_ms * 1e-3), "ms_per_step": warm_ms,
-                 "l2": "not flushed: the step replayed back to back"},
+        "config": config_of(meta, ws),
+        "l2": L2_NOTE, "timing": TIMING_NOTE,
+        "gpu_launches": head["gpu_launches"],
+        "roofline": head["roofline"],
+        "kernels": head["kernels"],
+        "step_gbs": head["step_gbs"], "step_frac_hbm": head["step_frac_hbm"],
+        "warm": head["warm"],
         "host_plan_us": host_plan_us,
-        "e2e": {"value": job_throughput(kv_tok, ws, e2e_s), "unit": "KV tokens/s",
-                "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3},
+        "e2e": e2e,
         "clocks": clocks,
         "cpu_baseline": None if cpu is None else {
             **{k2: cpu[k2] for k2 in ("value", "unit", "cores", "kind", "sample")},
             "value_1core": cpu1["value"], "sample_1core": cpu1["sample"]},
-        "plan": {"decode_warps": info.num_decode_warps, "decode_pieces": info.num_decode_pieces,
-                 "merge_groups": info.num_merge_groups, "prefill_tiles": info.num_prefill_tiles,
-                 "shared_prefix_ctas": info.num_shared_ctas,
-                 "gathered_rows": info.num_gather_rows * (meta.num_q_heads // meta.num_kv_heads)},
+        "plan": head["plan"],
     }
-    if meta.unique_blocks() * 16 < kv_tok and decode_ms:
-        line["unique_gbs"] = unique_bytes(meta) / (decode_ms * 1e-3) / 1e9
-    if fl:
-        line["prefill_tflops_step"] = fl / (step_ms * 1e-3) / 1e12
+    for k2 in ("step_roofline", "prefill_tflops_step", "unique_gbs"):
+        if k2 in head:
+            line[k2] = head[k2]
+    if others:
+        line["configs"] = {meta.name: {k2: head[k2] for k2 in
+                                       ("value", "ms_per_step", "roofline", "kernels", "step_gbs",
+                                        "step_frac_hbm", "plan", *[x for x in ("step_roofline",
+                                                                               "unique_gbs")
+                                                                   if x in head])}}
+        line["configs"].update({n: {**o, "config": config_of(workloads.make_config(n), ws)}
+                                for n, o in others.items()})
     print(json.dumps(line), flush=True)
 
 
@@ -719,9 +821,11 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="pkv", choices=["pkv", "reference"])
-    ap.add_argument("--config", default="small_decode",
+    ap.add_argument("--config", default=HEADLINE,
                     choices=list(workloads.CONFIGS) + ["state_checkpoint"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", action="store_true",
+                    help="time the named workload alone (no per-configuration summary)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -184,16 +184,32 @@ PKV_API pkv_status pkv_paged_kv_append(const void *k, const void *v, const int32
  * work tiles sized for num_sms SMs, assigns partial-result slots and sizes the
  * workspace.
  *   cu_q_lens, context_lens: HOST arrays (num_seqs+1 and num_seqs int32).
- *   num_sms: SMs of the target GPU (<= 0 means 152).
+ *   num_sms: SMs of the target GPU; <= 0 asks the CUDA runtime for the SM count
+ *   of the calling thread's current device (PKV_ERR_CUDA if there is none).
  *   plan: host buffer receiving plan_capacity bytes at most; may be NULL to
  *   query sizes only (info is always filled on success).
  * Returns PKV_ERR_WORKSPACE if plan is non-NULL and plan_capacity < info->plan_bytes.
  * The plan buffer is opaque; upload it unchanged (e.g. cudaMemcpyAsync) before
  * the attention call that uses it.
+ *
+ * Compared with the plainest form of this call -- (cu_q_lens, context_lens,
+ * num_seqs, num_q_heads, pool) -> plan -- three things are added, each because
+ * the plan depends on it or the caller should own it: num_sms (the work is cut
+ * into equal shares for that many SMs, so a plan is tied to a GPU size); a
+ * caller-owned plan buffer with its capacity (the library allocates nothing,
+ * host or device, and the caller picks pinned memory for an asynchronous
+ * upload); and the pkv_plan_info summary, which the attention call takes in
+ * place of parsing the device copy of the plan on the host.
  */
 PKV_API pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *context_lens, int32_t num_seqs,
                          int32_t num_q_heads, const pkv_pool_desc *desc, int32_t num_sms,
                          void *plan, int64_t plan_capacity, pkv_plan_info *info);
+
+/*
+ * Bytes of device workspace the attention call needs for a plan (the same
+ * value as info->workspace_bytes; 0 when the step needs none).  info NULL: 0.
+ */
+PKV_API size_t pkv_workspace_size(const pkv_plan_info *info);
 
 /*
  * Plan for a chain of `steps` decode steps of the same batch (the vllm-metal
@@ -219,15 +235,21 @@ PKV_API pkv_status pkv_plan_decode_chain(const int32_t *cu_q_lens, const int32_t
  * HOST copy of the step's block tables ([num_seqs][max_blocks_per_seq] int32,
  * the same entries the device copy holds): the plan then also carries the
  * physical ids of the first blocks each split-KV warp reads, so its first copies
- * start without waiting for a block-table read.  The attention kernel checks
- * those ids against the device block tables and reports a disagreement as
- * PKV_DEV_PLAN_MISMATCH.
+ * start without waiting for a block-table read, and sequences whose tables
+ * start with the same physical blocks read those blocks once per work unit.
+ * The attention kernel checks the carried ids against the device block tables;
+ * on a disagreement it reports PKV_DEV_PLAN_MISMATCH and writes no result built
+ * from the disagreeing blocks (those rows of out are left as they were).
+ * prefill_min_q: sequences with at least this many query tokens run on the
+ * tensor-core prefill kernel; 0 picks the default (64); a negative value keeps
+ * every sequence on the split-KV kernel (both compute the same function).
  */
 PKV_API pkv_status pkv_plan_step_ex(const int32_t *cu_q_lens, const int32_t *context_lens,
                                     int32_t num_seqs, int32_t num_q_heads,
                                     const pkv_pool_desc *desc, int32_t num_sms, int32_t steps,
                                     const int32_t *block_tables, int32_t max_blocks_per_seq,
-                                    void *plan, int64_t plan_capacity, pkv_plan_info *info);
+                                    int32_t prefill_min_q, void *plan, int64_t plan_capacity,
+                                    pkv_plan_info *info);
 
 /*
  * Device-side move to the next step of a decode chain: for every sequence s

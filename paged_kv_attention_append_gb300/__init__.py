@@ -23,13 +23,18 @@ import torch
 __all__ = [
     "PkvError", "PoolDesc", "PlanInfo", "StepPlan", "build", "library_path", "version",
     "status_string", "kernel_launch_count", "paged_kv_append", "plan_step",
-    "paged_varlen_attention", "DEV_STATUS",
+    "paged_varlen_attention", "DEV_STATUS", "workspace_size", "prepare_workspace",
+    "WORKSPACE_COUNTER_BYTES",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "_lib", "libpkv.so")
 _lock = threading.Lock()
 _lib = None
+
+# Leading bytes of every non-empty workspace that hold arrival counters; they
+# must be zero when a call starts and every call that completes leaves them so.
+WORKSPACE_COUNTER_BYTES = 65536
 
 DEV_STATUS = {0: "ok", 1: "bad slot", 2: "bad block id", 3: "pipeline wait timed out",
               4: "plan does not match device metadata"}
@@ -99,13 +104,15 @@ def _load():
                                                   i32, P, i64, ctypes.POINTER(PlanInfo)]
             lib.pkv_plan_decode_chain.restype = i32
             lib.pkv_plan_step_ex.argtypes = [P, P, i32, i32, ctypes.POINTER(PoolDesc), i32, i32,
-                                             P, i32, P, i64, ctypes.POINTER(PlanInfo)]
+                                             P, i32, i32, P, i64, ctypes.POINTER(PlanInfo)]
             lib.pkv_plan_step_ex.restype = i32
             lib.pkv_decode_advance.argtypes = [P, P, P, P, i32, i32, ctypes.POINTER(PoolDesc), P,
                                                P]
             lib.pkv_decode_advance.restype = i32
             lib.pkv_set_profile_events.argtypes = [i32, P, P]
             lib.pkv_set_profile_events.restype = i32
+            lib.pkv_workspace_size.argtypes = [ctypes.POINTER(PlanInfo)]
+            lib.pkv_workspace_size.restype = ctypes.c_size_t
             _lib = lib
     return _lib
 
@@ -240,6 +247,21 @@ def _host_i32(x) -> np.ndarray:
     return np.ascontiguousarray(np.asarray(x), dtype=np.int32)
 
 
+def workspace_size(info: PlanInfo) -> int:
+    """Device workspace bytes the attention call needs for this plan."""
+    return int(_load().pkv_workspace_size(ctypes.byref(info)))
+
+
+def prepare_workspace(ws: torch.Tensor, info: PlanInfo) -> torch.Tensor:
+    """Make a freshly allocated workspace ready for use: zero its arrival
+    counters (the leading WORKSPACE_COUNTER_BYTES bytes).  Calls that complete
+    leave them zero, so this is needed once per allocation (and again after a
+    call whose dev_status reported an error)."""
+    if int(info.workspace_bytes) > 0:
+        ws[:min(ws.numel(), WORKSPACE_COUNTER_BYTES)].zero_()
+    return ws
+
+
 class StepPlan:
     """Host step metadata plus its device copy and the workspace it needs."""
 
@@ -252,16 +274,19 @@ class StepPlan:
         self.upload(stream)
 
     def upload(self, stream=None):
+        """Copy the plan to the device and make sure the workspace is big enough.
+        With `stream`, the copy and the allocations are made on that stream."""
         dev = torch.device(self.device)
         nbytes = max(int(self.info.plan_bytes), 16)
-        if self.dev is None or self.dev.numel() < nbytes:
-            self.dev = torch.empty(nbytes, dtype=torch.uint8, device=dev)
         src = torch.from_numpy(self.host.view(np.uint8)[:nbytes])
         with torch.cuda.stream(stream) if stream is not None else _nullcontext():
+            if self.dev is None or self.dev.numel() < nbytes:
+                self.dev = torch.empty(nbytes, dtype=torch.uint8, device=dev)
             self.dev[:nbytes].copy_(src, non_blocking=False)
-        wsb = int(self.info.workspace_bytes)
-        if wsb > 0 and (self.workspace is None or self.workspace.numel() < wsb):
-            self.workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
+            wsb = workspace_size(self.info)
+            if wsb > 0 and (self.workspace is None or self.workspace.numel() < wsb):
+                self.workspace = prepare_workspace(
+                    torch.empty(wsb, dtype=torch.uint8, device=dev), self.info)
         return self
 
 
@@ -273,18 +298,21 @@ class _nullcontext:
         return False
 
 
-_plan_scratch = np.zeros(1 << 18, dtype=np.int32)   # 1 MiB, grown on demand
+_tls = threading.local()   # per thread: the size of its last plan, to size the next buffer
 
 
 def plan_step(cu_q_lens, context_lens, num_q_heads: int, kv_pool_or_desc, *, num_sms=None,
               device=None, upload=True, stream=None, chain_steps=None,
-              block_tables=None, out=None) -> StepPlan | tuple:
+              block_tables=None, prefill_min_q=None, out=None) -> StepPlan | tuple:
     """Build the host plan for one step (pkv_plan_step_ex) and upload it.
 
     cu_q_lens / context_lens: host arrays or tensors (copied to the host if on a GPU).
     chain_steps: plan a chain of that many decode steps instead.
     block_tables: the step's block tables (host copy) -- lets the plan carry each
-    split-KV warp's first block ids (checked on the device against the tables).
+    split-KV warp's first block ids (checked on the device against the tables)
+    and read blocks that sequences share once per work unit.
+    prefill_min_q: query tokens from which a sequence runs on the tensor-core
+    kernel (None or 0: the library's default; negative: no sequence does).
     out (with upload=False): a writable host buffer (numpy array or CPU tensor,
     e.g. pinned memory for an asynchronous upload) the plan is written into; the
     returned host bytes are then a view of it.
@@ -308,6 +336,7 @@ def plan_step(cu_q_lens, context_lens, num_q_heads: int, kv_pool_or_desc, *, num
         bt = _host_i32(block_tables)
         if bt.ndim != 2 or bt.shape[0] != ctx.shape[0]:
             raise ValueError("block_tables must be [num_seqs, max_blocks_per_seq]")
+    pmq = 0 if prefill_min_q is None else int(prefill_min_q)
 
     def call(buf, cap):
         return lib.pkv_plan_step_ex(
@@ -315,7 +344,7 @@ def plan_step(cu_q_lens, context_lens, num_q_heads: int, kv_pool_or_desc, *, num
             int(num_q_heads), ctypes.byref(desc), int(num_sms),
             1 if chain_steps is None else int(chain_steps),
             None if bt is None else bt.ctypes.data_as(ctypes.c_void_p),
-            0 if bt is None else bt.shape[1], buf, cap, ctypes.byref(info))
+            0 if bt is None else bt.shape[1], pmq, buf, cap, ctypes.byref(info))
     if out is not None and not upload:
         buf = out.numpy() if isinstance(out, torch.Tensor) else out
         if not buf.flags.c_contiguous or not buf.flags.writeable:
@@ -325,16 +354,19 @@ def plan_step(cu_q_lens, context_lens, num_q_heads: int, kv_pool_or_desc, *, num
             raise PkvError(st, name)
         n = (max(int(info.plan_bytes), 16) + 15) // 16 * 16
         return info, buf.reshape(-1).view(np.uint8)[:n].view(np.int32)
-    # one planning pass into a reused buffer (grown and redone only when a plan
-    # outgrows it), then a copy of the plan's bytes
-    global _plan_scratch
-    st = call(_plan_scratch.ctypes.data_as(ctypes.c_void_p), _plan_scratch.nbytes)
-    if st == 5 and int(info.plan_bytes) > _plan_scratch.nbytes:   # PKV_ERR_WORKSPACE
-        _plan_scratch = np.zeros((int(info.plan_bytes) * 2 + 15) // 16 * 4, dtype=np.int32)
-        st = call(_plan_scratch.ctypes.data_as(ctypes.c_void_p), _plan_scratch.nbytes)
+    # one planning pass into a fresh buffer sized from this thread's last plan
+    # (planned again only when the plan outgrows it); the buffer is the plan's
+    cap = getattr(_tls, "plan_cap", 1 << 16)
+    host = np.empty(cap // 4, dtype=np.int32)
+    st = call(host.ctypes.data_as(ctypes.c_void_p), host.nbytes)
+    if st == 5 and int(info.plan_bytes) > host.nbytes:   # PKV_ERR_WORKSPACE: grow and redo
+        host = np.empty((int(info.plan_bytes) + 15) // 16 * 4, dtype=np.int32)
+        st = call(host.ctypes.data_as(ctypes.c_void_p), host.nbytes)
     if st:
         raise PkvError(st, name)
-    host = _plan_scratch[:(max(int(info.plan_bytes), 16) + 15) // 16 * 4].copy()
+    n = (max(int(info.plan_bytes), 16) + 15) // 16 * 16
+    _tls.plan_cap = max(1 << 12, (n * 5 // 4 + 4095) // 4096 * 4096)
+    host = host[:n // 4]
     if not upload:
         return info, host
     return StepPlan(info, host, torch.device(device), stream)
@@ -377,35 +409,40 @@ def paged_varlen_attention(q, cu_q_lens, context_lens, block_tables, kv_pool, sc
 
     cu_q_lens / context_lens may be host or device arrays; a plan is built from
     host copies when none is given.  block_tables: int32 [num_seqs, max_blocks].
+    stream: run on this CUDA stream instead of the current one; the arrays this
+    call copies to the device, the workspace and `out` (when allocated here) are
+    then allocated on that stream, and the caller orders its use of `out` after it.
     """
     _check_cuda("q", q, torch.bfloat16, 3)
     _check_cuda("kv_pool", kv_pool, torch.bfloat16, 5)
     desc = pool_desc(kv_pool)
     dev = q.device
-    if plan is None:
-        plan = plan_step(cu_q_lens, context_lens, q.shape[1], desc, device=dev, stream=stream)
-    info = plan.info
-    if q.shape[0] != info.total_q or q.shape[1] != info.num_q_heads or q.shape[2] != desc.head_dim:
-        raise ValueError(f"q shape {tuple(q.shape)} does not match the plan "
-                         f"({info.total_q}, {info.num_q_heads}, {desc.head_dim})")
-    cu_d = _dev_i32(cu_q_lens, dev, "cu_q_lens")
-    ctx_d = _dev_i32(context_lens, dev, "context_lens")
-    bt_d = _dev_i32(block_tables, dev, "block_tables")
-    if bt_d.dim() != 2 or bt_d.shape[0] != info.num_seqs:
-        raise ValueError("block_tables must be [num_seqs, max_blocks_per_seq]")
-    if out is None:
-        out = torch.empty_like(q)
-    else:
-        _check_cuda("out", out, torch.bfloat16, 3)
-        if out.shape != q.shape:
-            raise ValueError("out must have q's shape")
-    if dev_status is not None:
-        _check_cuda("dev_status", dev_status, torch.int32)
-    ws = plan.workspace
-    st = _load().pkv_paged_varlen_attention(
-        _ptr(q), _ptr(cu_d), _ptr(ctx_d), _ptr(bt_d), bt_d.shape[1], _ptr(kv_pool),
-        ctypes.byref(desc), float(scale), ctypes.byref(info), _ptr(plan.dev), _ptr(out), _ptr(ws),
-        0 if ws is None else ws.numel(), _ptr(dev_status), _stream(stream, q))
+    ctx_mgr = torch.cuda.stream(stream) if stream is not None else _nullcontext()
+    with ctx_mgr:
+        if plan is None:
+            plan = plan_step(cu_q_lens, context_lens, q.shape[1], desc, device=dev, stream=stream)
+        info = plan.info
+        if q.shape[0] != info.total_q or q.shape[1] != info.num_q_heads or q.shape[2] != desc.head_dim:
+            raise ValueError(f"q shape {tuple(q.shape)} does not match the plan "
+                             f"({info.total_q}, {info.num_q_heads}, {desc.head_dim})")
+        cu_d = _dev_i32(cu_q_lens, dev, "cu_q_lens")
+        ctx_d = _dev_i32(context_lens, dev, "context_lens")
+        bt_d = _dev_i32(block_tables, dev, "block_tables")
+        if bt_d.dim() != 2 or bt_d.shape[0] != info.num_seqs:
+            raise ValueError("block_tables must be [num_seqs, max_blocks_per_seq]")
+        if out is None:
+            out = torch.empty_like(q)
+        else:
+            _check_cuda("out", out, torch.bfloat16, 3)
+            if out.shape != q.shape:
+                raise ValueError("out must have q's shape")
+        if dev_status is not None:
+            _check_cuda("dev_status", dev_status, torch.int32)
+        ws = plan.workspace
+        st = _load().pkv_paged_varlen_attention(
+            _ptr(q), _ptr(cu_d), _ptr(ctx_d), _ptr(bt_d), bt_d.shape[1], _ptr(kv_pool),
+            ctypes.byref(desc), float(scale), ctypes.byref(info), _ptr(plan.dev), _ptr(out),
+            _ptr(ws), 0 if ws is None else ws.numel(), _ptr(dev_status), _stream(stream, q))
     if st:
         raise PkvError(st, "pkv_paged_varlen_attention")
     return out

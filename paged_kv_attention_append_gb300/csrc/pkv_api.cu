@@ -12,6 +12,23 @@ namespace pkv {
 static std::atomic<int64_t> g_launches{0};
 void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
+constexpr int kMaxDevices = 64;
+static std::atomic<int> g_sm_count[kMaxDevices];
+
+int device_sm_count() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  if (dev < kMaxDevices) {
+    const int c = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 0;
+  if (dev < kMaxDevices) g_sm_count[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
 constexpr int kNumKernelIds = 5;  // PKV_KERNEL_APPEND .. PKV_KERNEL_STATE
 
 struct ProfileEvents {
@@ -214,4 +231,8 @@ extern "C" pkv_status pkv_paged_varlen_attention(
   if (launch_decode(a, &launches)) return PKV_ERR_CUDA;
   if (launch_merge(a, &launches)) return PKV_ERR_CUDA;
   return PKV_OK;
+}
+
+extern "C" size_t pkv_workspace_size(const pkv_plan_info *info) {
+  return info && info->workspace_bytes > 0 ? (size_t)info->workspace_bytes : 0;
 }

@@ -51,7 +51,9 @@ int launch_append(const void *k, const void *v, const int32_t *slot_mapping, int
   const int64_t vecs = 2ll * desc.num_kv_heads * (desc.head_dim / 8) * num_tokens;
   const int threads = 256;
   int64_t blocks = (vecs + threads - 1) / threads;
-  blocks = blocks < 1 ? 1 : (blocks > 152 * 16 ? 152 * 16 : blocks);
+  // a grid-stride loop: at most 16 CTAs of 256 threads per SM
+  const int64_t cap = 16ll * (device_sm_count() > 0 ? device_sm_count() : 1);
+  blocks = blocks < 1 ? 1 : (blocks > cap ? cap : blocks);
   profile_begin(PKV_KERNEL_APPEND, stream);
   if (desc.head_dim == 128)
     append_kernel<128><<<(unsigned)blocks, threads, 0, stream>>>(

@@ -262,6 +262,10 @@ int make_pool_map(void *map, const void *pool, const pkv_pool_desc &desc);
 
 void count_launches(int n);
 
+// Streaming multiprocessors of the calling thread's current device (cached per
+// device); 0 when no device can be queried.
+int device_sm_count();
+
 // Profiling hook (pkv_set_profile_events): events recorded around launches of
 // one kernel id on the launching stream; per host thread.
 void profile_begin(int which, pkv_stream stream);

@@ -51,9 +51,8 @@ namespace {
 
 constexpr int kDecodeWarpsPerSm = 8;
 constexpr int kMinBlocksPerWarp = 4;
-// Query tokens from which a sequence's rows go to the tensor-core kernel
-// (default 64; the environment variable PKV_PREFILL_MIN_Q overrides it, 0 or
-// a negative value keeps every row on the split-KV kernel).
+// Query tokens from which a sequence's rows go to the tensor-core kernel, when
+// the caller leaves the choice to the planner (prefill_min_q == 0).
 constexpr int kPrefillMinQDefault = 64;
 // Relative costs used to give the persistent prefill CTAs equal work: a CTA
 // runs a work item's sub-tiles one after the other, each a pass over its key
@@ -63,11 +62,11 @@ constexpr int64_t kTileCost = 8, kPassStartCost = 24;
 // CTAs get at least this many key tiles of work.
 constexpr int64_t kMinTilesPerCta = 4;
 
-int prefill_min_q() {
-  const char *env = std::getenv("PKV_PREFILL_MIN_Q");
-  if (!env || !*env) return kPrefillMinQDefault;
-  const long v = std::strtol(env, nullptr, 10);
-  return v <= 0 ? INT_MAX : (int)std::min<long>(v, INT_MAX);
+// 0: the default; > 0: that many query tokens; < 0: no sequence (every row on
+// the split-KV kernel).
+int prefill_threshold(int32_t prefill_min_q) {
+  if (prefill_min_q == 0) return kPrefillMinQDefault;
+  return prefill_min_q < 0 ? INT_MAX : prefill_min_q;
 }
 
 pkv_status check_desc(const pkv_pool_desc *desc, int32_t num_q_heads) {
@@ -115,15 +114,16 @@ using namespace pkv;
 static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_lens,
                             int32_t num_seqs, int32_t num_q_heads, const pkv_pool_desc *desc,
                             int32_t num_sms, int32_t lookahead, const int32_t *block_tables,
-                            int32_t max_blocks_per_seq, void *plan, int64_t plan_capacity,
-                            pkv_plan_info *info) {
+                            int32_t max_blocks_per_seq, int32_t prefill_min_q, void *plan,
+                            int64_t plan_capacity, pkv_plan_info *info) {
   if (!info) return PKV_ERR_NULL;
   if (lookahead < 0) return PKV_ERR_RANGE;
   pkv_status st = check_desc(desc, num_q_heads);
   if (st != PKV_OK) return st;
   if (num_seqs < 0) return PKV_ERR_SHAPE;
   if (num_seqs > 0 && (!cu_q_lens || !context_lens)) return PKV_ERR_NULL;
-  if (num_sms <= 0) num_sms = 152;
+  if (num_sms <= 0) num_sms = device_sm_count();
+  if (num_sms <= 0) return PKV_ERR_CUDA;
 
   const int32_t hkv = desc->num_kv_heads;
   const int32_t group = num_q_heads / hkv;
@@ -131,7 +131,7 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
 
   // ---- validate; build decode segments and prefill tiles
   if (num_seqs > 0 && cu_q_lens[0] != 0) return PKV_ERR_SHAPE;
-  const int min_q_prefill = prefill_min_q();
+  const int min_q_prefill = prefill_threshold(prefill_min_q);
   std::vector<Segment> segs;
   std::vector<DUnit> dunits;
   std::vector<PrefillTile> pairs;                 // sub-tile pairs, key range not yet cut
@@ -853,11 +853,12 @@ extern "C" pkv_status pkv_plan_step_ex(const int32_t *cu_q_lens, const int32_t *
                                        int32_t num_seqs, int32_t num_q_heads,
                                        const pkv_pool_desc *desc, int32_t num_sms, int32_t steps,
                                        const int32_t *block_tables, int32_t max_blocks_per_seq,
-                                       void *plan, int64_t plan_capacity, pkv_plan_info *info) {
+                                       int32_t prefill_min_q, void *plan, int64_t plan_capacity,
+                                       pkv_plan_info *info) {
   if (steps < 1) return PKV_ERR_RANGE;
   if (block_tables && max_blocks_per_seq < 0) return PKV_ERR_SHAPE;
   return plan_impl(cu_q_lens, context_lens, num_seqs, num_q_heads, desc, num_sms, steps - 1,
-                   block_tables, max_blocks_per_seq, plan, plan_capacity, info);
+                   block_tables, max_blocks_per_seq, prefill_min_q, plan, plan_capacity, info);
 }
 
 extern "C" pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *context_lens,
@@ -865,7 +866,7 @@ extern "C" pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *con
                                     const pkv_pool_desc *desc, int32_t num_sms, void *plan,
                                     int64_t plan_capacity, pkv_plan_info *info) {
   return plan_impl(cu_q_lens, context_lens, num_seqs, num_q_heads, desc, num_sms, 0, nullptr, 0,
-                   plan, plan_capacity, info);
+                   0, plan, plan_capacity, info);
 }
 
 extern "C" pkv_status pkv_plan_decode_chain(const int32_t *cu_q_lens, const int32_t *context_lens,
@@ -874,5 +875,5 @@ extern "C" pkv_status pkv_plan_decode_chain(const int32_t *cu_q_lens, const int3
                                             int32_t steps, void *plan, int64_t plan_capacity,
                                             pkv_plan_info *info) {
   return pkv_plan_step_ex(cu_q_lens, context_lens, num_seqs, num_q_heads, desc, num_sms, steps,
-                          nullptr, 0, plan, plan_capacity, info);
+                          nullptr, 0, 0, plan, plan_capacity, info);
 }

@@ -19,3 +19,17 @@ def cuda_device():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     return torch.device("cuda:0")
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Per-case attention errors against the oracle: the mean error over the
+    bf16-rounding floor and the worst element over its bound."""
+    try:
+        import parity_bar
+    except ImportError:
+        return
+    lines = parity_bar.summary_lines()
+    if lines:
+        terminalreporter.write_sep("-", "attention parity vs the fp64 oracle (bf16 floor)")
+        for ln in lines:
+            terminalreporter.write_line(ln)

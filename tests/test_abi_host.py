@@ -525,3 +525,47 @@ def test_step_generator_slots_are_distinct():
     for meta in metas:
         sl = meta.slot_mapping[meta.slot_mapping >= 0]
         assert len(np.unique(sl)) == len(sl), meta.name
+
+
+def test_workspace_size_matches_the_plan_summary(pkv):
+    for name in ("small_decode", "agent_mixed", "tiny_decode"):
+        meta = workloads.make_config(name)
+        desc = pkv.PoolDesc(meta.num_blocks, 16, meta.num_kv_heads, meta.head_dim)
+        info, _ = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, desc,
+                                num_sms=152, upload=False)
+        assert pkv.workspace_size(info) == info.workspace_bytes
+        # a step with split results starts its workspace with the counter area
+        if info.workspace_bytes:
+            assert info.workspace_bytes >= pkv.WORKSPACE_COUNTER_BYTES
+    lib = ctypes.CDLL(pkv.library_path())
+    lib.pkv_workspace_size.restype = ctypes.c_size_t
+    assert lib.pkv_workspace_size(None) == 0
+
+
+def test_prefill_min_q_is_a_planner_argument(pkv):
+    meta = workloads.build_step("pmq", 5, [300, 200, 1], [900, 700, 50], 8, 2, 128)
+    desc = pkv.PoolDesc(meta.num_blocks, 16, 2, 128)
+
+    def tiles(pmq):
+        info, host = pkv.plan_step(meta.cu_q_lens, meta.context_lens, 8, desc, num_sms=152,
+                                   upload=False, prefill_min_q=pmq)
+        pf = parse_plan(info, host)[4]
+        return sorted({int(t[0]) for t in pf}), info
+    assert tiles(None)[0] == [0, 1]      # default: from 64 query tokens
+    assert tiles(250)[0] == [0]
+    seqs, info = tiles(-1)               # none: every row on the split-KV kernel
+    assert seqs == [] and info.num_prefill_tiles == 0 and info.num_decode_warps > 0
+
+
+def test_planner_asks_the_device_for_its_sm_count(pkv):
+    """num_sms <= 0 means "the current device's SM count"; with no device the
+    planner says so instead of guessing."""
+    meta = workloads.tiny_decode()
+    desc = pkv.PoolDesc(meta.num_blocks, 16, meta.num_kv_heads, meta.head_dim)
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    with pytest.raises(pkv.PkvError) as e:
+        pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, desc, num_sms=0,
+                      upload=False)
+    assert e.value.status == 6      # PKV_ERR_CUDA
