@@ -524,12 +524,14 @@ class StepBench:
                      "gathered_rows": info.num_gather_rows * (meta.num_q_heads // meta.num_kv_heads)},
         }
         if fl:
-            # the step as a whole against both roofs: t_roofline = max(bytes / BW, flops / peak)
-            t_b = bytes_alg / (pk["hbm_gbs"] * 1e9)
+            # the step as a whole against both roofs: t_roofline = max(bytes / BW, flops / peak),
+            # bytes counting blocks several sequences share once (what HBM must deliver)
+            step_bytes = min(bytes_alg, unique_bytes(meta)) if self.nch == 1 else bytes_alg
+            t_b = step_bytes / (pk["hbm_gbs"] * 1e9)
             t_f = fl / (pk["bf16_tflops"] * 1e12)
             t_s = self.step_ms * 1e-3
             out["step_roofline"] = {
-                "bytes": bytes_alg, "flops": fl, "t_bytes_ms": t_b * 1e3, "t_flops_ms": t_f * 1e3,
+                "bytes": step_bytes, "flops": fl, "t_bytes_ms": t_b * 1e3, "t_flops_ms": t_f * 1e3,
                 "t_roofline_ms": max(t_b, t_f) * 1e3, "frac": max(t_b, t_f) / t_s,
                 "frac_hbm": t_b / t_s, "frac_tensor": t_f / t_s,
                 "bound": "tensor" if t_f >= t_b else "hbm"}

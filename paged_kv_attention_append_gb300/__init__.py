@@ -23,18 +23,13 @@ import torch
 __all__ = [
     "PkvError", "PoolDesc", "PlanInfo", "StepPlan", "build", "library_path", "version",
     "status_string", "kernel_launch_count", "paged_kv_append", "plan_step",
-    "paged_varlen_attention", "DEV_STATUS", "workspace_size", "prepare_workspace",
-    "WORKSPACE_COUNTER_BYTES",
+    "paged_varlen_attention", "DEV_STATUS", "workspace_size",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_PKG, "_lib", "libpkv.so")
 _lock = threading.Lock()
 _lib = None
-
-# Leading bytes of every non-empty workspace that hold arrival counters; they
-# must be zero when a call starts and every call that completes leaves them so.
-WORKSPACE_COUNTER_BYTES = 65536
 
 DEV_STATUS = {0: "ok", 1: "bad slot", 2: "bad block id", 3: "pipeline wait timed out",
               4: "plan does not match device metadata"}
@@ -252,16 +247,6 @@ def workspace_size(info: PlanInfo) -> int:
     return int(_load().pkv_workspace_size(ctypes.byref(info)))
 
 
-def prepare_workspace(ws: torch.Tensor, info: PlanInfo) -> torch.Tensor:
-    """Make a freshly allocated workspace ready for use: zero its arrival
-    counters (the leading WORKSPACE_COUNTER_BYTES bytes).  Calls that complete
-    leave them zero, so this is needed once per allocation (and again after a
-    call whose dev_status reported an error)."""
-    if int(info.workspace_bytes) > 0:
-        ws[:min(ws.numel(), WORKSPACE_COUNTER_BYTES)].zero_()
-    return ws
-
-
 class StepPlan:
     """Host step metadata plus its device copy and the workspace it needs."""
 
@@ -285,8 +270,7 @@ class StepPlan:
             self.dev[:nbytes].copy_(src, non_blocking=False)
             wsb = workspace_size(self.info)
             if wsb > 0 and (self.workspace is None or self.workspace.numel() < wsb):
-                self.workspace = prepare_workspace(
-                    torch.empty(wsb, dtype=torch.uint8, device=dev), self.info)
+                self.workspace = torch.empty(wsb, dtype=torch.uint8, device=dev)
         return self
 
 

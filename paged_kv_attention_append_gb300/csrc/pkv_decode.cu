@@ -77,6 +77,7 @@ struct DecodeParams {
   int32_t lookahead;           // plan sized for this many further steps (chained decode)
   int32_t num_merges;          // all merge groups: decode ones, then prefill ones
   int32_t num_decode_merges;
+  int32_t num_partials;
   int32_t num_warps;
   int32_t num_seqs;
   int32_t max_blocks_per_seq;
@@ -116,12 +117,16 @@ __device__ __forceinline__ void write_piece(const DecodeParams &p, const Piece &
 constexpr int kMergeThreads = 256;
 
 // Combines one row's 4 columns over nsplit partial slots (slot stride `rows`).
+// A split whose m is NaN was written by a piece that found its plan
+// disagreeing with the device tables: the row is then `poisoned` and must not
+// be written.
 template <int D>
 __device__ __forceinline__ float4 merge_row(const float2 *ml, const float4 *po, int nsplit,
-                                            int rows, float &L) {
+                                            int rows, float &L, bool &poisoned) {
   constexpr int kChunks = D / 4;
   float M = -INFINITY;
   L = 0.f;
+  poisoned = false;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   constexpr int kBatch = 8;  // splits whose loads are all issued before any is used
   for (int j0 = 0; j0 < nsplit; j0 += kBatch) {
@@ -135,8 +140,9 @@ __device__ __forceinline__ float4 merge_row(const float2 *ml, const float4 *po, 
     }
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
+      poisoned |= v[u].x != v[u].x;
       // skip padding entries and splits in which this row saw no key
-      if (v[u].x == -INFINITY) continue;
+      if (v[u].x == -INFINITY || v[u].x != v[u].x) continue;
       const float mn = fmaxf(M, v[u].x);
       const float a = fast_exp2(M - mn), b = fast_exp2(v[u].x - mn);
       L = L * a + v[u].y * b;
@@ -150,18 +156,38 @@ __device__ __forceinline__ float4 merge_row(const float2 *ml, const float4 *po, 
   return acc;
 }
 
+__device__ __forceinline__ void store_row4(__nv_bfloat16 *dst, float4 acc, float L) {
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  uint2 pk;
+  pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+  pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+  *reinterpret_cast<uint2 *>(dst) = pk;
+}
+
+// A piece that cannot contribute a result (its plan disagrees with the device
+// metadata) writes nothing to out; when it is one part of a merge group, every
+// row of its partial slot is marked (m = NaN) so the merge writes none of the
+// group's rows either.
+__device__ __forceinline__ void poison_piece(const DecodeParams &p, int part, int lane) {
+  if (part < 0 || part >= p.num_partials) return;
+  if (lane < kRowsPerTile)
+    p.part_ml[(int64_t)part * kRowsPerTile + lane] = make_float2(__int_as_float(0x7fc00000), 0.f);
+}
+
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams p) {
   constexpr int kChunks = D / 4;  // float4 chunks of a row
   const int64_t t = (int64_t)blockIdx.x * kMergeThreads + threadIdx.x;
-  const int64_t n_dec = (int64_t)p.num_decode_merges * kRowsPerTile * kChunks;
+  // decode groups, then prefill groups
+  const int n_dg = p.num_decode_merges;
+  const int64_t n_dec = (int64_t)n_dg * kRowsPerTile * kChunks;
   const bool dec = t < n_dec;
   const int rows = dec ? kRowsPerTile : kPrefillRows;
   const int64_t tt = dec ? t : t - n_dec;
   const int64_t gi = tt / (rows * kChunks);
   const int rem = (int)(tt % (rows * kChunks));
   const int row = rem / kChunks, ch = rem % kChunks;
-  const bool in = gi < (dec ? p.num_decode_merges : p.num_merges - p.num_decode_merges);
+  const bool in = gi < (dec ? n_dg : p.num_merges - p.num_decode_merges);
   // the plan is not written by the kernels before this one: the group is read
   // while they finish; only the partials wait
   MergeGroup g;
@@ -171,21 +197,20 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
   const int G = p.group;
   const int nrows = dec ? g.n_q * G : g.n_q;
   if (row >= nrows || nrows > rows || g.seq < 0 || g.seq >= p.num_seqs || g.nsplit < 1 ||
-      g.kind != (dec ? 0 : 1) || g.q_row0 < 0 || g.q_row0 + (dec ? g.n_q : nrows) > p.total_q)
+      g.kind != (dec ? 0 : 1) || g.q_row0 < 0 ||
+      g.q_row0 + (dec ? g.n_q : nrows) > p.total_q)
     return;
   const float2 *ml = (dec ? p.part_ml : p.ppart_ml) + (int64_t)g.part0 * rows + row;
   const float4 *po = reinterpret_cast<const float4 *>((dec ? p.part_o : p.ppart_o) +
                                                       ((int64_t)g.part0 * rows + row) * D) +
                      ch;
   float L;
-  const float4 acc = merge_row<D>(ml, po, g.nsplit, rows, L);
-  const float inv = L > 0.f ? 1.f / L : 0.f;
+  bool poisoned;
+  const float4 acc = merge_row<D>(ml, po, g.nsplit, rows, L, poisoned);
+  if (poisoned) return;
   const int64_t tok = g.q_row0 + (dec ? row / G : row);
   const int hq = dec ? g.h * G + row % G : g.h;
-  uint2 pk;
-  pk.x = pack_bf16x2(acc.x * inv, acc.y * inv);
-  pk.y = pack_bf16x2(acc.z * inv, acc.w * inv);
-  *reinterpret_cast<uint2 *>(p.out + (tok * p.num_q_heads + hq) * D + 4 * ch) = pk;
+  store_row4(p.out + (tok * p.num_q_heads + hq) * D + 4 * ch, acc, L);
 }
 
 // Q fragments (A operand) of a row group: rows r and r + 8 of the group's R rows
@@ -455,6 +480,8 @@ __device__ __forceinline__ void shared_cta(const CUtensorMap &pool_map, const De
     pc.part = rg.part;
     pc.q_row0 = rg.q_row0;
     write_piece<D>(p, pc, o, m_lo, m_hi, l_lo, l_hi, R, cu0, r, c);
+  } else if (good && item_ok && lw < n_rg) {
+    poison_piece(p, rg.part, lane);
   }
 }
 
@@ -648,6 +675,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
     for (int nt = 0; nt < kNt; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
     float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+    bool head_bad = false;  // the plan's block ids for this piece disagree with the table
 
     for (int kb = pc.kb_begin; kb < pc.kb_end; ++kb) {
       const bool ok = mbar_wait(smem_u32(&bars[stage]), phase);
@@ -659,9 +687,13 @@ __global__ void __launch_bounds__(kThreads, 2)
       ++consumed;
       if (consumed == 1) {  // the check entries have landed by now: compare the inline ids
         const int want = lane == 0 ? fb0 : lane == 1 ? fb1 : lane == 2 ? fb2 : -1;
-        if (want >= 0 && want != head_chk) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
+        const bool bad = want >= 0 && want != head_chk;
+        if (bad) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
+        // blocks loaded from ids the table does not hold: nothing of this
+        // piece is used or written
+        head_bad = __any_sync(0xffffffffu, bad);
       }
-      if (valid && stage_ok[stage]) {
+      if (valid && !head_bad && stage_ok[stage]) {
         const uint32_t sK = smem_u32(ring + stage * C::kStageBytes);
         block_update<D>(sK, sK + C::kSlabBytes, qa, kb * kBlockSize, q_pos0, lim_lo, lim_hi, sl2,
                         r, c, m_lo, m_hi, l_lo, l_hi, o);
@@ -674,7 +706,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
     }
     if (abandoned) break;
-    if (valid) write_piece<D>(p, pc, o, m_lo, m_hi, l_lo, l_hi, R, cu0, r, c);
+    if (valid && !head_bad)
+      write_piece<D>(p, pc, o, m_lo, m_hi, l_lo, l_hi, R, cu0, r, c);
+    else
+      poison_piece(p, pc.part, lane);
   }
   if (abandoned) {
     // drain this warp's copies still in flight (bounded) before exiting
@@ -692,51 +727,51 @@ __device__ __forceinline__ void write_piece(const DecodeParams &p, const Piece &
                                             float l_lo, float l_hi, int R, int cu0, int r, int c) {
   const int G = p.group;
   l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
-    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
-    l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
-    l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int row = r + 8 * half;
-      if (row >= R) continue;
-      const float l = half ? l_hi : l_lo;
-      const float m = half ? m_hi : m_lo;
-      const int64_t tok = cu0 + pc.qi0 + row / G;
-      const int hq = pc.h * G + row % G;
+  for (int half = 0; half < 2; ++half) {
+    const int row = r + 8 * half;
+    if (row >= R) continue;
+    const float l = half ? l_hi : l_lo;
+    const float m = half ? m_hi : m_lo;
+    const int64_t tok = cu0 + pc.qi0 + row / G;
+    const int hq = pc.h * G + row % G;
 #pragma unroll
-      for (int j = 0; j < D / 64; ++j) {
-        float v[16];
+    for (int j = 0; j < D / 64; ++j) {
+      float v[16];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          v[t] = o[8 * j + t][2 * half];
-          v[8 + t] = o[8 * j + t][2 * half + 1];
-        }
-        if (pc.part < 0) {
-          const float inv = l > 0.f ? 1.f / l : 0.f;
-          uint4 a, b;
-          a.x = pack_bf16x2(v[0] * inv, v[1] * inv);
-          a.y = pack_bf16x2(v[2] * inv, v[3] * inv);
-          a.z = pack_bf16x2(v[4] * inv, v[5] * inv);
-          a.w = pack_bf16x2(v[6] * inv, v[7] * inv);
-          b.x = pack_bf16x2(v[8] * inv, v[9] * inv);
-          b.y = pack_bf16x2(v[10] * inv, v[11] * inv);
-          b.z = pack_bf16x2(v[12] * inv, v[13] * inv);
-          b.w = pack_bf16x2(v[14] * inv, v[15] * inv);
-          uint4 *dst = reinterpret_cast<uint4 *>(p.out + (tok * p.num_q_heads + hq) * D + 64 * j +
-                                                 16 * c);
-          dst[0] = a;
-          dst[1] = b;
-        } else {
-          float4 *dst = reinterpret_cast<float4 *>(
-              p.part_o + ((int64_t)pc.part * kRowsPerTile + row) * D + 64 * j + 16 * c);
-          dst[0] = make_float4(v[0], v[1], v[2], v[3]);
-          dst[1] = make_float4(v[4], v[5], v[6], v[7]);
-          dst[2] = make_float4(v[8], v[9], v[10], v[11]);
-          dst[3] = make_float4(v[12], v[13], v[14], v[15]);
-        }
+      for (int t = 0; t < 8; ++t) {
+        v[t] = o[8 * j + t][2 * half];
+        v[8 + t] = o[8 * j + t][2 * half + 1];
       }
-      if (pc.part >= 0 && c == 0)
-        p.part_ml[(int64_t)pc.part * kRowsPerTile + row] = make_float2(m, l);
+      if (pc.part < 0) {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint4 a, b;
+        a.x = pack_bf16x2(v[0] * inv, v[1] * inv);
+        a.y = pack_bf16x2(v[2] * inv, v[3] * inv);
+        a.z = pack_bf16x2(v[4] * inv, v[5] * inv);
+        a.w = pack_bf16x2(v[6] * inv, v[7] * inv);
+        b.x = pack_bf16x2(v[8] * inv, v[9] * inv);
+        b.y = pack_bf16x2(v[10] * inv, v[11] * inv);
+        b.z = pack_bf16x2(v[12] * inv, v[13] * inv);
+        b.w = pack_bf16x2(v[14] * inv, v[15] * inv);
+        uint4 *dst =
+            reinterpret_cast<uint4 *>(p.out + (tok * p.num_q_heads + hq) * D + 64 * j + 16 * c);
+        dst[0] = a;
+        dst[1] = b;
+      } else {
+        float4 *dst = reinterpret_cast<float4 *>(
+            p.part_o + ((int64_t)pc.part * kRowsPerTile + row) * D + 64 * j + 16 * c);
+        dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+        dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+        dst[2] = make_float4(v[8], v[9], v[10], v[11]);
+        dst[3] = make_float4(v[12], v[13], v[14], v[15]);
+      }
+    }
+    if (pc.part >= 0 && c == 0)
+      p.part_ml[(int64_t)pc.part * kRowsPerTile + row] = make_float2(m, l);
   }
 }
 
@@ -779,6 +814,7 @@ DecodeParams make_params(const AttnArgs &a) {
   p.num_merges = a.num_merge_groups;
   p.lookahead = a.lookahead;
   p.num_decode_merges = a.num_decode_merges;
+  p.num_partials = a.num_partials;
   p.ppart_o = a.ppart_o;
   p.ppart_ml = reinterpret_cast<const float2 *>(a.ppart_ml);
   p.dev_status = a.dev_status;

@@ -534,9 +534,6 @@ def test_workspace_size_matches_the_plan_summary(pkv):
         info, _ = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, desc,
                                 num_sms=152, upload=False)
         assert pkv.workspace_size(info) == info.workspace_bytes
-        # a step with split results starts its workspace with the counter area
-        if info.workspace_bytes:
-            assert info.workspace_bytes >= pkv.WORKSPACE_COUNTER_BYTES
     lib = ctypes.CDLL(pkv.library_path())
     lib.pkv_workspace_size.restype = ctypes.c_size_t
     assert lib.pkv_workspace_size(None) == 0
@@ -569,3 +566,29 @@ def test_planner_asks_the_device_for_its_sm_count(pkv):
         pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, desc, num_sms=0,
                       upload=False)
     assert e.value.status == 6      # PKV_ERR_CUDA
+
+
+def test_planning_from_several_threads_gives_each_its_own_plan(pkv):
+    """Plans made at the same time on several host threads (the library call
+    releases the GIL) are each identical, byte for byte, to the plan made alone."""
+    import threading
+    steps = [workloads.make_config(n) for n in ("small_decode", "agent_mixed", "wide_verify")]
+    descs = [pkv.PoolDesc(m.num_blocks, 16, m.num_kv_heads, m.head_dim) for m in steps]
+    alone = [pkv.plan_step(m.cu_q_lens, m.context_lens, m.num_q_heads, d, num_sms=152,
+                           upload=False, block_tables=m.block_tables)[1].copy()
+             for m, d in zip(steps, descs)]
+    bad = []
+
+    def worker(i):
+        m, d = steps[i % 3], descs[i % 3]
+        for _ in range(30):
+            _, host = pkv.plan_step(m.cu_q_lens, m.context_lens, m.num_q_heads, d, num_sms=152,
+                                    upload=False, block_tables=m.block_tables)
+            if not np.array_equal(host, alone[i % 3]):
+                bad.append(i)
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(6)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not bad

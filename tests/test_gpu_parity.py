@@ -39,26 +39,25 @@ def bits(t):
 
 def guarded_out(shape, dev):
     """An output tensor inside a buffer with canary rows on both sides."""
-    buf = torch.full((shape[0] + 2 * OUT_GUARD_ROWS, *shape[1:]), OUT_CANARY - 65536,
+    buf = torch.full((shape[0] + 2 * OUT_GUARD_ROWS, *shape[1:]), OUT_CANARY,
                      dtype=torch.int16, device=dev).view(torch.bfloat16)
     return buf, buf[OUT_GUARD_ROWS:OUT_GUARD_ROWS + shape[0]]
 
 
-def guarded_workspace(pkv, plan, dev):
+def guarded_workspace(plan, dev):
     """Replace the plan's workspace by one inside a buffer with canary bytes on
-    both sides; the counter area the kernels expect at zero stays zero."""
+    both sides (the workspace itself starts filled with canary bytes too: its
+    contents on entry must not matter)."""
     n = int(plan.info.workspace_bytes)
     buf = torch.full((n + 2 * WS_GUARD_BYTES,), WS_CANARY, dtype=torch.uint8, device=dev)
-    ws = buf[WS_GUARD_BYTES:WS_GUARD_BYTES + n]
-    pkv.prepare_workspace(ws, plan.info)
-    plan.workspace = ws
+    plan.workspace = buf[WS_GUARD_BYTES:WS_GUARD_BYTES + n]
     return buf
 
 
 def check_guards(out_buf, ws_buf, what=""):
     g = OUT_GUARD_ROWS
     ob = out_buf.view(torch.int16)
-    canary = torch.tensor(OUT_CANARY - 65536, dtype=torch.int16, device=ob.device)
+    canary = torch.tensor(OUT_CANARY, dtype=torch.int16, device=ob.device)
     assert bool((ob[:g] == canary).all()) and bool((ob[ob.shape[0] - g:] == canary).all()), \
         f"{what}: a kernel wrote outside out"
     wb = ws_buf
@@ -80,7 +79,7 @@ def gpu_step(pkv, meta, q, k, v, pool, dev, *, num_sms=None, check_status=True, 
     plan = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, pd, num_sms=num_sms,
                          block_tables=meta.block_tables if tables else None,
                          prefill_min_q=prefill_min_q)
-    ws_buf = guarded_workspace(pkv, plan, dev)
+    ws_buf = guarded_workspace(plan, dev)
     out_buf, out = guarded_out(tuple(qd.shape), dev)
     pkv.paged_varlen_attention(qd, meta.cu_q_lens, meta.context_lens,
                                torch.from_numpy(meta.block_tables).to(dev), pd, meta.scale,
@@ -300,6 +299,28 @@ def test_bad_block_id_is_reported_not_faulted(pkv, cuda_device):
     # the other sequence is unaffected
     want, _ = oracle.run_step(meta, q, k, v, pool)
     assert_close(out[1:], want[1:])
+
+
+def test_attention_on_a_side_stream_with_host_arrays(pkv, cuda_device):
+    """The call runs on a non-default stream with host cu_q_lens / context_lens /
+    block tables: the arrays it copies to the device and the output it
+    allocates belong to that stream, so the result read after syncing that
+    stream alone matches the oracle."""
+    meta = workloads.build_step("side", 61, [1, 3, 130], [700, 90, 400], 8, 2, 128)
+    q, k, v, pool = workloads.make_values(meta)
+    want, pool_want = oracle.run_step(meta, q, k, v, pool)
+    dev = cuda_device
+    pd = torch.from_numpy(pool_want.view(np.int16)).view(torch.bfloat16).to(dev)
+    s = torch.cuda.Stream(dev)
+    qd = q.to(dev)
+    torch.cuda.synchronize(dev)
+    outs = []
+    for _ in range(3):      # temporaries freed between calls may be reused by the next
+        outs.append(pkv.paged_varlen_attention(qd, meta.cu_q_lens, meta.context_lens,
+                                               meta.block_tables, pd, meta.scale, stream=s))
+    s.synchronize()
+    for o in outs:
+        assert_close(o.cpu(), want, "side stream")
 
 
 def test_in_tree_library_is_loaded(pkv):
@@ -557,7 +578,8 @@ def test_plan_with_block_tables_same_result_and_mismatch_reported(pkv, cuda_devi
     """A plan that carries the first block ids (from the host tables) gives the
     same bits as one that does not; host tables that disagree with the device
     copy are reported as a plan mismatch (the ids are range-checked first, so
-    only in-pool blocks are read)."""
+    only in-pool blocks are read), and no output row is built from the blocks
+    the plan named: every row is either left as it was or correct."""
     meta = workloads.small_decode()
     q, k, v, pool = workloads.make_values(meta)
     dev = cuda_device
@@ -579,11 +601,20 @@ def test_plan_with_block_tables_same_result_and_mismatch_reported(pkv, cuda_devi
     wrong = np.roll(meta.block_tables, 1, axis=0)          # other sequences' blocks
     plan = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads, pd,
                          block_tables=wrong)
+    out_buf, out = guarded_out(tuple(qd.shape), dev)
     pkv.paged_varlen_attention(qd, meta.cu_q_lens, meta.context_lens, bt, pd, meta.scale,
-                               plan=plan, dev_status=status)
+                               plan=plan, out=out, dev_status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 4      # PKV_DEV_PLAN_MISMATCH
-
+    ob = out.view(torch.int16).cpu().reshape(-1, meta.head_dim)
+    untouched = (ob == OUT_CANARY).all(dim=1).numpy()
+    assert untouched.sum() > 0
+    want, _ = oracle.run_step(meta, q, k, v, pool)
+    got = out.cpu().reshape(-1, meta.head_dim)
+    written = ~untouched
+    if written.any():
+        parity_bar.check(got[torch.from_numpy(written)], want.reshape(-1, meta.head_dim)[written],
+                         "rows written under a plan mismatch")
 
 
 @pytest.mark.parametrize("name,num_sms", [("shared_prefix_verify", 152), ("mtp_draft", 152),
