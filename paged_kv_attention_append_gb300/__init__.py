@@ -23,7 +23,7 @@ import torch
 __all__ = [
     "PkvError", "PoolDesc", "PlanInfo", "StepPlan", "build", "library_path", "version",
     "status_string", "kernel_launch_count", "paged_kv_append", "plan_step",
-    "paged_varlen_attention", "DEV_STATUS", "workspace_size",
+    "paged_varlen_attention", "DEV_STATUS", "workspace_size", "BoundStep",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -430,3 +430,72 @@ def paged_varlen_attention(q, cu_q_lens, context_lens, block_tables, kv_pool, sc
     if st:
         raise PkvError(st, "pkv_paged_varlen_attention")
     return out
+
+
+class BoundStep:
+    """One step's KV append and attention with their arguments checked once.
+
+    A serving loop that reuses the same device buffers every step (inputs copied
+    into them, the plan re-made into the same pinned buffer) binds them here and
+    calls run() per step: each run is two calls into the library with
+    pre-marshalled arguments, no tensor checks and no allocation.  `plan` is
+    read at run time (plan.info, plan.dev and plan.workspace may be replaced
+    between runs, e.g. with each step's new plan summary), so the step's shape
+    may change as long as the bound buffers stay large enough for it: run()
+    re-checks the sizes the plan states against the bound tensors.
+    """
+
+    def __init__(self, k, v, slot_mapping, q, cu_q_lens, context_lens, block_tables, kv_pool,
+                 scale: float, plan: StepPlan, out, *, dev_status=None, stream=None):
+        _check_cuda("kv_pool", kv_pool, torch.bfloat16, 5)
+        for name, t, ndim in (("k", k, 3), ("v", v, 3), ("q", q, 3), ("out", out, 3)):
+            _check_cuda(name, t, torch.bfloat16, ndim)
+        for name, t, ndim in (("slot_mapping", slot_mapping, 1), ("cu_q_lens", cu_q_lens, 1),
+                              ("context_lens", context_lens, 1), ("block_tables", block_tables, 2)):
+            _check_cuda(name, t, torch.int32, ndim)
+        if dev_status is not None:
+            _check_cuda("dev_status", dev_status, torch.int32)
+        desc = pool_desc(kv_pool)
+        if k.shape[1:] != (desc.num_kv_heads, desc.head_dim) or v.shape != k.shape:
+            raise ValueError("k/v must be [n, num_kv_heads, head_dim] of the pool")
+        if out.shape != q.shape or q.shape[2] != desc.head_dim:
+            raise ValueError("out must have q's shape, [total_q, num_q_heads, head_dim]")
+        if slot_mapping.shape[0] != k.shape[0]:
+            raise ValueError("slot_mapping needs one entry per new token")
+        self.plan = plan
+        self._tensors = (k, v, slot_mapping, q, cu_q_lens, context_lens, block_tables, kv_pool,
+                         out, dev_status)   # kept alive while bound
+        self._desc = desc
+        self._lib = _load()
+        self._stream = _stream(stream, q)
+        self._n_new = k.shape[0]
+        self._shape = (q.shape[0], q.shape[1], cu_q_lens.shape[0], block_tables.shape[0],
+                       block_tables.shape[1])
+        vp = ctypes.c_void_p
+        self._append = (vp(k.data_ptr()), vp(v.data_ptr()), vp(slot_mapping.data_ptr()),
+                        ctypes.c_int32(self._n_new), vp(kv_pool.data_ptr()), ctypes.byref(desc),
+                        vp(_ptr(dev_status)), vp(self._stream))
+        self._attn_head = (vp(q.data_ptr()), vp(cu_q_lens.data_ptr()), vp(context_lens.data_ptr()),
+                           vp(block_tables.data_ptr()), ctypes.c_int32(block_tables.shape[1]),
+                           vp(kv_pool.data_ptr()), ctypes.byref(desc), ctypes.c_float(scale))
+        self._out = vp(out.data_ptr())
+        self._tail = (vp(_ptr(dev_status)), vp(self._stream))
+
+    def run(self) -> None:
+        """Enqueue this step's append and attention on the bound stream."""
+        info = self.plan.info
+        total_q, hq, n_cu, n_bt, max_blocks = self._shape
+        if (info.total_q != total_q or info.num_q_heads != hq or info.num_seqs + 1 != n_cu or
+                info.num_seqs != n_bt):
+            raise ValueError("the plan does not match the bound buffers")
+        lib = self._lib
+        st = lib.pkv_paged_kv_append(*self._append)
+        if st:
+            raise PkvError(st, "pkv_paged_kv_append")
+        ws = self.plan.workspace
+        st = lib.pkv_paged_varlen_attention(
+            *self._attn_head, ctypes.byref(info), ctypes.c_void_p(self.plan.dev.data_ptr()),
+            self._out, ctypes.c_void_p(None if ws is None else ws.data_ptr()),
+            ctypes.c_int64(0 if ws is None else ws.numel()), *self._tail)
+        if st:
+            raise PkvError(st, "pkv_paged_varlen_attention")

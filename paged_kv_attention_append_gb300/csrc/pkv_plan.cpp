@@ -40,7 +40,6 @@
 #include <climits>
 #include <cstdlib>
 #include <cstring>
-#include <map>
 #include <queue>
 #include <vector>
 
@@ -92,6 +91,19 @@ constexpr int32_t kMinSharedBlocks = 8;
 constexpr int32_t kKeyTileBlocks = 128 / kBlockSize;
 constexpr int64_t kGatherMinRows = 64;
 
+// The planner's working arrays, kept per host thread so a plan allocates
+// nothing once a thread has planned a step of that size.
+struct PlanScratch {
+  std::vector<std::pair<int32_t, int32_t>> by_first;
+  std::vector<Segment> segs;
+  std::vector<DUnit> dunits;
+  std::vector<Piece> pieces;
+  std::vector<int32_t> warp_begin, seg_first, seg_count, seg_of, unit_kb0, shared_len;
+  std::vector<int64_t> cut;
+  std::vector<MergeGroup> merges;
+};
+thread_local PlanScratch t_scratch;
+
 PrefillTile new_tile() {
   PrefillTile t;
   std::memset(&t, 0, sizeof t);
@@ -132,8 +144,11 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   // ---- validate; build decode segments and prefill tiles
   if (num_seqs > 0 && cu_q_lens[0] != 0) return PKV_ERR_SHAPE;
   const int min_q_prefill = prefill_threshold(prefill_min_q);
-  std::vector<Segment> segs;
-  std::vector<DUnit> dunits;
+  PlanScratch &S = t_scratch;
+  std::vector<Segment> &segs = S.segs;
+  std::vector<DUnit> &dunits = S.dunits;
+  segs.clear();
+  dunits.clear();
   std::vector<PrefillTile> pairs;                 // sub-tile pairs, key range not yet cut
   std::vector<std::array<int32_t, 2>> pair_nt;   // key tiles seen by each sub-tile
   int64_t kv_tokens = 0, total_blocks = 0;
@@ -200,7 +215,8 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   // row of each of them sees in full.  Those blocks are read once per CTA by
   // shared items; the rest of each row group's keys (its suffix) go to the
   // per-warp ranges below.
-  std::vector<int32_t> shared_len(num_seqs, 0);
+  std::vector<int32_t> &shared_len = S.shared_len;
+  shared_len.assign(num_seqs, 0);
   struct Group {
     std::vector<int32_t> members;
     int32_t len;  // shared blocks handled as shared (whole key tiles when tc)
@@ -208,25 +224,32 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   };
   std::vector<Group> groups;
   if (block_tables && max_blocks_per_seq > 0) {
-    std::map<int32_t, std::vector<int32_t>> by_first;
+    // sequences keyed by their first physical block; runs of equal keys are
+    // candidate groups (in order of first block, members in sequence order)
+    std::vector<std::pair<int32_t, int32_t>> &by_first = S.by_first;
+    by_first.clear();
     for (int32_t s = 0; s < num_seqs; ++s) {
       const int32_t qs = cu_q_lens[s + 1] - cu_q_lens[s];
       if (qs <= 0 || qs >= min_q_prefill) continue;
       const int32_t vis = std::min((context_lens[s] - qs + 1) / kBlockSize, max_blocks_per_seq);
-      if (vis >= kMinSharedBlocks) by_first[block_tables[(int64_t)s * max_blocks_per_seq]].push_back(s);
+      if (vis >= kMinSharedBlocks) by_first.push_back({block_tables[(int64_t)s * max_blocks_per_seq], s});
     }
-    for (auto &kv : by_first) {
-      const std::vector<int32_t> &mem = kv.second;
-      if (mem.size() < 2) continue;
+    std::sort(by_first.begin(), by_first.end());
+    std::vector<int32_t> mem;
+    for (size_t a = 0, b = 0; a < by_first.size(); a = b) {
+      while (b < by_first.size() && by_first[b].first == by_first[a].first) ++b;
+      if (b - a < 2) continue;
+      mem.clear();
+      for (size_t i = a; i < b; ++i) mem.push_back(by_first[i].second);
       int32_t len = INT32_MAX;
       for (int32_t m : mem)
         len = std::min(len, std::min((context_lens[m] - (cu_q_lens[m + 1] - cu_q_lens[m]) + 1) /
                                          kBlockSize, max_blocks_per_seq));
       const int32_t *t0 = block_tables + (int64_t)mem[0] * max_blocks_per_seq;
-      for (int32_t b = 1; b < len; ++b)
+      for (int32_t kb = 1; kb < len; ++kb)
         for (size_t i = 1; i < mem.size(); ++i)
-          if (block_tables[(int64_t)mem[i] * max_blocks_per_seq + b] != t0[b]) {
-            len = b;
+          if (block_tables[(int64_t)mem[i] * max_blocks_per_seq + kb] != t0[kb]) {
+            len = kb;
             break;
           }
       if (len < kMinSharedBlocks) continue;
@@ -249,7 +272,8 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
     std::vector<int32_t> units;
   };
   std::vector<Stream> streams;
-  std::vector<int32_t> unit_kb0(dunits.size(), 0);
+  std::vector<int32_t> &unit_kb0 = S.unit_kb0;
+  unit_kb0.assign(dunits.size(), 0);
   {
     std::vector<int32_t> unit_first(num_seqs, -1);  // decode units are in sequence order
     for (size_t u = dunits.size(); u-- > 0;) unit_first[dunits[u].seq] = (int32_t)u;
@@ -285,7 +309,8 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   }
 
   // suffix segments: (row group, KV head) keys past the shared blocks
-  std::vector<int32_t> seg_of(dunits.size() * hkv, -1);
+  std::vector<int32_t> &seg_of = S.seg_of;
+  seg_of.assign(dunits.size() * hkv, -1);
   for (size_t u = 0; u < dunits.size(); ++u) {
     const DUnit &du = dunits[u];
     const int32_t kb0 = std::min(unit_kb0[u], du.nb);
@@ -308,7 +333,8 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   const int64_t slots = (int64_t)num_sms * kDecodeWarpsPerSm;
   std::vector<SharedItem> sitems;
   // shared parts of each (decode unit, KV head): (item, warp slot)
-  std::vector<std::vector<std::array<int32_t, 2>>> unit_shared(dunits.size() * hkv);
+  // (allocated only when there are shared streams)
+  std::vector<std::vector<std::array<int32_t, 2>>> unit_shared(streams.empty() ? 0 : dunits.size() * hkv);
   if (!streams.empty()) {
     int64_t sh_blocks = 0, max_len = 0;
     for (const Stream &st : streams) {
@@ -467,11 +493,25 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
                                    (total_blocks + avail - 1) / avail + kMinBlocksPerWarp);
   if (whole_segments) nw64 = (int64_t)segs.size();
   const int32_t num_warps = total_blocks > 0 ? (int32_t)std::max<int64_t>(nw64, 1) : 0;
-  std::vector<int32_t> warp_begin(num_warps + 1, 0);
-  std::vector<Piece> pieces;
-  std::vector<int32_t> piece_seg;
-  pieces.reserve(segs.size() + num_warps);  // a range adds at most one piece beyond its segments
-  piece_seg.reserve(segs.size() + num_warps);
+  std::vector<int32_t> &warp_begin = S.warp_begin;
+  warp_begin.assign(num_warps + 1, 0);
+  // Pieces go straight into the caller's plan buffer when it surely holds them
+  // (their offset depends only on the warp count; a range adds at most one
+  // piece beyond its segments), else into a scratch array copied at the end.
+  const int64_t off_pieces = (int64_t)sizeof(PlanHeader) + align_up(4ll * (num_warps + 1), 32) +
+                             (int64_t)num_warps * (int64_t)sizeof(WarpHead);
+  const int64_t max_pieces = (int64_t)segs.size() + num_warps;
+  const bool pieces_in_plan =
+      plan && plan_capacity >= off_pieces + max_pieces * (int64_t)sizeof(Piece);
+  if (!pieces_in_plan) S.pieces.resize((size_t)max_pieces);
+  Piece *const pieces =
+      pieces_in_plan ? reinterpret_cast<Piece *>(static_cast<char *>(plan) + off_pieces)
+                     : S.pieces.data();
+  int32_t npieces = 0;
+  // each segment's pieces are consecutive: its first one and how many
+  std::vector<int32_t> &seg_first = S.seg_first, &seg_count = S.seg_count;
+  seg_first.assign(segs.size(), -1);
+  seg_count.assign(segs.size(), 0);
   {
     // Equal cost, not equal blocks: a block costs kBlockCost and starting a
     // segment (its q rows and lengths, a fresh table window) costs kPieceCost, so
@@ -482,7 +522,8 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
     // at least kMinBlocksPerWarp blocks per warp every share holds a block.
     constexpr int64_t kBlockCost = 2, kPieceCost = 6;
     const int64_t total_cost = kBlockCost * total_blocks + kPieceCost * (int64_t)segs.size();
-    std::vector<int64_t> cut(num_warps + 1, total_blocks);  // first block of each warp
+    std::vector<int64_t> &cut = S.cut;  // first block of each warp
+    cut.assign(num_warps + 1, total_blocks);
     cut[0] = 0;
     if (whole_segments) {
       int64_t blk = 0;
@@ -495,16 +536,38 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
       // m * num_warps >= w * total_cost; the midpoints of a segment starting at
       // cost c are c + kPieceCost + kBlockCost * i + kBlockCost / 2, so each
       // boundary is found with one division per warp, not a walk over blocks
+      // (one division per segment: from one warp to the next the numerator grows
+      // by total_cost, so the quotient and remainder are carried forward)
+      const int64_t d2 = kBlockCost * std::max<int64_t>(num_warps, 1);
+      const int64_t tq = total_cost / d2, tr = total_cost % d2;
       int64_t cost = 0, blk = 0;
       int32_t w = 1;
       for (const Segment &g : segs) {
         const int64_t first_mid = cost + kPieceCost + kBlockCost / 2;
         const int64_t last_mid = first_mid + kBlockCost * (g.nb - 1);
+        bool carried = false;  // q, r hold need / d2 and need % d2 for warp w
+        int64_t q = 0, r = 0;
         while (w < num_warps && last_mid * num_warps >= (int64_t)w * total_cost) {
           const int64_t need = (int64_t)w * total_cost - first_mid * num_warps;  // >= 2i * nw
-          int64_t i = need <= 0 ? 0 : (need + kBlockCost * num_warps - 1) / (kBlockCost * num_warps);
+          int64_t i = 0;
+          if (need > 0) {
+            if (!carried) {
+              q = need / d2;
+              r = need % d2;
+              carried = true;
+            }
+            i = q + (r > 0 ? 1 : 0);  // ceil(need / d2)
+          }
           if (i > g.nb - 1) i = g.nb - 1;
           cut[w++] = blk + i;
+          if (carried) {
+            q += tq;
+            r += tr;
+            if (r >= d2) {
+              ++q;
+              r -= d2;
+            }
+          }
         }
         cost += kPieceCost + kBlockCost * g.nb;
         blk += g.nb;
@@ -514,13 +577,13 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
     size_t k = 0;
     int64_t seg_off = 0;  // global block offset of segment k
     for (int32_t w = 0; w < num_warps; ++w) {
-      warp_begin[w] = (int32_t)pieces.size();
+      warp_begin[w] = npieces;
       int64_t a = cut[w], b = cut[w + 1];
       while (a < b) {
         while (seg_off + segs[k].nb <= a) seg_off += segs[k++].nb;
         const Segment &g = segs[k];
         int64_t e = std::min<int64_t>(b, seg_off + g.nb);
-        Piece p;
+        Piece &p = pieces[npieces];
         p.seq = g.seq;
         p.qi0 = g.qi0;
         p.n_q = g.n_q;
@@ -529,31 +592,28 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
         p.kb_end = g.kb0 + (int32_t)(e - seg_off);
         p.part = -1;
         p.q_row0 = cu_q_lens[g.seq] + g.qi0;
-        pieces.push_back(p);
-        piece_seg.push_back((int32_t)k);
+        if (seg_first[k] < 0) seg_first[k] = npieces;
+        ++seg_count[k];
+        ++npieces;
         a = e;
       }
     }
-    warp_begin[num_warps] = (int32_t)pieces.size();
+    warp_begin[num_warps] = npieces;
   }
   // partial slots: every (decode unit, KV head) result whose keys are split over
   // several parts (shared-prefix chunks and suffix pieces) gets one slot per part
   // and a merge group; a result in one part is written directly
-  std::vector<MergeGroup> merges;
+  std::vector<MergeGroup> &merges = S.merges;
+  merges.clear();
   int32_t parts = 0;
   {
-    std::vector<int32_t> seg_first(segs.size(), -1), seg_count(segs.size(), 0);
-    for (size_t i = 0; i < pieces.size(); ++i) {
-      const int32_t k = piece_seg[i];
-      if (seg_first[k] < 0) seg_first[k] = (int32_t)i;
-      ++seg_count[k];
-    }
     // gathered prefix chunks always write partials: their unit gets a merge
     // group even when nothing else splits it
-    std::vector<int32_t> casc_part0(dunits.size() * hkv, -1);
+    std::vector<int32_t> casc_part0(gather.empty() ? 0 : dunits.size() * hkv, -1);
+    static const std::vector<std::array<int32_t, 2>> kNoShared;
     for (size_t u = 0; u < dunits.size(); ++u)
       for (int32_t h = 0; h < hkv; ++h) {
-        const auto &sh = unit_shared[u * hkv + h];
+        const auto &sh = unit_shared.empty() ? kNoShared : unit_shared[u * hkv + h];
         const int32_t k = seg_of[u * hkv + h];
         const int32_t np = k >= 0 ? seg_count[k] : 0;
         const int32_t nc = unit_casc[u];
@@ -568,7 +628,7 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
         m.h = h;
         m.part0 = parts;
         m.nsplit = total;
-        casc_part0[u * hkv + h] = nc > 0 ? parts : -1;
+        if (!casc_part0.empty()) casc_part0[u * hkv + h] = nc > 0 ? parts : -1;
         parts += nc;
         for (const auto &si : sh) sitems[si[0]].rg[si[1]].part = parts++;
         for (int32_t t = 0; t < np; ++t) pieces[seg_first[k] + t].part = parts++;
@@ -755,7 +815,7 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
 
   // ---- sizes
   const PlanOffsets off =
-      plan_offsets(num_warps, (int32_t)pieces.size(), (int32_t)merges.size(),
+      plan_offsets(num_warps, npieces, (int32_t)merges.size(),
                    (int32_t)sitems.size(), (int32_t)ptiles.size(), n_pf_ctas, (int32_t)gather.size());
   std::memset(info, 0, sizeof *info);
   info->num_seqs = num_seqs;
@@ -764,7 +824,7 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   info->head_dim = desc->head_dim;
   info->total_q = num_seqs > 0 ? cu_q_lens[num_seqs] : 0;
   info->num_decode_warps = num_warps;
-  info->num_decode_pieces = (int32_t)pieces.size();
+  info->num_decode_pieces = npieces;
   info->num_merge_groups = (int32_t)merges.size();
   info->num_partials = parts;
   info->num_prefill_tiles = (int32_t)ptiles.size();
@@ -835,7 +895,8 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
         wh.blk[i] = block_tables[(int64_t)wh.first.seq * max_blocks_per_seq + kb];
     }
   }
-  if (!pieces.empty()) std::memcpy(p + off.pieces, pieces.data(), pieces.size() * sizeof(Piece));
+  if (npieces > 0 && !pieces_in_plan)
+    std::memcpy(p + off.pieces, pieces, (size_t)npieces * sizeof(Piece));
   if (!merges.empty())
     std::memcpy(p + off.merges, merges.data(), merges.size() * sizeof(MergeGroup));
   if (!sitems.empty())

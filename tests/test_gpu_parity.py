@@ -323,6 +323,37 @@ def test_attention_on_a_side_stream_with_host_arrays(pkv, cuda_device):
         assert_close(o.cpu(), want, "side stream")
 
 
+def test_bound_step_matches_the_plain_calls(pkv, cuda_device):
+    """A BoundStep (arguments checked once, replayed per step) gives the same
+    pool and output bits as the plain append + attention calls, across two
+    steps whose plans differ (a new plan summary each run)."""
+    dev = cuda_device
+    meta = workloads.build_step("bound", 71, [1, 2, 1], [300, 900, 45], 16, 4, 128)
+    q, k, v, pool = workloads.make_values(meta)
+    qd, kd, vd = q.to(dev), k.to(dev), v.to(dev)
+    cu = torch.from_numpy(meta.cu_q_lens).to(dev)
+    ctx = torch.from_numpy(meta.context_lens).to(dev)
+    bt = torch.from_numpy(meta.block_tables).to(dev)
+    sl = torch.from_numpy(meta.slot_mapping).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    pa, pb = pool.to(dev), pool.to(dev)
+    plan = pkv.plan_step(meta.cu_q_lens, meta.context_lens, 16, pa, block_tables=meta.block_tables)
+    ref = [None, None]
+    out_b = torch.empty_like(qd)
+    b = pkv.BoundStep(kd, vd, sl, qd, cu, ctx, bt, pb, meta.scale, plan, out_b, dev_status=status)
+    for step, sms in enumerate((152, 5)):      # the second step has another plan
+        p2 = pkv.plan_step(meta.cu_q_lens, meta.context_lens, 16, pa, num_sms=sms,
+                           block_tables=meta.block_tables)
+        pkv.paged_kv_append(kd, vd, sl, pa, dev_status=status)
+        ref[step] = pkv.paged_varlen_attention(qd, cu, ctx, bt, pa, meta.scale, plan=p2,
+                                               dev_status=status)
+        plan.info, plan.dev, plan.workspace = p2.info, p2.dev, p2.workspace
+        b.run()
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert torch.equal(out_b, ref[step]) and torch.equal(pa, pb)
+
+
 def test_in_tree_library_is_loaded(pkv):
     import os
     assert os.path.exists(pkv.library_path())
