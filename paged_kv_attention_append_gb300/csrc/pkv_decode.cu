@@ -75,6 +75,11 @@ struct DecodeParams {
   const float2 *ppart_ml;
   int32_t *dev_status;
   int32_t lookahead;           // plan sized for this many further steps (chained decode)
+  int32_t after_prefill;       // launched right behind this call's tensor-core kernel: the
+                               // pool is complete when this kernel starts (that kernel lets
+                               // it launch only after its own wait for the append), so no
+                               // wait precedes the pool reads; every warp waits at its end
+                               // instead, so this kernel completes after that one
   int32_t num_merges;          // all merge groups: decode ones, then prefill ones
   int32_t num_decode_merges;
   int32_t num_partials;
@@ -398,7 +403,7 @@ __device__ __forceinline__ void shared_cta(const CUtensorMap &pool_map, const De
   int win_base = kb0, win_val = -1;
   if (lw == 0 && item_ok && kb0 + lane < kb1) win_val = __ldg(table + kb0 + lane);
   __syncthreads();  // barrier initialisation visible to every warp
-  pdl_wait();
+  if (!p.after_prefill) pdl_wait();
   const int nblk = item_ok ? kb1 - kb0 : 0;
   int issued = 0;
   auto issue = [&](int j) {  // the pair's first warp, whole warp
@@ -505,6 +510,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (lane == 0) prefetch_tmap(&pool_map);  // fetched beside the metadata reads below
   if (blockIdx.x >= p.num_indep_ctas) {  // CTA-uniform: a shared-prefix CTA
     shared_cta<D, NSTAGE>(pool_map, p, smem, warp, lane);
+    if (p.after_prefill) pdl_wait();
     return;
   }
   const int gw = blockIdx.x * kWarps + warp;
@@ -566,8 +572,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int s = 0; s < NSTAGE; ++s) mbar_init(smem_u32(&bars[s]), 1);
     fence_mbar_init();
   }
-  pdl_wait();
-  if (!has_warp || pb >= pe) return;
+  if (!p.after_prefill) pdl_wait();
+  if (!has_warp || pb >= pe) {
+    if (p.after_prefill) pdl_wait();
+    return;
+  }
   __syncwarp();
 
   // ---- producer: walks the warp's pieces block by block.  Called by the whole
@@ -716,6 +725,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int j = consumed; j < issued; ++j)
       mbar_wait(smem_u32(&bars[j % NSTAGE]), (uint32_t)((j / NSTAGE) & 1));
   }
+  if (p.after_prefill) pdl_wait();
 }
 
 // ---- piece epilogue straight from registers: lane (r, c) holds head_dim
@@ -813,6 +823,7 @@ DecodeParams make_params(const AttnArgs &a) {
   p.part_ml = reinterpret_cast<float2 *>(a.part_ml);
   p.num_merges = a.num_merge_groups;
   p.lookahead = a.lookahead;
+  p.after_prefill = a.num_prefill_tiles > 0 && a.num_prefill_ctas > 0 ? 1 : 0;
   p.num_decode_merges = a.num_decode_merges;
   p.num_partials = a.num_partials;
   p.ppart_o = a.ppart_o;

@@ -322,6 +322,11 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
     }
   }
 
+  // Both kernels get every SM: the tensor-core kernel's persistent CTAs take one
+  // SM each, and the split-KV kernel, which it lets launch once the pool is
+  // complete, starts on each SM as soon as that SM's CTA has finished.
+  const int32_t pf_sms = num_sms, dec_sms = num_sms;
+
   // ---- shared-block items: per stream and KV head, its row groups in pairs (one
   // item per pair of warps), the stream cut into equal chunks.  A chunk of B
   // blocks holds two warp slots for about B block steps, as long as a warp range
@@ -330,7 +335,7 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   // a chunk each (a pair streams through a ring twice a warp's depth, so it
   // keeps pace with a somewhat shorter warp range; measured on 4- and 8-token
   // windows: 3/4 beats 1/2 and 1).
-  const int64_t slots = (int64_t)num_sms * kDecodeWarpsPerSm;
+  const int64_t slots = (int64_t)dec_sms * kDecodeWarpsPerSm;
   std::vector<SharedItem> sitems;
   // shared parts of each (decode unit, KV head): (item, warp slot)
   // (allocated only when there are shared streams)
@@ -444,7 +449,7 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
       }
     }
     if (!cpairs.empty()) {
-      const int64_t want = std::max<int64_t>(1, num_sms / (int64_t)cpairs.size());
+      const int64_t want = std::max<int64_t>(1, pf_sms / (int64_t)cpairs.size());
       for (const CPair &cp : cpairs) {
         const Group &g = groups[cp.gi];
         const int32_t kt = g.len / kKeyTileBlocks;
@@ -667,7 +672,7 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
       ntiles += (t.kt1 - t.kt0) * (t.n_q[1] > 0 ? 2 : 1);
     }
     n_pf_ctas = (int32_t)std::max<int64_t>(
-        1, std::min<int64_t>(num_sms, std::max<int64_t>(ntiles / kMinTilesPerCta,
+        1, std::min<int64_t>(pf_sms, std::max<int64_t>(ntiles / kMinTilesPerCta,
                                                         (int64_t)casc_items.size())));
     const int64_t target = (total + n_pf_ctas - 1) / n_pf_ctas;
     std::vector<size_t> order(pairs.size());

@@ -88,7 +88,8 @@ enum {
   B_P_FULL = B_S_FULL + kSBufs,  // + buffer: P(j) written to TMEM (4 warps arrive)
   B_FREE = B_P_FULL + kSBufs,    // + buffer: O += P(j) V_j completed (buffer reusable)
   B_DRAIN = B_FREE + kSBufs,     // + issuer: every MMA it issued completed
-  B_COUNT = B_DRAIN + 2
+  B_GATE = B_DRAIN + 2,          // the K producer's wait for the preceding kernel returned
+  B_COUNT = B_GATE + 1
 };
 
 template <int D>
@@ -239,12 +240,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // launched early behind the preceding kernel: let our dependents launch.  The
-  // plan, q and the step metadata are not written by the kernels this one
-  // follows (the KV append writes only the pool), so barriers, TMEM, the work
-  // items and the q tiles go ahead; the producer waits for the predecessor
-  // before its first pool read, and no other role reads the pool.
-  pdl_trigger();
+  // Launched early behind the preceding kernel.  The plan, q and the step
+  // metadata are not written by the kernels this one follows (the KV append
+  // writes only the pool), so barriers, TMEM, the work items and the q tiles
+  // go ahead; the producers wait for the predecessor before their first pool
+  // read, and no other role reads the pool.  Dependents are let launch only
+  // after that wait (each warp once the K producer's wait has returned): the
+  // split-KV kernel that follows in the same call then runs beside this one on
+  // the other SMs, and finds the pool complete without a wait of its own.
   // this CTA's bin of work items, run one after another, each as one pass per
   // present sub-tile; every barrier keeps counting phases across passes (an
   // item that fails its checks is skipped by every role alike and reported by
@@ -271,6 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(bar(B_DRAIN + 0), 1);
     mbar_init(bar(B_DRAIN + 1), 1);
+    mbar_init(bar(B_GATE), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -425,6 +429,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!waited) {
           pdl_wait();
           waited = true;
+          if (r == 0 && lane == 0) mbar_arrive(bar(B_GATE));
+          pdl_trigger();
         }
         // the physical block of this lane (< 8) in relative tile j: checked once
         // per tile; ids past the context (-1) are zero-filled
@@ -452,7 +458,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // the kernel must not complete before its predecessor (the next kernel's
     // wait covers ours only), even when this CTA had no valid item
-    if (!waited) pdl_wait();
+    if (!waited) {
+      pdl_wait();
+      if (r == 0 && lane == 0) mbar_arrive(bar(B_GATE));
+      pdl_trigger();
+    }
     // our copies still in flight land before the CTA can exit: only the last
     // load of each slot can be pending (a slot is refilled after it was consumed)
     if (lane == 0) {
@@ -461,6 +471,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (r == 0 && npass > 0) mbar_wait(bar(B_Q_FULL), (uint32_t)((npass - 1) & 1));
     }
   } else if (warp == kSWarp || warp == kPvWarp) {
+    // dependents may launch once the pool is known complete (bounded wait)
+    if (mbar_wait(bar(B_GATE), 0)) pdl_trigger();
     // ======================================================== MMA issuers
     // Tile g (counted over the CTA's passes) uses S buffer g % 3 and load g of
     // the K and of the V ring.  The S issuer
@@ -539,6 +551,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp < kSoftmaxWarps) {
     // ======================================================== softmax (4 warps)
+    // dependents may launch once the pool is known complete (bounded wait)
+    if (__all_sync(0xffffffffu, mbar_wait(bar(B_GATE), 0))) pdl_trigger();
     const int quarter = warp;             // TMEM lane quarter
     const int row = quarter * 32 + lane;  // query row = TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;

@@ -426,8 +426,9 @@ def test_prefill_split_kv_and_persistent_items_match_oracle(pkv, cuda_device, nu
     q, k, v, pool = workloads.make_values(meta)
     info, _ = pkv.plan_step(meta.cu_q_lens, meta.context_lens, 8, pkv.pool_desc(pool),
                             num_sms=num_sms, upload=False)
-    assert info.num_prefill_ctas == min(num_sms, info.num_prefill_tiles)
-    if num_sms in (5, 7):
+    # the persistent CTAs take the SMs the split-KV work leaves (at least one)
+    assert 1 <= info.num_prefill_ctas <= min(num_sms, info.num_prefill_tiles)
+    if num_sms in (7, 19):
         assert info.num_prefill_merges > 0      # some query tiles are cut along their keys
     want, _ = oracle.run_step(meta, q, k, v, pool)
     out, _, _ = gpu_step(pkv, meta, q, k, v, pool, cuda_device, num_sms=num_sms)
