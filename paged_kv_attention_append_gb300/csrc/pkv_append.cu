@@ -54,6 +54,9 @@ int launch_append(const void *k, const void *v, const int32_t *slot_mapping, int
   // a grid-stride loop: at most 16 CTAs of 256 threads per SM
   const int64_t cap = 16ll * (device_sm_count() > 0 ? device_sm_count() : 1);
   blocks = blocks < 1 ? 1 : (blocks > cap ? cap : blocks);
+  const cudaError_t pe = desc.head_dim == 128 ? prepare_kernel<append_kernel<128>>(0)
+                                              : prepare_kernel<append_kernel<64>>(0);
+  if (pe != cudaSuccess) return (int)pe;
   profile_begin(PKV_KERNEL_APPEND, stream);
   if (desc.head_dim == 128)
     append_kernel<128><<<(unsigned)blocks, threads, 0, stream>>>(
@@ -99,6 +102,8 @@ int launch_decode_advance(int32_t *context_lens, int32_t *slot_mapping, const in
                           const int32_t *block_tables, int32_t max_blocks_per_seq,
                           int32_t num_seqs, int32_t num_blocks, int32_t *dev_status,
                           pkv_stream stream) {
+  const cudaError_t pe = prepare_kernel<decode_advance_kernel>(0);
+  if (pe != cudaSuccess) return (int)pe;
   decode_advance_kernel<<<(unsigned)((num_seqs + 127) / 128), 128, 0, stream>>>(
       context_lens, slot_mapping, cu_q_lens, block_tables, max_blocks_per_seq, num_seqs,
       num_blocks, dev_status);

@@ -848,8 +848,7 @@ template <int D, int NSTAGE>
 int launch_decode_t(const AttnArgs &a, const CUtensorMap &map) {
   using C = DecodeCfg<D, NSTAGE>;
   auto kern = decode_kernel<D, NSTAGE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::kSmemBytes);
+  cudaError_t e = prepare_kernel<decode_kernel<D, NSTAGE>>(C::kSmemBytes);
   if (e != cudaSuccess) return (int)e;
   const unsigned grid = (unsigned)((a.num_decode_warps + kWarps - 1) / kWarps + a.num_shared_ctas);
   profile_begin(PKV_KERNEL_DECODE, a.stream);
@@ -902,6 +901,9 @@ int launch_merge(const AttnArgs &a, int *launches) {
                           (a.desc.head_dim / 4);
   const dim3 grid((unsigned)((threads + kMergeThreads - 1) / kMergeThreads));
   const bool pdl = !profiling_active();
+  const cudaError_t pe = a.desc.head_dim == 128 ? prepare_kernel<merge_kernel<128>>(0)
+                                                : prepare_kernel<merge_kernel<64>>(0);
+  if (pe != cudaSuccess) return (int)pe;
   profile_begin(PKV_KERNEL_MERGE, a.stream);
   const cudaError_t le =
       a.desc.head_dim == 128

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <utility>
 
 #include "pkv_internal.h"
@@ -192,6 +193,23 @@ __device__ __forceinline__ uint4 ldg128_nc(const void *p) {
 }
 
 // ---------------------------------------------------------------- host: launches
+// Once per kernel and device (not on every launch): the dynamic shared memory
+// the kernel launches with, when it has any.  Returns the first error.  (One
+// table per kernel: Kern is the kernel itself, not its signature.)
+template <auto Kern>
+inline cudaError_t prepare_kernel(int dyn_smem) {
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> done[kMaxDev];  // 0: not yet, 1: set
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  if (dev >= 0 && dev < kMaxDev && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  cudaError_t e = cudaSuccess;
+  if (dyn_smem > 0)
+    e = cudaFuncSetAttribute(Kern, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem);
+  if (e == cudaSuccess && dev >= 0 && dev < kMaxDev) done[dev].store(1, std::memory_order_release);
+  return e;
+}
+
 // Launch `kern` on `stream`; with `pdl` the launch may begin before the
 // preceding kernel of the stream completes (the kernel must call pdl_wait()
 // before it touches that kernel's outputs).

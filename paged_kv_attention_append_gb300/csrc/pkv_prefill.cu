@@ -847,8 +847,7 @@ int launch_prefill_t(const AttnArgs &a, const CUtensorMap &qmap, const CUtensorM
                      const CUtensorMap &qrmap, const CUtensorMap &kvmap) {
   using C = PrefillCfg<D>;
   auto kern = prefill_kernel<D>;
-  cudaError_t e =
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  cudaError_t e = prepare_kernel<prefill_kernel<D>>(C::kSmemBytes);
   if (e != cudaSuccess) return (int)e;
   PrefillParams p;
   p.out = static_cast<__nv_bfloat16 *>(a.out);

@@ -65,6 +65,8 @@ int launch_state_checkpoint(const void *src, const int32_t *dst_slots, int32_t n
   // a grid-stride loop: at most 8 CTAs per SM
   const int64_t cap = 8ll * (device_sm_count() > 0 ? device_sm_count() : 1);
   blocks = blocks < 1 ? 1 : (blocks > cap ? cap : blocks);
+  const cudaError_t pe = prepare_kernel<state_checkpoint_kernel>(0);
+  if (pe != cudaSuccess) return (int)pe;
   profile_begin(PKV_KERNEL_STATE, stream);
   state_checkpoint_kernel<<<(unsigned)blocks, kStateThreads, 0, stream>>>(
       static_cast<const uint4 *>(src), dst_slots, total, vecs_per_row, static_cast<uint4 *>(pool),
