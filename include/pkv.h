@@ -282,13 +282,20 @@ PKV_API pkv_status pkv_decode_advance(int32_t *context_lens, int32_t *slot_mappi
  *   aligned; contents on entry do not matter).  Rows of sequences with
  *   q_len == 0 do not exist.  Accumulation is fp32; out is rounded once to bf16.
  *   Kernels are launched with programmatic stream serialisation: their launch
- *   overlaps the tail of the preceding kernel on the stream.  Each waits for
- *   that kernel to complete (griddepcontrol.wait) before it reads kv_pool or
- *   the workspace; the plan, q, cu_q_lens, context_lens and block_tables are
- *   read before that wait.  A kernel that lets its dependents launch early
+ *   overlaps the tail of the preceding kernel on the stream.  The first kernel
+ *   of the call waits for that preceding kernel to complete
+ *   (griddepcontrol.wait) before it reads kv_pool or the workspace; the plan,
+ *   q, cu_q_lens, context_lens and block_tables are read before that wait.  A
+ *   kernel that lets its dependents launch early
  *   (griddepcontrol.launch_dependents) and runs right before this call must
  *   therefore not write those five: this library's KV append writes only
- *   kv_pool; kernels that do not signal early are simply waited for.
+ *   kv_pool; kernels that do not signal early are simply waited for.  Inside
+ *   the call, when a step has both tensor-core and split-KV work, the
+ *   tensor-core kernel lets the split-KV kernel launch only once its own wait
+ *   has returned, so the split-KV kernel reads the pool without a further wait
+ *   and starts on each SM the tensor-core kernel's persistent CTAs leave; it
+ *   waits at its end instead, so every kernel of the call completes after the
+ *   ones before it (the call as a whole is stream-ordered).
  */
 PKV_API pkv_status pkv_paged_varlen_attention(const void *q, const int32_t *cu_q_lens,
                                       const int32_t *context_lens, const int32_t *block_tables,
