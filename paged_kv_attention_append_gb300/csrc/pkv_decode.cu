@@ -31,6 +31,7 @@
 //    M = max_j m_j, out = sum_j 2^(m_j - M) O_j / sum_j 2^(m_j - M) l_j.
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 
@@ -82,6 +83,7 @@ struct DecodeParams {
                                // instead, so this kernel completes after that one
   int32_t num_merges;          // all merge groups: decode ones, then prefill ones
   int32_t num_decode_merges;
+  int32_t merge_lanes_log2;    // lanes that share one decode row's splits (merge kernel)
   int32_t num_partials;
   int32_t num_warps;
   int32_t num_seqs;
@@ -116,32 +118,38 @@ __device__ __forceinline__ void write_piece(const DecodeParams &p, const Piece &
 //   M = max_j m_j,  out = sum_j 2^(m_j - M) O_j / sum_j 2^(m_j - M) l_j.
 // One thread per (merge group, row, 4 output columns) makes a single pass over
 // the group's splits with a running max (each new split rescales the running
-// sums), unrolled so several splits' loads are in flight at once.  Decode
-// groups come first (partial slots of 16 rows), then prefill groups (slots of
-// 128 rows); both write bf16 rows of out.
+// sums), unrolled so several splits' loads are in flight at once.  A decode row
+// with many splits has them dealt out over 2^merge_lanes_log2 adjacent lanes
+// (split j to lane j mod that count), whose (M, L, O) are then combined by the
+// same rule with xor shuffles, so the loads of all its splits are in flight
+// together.  Decode groups come first (partial slots of 16 rows), then prefill
+// groups (slots of 128 rows); both write bf16 rows of out.
 constexpr int kMergeThreads = 256;
 
-// Combines one row's 4 columns over nsplit partial slots (slot stride `rows`).
-// A split whose m is NaN was written by a piece that found its plan
-// disagreeing with the device tables: the row is then `poisoned` and must not
-// be written.
+// Combines one row's 4 columns over partial slots 0, step, 2 step, .. < nsplit
+// (slot stride `rows`), returning the unnormalised sum with its max M and
+// denominator L.  A split whose m is NaN was written by a piece that found its
+// plan disagreeing with the device tables: the row is then `poisoned` and must
+// not be written.
 template <int D>
 __device__ __forceinline__ float4 merge_row(const float2 *ml, const float4 *po, int nsplit,
-                                            int rows, float &L, bool &poisoned) {
+                                            int step, int rows, float &M, float &L,
+                                            bool &poisoned) {
   constexpr int kChunks = D / 4;
-  float M = -INFINITY;
+  M = -INFINITY;
   L = 0.f;
   poisoned = false;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   constexpr int kBatch = 8;  // splits whose loads are all issued before any is used
-  for (int j0 = 0; j0 < nsplit; j0 += kBatch) {
+  for (int j0 = 0; j0 < nsplit; j0 += kBatch * step) {
     float2 v[kBatch];
     float4 x[kBatch];
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {  // predicated: nothing is loaded past the last split
-      const bool in = j0 + u < nsplit;
-      v[u] = in ? ml[(int64_t)(j0 + u) * rows] : make_float2(-INFINITY, 0.f);
-      x[u] = in ? po[(int64_t)(j0 + u) * rows * kChunks] : make_float4(0.f, 0.f, 0.f, 0.f);
+      const int j = j0 + u * step;
+      const bool in = j < nsplit;
+      v[u] = in ? ml[(int64_t)j * rows] : make_float2(-INFINITY, 0.f);
+      x[u] = in ? po[(int64_t)j * rows * kChunks] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
@@ -182,13 +190,16 @@ __device__ __forceinline__ void poison_piece(const DecodeParams &p, int part, in
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams p) {
   constexpr int kChunks = D / 4;  // float4 chunks of a row
-  const int64_t t = (int64_t)blockIdx.x * kMergeThreads + threadIdx.x;
-  // decode groups, then prefill groups
+  const int64_t t0 = (int64_t)blockIdx.x * kMergeThreads + threadIdx.x;
+  // decode groups (2^lanes_log2 lanes per row and chunk), then prefill groups
   const int n_dg = p.num_decode_merges;
-  const int64_t n_dec = (int64_t)n_dg * kRowsPerTile * kChunks;
-  const bool dec = t < n_dec;
+  const int lanes_log2 = p.merge_lanes_log2;
+  const int64_t n_dec = ((int64_t)n_dg * kRowsPerTile * kChunks) << lanes_log2;
+  const bool dec = t0 < n_dec;
+  const int S = dec ? 1 << lanes_log2 : 1;
+  const int sub = dec ? (int)(t0 & (S - 1)) : 0;
   const int rows = dec ? kRowsPerTile : kPrefillRows;
-  const int64_t tt = dec ? t : t - n_dec;
+  const int64_t tt = dec ? t0 >> lanes_log2 : t0 - n_dec;
   const int64_t gi = tt / (rows * kChunks);
   const int rem = (int)(tt % (rows * kChunks));
   const int row = rem / kChunks, ch = rem % kChunks;
@@ -198,6 +209,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
   MergeGroup g;
   if (in) g = p.merges[dec ? gi : p.num_decode_merges + gi];
   pdl_wait();  // the partials are complete and visible
+  // every lane of a row's lane group takes the same exits (they depend on the
+  // group, row and chunk only)
   if (!in) return;
   const int G = p.group;
   const int nrows = dec ? g.n_q * G : g.n_q;
@@ -205,14 +218,38 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
       g.kind != (dec ? 0 : 1) || g.q_row0 < 0 ||
       g.q_row0 + (dec ? g.n_q : nrows) > p.total_q)
     return;
-  const float2 *ml = (dec ? p.part_ml : p.ppart_ml) + (int64_t)g.part0 * rows + row;
-  const float4 *po = reinterpret_cast<const float4 *>((dec ? p.part_o : p.ppart_o) +
-                                                      ((int64_t)g.part0 * rows + row) * D) +
-                     ch;
-  float L;
+  const int64_t slot0 = (int64_t)g.part0 + sub;  // this lane's first split
+  const float2 *ml = (dec ? p.part_ml : p.ppart_ml) + slot0 * rows + row;
+  const float4 *po =
+      reinterpret_cast<const float4 *>((dec ? p.part_o : p.ppart_o) + (slot0 * rows + row) * D) +
+      ch;
+  float M, L;
   bool poisoned;
-  const float4 acc = merge_row<D>(ml, po, g.nsplit, rows, L, poisoned);
-  if (poisoned) return;
+  float4 acc = merge_row<D>(ml, po, g.nsplit - sub, S, rows, M, L, poisoned);
+  if (S > 1) {
+    // lanes sub and sub ^ o hold disjoint sets of the row's splits: combine
+    const unsigned mask = ((1u << S) - 1u) << ((threadIdx.x & 31) & ~(S - 1));
+    for (int o = 1; o < S; o <<= 1) {
+      const float Mo = __shfl_xor_sync(mask, M, o);
+      const float Lo = __shfl_xor_sync(mask, L, o);
+      float4 ao;
+      ao.x = __shfl_xor_sync(mask, acc.x, o);
+      ao.y = __shfl_xor_sync(mask, acc.y, o);
+      ao.z = __shfl_xor_sync(mask, acc.z, o);
+      ao.w = __shfl_xor_sync(mask, acc.w, o);
+      poisoned = __shfl_xor_sync(mask, (int)poisoned, o) != 0 || poisoned;
+      const float mn = fmaxf(M, Mo);
+      const float a = M == -INFINITY ? 0.f : fast_exp2(M - mn);
+      const float b = Mo == -INFINITY ? 0.f : fast_exp2(Mo - mn);
+      L = L * a + Lo * b;
+      acc.x = acc.x * a + ao.x * b;
+      acc.y = acc.y * a + ao.y * b;
+      acc.z = acc.z * a + ao.z * b;
+      acc.w = acc.w * a + ao.w * b;
+      M = mn;
+    }
+  }
+  if (poisoned || sub != 0) return;
   const int64_t tok = g.q_row0 + (dec ? row / G : row);
   const int hq = dec ? g.h * G + row % G : g.h;
   store_row4(p.out + (tok * p.num_q_heads + hq) * D + 4 * ch, acc, L);
@@ -825,6 +862,7 @@ DecodeParams make_params(const AttnArgs &a) {
   p.lookahead = a.lookahead;
   p.after_prefill = a.num_prefill_tiles > 0 && a.num_prefill_ctas > 0 ? 1 : 0;
   p.num_decode_merges = a.num_decode_merges;
+  p.merge_lanes_log2 = 0;
   p.num_partials = a.num_partials;
   p.ppart_o = a.ppart_o;
   p.ppart_ml = reinterpret_cast<const float2 *>(a.ppart_ml);
@@ -896,21 +934,34 @@ int launch_decode(const AttnArgs &a, int *launches) {
 
 int launch_merge(const AttnArgs &a, int *launches) {
   if (a.num_merge_groups <= 0) return 0;
-  const int64_t threads = ((int64_t)a.num_decode_merges * kRowsPerTile +
-                           (int64_t)(a.num_merge_groups - a.num_decode_merges) * kPrefillRows) *
-                          (a.desc.head_dim / 4);
+  // lanes per decode row: enough that a group of the average split count has
+  // all its splits' loads in one batch of 8 per lane (1, 2, 4 or 8 lanes), as
+  // long as the decode threads stay within about one resident wave (many
+  // groups already keep every SM busy; more threads would only queue)
+  const int64_t chunks = a.desc.head_dim / 4;
+  int lanes_log2 = 0;
+  if (a.num_decode_merges > 0) {
+    const int64_t avg = ((int64_t)a.num_partials + a.num_decode_merges - 1) / a.num_decode_merges;
+    const int64_t budget = (int64_t)std::max(device_sm_count(), 1) * 1024;
+    const int64_t base = (int64_t)a.num_decode_merges * kRowsPerTile * chunks;
+    while (lanes_log2 < 3 && avg > (8ll << lanes_log2) && (base << (lanes_log2 + 1)) <= budget)
+      ++lanes_log2;
+  }
+  const int64_t threads =
+      (((int64_t)a.num_decode_merges * kRowsPerTile * chunks) << lanes_log2) +
+      (int64_t)(a.num_merge_groups - a.num_decode_merges) * kPrefillRows * chunks;
   const dim3 grid((unsigned)((threads + kMergeThreads - 1) / kMergeThreads));
   const bool pdl = !profiling_active();
   const cudaError_t pe = a.desc.head_dim == 128 ? prepare_kernel<merge_kernel<128>>(0)
                                                 : prepare_kernel<merge_kernel<64>>(0);
   if (pe != cudaSuccess) return (int)pe;
+  DecodeParams mp = make_params(a);
+  mp.merge_lanes_log2 = lanes_log2;
   profile_begin(PKV_KERNEL_MERGE, a.stream);
   const cudaError_t le =
       a.desc.head_dim == 128
-          ? launch_kernel(merge_kernel<128>, grid, dim3(kMergeThreads), 0, a.stream, pdl,
-                          make_params(a))
-          : launch_kernel(merge_kernel<64>, grid, dim3(kMergeThreads), 0, a.stream, pdl,
-                          make_params(a));
+          ? launch_kernel(merge_kernel<128>, grid, dim3(kMergeThreads), 0, a.stream, pdl, mp)
+          : launch_kernel(merge_kernel<64>, grid, dim3(kMergeThreads), 0, a.stream, pdl, mp);
   profile_end(PKV_KERNEL_MERGE, a.stream);
   const int e = le != cudaSuccess ? (int)le : (int)cudaGetLastError();
   if (!e) {

@@ -45,6 +45,13 @@
 //              TMEM; so after a pass's first tile the exponentials are taken
 //              against the current reference with the row max found in the
 //              same sweep, and a tile whose max moved the reference is redone.
+// A pass ends with O / l.  For a whole 128-token sub-tile the softmax warps
+// write it as bf16 into a V-ring slot that the V producer leaves empty after
+// that pass's tiles (the next pass's first V tiles are not needed before this
+// output is written), and thread 0 stores it with one bulk tensor store per
+// 64-column half; the slot returns to the producer a tile later.  Shorter
+// sub-tiles store their rows directly, and split or gathered ones write fp32
+// partials for the merge; neither takes a slot.
 // TMEM holds three S buffers and O (3 x 128 + D <= 512 columns), so S(j+1) and
 // S(j+2) are computed while the softmax of tile j runs; S(j+3) reuses the
 // buffer of S(j) once O += P(j) V_j has read P(j).  Only the softmax and the
@@ -89,7 +96,8 @@ enum {
   B_FREE = B_P_FULL + kSBufs,    // + buffer: O += P(j) V_j completed (buffer reusable)
   B_DRAIN = B_FREE + kSBufs,     // + issuer: every MMA it issued completed
   B_GATE = B_DRAIN + 2,          // the K producer's wait for the preceding kernel returned
-  B_COUNT = B_GATE + 1
+  B_STAGED = B_GATE + 1,         // a pass's output is in its staging slot (4 warps arrive)
+  B_COUNT = B_STAGED + 1
 };
 
 template <int D>
@@ -229,12 +237,28 @@ __device__ __forceinline__ ItemMeta load_item(const PrefillParams &p, int it) {
   return m;
 }
 
-template <int D>
+// Whether pass x of an item writes its output through a staging slot: a whole
+// 128-token sub-tile of contiguous tokens whose keys are not split, in the
+// kernel instance built with staging.  Every role evaluates it alike, so all
+// agree on the V ring's staging indices.
+template <bool kStage>
+__device__ __forceinline__ bool stages_output(const ItemMeta &m, int x) {
+  const int nq = x ? m.t.n_q[1] : m.t.n_q[0];
+  const int part = x ? m.t.part[1] : m.t.part[0];
+  return kStage && !m.gathered && part < 0 && nq == kPrefillRows;
+}
+
+// kStage: whole sub-tiles leave through a staging slot and bulk tensor stores
+// (the instance for steps without gathered sub-tiles); without it every output
+// row is stored directly, which keeps the gathered sub-tiles' code as lean as
+// before.  Both compute the same result.
+template <int D, bool kStage>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap q_map,
                    const __grid_constant__ CUtensorMap qg_map,
                    const __grid_constant__ CUtensorMap qr_map,
-                   const __grid_constant__ CUtensorMap kv_map, const PrefillParams p) {
+                   const __grid_constant__ CUtensorMap kv_map,
+                   const __grid_constant__ CUtensorMap o_map, const PrefillParams p) {
   using C = PrefillCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -275,6 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(B_DRAIN + 0), 1);
     mbar_init(bar(B_DRAIN + 1), 1);
     mbar_init(bar(B_GATE), 1);
+    mbar_init(bar(B_STAGED), kSoftmaxWarps);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -313,6 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&q_map);
         prefetch_tmap(&qg_map);
         prefetch_tmap(&qr_map);
+        prefetch_tmap(&o_map);
       }
       prefetch_tmap(&kv_map);
     }
@@ -454,6 +480,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           good = load_tile(m.t.h, tile_phys(j));
         }
+        // after a pass that stages its output, the V ring's next index holds no
+        // tile: it is that output's staging slot.  Its FULL phase completes
+        // here, once its previous occupant was released; the softmax warps
+        // release it (EMPTY).
+        if (good && r == 1 && stages_output<kStage>(m, x)) {
+          const int n = nld, s = n % C::kSlots;
+          if (n >= C::kSlots &&
+              !__all_sync(0xffffffffu, mbar_wait(bar(B_EMPTY + kMaxSlots + s),
+                                                 (uint32_t)(((n / C::kSlots) - 1) & 1)))) {
+            if (lane == 0) fail();
+            good = false;
+            break;
+          }
+          if (lane == 0) mbar_arrive(bar(B_FULL + kMaxSlots + s));
+          __syncwarp();
+          ++nld;
+        }
       }
     }
     // the kernel must not complete before its predecessor (the next kernel's
@@ -474,9 +517,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // dependents may launch once the pool is known complete (bounded wait)
     if (mbar_wait(bar(B_GATE), 0)) pdl_trigger();
     // ======================================================== MMA issuers
-    // Tile g (counted over the CTA's passes) uses S buffer g % 3 and load g of
-    // the K and of the V ring.  The S issuer
-    // runs S(g) once K_j landed and O += P(g-3) V has completed (it read P(g-3)
+    // Tile g (counted over the CTA's passes) uses S buffer g % 3, load g of the
+    // K ring and index g + (passes before it) of the V ring, whose index after
+    // each pass is that pass's output staging slot.  The S issuer runs S(g) once K_j landed and O += P(g-3) V has completed (it read P(g-3)
     // from the same buffer); the PV issuer runs O += P(g) V_j once P(g) is in
     // TMEM and V_j landed.  Consecutive PV MMAs accumulate into O in issue
     // order; the softmax rescales O only after waiting for the previous PV.
@@ -495,6 +538,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       const uint32_t sq = smem_u32(smem + C::kOffQ);
       int npass = 0, g = 0;  // passes; tiles
+      int nst = 0;           // passes that staged their output (V ring indices)
       bool good = true;
       for (int it = it0; it < it1 && good; ++it) {
         const ItemMeta m = load_item(p, it);
@@ -525,9 +569,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (good) tc::commit(bar(B_Q_EMPTY));  // every S of the pass issued
           } else {
             for (int j = 0; good && j < ntx; ++j, ++g) {
-              const int s = g % C::kSlots, b = g % kSBufs;
+              // V ring index: a staging index follows each earlier staged pass
+              const int vi = g + nst, s = vi % C::kSlots, b = g % kSBufs;
               if (!wait(B_P_FULL + b, g / kSBufs)) good = false;
-              else if (!wait(B_FULL + kMaxSlots + s, g / C::kSlots)) good = false;
+              else if (!wait(B_FULL + kMaxSlots + s, vi / C::kSlots)) good = false;
               if (!good) break;
               tc::fence_after_sync();
               const uint32_t sv = smem_u32(smem + C::kOffRing + (C::kSlots + s) * C::kSlotBytes);
@@ -542,6 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           ++npass;
+          if (stages_output<kStage>(m, x)) ++nst;
         }
       }
       // every MMA issued so far completes before TMEM is released
@@ -558,7 +604,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
     const uint32_t to = t_o + lane_off;
-    int g = 0;  // tiles of earlier passes
+    int g = 0;        // tiles of earlier passes
+    int nstaged = 0;  // passes whose output went through a staging slot
+    int pend = -1;    // thread 0: V slot whose staged output a bulk store still reads
     bool good = true;
     for (int it = it0; it < it1 && good; ++it) {
       const ItemMeta m = load_item(p, it);
@@ -705,6 +753,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(B_P_FULL + b));
+          if (pend >= 0) {
+            // thread 0: the previous pass's staged output is read out by now
+            // (one tile later); its V slot goes back to the producer
+            bulk_wait_read();
+            mbar_arrive(bar(B_EMPTY + kMaxSlots + pend));
+            pend = -1;
+          }
         }
         if (!good) break;
         // ---- epilogue: O / l, once the pass's last O += P V completed.  The
@@ -781,25 +836,73 @@ __global__ void __launch_bounds__(kThreads, 1)
           continue;
         }
         const float inv = l > 0.f ? 1.f / l : 0.f;
-        __nv_bfloat16 *orow = p.out + ((int64_t)out_row * p.num_q_heads + hq) * D;
+        auto pack8 = [&](const uint32_t *o) {
+          uint4 w;
+          w.x = pack_bf16x2(__uint_as_float(o[0]) * inv, __uint_as_float(o[1]) * inv);
+          w.y = pack_bf16x2(__uint_as_float(o[2]) * inv, __uint_as_float(o[3]) * inv);
+          w.z = pack_bf16x2(__uint_as_float(o[4]) * inv, __uint_as_float(o[5]) * inv);
+          w.w = pack_bf16x2(__uint_as_float(o[6]) * inv, __uint_as_float(o[7]) * inv);
+          return w;
+        };
+        if (stages_output<kStage>(m, x)) {
+          // a whole sub-tile: its rows go as bf16 into the staging slot (the V
+          // ring's index after this pass's tiles) in the layout of the output
+          // tensor map's 128-byte swizzle (16-byte piece c of row r at
+          // r * 128 + (c ^ (r & 7)) * 16 of its 64-column half), and thread 0
+          // writes them out with one bulk tensor store per half.  The slot's
+          // previous occupant was released long before (bounded wait).
+          const int vs = g + nstaged, ss = vs % C::kSlots;
+          if (vs >= C::kSlots &&
+              !__all_sync(0xffffffffu, mbar_wait(bar(B_EMPTY + kMaxSlots + ss),
+                                                 (uint32_t)(((vs / C::kSlots) - 1) & 1)))) {
+            fail();
+            break;
+          }
+          uint8_t *stage = smem + C::kOffRing + (C::kSlots + ss) * C::kSlotBytes;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          if (row < n_q) {
-            uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
+          for (int hh = 0; hh < C::kHalves; ++hh)
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
-              uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(ov[c][8 * v4 + 0]) * inv, __uint_as_float(ov[c][8 * v4 + 1]) * inv);
-              w.y = pack_bf16x2(__uint_as_float(ov[c][8 * v4 + 2]) * inv, __uint_as_float(ov[c][8 * v4 + 3]) * inv);
-              w.z = pack_bf16x2(__uint_as_float(ov[c][8 * v4 + 4]) * inv, __uint_as_float(ov[c][8 * v4 + 5]) * inv);
-              w.w = pack_bf16x2(__uint_as_float(ov[c][8 * v4 + 6]) * inv, __uint_as_float(ov[c][8 * v4 + 7]) * inv);
-              dst[v4] = w;
+            for (int c = 0; c < 8; ++c)
+              *reinterpret_cast<uint4 *>(stage + hh * C::kQHalfBytes + row * 128 +
+                                         ((c ^ (row & 7)) << 4)) =
+                  pack8(&ov[2 * hh + c / 4][8 * (c % 4)]);
+          tc::fence_proxy_async_smem();  // visible to the bulk copy
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(B_STAGED));
+          const uint32_t staged_parity = (uint32_t)(nstaged++ & 1);
+          if (warp == 0) {
+            bool ok = true;
+            if (lane == 0) {
+              ok = mbar_wait(bar(B_STAGED), staged_parity);
+              if (ok) {
+#pragma unroll
+                for (int hh = 0; hh < C::kHalves; ++hh)
+                  tma_store_3d(&o_map, smem_u32(stage + hh * C::kQHalfBytes), hh * 64, hq,
+                               out_row);
+                bulk_commit();
+                pend = ss;  // released once the store has read it, one tile later
+              } else {
+                fail();
+              }
+            }
+            if (!__all_sync(0xffffffffu, ok)) break;
+          }
+        } else {
+          __nv_bfloat16 *orow = p.out + ((int64_t)out_row * p.num_q_heads + hq) * D;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            if (row < n_q) {
+              uint4 *dst = reinterpret_cast<uint4 *>(orow + 32 * c);
+#pragma unroll
+              for (int v4 = 0; v4 < 4; ++v4) dst[v4] = pack8(&ov[c][8 * v4]);
             }
           }
         }
         tc::fence_before_sync();
       }
     }
+    // the last staged output has been written before the CTA exits
+    if (warp == 0 && lane == 0) bulk_wait();
   }
 
   // ---- teardown: every role has drained its own asynchronous work
@@ -826,8 +929,9 @@ EncodeTiledFn encoder() {
   return reinterpret_cast<EncodeTiledFn>(ptr);
 }
 
-// 3-D view of q: [total_q][Hq][D], box = `tokens` tokens x `heads` heads x 64
-// elements (128 x 1 for contiguous sub-tiles, 1 x G for gathered ones).
+// 3-D view of q (or of out, which has its shape): [total_q][Hq][D], box =
+// `tokens` tokens x `heads` heads x 64 elements (128 x 1 for contiguous
+// sub-tiles, 1 x G for gathered ones).
 int make_q_map(CUtensorMap *map, const void *q, int64_t total_q, int hq, int d, int heads,
                int tokens) {
   EncodeTiledFn enc = encoder();
@@ -844,10 +948,15 @@ int make_q_map(CUtensorMap *map, const void *q, int64_t total_q, int hq, int d, 
 
 template <int D>
 int launch_prefill_t(const AttnArgs &a, const CUtensorMap &qmap, const CUtensorMap &qgmap,
-                     const CUtensorMap &qrmap, const CUtensorMap &kvmap) {
+                     const CUtensorMap &qrmap, const CUtensorMap &kvmap,
+                     const CUtensorMap &omap) {
   using C = PrefillCfg<D>;
-  auto kern = prefill_kernel<D>;
-  cudaError_t e = prepare_kernel<prefill_kernel<D>>(C::kSmemBytes);
+  // staging pays on contiguous prefill; the gathered sub-tiles' passes run
+  // faster in the instance without it
+  const bool stage = a.num_gather_rows == 0;
+  auto kern = stage ? prefill_kernel<D, true> : prefill_kernel<D, false>;
+  cudaError_t e = stage ? prepare_kernel<prefill_kernel<D, true>>(C::kSmemBytes)
+                        : prepare_kernel<prefill_kernel<D, false>>(C::kSmemBytes);
   if (e != cudaSuccess) return (int)e;
   PrefillParams p;
   p.out = static_cast<__nv_bfloat16 *>(a.out);
@@ -875,7 +984,7 @@ int launch_prefill_t(const AttnArgs &a, const CUtensorMap &qmap, const CUtensorM
   p.scale_log2 = a.scale * 1.4426950408889634f;
   profile_begin(PKV_KERNEL_PREFILL, a.stream);
   e = launch_kernel(kern, dim3((unsigned)a.num_prefill_ctas), dim3(kThreads), C::kSmemBytes,
-                    a.stream, !profiling_active(), qmap, qgmap, qrmap, kvmap, p);
+                    a.stream, !profiling_active(), qmap, qgmap, qrmap, kvmap, omap, p);
   profile_end(PKV_KERNEL_PREFILL, a.stream);
   return e != cudaSuccess ? (int)e : (int)cudaGetLastError();
 }
@@ -884,7 +993,7 @@ int launch_prefill_t(const AttnArgs &a, const CUtensorMap &qmap, const CUtensorM
 
 int launch_prefill(const AttnArgs &a, int *launches) {
   if (a.num_prefill_tiles <= 0 || a.num_prefill_ctas <= 0) return 0;
-  CUtensorMap qmap, qgmap, qrmap, kvmap;
+  CUtensorMap qmap, qgmap, qrmap, kvmap, omap;
   const int group = a.num_q_heads / a.desc.num_kv_heads;
   int e = make_q_map(&qmap, a.q, a.total_q, a.num_q_heads, a.desc.head_dim, 1, kPrefillRows);
   if (e) return e;
@@ -895,8 +1004,11 @@ int launch_prefill(const AttnArgs &a, int *launches) {
   if (e) return e;
   e = make_pool_map(&kvmap, a.kv_pool, a.desc);
   if (e) return e;
-  e = a.desc.head_dim == 128 ? launch_prefill_t<128>(a, qmap, qgmap, qrmap, kvmap)
-                             : launch_prefill_t<64>(a, qmap, qgmap, qrmap, kvmap);
+  // out has q's shape: whole 128-token sub-tiles are stored through this map
+  e = make_q_map(&omap, a.out, a.total_q, a.num_q_heads, a.desc.head_dim, 1, kPrefillRows);
+  if (e) return e;
+  e = a.desc.head_dim == 128 ? launch_prefill_t<128>(a, qmap, qgmap, qrmap, kvmap, omap)
+                             : launch_prefill_t<64>(a, qmap, qgmap, qrmap, kvmap, omap);
   if (!e) {
     ++*launches;
     count_launches(1);

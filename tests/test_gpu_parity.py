@@ -435,6 +435,28 @@ def test_prefill_split_kv_and_persistent_items_match_oracle(pkv, cuda_device, nu
     assert_close(out, want, f"split prefill on {num_sms} SMs")
 
 
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("num_sms", [1, 3, 152])
+def test_prefill_whole_sub_tiles_short_passes_match_oracle(pkv, cuda_device, d, num_sms):
+    """Whole 128-token sub-tiles leave the tensor-core kernel through a V-ring
+    slot and a bulk tensor store, ragged ones row by row.  Passes of one to
+    three key tiles, many of them on one CTA (one or three SMs), put the
+    output's staging slots next to one another in the ring.  Every row of the
+    step (whole, ragged and decode) is checked against the oracle; out starts
+    as NaN canaries, so a row left unwritten fails, and the guard rows around
+    out show any store past its ends."""
+    ql = [128, 128, 256, 128, 200, 128, 1]
+    cl = [128, 200, 256, 300, 260, 384, 90]
+    meta = workloads.build_step("whole_tiles", 17 + d + num_sms, ql, cl, 8, 2, d)
+    q, k, v, pool = workloads.make_values(meta)
+    info, _ = pkv.plan_step(meta.cu_q_lens, meta.context_lens, 8, pkv.pool_desc(pool),
+                            num_sms=num_sms, upload=False)
+    assert info.num_prefill_tiles > 0
+    want, _ = oracle.run_step(meta, q, k, v, pool)
+    out, _, _ = gpu_step(pkv, meta, q, k, v, pool, cuda_device, num_sms=num_sms)
+    assert_close(out, want, f"whole sub-tiles D={d} on {num_sms} SMs")
+
+
 # ------------------------------------------------------------------ state-row checkpoint
 
 @pytest.mark.parametrize("num_slots,row_bytes,n", [
