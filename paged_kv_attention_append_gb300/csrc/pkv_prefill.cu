@@ -49,7 +49,8 @@
 // write it as bf16 into a V-ring slot that the V producer leaves empty after
 // that pass's tiles (the next pass's first V tiles are not needed before this
 // output is written), and thread 0 stores it with one bulk tensor store per
-// 64-column half; the slot returns to the producer a tile later.  Shorter
+// 64-column half; the slot returns to the producer once the copy has read it.
+// Shorter
 // sub-tiles store their rows directly, and split or gathered ones write fp32
 // partials for the merge; neither takes a slot.
 // TMEM holds three S buffers and O (3 x 128 + D <= 512 columns), so S(j+1) and
@@ -606,7 +607,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t to = t_o + lane_off;
     int g = 0;        // tiles of earlier passes
     int nstaged = 0;  // passes whose output went through a staging slot
-    int pend = -1;    // thread 0: V slot whose staged output a bulk store still reads
     bool good = true;
     for (int it = it0; it < it1 && good; ++it) {
       const ItemMeta m = load_item(p, it);
@@ -753,13 +753,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(bar(B_P_FULL + b));
-          if (pend >= 0) {
-            // thread 0: the previous pass's staged output is read out by now
-            // (one tile later); its V slot goes back to the producer
-            bulk_wait_read();
-            mbar_arrive(bar(B_EMPTY + kMaxSlots + pend));
-            pend = -1;
-          }
         }
         if (!good) break;
         // ---- epilogue: O / l, once the pass's last O += P V completed.  The
@@ -880,7 +873,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                   tma_store_3d(&o_map, smem_u32(stage + hh * C::kQHalfBytes), hh * 64, hq,
                                out_row);
                 bulk_commit();
-                pend = ss;  // released once the store has read it, one tile later
+                // the slot goes back to the V producer once the copy has read
+                // it (waiting here keeps this release out of the tile loop)
+                bulk_wait_read();
+                mbar_arrive(bar(B_EMPTY + kMaxSlots + ss));
               } else {
                 fail();
               }
