@@ -400,7 +400,8 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   // ---- gathered sub-tiles (tc groups): per group and KV head, the members'
   // query tokens in sub-tiles of up to 128 / G tokens (G rows each), neighbours
   // paired; every pair is cut along the prefix's key tiles into nc equal chunks,
-  // nc chosen so the items about fill the SMs (at least 2 key tiles each)
+  // nc chosen so the items about fill their share of the SMs (at least 2 key
+  // tiles each)
   std::vector<GatherRow> gather;          // part0 filled once partial slots are known
   std::vector<int32_t> gather_uh;         // (decode unit * hkv + KV head) of each entry
   std::vector<PrefillTile> casc_items;    // already cut along keys
@@ -449,7 +450,21 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
       }
     }
     if (!cpairs.empty()) {
-      const int64_t want = std::max<int64_t>(1, pf_sms / (int64_t)cpairs.size());
+      // The items take a share of the SMs; the split-KV kernel streams the
+      // step's own blocks on the rest meanwhile.  Share = prefix tile passes /
+      // (tile passes + streamed block-heads / 32), at least one half: one tile
+      // pass weighed as 32 block-heads put both shared-prefix workloads at
+      // their measured optimum (96 and 80 of 152 SMs).  Integer arithmetic, so
+      // every host plans alike.
+      int64_t pf_work = 0;
+      for (const CPair &cp : cpairs) pf_work += (int64_t)cp.nsub * (groups[cp.gi].len / kKeyTileBlocks);
+      const int64_t ncp = (int64_t)cpairs.size();
+      int64_t num = 32 * pf_work, den = 32 * pf_work + total_blocks;  // share = num / den
+      if (2 * num < den) {
+        num = 1;
+        den = 2;
+      }
+      const int64_t want = std::max<int64_t>(1, (2 * num * pf_sms + den * ncp) / (2 * den * ncp));
       for (const CPair &cp : cpairs) {
         const Group &g = groups[cp.gi];
         const int32_t kt = g.len / kKeyTileBlocks;
