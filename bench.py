@@ -366,11 +366,22 @@ class StepBench:
         self.plan = pkv.StepPlan(self.info, self.host_plan, dev)
 
     def host_plan_us(self, reps=50):
+        """Host planning per step as the e2e loop does it: one bound planner call
+        (pkv_plan_step_ex) over the step's int32 arrays into a reused buffer."""
+        import numpy as np
+        import torch
         m = self.meta
+        cu = np.ascontiguousarray(m.cu_q_lens, dtype=np.int32)
+        ctx = np.ascontiguousarray(m.context_lens, dtype=np.int32)
+        bt = np.ascontiguousarray(m.block_tables, dtype=np.int32)
+        out = np.zeros(((int(self.info.plan_bytes) + 4095) // 4096 + 1) * 1024, dtype=np.int32)
+        planner = self.pkv.BoundPlan(
+            cu, ctx, m.num_q_heads, self.pool, out, chain_steps=self.chain_arg, block_tables=bt,
+            num_sms=torch.cuda.get_device_properties(self.dev).multi_processor_count)
+        planner.run()
         t0 = time.perf_counter()
         for _ in range(reps):
-            self.pkv.plan_step(m.cu_q_lens, m.context_lens, m.num_q_heads, self.pool, upload=False,
-                               chain_steps=self.chain_arg, block_tables=m.block_tables)
+            planner.run()
         return (time.perf_counter() - t0) / reps * 1e6
 
     def step(self):
@@ -587,30 +598,33 @@ class StepBench:
         plan_e2e = pkv.StepPlan(info, self.host_plan, dev)
         plan_e2e.dev = dplan.view(torch.uint8)
         d2h = sum(o.numel() * o.element_size() for o in outs_h)
-        # every step reuses the same device buffers: their arguments are bound once
+        # every step reuses the same host and device buffers: the planner call,
+        # the copies and the kernel calls have their arguments bound once
         bound = [pkv.BoundStep(dk, dv, ds, dq, dcu, dctx, dbt, self.pool, meta.scale, plan_e2e,
                                self.outs[t], dev_status=self.status, stream=stream)
                  for t, (dq, dk, dv) in enumerate(dvals)]
+        planner = pkv.BoundPlan(cu_np, ctx_np, meta.num_q_heads, self.pool, plan_np,
+                                num_sms=num_sms, chain_steps=self.chain_arg, block_tables=bt_np)
+        up = pkv.BoundCopy(buf_d, buf_h, stream=stream)
+        down = [pkv.BoundCopy(oh, o, stream=stream) for oh, o in zip(outs_h, self.outs)]
         times = []
         with torch.cuda.stream(stream):
             for i in range(args.warmup + args.steps):
                 torch.cuda.synchronize(dev)
                 t0 = time.perf_counter()
                 if split_copy:  # large inputs go up while the host plans
-                    buf_d[:plan_off].copy_(buf_h[:plan_off], non_blocking=True)
-                inf2, hp2 = pkv.plan_step(cu_np, ctx_np, meta.num_q_heads, self.pool, upload=False,
-                                          chain_steps=self.chain_arg, block_tables=bt_np,
-                                          num_sms=num_sms, out=plan_np)
-                n = (plan_off + hp2.nbytes + 15) // 16 * 16
+                    up.run(plan_off)
+                inf2, plan_nb = planner.run()
+                n = (plan_off + plan_nb + 15) // 16 * 16
                 n0 = plan_off if split_copy else 0
-                buf_d[n0:n].copy_(buf_h[n0:n], non_blocking=True)
+                up.run(n - n0, n0)
                 plan_e2e.info = inf2
                 for t, b in enumerate(bound):
                     b.run()
                     if t + 1 < self.nch:
                         pkv.decode_advance(dctx, ds, dcu, dbt, self.pool, dev_status=self.status)
-                for oh, o in zip(outs_h, self.outs):
-                    oh.copy_(o, non_blocking=True)
+                for d in down:
+                    d.run()
                 stream.synchronize()
                 if i >= args.warmup:
                     times.append(time.perf_counter() - t0)

@@ -212,6 +212,19 @@ PKV_API pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *contex
 PKV_API size_t pkv_workspace_size(const pkv_plan_info *info);
 
 /*
+ * Stream-ordered copy of `bytes` bytes from src to dst on `stream`, for moving
+ * a step's inputs and plan up and its output back without leaving this API:
+ * host to device, device to host or device to device, the direction taken from
+ * the pointers (unified addressing).  The call returns once the copy is queued;
+ * it is asynchronous with respect to the host only when the host side is pinned
+ * (page-locked) memory, and the caller keeps both buffers alive and unchanged
+ * until the stream has passed the copy.  bytes == 0: nothing is queued.
+ * Errors: PKV_ERR_RANGE (bytes < 0), PKV_ERR_NULL (a NULL pointer with
+ * bytes > 0), PKV_ERR_CUDA (the runtime refused the copy).
+ */
+PKV_API pkv_status pkv_copy_async(void *dst, const void *src, int64_t bytes, pkv_stream stream);
+
+/*
  * Plan for a chain of `steps` decode steps of the same batch (the vllm-metal
  * page's MLX engine, "Chained greedy decode": several decode steps built into
  * one graph and run with a single sync per chunk).  context_lens are those of

@@ -23,7 +23,8 @@ import torch
 __all__ = [
     "PkvError", "PoolDesc", "PlanInfo", "StepPlan", "build", "library_path", "version",
     "status_string", "kernel_launch_count", "paged_kv_append", "plan_step",
-    "paged_varlen_attention", "DEV_STATUS", "workspace_size", "BoundStep",
+    "paged_varlen_attention", "DEV_STATUS", "workspace_size", "BoundStep", "BoundPlan",
+    "BoundCopy", "copy_async",
 ]
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
@@ -108,6 +109,8 @@ def _load():
             lib.pkv_set_profile_events.restype = i32
             lib.pkv_workspace_size.argtypes = [ctypes.POINTER(PlanInfo)]
             lib.pkv_workspace_size.restype = ctypes.c_size_t
+            lib.pkv_copy_async.argtypes = [P, P, i64, P]
+            lib.pkv_copy_async.restype = i32
             _lib = lib
     return _lib
 
@@ -247,6 +250,53 @@ def workspace_size(info: PlanInfo) -> int:
     return int(_load().pkv_workspace_size(ctypes.byref(info)))
 
 
+def _buffer_span(t):
+    """(address, bytes) of a contiguous tensor or numpy array."""
+    if isinstance(t, torch.Tensor):
+        if not t.is_contiguous():
+            raise ValueError("copy buffers must be contiguous")
+        return t.data_ptr(), t.numel() * t.element_size()
+    a = np.asarray(t)
+    if not a.flags.c_contiguous:
+        raise ValueError("copy buffers must be contiguous")
+    return a.ctypes.data, a.nbytes
+
+
+def copy_async(dst, src, nbytes=None, *, stream=None) -> None:
+    """Queue a copy of nbytes (default: all of src) from src to dst on `stream`
+    (pkv_copy_async): host<->device or device<->device, the direction from the
+    pointers; asynchronous for pinned host memory.  dst and src: contiguous
+    tensors (or numpy arrays on the host side)."""
+    BoundCopy(dst, src, stream=stream).run(nbytes)
+
+
+class BoundCopy:
+    """pkv_copy_async between two fixed buffers with its arguments marshalled
+    once: run(nbytes, offset) copies src[offset : offset + nbytes] to the same
+    byte range of dst on the bound stream (the whole of src by default).  For a
+    loop that moves each step's inputs up and its output back through the same
+    pinned and device buffers."""
+
+    def __init__(self, dst, src, *, stream=None):
+        self._dst, dn = _buffer_span(dst)
+        self._src, sn = _buffer_span(src)
+        self._n = min(dn, sn)
+        dev_t = dst if isinstance(dst, torch.Tensor) and dst.is_cuda else src
+        if not (isinstance(dev_t, torch.Tensor) and dev_t.is_cuda):
+            raise ValueError("one side of the copy must be a CUDA tensor")
+        self._keep = (dst, src)
+        self._stream = ctypes.c_void_p(_stream(stream, dev_t))
+        self._f = _load().pkv_copy_async
+
+    def run(self, nbytes=None, offset: int = 0) -> None:
+        n = self._n - offset if nbytes is None else int(nbytes)
+        if offset < 0 or n < 0 or offset + n > self._n:
+            raise ValueError(f"copy of {n} bytes at {offset} exceeds the bound buffers ({self._n})")
+        st = self._f(self._dst + offset, self._src + offset, n, self._stream)
+        if st:
+            raise PkvError(st, "pkv_copy_async")
+
+
 class StepPlan:
     """Host step metadata plus its device copy and the workspace it needs."""
 
@@ -354,6 +404,63 @@ def plan_step(cu_q_lens, context_lens, num_q_heads: int, kv_pool_or_desc, *, num
     if not upload:
         return info, host
     return StepPlan(info, host, torch.device(device), stream)
+
+
+class BoundPlan:
+    """pkv_plan_step_ex over fixed host arrays with its arguments marshalled once.
+
+    For a serving loop that rewrites the step's metadata in place (e.g. views of
+    one pinned buffer) and plans every step into the same host buffer `out`:
+    run() is one call into the planner; it returns (info, nbytes), info being
+    this object's PlanInfo (overwritten by the next run) and nbytes the plan's
+    size in `out`.  The arrays must be C-contiguous int32 numpy arrays whose
+    shapes stay fixed (their contents may change between runs); the other
+    arguments mean what they mean for plan_step.
+    """
+
+    def __init__(self, cu_q_lens, context_lens, num_q_heads: int, kv_pool_or_desc, out, *,
+                 num_sms=None, chain_steps=None, block_tables=None, prefill_min_q=None):
+        arrays = [("cu_q_lens", cu_q_lens), ("context_lens", context_lens)]
+        if block_tables is not None:
+            arrays.append(("block_tables", block_tables))
+        for name, a in arrays:
+            if not (isinstance(a, np.ndarray) and a.dtype == np.int32 and a.flags.c_contiguous):
+                raise TypeError(f"{name} must be a C-contiguous int32 numpy array")
+        if cu_q_lens.ndim != 1 or context_lens.ndim != 1 or \
+                cu_q_lens.shape[0] != context_lens.shape[0] + 1:
+            raise ValueError("cu_q_lens must have num_seqs + 1 entries and context_lens num_seqs")
+        if block_tables is not None and (block_tables.ndim != 2 or
+                                         block_tables.shape[0] != context_lens.shape[0]):
+            raise ValueError("block_tables must be [num_seqs, max_blocks_per_seq]")
+        buf = out.numpy() if isinstance(out, torch.Tensor) else out
+        if not (isinstance(buf, np.ndarray) and buf.flags.c_contiguous and buf.flags.writeable):
+            raise ValueError("out must be a contiguous writable host buffer")
+        self.desc = (kv_pool_or_desc if isinstance(kv_pool_or_desc, PoolDesc)
+                     else pool_desc(kv_pool_or_desc))
+        if num_sms is None:
+            device = (kv_pool_or_desc.device if isinstance(kv_pool_or_desc, torch.Tensor)
+                      else "cuda")
+            num_sms = (torch.cuda.get_device_properties(torch.device(device)).multi_processor_count
+                       if torch.cuda.is_available() else 152)
+        self.info = PlanInfo()
+        self._keep = (cu_q_lens, context_lens, block_tables, buf)
+        self._out = buf.reshape(-1).view(np.uint8)
+        vp = ctypes.c_void_p
+        self._args = (vp(cu_q_lens.ctypes.data), vp(context_lens.ctypes.data),
+                      ctypes.c_int32(context_lens.shape[0]), ctypes.c_int32(int(num_q_heads)),
+                      ctypes.byref(self.desc), ctypes.c_int32(int(num_sms)),
+                      ctypes.c_int32(1 if chain_steps is None else int(chain_steps)),
+                      vp(None if block_tables is None else block_tables.ctypes.data),
+                      ctypes.c_int32(0 if block_tables is None else block_tables.shape[1]),
+                      ctypes.c_int32(0 if prefill_min_q is None else int(prefill_min_q)),
+                      vp(buf.ctypes.data), ctypes.c_int64(buf.nbytes), ctypes.byref(self.info))
+        self._f = _load().pkv_plan_step_ex
+
+    def run(self):
+        st = self._f(*self._args)
+        if st:
+            raise PkvError(st, "pkv_plan_step_ex")
+        return self.info, (max(int(self.info.plan_bytes), 16) + 15) // 16 * 16
 
 
 def decode_advance(context_lens, slot_mapping, cu_q_lens, block_tables, kv_pool, *,

@@ -236,3 +236,12 @@ extern "C" pkv_status pkv_paged_varlen_attention(
 extern "C" size_t pkv_workspace_size(const pkv_plan_info *info) {
   return info && info->workspace_bytes > 0 ? (size_t)info->workspace_bytes : 0;
 }
+
+extern "C" pkv_status pkv_copy_async(void *dst, const void *src, int64_t bytes, pkv_stream stream) {
+  if (bytes < 0) return PKV_ERR_RANGE;
+  if (bytes == 0) return PKV_OK;
+  if (!dst || !src) return PKV_ERR_NULL;
+  return cudaMemcpyAsync(dst, src, (size_t)bytes, cudaMemcpyDefault, stream) == cudaSuccess
+             ? PKV_OK
+             : PKV_ERR_CUDA;
+}

@@ -124,7 +124,7 @@ __device__ __forceinline__ void write_piece(const DecodeParams &p, const Piece &
 // same rule with xor shuffles, so the loads of all its splits are in flight
 // together.  Decode groups come first (partial slots of 16 rows), then prefill
 // groups (slots of 128 rows); both write bf16 rows of out.
-constexpr int kMergeThreads = 256;
+constexpr int kMergeThreads = 128;
 
 // Combines one row's 4 columns over partial slots 0, step, 2 step, .. < nsplit
 // (slot stride `rows`), returning the unnormalised sum with its max M and

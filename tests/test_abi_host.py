@@ -539,6 +539,46 @@ def test_workspace_size_matches_the_plan_summary(pkv):
     assert lib.pkv_workspace_size(None) == 0
 
 
+@pytest.mark.parametrize("name", ["small_decode", "agent_mixed", "shared_prefix_verify",
+                                  "decode_chain"])
+def test_bound_planner_writes_the_plan_step_bytes(pkv, name):
+    """BoundPlan is argument marshalling only: over the same arrays it writes the
+    bytes plan_step writes, run after run, and follows in-place edits of them."""
+    meta = workloads.make_config(name)
+    desc = pkv.PoolDesc(meta.num_blocks, 16, meta.num_kv_heads, meta.head_dim)
+    cu, ctx = meta.cu_q_lens.astype(np.int32).copy(), meta.context_lens.astype(np.int32).copy()
+    bt = meta.block_tables.astype(np.int32).copy()
+    chain = 3 if name == "decode_chain" else None
+    out = np.zeros(1 << 17, np.int32)
+    bp = pkv.BoundPlan(cu, ctx, meta.num_q_heads, desc, out, num_sms=152, block_tables=bt,
+                       chain_steps=chain)
+    for step in range(2):
+        info, nb = bp.run()
+        want_info, want = pkv.plan_step(cu, ctx, meta.num_q_heads, desc, upload=False,
+                                        num_sms=152, block_tables=bt, chain_steps=chain)
+        assert nb == want.nbytes and info.plan_bytes == want_info.plan_bytes
+        assert np.array_equal(out.view(np.uint8)[:nb], want.view(np.uint8)[:nb])
+        assert info.workspace_bytes == want_info.workspace_bytes
+        if name != "decode_chain":
+            ctx[-1] += 16   # the next step: one sequence gains a block
+    with pytest.raises(TypeError):
+        pkv.BoundPlan(cu.astype(np.int64), ctx, meta.num_q_heads, desc, out, num_sms=152)
+    with pytest.raises(ValueError):
+        pkv.BoundPlan(cu[:-1], ctx, meta.num_q_heads, desc, out, num_sms=152)
+
+
+def test_copy_entry_point_checks_its_arguments(pkv):
+    """pkv_copy_async's argument errors come back without touching a device."""
+    lib = ctypes.CDLL(pkv.library_path())
+    P = ctypes.c_void_p
+    lib.pkv_copy_async.argtypes = [P, P, ctypes.c_int64, P]
+    buf = ctypes.create_string_buffer(64)
+    assert lib.pkv_copy_async(None, None, 0, None) == 0                  # nothing queued
+    assert lib.pkv_copy_async(None, ctypes.addressof(buf), 16, None) == 1  # PKV_ERR_NULL
+    assert lib.pkv_copy_async(ctypes.addressof(buf), None, 16, None) == 1
+    assert lib.pkv_copy_async(ctypes.addressof(buf), ctypes.addressof(buf), -1, None) == 3
+
+
 def test_prefill_min_q_is_a_planner_argument(pkv):
     meta = workloads.build_step("pmq", 5, [300, 200, 1], [900, 700, 50], 8, 2, 128)
     desc = pkv.PoolDesc(meta.num_blocks, 16, 2, 128)

@@ -354,6 +354,69 @@ def test_bound_step_matches_the_plain_calls(pkv, cuda_device):
         assert torch.equal(out_b, ref[step]) and torch.equal(pa, pb)
 
 
+def test_bound_copies_and_planner_serve_a_step_from_host_buffers(pkv, cuda_device):
+    """The serving loop through the library alone: pinned inputs go up with one
+    bound copy, the plan is made by the bound planner into the same pinned
+    buffer and goes up behind them, the bound step runs and a bound copy brings
+    out back.  The result has the bits of the plain calls, and copy_async moves
+    bytes both ways unchanged."""
+    dev = cuda_device
+    g = torch.Generator().manual_seed(3)
+    src = torch.randint(0, 255, (12345,), dtype=torch.uint8, generator=g).pin_memory()
+    mid = torch.empty(12345, dtype=torch.uint8, device=dev)
+    back = torch.zeros(12345, dtype=torch.uint8).pin_memory()
+    pkv.copy_async(mid, src)
+    pkv.copy_async(back, mid, 12000)
+    torch.cuda.synchronize()
+    assert torch.equal(back[:12000], src[:12000]) and int(back[12000:].sum()) == 0
+
+    meta = workloads.build_step("serve", 72, [1, 2, 1, 1], [300, 900, 45, 2000], 16, 4, 128)
+    q, k, v, pool = workloads.make_values(meta)
+    parts = [torch.from_numpy(meta.slot_mapping), torch.from_numpy(meta.cu_q_lens),
+             torch.from_numpy(meta.context_lens), torch.from_numpy(meta.block_tables), q, k, v,
+             torch.zeros(1 << 15, dtype=torch.int32)]
+    offs, n = [], 0
+    for t in parts:
+        offs.append(n)
+        n += (t.numel() * t.element_size() + 15) // 16 * 16
+    hbuf = torch.zeros(n, dtype=torch.uint8).pin_memory()
+    dbuf = torch.empty(n, dtype=torch.uint8, device=dev)
+    hv, dv = [], []
+    for t, o in zip(parts, offs):
+        nb = t.numel() * t.element_size()
+        h = hbuf[o:o + nb].view(t.dtype).view(t.shape)
+        h.copy_(t)
+        hv.append(h)
+        dv.append(dbuf[o:o + nb].view(t.dtype).view(t.shape))
+    ds, dcu, dctx, dbt, dq, dk, dvv, dplan = dv
+    pool_a, pool_b = pool.to(dev), pool.to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    planner = pkv.BoundPlan(hv[1].numpy(), hv[2].numpy(), 16, pool_b, hv[-1].numpy(),
+                            block_tables=hv[3].numpy())
+    info, plan_nb = planner.run()
+    plan = pkv.StepPlan(info, hv[-1].numpy().view(np.uint8)[:plan_nb].view(np.int32), dev)
+    plan.dev = dplan.view(torch.uint8)
+    out_b = torch.empty_like(dq)
+    out_h = torch.empty(out_b.shape, dtype=out_b.dtype).pin_memory()
+    up = pkv.BoundCopy(dbuf, hbuf)
+    down = pkv.BoundCopy(out_h, out_b)
+    step = pkv.BoundStep(dk, dvv, ds, dq, dcu, dctx, dbt, pool_b, meta.scale, plan, out_b,
+                         dev_status=status)
+    up.run(offs[-1] + plan_nb)
+    step.run()
+    down.run()
+    torch.cuda.synchronize()
+    pkv.paged_kv_append(k.to(dev), v.to(dev), torch.from_numpy(meta.slot_mapping).to(dev), pool_a)
+    ref = pkv.paged_varlen_attention(q.to(dev), meta.cu_q_lens, meta.context_lens,
+                                     torch.from_numpy(meta.block_tables).to(dev), pool_a,
+                                     meta.scale, plan=pkv.plan_step(
+                                         meta.cu_q_lens, meta.context_lens, 16, pool_a,
+                                         block_tables=meta.block_tables))
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(out_h, ref.cpu()) and torch.equal(pool_a, pool_b)
+
+
 def test_in_tree_library_is_loaded(pkv):
     import os
     assert os.path.exists(pkv.library_path())
