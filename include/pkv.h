@@ -117,6 +117,10 @@ typedef struct pkv_plan_info {
   int32_t num_gather_rows;      /* query tokens listed by the tensor-core shared-prefix
                                    items (a prefix many query rows share is read once per
                                    128 rows on the tensor cores; needs host block tables) */
+  int32_t merge_rows;           /* query rows of the largest decode merge group (its row
+                                   group's tokens x the G heads of a KV head, <= 16; 0 when
+                                   there is none): the merge launch covers that many rows
+                                   of every decode group */
   int64_t kv_tokens;         /* sum of context_lens over sequences with q_len > 0 */
   int64_t decode_blocks;     /* (KV block, KV head) pairs the split-KV kernel attends, each
                                 counted once: per sequence (however many row groups read

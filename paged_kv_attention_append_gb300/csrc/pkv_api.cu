@@ -217,6 +217,9 @@ extern "C" pkv_status pkv_paged_varlen_attention(
   a.ppart_o = reinterpret_cast<float *>(wb ? wb + off_po : nullptr);
   a.ppart_ml = reinterpret_cast<float *>(wb ? wb + off_pml : nullptr);
   a.num_decode_merges = info->num_merge_groups - info->num_prefill_merges;
+  a.merge_rows = info->merge_rows;
+  if (a.num_decode_merges > 0 && (info->merge_rows < 1 || info->merge_rows > kRowsPerTile))
+    return PKV_ERR_SHAPE;
   if (info->lookahead < 0 || (info->lookahead > 0 && info->num_prefill_tiles > 0))
     return PKV_ERR_SHAPE;
   a.lookahead = info->lookahead;

@@ -84,6 +84,7 @@ struct DecodeParams {
   int32_t num_merges;          // all merge groups: decode ones, then prefill ones
   int32_t num_decode_merges;
   int32_t merge_lanes_log2;    // lanes that share one decode row's splits (merge kernel)
+  int32_t merge_rows;          // rows the merge launch covers per decode group
   int32_t num_partials;
   int32_t num_warps;
   int32_t num_seqs;
@@ -191,17 +192,19 @@ template <int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams p) {
   constexpr int kChunks = D / 4;  // float4 chunks of a row
   const int64_t t0 = (int64_t)blockIdx.x * kMergeThreads + threadIdx.x;
-  // decode groups (2^lanes_log2 lanes per row and chunk), then prefill groups
+  // decode groups (their first merge_rows rows, 2^lanes_log2 lanes per row and
+  // chunk), then prefill groups
   const int n_dg = p.num_decode_merges;
   const int lanes_log2 = p.merge_lanes_log2;
-  const int64_t n_dec = ((int64_t)n_dg * kRowsPerTile * kChunks) << lanes_log2;
+  const int64_t n_dec = ((int64_t)n_dg * p.merge_rows * kChunks) << lanes_log2;
   const bool dec = t0 < n_dec;
   const int S = dec ? 1 << lanes_log2 : 1;
   const int sub = dec ? (int)(t0 & (S - 1)) : 0;
-  const int rows = dec ? kRowsPerTile : kPrefillRows;
+  const int rows = dec ? kRowsPerTile : kPrefillRows;    // rows of a partial slot
+  const int mrows = dec ? p.merge_rows : kPrefillRows;  // rows covered per group
   const int64_t tt = dec ? t0 >> lanes_log2 : t0 - n_dec;
-  const int64_t gi = tt / (rows * kChunks);
-  const int rem = (int)(tt % (rows * kChunks));
+  const int64_t gi = tt / (mrows * kChunks);
+  const int rem = (int)(tt % (mrows * kChunks));
   const int row = rem / kChunks, ch = rem % kChunks;
   const bool in = gi < (dec ? n_dg : p.num_merges - p.num_decode_merges);
   // the plan is not written by the kernels before this one: the group is read
@@ -863,6 +866,7 @@ DecodeParams make_params(const AttnArgs &a) {
   p.after_prefill = a.num_prefill_tiles > 0 && a.num_prefill_ctas > 0 ? 1 : 0;
   p.num_decode_merges = a.num_decode_merges;
   p.merge_lanes_log2 = 0;
+  p.merge_rows = a.merge_rows;
   p.num_partials = a.num_partials;
   p.ppart_o = a.ppart_o;
   p.ppart_ml = reinterpret_cast<const float2 *>(a.ppart_ml);
@@ -943,12 +947,12 @@ int launch_merge(const AttnArgs &a, int *launches) {
   if (a.num_decode_merges > 0) {
     const int64_t avg = ((int64_t)a.num_partials + a.num_decode_merges - 1) / a.num_decode_merges;
     const int64_t budget = (int64_t)std::max(device_sm_count(), 1) * 1024;
-    const int64_t base = (int64_t)a.num_decode_merges * kRowsPerTile * chunks;
+    const int64_t base = (int64_t)a.num_decode_merges * a.merge_rows * chunks;
     while (lanes_log2 < 3 && avg > (8ll << lanes_log2) && (base << (lanes_log2 + 1)) <= budget)
       ++lanes_log2;
   }
   const int64_t threads =
-      (((int64_t)a.num_decode_merges * kRowsPerTile * chunks) << lanes_log2) +
+      (((int64_t)a.num_decode_merges * a.merge_rows * chunks) << lanes_log2) +
       (int64_t)(a.num_merge_groups - a.num_decode_merges) * kPrefillRows * chunks;
   const dim3 grid((unsigned)((threads + kMergeThreads - 1) / kMergeThreads));
   const bool pdl = !profiling_active();

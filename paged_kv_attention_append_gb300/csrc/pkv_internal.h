@@ -237,6 +237,7 @@ struct AttnArgs {
   float *ppart_o;
   float *ppart_ml;
   int32_t num_decode_merges;  // merge_groups[0 .. num_decode_merges) are kind 0
+  int32_t merge_rows;         // rows of the largest decode merge group
   int32_t lookahead;          // further decode steps the plan covers (chained decode)
   int32_t *dev_status;
   pkv_stream stream;

@@ -626,6 +626,7 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   std::vector<MergeGroup> &merges = S.merges;
   merges.clear();
   int32_t parts = 0;
+  int32_t merge_rows = 0;  // rows of the largest decode merge group
   {
     // gathered prefix chunks always write partials: their unit gets a merge
     // group even when nothing else splits it
@@ -648,6 +649,7 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
         m.h = h;
         m.part0 = parts;
         m.nsplit = total;
+        merge_rows = std::max(merge_rows, dunits[u].n_q * group);
         if (!casc_part0.empty()) casc_part0[u * hkv + h] = nc > 0 ? parts : -1;
         parts += nc;
         for (const auto &si : sh) sitems[si[0]].rg[si[1]].part = parts++;
@@ -855,6 +857,7 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
                       (ptiles.empty() ? 0 : 1);
   info->num_shared_ctas = (int32_t)(sitems.size() / kSharedItemsPerCta);
   info->num_gather_rows = (int32_t)gather.size();
+  info->merge_rows = merge_rows;
   info->max_blocks_needed = max_nb;
   info->kv_tokens = kv_tokens;
   // blocks the split-KV kernel attends, each once: every decode-class sequence's

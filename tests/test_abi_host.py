@@ -207,6 +207,11 @@ def check_plan(meta, info, host, num_sms):
     assert np.array_equal(mer[:, 7], meta.cu_q_lens[mer[:, 0]] + mer[:, 1])   # packed first row
     assert info.num_prefill_merges == int((mer[:, 6] == 1).sum())
     assert np.all(mer[:nm - info.num_prefill_merges, 6] == 0)   # decode groups first
+    dmer = mer[:nm - info.num_prefill_merges]
+    g = meta.num_q_heads // meta.num_kv_heads
+    # the merge launch covers the largest decode group's rows (n_q tokens x G heads)
+    assert info.merge_rows == (int(dmer[:, 2].max()) * g if len(dmer) else 0)
+    assert info.merge_rows <= 16
     assert info.num_kernels == (info.num_decode_warps > 0) + (info.num_merge_groups > 0) + \
         (info.num_prefill_tiles > 0)
 
