@@ -591,10 +591,6 @@ class StepBench:
         num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
         outs_h = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in self.outs]
         h2d = (plan_off + int(info.plan_bytes) + 15) // 16 * 16  # bytes copied per step
-        # one copy after planning, or -- when the step's inputs are large enough
-        # for their transfer to matter -- the inputs first, overlapping the
-        # planning, then the plan
-        split_copy = plan_off > (4 << 20)
         plan_e2e = pkv.StepPlan(info, self.host_plan, dev)
         plan_e2e.dev = dplan.view(torch.uint8)
         d2h = sum(o.numel() * o.element_size() for o in outs_h)
@@ -612,15 +608,18 @@ class StepBench:
             for i in range(args.warmup + args.steps):
                 torch.cuda.synchronize(dev)
                 t0 = time.perf_counter()
-                if split_copy:  # large inputs go up while the host plans
-                    up.run(plan_off)
+                # the inputs go up and the first step's KV append (it needs no
+                # plan) runs while the host plans; the plan follows
+                up.run(plan_off)
+                bound[0].run_append()
                 inf2, plan_nb = planner.run()
                 n = (plan_off + plan_nb + 15) // 16 * 16
-                n0 = plan_off if split_copy else 0
-                up.run(n - n0, n0)
+                up.run(n - plan_off, plan_off)
                 plan_e2e.info = inf2
                 for t, b in enumerate(bound):
-                    b.run()
+                    if t > 0:
+                        b.run_append()
+                    b.run_attention()
                     if t + 1 < self.nch:
                         pkv.decode_advance(dctx, ds, dcu, dbt, self.pool, dev_status=self.status)
                 for d in down:

@@ -591,17 +591,26 @@ class BoundStep:
 
     def run(self) -> None:
         """Enqueue this step's append and attention on the bound stream."""
+        self.run_append()
+        self.run_attention()
+
+    def run_append(self) -> None:
+        """Enqueue the step's KV append alone: it needs no plan, so a serving loop
+        may queue it as soon as the step's new K/V are on the device and plan the
+        step meanwhile (run_attention then follows it on the same stream)."""
+        st = self._lib.pkv_paged_kv_append(*self._append)
+        if st:
+            raise PkvError(st, "pkv_paged_kv_append")
+
+    def run_attention(self) -> None:
+        """Enqueue the step's attention with the plan as it stands now."""
         info = self.plan.info
         total_q, hq, n_cu, n_bt, max_blocks = self._shape
         if (info.total_q != total_q or info.num_q_heads != hq or info.num_seqs + 1 != n_cu or
                 info.num_seqs != n_bt):
             raise ValueError("the plan does not match the bound buffers")
-        lib = self._lib
-        st = lib.pkv_paged_kv_append(*self._append)
-        if st:
-            raise PkvError(st, "pkv_paged_kv_append")
         ws = self.plan.workspace
-        st = lib.pkv_paged_varlen_attention(
+        st = self._lib.pkv_paged_varlen_attention(
             *self._attn_head, ctypes.byref(info), ctypes.c_void_p(self.plan.dev.data_ptr()),
             self._out, ctypes.c_void_p(None if ws is None else ws.data_ptr()),
             ctypes.c_int64(0 if ws is None else ws.numel()), *self._tail)

@@ -24,24 +24,37 @@ __global__ void __launch_bounds__(256) append_kernel(const uint4 *__restrict__ k
   const int64_t per_token = 2ll * hkv * kVecPerRow;
   const int64_t total = per_token * num_tokens;
   const int64_t nslots = (int64_t)num_blocks * kBlockSize;
-  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
-       idx += (int64_t)gridDim.x * blockDim.x) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  // vector idx: its source, and its destination (null: padding token or a bad
+  // slot, reported once per token)
+  auto locate = [&](int64_t idx, const uint4 *&src, uint4 *&dst) {
     const int32_t t = (int32_t)(idx / per_token);
     int32_t rem = (int32_t)(idx - (int64_t)t * per_token);
     const int32_t kv = rem / (hkv * kVecPerRow);
     rem -= kv * hkv * kVecPerRow;
     const int32_t h = rem / kVecPerRow;
     const int32_t vec = rem - h * kVecPerRow;
+    src = (kv == 0 ? k : v) + ((int64_t)t * hkv + h) * kVecPerRow + vec;
     const int64_t slot = __ldg(slot_mapping + t);
-    if (slot < 0) continue;  // padding token
+    dst = nullptr;
     if (slot >= nslots) {
       if (kv == 0 && h == 0 && vec == 0) report(dev_status, PKV_DEV_BAD_SLOT);
-      continue;
+    } else if (slot >= 0) {
+      const int64_t blk = slot / kBlockSize, off = slot % kBlockSize;
+      dst = pool + (((blk * 2 + kv) * hkv + h) * kBlockSize + off) * kVecPerRow + vec;
     }
-    const int64_t blk = slot / kBlockSize, off = slot % kBlockSize;
-    const uint4 *src = (kv == 0 ? k : v) + ((int64_t)t * hkv + h) * kVecPerRow + vec;
-    uint4 *dst = pool + (((blk * 2 + kv) * hkv + h) * kBlockSize + off) * kVecPerRow + vec;
-    *dst = ldg128_nc(src);
+  };
+  // two vectors a thread per round, both loads issued before either store
+  for (int64_t i0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i0 < total; i0 += 2 * stride) {
+    const int64_t i1 = i0 + stride;
+    const uint4 *s0, *s1 = nullptr;
+    uint4 *d0, *d1 = nullptr;
+    locate(i0, s0, d0);
+    if (i1 < total) locate(i1, s1, d1);
+    const uint4 x0 = d0 ? ldg128_nc(s0) : make_uint4(0, 0, 0, 0);
+    const uint4 x1 = d1 ? ldg128_nc(s1) : make_uint4(0, 0, 0, 0);
+    if (d0) *d0 = x0;
+    if (d1) *d1 = x1;
   }
 }
 
@@ -51,8 +64,10 @@ int launch_append(const void *k, const void *v, const int32_t *slot_mapping, int
   const int64_t vecs = 2ll * desc.num_kv_heads * (desc.head_dim / 8) * num_tokens;
   const int threads = 256;
   int64_t blocks = (vecs + threads - 1) / threads;
-  // a grid-stride loop: at most 16 CTAs of 256 threads per SM
-  const int64_t cap = 16ll * (device_sm_count() > 0 ? device_sm_count() : 1);
+  // one resident wave at most (8 CTAs of 256 threads per SM), two vectors a
+  // thread per round of the grid-stride loop
+  const int64_t cap = 8ll * (device_sm_count() > 0 ? device_sm_count() : 1);
+  blocks = (blocks + 1) / 2;
   blocks = blocks < 1 ? 1 : (blocks > cap ? cap : blocks);
   const cudaError_t pe = desc.head_dim == 128 ? prepare_kernel<append_kernel<128>>(0)
                                               : prepare_kernel<append_kernel<64>>(0);

@@ -311,14 +311,23 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   // suffix segments: (row group, KV head) keys past the shared blocks
   std::vector<int32_t> &seg_of = S.seg_of;
   seg_of.assign(dunits.size() * hkv, -1);
-  for (size_t u = 0; u < dunits.size(); ++u) {
-    const DUnit &du = dunits[u];
-    const int32_t kb0 = std::min(unit_kb0[u], du.nb);
-    if (du.nb <= kb0) continue;
-    for (int32_t h = 0; h < hkv; ++h) {
-      seg_of[u * hkv + h] = (int32_t)segs.size();
-      segs.push_back({du.seq, du.qi0, du.n_q, h, kb0, du.nb - kb0});
-      total_blocks += du.nb - kb0;
+  {
+    size_t nseg = 0;
+    for (size_t u = 0; u < dunits.size(); ++u)
+      if (dunits[u].nb > std::min(unit_kb0[u], dunits[u].nb)) nseg += (size_t)hkv;
+    segs.resize(nseg);
+    Segment *sg = segs.data();
+    int32_t *so = seg_of.data();
+    int32_t k = 0;
+    for (size_t u = 0; u < dunits.size(); ++u) {
+      const DUnit du = dunits[u];
+      const int32_t kb0 = std::min(unit_kb0[u], du.nb);
+      if (du.nb <= kb0) continue;
+      for (int32_t h = 0; h < hkv; ++h, ++k) {
+        so[u * hkv + h] = k;
+        sg[k] = {du.seq, du.qi0, du.n_q, h, kb0, du.nb - kb0};
+      }
+      total_blocks += (int64_t)hkv * (du.nb - kb0);
     }
   }
 
@@ -596,29 +605,28 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
     }
     size_t k = 0;
     int64_t seg_off = 0;  // global block offset of segment k
+    const Segment *sg = segs.data();
+    const int64_t *ct = cut.data();
+    int32_t *wb = warp_begin.data(), *sf = seg_first.data(), *sc = seg_count.data();
+    int32_t np = 0;
     for (int32_t w = 0; w < num_warps; ++w) {
-      warp_begin[w] = npieces;
-      int64_t a = cut[w], b = cut[w + 1];
+      wb[w] = np;
+      int64_t a = ct[w];
+      const int64_t b = ct[w + 1];
       while (a < b) {
-        while (seg_off + segs[k].nb <= a) seg_off += segs[k++].nb;
-        const Segment &g = segs[k];
-        int64_t e = std::min<int64_t>(b, seg_off + g.nb);
-        Piece &p = pieces[npieces];
-        p.seq = g.seq;
-        p.qi0 = g.qi0;
-        p.n_q = g.n_q;
-        p.h = g.h;
-        p.kb_begin = g.kb0 + (int32_t)(a - seg_off);
-        p.kb_end = g.kb0 + (int32_t)(e - seg_off);
-        p.part = -1;
-        p.q_row0 = cu_q_lens[g.seq] + g.qi0;
-        if (seg_first[k] < 0) seg_first[k] = npieces;
-        ++seg_count[k];
-        ++npieces;
+        while (seg_off + sg[k].nb <= a) seg_off += sg[k++].nb;
+        const Segment g = sg[k];
+        const int64_t e = std::min<int64_t>(b, seg_off + g.nb);
+        pieces[np] = {g.seq, g.qi0, g.n_q, g.h, g.kb0 + (int32_t)(a - seg_off),
+                      g.kb0 + (int32_t)(e - seg_off), -1, cu_q_lens[g.seq] + g.qi0};
+        if (sf[k] < 0) sf[k] = np;
+        ++sc[k];
+        ++np;
         a = e;
       }
     }
-    warp_begin[num_warps] = npieces;
+    npieces = np;
+    wb[num_warps] = npieces;
   }
   // partial slots: every (decode unit, KV head) result whose keys are split over
   // several parts (shared-prefix chunks and suffix pieces) gets one slot per part
@@ -632,30 +640,29 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
     // group even when nothing else splits it
     std::vector<int32_t> casc_part0(gather.empty() ? 0 : dunits.size() * hkv, -1);
     static const std::vector<std::array<int32_t, 2>> kNoShared;
-    for (size_t u = 0; u < dunits.size(); ++u)
+    merges.resize(dunits.size() * (size_t)hkv);  // at most one group per (unit, KV head)
+    MergeGroup *mg = merges.data();
+    const int32_t *so = seg_of.data(), *sf = seg_first.data(), *sc = seg_count.data();
+    size_t nm = 0;
+    for (size_t u = 0; u < dunits.size(); ++u) {
+      const DUnit du = dunits[u];
+      const int32_t nc = unit_casc[u];
       for (int32_t h = 0; h < hkv; ++h) {
         const auto &sh = unit_shared.empty() ? kNoShared : unit_shared[u * hkv + h];
-        const int32_t k = seg_of[u * hkv + h];
-        const int32_t np = k >= 0 ? seg_count[k] : 0;
-        const int32_t nc = unit_casc[u];
+        const int32_t k = so[u * hkv + h];
+        const int32_t np = k >= 0 ? sc[k] : 0;
         const int32_t total = nc + (int32_t)sh.size() + np;
         if (total <= 1 && nc == 0) continue;
-        MergeGroup m;
-        std::memset(&m, 0, sizeof m);
-        m.seq = dunits[u].seq;
-        m.qi0 = dunits[u].qi0;
-        m.q_row0 = cu_q_lens[dunits[u].seq] + dunits[u].qi0;
-        m.n_q = dunits[u].n_q;
-        m.h = h;
-        m.part0 = parts;
-        m.nsplit = total;
-        merge_rows = std::max(merge_rows, dunits[u].n_q * group);
+        mg[nm++] = {du.seq, du.qi0, du.n_q, h, parts, total, 0, cu_q_lens[du.seq] + du.qi0};
+        merge_rows = std::max(merge_rows, du.n_q * group);
         if (!casc_part0.empty()) casc_part0[u * hkv + h] = nc > 0 ? parts : -1;
         parts += nc;
         for (const auto &si : sh) sitems[si[0]].rg[si[1]].part = parts++;
-        for (int32_t t = 0; t < np; ++t) pieces[seg_first[k] + t].part = parts++;
-        merges.push_back(m);
+        Piece *pc = pieces + (k >= 0 ? sf[k] : 0);
+        for (int32_t t = 0; t < np; ++t) pc[t].part = parts++;
       }
+    }
+    merges.resize(nm);
     for (size_t i = 0; i < gather.size(); ++i) gather[i].part0 = casc_part0[gather_uh[i]];
   }
   // ---- prefill work per persistent CTA (at most one per SM), equal cost:

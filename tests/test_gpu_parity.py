@@ -402,8 +402,10 @@ def test_bound_copies_and_planner_serve_a_step_from_host_buffers(pkv, cuda_devic
     down = pkv.BoundCopy(out_h, out_b)
     step = pkv.BoundStep(dk, dvv, ds, dq, dcu, dctx, dbt, pool_b, meta.scale, plan, out_b,
                          dev_status=status)
-    up.run(offs[-1] + plan_nb)
-    step.run()
+    up.run(offs[-1])                 # the inputs, then the append (it needs no plan)
+    step.run_append()
+    up.run(plan_nb, offs[-1])        # the plan behind them
+    step.run_attention()
     down.run()
     torch.cuda.synchronize()
     pkv.paged_kv_append(k.to(dev), v.to(dev), torch.from_numpy(meta.slot_mapping).to(dev), pool_a)
