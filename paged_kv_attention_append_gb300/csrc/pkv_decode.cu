@@ -128,11 +128,12 @@ __device__ __forceinline__ void write_piece(const DecodeParams &p, const Piece &
 constexpr int kMergeThreads = 128;
 
 // Combines one row's 4 columns over partial slots 0, step, 2 step, .. < nsplit
-// (slot stride `rows`), returning the unnormalised sum with its max M and
+// (slot stride `rows`), kBatch splits' loads issued before any is used,
+// returning the unnormalised sum with its max M and
 // denominator L.  A split whose m is NaN was written by a piece that found its
 // plan disagreeing with the device tables: the row is then `poisoned` and must
 // not be written.
-template <int D>
+template <int D, int kBatch>
 __device__ __forceinline__ float4 merge_row(const float2 *ml, const float4 *po, int nsplit,
                                             int step, int rows, float &M, float &L,
                                             bool &poisoned) {
@@ -141,7 +142,6 @@ __device__ __forceinline__ float4 merge_row(const float2 *ml, const float4 *po, 
   L = 0.f;
   poisoned = false;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  constexpr int kBatch = 8;  // splits whose loads are all issued before any is used
   for (int j0 = 0; j0 < nsplit; j0 += kBatch * step) {
     float2 v[kBatch];
     float4 x[kBatch];
@@ -188,7 +188,7 @@ __device__ __forceinline__ void poison_piece(const DecodeParams &p, int part, in
     p.part_ml[(int64_t)part * kRowsPerTile + lane] = make_float2(__int_as_float(0x7fc00000), 0.f);
 }
 
-template <int D>
+template <int D, int kBatch>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams p) {
   constexpr int kChunks = D / 4;  // float4 chunks of a row
   const int64_t t0 = (int64_t)blockIdx.x * kMergeThreads + threadIdx.x;
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const DecodeParams
       ch;
   float M, L;
   bool poisoned;
-  float4 acc = merge_row<D>(ml, po, g.nsplit - sub, S, rows, M, L, poisoned);
+  float4 acc = merge_row<D, kBatch>(ml, po, g.nsplit - sub, S, rows, M, L, poisoned);
   if (S > 1) {
     // lanes sub and sub ^ o hold disjoint sets of the row's splits: combine
     const unsigned mask = ((1u << S) - 1u) << ((threadIdx.x & 31) & ~(S - 1));
@@ -956,16 +956,22 @@ int launch_merge(const AttnArgs &a, int *launches) {
       (int64_t)(a.num_merge_groups - a.num_decode_merges) * kPrefillRows * chunks;
   const dim3 grid((unsigned)((threads + kMergeThreads - 1) / kMergeThreads));
   const bool pdl = !profiling_active();
-  const cudaError_t pe = a.desc.head_dim == 128 ? prepare_kernel<merge_kernel<128>>(0)
-                                                : prepare_kernel<merge_kernel<64>>(0);
+  // 8 splits' loads in flight a lane; a grid larger than one wave of that
+  // instance (6 CTAs an SM) takes the one with 6, whose registers let 8 CTAs
+  // share an SM (shared_prefix_verify's merge 13.9 -> 11.9 us; a 128-CTA grid
+  // does better with the 8)
+  const bool wide = (int64_t)grid.x > 6ll * std::max(device_sm_count(), 1);
+  auto kern = a.desc.head_dim == 128 ? (wide ? merge_kernel<128, 6> : merge_kernel<128, 8>)
+                                     : (wide ? merge_kernel<64, 6> : merge_kernel<64, 8>);
+  const cudaError_t pe =
+      a.desc.head_dim == 128
+          ? (wide ? prepare_kernel<merge_kernel<128, 6>>(0) : prepare_kernel<merge_kernel<128, 8>>(0))
+          : (wide ? prepare_kernel<merge_kernel<64, 6>>(0) : prepare_kernel<merge_kernel<64, 8>>(0));
   if (pe != cudaSuccess) return (int)pe;
   DecodeParams mp = make_params(a);
   mp.merge_lanes_log2 = lanes_log2;
   profile_begin(PKV_KERNEL_MERGE, a.stream);
-  const cudaError_t le =
-      a.desc.head_dim == 128
-          ? launch_kernel(merge_kernel<128>, grid, dim3(kMergeThreads), 0, a.stream, pdl, mp)
-          : launch_kernel(merge_kernel<64>, grid, dim3(kMergeThreads), 0, a.stream, pdl, mp);
+  const cudaError_t le = launch_kernel(kern, grid, dim3(kMergeThreads), 0, a.stream, pdl, mp);
   profile_end(PKV_KERNEL_MERGE, a.stream);
   const int e = le != cudaSuccess ? (int)le : (int)cudaGetLastError();
   if (!e) {
