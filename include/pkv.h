@@ -372,7 +372,9 @@ PKV_API pkv_status pkv_state_checkpoint(const void *src, const int32_t *dst_slot
  *    the stream.  The first call made with a given device current looks up the
  *    array's device address on that device (cudaGetSymbolAddress, which may
  *    load the library's module there); make that first call before any stream
- *    capture.
+ *    capture.  The address is kept for the life of the loaded library: after
+ *    cudaDeviceReset on a device, do not call this entry point on that device
+ *    again in the same process (the kept address would be stale).
  *  - All calls on a device share the one array and it keeps the last call's
  *    contents.  Nothing in it needs to start at zero (every partial is written
  *    before it is read).  Calls whose work overlaps on the GPU (different
