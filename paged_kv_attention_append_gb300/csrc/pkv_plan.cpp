@@ -460,18 +460,19 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
     }
     if (!cpairs.empty()) {
       // The items take a share of the SMs; the split-KV kernel streams the
-      // step's own blocks on the rest meanwhile.  Share = prefix tile passes /
-      // (tile passes + streamed block-heads / 32), at least one half: one tile
-      // pass weighed as 32 block-heads put both shared-prefix workloads at
-      // their measured optimum (96 and 80 of 152 SMs).  Integer arithmetic, so
-      // every host plans alike.
+      // step's own blocks on the rest meanwhile (its warps there take a larger
+      // share of the blocks: see the warp cut below).  Share = prefix tile
+      // passes / (tile passes + streamed block-heads / 16), at least 15/32:
+      // with that cut, a tile pass weighed as 16 block-heads put both
+      // shared-prefix workloads at their measured optimum (80 and 72 of 152
+      // SMs).  Integer arithmetic, so every host plans alike.
       int64_t pf_work = 0;
       for (const CPair &cp : cpairs) pf_work += (int64_t)cp.nsub * (groups[cp.gi].len / kKeyTileBlocks);
       const int64_t ncp = (int64_t)cpairs.size();
-      int64_t num = 32 * pf_work, den = 32 * pf_work + total_blocks;  // share = num / den
-      if (2 * num < den) {
-        num = 1;
-        den = 2;
+      int64_t num = 16 * pf_work, den = 16 * pf_work + total_blocks;  // share = num / den
+      if (32 * num < 15 * den) {
+        num = 15;
+        den = 32;
       }
       const int64_t want = std::max<int64_t>(1, (2 * num * pf_sms + den * ncp) / (2 * den * ncp));
       for (const CPair &cp : cpairs) {
@@ -551,6 +552,25 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
     // at least kMinBlocksPerWarp blocks per warp every share holds a block.
     constexpr int64_t kBlockCost = 2, kPieceCost = 6;
     const int64_t total_cost = kBlockCost * total_blocks + kPieceCost * (int64_t)segs.size();
+    // Warps of the split-KV CTAs dispatched first: when gathered prefix items
+    // are the step's only tensor-core work and leave SMs free, the lowest-index
+    // CTAs start on those SMs at once and stream while the items run; the rest
+    // start only as the items' CTAs exit.  With equal shares the early CTAs
+    // finished soon after the items and their SMs then sat idle while the late
+    // ones streamed; the early warps now take kEarlyWeight / kLateWeight times
+    // a late warp's share of the cost (4:1 measured best of 2:1 .. 5:1 on both
+    // shared-prefix workloads).  The order in which CTAs are dispatched only
+    // moves the balance, never the result.
+    constexpr int64_t kEarlyWeight = 4, kLateWeight = 1;
+    int64_t early = 0;
+    if (pairs.empty() && !casc_items.empty() && (int64_t)casc_items.size() < dec_sms)
+      early = std::min<int64_t>(num_warps, (dec_sms - (int64_t)casc_items.size()) * kDecodeWarpsPerSm);
+    const int64_t w_early = early > 0 ? kEarlyWeight : 1, w_late = early > 0 ? kLateWeight : 1;
+    const int64_t ctot = early * w_early + ((int64_t)num_warps - early) * w_late;
+    // cost position where warp w's share starts, times ctot
+    auto cw = [&](int64_t w) {
+      return (std::min<int64_t>(w, early) * w_early + std::max<int64_t>(0, w - early) * w_late) * total_cost;
+    };
     std::vector<int64_t> &cut = S.cut;  // first block of each warp
     cut.assign(num_warps + 1, total_blocks);
     cut[0] = 0;
@@ -567,8 +587,9 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
       // boundary is found with one division per warp, not a walk over blocks
       // (one division per segment: from one warp to the next the numerator grows
       // by total_cost, so the quotient and remainder are carried forward)
-      const int64_t d2 = kBlockCost * std::max<int64_t>(num_warps, 1);
-      const int64_t tq = total_cost / d2, tr = total_cost % d2;
+      const int64_t d2 = kBlockCost * std::max<int64_t>(ctot, 1);
+      const int64_t tqa = w_early * total_cost / d2, tra = w_early * total_cost % d2;
+      const int64_t tqb = w_late * total_cost / d2, trb = w_late * total_cost % d2;
       int64_t cost = 0, blk = 0;
       int32_t w = 1;
       for (const Segment &g : segs) {
@@ -576,8 +597,8 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
         const int64_t last_mid = first_mid + kBlockCost * (g.nb - 1);
         bool carried = false;  // q, r hold need / d2 and need % d2 for warp w
         int64_t q = 0, r = 0;
-        while (w < num_warps && last_mid * num_warps >= (int64_t)w * total_cost) {
-          const int64_t need = (int64_t)w * total_cost - first_mid * num_warps;  // >= 2i * nw
+        while (w < num_warps && last_mid * ctot >= cw(w)) {
+          const int64_t need = cw(w) - first_mid * ctot;  // >= 2i * ctot
           int64_t i = 0;
           if (need > 0) {
             if (!carried) {
@@ -588,10 +609,12 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
             i = q + (r > 0 ? 1 : 0);  // ceil(need / d2)
           }
           if (i > g.nb - 1) i = g.nb - 1;
+          // the next warp's start grows by this warp's weight
+          const bool e = w < early;
           cut[w++] = blk + i;
           if (carried) {
-            q += tq;
-            r += tr;
+            q += e ? tqa : tqb;
+            r += e ? tra : trb;
             if (r >= d2) {
               ++q;
               r -= d2;
@@ -917,6 +940,12 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   WarpHead *heads = reinterpret_cast<WarpHead *>(p + off.warp_head);
   for (int32_t w = 0; w < num_warps; ++w) {
     WarpHead &wh = heads[w];
+    if (warp_begin[w] >= warp_begin[w + 1]) {  // a warp without blocks
+      std::memset(&wh, 0, sizeof wh);
+      wh.first.seq = -1;
+      for (int i = 0; i < 4; ++i) wh.blk[i] = -1;
+      continue;
+    }
     wh.first = pieces[warp_begin[w]];
     for (int i = 0; i < 4; ++i) {
       const int32_t kb = wh.first.kb_begin + i;
