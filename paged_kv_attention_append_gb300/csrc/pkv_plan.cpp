@@ -562,14 +562,24 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
     // shared-prefix workloads).  The order in which CTAs are dispatched only
     // moves the balance, never the result.
     constexpr int64_t kEarlyWeight = 4, kLateWeight = 1;
-    int64_t early = 0;
-    if (pairs.empty() && !casc_items.empty() && (int64_t)casc_items.size() < dec_sms)
-      early = std::min<int64_t>(num_warps, (dec_sms - (int64_t)casc_items.size()) * kDecodeWarpsPerSm);
-    const int64_t w_early = early > 0 ? kEarlyWeight : 1, w_late = early > 0 ? kLateWeight : 1;
-    const int64_t ctot = early * w_early + ((int64_t)num_warps - early) * w_late;
-    // cost position where warp w's share starts, times ctot
-    auto cw = [&](int64_t w) {
-      return (std::min<int64_t>(w, early) * w_early + std::max<int64_t>(0, w - early) * w_late) * total_cost;
+    constexpr int kMaxGroups = 2;
+    int ngroups = 1;  // warps gbeg[g] .. gbeg[g+1]-1 take weight gwt[g]
+    int64_t gbeg[kMaxGroups + 1] = {0, (int64_t)num_warps, (int64_t)num_warps};
+    int64_t gwt[kMaxGroups] = {1, 1};
+    if (pairs.empty() && !casc_items.empty() && (int64_t)casc_items.size() < dec_sms) {
+      ngroups = 2;
+      gbeg[1] = std::min<int64_t>(num_warps,
+                                  (dec_sms - (int64_t)casc_items.size()) * kDecodeWarpsPerSm);
+      gwt[0] = kEarlyWeight;
+      gwt[1] = kLateWeight;
+    }
+    int64_t ctot = 0;  // the warps' summed weights
+    for (int g = 0; g < ngroups; ++g) ctot += gwt[g] * (gbeg[g + 1] - gbeg[g]);
+    // group of warp w (w never decreases between calls: walked forward)
+    int cgrp = 0;
+    auto grp = [&](int64_t w) {
+      while (cgrp + 1 < ngroups && w >= gbeg[cgrp + 1]) ++cgrp;
+      return cgrp;
     };
     std::vector<int64_t> &cut = S.cut;  // first block of each warp
     cut.assign(num_warps + 1, total_blocks);
@@ -582,43 +592,43 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
       }
     } else {
       // warp w >= 1 starts at the first block whose midpoint m satisfies
-      // m * num_warps >= w * total_cost; the midpoints of a segment starting at
-      // cost c are c + kPieceCost + kBlockCost * i + kBlockCost / 2, so each
-      // boundary is found with one division per warp, not a walk over blocks
-      // (one division per segment: from one warp to the next the numerator grows
-      // by total_cost, so the quotient and remainder are carried forward)
-      const int64_t d2 = kBlockCost * std::max<int64_t>(ctot, 1);
-      const int64_t tqa = w_early * total_cost / d2, tra = w_early * total_cost % d2;
-      const int64_t tqb = w_late * total_cost / d2, trb = w_late * total_cost % d2;
-      int64_t cost = 0, blk = 0;
+      // m * ctot >= X(w) = (summed weights of warps 0 .. w-1) * total_cost, i.e.
+      // m >= T(w) = ceil(X(w) / ctot); the midpoints of a segment starting at
+      // cost c are c + kPieceCost + kBlockCost * i + kBlockCost / 2.  X(w) / ctot
+      // is carried from warp to warp as a quotient and remainder (X grows by
+      // the warp's weight times total_cost), so the whole cut takes no
+      // division per warp or per segment.
+      static_assert(kBlockCost == 2, "the block index below halves a cost distance");
+      const int64_t cdiv = std::max<int64_t>(ctot, 1);  // ctot is 0 only without warps
+      int64_t dq[kMaxGroups], dr[kMaxGroups];  // a warp's weight x total_cost over ctot
+      for (int g = 0; g < ngroups; ++g) {
+        dq[g] = gwt[g] * total_cost / cdiv;
+        dr[g] = gwt[g] * total_cost % cdiv;
+      }
+      int64_t tq = 0, tr = 0;  // X(w) = tq * ctot + tr, 0 <= tr < ctot
       int32_t w = 1;
+      if (num_warps > 1) {
+        const int g0 = grp(0);
+        tq = dq[g0];
+        tr = dr[g0];
+      }
+      int64_t cost = 0, blk = 0;
       for (const Segment &g : segs) {
         const int64_t first_mid = cost + kPieceCost + kBlockCost / 2;
         const int64_t last_mid = first_mid + kBlockCost * (g.nb - 1);
-        bool carried = false;  // q, r hold need / d2 and need % d2 for warp w
-        int64_t q = 0, r = 0;
-        while (w < num_warps && last_mid * ctot >= cw(w)) {
-          const int64_t need = cw(w) - first_mid * ctot;  // >= 2i * ctot
-          int64_t i = 0;
-          if (need > 0) {
-            if (!carried) {
-              q = need / d2;
-              r = need % d2;
-              carried = true;
-            }
-            i = q + (r > 0 ? 1 : 0);  // ceil(need / d2)
-          }
+        while (w < num_warps) {
+          const int64_t t = tq + (tr > 0 ? 1 : 0);  // T(w)
+          if (last_mid < t) break;
+          int64_t i = t > first_mid ? (t - first_mid + 1) >> 1 : 0;  // ceil((t - first_mid) / 2)
           if (i > g.nb - 1) i = g.nb - 1;
           // the next warp's start grows by this warp's weight
-          const bool e = w < early;
+          const int gw = grp(w);
           cut[w++] = blk + i;
-          if (carried) {
-            q += e ? tqa : tqb;
-            r += e ? tra : trb;
-            if (r >= d2) {
-              ++q;
-              r -= d2;
-            }
+          tq += dq[gw];
+          tr += dr[gw];
+          if (tr >= cdiv) {
+            ++tq;
+            tr -= cdiv;
           }
         }
         cost += kPieceCost + kBlockCost * g.nb;

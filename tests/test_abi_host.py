@@ -245,6 +245,10 @@ def test_planner_handles_zero_length_queries_and_empty_steps(pkv):
     info, host = pkv.plan_step(np.array([0], np.int32), np.array([], np.int32), 4, desc,
                                num_sms=152, upload=False)
     assert info.num_decode_warps == 0 and info.num_kernels == 0 and info.workspace_bytes == 0
+    # a step of prefill chunks only: no split-KV warps at all
+    info, host = pkv.plan_step(np.array([0, 300, 500], np.int32), np.array([300, 900], np.int32), 4,
+                               pkv.PoolDesc(200, 16, 2, 64), num_sms=152, upload=False)
+    assert info.num_decode_warps == 0 and info.num_prefill_tiles > 0
 
 
 @pytest.mark.parametrize("cu,ctx,hq,desc,err", [
