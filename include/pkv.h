@@ -112,8 +112,10 @@ typedef struct pkv_plan_info {
   int32_t num_prefill_merges;   /* prefill merge groups (the last ones of num_merge_groups) */
   int32_t lookahead;            /* further decode steps the plan stays valid for (chained
                                    decode, pkv_plan_decode_chain); 0 for a single step */
-  int32_t num_shared_ctas;      /* split-KV CTAs that read a prefix several sequences share
-                                   once for up to 4 row groups (needs host block tables) */
+  int32_t num_shared_ctas;      /* split-KV CTAs whose warp pairs each read blocks several row
+                                   groups share once for two of them: a prefix several
+                                   sequences share (needs host block tables), or a verify
+                                   window wider than one row group */
   int32_t num_gather_rows;      /* query tokens listed by the tensor-core shared-prefix
                                    items (a prefix many query rows share is read once per
                                    128 rows on the tensor cores; needs host block tables) */
@@ -121,6 +123,8 @@ typedef struct pkv_plan_info {
                                    group's tokens x the G heads of a KV head, <= 16; 0 when
                                    there is none): the merge launch covers that many rows
                                    of every decode group */
+  int32_t num_shared_items;     /* shared-block items of those CTAs' warp pairs (each pair
+                                   runs a chain of them, one after another) */
   int64_t kv_tokens;         /* sum of context_lens over sequences with q_len > 0 */
   int64_t decode_blocks;     /* (KV block, KV head) pairs the split-KV kernel attends, each
                                 counted once: per sequence (however many row groups read

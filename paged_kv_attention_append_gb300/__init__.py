@@ -52,7 +52,7 @@ class PlanInfo(ctypes.Structure):
         "num_seqs", "num_q_heads", "num_kv_heads", "head_dim", "total_q", "num_decode_warps",
         "num_decode_pieces", "num_merge_groups", "num_partials", "num_prefill_tiles", "num_kernels",
         "max_blocks_needed", "num_prefill_ctas", "num_prefill_partials", "num_prefill_merges",
-        "lookahead", "num_shared_ctas", "num_gather_rows", "merge_rows")] + [
+        "lookahead", "num_shared_ctas", "num_gather_rows", "merge_rows", "num_shared_items")] + [
             (n, ctypes.c_int64) for n in (
             "kv_tokens", "decode_blocks", "plan_bytes", "workspace_bytes", "gather_pairs")]
 

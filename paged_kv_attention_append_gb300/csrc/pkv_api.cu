@@ -184,16 +184,19 @@ extern "C" pkv_status pkv_paged_varlen_attention(
   if (info->num_prefill_ctas < 0 || info->num_prefill_ctas > info->num_prefill_tiles ||
       (info->num_prefill_tiles > 0 && info->num_prefill_ctas == 0))
     return PKV_ERR_SHAPE;
-  if (info->num_shared_ctas < 0 || info->num_gather_rows < 0) return PKV_ERR_SHAPE;
+  if (info->num_shared_ctas < 0 || info->num_gather_rows < 0 ||
+      info->num_shared_items < info->num_shared_ctas * kSharedItemsPerCta)
+    return PKV_ERR_SHAPE;
   const PlanOffsets off =
       plan_offsets(info->num_decode_warps, info->num_decode_pieces, info->num_merge_groups,
-                   info->num_shared_ctas * kSharedItemsPerCta, info->num_prefill_tiles,
-                   info->num_prefill_ctas, info->num_gather_rows);
+                   info->num_shared_items, info->num_prefill_tiles, info->num_prefill_ctas,
+                   info->num_gather_rows);
   a.warp_begin = reinterpret_cast<const int32_t *>(pb + off.warp_begin);
   a.warp_head = reinterpret_cast<const WarpHead *>(pb + off.warp_head);
   a.num_decode_warps = info->num_decode_warps;
   a.shared_items = reinterpret_cast<const SharedItem *>(pb + off.shared);
   a.num_shared_ctas = info->num_shared_ctas;
+  a.num_shared_items = info->num_shared_items;
   a.pieces = reinterpret_cast<const Piece *>(pb + off.pieces);
   a.merge_groups = reinterpret_cast<const MergeGroup *>(pb + off.merges);
   a.num_merge_groups = info->num_merge_groups;

@@ -69,6 +69,7 @@ struct DecodeParams {
   const Piece *pieces;
   const SharedItem *shared;    // shared-prefix CTAs, after the num_indep_ctas CTAs of warp ranges
   int32_t num_indep_ctas;
+  int32_t num_shared_items;    // entries of `shared` (the pairs' chains)
   const MergeGroup *merges;
   float *part_o;
   float2 *part_ml;
@@ -382,14 +383,17 @@ __device__ __forceinline__ void block_update(uint32_t sK, uint32_t sV, const uin
   }
 }
 
-// Shared-block CTA: two independent pairs of warps.  Each pair takes one item --
-// up to two row groups that read the same blocks: the row groups of one verify
-// window wider than 16 rows, or row groups of sequences whose tables hold the same
-// prefix blocks -- and streams those blocks once through a ring pooled from its
-// two warps' rings.  The pair's first warp resolves the block table and issues
-// the copies; a stage is refilled once both warps have released it (an empty
-// mbarrier with two arrivals).  An item with no row group leaves its pair idle.
-// Every wait is bounded.
+// Shared-block CTA: two independent pairs of warps.  Each pair runs a chain of
+// items one after another (its first item at index = pair, then through
+// SharedItem::next) -- an item is up to two row groups that read the same
+// blocks: the row groups of one verify window wider than 16 rows, or row groups
+// of sequences whose tables hold the same prefix blocks -- and streams each
+// item's blocks once through a ring pooled from its two warps' rings.  The
+// pair's first warp resolves the block tables and issues the copies, running
+// ahead across item boundaries; a stage is refilled once both warps have
+// released it (an empty mbarrier with two arrivals).  An item with no row group
+// contributes nothing; an invalid item is reported and skipped; a `next` that
+// is not a later index inside the array ends the chain.  Every wait is bounded.
 template <int D, int NSTAGE>
 __device__ __forceinline__ void shared_cta(const CUtensorMap &pool_map, const DecodeParams &p,
                                            uint8_t *smem, int warp, int lane) {
@@ -399,21 +403,7 @@ __device__ __forceinline__ void shared_cta(const CUtensorMap &pool_map, const De
   const int r = lane >> 2, c = lane & 3;
   const int G = p.group, hkv = p.num_kv_heads;
   const int pair = warp / kSharedRowGroups, lw = warp % kSharedRowGroups;
-  const SharedItem &item =
-      p.shared[(blockIdx.x - p.num_indep_ctas) * kSharedItemsPerCta + pair];
-  const int seq0 = item.seq0, h = item.h, kb0 = item.kb_begin, kb1 = item.kb_end;
-  const int n_rg = item.n_rg;
-  const bool item_ok = seq0 >= 0 && seq0 < p.num_seqs && h >= 0 && h < hkv && kb0 >= 0 &&
-                       kb0 <= kb1 && kb1 <= p.max_blocks_per_seq && n_rg >= 1 &&
-                       n_rg <= kSharedRowGroups;
-  SharedRowGroup rg;
-  rg.seq = -1;
-  rg.qi0 = rg.n_q = rg.q_row0 = 0;
-  rg.part = -1;
-  if (item_ok && lw < n_rg) rg = item.rg[lw];
-  bool mine = item_ok && lw < n_rg && rg.seq >= 0 && rg.seq < p.num_seqs && rg.qi0 >= 0 &&
-              rg.n_q >= 1 && rg.n_q * G <= kRowsPerTile && rg.q_row0 >= 0 &&
-              rg.q_row0 + rg.n_q <= p.total_q;
+  const int head = (blockIdx.x - p.num_indep_ctas) * kSharedItemsPerCta + pair;
   uint8_t *ring = smem + pair * kSharedRowGroups * C::kRingBytes;  // the pair's warps' rings
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::kBarOffset) + pair * 2 * kS;
   uint64_t *empty = full + kS;
@@ -424,43 +414,103 @@ __device__ __forceinline__ void shared_cta(const CUtensorMap &pool_map, const De
       mbar_init(smem_u32(&empty[s]), kSharedRowGroups);
     }
     fence_mbar_init();
-    if (!item_ok && n_rg != 0) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
   }
-  // q rows, lengths and the first table window are not written by the kernels
-  // this one follows: read before the programmatic-launch wait
+  auto item_ok = [&](const SharedItem &it) {
+    return it.seq0 >= 0 && it.seq0 < p.num_seqs && it.h >= 0 && it.h < hkv && it.kb_begin >= 0 &&
+           it.kb_begin <= it.kb_end && it.kb_end <= p.max_blocks_per_seq && it.n_rg >= 1 &&
+           it.n_rg <= kSharedRowGroups;
+  };
+  auto next_of = [&](int idx, const SharedItem &it) {
+    return it.next > idx && it.next < p.num_shared_items ? it.next : -1;
+  };
+  const int first = head < p.num_shared_items ? head : -1;
+
+  // ---- producer state (the pair's first warp; whole warp, uniform): item
+  // p_idx, its next block p_j of p_n, and a table window (lane i holds entry
+  // win_base + i of the item's sequence)
+  int p_idx = first, p_j = 0, p_n = 0, p_seq = 0, p_h = 0, p_kb0 = 0, p_next = -1;
+  int win_base = 0, win_val = -1;
+  auto p_load = [&](int idx) {
+    const SharedItem &it = p.shared[idx];
+    const bool ok = item_ok(it);
+    p_seq = ok ? it.seq0 : 0;
+    p_h = ok ? it.h : 0;
+    p_kb0 = ok ? it.kb_begin : 0;
+    p_n = ok ? it.kb_end - it.kb_begin : 0;
+    p_next = next_of(idx, it);
+    p_j = 0;
+    win_base = p_kb0;
+    win_val = lane < p_n ? __ldg(p.block_tables + (int64_t)p_seq * p.max_blocks_per_seq + p_kb0 + lane)
+                         : -1;
+  };
+  // true when the chain still has a block to issue (moving to later items)
+  auto p_more = [&]() {
+    while (p_idx >= 0 && p_j >= p_n) {
+      p_idx = p_next;
+      if (p_idx >= 0) p_load(p_idx);
+    }
+    return p_idx >= 0;
+  };
+  if (lw == 0 && first >= 0) p_load(first);
+
+  // ---- the consumers' first item: q rows, lengths and the first table window
+  // are not written by the kernels this one follows: read before the wait
+  // the current item: the fields used, its checks, this warp's row group
+  int c_idx = first, c_h = 0, c_kb0 = 0, c_kb1 = 0, c_next = -1;
   uint32_t qa[2 * kL][4];
-  load_q_frags<D>(p, mine ? rg.q_row0 : 0, mine ? rg.n_q * G : 0, h, r, c, qa);
+  SharedRowGroup rg;
   int cu0 = 0, qs = 0, ctx = 0;
-  if (mine) {
-    cu0 = __ldg(p.cu_q_lens + rg.seq);
-    qs = __ldg(p.cu_q_lens + rg.seq + 1) - cu0;
-    ctx = __ldg(p.context_lens + rg.seq);
-    mine = rg.qi0 + rg.n_q <= qs && qs <= ctx && rg.q_row0 == cu0 + rg.qi0 &&
-           kb1 <= (ctx + p.lookahead * qs - qs + rg.qi0 + rg.n_q - 1) / kBlockSize + 1;
-    if (!mine && lane == 0) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
-  }
-  const int32_t *table = p.block_tables + (int64_t)(item_ok ? seq0 : 0) * p.max_blocks_per_seq;
-  int win_base = kb0, win_val = -1;
-  if (lw == 0 && item_ok && kb0 + lane < kb1) win_val = __ldg(table + kb0 + lane);
+  bool cur_ok = false, has_rg = false, mine = false;
+  auto c_setup = [&]() {  // both warps: item c_idx's row group, q and lengths
+    const SharedItem &it = p.shared[c_idx];
+    cur_ok = item_ok(it);
+    const int n_rg = it.n_rg;
+    if (!cur_ok && n_rg != 0 && lw == 0 && lane == 0) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
+    c_h = cur_ok ? it.h : 0;
+    c_kb0 = cur_ok ? it.kb_begin : 0;
+    c_kb1 = cur_ok ? it.kb_end : 0;
+    c_next = next_of(c_idx, it);
+    rg.seq = -1;
+    rg.qi0 = rg.n_q = rg.q_row0 = 0;
+    rg.part = -1;
+    has_rg = cur_ok && lw < n_rg;
+    if (has_rg) rg = it.rg[lw];
+    mine = has_rg && rg.seq >= 0 && rg.seq < p.num_seqs && rg.qi0 >= 0 &&
+           rg.n_q >= 1 && rg.n_q * G <= kRowsPerTile && rg.q_row0 >= 0 &&
+           rg.q_row0 + rg.n_q <= p.total_q;
+    load_q_frags<D>(p, mine ? rg.q_row0 : 0, mine ? rg.n_q * G : 0, c_h, r, c, qa);
+    cu0 = qs = ctx = 0;
+    if (mine) {
+      cu0 = __ldg(p.cu_q_lens + rg.seq);
+      qs = __ldg(p.cu_q_lens + rg.seq + 1) - cu0;
+      ctx = __ldg(p.context_lens + rg.seq);
+      mine = rg.qi0 + rg.n_q <= qs && qs <= ctx && rg.q_row0 == cu0 + rg.qi0 &&
+             c_kb1 <= (ctx + p.lookahead * qs - qs + rg.qi0 + rg.n_q - 1) / kBlockSize + 1;
+      if (!mine && lane == 0) report(p.dev_status, PKV_DEV_PLAN_MISMATCH);
+    }
+  };
+  if (c_idx >= 0) c_setup();
   __syncthreads();  // barrier initialisation visible to every warp
   if (!p.after_prefill) pdl_wait();
-  const int nblk = item_ok ? kb1 - kb0 : 0;
-  int issued = 0;
-  auto issue = [&](int j) {  // the pair's first warp, whole warp
-    const int kb = kb0 + j;
+
+  int issued = 0;  // blocks issued into the pooled ring (the producer's count)
+  auto issue = [&]() {  // the pair's first warp, whole warp: the chain's next block
+    const int kb = p_kb0 + p_j;
     if (kb >= win_base + 32) {
       win_base = kb;
-      win_val = kb + lane < kb1 ? __ldg(table + kb + lane) : -1;
+      win_val = kb + lane < p_kb0 + p_n
+                    ? __ldg(p.block_tables + (int64_t)p_seq * p.max_blocks_per_seq + kb + lane)
+                    : -1;
     }
     const int phys = __shfl_sync(0xffffffffu, win_val, (kb - win_base) & 31);
     const bool ok = phys >= 0 && phys < p.num_blocks;
-    const int s = j % kS;
+    const int s = issued % kS;
     const uint32_t bar = smem_u32(&full[s]);
     if (lane == 0) {
       stage_ok[s] = ok ? 1 : 0;
       if (ok) {
         mbar_arrive_expect_tx(bar, C::kStageBytes);
-        const int row_k = ((phys * 2 + 0) * hkv + h) * kBlockSize;
+        const int row_k = ((phys * 2 + 0) * hkv + p_h) * kBlockSize;
         const uint32_t dst = smem_u32(ring + s * C::kStageBytes);
         tma_load_4d(dst, &pool_map, 0, 0, 0, row_k >> 3, bar);
         tma_load_4d(dst + C::kSlabBytes, &pool_map, 0, 0, 0, (row_k + hkv * kBlockSize) >> 3, bar);
@@ -469,65 +519,73 @@ __device__ __forceinline__ void shared_cta(const CUtensorMap &pool_map, const De
         mbar_arrive(bar);  // complete the phase without data; the block is skipped
       }
     }
+    ++p_j;
     ++issued;
   };
   if (lw == 0)
-    for (int j = 0; j < min(nblk, kS); ++j) issue(j);
+    for (int k = 0; k < kS && p_more(); ++k) issue();
 
   const float sl2 = p.scale_log2;
-  const int R = mine ? rg.n_q * G : 0;
-  const int q_pos0 = ctx - qs + rg.qi0;
-  const int lim_lo = r < R ? q_pos0 + r / G : -1;
-  const int lim_hi = r + 8 < R ? q_pos0 + (r + 8) / G : -1;
-  float o[kNt][4];
-#pragma unroll
-  for (int nt = 0; nt < kNt; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
-  float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
   bool good = true;
-  int done = 0;
-  for (int j = 0; j < nblk; ++j) {
-    const int s = j % kS;
-    const uint32_t par = (uint32_t)((j / kS) & 1);
-    if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full[s]), par))) {
-      if (lane == 0) report(p.dev_status, PKV_DEV_TIMEOUT);
-      good = false;
-      break;
-    }
-    ++done;
-    if (mine && stage_ok[s]) {
-      const uint32_t sK = smem_u32(ring + s * C::kStageBytes);
-      block_update<D>(sK, sK + C::kSlabBytes, qa, (kb0 + j) * kBlockSize, q_pos0, lim_lo, lim_hi,
-                      sl2, r, c, m_lo, m_hi, l_lo, l_hi, o);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
-    if (lw == 0 && j + kS < nblk) {  // refill once both warps released the stage
-      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[s]), par))) {
+  int done = 0;  // blocks consumed (both warps walk the same chain)
+  while (c_idx >= 0 && good) {
+    const int R = mine ? rg.n_q * G : 0;
+    const int q_pos0 = ctx - qs + rg.qi0;
+    const int lim_lo = r < R ? q_pos0 + r / G : -1;
+    const int lim_hi = r + 8 < R ? q_pos0 + (r + 8) / G : -1;
+    const int kb0 = c_kb0;
+    const int nblk = c_kb1 - c_kb0;
+    float o[kNt][4];
+#pragma unroll
+    for (int nt = 0; nt < kNt; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+    float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+    for (int j = 0; j < nblk; ++j) {
+      const int s = done % kS;
+      const uint32_t par = (uint32_t)((done / kS) & 1);
+      if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&full[s]), par))) {
         if (lane == 0) report(p.dev_status, PKV_DEV_TIMEOUT);
         good = false;
         break;
       }
-      issue(j + kS);
+      ++done;
+      if (mine && stage_ok[s]) {
+        const uint32_t sK = smem_u32(ring + s * C::kStageBytes);
+        block_update<D>(sK, sK + C::kSlabBytes, qa, (kb0 + j) * kBlockSize, q_pos0, lim_lo,
+                        lim_hi, sl2, r, c, m_lo, m_hi, l_lo, l_hi, o);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+      if (lw == 0 && p_more()) {  // refill once both warps released the stage
+        if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&empty[s]), par))) {
+          if (lane == 0) report(p.dev_status, PKV_DEV_TIMEOUT);
+          good = false;
+          break;
+        }
+        issue();
+      }
     }
+    if (!good) break;
+    if (mine) {
+      Piece pc;
+      pc.seq = rg.seq;
+      pc.qi0 = rg.qi0;
+      pc.n_q = rg.n_q;
+      pc.h = c_h;
+      pc.kb_begin = kb0;
+      pc.kb_end = c_kb1;
+      pc.part = rg.part;
+      pc.q_row0 = rg.q_row0;
+      write_piece<D>(p, pc, o, m_lo, m_hi, l_lo, l_hi, R, cu0, r, c);
+    } else if (has_rg) {  // this warp's row group, which could not be attended
+      poison_piece(p, rg.part, lane);
+    }
+    c_idx = c_next;
+    if (c_idx >= 0) c_setup();
   }
   // the issuing warp's copies still in flight land before the CTA exits
   if (lw == 0 && lane == 0)
     for (int j = done; j < issued; ++j)
       mbar_wait(smem_u32(&full[j % kS]), (uint32_t)((j / kS) & 1));
-  if (good && mine) {
-    Piece pc;
-    pc.seq = rg.seq;
-    pc.qi0 = rg.qi0;
-    pc.n_q = rg.n_q;
-    pc.h = h;
-    pc.kb_begin = kb0;
-    pc.kb_end = kb1;
-    pc.part = rg.part;
-    pc.q_row0 = rg.q_row0;
-    write_piece<D>(p, pc, o, m_lo, m_hi, l_lo, l_hi, R, cu0, r, c);
-  } else if (good && item_ok && lw < n_rg) {
-    poison_piece(p, rg.part, lane);
-  }
 }
 
 template <int D, int NSTAGE>
@@ -857,6 +915,7 @@ DecodeParams make_params(const AttnArgs &a) {
   p.warp_head = a.warp_head;
   p.shared = a.shared_items;
   p.num_indep_ctas = (a.num_decode_warps + kWarps - 1) / kWarps;
+  p.num_shared_items = a.num_shared_items;
   p.pieces = a.pieces;
   p.merges = a.merge_groups;
   p.part_o = a.part_o;

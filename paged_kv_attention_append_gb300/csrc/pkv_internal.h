@@ -22,7 +22,7 @@ constexpr int kDecodeWarpsPerCta = 4;
 //    ids: a warp reads its range and head with two independent loads and can
 //    start its first copies without waiting for a block-table read)
 //   [Piece x num_decode_pieces][MergeGroup x num_merge_groups]
-//   [SharedItem x num_shared_ctas * kSharedItemsPerCta]
+//   [SharedItem x num_shared_items]  (pair k's first item at index k)
 //   [prefill_begin: int32 x (num_prefill_ctas + 1), padded to 32 B; absent when 0 CTAs]
 //   [PrefillTile x num_prefill_tiles, grouped by CTA]
 //   [GatherRow x num_gather_rows] (the query tokens of gathered sub-tiles)
@@ -68,8 +68,10 @@ struct WarpHead {
 };
 static_assert(sizeof(WarpHead) == 48, "warp head is 48 bytes");
 
-// Shared-block work for one pair of split-KV warps (a CTA runs
-// kSharedItemsPerCta of them): row groups that read the same blocks -- of one
+// Shared-block work for one pair of split-KV warps (a CTA has
+// kSharedItemsPerCta pairs; pair k of the shared CTAs starts with item k and
+// runs the items chained from it through `next`, which is -1 after the last
+// and otherwise a later index): row groups that read the same blocks -- of one
 // verify window wider than 16 rows, or of sequences whose block tables start
 // with the same physical blocks -- read them once, each of the pair's warps
 // attending one row group to every loaded block.  Blocks kb_begin .. kb_end-1 of
@@ -92,7 +94,8 @@ struct SharedItem {
   int32_t kb_begin;
   int32_t kb_end;
   int32_t n_rg;
-  int32_t pad[3];
+  int32_t next;  // the pair's next item, or -1
+  int32_t pad[2];
   SharedRowGroup rg[kSharedRowGroups];
 };
 static_assert(sizeof(SharedItem) == 32 + 32 * kSharedRowGroups, "shared item layout");
@@ -222,6 +225,7 @@ struct AttnArgs {
   int32_t num_decode_warps;
   const SharedItem *shared_items;
   int32_t num_shared_ctas;
+  int32_t num_shared_items;   // SharedItem entries (the CTAs' pairs' chains)
   const Piece *pieces;
   const MergeGroup *merge_groups;
   int32_t num_merge_groups;

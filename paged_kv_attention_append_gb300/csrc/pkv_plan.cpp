@@ -336,75 +336,86 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   // complete, starts on each SM as soon as that SM's CTA has finished.
   const int32_t pf_sms = num_sms, dec_sms = num_sms;
 
-  // ---- shared-block items: per stream and KV head, its row groups in pairs (one
-  // item per pair of warps), the stream cut into equal chunks.  A chunk of B
-  // blocks holds two warp slots for about B block steps, as long as a warp range
-  // of B blocks; the chunk length is the smallest (from half a slot's cost) at
-  // which the warps left over for the independent segments carry at most 3/4 of
-  // a chunk each (a pair streams through a ring twice a warp's depth, so it
-  // keeps pace with a somewhat shorter warp range; measured on 4- and 8-token
-  // windows: 3/4 beats 1/2 and 1).
+  // ---- shared-block items: per stream and KV head, its row groups in pairs
+  // (a unit); the units' blocks are laid end to end and cut into P equal
+  // ranges, one per pair of warps, and a pair's items are the parts of the
+  // units its range covers, run one after another (chained through
+  // SharedItem::next, its first item at index = pair).  Under the full load of
+  // the step a pair streams its blocks at about a single warp's rate (both of
+  // its warps attend every block, and a stage is refilled only once both have
+  // released it), so P is where P pairs carrying the shared blocks take as long
+  // as the slots left over for the independent segments (same-box steps with
+  // 4- and 8-token windows, the pair's time per block taken as 3/4, 9/10, 1,
+  // 11/10, 5/4 and 3/2 of a warp's: 1 was best).
   const int64_t slots = (int64_t)dec_sms * kDecodeWarpsPerSm;
   std::vector<SharedItem> sitems;
+  int32_t n_pairs = 0;  // heads: sitems[0 .. n_pairs)
   // shared parts of each (decode unit, KV head): (item, warp slot)
   // (allocated only when there are shared streams)
   std::vector<std::vector<std::array<int32_t, 2>>> unit_shared(streams.empty() ? 0 : dunits.size() * hkv);
   if (!streams.empty()) {
-    int64_t sh_blocks = 0, max_len = 0;
-    for (const Stream &st : streams) {
-      const int64_t pairs = (int64_t)(st.units.size() + kSharedRowGroups - 1) / kSharedRowGroups;
-      sh_blocks += (int64_t)hkv * pairs * st.len;
-      max_len = std::max<int64_t>(max_len, st.len);
-    }
-    const int64_t ind_cost = 2 * total_blocks + 3 * (int64_t)segs.size();
-    const int64_t per_slot =
-        std::max<int64_t>(1, (ind_cost + 2 * kSharedRowGroups * sh_blocks) / slots);
-    auto items_for = [&](int64_t chunk) {
-      int64_t n = 0;
-      for (const Stream &st : streams) {
-        const int64_t pairs = (int64_t)(st.units.size() + kSharedRowGroups - 1) / kSharedRowGroups;
-        n += (int64_t)hkv * pairs * std::max<int64_t>(1, (st.len + chunk - 1) / chunk);
-      }
-      return n;
-    };
-    int64_t chunk = std::max<int64_t>(kMinBlocksPerWarp, per_slot / 2);
-    for (;;) {
-      const int64_t left = slots - kSharedRowGroups * items_for(chunk);
-      if (chunk >= max_len || (left > 0 && 4 * total_blocks <= 3 * left * chunk)) break;
-      chunk = std::min<int64_t>(max_len, chunk + std::max<int64_t>(1, chunk / 8));
-    }
-    for (const Stream &st : streams) {
-      const int64_t nch = std::max<int64_t>(1, (st.len + chunk - 1) / chunk);
+    // the units, in stream order: (stream, KV head, first row group)
+    std::vector<std::array<int32_t, 3>> units;
+    int64_t sh_blocks = 0;
+    for (size_t si = 0; si < streams.size(); ++si) {
+      const Stream &st = streams[si];
       for (int32_t h = 0; h < hkv; ++h)
-        for (size_t i0 = 0; i0 < st.units.size(); i0 += kSharedRowGroups)
-          for (int64_t ci = 0; ci < nch; ++ci) {
-            SharedItem it;
-            std::memset(&it, 0, sizeof it);
-            it.seq0 = st.seq0;
-            it.h = h;
-            it.kb_begin = (int32_t)(st.len * ci / nch);
-            it.kb_end = (int32_t)(st.len * (ci + 1) / nch);
-            it.n_rg = (int32_t)std::min<size_t>(kSharedRowGroups, st.units.size() - i0);
-            for (int32_t w = 0; w < it.n_rg; ++w) {
-              const DUnit &du = dunits[st.units[i0 + w]];
-              it.rg[w].seq = du.seq;
-              it.rg[w].qi0 = du.qi0;
-              it.rg[w].n_q = du.n_q;
-              it.rg[w].part = -1;
-              it.rg[w].q_row0 = cu_q_lens[du.seq] + du.qi0;
-              unit_shared[(size_t)st.units[i0 + w] * hkv + h].push_back({(int32_t)sitems.size(), w});
-            }
-            sitems.push_back(it);
-          }
+        for (size_t i0 = 0; i0 < st.units.size(); i0 += kSharedRowGroups) {
+          units.push_back({(int32_t)si, h, (int32_t)i0});
+          sh_blocks += st.len;
+        }
     }
-    // a CTA runs kSharedItemsPerCta items: pad with empty ones
-    while (sitems.size() % kSharedItemsPerCta) {
-      SharedItem it;
-      std::memset(&it, 0, sizeof it);
-      sitems.push_back(it);
+    // independent load in block steps of one warp: its blocks plus 3 per segment
+    const int64_t ind = total_blocks + 3 * (int64_t)segs.size();
+    const int64_t max_pairs = std::max<int64_t>(1, slots / kSharedRowGroups - (ind > 0 ? 1 : 0));
+    int64_t np2 = ind > 0 ? (sh_blocks * slots) / (ind + 2 * sh_blocks) : max_pairs;
+    np2 = std::max<int64_t>(1, std::min<int64_t>({np2, max_pairs, sh_blocks / kMinBlocksPerWarp}));
+    // whole CTAs
+    n_pairs = (int32_t)(np2 + (np2 % kSharedItemsPerCta ? kSharedItemsPerCta - np2 % kSharedItemsPerCta : 0));
+    sitems.assign(n_pairs, SharedItem{});
+    for (int32_t k = 0; k < n_pairs; ++k) {
+      std::memset(&sitems[k], 0, sizeof(SharedItem));
+      sitems[k].next = -1;  // an empty pair (n_rg == 0) until it gets an item
+    }
+    size_t u = 0;
+    int64_t u_off = 0;  // first position of unit u
+    for (int32_t k = 0; k < n_pairs; ++k) {
+      const int64_t lo = sh_blocks * k / n_pairs, hi = sh_blocks * (k + 1) / n_pairs;
+      int32_t prev = -1;
+      for (int64_t a = lo; a < hi;) {
+        while (u_off + streams[units[u][0]].len <= a) u_off += streams[units[u++][0]].len;
+        const Stream &st = streams[units[u][0]];
+        const int64_t e = std::min<int64_t>(hi, u_off + st.len);
+        SharedItem it;
+        std::memset(&it, 0, sizeof it);
+        it.seq0 = st.seq0;
+        it.h = units[u][1];
+        it.kb_begin = (int32_t)(a - u_off);
+        it.kb_end = (int32_t)(e - u_off);
+        const size_t i0 = (size_t)units[u][2];
+        it.n_rg = (int32_t)std::min<size_t>(kSharedRowGroups, st.units.size() - i0);
+        it.next = -1;
+        const int32_t idx = prev < 0 ? k : (int32_t)sitems.size();
+        for (int32_t w = 0; w < it.n_rg; ++w) {
+          const DUnit &du = dunits[st.units[i0 + w]];
+          it.rg[w].seq = du.seq;
+          it.rg[w].qi0 = du.qi0;
+          it.rg[w].n_q = du.n_q;
+          it.rg[w].part = -1;
+          it.rg[w].q_row0 = cu_q_lens[du.seq] + du.qi0;
+          unit_shared[(size_t)st.units[i0 + w] * hkv + it.h].push_back({idx, w});
+        }
+        if (prev < 0)
+          sitems[k] = it;
+        else
+          sitems.push_back(it);
+        if (prev >= 0) sitems[prev].next = idx;
+        prev = idx;
+        a = e;
+      }
     }
   }
-  const int64_t shared_slots = (int64_t)sitems.size() * kSharedRowGroups;
+  const int64_t shared_slots = (int64_t)n_pairs * kSharedRowGroups;
 
   // ---- gathered sub-tiles (tc groups): per group and KV head, the members'
   // query tokens in sub-tiles of up to 128 / G tokens (G rows each), neighbours
@@ -895,7 +906,8 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   info->num_prefill_merges = (int32_t)pmerges.size();
   info->num_kernels = (num_warps > 0 || !sitems.empty() ? 1 : 0) + (merges.empty() ? 0 : 1) +
                       (ptiles.empty() ? 0 : 1);
-  info->num_shared_ctas = (int32_t)(sitems.size() / kSharedItemsPerCta);
+  info->num_shared_ctas = n_pairs / kSharedItemsPerCta;
+  info->num_shared_items = (int32_t)sitems.size();
   info->num_gather_rows = (int32_t)gather.size();
   info->merge_rows = merge_rows;
   info->max_blocks_needed = max_nb;

@@ -51,8 +51,10 @@ def parse_plan(info, host):
     off_m = off_p + 8 * npc
     ncta = info.num_prefill_ctas
     nsh = info.num_shared_ctas
+    nitems = info.num_shared_items
+    assert nitems >= 2 * nsh             # two warp pairs per shared CTA, each starting a chain
     off_s = off_m + 8 * nm
-    off_b = off_s + 24 * 2 * nsh         # two 96-byte items per shared CTA
+    off_b = off_s + 24 * nitems          # 96-byte items
     off_f = off_b + (((ncta + 1 + 7) // 8) * 8 if ncta else 0)
     off_g = off_f + 16 * npf
     ng = info.num_gather_rows
@@ -66,7 +68,22 @@ def parse_plan(info, host):
     mer = words[off_m:off_s].reshape(nm, 8)
     pre = words[off_f:off_g].reshape(npf, 16)
     parse_plan.gather = words[off_g:off_g + 4 * ng].reshape(ng, 4)
-    parse_plan.shared = words[off_s:off_b].reshape(2 * nsh, 24)
+    parse_plan.shared = words[off_s:off_b].reshape(nitems, 24)
+    if nitems:
+        # every item is on exactly one pair's chain: pair k starts at item k and
+        # each `next` (word 5) names a later item or is -1
+        seen = np.zeros(nitems, bool)
+        for k in range(2 * nsh):
+            i = k
+            while i >= 0:
+                assert not seen[i]
+                seen[i] = True
+                nxt = int(parse_plan.shared[i, 5])
+                assert nxt == -1 or i < nxt < nitems
+                if nxt != -1:
+                    assert nxt >= 2 * nsh        # the chains' other items follow the heads
+                i = nxt
+        assert seen.all()
     pb = words[off_b:off_b + ncta + 1] if ncta else np.zeros(1, np.int32)
     if ncta:
         assert pb[0] == 0 and pb[-1] == npf and np.all(np.diff(pb) >= 1)   # no CTA without work
@@ -155,8 +172,8 @@ def check_plan(meta, info, host, num_sms):
             cost = [2 * per_warp[w] + 6 * int((pieces[wb[w]:wb[w + 1], 4] == 0).sum())
                     for w in range(nw)]
             assert max(cost) - min(cost) <= 2 * (2 + 6)
-        if num_sms is not None:
-            assert nw + 2 * len(sh) <= num_sms * 8
+        if num_sms is not None:      # warp slots: independent warps, then two per pair
+            assert nw + 2 * 2 * info.num_shared_ctas <= num_sms * 8
     assert np.all(pieces[:, 5] > pieces[:, 4])
     pieces = np.concatenate([pieces, sh_pieces])
     # every decode segment (row group x KV head) is covered exactly once, in order
