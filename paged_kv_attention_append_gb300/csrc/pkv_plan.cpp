@@ -101,6 +101,12 @@ struct PlanScratch {
   std::vector<int32_t> warp_begin, seg_first, seg_count, seg_of, unit_kb0, shared_len;
   std::vector<int64_t> cut;
   std::vector<MergeGroup> merges;
+  std::vector<std::array<int32_t, 3>> sh_ref;  // (unit * hkv + h, item, warp slot)
+  std::vector<std::array<int32_t, 2>> sh_list;  // (item, warp slot) grouped by key
+  std::vector<int32_t> sh_begin;                // key k: sh_list[sh_begin[k] .. sh_begin[k+1])
+  std::vector<int32_t> sh_fill;
+  std::vector<std::array<int32_t, 3>> sh_units;
+  std::vector<SharedItem> sitems;
 };
 thread_local PlanScratch t_scratch;
 
@@ -348,14 +354,17 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   // 4- and 8-token windows, the pair's time per block taken as 3/4, 9/10, 1,
   // 11/10, 5/4 and 3/2 of a warp's: 1 was best).
   const int64_t slots = (int64_t)dec_sms * kDecodeWarpsPerSm;
-  std::vector<SharedItem> sitems;
+  std::vector<SharedItem> &sitems = S.sitems;
+  sitems.clear();
   int32_t n_pairs = 0;  // heads: sitems[0 .. n_pairs)
-  // shared parts of each (decode unit, KV head): (item, warp slot)
-  // (allocated only when there are shared streams)
-  std::vector<std::vector<std::array<int32_t, 2>>> unit_shared(streams.empty() ? 0 : dunits.size() * hkv);
+  // shared parts of each (decode unit, KV head): (item, warp slot) in key order
+  // of the units' blocks, gathered into sh_list below
+  std::vector<std::array<int32_t, 3>> &sh_ref = S.sh_ref;
+  sh_ref.clear();
   if (!streams.empty()) {
     // the units, in stream order: (stream, KV head, first row group)
-    std::vector<std::array<int32_t, 3>> units;
+    std::vector<std::array<int32_t, 3>> &units = S.sh_units;
+    units.clear();
     int64_t sh_blocks = 0;
     for (size_t si = 0; si < streams.size(); ++si) {
       const Stream &st = streams[si];
@@ -372,11 +381,11 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
     np2 = std::max<int64_t>(1, std::min<int64_t>({np2, max_pairs, sh_blocks / kMinBlocksPerWarp}));
     // whole CTAs
     n_pairs = (int32_t)(np2 + (np2 % kSharedItemsPerCta ? kSharedItemsPerCta - np2 % kSharedItemsPerCta : 0));
-    sitems.assign(n_pairs, SharedItem{});
-    for (int32_t k = 0; k < n_pairs; ++k) {
-      std::memset(&sitems[k], 0, sizeof(SharedItem));
-      sitems[k].next = -1;  // an empty pair (n_rg == 0) until it gets an item
-    }
+    // a pair's range starts at most one item beyond the units it covers
+    sitems.reserve((size_t)n_pairs + units.size() + (size_t)n_pairs);
+    sitems.resize(n_pairs);
+    std::memset(sitems.data(), 0, (size_t)n_pairs * sizeof(SharedItem));
+    for (int32_t k = 0; k < n_pairs; ++k) sitems[k].next = -1;  // empty (n_rg == 0) until it gets an item
     size_t u = 0;
     int64_t u_off = 0;  // first position of unit u
     for (int32_t k = 0; k < n_pairs; ++k) {
@@ -403,7 +412,7 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
           it.rg[w].n_q = du.n_q;
           it.rg[w].part = -1;
           it.rg[w].q_row0 = cu_q_lens[du.seq] + du.qi0;
-          unit_shared[(size_t)st.units[i0 + w] * hkv + it.h].push_back({idx, w});
+          sh_ref.push_back({(int32_t)((size_t)st.units[i0 + w] * hkv + it.h), idx, w});
         }
         if (prev < 0)
           sitems[k] = it;
@@ -414,6 +423,20 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
         a = e;
       }
     }
+  }
+  // sh_ref grouped by key (a counting sort; each key keeps its creation order,
+  // i.e. its blocks' order)
+  std::vector<std::array<int32_t, 2>> &sh_list = S.sh_list;
+  std::vector<int32_t> &sh_begin = S.sh_begin;
+  if (!sh_ref.empty()) {
+    const size_t nkeys = dunits.size() * (size_t)hkv;
+    sh_begin.assign(nkeys + 1, 0);
+    for (const auto &rf : sh_ref) ++sh_begin[rf[0] + 1];
+    for (size_t k = 0; k < nkeys; ++k) sh_begin[k + 1] += sh_begin[k];
+    sh_list.resize(sh_ref.size());
+    std::vector<int32_t> &fill = S.sh_fill;  // per-key fill positions
+    fill.assign(sh_begin.begin(), sh_begin.end() - 1);
+    for (const auto &rf : sh_ref) sh_list[fill[rf[0]]++] = {rf[1], rf[2]};
   }
   const int64_t shared_slots = (int64_t)n_pairs * kSharedRowGroups;
 
@@ -683,7 +706,6 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
     // gathered prefix chunks always write partials: their unit gets a merge
     // group even when nothing else splits it
     std::vector<int32_t> casc_part0(gather.empty() ? 0 : dunits.size() * hkv, -1);
-    static const std::vector<std::array<int32_t, 2>> kNoShared;
     merges.resize(dunits.size() * (size_t)hkv);  // at most one group per (unit, KV head)
     MergeGroup *mg = merges.data();
     const int32_t *so = seg_of.data(), *sf = seg_first.data(), *sc = seg_count.data();
@@ -692,16 +714,18 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
       const DUnit du = dunits[u];
       const int32_t nc = unit_casc[u];
       for (int32_t h = 0; h < hkv; ++h) {
-        const auto &sh = unit_shared.empty() ? kNoShared : unit_shared[u * hkv + h];
+        const size_t key = u * hkv + h;
+        const int32_t sh0 = sh_ref.empty() ? 0 : sh_begin[key];
+        const int32_t sh1 = sh_ref.empty() ? 0 : sh_begin[key + 1];
         const int32_t k = so[u * hkv + h];
         const int32_t np = k >= 0 ? sc[k] : 0;
-        const int32_t total = nc + (int32_t)sh.size() + np;
+        const int32_t total = nc + (sh1 - sh0) + np;
         if (total <= 1 && nc == 0) continue;
         mg[nm++] = {du.seq, du.qi0, du.n_q, h, parts, total, 0, cu_q_lens[du.seq] + du.qi0};
         merge_rows = std::max(merge_rows, du.n_q * group);
         if (!casc_part0.empty()) casc_part0[u * hkv + h] = nc > 0 ? parts : -1;
         parts += nc;
-        for (const auto &si : sh) sitems[si[0]].rg[si[1]].part = parts++;
+        for (int32_t t = sh0; t < sh1; ++t) sitems[sh_list[t][0]].rg[sh_list[t][1]].part = parts++;
         Piece *pc = pieces + (k >= 0 ? sf[k] : 0);
         for (int32_t t = 0; t < np; ++t) pc[t].part = parts++;
       }
