@@ -774,3 +774,29 @@ def test_shared_prefix_random_steps_match_oracle(pkv, cuda_device, seed, num_seq
     for sms in (152, 9):
         out, _, _ = gpu_step(pkv, meta, q, k, v, pool, cuda_device, num_sms=sms)
         assert_close(out, want, f"seed {seed} sms {sms}")
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_verify_windows_chained_shared_items_match_oracle(pkv, cuda_device, seed):
+    """Verify windows of 8 tokens (two row groups that read the same blocks) go to
+    shared-block CTAs whose warp pairs run chains of items (items that split a
+    window's blocks between pairs; with 1 or 3 SMs the planner keeps the windows
+    on the per-warp ranges instead).  Every row against the oracle, and the
+    chains really occur."""
+    rng = np.random.default_rng(900 + seed)
+    n = 12
+    q_lens = [8 if i % 2 == 0 else 4 for i in range(n)]
+    ctx = [int(c) for c in rng.integers(160, 1500, size=n)]
+    meta = workloads.build_step("windows", 77 + seed, q_lens, ctx, 8, 2, 128, rng=rng)
+    q, k, v, pool = workloads.make_values(meta)
+    want, _ = oracle.run_step(meta, q, k, v, pool)
+    chained = False
+    for sms in (1, 3, 9, 37, 152):
+        info, _ = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads,
+                                pkv.pool_desc(pool), num_sms=sms, upload=False,
+                                block_tables=meta.block_tables)
+        assert info.num_shared_ctas > 0 or sms < 9
+        chained |= info.num_shared_items > 2 * info.num_shared_ctas
+        out, _, _ = gpu_step(pkv, meta, q, k, v, pool, cuda_device, num_sms=sms)
+        assert_close(out, want, f"windows seed {seed} sms {sms}")
+    assert chained
