@@ -26,7 +26,8 @@
 // tensor-core kernel as gathered sub-tiles: 128 rows (token x query head) taken
 // from all those sequences attend one key tile per MMA, each row writing a
 // partial result that the merge combines with its own suffix.  Smaller groups
-// use split-KV CTAs that stream the prefix once for up to 4 row groups.
+// use split-KV CTAs whose warp pairs stream the prefix once for two row groups
+// (as the two row groups of a wide verify window share their blocks).
 //
 // Prefill-class rows (tensor-core kernel): sequences with at least 64 query
 // tokens are cut into units of 128 query tokens x one query head.  Units of the
