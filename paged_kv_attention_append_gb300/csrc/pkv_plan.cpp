@@ -495,19 +495,21 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
     }
     if (!cpairs.empty()) {
       // The items take a share of the SMs; the split-KV kernel streams the
-      // step's own blocks on the rest meanwhile (its warps there take a larger
-      // share of the blocks: see the warp cut below).  Share = prefix tile
-      // passes / (tile passes + streamed block-heads / 16), at least 15/32:
-      // with that cut, a tile pass weighed as 16 block-heads put both
-      // shared-prefix workloads at their measured optimum (80 and 72 of 152
-      // SMs).  Integer arithmetic, so every host plans alike.
+      // step's own blocks on the rest meanwhile (only there: see the warp
+      // count below).  Share = prefix tile passes / (tile passes + streamed
+      // block-heads / 16), at least 7/16: a tile pass weighed as 16
+      // block-heads and that floor put both shared-prefix workloads at their
+      // measured optimum (same box, chunks per pair one fewer and one more:
+      // shared-prefix verify 80 of 152 SMs, 49.7 us against 50.1 at 64 and
+      // 58.1 at 96; MTP draft 64, 45.2 us against 47.7 at 56, 47.3 at 72 and
+      // 50.8 at 80).  Integer arithmetic, so every host plans alike.
       int64_t pf_work = 0;
       for (const CPair &cp : cpairs) pf_work += (int64_t)cp.nsub * (groups[cp.gi].len / kKeyTileBlocks);
       const int64_t ncp = (int64_t)cpairs.size();
       int64_t num = 16 * pf_work, den = 16 * pf_work + total_blocks;  // share = num / den
-      if (32 * num < 15 * den) {
-        num = 15;
-        den = 32;
+      if (16 * num < 7 * den) {
+        num = 7;
+        den = 16;
       }
       const int64_t want = std::max<int64_t>(1, (2 * num * pf_sms + den * ncp) / (2 * den * ncp));
       for (const CPair &cp : cpairs) {
@@ -554,6 +556,16 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   // (agent-shaped step, same box: 146.5 -> 144.3 us; 2/3 and 2/5 of the slots
   // in between, a quarter 149.7).
   if (!pairs.empty()) nw64 = std::min<int64_t>(nw64, std::max<int64_t>(1, avail / 2));
+  // With gathered prefix items as the step's only tensor-core work, the
+  // lowest-index split-KV CTAs start at once on the SMs the items leave free
+  // and stream while the items run; the others could start only as the items'
+  // CTAs exit, and then need several latency-bound us for however few blocks.
+  // So the split-KV work goes to the free SMs' warp slots alone (same box:
+  // shared-prefix verify 55.6 -> 49.7 us, MTP draft 49.5 -> 47.3 us against
+  // the same warps taking 4 times a late warp's share, 54.0 / 49.1 at 8 times).
+  if (pairs.empty() && !casc_items.empty() && (int64_t)casc_items.size() < dec_sms)
+    nw64 = std::min<int64_t>(nw64, std::max<int64_t>(1, (dec_sms - (int64_t)casc_items.size()) *
+                                                            kDecodeWarpsPerSm));
   // Small steps: when every segment fits a warp slot and the longest is within a
   // few blocks of the equal share, one warp per whole segment runs about as long
   // as the equal-cost cut and needs no partials or merge launch.
@@ -594,35 +606,6 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
     // at least kMinBlocksPerWarp blocks per warp every share holds a block.
     constexpr int64_t kBlockCost = 2, kPieceCost = 6;
     const int64_t total_cost = kBlockCost * total_blocks + kPieceCost * (int64_t)segs.size();
-    // Warps of the split-KV CTAs dispatched first: when gathered prefix items
-    // are the step's only tensor-core work and leave SMs free, the lowest-index
-    // CTAs start on those SMs at once and stream while the items run; the rest
-    // start only as the items' CTAs exit.  With equal shares the early CTAs
-    // finished soon after the items and their SMs then sat idle while the late
-    // ones streamed; the early warps now take kEarlyWeight / kLateWeight times
-    // a late warp's share of the cost (4:1 measured best of 2:1 .. 5:1 on both
-    // shared-prefix workloads).  The order in which CTAs are dispatched only
-    // moves the balance, never the result.
-    constexpr int64_t kEarlyWeight = 4, kLateWeight = 1;
-    constexpr int kMaxGroups = 2;
-    int ngroups = 1;  // warps gbeg[g] .. gbeg[g+1]-1 take weight gwt[g]
-    int64_t gbeg[kMaxGroups + 1] = {0, (int64_t)num_warps, (int64_t)num_warps};
-    int64_t gwt[kMaxGroups] = {1, 1};
-    if (pairs.empty() && !casc_items.empty() && (int64_t)casc_items.size() < dec_sms) {
-      ngroups = 2;
-      gbeg[1] = std::min<int64_t>(num_warps,
-                                  (dec_sms - (int64_t)casc_items.size()) * kDecodeWarpsPerSm);
-      gwt[0] = kEarlyWeight;
-      gwt[1] = kLateWeight;
-    }
-    int64_t ctot = 0;  // the warps' summed weights
-    for (int g = 0; g < ngroups; ++g) ctot += gwt[g] * (gbeg[g + 1] - gbeg[g]);
-    // group of warp w (w never decreases between calls: walked forward)
-    int cgrp = 0;
-    auto grp = [&](int64_t w) {
-      while (cgrp + 1 < ngroups && w >= gbeg[cgrp + 1]) ++cgrp;
-      return cgrp;
-    };
     std::vector<int64_t> &cut = S.cut;  // first block of each warp
     cut.assign(num_warps + 1, total_blocks);
     cut[0] = 0;
@@ -634,26 +617,16 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
       }
     } else {
       // warp w >= 1 starts at the first block whose midpoint m satisfies
-      // m * ctot >= X(w) = (summed weights of warps 0 .. w-1) * total_cost, i.e.
-      // m >= T(w) = ceil(X(w) / ctot); the midpoints of a segment starting at
-      // cost c are c + kPieceCost + kBlockCost * i + kBlockCost / 2.  X(w) / ctot
-      // is carried from warp to warp as a quotient and remainder (X grows by
-      // the warp's weight times total_cost), so the whole cut takes no
-      // division per warp or per segment.
+      // m * num_warps >= w * total_cost, i.e. m >= T(w) = ceil(w * total_cost /
+      // num_warps); the midpoints of a segment starting at cost c are c +
+      // kPieceCost + kBlockCost * i + kBlockCost / 2.  w * total_cost /
+      // num_warps is carried from warp to warp as a quotient and remainder, so
+      // the whole cut takes no division per warp or per segment.
       static_assert(kBlockCost == 2, "the block index below halves a cost distance");
-      const int64_t cdiv = std::max<int64_t>(ctot, 1);  // ctot is 0 only without warps
-      int64_t dq[kMaxGroups], dr[kMaxGroups];  // a warp's weight x total_cost over ctot
-      for (int g = 0; g < ngroups; ++g) {
-        dq[g] = gwt[g] * total_cost / cdiv;
-        dr[g] = gwt[g] * total_cost % cdiv;
-      }
-      int64_t tq = 0, tr = 0;  // X(w) = tq * ctot + tr, 0 <= tr < ctot
+      const int64_t nwd = std::max<int64_t>(num_warps, 1);
+      const int64_t dq = total_cost / nwd, dr = total_cost % nwd;
+      int64_t tq = dq, tr = dr;  // w * total_cost = tq * num_warps + tr, 0 <= tr < num_warps
       int32_t w = 1;
-      if (num_warps > 1) {
-        const int g0 = grp(0);
-        tq = dq[g0];
-        tr = dr[g0];
-      }
       int64_t cost = 0, blk = 0;
       for (const Segment &g : segs) {
         const int64_t first_mid = cost + kPieceCost + kBlockCost / 2;
@@ -663,14 +636,12 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
           if (last_mid < t) break;
           int64_t i = t > first_mid ? (t - first_mid + 1) >> 1 : 0;  // ceil((t - first_mid) / 2)
           if (i > g.nb - 1) i = g.nb - 1;
-          // the next warp's start grows by this warp's weight
-          const int gw = grp(w);
           cut[w++] = blk + i;
-          tq += dq[gw];
-          tr += dr[gw];
-          if (tr >= cdiv) {
+          tq += dq;
+          tr += dr;
+          if (tr >= nwd) {
             ++tq;
-            tr -= cdiv;
+            tr -= nwd;
           }
         }
         cost += kPieceCost + kBlockCost * g.nb;
