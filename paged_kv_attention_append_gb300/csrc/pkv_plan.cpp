@@ -442,10 +442,10 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   const int64_t shared_slots = (int64_t)n_pairs * kSharedRowGroups;
 
   // ---- gathered sub-tiles (tc groups): per group and KV head, the members'
-  // query tokens in sub-tiles of up to 128 / G tokens (G rows each), neighbours
-  // paired; every pair is cut along the prefix's key tiles into nc equal chunks,
-  // nc chosen so the items about fill their share of the SMs (at least 2 key
-  // tiles each)
+  // query tokens in sub-tiles of up to 128 / G tokens (G rows each); every
+  // sub-tile is cut along the prefix's key tiles into nc equal chunks, one work
+  // item each, nc chosen so the items about fill their share of the SMs (at
+  // least 2 key tiles each)
   std::vector<GatherRow> gather;          // part0 filled once partial slots are known
   std::vector<int32_t> gather_uh;         // (decode unit * hkv + KV head) of each entry
   std::vector<PrefillTile> casc_items;    // already cut along keys
@@ -482,13 +482,17 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
             gather_uh.push_back(tk[0] * hkv + h);
           }
         }
-        for (size_t k = 0; k < subs.size(); k += 2) {
+        // one sub-tile per item: a CTA's two sub-tiles would run as two
+        // passes over the same keys, each paying its start and its partial
+        // epilogue (same box: shared-prefix verify 50.7 -> 45.4 us, MTP draft
+        // 45.3 -> 44.8 us against pairs of sub-tiles)
+        for (size_t k = 0; k < subs.size(); ++k) {
           CPair cp;
           cp.gi = (int32_t)gi;
           cp.h = h;
           cp.sub[0] = subs[k];
-          cp.sub[1] = k + 1 < subs.size() ? subs[k + 1] : Sub{-1, 0};
-          cp.nsub = k + 1 < subs.size() ? 2 : 1;
+          cp.sub[1] = Sub{-1, 0};
+          cp.nsub = 1;
           cpairs.push_back(cp);
         }
       }
@@ -499,10 +503,10 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
       // count below).  Share = prefix tile passes / (tile passes + streamed
       // block-heads / 16), at least 7/16: a tile pass weighed as 16
       // block-heads and that floor put both shared-prefix workloads at their
-      // measured optimum (same box, chunks per pair one fewer and one more:
-      // shared-prefix verify 80 of 152 SMs, 49.7 us against 50.1 at 64 and
-      // 58.1 at 96; MTP draft 64, 45.2 us against 47.7 at 56, 47.3 at 72 and
-      // 50.8 at 80).  Integer arithmetic, so every host plans alike.
+      // measured optimum (same box, one chunk per sub-tile fewer and one more:
+      // shared-prefix verify 64 of 152 SMs, 45.4 us against 60.1 at 32 and
+      // 55.8 at 96; MTP draft 64, 44.8 us against 45.4 at 48 and 49.0 at
+      // 80).  Integer arithmetic, so every host plans alike.
       int64_t pf_work = 0;
       for (const CPair &cp : cpairs) pf_work += (int64_t)cp.nsub * (groups[cp.gi].len / kKeyTileBlocks);
       const int64_t ncp = (int64_t)cpairs.size();
