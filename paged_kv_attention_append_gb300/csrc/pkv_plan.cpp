@@ -553,13 +553,20 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   const int64_t avail = std::max<int64_t>(slots - shared_slots, 1);
   int64_t nw64 = (total_blocks + kMinBlocksPerWarp - 1) / kMinBlocksPerWarp;
   nw64 = std::min<int64_t>(nw64, avail);
-  // Behind a tensor-core prefill over every SM the split-KV CTAs start one after
-  // another, in index order, as its persistent CTAs exit, and a CTA's few blocks
-  // take a latency-bound ~8 us whatever their number: half the warp slots, on
-  // the SMs freed first, finish with the prefill instead of ~9 us after it
+  // Behind a tensor-core prefill whose persistent CTAs take every SM (enough
+  // key tiles for all of them) the split-KV CTAs start one after another, in
+  // index order, as those CTAs exit, and a CTA's few blocks take a
+  // latency-bound ~8 us whatever their number: half the warp slots, on the SMs
+  // freed first, finish with the prefill instead of ~9 us after it
   // (agent-shaped step, same box: 146.5 -> 144.3 us; 2/3 and 2/5 of the slots
-  // in between, a quarter 149.7).
-  if (!pairs.empty()) nw64 = std::min<int64_t>(nw64, std::max<int64_t>(1, avail / 2));
+  // in between, a quarter 149.7).  A smaller prefill leaves SMs free from the
+  // start and keeps every slot.
+  if (!pairs.empty()) {
+    int64_t pf_tiles = 0;
+    for (const auto &nt : pair_nt) pf_tiles += nt[0] + nt[1];
+    if (pf_tiles >= (int64_t)pf_sms * kMinTilesPerCta)
+      nw64 = std::min<int64_t>(nw64, std::max<int64_t>(1, avail / 2));
+  }
   // With gathered prefix items as the step's only tensor-core work, the
   // lowest-index split-KV CTAs start at once on the SMs the items leave free
   // and stream while the items run; the others could start only as the items'

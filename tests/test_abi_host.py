@@ -634,6 +634,34 @@ def test_planner_asks_the_device_for_its_sm_count(pkv):
     assert e.value.status == 6      # PKV_ERR_CUDA
 
 
+def test_split_kv_warps_beside_a_prefill(pkv):
+    """Behind a prefill whose persistent CTAs take every SM the split-KV work goes
+    to half the warp slots (the CTAs that start first, as those CTAs exit); a
+    small prefill chunk beside many decodes leaves SMs free from the start and
+    keeps every slot; with gathered prefix items only, the split-KV work goes to
+    the warp slots of the SMs the items leave free."""
+    desc = pkv.PoolDesc(60000, 16, 8, 128)
+    # 200 decodes at 2000 keys + a 64-token chunk at 1000: few prefill CTAs
+    q = [1] * 200 + [64]
+    ctx = [2000] * 200 + [1000]
+    cu = np.concatenate([[0], np.cumsum(q)]).astype(np.int32)
+    info, _ = pkv.plan_step(cu, np.array(ctx, np.int32), 40, desc, num_sms=152, upload=False)
+    assert 0 < info.num_prefill_ctas < 152 and info.num_decode_warps == 152 * 8
+    # the agent-shaped step: a 2048-token chunk whose tiles fill every SM
+    meta = workloads.make_config("agent_mixed")
+    info, _ = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads,
+                            pkv.PoolDesc(meta.num_blocks, 16, meta.num_kv_heads, meta.head_dim),
+                            num_sms=152, upload=False, block_tables=meta.block_tables)
+    assert info.num_prefill_ctas == 152 and info.num_decode_warps == 152 * 8 // 2
+    # gathered prefix items only
+    meta = workloads.make_config("shared_prefix_verify")
+    info, _ = pkv.plan_step(meta.cu_q_lens, meta.context_lens, meta.num_q_heads,
+                            pkv.PoolDesc(meta.num_blocks, 16, meta.num_kv_heads, meta.head_dim),
+                            num_sms=152, upload=False, block_tables=meta.block_tables)
+    assert info.num_gather_rows > 0 and info.num_shared_ctas == 0
+    assert info.num_decode_warps == (152 - info.num_prefill_ctas) * 8
+
+
 def test_planning_from_several_threads_gives_each_its_own_plan(pkv):
     """Plans made at the same time on several host threads (the library call
     releases the GIL) are each identical, byte for byte, to the plan made alone."""
