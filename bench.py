@@ -31,8 +31,9 @@ reported under `configs` (--only skips them).
   FLOPs / peak) over the measured step time).
 * e2e: the same metric through the public API from pinned HOST buffers: every
   step copies q, the new K/V, slot mapping, metadata and the plan host->device
-  (one pinned buffer, one transfer), plans on the host into pinned memory, runs
-  append + attention and copies out back (wall time per step).
+  (one pinned buffer, one transfer), plans on the host from the caller's host
+  arrays into pinned memory, runs append + attention and copies out back (wall
+  time per step).
 * cpu_baseline / --impl reference: the fp64 CPU oracle as it stands, on the
   host cores, on a bounded sample of the same workload.
 """
@@ -556,7 +557,11 @@ class StepBench:
         chained workload: all its steps' inputs in, one plan, every output back).
         The step's int32 metadata, every step's bf16 q/k/v and, last, the plan
         (written by the host planner each step) share one pinned buffer, so one
-        copy carries all of them."""
+        copy carries all of them.  The planner reads the caller's own host
+        arrays (lengths and block tables), not their staging copies in that
+        buffer: on Grace, host reads of pinned lines the device copy has just
+        read run slower (a 256-sequence plan 56-58 us from the staging copies,
+        43 us from the caller's arrays, the copy running or not)."""
         import torch
         pkv, dev, stream, meta, info = self.pkv, self.dev, self.stream, self.meta, self.info
 
@@ -587,7 +592,12 @@ class StepBench:
         plan_off = plan_hv.data_ptr() - buf_h.data_ptr()          # bytes, 16-byte aligned
         qkv_dv = dviews[4:-1]
         dvals = [tuple(qkv_dv[3 * t:3 * t + 3]) for t in range(len(self.vals))]
-        cu_np, ctx_np, bt_np, plan_np = cu_h.numpy(), ctx_h.numpy(), bt_h.numpy(), plan_hv.numpy()
+        plan_np = plan_hv.numpy()
+        cu_np = np.ascontiguousarray(self.meta.cu_q_lens, dtype=np.int32)
+        ctx_np = np.ascontiguousarray(self.meta.context_lens, dtype=np.int32)
+        bt_np = np.ascontiguousarray(self.meta.block_tables, dtype=np.int32)
+        assert (np.array_equal(cu_np, cu_h.numpy()) and np.array_equal(ctx_np, ctx_h.numpy())
+                and np.array_equal(bt_np, bt_h.numpy()))
         num_sms = torch.cuda.get_device_properties(dev).multi_processor_count
         outs_h = [torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in self.outs]
         h2d = (plan_off + int(info.plan_bytes) + 15) // 16 * 16  # bytes copied per step
