@@ -32,8 +32,9 @@ reported under `configs` (--only skips them).
 * e2e: the same metric through the public API from pinned HOST buffers: every
   step copies q, the new K/V, slot mapping, metadata and the plan host->device
   (one pinned buffer, one transfer), plans on the host from the caller's host
-  arrays into pinned memory, runs append + attention and copies out back (wall
-  time per step).
+  arrays into pinned memory (on the library's planning thread, while the copy
+  and the KV append are queued), runs append + attention and copies out back
+  (wall time per step).
 * cpu_baseline / --impl reference: the fp64 CPU oracle as it stands, on the
   host cores, on a bounded sample of the same workload.
 """
@@ -610,7 +611,8 @@ class StepBench:
                                self.outs[t], dev_status=self.status, stream=stream)
                  for t, (dq, dk, dv) in enumerate(dvals)]
         planner = pkv.BoundPlan(cu_np, ctx_np, meta.num_q_heads, self.pool, plan_np,
-                                num_sms=num_sms, chain_steps=self.chain_arg, block_tables=bt_np)
+                                num_sms=num_sms, chain_steps=self.chain_arg, block_tables=bt_np,
+                                spin_us=2000)
         up = pkv.BoundCopy(buf_d, buf_h, stream=stream)
         down = [pkv.BoundCopy(oh, o, stream=stream) for oh, o in zip(outs_h, self.outs)]
         times = []
@@ -618,11 +620,13 @@ class StepBench:
             for i in range(args.warmup + args.steps):
                 torch.cuda.synchronize(dev)
                 t0 = time.perf_counter()
-                # the inputs go up and the first step's KV append (it needs no
-                # plan) runs while the host plans; the plan follows
+                # the library's planning thread plans the step while this one
+                # queues the inputs' copy and the first step's KV append (it
+                # needs no plan); the plan follows them up
+                planner.post()
                 up.run(plan_off)
                 bound[0].run_append()
-                inf2, plan_nb = planner.run()
+                inf2, plan_nb = planner.wait()
                 n = (plan_off + plan_nb + 15) // 16 * 16
                 up.run(n - plan_off, plan_off)
                 plan_e2e.info = inf2
@@ -637,6 +641,7 @@ class StepBench:
                 stream.synchronize()
                 if i >= args.warmup:
                     times.append(time.perf_counter() - t0)
+        planner.close()
         assert int(self.status.item()) == 0, f"device status {int(self.status.item())}"
         e2e_s = max_over_ranks(statistics.mean(times), dev)
         kv_tok = sum(m.kv_tokens() for m in self.metas)

@@ -72,7 +72,8 @@ typedef enum pkv_status {
   PKV_ERR_WORKSPACE = 5,     /* plan or workspace buffer too small */
   PKV_ERR_CUDA = 6,          /* a CUDA runtime call failed (launch, attribute, ...) */
   PKV_ERR_DEVICE_CHECK = 7,  /* value written to *dev_status by a kernel */
-  PKV_ERR_ALIGN = 8          /* a device pointer is not 16-byte aligned */
+  PKV_ERR_ALIGN = 8,         /* a device pointer is not 16-byte aligned */
+  PKV_ERR_STATE = 9          /* a call out of order (pkv_planner_post / pkv_planner_wait) */
 } pkv_status;
 
 /* Device-side error codes written to *dev_status (first one wins). */
@@ -212,6 +213,50 @@ PKV_API pkv_status pkv_paged_kv_append(const void *k, const void *v, const int32
 PKV_API pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *context_lens, int32_t num_seqs,
                          int32_t num_q_heads, const pkv_pool_desc *desc, int32_t num_sms,
                          void *plan, int64_t plan_capacity, pkv_plan_info *info);
+
+/*
+ * Host planning on a worker thread.  A serving loop plans each step on the host
+ * while it also queues that step's input copy and KV append (the append needs
+ * no plan); with the planner on a thread of its own, the plan is computed while
+ * the calling thread issues those calls instead of after them.  A pkv_planner
+ * owns one thread and runs one pkv_plan_step_ex call at a time.
+ *
+ * pkv_planner_create: starts the thread.  After finishing a job the thread
+ * polls for the next one for spin_us microseconds (so a loop whose steps follow
+ * each other within that time hands a job over without a thread wake-up), then
+ * sleeps until one is posted; spin_us <= 0 sleeps at once.  *out receives the
+ * planner.  Errors: PKV_ERR_NULL (out NULL), PKV_ERR_RANGE (spin_us above
+ * 1,000,000), PKV_ERR_CUDA (no thread could be started).
+ *
+ * pkv_planner_destroy: finishes a posted job, stops and joins the thread and
+ * frees the planner.  NULL is a no-op.  Not to be called concurrently with
+ * another call on the same planner.
+ *
+ * pkv_planner_post: hands the thread one pkv_plan_step_ex call with these
+ * arguments and returns at once.  Every pointer must stay valid, and the arrays
+ * and *desc unchanged, until pkv_planner_wait has returned; the thread writes
+ * plan and *info.  num_sms <= 0 is resolved here, on the calling thread's
+ * current device (PKV_ERR_CUDA if there is none), not on the worker.
+ * PKV_ERR_STATE if a job is already posted and not yet waited for; PKV_ERR_NULL
+ * if planner is NULL.  The job's own errors come from pkv_planner_wait.
+ *
+ * pkv_planner_wait: waits (polling) until the posted job has finished and
+ * returns its status, the value pkv_plan_step_ex would have returned; *info
+ * and the plan buffer then hold its results.  PKV_ERR_STATE if no job is
+ * posted; PKV_ERR_NULL if planner is NULL.
+ *
+ * post and wait on one planner are meant for one calling thread at a time.
+ */
+typedef struct pkv_planner pkv_planner;
+PKV_API pkv_status pkv_planner_create(int32_t spin_us, pkv_planner **out);
+PKV_API void pkv_planner_destroy(pkv_planner *planner);
+PKV_API pkv_status pkv_planner_post(pkv_planner *planner, const int32_t *cu_q_lens,
+                                    const int32_t *context_lens, int32_t num_seqs,
+                                    int32_t num_q_heads, const pkv_pool_desc *desc,
+                                    int32_t num_sms, int32_t steps, const int32_t *block_tables,
+                                    int32_t max_blocks_per_seq, int32_t prefill_min_q, void *plan,
+                                    int64_t plan_capacity, pkv_plan_info *info);
+PKV_API pkv_status pkv_planner_wait(pkv_planner *planner);
 
 /*
  * Bytes of device workspace the attention call needs for a plan (the same

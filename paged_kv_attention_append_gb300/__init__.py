@@ -16,6 +16,7 @@ from __future__ import annotations
 import ctypes
 import os
 import threading
+import weakref
 
 import numpy as np
 import torch
@@ -112,6 +113,15 @@ def _load():
             lib.pkv_workspace_size.restype = ctypes.c_size_t
             lib.pkv_copy_async.argtypes = [P, P, i64, P]
             lib.pkv_copy_async.restype = i32
+            lib.pkv_planner_create.argtypes = [i32, ctypes.POINTER(P)]
+            lib.pkv_planner_create.restype = i32
+            lib.pkv_planner_destroy.argtypes = [P]
+            lib.pkv_planner_destroy.restype = None
+            lib.pkv_planner_post.argtypes = [P, P, P, i32, i32, ctypes.POINTER(PoolDesc), i32, i32,
+                                             P, i32, i32, P, i64, ctypes.POINTER(PlanInfo)]
+            lib.pkv_planner_post.restype = i32
+            lib.pkv_planner_wait.argtypes = [P]
+            lib.pkv_planner_wait.restype = i32
             _lib = lib
     return _lib
 
@@ -417,10 +427,18 @@ class BoundPlan:
     size in `out`.  The arrays must be C-contiguous int32 numpy arrays whose
     shapes stay fixed (their contents may change between runs); the other
     arguments mean what they mean for plan_step.
+
+    With `spin_us` set, the object also owns a planning thread (pkv_planner_*):
+    post() starts the same call there and returns at once, so the caller can
+    queue the step's input copy and KV append meanwhile; wait() returns what
+    run() returns once it has finished.  spin_us is how long the thread polls
+    for the next post before it sleeps.  The arrays and `out` must stay
+    unchanged from post() to wait().
     """
 
     def __init__(self, cu_q_lens, context_lens, num_q_heads: int, kv_pool_or_desc, out, *,
-                 num_sms=None, chain_steps=None, block_tables=None, prefill_min_q=None):
+                 num_sms=None, chain_steps=None, block_tables=None, prefill_min_q=None,
+                 spin_us=None):
         arrays = [("cu_q_lens", cu_q_lens), ("context_lens", context_lens)]
         if block_tables is not None:
             arrays.append(("block_tables", block_tables))
@@ -456,12 +474,43 @@ class BoundPlan:
                       ctypes.c_int32(0 if prefill_min_q is None else int(prefill_min_q)),
                       vp(buf.ctypes.data), ctypes.c_int64(buf.nbytes), ctypes.byref(self.info))
         self._f = _load().pkv_plan_step_ex
+        self._worker = None
+        if spin_us is not None:
+            lib = _load()
+            handle = ctypes.c_void_p()
+            st = lib.pkv_planner_create(int(spin_us), ctypes.byref(handle))
+            if st:
+                raise PkvError(st, "pkv_planner_create")
+            self._worker = handle
+            self._post, self._wait = lib.pkv_planner_post, lib.pkv_planner_wait
+            self._fin = weakref.finalize(self, lib.pkv_planner_destroy, handle)
 
     def run(self):
         st = self._f(*self._args)
         if st:
             raise PkvError(st, "pkv_plan_step_ex")
         return self.info, (max(int(self.info.plan_bytes), 16) + 15) // 16 * 16
+
+    def post(self) -> None:
+        if self._worker is None:
+            raise RuntimeError("BoundPlan was made without spin_us: it has no planning thread")
+        st = self._post(self._worker, *self._args)
+        if st:
+            raise PkvError(st, "pkv_planner_post")
+
+    def wait(self):
+        if self._worker is None:
+            raise RuntimeError("BoundPlan was made without spin_us: it has no planning thread")
+        st = self._wait(self._worker)
+        if st:
+            raise PkvError(st, "pkv_planner_wait")
+        return self.info, (max(int(self.info.plan_bytes), 16) + 15) // 16 * 16
+
+    def close(self) -> None:
+        """Stop and join the planning thread (also done when the object is collected)."""
+        if self._worker is not None:
+            self._fin()
+            self._worker = None
 
 
 def decode_advance(context_lens, slot_mapping, cu_q_lens, block_tables, kv_pool, *,

@@ -68,7 +68,7 @@ def build(verbose: bool = False, extra=()) -> str:
             print(log)
     if not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
         tmp = LIB + f".tmp{os.getpid()}"
-        cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
+        cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lpthread"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")

@@ -686,3 +686,87 @@ def test_planning_from_several_threads_gives_each_its_own_plan(pkv):
     for t in threads:
         t.join()
     assert not bad
+
+
+@pytest.mark.parametrize("spin_us", [0, 2000])
+def test_planning_thread_writes_the_plan_run_writes(pkv, spin_us):
+    """post()/wait() run the same planner call on the library's planning thread:
+    byte for byte the plan run() writes, step after step, whether the thread was
+    polling (spin_us 2000) or asleep (spin_us 0, and after a pause) when the job
+    came."""
+    import time
+    for name in ("small_decode", "agent_mixed", "shared_prefix_verify", "decode_chain"):
+        meta = workloads.make_config(name)
+        desc = pkv.PoolDesc(meta.num_blocks, 16, meta.num_kv_heads, meta.head_dim)
+        cu, ctx = meta.cu_q_lens.astype(np.int32).copy(), meta.context_lens.astype(np.int32).copy()
+        bt = meta.block_tables.astype(np.int32).copy()
+        chain = 3 if name == "decode_chain" else None
+        out_a, out_b = np.zeros(1 << 17, np.int32), np.zeros(1 << 17, np.int32)
+        sync = pkv.BoundPlan(cu, ctx, meta.num_q_heads, desc, out_a, num_sms=152, block_tables=bt,
+                             chain_steps=chain)
+        thr = pkv.BoundPlan(cu, ctx, meta.num_q_heads, desc, out_b, num_sms=152, block_tables=bt,
+                            chain_steps=chain, spin_us=spin_us)
+        for step in range(4):
+            want_info, want_nb = sync.run()
+            want_ws = want_info.workspace_bytes
+            out_b[:] = -1
+            thr.post()
+            if step == 2:
+                time.sleep(0.01)        # the thread has gone to sleep by now
+            info, nb = thr.wait()
+            assert nb == want_nb and info.workspace_bytes == want_ws
+            assert info.num_decode_warps == want_info.num_decode_warps
+            assert np.array_equal(out_b.view(np.uint8)[:nb], out_a.view(np.uint8)[:nb])
+            if name != "decode_chain":
+                ctx[-1] += 16
+        thr.close()
+        with pytest.raises(RuntimeError):
+            thr.post()
+
+
+def test_planning_thread_reports_errors_and_misuse(pkv):
+    """The job's own status comes back from wait(); a second post before wait, or
+    a wait with nothing posted, is PKV_ERR_STATE, and the planner stays usable."""
+    meta = workloads.tiny_decode()
+    desc = pkv.PoolDesc(meta.num_blocks, 16, meta.num_kv_heads, meta.head_dim)
+    cu, ctx = meta.cu_q_lens.astype(np.int32).copy(), meta.context_lens.astype(np.int32).copy()
+    out = np.zeros(1 << 14, np.int32)
+    bp = pkv.BoundPlan(cu, ctx, meta.num_q_heads, desc, out, num_sms=152, spin_us=100)
+    with pytest.raises(pkv.PkvError) as e:
+        bp.wait()
+    assert e.value.status == 9                      # PKV_ERR_STATE: nothing posted
+    bp.post()
+    with pytest.raises(pkv.PkvError) as e:
+        bp.post()
+    assert e.value.status == 9                      # PKV_ERR_STATE: still pending
+    info, nb = bp.wait()
+    assert info.num_seqs == len(ctx) and nb > 0
+    good = ctx.copy()
+    ctx[0] = -1                                     # an invalid step: PKV_ERR_RANGE from the job
+    bp.post()
+    with pytest.raises(pkv.PkvError) as e:
+        bp.wait()
+    assert e.value.status == 3
+    ctx[:] = good
+    bp.post()                                       # usable again
+    assert bp.wait()[0].num_seqs == len(ctx)
+    no_thread = pkv.BoundPlan(cu, ctx, meta.num_q_heads, desc, out, num_sms=152)
+    with pytest.raises(RuntimeError):
+        no_thread.post()
+
+
+def test_planning_thread_entry_points_check_their_arguments(pkv):
+    lib = ctypes.CDLL(pkv.library_path())
+    P = ctypes.c_void_p
+    lib.pkv_planner_create.argtypes = [ctypes.c_int32, ctypes.POINTER(P)]
+    lib.pkv_planner_destroy.argtypes = [P]
+    lib.pkv_planner_destroy.restype = None
+    lib.pkv_planner_wait.argtypes = [P]
+    h = P()
+    assert lib.pkv_planner_create(0, None) == 1                  # PKV_ERR_NULL
+    assert lib.pkv_planner_create(2000000, ctypes.byref(h)) == 3  # PKV_ERR_RANGE
+    assert lib.pkv_planner_wait(None) == 1
+    lib.pkv_planner_destroy(None)                                  # no-op
+    for spin in (0, 50, 1000):                                     # created and destroyed idle
+        assert lib.pkv_planner_create(spin, ctypes.byref(h)) == 0 and h.value
+        lib.pkv_planner_destroy(h)

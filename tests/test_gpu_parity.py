@@ -356,8 +356,9 @@ def test_bound_step_matches_the_plain_calls(pkv, cuda_device):
 
 def test_bound_copies_and_planner_serve_a_step_from_host_buffers(pkv, cuda_device):
     """The serving loop through the library alone: pinned inputs go up with one
-    bound copy, the plan is made by the bound planner into the same pinned
-    buffer and goes up behind them, the bound step runs and a bound copy brings
+    bound copy, the plan is made by the bound planner on its own thread (while
+    the copy and the append are queued) into the same pinned buffer and goes up
+    behind them, the bound step runs and a bound copy brings
     out back.  The result has the bits of the plain calls, and copy_async moves
     bytes both ways unchanged."""
     dev = cuda_device
@@ -392,7 +393,7 @@ def test_bound_copies_and_planner_serve_a_step_from_host_buffers(pkv, cuda_devic
     pool_a, pool_b = pool.to(dev), pool.to(dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     planner = pkv.BoundPlan(hv[1].numpy(), hv[2].numpy(), 16, pool_b, hv[-1].numpy(),
-                            block_tables=hv[3].numpy())
+                            block_tables=hv[3].numpy(), spin_us=500)
     info, plan_nb = planner.run()
     plan = pkv.StepPlan(info, hv[-1].numpy().view(np.uint8)[:plan_nb].view(np.int32), dev)
     plan.dev = dplan.view(torch.uint8)
@@ -402,8 +403,12 @@ def test_bound_copies_and_planner_serve_a_step_from_host_buffers(pkv, cuda_devic
     down = pkv.BoundCopy(out_h, out_b)
     step = pkv.BoundStep(dk, dvv, ds, dq, dcu, dctx, dbt, pool_b, meta.scale, plan, out_b,
                          dev_status=status)
+    hv[-1].zero_()
+    planner.post()                   # planned on the library's thread meanwhile:
     up.run(offs[-1])                 # the inputs, then the append (it needs no plan)
     step.run_append()
+    info2, plan_nb = planner.wait()
+    assert info2.plan_bytes == info.plan_bytes
     up.run(plan_nb, offs[-1])        # the plan behind them
     step.run_attention()
     down.run()
