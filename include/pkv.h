@@ -73,7 +73,8 @@ typedef enum pkv_status {
   PKV_ERR_CUDA = 6,          /* a CUDA runtime call failed (launch, attribute, ...) */
   PKV_ERR_DEVICE_CHECK = 7,  /* value written to *dev_status by a kernel */
   PKV_ERR_ALIGN = 8,         /* a device pointer is not 16-byte aligned */
-  PKV_ERR_STATE = 9          /* a call out of order (pkv_planner_post / pkv_planner_wait) */
+  PKV_ERR_STATE = 9,         /* a call out of order (pkv_planner_post / pkv_planner_wait) */
+  PKV_ERR_HOST_MEMORY = 10   /* the planner could not allocate its host scratch */
 } pkv_status;
 
 /* Device-side error codes written to *dev_status (first one wins). */
@@ -197,7 +198,9 @@ PKV_API pkv_status pkv_paged_kv_append(const void *k, const void *v, const int32
  *   of the calling thread's current device (PKV_ERR_CUDA if there is none).
  *   plan: host buffer receiving plan_capacity bytes at most; may be NULL to
  *   query sizes only (info is always filled on success).
- * Returns PKV_ERR_WORKSPACE if plan is non-NULL and plan_capacity < info->plan_bytes.
+ * Returns PKV_ERR_WORKSPACE if plan is non-NULL and plan_capacity < info->plan_bytes,
+ * PKV_ERR_HOST_MEMORY if the planner's own host scratch (reused per calling
+ * thread, grown with the step) could not be allocated.
  * The plan buffer is opaque; upload it unchanged (e.g. cudaMemcpyAsync) before
  * the attention call that uses it.
  *
@@ -238,7 +241,8 @@ PKV_API pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *contex
  * plan and *info.  num_sms <= 0 is resolved here, on the calling thread's
  * current device (PKV_ERR_CUDA if there is none), not on the worker.
  * PKV_ERR_STATE if a job is already posted and not yet waited for; PKV_ERR_NULL
- * if planner is NULL.  The job's own errors come from pkv_planner_wait.
+ * if planner is NULL.  The job's own errors come from pkv_planner_wait.  The
+ * thread keeps its own planner scratch, as any calling thread does.
  *
  * pkv_planner_wait: waits (polling) until the posted job has finished and
  * returns its status, the value pkv_plan_step_ex would have returned; *info

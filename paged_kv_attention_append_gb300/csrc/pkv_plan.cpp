@@ -1005,6 +1005,21 @@ static pkv_status plan_impl(const int32_t *cu_q_lens, const int32_t *context_len
   return PKV_OK;
 }
 
+// The planner's host scratch grows with the step; no C++ exception (a failed
+// allocation) leaves the C ABI: it becomes PKV_ERR_HOST_MEMORY.
+static pkv_status plan_guarded(const int32_t *cu_q_lens, const int32_t *context_lens,
+                               int32_t num_seqs, int32_t num_q_heads, const pkv_pool_desc *desc,
+                               int32_t num_sms, int32_t lookahead, const int32_t *block_tables,
+                               int32_t max_blocks_per_seq, int32_t prefill_min_q, void *plan,
+                               int64_t plan_capacity, pkv_plan_info *info) {
+  try {
+    return plan_impl(cu_q_lens, context_lens, num_seqs, num_q_heads, desc, num_sms, lookahead,
+                     block_tables, max_blocks_per_seq, prefill_min_q, plan, plan_capacity, info);
+  } catch (...) {
+    return PKV_ERR_HOST_MEMORY;
+  }
+}
+
 extern "C" pkv_status pkv_plan_step_ex(const int32_t *cu_q_lens, const int32_t *context_lens,
                                        int32_t num_seqs, int32_t num_q_heads,
                                        const pkv_pool_desc *desc, int32_t num_sms, int32_t steps,
@@ -1013,16 +1028,16 @@ extern "C" pkv_status pkv_plan_step_ex(const int32_t *cu_q_lens, const int32_t *
                                        pkv_plan_info *info) {
   if (steps < 1) return PKV_ERR_RANGE;
   if (block_tables && max_blocks_per_seq < 0) return PKV_ERR_SHAPE;
-  return plan_impl(cu_q_lens, context_lens, num_seqs, num_q_heads, desc, num_sms, steps - 1,
-                   block_tables, max_blocks_per_seq, prefill_min_q, plan, plan_capacity, info);
+  return plan_guarded(cu_q_lens, context_lens, num_seqs, num_q_heads, desc, num_sms, steps - 1,
+                      block_tables, max_blocks_per_seq, prefill_min_q, plan, plan_capacity, info);
 }
 
 extern "C" pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *context_lens,
                                     int32_t num_seqs, int32_t num_q_heads,
                                     const pkv_pool_desc *desc, int32_t num_sms, void *plan,
                                     int64_t plan_capacity, pkv_plan_info *info) {
-  return plan_impl(cu_q_lens, context_lens, num_seqs, num_q_heads, desc, num_sms, 0, nullptr, 0,
-                   0, plan, plan_capacity, info);
+  return plan_guarded(cu_q_lens, context_lens, num_seqs, num_q_heads, desc, num_sms, 0, nullptr, 0,
+                      0, plan, plan_capacity, info);
 }
 
 extern "C" pkv_status pkv_plan_decode_chain(const int32_t *cu_q_lens, const int32_t *context_lens,

@@ -33,8 +33,9 @@ def test_library_exports_every_declared_symbol(pkv):
 
 def test_version_and_status_strings(pkv):
     assert pkv.version() >= 100
-    for s in range(9):
+    for s in range(11):
         assert pkv.status_string(s).startswith("PKV_")
+    assert pkv.status_string(11) == "unknown pkv status"
 
 
 # ---------------------------------------------------------------- planner
