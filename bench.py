@@ -12,7 +12,7 @@ The line's workload is the high-concurrency decode step (256 sequences, 3.4 GB
 of KV), the largest of the five step shapes the metric is quoted on; the other
 four (tiny decode, small-model decode, the agent-shaped mixed step, the
 shared-prefix verify step) are timed in the same process, the same way, and
-reported under `configs` (--only skips them).
+reported under `configs`, each with its own e2e (--only skips them).
 
 * value: KV tokens/s = sum(context_lens) / device time per step, inputs resident
   in HBM, the step replayed from a CUDA graph, L2 flushed before every timed
@@ -685,6 +685,7 @@ def bench_pkv(args):
             b = StepBench(pkv, workloads.make_config(name), dev, stream)
             b.measure(args, flush_l2)
             others[name] = b.summary(ws, args.steps)
+            others[name]["e2e"] = b.e2e(args, ws)
             del b
             torch.cuda.empty_cache()
 
@@ -731,6 +732,7 @@ def bench_pkv(args):
                                         "step_frac_hbm", "plan", *[x for x in ("step_roofline",
                                                                                "unique_gbs")
                                                                    if x in head])}}
+        line["configs"][meta.name]["e2e"] = e2e
         line["configs"].update({n: {**o, "config": config_of(workloads.make_config(n), ws)}
                                 for n, o in others.items()})
     print(json.dumps(line), flush=True)
