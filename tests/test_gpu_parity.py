@@ -805,3 +805,48 @@ def test_verify_windows_chained_shared_items_match_oracle(pkv, cuda_device, seed
         out, _, _ = gpu_step(pkv, meta, q, k, v, pool, cuda_device, num_sms=sms)
         assert_close(out, want, f"windows seed {seed} sms {sms}")
     assert chained
+
+
+@pytest.mark.parametrize("window", [False, True])
+def test_planning_thread_serves_consecutive_steps(pkv, cuda_device, window):
+    """A serving loop over several decode steps whose contexts grow (plans of
+    changing size): each step is planned on the library's planning thread while
+    the step's KV append is queued, then attended with that plan; every step
+    matches the oracle and the pool ends bit-exact."""
+    steps = 5
+    meta, per_step = _chain_case(steps, seed=91, window=window)
+    _, _, _, pool = workloads.make_values(per_step[0])
+    vals = [workloads.make_values(m, seed=700 + t)[:3] for t, m in enumerate(per_step)]
+    pool_o, want = pool, []
+    for m, (q, k, v) in zip(per_step, vals):
+        out, pool_o = oracle.run_step(m, q, k, v, pool_o)
+        want.append(out)
+    dev = cuda_device
+    pd = pool.to(dev)
+    cu_h = meta.cu_q_lens.astype(np.int32).copy()
+    ctx_h = per_step[0].context_lens.astype(np.int32).copy()
+    bt_h = meta.block_tables.astype(np.int32).copy()
+    plan_h = np.zeros(1 << 18, np.int32)
+    planner = pkv.BoundPlan(cu_h, ctx_h, meta.num_q_heads, pd, plan_h, block_tables=bt_h,
+                            spin_us=200)
+    cu = torch.from_numpy(cu_h).to(dev)
+    bt = torch.from_numpy(bt_h).to(dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    sizes = set()
+    for t, (m, (q, k, v)) in enumerate(zip(per_step, vals)):
+        ctx_h[:] = m.context_lens
+        planner.post()
+        ctx = torch.from_numpy(m.context_lens).to(dev)
+        slots = torch.from_numpy(m.slot_mapping).to(dev)
+        pkv.paged_kv_append(k.to(dev), v.to(dev), slots, pd, dev_status=status)
+        info, nb = planner.wait()
+        sizes.add(int(info.plan_bytes))
+        plan = pkv.StepPlan(info, plan_h.view(np.uint8)[:nb].view(np.int32), dev)
+        out = pkv.paged_varlen_attention(q.to(dev), cu, ctx, bt, pd, meta.scale, plan=plan,
+                                         dev_status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert_close(out.cpu(), want[t], f"planning thread step {t}")
+    planner.close()
+    assert len(sizes) > 1          # the plans did change from step to step
+    assert np.array_equal(bits(pd), pool_o)
