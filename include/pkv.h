@@ -74,7 +74,7 @@ typedef enum pkv_status {
   PKV_ERR_DEVICE_CHECK = 7,  /* value written to *dev_status by a kernel */
   PKV_ERR_ALIGN = 8,         /* a device pointer is not 16-byte aligned */
   PKV_ERR_STATE = 9,         /* a call out of order (pkv_planner_post / pkv_planner_wait) */
-  PKV_ERR_HOST_MEMORY = 10   /* the planner could not allocate its host scratch */
+  PKV_ERR_HOST_MEMORY = 10   /* host memory or a thread for the planner could not be had */
 } pkv_status;
 
 /* Device-side error codes written to *dev_status (first one wins). */
@@ -229,7 +229,8 @@ PKV_API pkv_status pkv_plan_step(const int32_t *cu_q_lens, const int32_t *contex
  * each other within that time hands a job over without a thread wake-up), then
  * sleeps until one is posted; spin_us <= 0 sleeps at once.  *out receives the
  * planner.  Errors: PKV_ERR_NULL (out NULL), PKV_ERR_RANGE (spin_us above
- * 1,000,000), PKV_ERR_CUDA (no thread could be started).
+ * 1,000,000), PKV_ERR_HOST_MEMORY (the planner or its thread could not be
+ * created).
  *
  * pkv_planner_destroy: finishes a posted job, stops and joins the thread and
  * frees the planner.  NULL is a no-op.  Not to be called concurrently with

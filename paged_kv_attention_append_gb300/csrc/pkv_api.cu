@@ -98,7 +98,7 @@ extern "C" const char *pkv_status_string(int32_t status) {
     case PKV_ERR_DEVICE_CHECK: return "PKV_ERR_DEVICE_CHECK: a kernel reported an error";
     case PKV_ERR_ALIGN: return "PKV_ERR_ALIGN: a device pointer is not 16-byte aligned";
     case PKV_ERR_STATE: return "PKV_ERR_STATE: a planner call out of order";
-    case PKV_ERR_HOST_MEMORY: return "PKV_ERR_HOST_MEMORY: the planner's host scratch could not be allocated";
+    case PKV_ERR_HOST_MEMORY: return "PKV_ERR_HOST_MEMORY: host memory or a thread for the planner could not be had";
     default: return "unknown pkv status";
   }
 }

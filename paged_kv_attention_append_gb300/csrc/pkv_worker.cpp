@@ -49,7 +49,8 @@ struct pkv_planner {
     for (;;) {
       // poll for the next job for `spin`, then sleep until one is posted
       const auto t0 = std::chrono::steady_clock::now();
-      while (state.load(std::memory_order_acquire) != kPosted && !stop.load(std::memory_order_acquire)) {
+      while (state.load(std::memory_order_acquire) != kPosted &&
+             !stop.load(std::memory_order_acquire)) {
         if (std::chrono::steady_clock::now() - t0 >= spin) {
           std::unique_lock<std::mutex> lk(mu);
           cv.wait(lk, [&] {
@@ -73,13 +74,13 @@ extern "C" pkv_status pkv_planner_create(int32_t spin_us, pkv_planner **out) {
   *out = nullptr;
   if (spin_us > 1000000) return PKV_ERR_RANGE;
   pkv_planner *p = new (std::nothrow) pkv_planner;
-  if (!p) return PKV_ERR_CUDA;
+  if (!p) return PKV_ERR_HOST_MEMORY;
   p->spin = std::chrono::microseconds(spin_us > 0 ? spin_us : 0);
   try {
     p->worker = std::thread([p] { p->run(); });
   } catch (...) {
     delete p;
-    return PKV_ERR_CUDA;
+    return PKV_ERR_HOST_MEMORY;
   }
   *out = p;
   return PKV_OK;
@@ -110,8 +111,8 @@ extern "C" pkv_status pkv_planner_post(pkv_planner *p, const int32_t *cu_q_lens,
     num_sms = pkv::device_sm_count();
     if (num_sms <= 0) return PKV_ERR_CUDA;
   }
-  p->job = Job{cu_q_lens,   context_lens,  block_tables, num_seqs, num_q_heads, num_sms,
-               steps,       max_blocks_per_seq, prefill_min_q, desc, plan, plan_capacity, info};
+  p->job = Job{cu_q_lens, context_lens, block_tables, num_seqs, num_q_heads, num_sms, steps,
+               max_blocks_per_seq, prefill_min_q, desc, plan, plan_capacity, info};
   {
     // under the lock, so a worker about to sleep either sees the job or is woken
     std::lock_guard<std::mutex> lk(p->mu);
