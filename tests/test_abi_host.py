@@ -771,3 +771,41 @@ def test_planning_thread_entry_points_check_their_arguments(pkv):
     for spin in (0, 50, 1000):                                     # created and destroyed idle
         assert lib.pkv_planner_create(spin, ctypes.byref(h)) == 0 and h.value
         lib.pkv_planner_destroy(h)
+
+
+def test_two_planning_threads_at_once(pkv):
+    """Two planners, each with its own thread, posted to and waited on from two
+    Python threads at the same time: every plan is byte for byte the one the
+    synchronous call writes for the same step."""
+    import threading
+    names = ("small_decode", "shared_prefix_verify")
+    cases = []
+    for name in names:
+        meta = workloads.make_config(name)
+        desc = pkv.PoolDesc(meta.num_blocks, 16, meta.num_kv_heads, meta.head_dim)
+        cu, ctx = meta.cu_q_lens.astype(np.int32).copy(), meta.context_lens.astype(np.int32).copy()
+        bt = meta.block_tables.astype(np.int32).copy()
+        ref_info, ref = pkv.plan_step(cu, ctx, meta.num_q_heads, desc, num_sms=152, upload=False,
+                                      block_tables=bt)
+        out = np.zeros(1 << 17, np.int32)
+        bp = pkv.BoundPlan(cu, ctx, meta.num_q_heads, desc, out, num_sms=152, block_tables=bt,
+                           spin_us=500)
+        cases.append((bp, out, ref.view(np.uint8)[:ref_info.plan_bytes].copy()))
+    bad = []
+
+    def loop(i):
+        bp, out, ref = cases[i]
+        for _ in range(40):
+            out[:] = 0
+            bp.post()
+            _, nb = bp.wait()
+            if not np.array_equal(out.view(np.uint8)[:len(ref)], ref):
+                bad.append(i)
+    threads = [threading.Thread(target=loop, args=(i,)) for i in range(len(cases))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    for bp, _, _ in cases:
+        bp.close()
+    assert not bad
